@@ -1,0 +1,455 @@
+"""Decode-step benchmark: Qwen3-8B-shaped BF16 greedy decode at batch 1.
+
+One step = one token through the whole path: embedding gather, every decoder
+layer (RMSNorm + QKV GEMV, QK-norm + RoPE + K/V write + split-KV attention,
+O GEMV + residual, RMSNorm + gate/up GEMV, SwiGLU + down GEMV + residual), the
+final RMSNorm + LM-head GEMV and the on-device argmax that advances token and
+position, replayed as one captured CUDA graph per step. The workload runs 128
+greedy steps from context 4096; longer timed runs restart it every 128 steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Multi-GPU runs (torchrun) are independent
+replicas, one sequence per GPU, no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from transformer_decode_step_weight_gb300 import synth  # noqa: E402
+
+METRIC = "Qwen3-8B-shape decode tok/s @bs1; achieved HBM GB/s vs GB300 peak"
+RUN_LEN = 128          # greedy steps of one decode run (the workload)
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3-8b-bf16", choices=["qwen3-8b-bf16", "qwen3-0.6b"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=128)
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        self.idx = device_index
+
+    def start(self):
+        try:
+            bus = torch.cuda.get_device_properties(self.idx).pci_bus_id
+            sel = ["-i", bus] if bus else []
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", *sel, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- byte accounting
+
+
+def weight_bytes(s: synth.Shape, wtype: str) -> int:
+    """Bytes of weights one token streams: every projection, the LM head, norms, one embedding row."""
+    per_w = 2.0 if wtype == "bf16" else 34.0 / 32.0
+    layer = (s.qkv_rows * s.hidden + s.hidden * s.n_q_heads * s.head_dim + 2 * s.ffn * s.hidden +
+             s.hidden * s.ffn) * per_w + (2 * s.hidden + 2 * s.head_dim) * 2
+    return int(s.n_layers * layer + s.vocab * s.hidden * per_w + s.hidden * 2 + s.hidden * 2)
+
+
+def kv_bytes(s: synth.Shape, pos: int) -> int:
+    """K/V bytes one step at position `pos` reads (pos tokens) and writes (1 token), all layers."""
+    row = s.n_kv_heads * s.head_dim * 2 * 2       # K and V, bf16
+    return s.n_layers * row * (pos + 1)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_record(kernel_src: str):
+    """DRAM traffic per launch of the dominant kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "gemv_bf16_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec.get("source_sha") != sha:
+            return None
+        return rec
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args, dist, rank, world, local):
+    from transformer_decode_step_weight_gb300 import api
+    from transformer_decode_step_weight_gb300 import build as b
+
+    b.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[args.workload]
+    s = wl.shape
+    mt = synth.make_model(s, wl.wtype, args.seed + rank, dev, ctx=wl.ctx, steps=RUN_LEN)
+    dec = api.Decoder(mt, max_steps=RUN_LEN, device=dev)
+    tok0, pos0 = dec.tok.clone(), dec.pos.clone()
+
+    def reset():
+        dec.tok.copy_(tok0)
+        dec.pos.copy_(pos0)
+        dec.step_ctr.zero_()
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        dec.capture(1)
+        for _ in range(args.warmup):
+            dec.replay()
+        reset()
+    stream.synchronize()
+    assert api.check_device_error(stream) == 0
+
+    # ---- timed region: K graph replays (one token each)
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(K):
+            if i and i % RUN_LEN == 0:
+                reset()
+            dec.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(dist)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(dist, ms)
+    assert api.check_device_error(stream) == 0
+    toks = K * dec.batch * world
+    value = toks / (ms_max / 1e3)
+    # algorithmic bytes of the timed steps
+    wb = weight_bytes(s, wl.wtype)
+    step_bytes = [wb + kv_bytes(s, wl.ctx + (i % RUN_LEN)) for i in range(K)]
+    hbm_peak, peak_kind = peaks()
+    step_gbs = sum(step_bytes) / (ms / 1e3) / 1e9
+
+    # ---- dominant kernel: the BF16 GEMV, every launch of one token, events on its stream
+    roof = dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind)
+
+    # ---- end to end through the public API: per step H2D of the input token/position
+    # from pinned memory, the step, D2H of the next token, host reads it
+    e2e = run_e2e(dec, stream, args.e2e_steps, reset, dist, world)
+    launches = K * dec.launches_per_step
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(mt, s, wl)
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "description": wl.description, "global_batch": dec.batch * world,
+                       "ctx_start": wl.ctx, "decode_run_steps": RUN_LEN, "parallelism": f"replicas x{world}",
+                       "graph": "one CUDA graph per step, PDL between kernels",
+                       "l2": "inputs larger than L2 (15.1 GB of weights streamed per step)"},
+            "roofline": roof,
+            "step_roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                              "frac": round(step_gbs / hbm_peak, 4), "peak_kind": peak_kind,
+                              "bytes_per_step": int(sum(step_bytes) / K)},
+            "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+    dec.close()
+
+
+def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
+    """Average duration of gemv_bf16 launches over one token's projections (36 x QKV,
+    O, gate+up at K = hidden, and the LM head), timed with CUDA events on the stream
+    they run on, three passes; algorithmic bytes = the weight bytes each launch reads."""
+    x = torch.randn((1, max(s.hidden, s.n_q_heads * s.head_dim)), device=mt.embed.device).to(torch.bfloat16)
+    xo = x[:, : s.n_q_heads * s.head_dim].contiguous()
+    xh = x[:, : s.hidden].contiguous()
+    mats = []
+    for lt in mt.layers:
+        mats += [(lt.w_qkv, xh), (lt.w_o, xo), (lt.w_gu, xh)]
+    mats.append((mt.lm_head, xh))
+    ys = {id(w): torch.empty((1, w.shape[0]), dtype=torch.float32, device=x.device) for w, _ in mats}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for w, xx in mats:   # warm
+            api.gemv_bf16(w, xx, ys[id(w)], stream=stream)
+        e0.record(stream)
+        for _ in range(3):
+            for w, xx in mats:
+                api.gemv_bf16(w, xx, ys[id(w)], stream=stream)
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1)
+    n = 3 * len(mats)
+    bytes_per_launch = sum(w.numel() * 2 for w, _ in mats) / len(mats)
+    avg_s = ms / 1e3 / n
+    achieved = bytes_per_launch / avg_s / 1e9
+    rec = traffic_record(os.path.join(ROOT, "transformer_decode_step_weight_gb300", "csrc", "gemv_bf16.cu"))
+    traffic = None
+    if rec is not None:
+        traffic = rec.get("traffic_bytes_per_launch")
+    return {"bound": "hbm", "kernel": "gemv_bf16_kernel (K = hidden launches of one token)",
+            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+            "peak_kind": peak_kind, "avg_launch_us": round(avg_s * 1e6, 3),
+            "algorithmic_bytes_per_launch": int(bytes_per_launch), "traffic": traffic}
+
+
+def run_e2e(dec, stream, steps, reset, dist, world):
+    dev = dec.tok.device
+    h_in = torch.empty(2, dtype=torch.int32, pin_memory=True)
+    h_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    with torch.cuda.stream(stream):
+        reset()
+    stream.synchronize()
+    h_in[0] = int(dec.tok[0])
+    h_in[1] = int(dec.pos[0])
+    barrier(dist)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        with torch.cuda.stream(stream):
+            if i and i % RUN_LEN == 0:
+                reset()
+                stream.synchronize()
+                h_in[0] = int(dec.tok[0])
+                h_in[1] = int(dec.pos[0])
+            dec.tok[:1].copy_(h_in[0:1], non_blocking=True)
+            dec.pos[:1].copy_(h_in[1:2], non_blocking=True)
+            dec.replay()
+            h_out.copy_(dec.tok[:1], non_blocking=True)
+        stream.synchronize()
+        h_in[0] = int(h_out[0])
+        h_in[1] = h_in[1] + 1
+    dt = time.perf_counter() - t0
+    dt = max_over_ranks(dist, dt)
+    del dev
+    return {"value": round(steps * dec.batch * world / dt, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
+            "d2h_bytes_per_step": 4, "steps": steps}
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(mt, s, wl, n_layers_sample: int = 8):
+    """The CPU oracle, as it stands, on a bounded sample: n full-size decoder layers
+    (layer 0 of the model, at the workload's context) plus n/36 of the LM-head rows,
+    scaled to one token."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from helpers import oracle_caches, oracle_layer, oracle_dims
+    torch.set_num_threads(_cores())
+    od = oracle_dims(s)
+    ol = oracle_layer(mt.layers[0], mt.wtype)
+    ks, vs = oracle_caches(_OneLayer(mt), 0, wl.ctx + 1)
+    x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[0])]))
+    frac = n_layers_sample / s.n_layers
+    rows = np.arange(0, s.vocab, int(round(1 / frac)))
+    lm_bits = synth.bits_u16(mt.lm_head[torch.as_tensor(rows, device=mt.lm_head.device)])
+    fn = synth.bits_u16(mt.final_norm)
+    t0 = time.perf_counter()
+    res = x0
+    for _ in range(n_layers_sample):
+        res = oracle.layer_step(od, ol, x0, ks[0], vs[0], wl.ctx, mode="bf16", act="bf16")
+    xf = oracle.rmsnorm(res, oracle.bf16_to_f64(fn), s.rms_eps, "bf16")
+    oracle.gemv_bf16(lm_bits, xf)
+    dt = time.perf_counter() - t0
+    sec_per_tok = dt / frac
+    return {"value": round(1.0 / sec_per_tok, 5), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{n_layers_sample} of {s.n_layers} full-size decoder layers at context {wl.ctx} "
+                      f"plus {len(rows)} of {s.vocab} LM-head rows ({dt:.1f} s), scaled to one token"}
+
+
+class _OneLayer:
+    """View of a model's first layer's cache for the oracle helpers."""
+
+    def __init__(self, mt):
+        self.k_cache, self.v_cache = mt.k_cache[:1], mt.v_cache[:1]
+        self.page_table, self.seq_lens = mt.page_table, mt.seq_lens
+
+
+# ---------------------------------------------------------------- reference arm
+
+
+def run_reference(args, dist, rank, world, local):
+    """The CPU oracle as it stands, on the host cores: each step is one full-size
+    decoder layer plus 1/36 of the LM-head rows (1/36 of one token's work)."""
+    if rank != 0:
+        return
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from helpers import oracle_caches, oracle_dims, oracle_layer
+    wl = synth.WORKLOADS[args.workload]
+    s = wl.shape
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    mt = synth.make_model(s, wl.wtype, args.seed, dev, n_layers=1, ctx=wl.ctx, steps=1)
+    torch.set_num_threads(_cores())
+    od = oracle_dims(s)
+    ol = oracle_layer(mt.layers[0], wl.wtype)
+    ks, vs = oracle_caches(mt, 0, wl.ctx + 1)
+    x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[0])]))
+    rows = np.arange(0, s.vocab, s.n_layers)
+    lm_bits = synth.bits_u16(mt.lm_head[torch.as_tensor(rows, device=mt.lm_head.device)])
+    fn = oracle.bf16_to_f64(synth.bits_u16(mt.final_norm))
+    del mt
+
+    def one():
+        r = oracle.layer_step(od, ol, x0, ks[0], vs[0], wl.ctx, mode="bf16", act="bf16")
+        oracle.gemv_bf16(lm_bits, oracle.rmsnorm(r, fn, s.rms_eps, "bf16"))
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = time.perf_counter() - t0
+    tok_s = args.steps / s.n_layers / dt
+    sample = (f"each step: 1 of {s.n_layers} full-size decoder layers at context {wl.ctx} + {len(rows)} of "
+              f"{s.vocab} LM-head rows (1/{s.n_layers} of a token)")
+    out = {"impl": "reference", "metric": METRIC, "value": round(tok_s, 5), "unit": "tok/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.name, "description": wl.description, "global_batch": 1},
+           "cpu_baseline": {"value": round(tok_s, 5), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(tok_s, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            run_reference(args, None, 0, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0")))
+        return
+    dist, rank, world, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist, rank, world, local)
+        else:
+            run_ours(args, dist, rank, world, local)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,177 @@
+"""Parity of the whole decode step (qd_decode_step / the captured graph) with the
+CPU oracle.
+
+Protocol for greedy tokens (teacher-forced): the oracle follows the GPU's own
+token stream. At every step the GPU logits must match the oracle's within the
+relative max-abs tolerance (2e-2 for the BF16 path, 5e-3 for the f32-activation
+Q8_0 lane, 2e-2 for the dp4a lane), the GPU token must be the argmax of the GPU
+logits, and it must equal the oracle's argmax unless the oracle's top-1/top-2
+gap is below 4x the step's max-abs logit error (a near tie, logged).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import oracle_caches, oracle_model, rel_max_abs
+from transformer_decode_step_weight_gb300 import api, synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = {"bf16": 2e-2, "f32": 5e-3, "i8": 2e-2}
+
+
+def teacher_forced(dec, mt, steps, mode, act, lm_act=None, b=0, log=None):
+    """Run `steps` eager GPU steps and check each against the oracle."""
+    om = oracle_model(mt)
+    pos0 = int(mt.seq_lens[b])
+    ks, vs = oracle_caches(mt, b, pos0 + steps)
+    tok = int(mt.start_tok[b])
+    strict = 0
+    worst = 0.0
+    for t in range(steps):
+        dec.step()
+        torch.cuda.synchronize()
+        g = dec.logits[b].double().cpu().numpy()
+        gtok = int(dec.tok[b])
+        ref = oracle.decode_token(om, tok, pos0 + t, ks, vs, mode=mode, act=act, lm_act=lm_act)
+        err = rel_max_abs(g, ref)
+        worst = max(worst, err)
+        assert err < TOL[act], (t, err)
+        assert gtok == oracle.argmax_first(g), t
+        otok = oracle.argmax_first(ref)
+        if gtok == otok:
+            strict += 1
+        else:
+            top = np.sort(ref)[-2:]
+            gap = top[1] - top[0]
+            assert gap < 4 * np.max(np.abs(g - ref)), (t, gtok, otok, gap)
+        assert int(dec.out_tokens[b, t]) == gtok
+        tok = gtok
+    if log is not None:
+        log.update(strict=strict, steps=steps, worst_rel_err=worst)
+    assert api.check_device_error() == 0
+    return strict
+
+
+def test_tiny_bf16_model_teacher_forced(cuda_lib):
+    mt = synth.make_model(synth.TINY, "bf16", 1, DEV, ctx=20, steps=12)
+    dec = api.Decoder(mt, max_steps=12)
+    st = {}
+    teacher_forced(dec, mt, 12, "bf16", "bf16", log=st)
+    assert st["strict"] >= 11
+    assert int(dec.pos[0]) == 32 and int(dec.step_ctr[0]) == 12
+
+
+@pytest.mark.parametrize("act,lane", [("f32", api.QD_ACT_F32), ("i8", api.QD_ACT_I8)])
+def test_tiny_q8_model_teacher_forced(cuda_lib, act, lane):
+    mt = synth.make_model(synth.TINY, "q8_0", 2, DEV, ctx=40, steps=8)
+    dec = api.Decoder(mt, max_steps=8, act=lane)
+    st = {}
+    teacher_forced(dec, mt, 8, "f32", act, log=st)
+    assert st["strict"] >= 7
+
+
+def test_small_bf16_batch_paged_teacher_forced(cuda_lib):
+    # batch 3, 16-token pages through a random page table; every sequence checked
+    mt = synth.make_model(synth.SMALL, "bf16", 3, DEV, batch=3, ctx=[70, 129, 300], steps=6, paged=True)
+    om = oracle_model(mt)
+    caches = [oracle_caches(mt, b, int(mt.seq_lens[b]) + 6) for b in range(3)]
+    dec = api.Decoder(mt, max_steps=6)
+    toks = [int(t) for t in mt.start_tok]
+    for t in range(6):
+        dec.step()
+        torch.cuda.synchronize()
+        for b in range(3):
+            g = dec.logits[b].double().cpu().numpy()
+            ref = oracle.decode_token(om, toks[b], int(mt.seq_lens[b]) + t, caches[b][0], caches[b][1], mode="bf16",
+                                      act="bf16")
+            assert rel_max_abs(g, ref) < TOL["bf16"]
+            toks[b] = int(dec.tok[b])
+            assert toks[b] == oracle.argmax_first(g)
+    assert api.check_device_error() == 0
+
+
+def test_graph_replay_is_bit_identical_to_eager(cuda_lib):
+    runs = []
+    for use_graph in (False, True):
+        mt = synth.make_model(synth.SMALL, "bf16", 4, DEV, ctx=100, steps=8)
+        dec = api.Decoder(mt, max_steps=8)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            if use_graph:
+                dec.capture(4)
+                addr = (dec.tok.data_ptr(), dec.pos.data_ptr(), dec.logits.data_ptr())
+                dec.replay()
+                dec.replay()
+                assert addr == (dec.tok.data_ptr(), dec.pos.data_ptr(), dec.logits.data_ptr())
+            else:
+                for _ in range(8):
+                    dec.step()
+        s.synchronize()
+        runs.append((dec.out_tokens.clone(), dec.logits.clone(), mt.k_cache[0].clone(), dec.pos.clone()))
+        dec.close()
+    for a, b in zip(runs[0], runs[1]):
+        assert torch.equal(a, b)
+    assert int(runs[1][3][0]) == 108
+
+
+def test_qwen3_06b_layer_workload(cuda_lib):
+    """One Qwen3-0.6B-shaped layer at position 128 over a 128-token cache; input hidden ~ N(0, 1)."""
+    s = synth.QWEN3_06B
+    mt = synth.make_model(s, "bf16", 0, DEV, n_layers=1, ctx=128, steps=1)
+    hid = synth.make_hidden(0, s.hidden, DEV)
+    tok = int(mt.start_tok[0])
+    mt.embed[tok] = hid[0].to(torch.bfloat16)    # the layer input is this hidden state (bf16 storage)
+    om = oracle_model(mt)
+    ks, vs = oracle_caches(mt, 0, 129)
+    dec = api.Decoder(mt, max_steps=1)
+    dec.step()
+    torch.cuda.synchronize()
+    res = dec.residual()[0].double().cpu().numpy()
+    x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[tok]))
+    ref = oracle.layer_step(om.dims, om.layers[0], x0, ks[0], vs[0], 128, mode="bf16", act="bf16")
+    assert rel_max_abs(res, ref) < 2e-3
+    # the K/V rows written at slot 128 (bf16) against the oracle's
+    k_gpu = oracle.bf16_to_f64(synth.bits_u16(mt.k_cache[0][0, :, 128, :]))
+    v_gpu = oracle.bf16_to_f64(synth.bits_u16(mt.v_cache[0][0, :, 128, :]))
+    assert rel_max_abs(k_gpu, ks[0][:, 128]) < 1e-2
+    assert rel_max_abs(v_gpu, vs[0][:, 128]) < 1e-2
+    # LM head on the GPU's own final residual: sampled rows + the argmax
+    rows = np.arange(0, s.vocab, 37)
+    lg = dec.logits[0].double().cpu().numpy()
+    assert rel_max_abs(lg[rows], oracle.lm_head_rows(om, res, rows)) < 1e-3
+
+
+@pytest.mark.parametrize("wtype,act", [("bf16", "bf16"), ("q8_0", "f32"), ("q8_0", "i8")])
+def test_qwen3_8b_full_size_layer_and_head(cuda_lib, wtype, act):
+    """Full Qwen3-8B shapes in the launch configuration the bench uses: one layer at
+    context 4096 (2048 for Q8_0) checked whole, the 151936-row LM head sampled."""
+    s = synth.QWEN3_8B
+    ctx = 4096 if wtype == "bf16" else 2048
+    mt = synth.make_model(s, wtype, 3, DEV, n_layers=1, ctx=ctx, steps=1)
+    om = oracle_model(mt)
+    ks, vs = oracle_caches(mt, 0, ctx + 1)
+    lane = api.QD_ACT_I8 if act == "i8" else api.QD_ACT_F32
+    dec = api.Decoder(mt, max_steps=1, act=lane)
+    dec.step()
+    torch.cuda.synchronize()
+    res = dec.residual()[0].double().cpu().numpy()
+    mode = "bf16" if wtype == "bf16" else "f32"
+    x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[0])]))
+    ref = oracle.layer_step(om.dims, om.layers[0], x0, ks[0], vs[0], ctx, mode=mode, act=act)
+    assert rel_max_abs(res, ref) < TOL[act]
+    rows = np.arange(0, s.vocab, 101)
+    lg = dec.logits[0].double().cpu().numpy()
+    assert rel_max_abs(lg[rows], oracle.lm_head_rows(om, res, rows, mode=mode, act=act)) < TOL[act]
+    assert int(dec.tok[0]) == oracle.argmax_first(lg)
+    assert api.check_device_error() == 0
+
+
+def test_qwen3_06b_model_teacher_forced(cuda_lib):
+    """Qwen3-0.6B-shaped model (28 layers, tied head) at context 2048: 3 steps checked."""
+    mt = synth.make_model(synth.QWEN3_06B, "bf16", 5, DEV, ctx=2048, steps=3)
+    dec = api.Decoder(mt, max_steps=3)
+    st = {}
+    teacher_forced(dec, mt, 3, "bf16", "bf16", log=st)
+    assert st["strict"] >= 2

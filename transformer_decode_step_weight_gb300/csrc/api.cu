@@ -1,0 +1,541 @@
+// C ABI of libqd.so: argument validation, the decode-step schedule and the
+// whole-step CUDA graph. Kernels live in the other translation units.
+//
+// "GPU Kernel Lab" README, "Decode integration": the order of one decode step
+// and its fixed-address CUDA graph replay. "emit_qwen38_generate" rustdoc,
+// "Where the speed comes from": one launch per shared activation, one graph per
+// token with token/position advanced on the device, residual + norm (+ Q8
+// re-quantisation) fused into one kernel.
+#include "qd.h"
+#include "kernels.h"
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+namespace qd {
+
+static thread_local std::string g_last_error;
+
+static int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+static int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  return fail(QD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Sticky device error word; kernels receive its device address.
+__device__ int g_dev_error = 0;
+
+static int* dev_error_ptr() {
+  static int* ptr[64] = {nullptr};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
+    ptr[dev] = (int*)p;
+  }
+  return ptr[dev];
+}
+
+const DevInfo& dev_info() {
+  static DevInfo info[64];
+  static bool have[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!have[dev]) {
+    cudaDeviceGetAttribute(&info[dev].sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&info[dev].max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (info[dev].sm_count <= 0) info[dev].sm_count = 1;
+    have[dev] = true;
+  }
+  return info[dev];
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static Launch make_launch(cudaStream_t s, bool pdl) {
+  Launch L;
+  L.stream = s;
+  L.pdl = pdl;
+  L.err = dev_error_ptr();
+  return L;
+}
+
+}  // namespace qd
+
+using namespace qd;
+
+struct qd_layer {
+  qd_layer_dims dims;
+  qd_layer_weights w;
+};
+
+struct qd_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+  int steps;
+};
+
+extern "C" {
+
+const char* qd_last_error(void) { return qd::g_last_error.c_str(); }
+int qd_version(void) { return 1; }
+
+// ------------------------------------------------------------------ GEMVs
+int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32, float* y, int batch,
+                 cudaStream_t stream) {
+  if (!W || !x || !y) return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: null pointer");
+  if (rows < 1 || cols < 8) return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: rows=%d cols=%d", rows, cols);
+  if (!gemv_bf16_supported(cols, batch))
+    return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: cols=%d batch=%d (need cols%%8==0, cols<=32768, 1<=batch<=8)",
+                cols, batch);
+  if (!aligned16(W) || !aligned16(x) || !aligned16(y))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: pointers must be 16-byte aligned");
+  GemvBf16Args a;
+  a.W = W; a.R = rows; a.K = cols; a.batch = batch;
+  a.pro = x_is_f32 ? PRO_X_F32 : PRO_X_BF16;
+  a.x = x; a.norm_w = nullptr; a.eps = 0.f;
+  a.epi = EPI_STORE; a.y = y;
+  cudaError_t e = launch_gemv_bf16(a, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_bf16");
+}
+
+int qd_gemv_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const float* x_f32,
+                 const int8_t* x_q, const void* x_d_f16, qd_act act, float* y, cudaStream_t stream) {
+  if (!qs || !d_f16 || !y) return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: null pointer");
+  if (rows < 1 || cols < 32 || cols % 32) return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: rows=%d cols=%d", rows, cols);
+  if (!gemv_q8_supported(cols)) return fail(QD_ERR_UNSUPPORTED, "qd_gemv_q8_0: cols=%d too large", cols);
+  if (act == QD_ACT_F32 && !x_f32) return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: f32 lane needs x_f32");
+  if (act == QD_ACT_I8 && !(x_q && x_d_f16) && !x_f32)
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: i8 lane needs x_q and x_d (or x_f32 to quantise)");
+  if (act != QD_ACT_F32 && act != QD_ACT_I8) return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: bad act");
+  if (!aligned16(qs) || !aligned16(y) || (x_f32 && !aligned16(x_f32)) || (x_q && !aligned16(x_q)))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: pointers must be 16-byte aligned");
+  if (((uintptr_t)d_f16 & 1u) || (x_d_f16 && ((uintptr_t)x_d_f16 & 1u)))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: scale pointers must be 2-byte aligned");
+  GemvQ8Args a;
+  a.qs = qs; a.d = d_f16; a.R = rows; a.K = cols; a.act = act;
+  a.pro = PRO_X_F32; a.x = x_f32;
+  a.xq = (act == QD_ACT_I8 && x_q && x_d_f16) ? x_q : nullptr; a.xd = x_d_f16;
+  a.norm_w = nullptr; a.eps = 0.f; a.epi = EPI_STORE; a.y = y;
+  cudaError_t e = launch_gemv_q8(a, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_q8_0");
+}
+
+int qd_quantize_q8_0(const float* x, int n, int8_t* x_q, void* x_d_f16, cudaStream_t stream) {
+  if (!x || !x_q || !x_d_f16) return fail(QD_ERR_INVALID_ARG, "qd_quantize_q8_0: null pointer");
+  if (n < 0 || n % 32) return fail(QD_ERR_INVALID_ARG, "qd_quantize_q8_0: n=%d must be a multiple of 32", n);
+  if (n == 0) return QD_OK;
+  cudaError_t e = launch_quantize_q8(x, n, x_q, x_d_f16, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_quantize_q8_0");
+}
+
+// ------------------------------------------------------------------ attention
+size_t qd_attn_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int max_ctx) {
+  if (batch < 1 || n_kv_heads < 1 || n_q_heads < n_kv_heads || max_ctx < 1) return 0;
+  return attn_workspace_bytes(batch, n_q_heads, n_kv_heads, max_ctx);
+}
+
+static int check_attn_shape(const char* fn, int batch, int hq, int hkv, int hd, int ps, int max_pages,
+                            int n_pages) {
+  if (batch < 1 || hq < 1 || hkv < 1 || ps < 1 || max_pages < 1 || n_pages < 1)
+    return fail(QD_ERR_INVALID_ARG, "%s: bad sizes batch=%d hq=%d hkv=%d page_size=%d max_pages=%d n_pages=%d", fn,
+                batch, hq, hkv, ps, max_pages, n_pages);
+  if (hd != 128) return fail(QD_ERR_UNSUPPORTED, "%s: head_dim=%d (only 128)", fn, hd);
+  if (hq % hkv) return fail(QD_ERR_INVALID_ARG, "%s: n_q_heads %% n_kv_heads != 0", fn);
+  const int rep = hq / hkv;
+  if (rep != 1 && rep != 2 && rep != 4 && rep != 8)
+    return fail(QD_ERR_UNSUPPORTED, "%s: n_q_heads/n_kv_heads=%d (supported 1, 2, 4, 8)", fn, rep);
+  if ((long long)max_pages * ps > (1LL << 30)) return fail(QD_ERR_INVALID_ARG, "%s: context too large", fn);
+  return QD_OK;
+}
+
+int qd_attn_decode_paged(const float* q, const void* k_pages, const void* v_pages, const int32_t* page_table,
+                         const int32_t* seq_lens, int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                         int page_size, int max_pages, int n_pages, float scale, float* out, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_attn_shape("qd_attn_decode_paged", batch, n_q_heads, n_kv_heads, head_dim, page_size, max_pages,
+                            n_pages);
+  if (rc) return rc;
+  if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out || !workspace)
+    return fail(QD_ERR_INVALID_ARG, "qd_attn_decode_paged: null pointer");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) || !aligned16(workspace))
+    return fail(QD_ERR_INVALID_ARG, "qd_attn_decode_paged: pointers must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(QD_ERR_INVALID_ARG, "qd_attn_decode_paged: scale not finite");
+  const int max_ctx = max_pages * page_size;
+  const size_t need = attn_workspace_bytes(batch, n_q_heads, n_kv_heads, max_ctx);
+  if (workspace_bytes < need)
+    return fail(QD_ERR_WORKSPACE, "qd_attn_decode_paged: workspace %zu < %zu bytes", workspace_bytes, need);
+  AttnArgs a = {};
+  a.q = q; a.seq_lens = seq_lens;
+  a.k_pages = (void*)k_pages; a.v_pages = (void*)v_pages; a.page_table = page_table;
+  a.B = batch; a.Hq = n_q_heads; a.Hkv = n_kv_heads; a.D = head_dim;
+  a.page_size = page_size; a.max_pages = max_pages; a.n_pages = n_pages;
+  a.scale = scale; a.out_f32 = out; a.workspace = workspace; a.ws_bytes = workspace_bytes; a.max_ctx = max_ctx;
+  cudaError_t e = launch_attention(a, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_attn_decode_paged");
+}
+
+// ------------------------------------------------------------------ argmax
+size_t qd_argmax_workspace_bytes(int batch) { return batch < 1 ? 0 : argmax_workspace_bytes(batch); }
+
+int qd_argmax_advance(const float* logits, int vocab, int batch, int32_t* tok, int32_t* pos, int32_t* step,
+                      int32_t* out_tokens, int max_steps, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  if (!logits || !tok || !pos || !step || !out_tokens || !workspace)
+    return fail(QD_ERR_INVALID_ARG, "qd_argmax_advance: null pointer");
+  if (vocab < 1 || batch < 1 || max_steps < 1)
+    return fail(QD_ERR_INVALID_ARG, "qd_argmax_advance: vocab=%d batch=%d max_steps=%d", vocab, batch, max_steps);
+  if (workspace_bytes < argmax_workspace_bytes(batch))
+    return fail(QD_ERR_WORKSPACE, "qd_argmax_advance: workspace too small");
+  cudaError_t e = launch_argmax_advance(logits, vocab, batch, tok, pos, step, out_tokens, max_steps, workspace,
+                                        make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_argmax_advance");
+}
+
+int qd_rope_table_init(float* table, int max_pos, int head_dim, float theta, cudaStream_t stream) {
+  if (!table || max_pos < 1 || head_dim < 2 || head_dim % 2 || !(theta > 0.f))
+    return fail(QD_ERR_INVALID_ARG, "qd_rope_table_init: bad arguments");
+  cudaError_t e = launch_rope_table(table, max_pos, head_dim, theta, stream);
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_rope_table_init");
+}
+
+// ------------------------------------------------------------------ layers
+int qd_create_layer(const qd_layer_dims* d, const qd_layer_weights* w, qd_layer** out) {
+  if (!d || !w || !out) return fail(QD_ERR_INVALID_ARG, "qd_create_layer: null pointer");
+  *out = nullptr;
+  if (d->hidden < 32 || d->ffn < 32 || d->n_q_heads < 1 || d->n_kv_heads < 1)
+    return fail(QD_ERR_INVALID_ARG, "qd_create_layer: bad dims");
+  if (d->head_dim != 128) return fail(QD_ERR_UNSUPPORTED, "qd_create_layer: head_dim=%d (only 128)", d->head_dim);
+  if (d->n_q_heads % d->n_kv_heads) return fail(QD_ERR_INVALID_ARG, "qd_create_layer: Hq %% Hkv != 0");
+  const int rep = d->n_q_heads / d->n_kv_heads;
+  if (rep != 1 && rep != 2 && rep != 4 && rep != 8) return fail(QD_ERR_UNSUPPORTED, "qd_create_layer: Hq/Hkv=%d", rep);
+  if (!(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f)) return fail(QD_ERR_INVALID_ARG, "qd_create_layer: eps/theta");
+  if (!w->w_qkv || !w->w_o || !w->w_gu || !w->w_down || !w->ln_in || !w->ln_post || !w->q_norm || !w->k_norm)
+    return fail(QD_ERR_INVALID_ARG, "qd_create_layer: null weight pointer");
+  const int qdim = d->n_q_heads * d->head_dim;
+  if (d->wtype == QD_W_BF16) {
+    if (d->hidden % 8 || d->ffn % 8 || !gemv_bf16_supported(d->hidden, 1) || !gemv_bf16_supported(d->ffn, 1) ||
+        !gemv_bf16_supported(qdim, 1))
+      return fail(QD_ERR_UNSUPPORTED, "qd_create_layer: bf16 dims not supported");
+  } else if (d->wtype == QD_W_Q8_0) {
+    if (d->hidden % 32 || d->ffn % 32 || !gemv_q8_supported(d->hidden) || !gemv_q8_supported(d->ffn) ||
+        !gemv_q8_supported(qdim))
+      return fail(QD_ERR_UNSUPPORTED, "qd_create_layer: Q8_0 dims need multiples of 32");
+    if (!w->s_qkv || !w->s_o || !w->s_gu || !w->s_down)
+      return fail(QD_ERR_INVALID_ARG, "qd_create_layer: Q8_0 scales missing");
+    if (d->act != QD_ACT_F32 && d->act != QD_ACT_I8) return fail(QD_ERR_INVALID_ARG, "qd_create_layer: bad act");
+  } else {
+    return fail(QD_ERR_INVALID_ARG, "qd_create_layer: bad wtype");
+  }
+  const void* ptrs[] = {w->w_qkv, w->w_o, w->w_gu, w->w_down, w->ln_in, w->ln_post, w->q_norm, w->k_norm};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(QD_ERR_INVALID_ARG, "qd_create_layer: weights must be 16-byte aligned");
+  qd_layer* l = new qd_layer;
+  l->dims = *d;
+  l->w = *w;
+  *out = l;
+  return QD_OK;
+}
+
+int qd_destroy_layer(qd_layer* layer) {
+  delete layer;
+  return QD_OK;
+}
+
+// ------------------------------------------------------------------ decode step
+namespace {
+
+struct StepWs {
+  float* res;       // [B, H]
+  float* qkv;       // [B, QKV]
+  void* attn;       // [B, Hq*D] bf16 or f32
+  float* gu;        // [B, 2F]
+  void* attn_ws;
+  void* argmax_ws;
+  size_t total;
+};
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+StepWs step_ws_layout(const qd_step_args* a, void* base) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const int B = a->batch;
+  const size_t qkv = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+  unsigned char* p = (unsigned char*)base;
+  StepWs w;
+  size_t off = 0;
+  w.res = (float*)(p + off); off += al256((size_t)B * d.hidden * 4);
+  w.qkv = (float*)(p + off); off += al256((size_t)B * qkv * 4);
+  w.attn = (void*)(p + off); off += al256((size_t)B * d.n_q_heads * d.head_dim * 4);
+  w.gu = (float*)(p + off); off += al256((size_t)B * 2 * d.ffn * 4);
+  w.attn_ws = (void*)(p + off);
+  off += al256(attn_workspace_bytes(B, d.n_q_heads, d.n_kv_heads, a->max_pages * a->page_size));
+  w.argmax_ws = (void*)(p + off); off += al256(argmax_workspace_bytes(B));
+  w.total = off;
+  return w;
+}
+
+int validate_step(const qd_step_args* a) {
+  if (!a) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: null args");
+  if (!a->layers || a->n_layers < 1) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: no layers");
+  for (int i = 0; i < a->n_layers; ++i)
+    if (!a->layers[i]) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: layer %d is null", i);
+  const qd_layer_dims& d0 = a->layers[0]->dims;
+  for (int i = 1; i < a->n_layers; ++i) {
+    const qd_layer_dims& d = a->layers[i]->dims;
+    if (d.hidden != d0.hidden || d.n_q_heads != d0.n_q_heads || d.n_kv_heads != d0.n_kv_heads ||
+        d.head_dim != d0.head_dim || d.ffn != d0.ffn || d.wtype != d0.wtype || d.act != d0.act)
+      return fail(QD_ERR_INVALID_ARG, "qd_decode_step: layer %d dims differ from layer 0", i);
+  }
+  if (!a->embed || !a->final_norm || !a->lm_head || !a->k_cache || !a->v_cache || !a->page_table ||
+      !a->rope_table || !a->tok || !a->pos || !a->step || !a->out_tokens || !a->logits || !a->workspace)
+    return fail(QD_ERR_INVALID_ARG, "qd_decode_step: null pointer");
+  for (int i = 0; i < a->n_layers; ++i)
+    if (!a->k_cache[i] || !a->v_cache[i] || !aligned16(a->k_cache[i]) || !aligned16(a->v_cache[i]))
+      return fail(QD_ERR_INVALID_ARG, "qd_decode_step: cache %d null or unaligned", i);
+  if (a->vocab < 1 || a->max_steps < 1) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: vocab/max_steps");
+  if (a->batch < 1 || a->batch > 8)
+    return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batch=%d (the GEMV step supports 1..8)", a->batch);
+  if (d0.wtype == QD_W_Q8_0 && a->batch != 1)
+    return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 step supports batch 1");
+  if (d0.wtype == QD_W_BF16) {
+    const int ks[3] = {d0.hidden, d0.n_q_heads * d0.head_dim, d0.ffn};
+    for (int k : ks)
+      if (!gemv_bf16_supported(k, a->batch))
+        return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: GEMV K=%d with batch %d not supported", k, a->batch);
+  }
+  int rc = check_attn_shape("qd_decode_step", a->batch, d0.n_q_heads, d0.n_kv_heads, d0.head_dim, a->page_size,
+                            a->max_pages, a->n_pages);
+  if (rc) return rc;
+  if (a->rope_max_pos < 1) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: rope_max_pos");
+  const bool q8_head = a->lm_head_scales != nullptr;
+  if (q8_head) {
+    if (!gemv_q8_supported(d0.hidden)) return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 head dims");
+    if (a->batch != 1) return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 LM head supports batch 1");
+  }
+  if (!aligned16(a->embed) || !aligned16(a->lm_head) || !aligned16(a->logits) || !aligned16(a->workspace))
+    return fail(QD_ERR_INVALID_ARG, "qd_decode_step: pointers must be 16-byte aligned");
+  const StepWs w = step_ws_layout(a, a->workspace);
+  if (a->workspace_bytes < w.total)
+    return fail(QD_ERR_WORKSPACE, "qd_decode_step: workspace %zu < %zu bytes", a->workspace_bytes, w.total);
+  return QD_OK;
+}
+
+#define QD_TRY(expr, what)                        \
+  do {                                            \
+    cudaError_t e_ = (expr);                      \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+int run_step(const qd_step_args* a, cudaStream_t stream) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const StepWs w = step_ws_layout(a, a->workspace);
+  const Launch L = make_launch(stream, true);
+  const int B = a->batch;
+  const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int QKV = (Hq + 2 * Hkv) * D;
+  const bool q8 = d.wtype == QD_W_Q8_0;
+
+  QD_TRY(launch_embed(a->embed, H, a->vocab, a->tok, B, w.res, L), "embed");
+  for (int li = 0; li < a->n_layers; ++li) {
+    const qd_layer* l = a->layers[li];
+    // QKV projection, RMSNorm(res; ln_in) fused into the prologue
+    if (q8) {
+      GemvQ8Args g = {};
+      g.qs = (const int8_t*)l->w.w_qkv; g.d = l->w.s_qkv; g.R = QKV; g.K = H; g.act = d.act;
+      g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = l->w.ln_in; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.qkv;
+      QD_TRY(launch_gemv_q8(g, L), "qkv gemv q8");
+    } else {
+      GemvBf16Args g = {};
+      g.W = l->w.w_qkv; g.R = QKV; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
+      g.norm_w = l->w.ln_in; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.qkv;
+      QD_TRY(launch_gemv_bf16(g, L), "qkv gemv");
+    }
+    // QK-norm + RoPE + K/V cache write + split-KV attention + combine
+    AttnArgs at = {};
+    at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
+    at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps;
+    at.pos = a->pos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = a->page_table;
+    at.B = B; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
+    at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D);
+    if (q8) at.out_f32 = (float*)w.attn;
+    else at.out_bf16 = w.attn;
+    at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size;
+    QD_TRY(launch_attention(at, L), "attention");
+    // O projection + residual add
+    if (q8) {
+      GemvQ8Args g = {};
+      g.qs = (const int8_t*)l->w.w_o; g.d = l->w.s_o; g.R = H; g.K = Hq * D; g.act = d.act;
+      g.pro = PRO_X_F32; g.x = w.attn; g.epi = EPI_RESID_ADD; g.y = w.res;
+      QD_TRY(launch_gemv_q8(g, L), "o gemv q8");
+    } else {
+      GemvBf16Args g = {};
+      g.W = l->w.w_o; g.R = H; g.K = Hq * D; g.batch = B; g.pro = PRO_X_BF16; g.x = w.attn;
+      g.epi = EPI_RESID_ADD; g.y = w.res;
+      QD_TRY(launch_gemv_bf16(g, L), "o gemv");
+    }
+    // gate+up projection, RMSNorm(res; ln_post) fused into the prologue
+    if (q8) {
+      GemvQ8Args g = {};
+      g.qs = (const int8_t*)l->w.w_gu; g.d = l->w.s_gu; g.R = 2 * F; g.K = H; g.act = d.act;
+      g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = l->w.ln_post; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.gu;
+      QD_TRY(launch_gemv_q8(g, L), "gu gemv q8");
+    } else {
+      GemvBf16Args g = {};
+      g.W = l->w.w_gu; g.R = 2 * F; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
+      g.norm_w = l->w.ln_post; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.gu;
+      QD_TRY(launch_gemv_bf16(g, L), "gu gemv");
+    }
+    // down projection with SwiGLU formed on load, + residual add
+    if (q8) {
+      GemvQ8Args g = {};
+      g.qs = (const int8_t*)l->w.w_down; g.d = l->w.s_down; g.R = H; g.K = F; g.act = d.act;
+      g.pro = PRO_SWIGLU; g.x = w.gu; g.epi = EPI_RESID_ADD; g.y = w.res;
+      QD_TRY(launch_gemv_q8(g, L), "down gemv q8");
+    } else {
+      GemvBf16Args g = {};
+      g.W = l->w.w_down; g.R = H; g.K = F; g.batch = B; g.pro = PRO_SWIGLU; g.x = w.gu;
+      g.epi = EPI_RESID_ADD; g.y = w.res;
+      QD_TRY(launch_gemv_bf16(g, L), "down gemv");
+    }
+  }
+  // final RMSNorm + LM head
+  if (a->lm_head_scales) {
+    GemvQ8Args g = {};
+    g.qs = (const int8_t*)a->lm_head; g.d = a->lm_head_scales; g.R = a->vocab; g.K = H; g.act = a->lm_act;
+    g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = a->final_norm; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = a->logits;
+    QD_TRY(launch_gemv_q8(g, L), "lm head q8");
+  } else {
+    GemvBf16Args g = {};
+    g.W = a->lm_head; g.R = a->vocab; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
+    g.norm_w = a->final_norm; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = a->logits;
+    QD_TRY(launch_gemv_bf16(g, L), "lm head");
+  }
+  QD_TRY(launch_argmax_advance(a->logits, a->vocab, B, a->tok, a->pos, a->step, a->out_tokens, a->max_steps,
+                               w.argmax_ws, L),
+         "argmax");
+  return QD_OK;
+}
+
+}  // namespace
+
+size_t qd_step_workspace_bytes(const qd_step_args* a) {
+  if (!a || !a->layers || a->n_layers < 1 || !a->layers[0] || a->batch < 1) return 0;
+  return step_ws_layout(a, nullptr).total;
+}
+
+int qd_step_launch_count(const qd_step_args* a) {
+  if (!a || a->n_layers < 1) return 0;
+  return 1 + 5 * a->n_layers + 2;
+}
+
+int qd_decode_step(const qd_step_args* a, cudaStream_t stream) {
+  int rc = validate_step(a);
+  if (rc) return rc;
+  return run_step(a, stream);
+}
+
+int qd_graph_create(const qd_step_args* a, int steps_per_launch, cudaStream_t stream, qd_graph** out) {
+  if (!out) return fail(QD_ERR_INVALID_ARG, "qd_graph_create: null out");
+  *out = nullptr;
+  if (steps_per_launch < 1 || steps_per_launch > 4096)
+    return fail(QD_ERR_INVALID_ARG, "qd_graph_create: steps_per_launch=%d", steps_per_launch);
+  int rc = validate_step(a);
+  if (rc) return rc;
+  if (stream == 0) return fail(QD_ERR_INVALID_ARG, "qd_graph_create: capture needs a non-default stream");
+  cudaStreamCaptureStatus st;
+  QD_TRY(cudaStreamIsCapturing(stream, &st), "qd_graph_create");
+  if (st != cudaStreamCaptureStatusNone) return fail(QD_ERR_INVALID_ARG, "qd_graph_create: stream is capturing");
+  QD_TRY(cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal), "begin capture");
+  for (int i = 0; i < steps_per_launch; ++i) {
+    rc = run_step(a, stream);
+    if (rc) {
+      cudaGraph_t g;
+      cudaStreamEndCapture(stream, &g);
+      if (g) cudaGraphDestroy(g);
+      return rc;
+    }
+  }
+  cudaGraph_t graph;
+  QD_TRY(cudaStreamEndCapture(stream, &graph), "end capture");
+  cudaGraphExec_t exec;
+  cudaError_t e = cudaGraphInstantiate(&exec, graph, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return cuda_fail(e, "graph instantiate");
+  }
+  qd_graph* g = new qd_graph;
+  g->graph = graph;
+  g->exec = exec;
+  g->steps = steps_per_launch;
+  *out = g;
+  return QD_OK;
+}
+
+int qd_graph_launch(qd_graph* g, cudaStream_t stream) {
+  if (!g) return fail(QD_ERR_INVALID_ARG, "qd_graph_launch: null graph");
+  QD_TRY(cudaGraphLaunch(g->exec, stream), "graph launch");
+  return QD_OK;
+}
+
+int qd_graph_destroy(qd_graph* g) {
+  if (!g) return QD_OK;
+  cudaGraphExecDestroy(g->exec);
+  cudaGraphDestroy(g->graph);
+  delete g;
+  return QD_OK;
+}
+
+int qd_check_device_error(cudaStream_t stream, int* bits) {
+  if (!bits) return fail(QD_ERR_INVALID_ARG, "qd_check_device_error: null bits");
+  *bits = 0;
+  int* p = dev_error_ptr();
+  if (!p) return fail(QD_ERR_CUDA, "qd_check_device_error: no device error word");
+  int v = 0;
+  QD_TRY(cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, stream), "read error word");
+  QD_TRY(cudaStreamSynchronize(stream), "sync");
+  const int zero = 0;
+  QD_TRY(cudaMemcpyAsync(p, &zero, sizeof(int), cudaMemcpyHostToDevice, stream), "clear error word");
+  QD_TRY(cudaStreamSynchronize(stream), "sync");
+  *bits = v;
+  return QD_OK;
+}
+
+// ------------------------------------------------------------------ test exports
+int qd_debug_q8_block_dots(const int8_t* qs, int rows, int cols, const int8_t* x_q, int32_t* dots,
+                           cudaStream_t stream) {
+  if (!qs || !x_q || !dots || rows < 1 || cols < 32 || cols % 32)
+    return fail(QD_ERR_INVALID_ARG, "qd_debug_q8_block_dots: bad arguments");
+  if (!aligned16(qs) || !aligned16(x_q)) return fail(QD_ERR_INVALID_ARG, "qd_debug_q8_block_dots: alignment");
+  cudaError_t e = launch_q8_block_dots(qs, rows, cols, x_q, dots, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_debug_q8_block_dots");
+}
+
+int qd_debug_paged_indices(const int32_t* page_table, int batch, int max_pages, int page_size, int n_tokens,
+                           int32_t* idx, cudaStream_t stream) {
+  if (!page_table || !idx || batch < 1 || max_pages < 1 || page_size < 1 || n_tokens < 0 ||
+      (long long)n_tokens > (long long)max_pages * page_size)
+    return fail(QD_ERR_INVALID_ARG, "qd_debug_paged_indices: bad arguments");
+  cudaError_t e = launch_paged_indices(page_table, batch, max_pages, page_size, n_tokens, idx, stream);
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_debug_paged_indices");
+}
+
+}  // extern "C"

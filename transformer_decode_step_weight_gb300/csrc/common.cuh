@@ -1,0 +1,132 @@
+// Shared device helpers for the sm_103a decode kernels: streaming loads,
+// programmatic-dependent-launch controls, bf16 widening, reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "qd.h"
+
+#define QD_DEV __device__ __forceinline__
+
+namespace qd {
+
+// L2 policy for data read exactly once (weights, KV): evict first, so streamed
+// bytes do not push the small re-used activations out of L2.
+QD_DEV uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 128-bit streaming load through the non-coherent path without L1 allocation.
+QD_DEV uint4 ld_stream(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+QD_DEV uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Programmatic dependent launch. wait(): block until the grids this launch
+// depends on have completed and their memory is visible. Every kernel calls it
+// before touching memory written by an earlier kernel of the step, and before
+// its own first global write. launch_dependents(): allow the next kernel in
+// the stream to be scheduled now (it still waits before reading our results).
+QD_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QD_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// bf16 pair (packed in a 32-bit word, low half first) -> two floats, exactly.
+QD_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+QD_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// binary32 -> bf16 bits, round to nearest even (finite inputs).
+QD_DEV uint32_t f2bf_bits(float f) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+QD_DEV float round_bf16(float f) { return __uint_as_float(f2bf_bits(f) << 16); }
+
+QD_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+QD_DEV float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Sticky device error word (bits QD_DEVERR_*), one per process.
+QD_DEV void set_error(int* err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+}  // namespace qd
+
+// ---------------------------------------------------------------------------
+// Asynchronous bulk copies (TMA, non-tensor form) completing on an mbarrier.
+namespace qd {
+
+QD_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+QD_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+QD_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+QD_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+QD_DEV bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+QD_DEV uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for `phase` of the barrier to complete, giving up after about one
+// second (sets QD_DEVERR_TIMEOUT = 16 and returns false). Never unbounded.
+QD_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, int* err) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const uint64_t t0 = global_ns();
+  for (int i = 0; i < (1 << 24); ++i) {
+    if (mbar_try_wait(bar, phase)) return true;
+    if ((i & 255) == 255 && global_ns() - t0 > 1000000000ull) break;
+  }
+  set_error(err, QD_DEVERR_TIMEOUT);
+  return false;
+}
+
+// Global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.
+QD_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace qd

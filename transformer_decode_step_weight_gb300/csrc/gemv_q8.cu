@@ -1,0 +1,359 @@
+// Q8_0 weight-streaming GEMV, both activation lanes, and the activation
+// re-quantiser.
+//
+// "emit_qwen38_generate" rustdoc, "Where the speed comes from": at batch 1 a
+// Q8_0 GEMV reads the whole weight matrix and one activation vector, so it is
+// memory bound in either lane. ``deq`` selects the lane: activations kept in
+// f32 and every weight dequantised (~3 float operations per weight), or the
+// activation re-quantised per 32-block to int8 so the inner product is an
+// exact int32 dp4a sum scaled by both block scales. Item 3 of the same section
+// fuses the residual add, the next RMSNorm and the activation re-quantisation
+// into one kernel: here they are the GEMV's prologue, computed per CTA.
+//
+// Layout: int8 values [R, K] and f16 scales [R, K/32] as two arrays. A thread
+// owns C 16-weight half-blocks of every row of its CTA (one 16-byte value load
+// and one 2-byte scale load each; the two halves of a block sit in adjacent
+// lanes), so its activation slice — f32, or int8 plus scale — sits in
+// registers. Dequantisation in the f32 lane builds each
+// float from the byte with one byte-permute into the exponent pattern of 2^23
+// and one exact subtraction (2^23 + u - (2^23 + 128) = q).
+#include "common.cuh"
+#include "kernels.h"
+#include "launch.cuh"
+
+#include <algorithm>
+
+namespace qd {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSmemBudget = 96 * 1024;
+
+struct Q8Params {
+  const int8_t* qs;
+  const __half* d;
+  int R, K;
+  int rows_base, rows_extra;
+  int T, P, phase_rows;
+  int pro;
+  const float* x;
+  const int8_t* xq;
+  const __half* xd;
+  const __nv_bfloat16* norm_w;
+  float eps;
+  int epi;
+  float* y;
+};
+
+QD_DEV uint16_t ld_stream_u16(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// 4 signed bytes -> 4 exact floats
+QD_DEV void i8x4_to_f32(uint32_t w, float* f) {
+  const uint32_t u = w ^ 0x80808080u;
+  f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.0f;
+  f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.0f;
+  f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.0f;
+  f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.0f;
+}
+
+QD_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// Prologue that takes an already quantised activation (int8 + f16 scales).
+constexpr int PRO_Q8_GIVEN = 16;
+
+template <int C, int LANE, int U>
+__global__ void __launch_bounds__(kThreads, 1) gemv_q8_kernel(const Q8Params p) {
+  extern __shared__ float red[];
+  __shared__ float s_ss[kThreads / 32];
+  const int tid = threadIdx.x;
+  const int T = p.T, P = p.P, K = p.K, KB = p.K / 32, KC = p.K / 16;
+  const int g = tid / T, t = tid - g * T;
+  const int wpg = T >> 5, wig = t >> 5, lane = tid & 31;
+  const int nrows = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
+  const int r0 = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
+
+  // this thread owns 16-weight half-blocks ch[j] of every row (two threads per block)
+  int ch[C];
+  bool cv[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) {
+    ch[j] = j * T + t;
+    cv[j] = ch[j] < KC;
+  }
+
+  uint4 wq[U][C];
+  uint16_t wd[U][C];
+  auto load_batch = [&](int ph0, int nph, int k0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int lr = g + P * (k0 + u);
+      const bool ok = lr < nph;
+      const size_t r = (size_t)(r0 + ph0 + lr);
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (ok && cv[j]) {
+          wq[u][j] = ld_stream(p.qs + r * K + (size_t)ch[j] * 16);
+          wd[u][j] = ld_stream_u16(p.d + r * KB + (ch[j] >> 1));
+        } else {
+          wq[u][j] = make_uint4(0u, 0u, 0u, 0u);
+          wd[u][j] = 0;
+        }
+      }
+    }
+  };
+
+  load_batch(0, min(p.phase_rows, nrows), 0);
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // ---- activation half-blocks (f32), then the lane's form of them
+  float xf[C][16];
+  uint32_t xq[C][4];
+  float xd[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) xf[j][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) xq[j][e] = 0u;
+    xd[j] = 0.f;
+  }
+  if (p.pro == PRO_Q8_GIVEN) {
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      if (!cv[j]) continue;
+      const uint4 a = *(const uint4*)(p.xq + (size_t)ch[j] * 16);
+      xq[j][0] = a.x; xq[j][1] = a.y; xq[j][2] = a.z; xq[j][3] = a.w;
+      xd[j] = __half2float(p.xd[ch[j] >> 1]);
+    }
+  } else {
+    if (p.pro == PRO_SWIGLU) {
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (!cv[j]) continue;
+        const float* gp = p.x + (size_t)ch[j] * 16;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 gg = *(const float4*)(gp + e), uu = *(const float4*)(gp + K + e);
+          xf[j][e] = silu(gg.x) * uu.x;
+          xf[j][e + 1] = silu(gg.y) * uu.y;
+          xf[j][e + 2] = silu(gg.z) * uu.z;
+          xf[j][e + 3] = silu(gg.w) * uu.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (!cv[j]) continue;
+        const float* xp = p.x + (size_t)ch[j] * 16;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 a = *(const float4*)(xp + e);
+          xf[j][e] = a.x; xf[j][e + 1] = a.y; xf[j][e + 2] = a.z; xf[j][e + 3] = a.w;
+        }
+      }
+      if (p.pro == PRO_RMSNORM) {
+        float s = 0.f;
+        if (g == 0) {
+#pragma unroll
+          for (int j = 0; j < C; ++j)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s = fmaf(xf[j][e], xf[j][e], s);
+        }
+        s = warp_sum(s);
+        if (lane == 0) s_ss[tid >> 5] = s;
+        __syncthreads();
+        float tot = 0.f;
+        for (int i = 0; i < wpg; ++i) tot += s_ss[i];
+        const float inv = 1.0f / sqrtf(tot / (float)K + p.eps);
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+          if (!cv[j]) continue;
+#pragma unroll
+          for (int e = 0; e < 16; e += 8) {
+            const uint4 wn = *(const uint4*)(p.norm_w + (size_t)ch[j] * 16 + e);
+            const float nw[8] = {bf_lo(wn.x), bf_hi(wn.x), bf_lo(wn.y), bf_hi(wn.y),
+                                 bf_lo(wn.z), bf_hi(wn.z), bf_lo(wn.w), bf_hi(wn.w)};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) xf[j][e + k] = nw[k] * (xf[j][e + k] * inv);
+          }
+        }
+      }
+    }
+    if (LANE == 1) {
+      // re-quantise per 32-block: the two halves of a block sit in lanes t, t^1
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(xf[j][e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const float d = amax / 127.0f;
+        const float id = d != 0.0f ? 1.0f / d : 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t packed = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            int v = (int)roundf(xf[j][w * 4 + k] * id);
+            v = max(-127, min(127, v));
+            packed |= ((uint32_t)(v & 0xff)) << (8 * k);
+          }
+          xq[j][w] = packed;
+        }
+        xd[j] = __half2float(__float2half_rn(d));
+      }
+    }
+  }
+
+  for (int ph0 = 0; ph0 < nrows; ph0 += p.phase_rows) {
+    const int nph = min(p.phase_rows, nrows - ph0);
+    const int nk = (g < nph) ? (nph - g + P - 1) / P : 0;
+    const int nbat = (nk + U - 1) / U;
+    if (ph0 > 0) load_batch(ph0, nph, 0);
+    for (int bi = 0; bi < nbat; ++bi) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int lr = g + P * (bi * U + u);
+        if (lr < nph) {
+          float s = 0.f;
+#pragma unroll
+          for (int j = 0; j < C; ++j) {
+            const uint32_t wv[4] = {wq[u][j].x, wq[u][j].y, wq[u][j].z, wq[u][j].w};
+            const float dw = __half2float(__ushort_as_half(wd[u][j]));
+            if (LANE == 0) {
+              float bs = 0.f;
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                float f[4];
+                i8x4_to_f32(wv[w], f);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) bs = fmaf(f[k], xf[j][w * 4 + k], bs);
+              }
+              s = fmaf(dw, bs, s);
+            } else {
+              int acc = 0;
+#pragma unroll
+              for (int w = 0; w < 4; ++w) acc = __dp4a((int)wv[w], (int)xq[j][w], acc);
+              s = fmaf((float)acc, dw * xd[j], s);
+            }
+          }
+          s = warp_sum(s);
+          if (lane == 0) red[lr * wpg + wig] = s;
+        }
+      }
+      if (bi + 1 < nbat) load_batch(ph0, nph, (bi + 1) * U);
+    }
+    __syncthreads();
+    for (int i = tid; i < nph; i += blockDim.x) {
+      float s = 0.f;
+      for (int k = 0; k < wpg; ++k) s += red[i * wpg + k];
+      float* yp = p.y + r0 + ph0 + i;
+      if (p.epi == EPI_RESID_ADD) *yp += s;
+      else *yp = s;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void quantize_q8_kernel(const float* x, int n, int8_t* xq, __half* xd) {
+  const int blk = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (blk * 32 >= n) return;
+  const float v = x[blk * 32 + lane];
+  const float amax = warp_max(fabsf(v));
+  const float d = amax / 127.0f;
+  const float id = d != 0.0f ? 1.0f / d : 0.0f;
+  int q = (int)roundf(v * id);
+  q = max(-127, min(127, q));
+  xq[blk * 32 + lane] = (int8_t)q;
+  if (lane == 0) xd[blk] = __float2half_rn(d);
+}
+
+__global__ void q8_block_dots_kernel(const int8_t* qs, int R, int K, const int8_t* xq, int32_t* dots) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int KB = K / 32;
+  if (i >= (long long)R * KB) return;
+  const long long r = i / KB;
+  const int b = (int)(i % KB);
+  const int* w = (const int*)(qs + r * K + (size_t)b * 32);
+  const int* a = (const int*)(xq + (size_t)b * 32);
+  int acc = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc = __dp4a(w[k], a[k], acc);
+  dots[i] = acc;
+}
+
+template <int C, int LANE>
+cudaError_t launch_cl(const Q8Params& p, int grid, int threads, size_t smem, const Launch& L) {
+  constexpr int U = 8 / C;
+  auto k = gemv_q8_kernel<C, LANE, U>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(k, dim3(grid), dim3(threads), smem, L, p);
+}
+
+int pick_c(int K) {
+  const int chunks = K / 16;
+  static const int opts[] = {1, 2, 4};
+  for (int c : opts)
+    if (chunks <= c * kThreads) return c;
+  return 0;
+}
+
+}  // namespace
+
+bool gemv_q8_supported(int K) { return K > 0 && K % 32 == 0 && pick_c(K) > 0; }
+
+cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
+  const int C = pick_c(a.K);
+  const int KC = a.K / 16;
+  const int T = std::min(kThreads, ((ceil_div(KC, C) + 31) / 32) * 32);
+  const int P = std::max(1, kThreads / T);
+  const int threads = T * P;
+  const int grid = std::max(1, std::min(a.R, dev_info().sm_count));
+  const int wpg = T / 32;
+  const int rows_max = ceil_div(a.R, grid);
+  const int phase_rows = std::max(1, std::min(rows_max, kSmemBudget / (wpg * 4)));
+  Q8Params p;
+  p.qs = a.qs;
+  p.d = (const __half*)a.d;
+  p.R = a.R; p.K = a.K;
+  p.rows_base = a.R / grid; p.rows_extra = a.R % grid;
+  p.T = T; p.P = P; p.phase_rows = phase_rows;
+  p.pro = a.pro; p.x = (const float*)a.x; p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps;
+  p.xq = a.xq; p.xd = (const __half*)a.xd;
+  if (a.act == 1 && a.xq != nullptr) p.pro = PRO_Q8_GIVEN;
+  p.epi = a.epi; p.y = a.y;
+  const size_t smem = (size_t)phase_rows * wpg * 4;
+  switch (C) {
+    case 1: return a.act == 1 ? launch_cl<1, 1>(p, grid, threads, smem, L) : launch_cl<1, 0>(p, grid, threads, smem, L);
+    case 2: return a.act == 1 ? launch_cl<2, 1>(p, grid, threads, smem, L) : launch_cl<2, 0>(p, grid, threads, smem, L);
+    default: return a.act == 1 ? launch_cl<4, 1>(p, grid, threads, smem, L) : launch_cl<4, 0>(p, grid, threads, smem, L);
+  }
+}
+
+cudaError_t launch_quantize_q8(const float* x, int n, int8_t* xq, void* xd, const Launch& L) {
+  const int threads = 256;
+  const int blocks = ceil_div((long long)n, threads);
+  if (blocks == 0) return cudaSuccess;
+  return launch_ex(quantize_q8_kernel, dim3(blocks), dim3(threads), 0, L, x, n, xq, (__half*)xd);
+}
+
+cudaError_t launch_q8_block_dots(const int8_t* qs, int R, int K, const int8_t* xq, int32_t* dots,
+                                 const Launch& L) {
+  const long long n = (long long)R * (K / 32);
+  if (n == 0) return cudaSuccess;
+  q8_block_dots_kernel<<<(int)((n + 255) / 256), 256, 0, L.stream>>>(qs, R, K, xq, dots);
+  return cudaGetLastError();
+}
+
+}  // namespace qd

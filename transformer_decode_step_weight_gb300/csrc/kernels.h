@@ -1,0 +1,100 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Host-only declarations; no CUDA device code here.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qd {
+
+struct DevInfo {
+  int sm_count;
+  int max_smem_optin;
+};
+const DevInfo& dev_info();
+
+// Launch options shared by every kernel launch of a decode step.
+struct Launch {
+  cudaStream_t stream;
+  bool pdl;          // programmatic dependent launch attribute
+  int* err;          // sticky device error word
+};
+
+// ----------------------------------------------------------------- GEMV bf16
+enum GemvPro { PRO_X_BF16 = 0, PRO_X_F32 = 1, PRO_RMSNORM = 2, PRO_SWIGLU = 3 };
+enum GemvEpi { EPI_STORE = 0, EPI_RESID_ADD = 1 };
+
+struct GemvBf16Args {
+  const void* W;          // bf16 [R, K]
+  int R, K, batch;
+  int pro;                // GemvPro
+  const void* x;          // PRO_X_BF16: bf16 [batch, K]; PRO_X_F32: f32 [batch, K];
+                          // PRO_RMSNORM: f32 residual [batch, K]; PRO_SWIGLU: f32 [batch, 2K]
+  const void* norm_w;     // bf16 [K] (PRO_RMSNORM)
+  float eps;
+  int epi;                // GemvEpi
+  float* y;               // f32 [batch, R]
+};
+bool gemv_bf16_supported(int K, int batch);
+cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L);
+
+// ----------------------------------------------------------------- GEMV Q8_0
+struct GemvQ8Args {
+  const int8_t* qs;       // int8 [R, K]
+  const void* d;          // f16 [R, K/32]
+  int R, K;
+  int act;                // 0 = f32 lane, 1 = i8 lane
+  int pro;                // GemvPro (PRO_X_BF16 not used)
+  const void* x;          // f32 x / residual / gu  (f32 lane and prologue source)
+  const int8_t* xq;       // i8 lane, PRO_X_F32 with pre-quantised input (may be null)
+  const void* xd;         // f16 [K/32]
+  const void* norm_w;
+  float eps;
+  int epi;
+  float* y;
+};
+bool gemv_q8_supported(int K);
+cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L);
+cudaError_t launch_quantize_q8(const float* x, int n, int8_t* xq, void* xd, const Launch& L);
+cudaError_t launch_q8_block_dots(const int8_t* qs, int R, int K, const int8_t* xq, int32_t* dots,
+                                 const Launch& L);
+
+// ----------------------------------------------------------------- attention
+struct AttnArgs {
+  // q source: either ready q (f32 [B, Hq, D]) or the fused QKV output
+  const float* q;         // ready q, or null
+  const float* qkv;       // f32 [B, (Hq + 2Hkv) * D] (fused mode), or null
+  const void* q_norm;     // bf16 [D] (fused)
+  const void* k_norm;     // bf16 [D] (fused)
+  const float* rope;      // f32 [rope_max_pos, D/2, 2] (fused)
+  int rope_max_pos;
+  float eps;
+  const int32_t* pos;     // fused: int32 [B], token position (keys 0..pos)
+  const int32_t* seq_lens;// standalone: int32 [B], keys 0..len-1
+  void* k_pages;          // bf16 [n_pages, Hkv, ps, D]
+  void* v_pages;
+  const int32_t* page_table;
+  int B, Hq, Hkv, D, page_size, max_pages, n_pages;
+  float scale;
+  float* out_f32;         // standalone output f32 [B, Hq, D]
+  void* out_bf16;         // fused output bf16 [B, Hq*D]
+  void* workspace;
+  size_t ws_bytes;
+  int max_ctx;            // upper bound of keys per sequence (sizes the split grid)
+};
+size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx);
+cudaError_t launch_attention(const AttnArgs& a, const Launch& L);
+cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float theta, cudaStream_t s);
+
+// ----------------------------------------------------------------- misc
+size_t argmax_workspace_bytes(int B);
+cudaError_t launch_argmax_advance(const float* logits, int V, int B, int32_t* tok, int32_t* pos,
+                                  int32_t* step, int32_t* out_tokens, int max_steps, void* ws,
+                                  const Launch& L);
+cudaError_t launch_embed(const void* embed, int H, int V, const int32_t* tok, int B, float* res,
+                         const Launch& L);
+cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_tokens,
+                                 int32_t* idx, cudaStream_t s);
+
+}  // namespace qd

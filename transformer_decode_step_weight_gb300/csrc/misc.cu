@@ -1,0 +1,181 @@
+// Embedding gather, greedy argmax with on-device token/position advance, and
+// the paged-index debug export.
+//
+// "GPU Kernel Lab" README, "Decode integration": fixed token/position buffers
+// feed the step, and the LM-head GEMV is followed by argmax + token/position
+// update on the device. "emit_qwen38_generate" rustdoc, "Where the speed comes
+// from", item 2: the sampled token and the position advance ON DEVICE so no
+// graph replay needs a host round trip.
+#include "common.cuh"
+#include "kernels.h"
+#include "launch.cuh"
+
+#include <climits>
+
+namespace qd {
+namespace {
+
+constexpr int kArgmaxBlocks = 32;
+constexpr int kArgmaxThreads = 512;
+
+// res[b, :] = f32(embed[tok[b], :])
+__global__ void __launch_bounds__(256) embed_kernel(const __nv_bfloat16* embed, int H, int V,
+                                                    const int32_t* tok, float* res, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.y;
+  int t = tok[b];
+  if (t < 0 || t >= V) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_error(err, QD_DEVERR_PAGE);
+    t = 0;
+  }
+  const __nv_bfloat16* row = embed + (size_t)t * H;
+  for (int i = (blockIdx.x * blockDim.x + threadIdx.x) * 8; i < H; i += gridDim.x * blockDim.x * 8) {
+    const uint4 v = *(const uint4*)(row + i);
+    float4 a = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
+    float4 c = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
+    *(float4*)(res + (size_t)b * H + i) = a;
+    *(float4*)(res + (size_t)b * H + i + 4) = c;
+  }
+}
+
+// (value, index) candidates; NaN maps to (-inf, INT_MAX) so it never wins and
+// an all-NaN row is recognisable.
+struct Cand {
+  float v;
+  int i;
+};
+QD_DEV bool better(const Cand& a, const Cand& b) { return a.v > b.v || (a.v == b.v && a.i < b.i); }
+
+QD_DEV Cand block_argmax(Cand c, Cand* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand d;
+    d.v = __shfl_xor_sync(0xffffffffu, c.v, o);
+    d.i = __shfl_xor_sync(0xffffffffu, c.i, o);
+    if (better(d, c)) c = d;
+  }
+  if (lane == 0) sh[warp] = c;
+  __syncthreads();
+  if (warp == 0) {
+    c = lane < (int)(blockDim.x >> 5) ? sh[lane] : Cand{-INFINITY, INT_MAX};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Cand d;
+      d.v = __shfl_xor_sync(0xffffffffu, c.v, o);
+      d.i = __shfl_xor_sync(0xffffffffu, c.i, o);
+      if (better(d, c)) c = d;
+    }
+  }
+  return c;  // valid in warp 0
+}
+
+struct ArgmaxParams {
+  const float* logits;
+  int V, B;
+  int32_t *tok, *pos, *step, *out;
+  int max_steps;
+  Cand* cand;  // [B, kArgmaxBlocks]
+  int* cnt;    // [B]
+  int* err;
+};
+
+__global__ void __launch_bounds__(kArgmaxThreads) argmax_advance_kernel(const ArgmaxParams p) {
+  __shared__ Cand sh[32];
+  __shared__ int s_ticket;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.y;
+  const float* row = p.logits + (size_t)b * p.V;
+  const int per = (p.V + gridDim.x - 1) / gridDim.x;
+  const int lo = blockIdx.x * per, hi = min(p.V, lo + per);
+  Cand c{-INFINITY, INT_MAX};
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    const float v = row[i];
+    Cand d{isnan(v) ? -INFINITY : v, isnan(v) ? INT_MAX : i};
+    if (better(d, c)) c = d;
+  }
+  c = block_argmax(c, sh);
+  if (threadIdx.x == 0) {
+    p.cand[b * gridDim.x + blockIdx.x] = c;
+    __threadfence();
+    s_ticket = atomicAdd(p.cnt + b, 1);
+  }
+  __syncthreads();
+  if (s_ticket != (int)gridDim.x - 1) return;
+  __threadfence();
+  // last block of this row: reduce the candidates in block order
+  if (threadIdx.x == 0) {
+    Cand best{-INFINITY, INT_MAX};
+    for (int k = 0; k < (int)gridDim.x; ++k) {
+      Cand d;
+      d.v = __ldcg(&p.cand[b * gridDim.x + k].v);
+      d.i = __ldcg(&p.cand[b * gridDim.x + k].i);
+      if (better(d, best)) best = d;
+    }
+    int t = best.i;
+    if (t == INT_MAX) {
+      set_error(p.err, QD_DEVERR_NAN);
+      t = 0;
+    }
+    const int st = p.step[b];
+    if (st >= 0 && st < p.max_steps) p.out[(size_t)b * p.max_steps + st] = t;
+    else set_error(p.err, QD_DEVERR_STEPS);
+    p.tok[b] = t;
+    p.pos[b] += 1;
+    p.step[b] = st + 1;
+    p.cnt[b] = 0;
+  }
+}
+
+__global__ void paged_indices_kernel(const int32_t* pt, int B, int max_pages, int ps, int n,
+                                     int32_t* idx) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)B * n) return;
+  const int b = (int)(i / n), t = (int)(i % n);
+  idx[i] = pt[(size_t)b * max_pages + t / ps] * ps + t % ps;
+}
+
+}  // namespace
+
+size_t argmax_workspace_bytes(int B) {
+  return (((size_t)B * kArgmaxBlocks * sizeof(Cand) + 255) & ~(size_t)255) + (size_t)B * 4;
+}
+
+cudaError_t launch_argmax_advance(const float* logits, int V, int B, int32_t* tok, int32_t* pos,
+                                  int32_t* step, int32_t* out_tokens, int max_steps, void* ws,
+                                  const Launch& L) {
+  ArgmaxParams p;
+  p.logits = logits;
+  p.V = V;
+  p.B = B;
+  p.tok = tok;
+  p.pos = pos;
+  p.step = step;
+  p.out = out_tokens;
+  p.max_steps = max_steps;
+  p.cand = (Cand*)ws;
+  p.cnt = (int*)((unsigned char*)ws + (((size_t)B * kArgmaxBlocks * sizeof(Cand) + 255) & ~(size_t)255));
+  p.err = L.err;
+  const int blocks = std::min(kArgmaxBlocks, std::max(1, ceil_div(V, kArgmaxThreads * 4)));
+  return launch_ex(argmax_advance_kernel, dim3(blocks, B), dim3(kArgmaxThreads), 0, L, p);
+}
+
+cudaError_t launch_embed(const void* embed, int H, int V, const int32_t* tok, int B, float* res,
+                         const Launch& L) {
+  const int threads = 256;
+  const int blocks = std::max(1, std::min(8, ceil_div(H, threads * 8)));
+  return launch_ex(embed_kernel, dim3(blocks, B), dim3(threads), 0, L, (const __nv_bfloat16*)embed, H,
+                   V, tok, res, L.err);
+}
+
+cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_tokens,
+                                 int32_t* idx, cudaStream_t s) {
+  const long long n = (long long)B * n_tokens;
+  if (n == 0) return cudaSuccess;
+  paged_indices_kernel<<<(int)((n + 255) / 256), 256, 0, s>>>(pt, B, max_pages, ps, n_tokens, idx);
+  return cudaGetLastError();
+}
+
+}  // namespace qd
