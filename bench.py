@@ -47,6 +47,12 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=128)
+    ap.add_argument("--no-probe", action="store_true", help="skip the dominant-kernel event probe")
+    ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "attention"],
+                    help="time one kernel alone on a full-size shape (profiling aid) instead of the step")
+    ap.add_argument("--rows", type=int, default=24576)
+    ap.add_argument("--cols", type=int, default=4096)
+    ap.add_argument("--ctx", type=int, default=4224)
     return ap.parse_args()
 
 
@@ -242,7 +248,7 @@ def run_ours(args, dist, rank, world, local):
     step_gbs = sum(step_bytes) / (ms / 1e3) / 1e9
 
     # ---- dominant kernel: the BF16 GEMV, every launch of one token, events on its stream
-    roof = dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind)
+    roof = None if args.no_probe else dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind)
 
     # ---- end to end through the public API: per step H2D of the input token/position
     # from pinned memory, the step, D2H of the next token, host reads it
@@ -310,6 +316,8 @@ def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
 
 
 def run_e2e(dec, stream, steps, reset, dist, world):
+    if steps <= 0:
+        return None
     dev = dec.tok.device
     h_in = torch.empty(2, dtype=torch.int32, pin_memory=True)
     h_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
@@ -433,8 +441,68 @@ def run_reference(args, dist, rank, world, local):
     print(json.dumps(out), flush=True)
 
 
+def run_kernel(args):
+    """One kernel alone, `steps` launches on distinct buffers larger than L2 where the
+    shape allows, timed with CUDA events; prints achieved GB/s of algorithmic bytes."""
+    from transformer_decode_step_weight_gb300 import api
+    from transformer_decode_step_weight_gb300 import build as b
+    b.build()
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed)
+    R, K = args.rows, args.cols
+    stream = torch.cuda.Stream(device=dev)
+    copies = max(1, min(4, int(2 * 129e6 // max(1, R * K)) + 1))
+    if args.kernel == "gemv_bf16":
+        Ws = [(torch.randn((R, K), generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(copies)]
+        x = torch.randn((1, K), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((1, R), device=dev)
+        nbytes = R * K * 2
+        fn = lambda i: api.gemv_bf16(Ws[i % copies], x, y, stream=stream)  # noqa: E731
+    elif args.kernel in ("gemv_q8_f32", "gemv_q8_i8"):
+        qs = [torch.randint(-127, 128, (R, K), generator=g, device=dev, dtype=torch.int16).to(torch.int8)
+              for _ in range(copies)]
+        ds = [(torch.randn((R, K // 32), generator=g, device=dev).abs() * 0.002).to(torch.float16)
+              for _ in range(copies)]
+        x = torch.randn(K, generator=g, device=dev)
+        y = torch.empty(R, device=dev)
+        lane = api.QD_ACT_I8 if args.kernel.endswith("i8") else api.QD_ACT_F32
+        nbytes = R * K + R * (K // 32) * 2
+        fn = lambda i: api.gemv_q8_0(qs[i % copies], ds[i % copies], x=x, act=lane, y=y, stream=stream)  # noqa: E731
+    else:
+        s = synth.QWEN3_8B
+        n = args.ctx
+        kp = torch.randn((1, s.n_kv_heads, n, 128), generator=g, device=dev).to(torch.bfloat16)
+        vp = torch.randn((1, s.n_kv_heads, n, 128), generator=g, device=dev).to(torch.bfloat16)
+        q = torch.randn((1, s.n_q_heads, 128), generator=g, device=dev)
+        pt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+        sl = torch.tensor([n], dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        ws = torch.zeros(api.attn_workspace_bytes(1, s.n_q_heads, s.n_kv_heads, n), dtype=torch.uint8, device=dev)
+        nbytes = 2 * s.n_kv_heads * n * 128 * 2
+        fn = lambda i: api.attn_decode_paged(q, kp, vp, pt, sl, 0.0884, out=out, workspace=ws, stream=stream)  # noqa
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            fn(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            fn(i)
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, kind = peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"kernel": args.kernel, "rows": R, "cols": K, "ctx": args.ctx, "us_per_launch": round(ms * 1e3, 3),
+                      "algorithmic_bytes": nbytes, "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                      "peak_kind": kind, "copies": copies}), flush=True)
+
+
 def main():
     args = parse()
+    if args.kernel:
+        run_kernel(args)
+        return
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; other ranks exit without work
         if int(os.environ.get("RANK", "0")) == 0:

@@ -19,5 +19,5 @@ def cuda_lib():
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from transformer_decode_step_weight_gb300 import _lib
-    return _lib.lib()
+    from transformer_decode_step_weight_gb300 import api
+    return api.lib()
