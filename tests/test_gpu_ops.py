@@ -183,11 +183,12 @@ def test_attention_page_permutation_is_bitwise_invariant(cuda_lib):
     lens = [300, 77]
     q, kp, vp, pt, sl = _attn_case(2, 32, 8, lens, 16, 42, True)
     out1 = api.attn_decode_paged(q, kp, vp, pt, sl, 1 / math.sqrt(128))
-    new_pt = torch.full_like(pt, 0)
+    # lay each sequence's used pages out in logical order and point an identity-like table at them
+    new_pt = torch.zeros_like(pt)
     kp2, vp2 = torch.zeros_like(kp), torch.zeros_like(vp)
     nxt = 0
-    for b in range(2):
-        for j in range(pt.shape[1]):
+    for b, n in enumerate(lens):
+        for j in range(-(-n // 16)):
             src = int(pt[b, j])
             kp2[nxt], vp2[nxt] = kp[src], vp[src]
             new_pt[b, j] = nxt

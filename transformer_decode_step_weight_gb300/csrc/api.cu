@@ -34,6 +34,7 @@ static int fail(int code, const char* fmt, ...) {
 }
 
 static int cuda_fail(cudaError_t e, const char* what) {
+  cudaGetLastError();  // a rejected launch must not leave its error for the caller's next CUDA call
   return fail(QD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
@@ -372,7 +373,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     // QK-norm + RoPE + K/V cache write + split-KV attention + combine
     AttnArgs at = {};
     at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
-    at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps;
+    at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps; at.act_bf16 = !q8;
     at.pos = a->pos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = a->page_table;
     at.B = B; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
     at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D);

@@ -11,25 +11,34 @@
 // through a page table.
 //
 // GB300 design:
-//   * grid (split, kv head, sequence), 128 threads; each CTA owns 64 tokens of
-//     one kv head and all REP = Hq/Hkv q heads that read it;
-//   * one thread issues TMA bulk copies (cp.async.bulk, 256 B per token row,
-//     one copy per contiguous page segment) of the chunk's K and V into shared
-//     memory on an mbarrier while the CTA computes q (and the new k, v);
-//   * scores, softmax and P.V run from shared memory in f32; a split writes
-//     (m, l, acc[REP][128]) to the workspace and takes a ticket; the last split
-//     of a (sequence, kv head) combines all partials in split order (fixed, so
-//     the result is deterministic) and resets the ticket to zero. No spin-wait.
+//   * grid (split, kv head, sequence), 128 threads; a CTA owns `chunk` tokens
+//     (a multiple of 64) of one kv head and all REP = Hq/Hkv q heads reading it;
+//     the host sizes `chunk` so the grid is about two CTAs per SM at batch 1
+//     and one split per sequence at large batch;
+//   * the chunk streams through shared memory in 64-token tiles: one thread
+//     issues TMA bulk copies (cp.async.bulk, one per contiguous page segment)
+//     of a tile's K and V rows into a 2-stage ring on mbarriers, so the next
+//     tile loads while the current one is scored;
+//   * per tile: scores from shared memory in f32, an online-softmax update of
+//     the running (max, sum) per head, then P.V into per-lane accumulators;
+//   * a split publishes (m, l, acc[REP][128]) to the workspace and takes a
+//     ticket; the last split of a (sequence, kv head) combines all partials in
+//     split order (fixed, so results are deterministic) with every load issued
+//     in parallel, and resets the ticket. No spin-wait anywhere.
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
+
+#include <algorithm>
 
 namespace qd {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kChunk = 64;
+constexpr int kTile = 64;
+constexpr int kStages = 2;
 constexpr int kThreads = 128;
+constexpr int kMaxSplits = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
@@ -40,12 +49,13 @@ struct AttnParams {
   const float2* rope;
   int rope_max_pos;
   float eps;
+  int act_bf16;
   const int32_t* pos;
   const int32_t* seq_lens;
   __nv_bfloat16* k_pages;
   __nv_bfloat16* v_pages;
   const int32_t* page_table;
-  int B, Hq, Hkv, page_size, max_pages, n_pages, n_splits;
+  int B, Hq, Hkv, page_size, max_pages, n_pages, n_splits, chunk;
   float scale_log2;
   float* out_f32;
   __nv_bfloat16* out_bf16;
@@ -56,23 +66,22 @@ struct AttnParams {
 };
 
 struct Carve {
-  size_t k, v, q, s, ml, bar, total;
+  size_t kv, q, s, run, bar, total;
 };
 __host__ __device__ inline Carve carve(int rep) {
   Carve c;
-  c.k = 0;
-  c.v = c.k + kChunk * kD * 2;
-  c.q = c.v + kChunk * kD * 2;
-  c.s = c.q + (size_t)rep * kD * 4;
-  c.ml = c.s + (size_t)rep * kChunk * 4;
-  c.bar = c.ml + 64 * 4;
-  c.total = c.bar + 16;
+  c.kv = 0;                                          // kStages x (K tile, V tile)
+  c.q = c.kv + (size_t)kStages * 2 * kTile * kD * 2;
+  c.s = c.q + (size_t)rep * kD * 4;                  // scores / probabilities [REP][64]
+  c.run = c.s + (size_t)rep * kTile * 4;             // m[REP], l[REP], alpha[REP], scratch
+  c.bar = c.run + 64 * 4;
+  c.total = c.bar + kStages * 8;
   return c;
 }
 
-// Per-head RMSNorm (Qwen cast order) + RoPE of one 128-vector held one element
-// per thread; returns this thread's rotated element (f32). `red` holds 4 floats.
-QD_DEV float norm_rope(float x, const __nv_bfloat16* w, const float2* rope_row, float eps,
+// Per-head RMSNorm (Qwen cast order; rounded to bf16 when the activations are
+// bf16) + rotate-half RoPE of a 128-vector held one element per thread.
+QD_DEV float norm_rope(float x, const __nv_bfloat16* w, const float2* rope_row, float eps, bool rnd,
                        float* red, float* xs) {
   const int d = threadIdx.x;
   float ss = warp_sum(x * x);
@@ -80,27 +89,51 @@ QD_DEV float norm_rope(float x, const __nv_bfloat16* w, const float2* rope_row, 
   __syncthreads();
   ss = (red[0] + red[1]) + (red[2] + red[3]);
   const float inv = 1.0f / sqrtf(ss / (float)kD + eps);
-  const float y = round_bf16(__bfloat162float(w[d]) * round_bf16(x * inv));
+  float n = x * inv;
+  if (rnd) n = round_bf16(n);
+  float y = __bfloat162float(w[d]) * n;
+  if (rnd) y = round_bf16(y);
   xs[d] = y;
   __syncthreads();
-  const int j = d & 63;
-  const float2 cs = rope_row[j];
+  const float2 cs = rope_row[d & 63];
   const float other = xs[d ^ 64];
   const float r = (d < 64) ? (y * cs.x - other * cs.y) : (y * cs.x + other * cs.y);
-  __syncthreads();  // xs and red are reused by the next call
+  __syncthreads();
   return r;
+}
+
+// Issue the TMA copies of tile rows [t, t + n) of kv head g into stage smem.
+QD_DEV void issue_tile(const AttnParams& p, int b, int g, int t, int n, __nv_bfloat16* sK, __nv_bfloat16* sV,
+                       uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, (uint32_t)n * kD * 2 * 2);
+  const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
+  const int ps = p.page_size;
+  const int t0 = t, end = t + n;
+  while (t < end) {
+    const int lp = t / ps;
+    int page = pt[lp];
+    if (page < 0 || page >= p.n_pages) {
+      set_error(p.err, QD_DEVERR_PAGE);
+      page = 0;
+    }
+    const int seg_end = min(end, (lp + 1) * ps);
+    const size_t off = (((size_t)page * p.Hkv + g) * ps + (t - lp * ps)) * kD;
+    const uint32_t bytes = (uint32_t)(seg_end - t) * kD * 2;
+    bulk_g2s(sK + (size_t)(t - t0) * kD, p.k_pages + off, bytes, bar);
+    bulk_g2s(sV + (size_t)(t - t0) * kD, p.v_pages + off, bytes, bar);
+    t = seg_end;
+  }
 }
 
 template <int REP, bool FUSED>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const Carve cv = carve(REP);
-  __nv_bfloat16* sK = (__nv_bfloat16*)(smem + cv.k);
-  __nv_bfloat16* sV = (__nv_bfloat16*)(smem + cv.v);
+  __nv_bfloat16* sKV = (__nv_bfloat16*)(smem + cv.kv);
   float* sQ = (float*)(smem + cv.q);
   float* sS = (float*)(smem + cv.s);
-  float* sML = (float*)(smem + cv.ml);  // [0..REP) m, [REP..2REP) l, [32..36) scratch
-  uint64_t* bar = (uint64_t*)(smem + cv.bar);
+  float* sRun = (float*)(smem + cv.run);  // [0,REP) m, [8,8+REP) l, [16,16+REP) alpha, [32,36) scratch
+  uint64_t* bars = (uint64_t*)(smem + cv.bar);
   __shared__ int s_ticket;
   __shared__ float s_x[kD];
 
@@ -122,47 +155,38 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     if (s == 0 && tid == 0) set_error(p.err, QD_DEVERR_POS);
     return;
   }
-  const int n_act = (len + kChunk - 1) / kChunk;
-  if (len == 0) {  // empty sequence: zero output (standalone form only)
+  const size_t head0 = (size_t)b * p.Hq + g * REP;
+  if (len == 0) {  // empty sequence (standalone form only): zero output
     if (s == 0 && !FUSED)
-      for (int i = 0; i < REP; ++i)
-        p.out_f32[((size_t)b * p.Hq + g * REP + i) * kD + tid] = 0.f;
+      for (int i = 0; i < REP; ++i) p.out_f32[(head0 + i) * kD + tid] = 0.f;
     return;
   }
+  const int n_act = (len + p.chunk - 1) / p.chunk;
   if (s >= n_act) return;
+  const int t0 = s * p.chunk;
+  const int t_end = min(t0 + p.chunk, len);          // keys [t0, t_end)
+  const int n_tiles = (t_end - t0 + kTile - 1) / kTile;
+  // in the fused form the current token `pos` is not read from the cache
+  const int copy_end = FUSED ? min(t_end, pos) : t_end;
 
-  const int t0 = s * kChunk;
-  const int nv = min(kChunk, len - t0);
-  const int ncopy = FUSED ? min(nv, pos - t0) : nv;
-  const int ps = p.page_size;
+  auto stage_k = [&](int st) { return sKV + (size_t)st * 2 * kTile * kD; };
+  auto stage_v = [&](int st) { return sKV + (size_t)st * 2 * kTile * kD + kTile * kD; };
 
   if (tid == 0) {
-    mbar_init(bar, 1);
+    for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
   __syncthreads();
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)ncopy * kD * 2 * 2);
-    const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
-    int t = t0;
-    const int end = t0 + ncopy;
-    while (t < end) {
-      const int lp = t / ps;
-      int page = pt[lp];
-      if (page < 0 || page >= p.n_pages) {
-        set_error(p.err, QD_DEVERR_PAGE);
-        page = 0;
-      }
-      const int seg_end = min(end, (lp + 1) * ps);
-      const size_t off = (((size_t)page * p.Hkv + g) * ps + (t - lp * ps)) * kD;
-      const uint32_t bytes = (uint32_t)(seg_end - t) * kD * 2;
-      bulk_g2s(sK + (size_t)(t - t0) * kD, p.k_pages + off, bytes, bar);
-      bulk_g2s(sV + (size_t)(t - t0) * kD, p.v_pages + off, bytes, bar);
-      t = seg_end;
+    for (int st = 0; st < kStages && st < n_tiles; ++st) {
+      const int ts = t0 + st * kTile;
+      issue_tile(p, b, g, ts, max(0, min(ts + kTile, copy_end) - ts), stage_k(st), stage_v(st), &bars[st]);
     }
   }
 
-  // ---- q for the REP heads of this kv head (pre-scaled by scale * log2 e)
+  // ---- q for the REP heads of this kv head (pre-scaled by scale * log2 e); new k, v
+  float k_new = 0.f, v_new = 0.f;
+  const bool own_pos = FUSED && pos >= t0 && pos < t_end;
   if (FUSED) {
     const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
     const float* qkv = p.qkv + (size_t)b * qkv_w;
@@ -170,107 +194,138 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
 #pragma unroll 1
     for (int i = 0; i < REP; ++i) {
       const float x = qkv[(g * REP + i) * kD + tid];
-      const float r = norm_rope(x, p.q_norm, rope_row, p.eps, sML + 32, s_x);
-      sQ[i * kD + tid] = r * p.scale_log2;
+      sQ[i * kD + tid] = norm_rope(x, p.q_norm, rope_row, p.eps, p.act_bf16, sRun + 32, s_x) * p.scale_log2;
     }
-    if (pos < t0 + kChunk) {  // this split holds the current token: build and store k, v
+    if (own_pos) {  // this split holds the current token: build k, v and store them in the cache
       const float kx = qkv[(p.Hq + g) * kD + tid];
-      const float kr = round_bf16(norm_rope(kx, p.k_norm, rope_row, p.eps, sML + 32, s_x));
-      const float vr = round_bf16(qkv[(p.Hq + p.Hkv + g) * kD + tid]);
-      const int lp = pos / ps;
-      int page = p.page_table[(size_t)b * p.max_pages + lp];
+      k_new = round_bf16(norm_rope(kx, p.k_norm, rope_row, p.eps, p.act_bf16, sRun + 32, s_x));
+      v_new = round_bf16(qkv[(p.Hq + p.Hkv + g) * kD + tid]);
+      const int lp = pos / p.page_size;
+      const int page = p.page_table[(size_t)b * p.max_pages + lp];
       if (page < 0 || page >= p.n_pages) {
         if (tid == 0) set_error(p.err, QD_DEVERR_PAGE);
       } else {
-        const size_t off = (((size_t)page * p.Hkv + g) * ps + (pos - lp * ps)) * kD + tid;
-        p.k_pages[off] = __float2bfloat16_rn(kr);
-        p.v_pages[off] = __float2bfloat16_rn(vr);
+        const size_t off = (((size_t)page * p.Hkv + g) * p.page_size + (pos - lp * p.page_size)) * kD + tid;
+        p.k_pages[off] = __float2bfloat16_rn(k_new);
+        p.v_pages[off] = __float2bfloat16_rn(v_new);
       }
-      sK[(size_t)(pos - t0) * kD + tid] = __float2bfloat16_rn(kr);
-      sV[(size_t)(pos - t0) * kD + tid] = __float2bfloat16_rn(vr);
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < REP; ++i)
-      sQ[i * kD + tid] = p.q[((size_t)b * p.Hq + g * REP + i) * kD + tid] * p.scale_log2;
+    for (int i = 0; i < REP; ++i) sQ[i * kD + tid] = p.q[(head0 + i) * kD + tid] * p.scale_log2;
+  }
+  if (tid < REP) {
+    sRun[tid] = -INFINITY;
+    sRun[8 + tid] = 0.f;
   }
   __syncthreads();
-  if (!mbar_wait_bounded(bar, 0, p.err)) {
-    mbar_wait_bounded(bar, 0, p.err);  // give copies in flight a second bounded chance
-    return;
-  }
 
-  // ---- scores: lane = (token half, 16-byte dim chunk); warp w owns pairs [8w, 8w + 8)
   const int half = lane >> 4, dc = lane & 15;
   float qr[REP][8];
 #pragma unroll
   for (int i = 0; i < REP; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) qr[i][e] = sQ[i * kD + dc * 8 + e];
-
-#pragma unroll 2
-  for (int pi = warp * 8; pi < warp * 8 + 8; ++pi) {
-    const int tt = 2 * pi + half;
-    const bool ok = tt < nv;
-    uint4 kw = make_uint4(0u, 0u, 0u, 0u);
-    if (ok) kw = *(const uint4*)(sK + (size_t)tt * kD + dc * 8);
-    const float kf[8] = {bf_lo(kw.x), bf_hi(kw.x), bf_lo(kw.y), bf_hi(kw.y),
-                         bf_lo(kw.z), bf_hi(kw.z), bf_lo(kw.w), bf_hi(kw.w)};
-#pragma unroll
-    for (int i = 0; i < REP; ++i) {
-      float a = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) a = fmaf(kf[e], qr[i][e], a);
-      a += __shfl_xor_sync(0xffffffffu, a, 8);
-      a += __shfl_xor_sync(0xffffffffu, a, 4);
-      a += __shfl_xor_sync(0xffffffffu, a, 2);
-      a += __shfl_xor_sync(0xffffffffu, a, 1);
-      if (dc == 0) sS[i * kChunk + tt] = ok ? a : -INFINITY;
-    }
-  }
-  __syncthreads();
-
-  // ---- chunk softmax per head (log2 domain)
-  for (int i = warp; i < REP; i += kThreads / 32) {
-    const float a0 = sS[i * kChunk + lane], a1 = sS[i * kChunk + lane + 32];
-    const float m = warp_max(fmaxf(a0, a1));
-    const float e0 = exp2f(a0 - m), e1 = exp2f(a1 - m);
-    const float l = warp_sum(e0 + e1);
-    sS[i * kChunk + lane] = e0;
-    sS[i * kChunk + lane + 32] = e1;
-    if (lane == 0) {
-      sML[i] = m;
-      sML[REP + i] = l;
-    }
-  }
-  __syncthreads();
-
-  // ---- P . V
   float acc[REP][8];
 #pragma unroll
   for (int i = 0; i < REP; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int st = it % kStages;
+    const int ts = t0 + it * kTile;
+    const int nv = min(kTile, t_end - ts);
+    __nv_bfloat16* sK = stage_k(st);
+    __nv_bfloat16* sV = stage_v(st);
+    if (!mbar_wait_bounded(&bars[st], (uint32_t)((it / kStages) & 1), p.err)) {
+      for (int k = 1; k < kStages && it + k < n_tiles; ++k)
+        mbar_wait_bounded(&bars[(it + k) % kStages], (uint32_t)(((it + k) / kStages) & 1), p.err);
+      return;
+    }
+    if (own_pos && pos >= ts && pos < ts + kTile) {
+      sK[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(k_new);
+      sV[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(v_new);
+    }
+    __syncthreads();
+
+    // scores: lane = (token of a pair, 16-byte dim chunk); warp w owns pairs [8w, 8w + 8)
 #pragma unroll 2
-  for (int pi = warp * 8; pi < warp * 8 + 8; ++pi) {
-    const int tt = 2 * pi + half;
-    if (tt < nv) {
-      const uint4 vw = *(const uint4*)(sV + (size_t)tt * kD + dc * 8);
-      const float vf[8] = {bf_lo(vw.x), bf_hi(vw.x), bf_lo(vw.y), bf_hi(vw.y),
-                           bf_lo(vw.z), bf_hi(vw.z), bf_lo(vw.w), bf_hi(vw.w)};
+    for (int pi = warp * 8; pi < warp * 8 + 8; ++pi) {
+      const int tt = 2 * pi + half;
+      const bool ok = tt < nv;
+      uint4 kw = make_uint4(0u, 0u, 0u, 0u);
+      if (ok) kw = *(const uint4*)(sK + (size_t)tt * kD + dc * 8);
+      const float kf[8] = {bf_lo(kw.x), bf_hi(kw.x), bf_lo(kw.y), bf_hi(kw.y),
+                           bf_lo(kw.z), bf_hi(kw.z), bf_lo(kw.w), bf_hi(kw.w)};
 #pragma unroll
       for (int i = 0; i < REP; ++i) {
-        const float pp = sS[i * kChunk + tt];
+        float a = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pp, vf[e], acc[i][e]);
+        for (int e = 0; e < 8; ++e) a = fmaf(kf[e], qr[i][e], a);
+        a += __shfl_xor_sync(0xffffffffu, a, 8);
+        a += __shfl_xor_sync(0xffffffffu, a, 4);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        if (dc == 0) sS[i * kTile + tt] = ok ? a : -INFINITY;
       }
     }
+    __syncthreads();
+
+    // online softmax update per head (log2 domain)
+    for (int i = warp; i < REP; i += kThreads / 32) {
+      const float a0 = sS[i * kTile + lane], a1 = sS[i * kTile + lane + 32];
+      const float m_old = sRun[i];
+      const float m_new = fmaxf(m_old, warp_max(fmaxf(a0, a1)));
+      const float e0 = exp2f(a0 - m_new), e1 = exp2f(a1 - m_new);
+      const float l = warp_sum(e0 + e1);
+      sS[i * kTile + lane] = e0;
+      sS[i * kTile + lane + 32] = e1;
+      __syncwarp();
+      if (lane == 0) {
+        const float alpha = exp2f(m_old - m_new);   // 0 on the first tile
+        sRun[16 + i] = alpha;
+        sRun[8 + i] = sRun[8 + i] * alpha + l;
+        sRun[i] = m_new;
+      }
+    }
+    __syncthreads();
+
+    // P . V with the running accumulators rescaled
+#pragma unroll
+    for (int i = 0; i < REP; ++i) {
+      const float alpha = sRun[16 + i];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[i][e] *= alpha;
+    }
+#pragma unroll 2
+    for (int pi = warp * 8; pi < warp * 8 + 8; ++pi) {
+      const int tt = 2 * pi + half;
+      if (tt < nv) {
+        const uint4 vw = *(const uint4*)(sV + (size_t)tt * kD + dc * 8);
+        const float vf[8] = {bf_lo(vw.x), bf_hi(vw.x), bf_lo(vw.y), bf_hi(vw.y),
+                             bf_lo(vw.z), bf_hi(vw.z), bf_lo(vw.w), bf_hi(vw.w)};
+#pragma unroll
+        for (int i = 0; i < REP; ++i) {
+          const float pp = sS[i * kTile + tt];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pp, vf[e], acc[i][e]);
+        }
+      }
+    }
+    __syncthreads();  // the stage and the probabilities are free again
+    if (tid == 0 && it + kStages < n_tiles) {
+      const int tn = t0 + (it + kStages) * kTile;
+      issue_tile(p, b, g, tn, max(0, min(tn + kTile, copy_end) - tn), sK, sV, &bars[st]);
+    }
   }
+
+  // ---- reduce the two token halves and the four warps
 #pragma unroll
   for (int i = 0; i < REP; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], 16);
-  float* sRed = (float*)sK;  // K tile no longer needed: [4 warps][REP][128]
+  float* sRed = (float*)sKV;  // [4 warps][REP][128] f32 (the ring is idle now)
   if (half == 0) {
 #pragma unroll
     for (int i = 0; i < REP; ++i)
@@ -284,11 +339,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     o[i] = (sRed[(0 * REP + i) * kD + tid] + sRed[(1 * REP + i) * kD + tid]) +
            (sRed[(2 * REP + i) * kD + tid] + sRed[(3 * REP + i) * kD + tid]);
 
-  const size_t head0 = (size_t)b * p.Hq + g * REP;
-  if (n_act == 1) {  // a single split is already complete
+  if (n_act == 1) {  // one split: already complete
 #pragma unroll
     for (int i = 0; i < REP; ++i) {
-      const float r = o[i] / sML[REP + i];
+      const float r = o[i] / sRun[8 + i];
       if (p.out_bf16) p.out_bf16[(head0 + i) * kD + tid] = __float2bfloat16_rn(r);
       else p.out_f32[(head0 + i) * kD + tid] = r;
     }
@@ -296,12 +350,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   }
 
   // ---- publish the partial, take a ticket; the last split combines
-  const size_t slot = ((size_t)b * p.Hkv + g) * p.n_splits + s;
+  const size_t slot0 = ((size_t)b * p.Hkv + g) * p.n_splits;
+  const size_t slot = slot0 + s;
 #pragma unroll
   for (int i = 0; i < REP; ++i) p.ws_acc[(slot * REP + i) * kD + tid] = o[i];
   if (tid < REP) {
-    p.ws_ml[(slot * REP + tid) * 2 + 0] = sML[tid];
-    p.ws_ml[(slot * REP + tid) * 2 + 1] = sML[REP + tid];
+    p.ws_ml[(slot * REP + tid) * 2 + 0] = sRun[tid];
+    p.ws_ml[(slot * REP + tid) * 2 + 1] = sRun[8 + tid];
   }
   __threadfence();
   __syncthreads();
@@ -310,20 +365,50 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   if (s_ticket != n_act - 1) return;
   __threadfence();
 
-  const size_t slot0 = ((size_t)b * p.Hkv + g) * p.n_splits;
-#pragma unroll 1
-  for (int i = 0; i < REP; ++i) {
+  // weights w[k][i] = exp2(m_k - M_i), sums l[k][i], totals L_i, all in shared memory
+  float* sW = (float*)sKV + 4 * REP * kD;       // after sRed: [kMaxSplits][REP]
+  float* sLk = sW + kMaxSplits * REP;           // [kMaxSplits][REP]
+  float* sL = sLk + kMaxSplits * REP;           // [REP]
+  for (int idx = tid; idx < n_act * REP; idx += kThreads) {
+    sW[idx] = __ldcg(p.ws_ml + (slot0 * REP + idx) * 2);
+    sLk[idx] = __ldcg(p.ws_ml + (slot0 * REP + idx) * 2 + 1);
+  }
+  __syncthreads();
+  if (tid < REP) {
     float M = -INFINITY;
-    for (int k = 0; k < n_act; ++k) M = fmaxf(M, __ldcg(p.ws_ml + ((slot0 + k) * REP + i) * 2));
-    float L = 0.f, O = 0.f;
+    for (int k = 0; k < n_act; ++k) M = fmaxf(M, sW[k * REP + tid]);
+    float L = 0.f;
     for (int k = 0; k < n_act; ++k) {
-      const float m = __ldcg(p.ws_ml + ((slot0 + k) * REP + i) * 2);
-      const float l = __ldcg(p.ws_ml + ((slot0 + k) * REP + i) * 2 + 1);
-      const float w = exp2f(m - M);
-      L = fmaf(w, l, L);
-      O = fmaf(w, __ldcg(p.ws_acc + ((slot0 + k) * REP + i) * kD + tid), O);
+      const float w = exp2f(sW[k * REP + tid] - M);
+      sW[k * REP + tid] = w;
+      L = fmaf(w, sLk[k * REP + tid], L);
     }
-    const float r = O / L;
+    sL[tid] = L;
+  }
+  __syncthreads();
+  // thread d accumulates dim d of every head; the loads are independent
+  float O[REP];
+#pragma unroll
+  for (int i = 0; i < REP; ++i) O[i] = 0.f;
+  const float* accp = p.ws_acc + slot0 * REP * kD + tid;
+  int k = 0;
+  for (; k + 4 <= n_act; k += 4) {
+    float v[4][REP];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < REP; ++i) v[u][i] = __ldcg(accp + ((size_t)(k + u) * REP + i) * kD);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < REP; ++i) O[i] = fmaf(sW[(k + u) * REP + i], v[u][i], O[i]);
+  }
+  for (; k < n_act; ++k)
+#pragma unroll
+    for (int i = 0; i < REP; ++i) O[i] = fmaf(sW[k * REP + i], __ldcg(accp + ((size_t)k * REP + i) * kD), O[i]);
+#pragma unroll
+  for (int i = 0; i < REP; ++i) {
+    const float r = O[i] / sL[i];
     if (p.out_bf16) p.out_bf16[(head0 + i) * kD + tid] = __float2bfloat16_rn(r);
     else p.out_f32[(head0 + i) * kD + tid] = r;
   }
@@ -344,21 +429,41 @@ template <int REP, bool FUSED>
 cudaError_t launch_rep(const AttnParams& prm, const Launch& L) {
   auto k = attn_kernel<REP, FUSED>;
   const size_t smem = carve(REP).total;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   dim3 grid(prm.n_splits, prm.Hkv, prm.B);
   return launch_ex(k, grid, dim3(kThreads), smem, L, prm);
 }
 
 }  // namespace
 
+// Tokens per split: about two CTAs per SM at small batch, a single split per
+// sequence once batch x kv heads fills the GPU, never more than kMaxSplits.
+int attn_chunk(int B, int Hkv, int max_ctx) {
+  const int sms = dev_info().sm_count;
+  const int pairs = std::max(1, B * Hkv);
+  const int want = std::max(1, (2 * sms + pairs - 1) / pairs);
+  int chunk = (max_ctx + want - 1) / want;
+  chunk = std::max(kTile, ((chunk + kTile - 1) / kTile) * kTile);
+  while ((max_ctx + chunk - 1) / chunk > kMaxSplits) chunk += kTile;
+  return chunk;
+}
+
+// Sized for the largest split count any device could choose (64-token chunks,
+// capped at kMaxSplits), so the size does not depend on the SM count.
+static size_t slots_cap(int B, int Hkv, int max_ctx) {
+  return (size_t)B * Hkv * std::min<size_t>((size_t)kMaxSplits, (size_t)(max_ctx + kTile - 1) / kTile);
+}
+
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx) {
   const int rep = Hq / Hkv;
-  const size_t splits = (size_t)(max_ctx + kChunk - 1) / kChunk;
-  const size_t slots = (size_t)B * Hkv * splits;
-  size_t acc = slots * rep * kD * 4;
-  size_t ml = slots * rep * 2 * 4;
-  size_t cnt = (size_t)B * Hkv * 4;
+  const size_t slots = slots_cap(B, Hkv, max_ctx);
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return al(acc) + al(ml) + al(cnt);
+  return al(slots * rep * kD * 4) + al(slots * rep * 2 * 4) + al((size_t)B * Hkv * 4);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
@@ -371,6 +476,7 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   p.rope = (const float2*)a.rope;
   p.rope_max_pos = a.rope_max_pos;
   p.eps = a.eps;
+  p.act_bf16 = a.act_bf16;
   p.pos = a.pos;
   p.seq_lens = a.seq_lens;
   p.k_pages = (__nv_bfloat16*)a.k_pages;
@@ -378,11 +484,12 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   p.page_table = a.page_table;
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv;
   p.page_size = a.page_size; p.max_pages = a.max_pages; p.n_pages = a.n_pages;
-  p.n_splits = (a.max_ctx + kChunk - 1) / kChunk;
+  p.chunk = attn_chunk(a.B, a.Hkv, a.max_ctx);
+  p.n_splits = (a.max_ctx + p.chunk - 1) / p.chunk;
   p.scale_log2 = a.scale * kLog2e;
   p.out_f32 = a.out_f32;
   p.out_bf16 = (__nv_bfloat16*)a.out_bf16;
-  const size_t slots = (size_t)a.B * a.Hkv * p.n_splits;
+  const size_t slots = slots_cap(a.B, a.Hkv, a.max_ctx);
   auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
   unsigned char* ws = (unsigned char*)a.workspace;
   p.ws_acc = (float*)ws;

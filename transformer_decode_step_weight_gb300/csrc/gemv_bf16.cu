@@ -30,6 +30,7 @@
 #include "launch.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace qd {
 namespace {
@@ -50,16 +51,15 @@ struct GemvParams {
   float* y;
 };
 
-QD_DEV float dot8(const uint4& w, const float* x) {
-  float s = bf_lo(w.x) * x[0];
-  s = fmaf(bf_hi(w.x), x[1], s);
-  s = fmaf(bf_lo(w.y), x[2], s);
-  s = fmaf(bf_hi(w.y), x[3], s);
-  s = fmaf(bf_lo(w.z), x[4], s);
-  s = fmaf(bf_hi(w.z), x[5], s);
-  s = fmaf(bf_lo(w.w), x[6], s);
-  s = fmaf(bf_hi(w.w), x[7], s);
-  return s;
+QD_DEV float dot8(const uint4& w, const float* x) {  // two independent chains of four
+  float a = bf_lo(w.x) * x[0], b = bf_hi(w.x) * x[1];
+  a = fmaf(bf_lo(w.y), x[2], a);
+  b = fmaf(bf_hi(w.y), x[3], b);
+  a = fmaf(bf_lo(w.z), x[4], a);
+  b = fmaf(bf_hi(w.z), x[5], b);
+  a = fmaf(bf_lo(w.w), x[6], a);
+  b = fmaf(bf_hi(w.w), x[7], b);
+  return a + b;
 }
 
 QD_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -274,6 +274,246 @@ int pick_c(int K) {
   return 0;
 }
 
+// ---------------------------------------------------------------------------
+// Batch-1 form on a TMA ring. One producer warp streams the CTA's contiguous
+// weight rows into a shared-memory ring with cp.async.bulk (a few rows per
+// stage, ~96 KB in flight per SM, issued before the programmatic-dependent
+// wait because weights never depend on an earlier kernel); eight consumer
+// warps own fixed 16-byte column chunks of every row (activation slice in
+// registers), read the stage from shared memory, reduce each row with warp
+// shuffles and a fixed-order sum over warps. At ~100 KB of shared memory and
+// <= 113 registers a thread, the next kernel's CTA fits beside this one and
+// fills its own ring while this one drains.
+constexpr int kCons = 256;          // consumer threads
+constexpr int kRingMax = 192 * 1024; // largest ring the launcher may choose
+constexpr int kPhaseRows = 128;     // rows reduced per phase
+
+struct RingParams {
+  const __nv_bfloat16* W;
+  int R, K;
+  int ring_bytes;
+  int rows_base, rows_extra;
+  int T, P, rps, ns, stage_bytes;
+  int pro;
+  const void* x;
+  const __nv_bfloat16* norm_w;
+  float eps;
+  int epi;
+  float* y;
+  int* err;
+};
+
+QD_DEV void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
+QD_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int C, int RPS>
+__global__ void __launch_bounds__(kCons + 32, 2) gemv_ring_kernel(const RingParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = (uint64_t*)(smem + p.ring_bytes);
+  uint64_t* empty = full + 16;
+  float* red = (float*)(empty + 16);            // [kPhaseRows][wpg]
+  __shared__ float s_ss[kCons / 32];
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int K = p.K, ns = p.ns;
+  const int nrows = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
+  const int r0 = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
+  const int n_stages = (nrows + p.P * RPS - 1) / (p.P * RPS);
+  const size_t row_bytes = (size_t)K * 2;
+
+  if (tid == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCons / 32);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (tid >= kCons) {  // ---- producer warp: weights only, so no dependency wait
+    if (lane == 0) {
+      const unsigned char* src = (const unsigned char*)(p.W + (size_t)r0 * K);
+      for (int i = 0; i < n_stages; ++i) {
+        const int slot = i % ns;
+        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) return;
+        const int srows = p.P * RPS;
+        const int rows_i = min(srows, nrows - i * srows);
+        const uint32_t bytes = (uint32_t)(rows_i * row_bytes);
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        bulk_g2s(ring + (size_t)slot * p.stage_bytes, src + (size_t)i * srows * row_bytes, bytes, &full[slot]);
+      }
+    }
+    return;
+  }
+
+  // ---- consumers
+  const int T = p.T, P = p.P;
+  const int g = tid / T, t = tid - g * T;
+  const int wpg = T >> 5, wig = t >> 5;
+  int col[C];
+  bool cv[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) {
+    col[j] = (j * T + t) * 8;
+    cv[j] = col[j] < K;
+  }
+  pdl_wait();
+
+  float x[C][8];
+#pragma unroll
+  for (int j = 0; j < C; ++j)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[j][e] = 0.f;
+  if (p.pro == PRO_X_BF16) {
+    const __nv_bfloat16* xb = (const __nv_bfloat16*)p.x;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      if (!cv[j]) continue;
+      const uint4 v = *(const uint4*)(xb + col[j]);
+      x[j][0] = bf_lo(v.x); x[j][1] = bf_hi(v.x); x[j][2] = bf_lo(v.y); x[j][3] = bf_hi(v.y);
+      x[j][4] = bf_lo(v.z); x[j][5] = bf_hi(v.z); x[j][6] = bf_lo(v.w); x[j][7] = bf_hi(v.w);
+    }
+  } else if (p.pro == PRO_X_F32 || p.pro == PRO_RMSNORM) {
+    const float* xf = (const float*)p.x;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      if (!cv[j]) continue;
+      const float4 a = *(const float4*)(xf + col[j]);
+      const float4 c = *(const float4*)(xf + col[j] + 4);
+      x[j][0] = a.x; x[j][1] = a.y; x[j][2] = a.z; x[j][3] = a.w;
+      x[j][4] = c.x; x[j][5] = c.y; x[j][6] = c.z; x[j][7] = c.w;
+    }
+    if (p.pro == PRO_X_F32) {
+#pragma unroll
+      for (int j = 0; j < C; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[j][e] = round_bf16(x[j][e]);
+    } else {
+      float ss = 0.f;
+      if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < C; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss = fmaf(x[j][e], x[j][e], ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_ss[tid >> 5] = ss;
+      cons_sync();
+      float tot = 0.f;
+      for (int i = 0; i < wpg; ++i) tot += s_ss[i];
+      const float inv = 1.0f / sqrtf(tot / (float)K + p.eps);
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (!cv[j]) continue;
+        const uint4 wn = *(const uint4*)(p.norm_w + col[j]);
+        const float nw[8] = {bf_lo(wn.x), bf_hi(wn.x), bf_lo(wn.y), bf_hi(wn.y),
+                             bf_lo(wn.z), bf_hi(wn.z), bf_lo(wn.w), bf_hi(wn.w)};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[j][e] = round_bf16(nw[e] * round_bf16(x[j][e] * inv));
+      }
+    }
+  } else {  // PRO_SWIGLU
+    const float* gu = (const float*)p.x;
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      if (!cv[j]) continue;
+      const float* gp = gu + col[j];
+      const float4 g0 = *(const float4*)gp, g1 = *(const float4*)(gp + 4);
+      const float4 u0 = *(const float4*)(gp + K), u1 = *(const float4*)(gp + K + 4);
+      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[j][e] = round_bf16(silu(gg[e]) * uu[e]);
+    }
+  }
+
+  // stage = P groups x RPS rows; group g owns rows [g*RPS, g*RPS + RPS) of every stage
+  const int stage_rows = P * RPS;
+  int ph_base = 0;  // first local row of the current reduction phase
+  for (int i = 0; i < n_stages; ++i) {
+    const int slot = i % ns;
+    if (!mbar_wait_bounded(&full[slot], (uint32_t)((i / ns) & 1), p.err)) {
+      for (int k = 1; k < ns && i + k < n_stages; ++k)
+        mbar_wait_bounded(&full[(i + k) % ns], (uint32_t)(((i + k) / ns) & 1), p.err);
+      return;
+    }
+    const int row0 = i * stage_rows + g * RPS;          // local row of this group's first row
+    const unsigned char* base = ring + (size_t)slot * p.stage_bytes + (size_t)g * RPS * row_bytes;
+    const int nv = min(RPS, nrows - row0);              // valid rows of the group (may be <= 0)
+    uint4 w[RPS][C];
+#pragma unroll
+    for (int r = 0; r < RPS; ++r)
+#pragma unroll
+      for (int j = 0; j < C; ++j)
+        w[r][j] = (r < nv && cv[j]) ? *(const uint4*)(base + (size_t)r * row_bytes + (size_t)col[j] * 2)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);           // the stage is in registers now
+    float v[RPS];
+#pragma unroll
+    for (int r = 0; r < RPS; ++r) {
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < C; ++j) a += dot8(w[r][j], x[j]);
+      v[r] = a;
+    }
+    // transposed butterfly: after it, lane l holds the warp sum of row rsel(l)
+    int rsel = 0;
+#pragma unroll
+    for (int L = 16, n = RPS; L >= 1; L >>= 1) {
+      if (n > 1) {
+        const int h = n / 2;
+        const bool up = (lane & L) != 0;
+#pragma unroll
+        for (int k = 0; k < h; ++k) {
+          const float send = up ? v[k] : v[k + h];
+          const float keep = up ? v[k + h] : v[k];
+          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, L);
+        }
+        if (up) rsel += h;
+        n = h;
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], L);
+      }
+    }
+    constexpr int kLowMask = 32 / RPS - 1;              // lanes below the halving levels
+    if ((lane & kLowMask) == 0 && rsel < nv)
+      red[(row0 + rsel - ph_base) * wpg + wig] = v[0];
+    const int done = min((i + 1) * stage_rows, nrows);
+    if (done + stage_rows - ph_base > kPhaseRows || i + 1 == n_stages) {  // the next stage would not fit
+      const int nph = done - ph_base;
+      cons_sync();
+      for (int r = tid; r < nph; r += kCons) {
+        float acc = 0.f;
+        for (int k = 0; k < wpg; ++k) acc += red[r * wpg + k];
+        float* yp = p.y + r0 + ph_base + r;
+        if (p.epi == EPI_RESID_ADD) *yp += acc;
+        else *yp = acc;
+      }
+      cons_sync();
+      ph_base = done;
+    }
+  }
+}
+
+template <int C>
+cudaError_t launch_ring_c(const RingParams& p, int grid, size_t smem, const Launch& L) {
+  constexpr int RPS = C == 1 ? 8 : C == 2 ? 4 : C <= 4 ? 2 : 1;
+  auto k = gemv_ring_kernel<C, RPS>;
+  static bool attr_set = false;
+  if (!attr_set) {  // the largest size any launch of this kernel may ask for
+    const int most = kRingMax + 32 * 8 + kPhaseRows * (kCons / 32) * 4;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(k, dim3(grid), dim3(kCons + 32), smem, L, p);
+}
+
 }  // namespace
 
 bool gemv_bf16_supported(int K, int batch) {
@@ -283,7 +523,60 @@ bool gemv_bf16_supported(int K, int batch) {
   return nb * c <= 8;
 }
 
+static int ring_c(int K) {
+  const int chunks = K / 8;
+  static const int opts[] = {1, 2, 3, 4, 6};
+  for (int c : opts)
+    if (chunks <= c * kCons) return c;
+  return 0;
+}
+
+// Ring geometry: a stage is P x RPS whole rows; the ring holds ~ring_kb KB of
+// stages (default 96, so two CTAs' shared memory fits one SM). QD_GEMV_RING_KB
+// overrides it (tuning); QD_GEMV_RING=0 selects the register-streaming kernel.
+struct RingTuning {
+  int enabled = 1, ring_kb = 96;
+  RingTuning() {
+    if (const char* v = getenv("QD_GEMV_RING")) enabled = atoi(v) != 0;
+    if (const char* v = getenv("QD_GEMV_RING_KB")) ring_kb = std::max(16, std::min(kRingMax / 1024, atoi(v)));
+  }
+};
+static const RingTuning& ring_tuning() {
+  static RingTuning t;
+  return t;
+}
+
 cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
+  const RingTuning& tu = ring_tuning();
+  const int rc = (a.batch == 1 && tu.enabled) ? ring_c(a.K) : 0;
+  const int ring_bytes = tu.ring_kb * 1024;
+  const int rc_rps = rc == 1 ? 8 : rc == 2 ? 4 : rc <= 4 ? 2 : 1;
+  if (rc > 0 && (size_t)a.K * 2 * rc_rps * 2 <= (size_t)kRingMax) {
+    const int chunks = a.K / 8;
+    RingParams p;
+    p.W = (const __nv_bfloat16*)a.W;
+    p.R = a.R; p.K = a.K;
+    const int grid = std::max(1, std::min(a.R, dev_info().sm_count));
+    p.rows_base = a.R / grid; p.rows_extra = a.R % grid;
+    p.T = std::min(kCons, ((ceil_div(chunks, rc) + 31) / 32) * 32);
+    p.P = std::max(1, kCons / p.T);
+    const int row_bytes = a.K * 2;
+    const int rps = rc == 1 ? 8 : rc == 2 ? 4 : rc <= 4 ? 2 : 1;     // must match launch_ring_c
+    p.rps = rps;
+    p.stage_bytes = ((p.P * rps * row_bytes + 127) / 128) * 128;
+    p.ns = std::max(2, std::min(16, ring_bytes / p.stage_bytes));
+    p.ring_bytes = p.ns * p.stage_bytes;
+    p.pro = a.pro; p.x = a.x; p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps;
+    p.epi = a.epi; p.y = a.y; p.err = L.err;
+    const size_t smem = (size_t)p.ring_bytes + 32 * 8 + (size_t)kPhaseRows * (p.T / 32) * 4;
+    switch (rc) {
+      case 1: return launch_ring_c<1>(p, grid, smem, L);
+      case 2: return launch_ring_c<2>(p, grid, smem, L);
+      case 3: return launch_ring_c<3>(p, grid, smem, L);
+      case 4: return launch_ring_c<4>(p, grid, smem, L);
+      default: return launch_ring_c<6>(p, grid, smem, L);
+    }
+  }
   const int C = pick_c(a.K);
   const int chunks = a.K / 8;
   const int T = std::min(kThreads, ((ceil_div(chunks, C) + 31) / 32) * 32);

@@ -70,6 +70,7 @@ struct AttnArgs {
   const float* rope;      // f32 [rope_max_pos, D/2, 2] (fused)
   int rope_max_pos;
   float eps;
+  int act_bf16;           // fused: QK-norm output rounded to bf16 (bf16 activations)
   const int32_t* pos;     // fused: int32 [B], token position (keys 0..pos)
   const int32_t* seq_lens;// standalone: int32 [B], keys 0..len-1
   void* k_pages;          // bf16 [n_pages, Hkv, ps, D]
@@ -84,6 +85,7 @@ struct AttnArgs {
   int max_ctx;            // upper bound of keys per sequence (sizes the split grid)
 };
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx);
+int attn_chunk(int B, int Hkv, int max_ctx);
 cudaError_t launch_attention(const AttnArgs& a, const Launch& L);
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float theta, cudaStream_t s);
 
