@@ -128,6 +128,28 @@ int qd_attn_decode_paged(const float* q, const void* k_pages, const void* v_page
                          int max_pages, int n_pages, float scale, float* out,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Allocation-free variant of qd_attn_decode_paged. (The pages describe no    */
+/* such call; it exists for callers that cannot allocate device memory:       */
+/* hosts whose device memory is reserved up front by their own pool, plugins  */
+/* handed only input and output buffers, and latency-critical loops where     */
+/* cudaMalloc/cudaFree would add an implicit device synchronisation.)          */
+/* Same arguments, layouts and result as qd_attn_decode_paged, without the    */
+/* workspace: the split-KV scratch is a static 8 MiB device array inside the  */
+/* library, held by every GPU that loads it until the process exits. Shapes   */
+/* whose workspace (qd_attn_workspace_bytes) exceeds 8 MiB are rejected with  */
+/* QD_ERR_WORKSPACE. The call allocates nothing; it clears the scratch's      */
+/* ticket counters with cudaMemsetAsync on `stream` before the launch. The    */
+/* first call on each device looks up the array's device address            */
+/* (cudaGetSymbolAddress) with that device current; make that first call     */
+/* before any stream capture. All calls share the one array, which keeps the  */
+/* last call's contents: calls that overlap on the GPU (for example on two     */
+/* streams) race on it and must be serialised by the caller.                 */
+int qd_attn_decode_paged_noalloc(const float* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* page_table, const int32_t* seq_lens, int batch,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int page_size,
+                                 int max_pages, int n_pages, float scale, float* out,
+                                 cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Greedy argmax + on-device advance ([KL-DEC] "LM-head GEMV + argmax +        */
 /* token/position update"; [EQ-SPEED] item 2).                                  */

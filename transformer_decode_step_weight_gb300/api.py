@@ -59,6 +59,7 @@ _SIGS = {
     "qd_quantize_q8_0": (_i, [_vp, _i, _vp, _vp, _vp]),
     "qd_attn_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "qd_attn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
+    "qd_attn_decode_paged_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp]),
     "qd_argmax_workspace_bytes": (_sz, [_i]),
     "qd_argmax_advance": (_i, [_vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _sz, _vp]),
     "qd_rope_table_init": (_i, [_vp, _i, _i, _f, _vp]),
@@ -165,6 +166,18 @@ def attn_decode_paged(q, k_pages, v_pages, page_table, seq_lens, scale, out=None
     _check(lib().qd_attn_decode_paged(_p(q), _p(k_pages), _p(v_pages), _p(page_table), _p(seq_lens), B, Hq, Hkv,
                                       D, ps, max_pages, n_pages, float(scale), _p(out), _p(workspace),
                                       workspace.numel(), _stream(stream)))
+    return out
+
+
+def attn_decode_paged_noalloc(q, k_pages, v_pages, page_table, seq_lens, scale, out=None, stream=None):
+    """qd_attn_decode_paged with the library's static scratch instead of a workspace."""
+    B, Hq, D = q.shape
+    n_pages, Hkv, ps, _ = k_pages.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib().qd_attn_decode_paged_noalloc(_p(q), _p(k_pages), _p(v_pages), _p(page_table), _p(seq_lens), B,
+                                              Hq, Hkv, D, ps, page_table.shape[1], n_pages, float(scale), _p(out),
+                                              _stream(stream)))
     return out
 
 

@@ -194,6 +194,38 @@ int qd_attn_decode_paged(const float* q, const void* k_pages, const void* v_page
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_attn_decode_paged");
 }
 
+int qd_attn_decode_paged_noalloc(const float* q, const void* k_pages, const void* v_pages,
+                                 const int32_t* page_table, const int32_t* seq_lens, int batch, int n_q_heads,
+                                 int n_kv_heads, int head_dim, int page_size, int max_pages, int n_pages,
+                                 float scale, float* out, cudaStream_t stream) {
+  int rc = check_attn_shape("qd_attn_decode_paged_noalloc", batch, n_q_heads, n_kv_heads, head_dim, page_size,
+                            max_pages, n_pages);
+  if (rc) return rc;
+  if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !out)
+    return fail(QD_ERR_INVALID_ARG, "qd_attn_decode_paged_noalloc: null pointer");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return fail(QD_ERR_INVALID_ARG, "qd_attn_decode_paged_noalloc: pointers must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(QD_ERR_INVALID_ARG, "qd_attn_decode_paged_noalloc: scale not finite");
+  const int max_ctx = max_pages * page_size;
+  const size_t need = attn_workspace_bytes(batch, n_q_heads, n_kv_heads, max_ctx);
+  if (need > attn_noalloc_scratch_bytes())
+    return fail(QD_ERR_WORKSPACE,
+                "qd_attn_decode_paged_noalloc: this shape needs %zu bytes of scratch, more than the %zu-byte "
+                "static array; use qd_attn_decode_paged with a caller-provided workspace",
+                need, attn_noalloc_scratch_bytes());
+  void* scratch = nullptr;
+  cudaError_t e = attn_noalloc_scratch(batch, n_q_heads, n_kv_heads, max_ctx, &scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "qd_attn_decode_paged_noalloc: scratch set-up");
+  AttnArgs a = {};
+  a.q = q; a.seq_lens = seq_lens;
+  a.k_pages = (void*)k_pages; a.v_pages = (void*)v_pages; a.page_table = page_table;
+  a.B = batch; a.Hq = n_q_heads; a.Hkv = n_kv_heads; a.D = head_dim;
+  a.page_size = page_size; a.max_pages = max_pages; a.n_pages = n_pages;
+  a.scale = scale; a.out_f32 = out; a.workspace = scratch; a.ws_bytes = need; a.max_ctx = max_ctx;
+  e = launch_attention(a, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_attn_decode_paged_noalloc");
+}
+
 // ------------------------------------------------------------------ argmax
 size_t qd_argmax_workspace_bytes(int batch) { return batch < 1 ? 0 : argmax_workspace_bytes(batch); }
 

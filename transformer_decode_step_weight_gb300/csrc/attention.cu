@@ -30,6 +30,7 @@
 #include "launch.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace qd {
 namespace {
@@ -517,6 +518,67 @@ cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float the
   const int blocks = (int)((n + threads - 1) / threads);
   rope_table_kernel<<<blocks, threads, 0, s>>>((float2*)table, max_pos, half, (double)theta);
   return cudaGetLastError();
+}
+
+}  // namespace qd
+
+// ---------------------------------------------------------------------------
+// Allocation-free form of qd_attn_decode_paged.
+//
+// Some callers cannot allocate device memory for the split-KV scratch: hosts
+// whose device memory is fully reserved up front by their own pool, plugins
+// that are handed only input and output buffers, and latency-critical loops
+// where cudaMalloc / cudaFree would add an implicit device synchronisation.
+// For them the scratch lives in this file-scope device array. Every GPU that
+// loads the library holds it until the process exits.
+static constexpr size_t kNoAllocScratchBytes = 8u << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
+
+namespace qd {
+namespace {
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+
+// Device address of g_attn_scratch on the current device, looked up once per
+// device (the name is only a host-side stand-in for the device array).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_attn_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace qd
+
+namespace qd {
+
+size_t attn_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+// The ticket counters are the last block of the workspace (see
+// attn_workspace_bytes). They must start at zero, and a call that was cut short
+// could have left them non-zero, so they are cleared on every call.
+cudaError_t attn_noalloc_scratch(int B, int Hq, int Hkv, int max_ctx, void** ptr, cudaStream_t stream) {
+  const size_t bytes = attn_workspace_bytes(B, Hq, Hkv, max_ctx);
+  const size_t cnt = (((size_t)B * Hkv * 4) + 255) & ~(size_t)255;
+  if (bytes > kNoAllocScratchBytes || bytes < cnt) return cudaErrorInvalidValue;
+  void* base = nullptr;
+  cudaError_t e = scratch_address(&base);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync((unsigned char*)base + bytes - cnt, 0, cnt, stream);
+  if (e != cudaSuccess) return e;
+  *ptr = base;
+  return cudaSuccess;
 }
 
 }  // namespace qd

@@ -87,6 +87,11 @@ struct AttnArgs {
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx);
 int attn_chunk(int B, int Hkv, int max_ctx);
 cudaError_t launch_attention(const AttnArgs& a, const Launch& L);
+// Static scratch of the allocation-free attention entry point: its capacity,
+// and its device address with the ticket counters of the shape's workspace
+// cleared on `stream` (no allocation).
+size_t attn_noalloc_scratch_bytes();
+cudaError_t attn_noalloc_scratch(int B, int Hq, int Hkv, int max_ctx, void** ptr, cudaStream_t stream);
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float theta, cudaStream_t s);
 
 // ----------------------------------------------------------------- misc
