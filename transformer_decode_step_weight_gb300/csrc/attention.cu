@@ -64,6 +64,7 @@ struct AttnParams {
   float* ws_ml;
   int* ws_cnt;
   int* err;
+  int trig_late;
 };
 
 struct Carve {
@@ -80,27 +81,21 @@ __host__ __device__ inline Carve carve(int rep) {
   return c;
 }
 
-// Per-head RMSNorm (Qwen cast order; rounded to bf16 when the activations are
-// bf16) + rotate-half RoPE of a 128-vector held one element per thread.
-QD_DEV float norm_rope(float x, const __nv_bfloat16* w, const float2* rope_row, float eps, bool rnd,
-                       float* red, float* xs) {
-  const int d = threadIdx.x;
-  float ss = warp_sum(x * x);
-  if ((d & 31) == 0) red[d >> 5] = ss;
-  __syncthreads();
-  ss = (red[0] + red[1]) + (red[2] + red[3]);
-  const float inv = 1.0f / sqrtf(ss / (float)kD + eps);
-  float n = x * inv;
-  if (rnd) n = round_bf16(n);
-  float y = __bfloat162float(w[d]) * n;
-  if (rnd) y = round_bf16(y);
-  xs[d] = y;
-  __syncthreads();
-  const float2 cs = rope_row[d & 63];
-  const float other = xs[d ^ 64];
-  const float r = (d < 64) ? (y * cs.x - other * cs.y) : (y * cs.x + other * cs.y);
-  __syncthreads();
-  return r;
+// N adjacent floats through L2 (partials written by other CTAs of this grid).
+template <int N>
+QD_DEV void load_cg(const float* src, float* dst) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < N; j += 4) {
+      const float4 v = __ldcg((const float4*)(src + j));
+      dst[j] = v.x; dst[j + 1] = v.y; dst[j + 2] = v.z; dst[j + 3] = v.w;
+    }
+  } else if constexpr (N == 2) {
+    const float2 v = __ldcg((const float2*)src);
+    dst[0] = v.x; dst[1] = v.y;
+  } else {
+    dst[0] = __ldcg(src);
+  }
 }
 
 // Issue the TMA copies of tile rows [t, t + n) of kv head g into stage smem.
@@ -142,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   pdl_wait();
-  pdl_launch_dependents();
+  if (!p.trig_late) pdl_launch_dependents();
 
   int len, pos = 0;
   if (FUSED) {
@@ -154,6 +149,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   const int cap = p.max_pages * p.page_size;
   if (len < 0 || len > cap || (FUSED && (pos < 0 || pos >= p.rope_max_pos))) {
     if (s == 0 && tid == 0) set_error(p.err, QD_DEVERR_POS);
+    pdl_launch_dependents();
     return;
   }
   const size_t head0 = (size_t)b * p.Hq + g * REP;
@@ -185,22 +181,52 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     }
   }
 
-  // ---- q for the REP heads of this kv head (pre-scaled by scale * log2 e); new k, v
+  // ---- q for the REP heads of this kv head (pre-scaled by scale * log2 e); new k, v.
+  // All head vectors load at once; one barrier for the sums of squares, one for RoPE.
   float k_new = 0.f, v_new = 0.f;
   const bool own_pos = FUSED && pos >= t0 && pos < t_end;
   if (FUSED) {
     const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
     const float* qkv = p.qkv + (size_t)b * qkv_w;
-    const float2* rope_row = p.rope + (size_t)pos * (kD / 2);
-#pragma unroll 1
-    for (int i = 0; i < REP; ++i) {
-      const float x = qkv[(g * REP + i) * kD + tid];
-      sQ[i * kD + tid] = norm_rope(x, p.q_norm, rope_row, p.eps, p.act_bf16, sRun + 32, s_x) * p.scale_log2;
+    const float2 cs = p.rope[(size_t)pos * (kD / 2) + (tid & 63)];
+    float xv[REP + 1];
+#pragma unroll
+    for (int i = 0; i < REP; ++i) xv[i] = qkv[(g * REP + i) * kD + tid];
+    xv[REP] = own_pos ? qkv[(p.Hq + g) * kD + tid] : 0.f;
+    const float vx = own_pos ? qkv[(p.Hq + p.Hkv + g) * kD + tid] : 0.f;
+    float* red = sS;  // [4 warps][REP + 1] scratch before the first tile
+#pragma unroll
+    for (int i = 0; i <= REP; ++i) {
+      const float ss = warp_sum(xv[i] * xv[i]);
+      if (lane == 0) red[warp * (REP + 1) + i] = ss;
     }
-    if (own_pos) {  // this split holds the current token: build k, v and store them in the cache
-      const float kx = qkv[(p.Hq + g) * kD + tid];
-      k_new = round_bf16(norm_rope(kx, p.k_norm, rope_row, p.eps, p.act_bf16, sRun + 32, s_x));
-      v_new = round_bf16(qkv[(p.Hq + p.Hkv + g) * kD + tid]);
+    __syncthreads();
+    float y[REP + 1];
+#pragma unroll
+    for (int i = 0; i <= REP; ++i) {
+      const float tot = (red[i] + red[(REP + 1) + i]) + (red[2 * (REP + 1) + i] + red[3 * (REP + 1) + i]);
+      const float inv = 1.0f / sqrtf(tot / (float)kD + p.eps);
+      float n = xv[i] * inv;
+      if (p.act_bf16) n = round_bf16(n);
+      const __nv_bfloat16* w = i < REP ? p.q_norm : p.k_norm;
+      y[i] = __bfloat162float(w[tid]) * n;
+      if (p.act_bf16) y[i] = round_bf16(y[i]);
+      if (i < REP) sQ[i * kD + tid] = y[i];
+      else s_x[tid] = y[i];
+    }
+    __syncthreads();
+    float r[REP + 1];
+#pragma unroll
+    for (int i = 0; i <= REP; ++i) {
+      const float other = i < REP ? sQ[i * kD + (tid ^ 64)] : s_x[tid ^ 64];
+      r[i] = (tid < 64) ? (y[i] * cs.x - other * cs.y) : (y[i] * cs.x + other * cs.y);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < REP; ++i) sQ[i * kD + tid] = r[i] * p.scale_log2;
+    if (own_pos) {  // this split holds the current token: store k, v in the cache
+      k_new = round_bf16(r[REP]);
+      v_new = round_bf16(vx);
       const int lp = pos / p.page_size;
       const int page = p.page_table[(size_t)b * p.max_pages + lp];
       if (page < 0 || page >= p.n_pages) {
@@ -259,17 +285,38 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
       if (ok) kw = *(const uint4*)(sK + (size_t)tt * kD + dc * 8);
       const float kf[8] = {bf_lo(kw.x), bf_hi(kw.x), bf_lo(kw.y), bf_hi(kw.y),
                            bf_lo(kw.z), bf_hi(kw.z), bf_lo(kw.w), bf_hi(kw.w)};
+      float v[REP];
 #pragma unroll
       for (int i = 0; i < REP; ++i) {
-        float a = 0.f;
+        float a = 0.f, c = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a = fmaf(kf[e], qr[i][e], a);
-        a += __shfl_xor_sync(0xffffffffu, a, 8);
-        a += __shfl_xor_sync(0xffffffffu, a, 4);
-        a += __shfl_xor_sync(0xffffffffu, a, 2);
-        a += __shfl_xor_sync(0xffffffffu, a, 1);
-        if (dc == 0) sS[i * kTile + tt] = ok ? a : -INFINITY;
+        for (int e = 0; e < 8; e += 2) {
+          a = fmaf(kf[e], qr[i][e], a);
+          c = fmaf(kf[e + 1], qr[i][e + 1], c);
+        }
+        v[i] = a + c;
       }
+      // transposed butterfly over the 16 lanes of this token: afterwards lane
+      // (dc) holds the full dot of head hsel(dc)
+      int hsel = 0;
+#pragma unroll
+      for (int L = 8, n = REP; L >= 1; L >>= 1) {
+        if (n > 1) {
+          const int h = n / 2;
+          const bool up = (lane & L) != 0;
+#pragma unroll
+          for (int k = 0; k < h; ++k) {
+            const float send = up ? v[k] : v[k + h];
+            const float keep = up ? v[k + h] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, L);
+          }
+          if (up) hsel += h;
+          n = h;
+        } else {
+          v[0] += __shfl_xor_sync(0xffffffffu, v[0], L);
+        }
+      }
+      if ((dc & (16 / REP - 1)) == 0) sS[hsel * kTile + tt] = ok ? v[0] : -INFINITY;
     }
     __syncthreads();
 
@@ -320,6 +367,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
       issue_tile(p, b, g, tn, max(0, min(tn + kTile, copy_end) - tn), sK, sV, &bars[st]);
     }
   }
+
+  pdl_launch_dependents();  // all K/V of this split is in shared memory
 
   // ---- reduce the two token halves and the four warps
 #pragma unroll
@@ -387,31 +436,34 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     sL[tid] = L;
   }
   __syncthreads();
-  // thread d accumulates dim d of every head; the loads are independent
+  // thread t accumulates elements [t*REP, t*REP + REP) of the [REP][128]
+  // partials (one head, REP adjacent dims); 16 splits of loads in flight
+  const int e0 = tid * REP, hi = e0 / kD;
   float O[REP];
 #pragma unroll
-  for (int i = 0; i < REP; ++i) O[i] = 0.f;
-  const float* accp = p.ws_acc + slot0 * REP * kD + tid;
-  int k = 0;
-  for (; k + 4 <= n_act; k += 4) {
-    float v[4][REP];
+  for (int j = 0; j < REP; ++j) O[j] = 0.f;
+  const float* accp = p.ws_acc + slot0 * REP * kD + e0;
+  for (int k0 = 0; k0 < n_act; k0 += 16) {
+    float v[16][REP];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < 16; ++u)
+      if (k0 + u < n_act) load_cg<REP>(accp + (size_t)(k0 + u) * REP * kD, v[u]);
 #pragma unroll
-      for (int i = 0; i < REP; ++i) v[u][i] = __ldcg(accp + ((size_t)(k + u) * REP + i) * kD);
+    for (int u = 0; u < 16; ++u) {
+      if (k0 + u < n_act) {
+        const float w = sW[(k0 + u) * REP + hi];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int i = 0; i < REP; ++i) O[i] = fmaf(sW[(k + u) * REP + i], v[u][i], O[i]);
+        for (int j = 0; j < REP; ++j) O[j] = fmaf(w, v[u][j], O[j]);
+      }
+    }
   }
-  for (; k < n_act; ++k)
+  const float invL = 1.0f / sL[hi];
 #pragma unroll
-    for (int i = 0; i < REP; ++i) O[i] = fmaf(sW[k * REP + i], __ldcg(accp + ((size_t)k * REP + i) * kD), O[i]);
-#pragma unroll
-  for (int i = 0; i < REP; ++i) {
-    const float r = O[i] / sL[i];
-    if (p.out_bf16) p.out_bf16[(head0 + i) * kD + tid] = __float2bfloat16_rn(r);
-    else p.out_f32[(head0 + i) * kD + tid] = r;
+  for (int j = 0; j < REP; ++j) {
+    const float r = O[j] * invL;
+    const size_t o = (head0 + hi) * kD + (e0 - hi * kD) + j;
+    if (p.out_bf16) p.out_bf16[o] = __float2bfloat16_rn(r);
+    else p.out_f32[o] = r;
   }
   if (tid == 0) p.ws_cnt[(size_t)b * p.Hkv + g] = 0;
 }
@@ -497,6 +549,7 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   p.ws_ml = (float*)(ws + al(slots * rep * kD * 4));
   p.ws_cnt = (int*)(ws + al(slots * rep * kD * 4) + al(slots * rep * 2 * 4));
   p.err = L.err;
+  p.trig_late = L.trig_late;
   const bool fused = a.qkv != nullptr;
 #define QD_ATTN_CASE(R)                                                      \
   case R:                                                                    \

@@ -18,6 +18,7 @@ const DevInfo& dev_info();
 struct Launch {
   cudaStream_t stream;
   bool pdl;          // programmatic dependent launch attribute
+  int trig_late;     // 1: let the next kernel launch only near the end of this one
   int* err;          // sticky device error word
 };
 
