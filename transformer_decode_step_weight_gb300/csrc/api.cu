@@ -93,6 +93,17 @@ static int pdl_trigger_late() {
   return late;
 }
 
+// QD_ATTN_CLUSTER=n (2..16) makes the decode step split each sequence over a
+// thread block cluster of at most n CTAs; the default (0) uses the workspace
+// split-KV form, which measured faster on the Qwen3-8B step.
+static int attn_cluster_enabled() {
+  static const int n = [] {
+    const char* v = getenv("QD_ATTN_CLUSTER");
+    return v ? atoi(v) : 0;
+  }();
+  return n;
+}
+
 static Launch make_launch(cudaStream_t s, bool pdl) {
   Launch L;
   L.stream = s;
@@ -434,7 +445,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D);
     if (q8) at.out_f32 = (float*)w.attn;
     else at.out_bf16 = w.attn;
-    at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size;
+    at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.use_cluster = attn_cluster_enabled();
     QD_TRY(launch_attention(at, L), "attention");
     // O projection + residual add
     if (q8) {

@@ -11,11 +11,12 @@
 // through a page table.
 //
 // GB300 design:
-//   * grid (split, kv head, sequence), 128 threads; a CTA owns `chunk` tokens
-//     (a multiple of 64) of one kv head and all REP = Hq/Hkv q heads reading it;
-//     the host sizes `chunk` so the grid is about two CTAs per SM at batch 1
+//   * grid (split, kv head, sequence), 512 threads (256 for 8 q heads per kv
+//     head); a CTA owns `chunk` tokens
+//     (a multiple of 128) of one kv head and all REP = Hq/Hkv q heads reading it;
+//     the host sizes `chunk` so the grid is about one CTA per SM at batch 1
 //     and one split per sequence at large batch;
-//   * the chunk streams through shared memory in 64-token tiles: one thread
+//   * the chunk streams through shared memory in 128-token tiles: one thread
 //     issues TMA bulk copies (cp.async.bulk, one per contiguous page segment)
 //     of a tile's K and V rows into a 2-stage ring on mbarriers, so the next
 //     tile loads while the current one is scored;
@@ -36,9 +37,10 @@ namespace qd {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTile = 64;
+constexpr int kTile = 128;
 constexpr int kStages = 2;
-constexpr int kThreads = 128;
+// 512 threads (16 warps) per CTA; 256 when 8 q heads share a kv head (register budget)
+__host__ __device__ constexpr int threads_for(int rep) { return rep >= 8 ? 256 : 512; }
 constexpr int kMaxSplits = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -121,8 +123,31 @@ QD_DEV void issue_tile(const AttnParams& p, int b, int g, int t, int n, __nv_bfl
   }
 }
 
-template <int REP, bool FUSED>
-__global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
+// Thread-block-cluster helpers: a full cluster barrier and distributed shared
+// memory loads from a peer CTA (the cluster spans grid x, so a CTA's rank in
+// its cluster is blockIdx.x).
+QD_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+QD_DEV float ld_peer(const float* local, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// CLUSTER = false: split s of `chunk` tokens, partials through the workspace and
+//   a ticket (the last split combines).
+// CLUSTER = true: the gridDim.x CTAs of a (kv head, sequence) form one thread
+//   block cluster and split the sequence evenly; the partials stay in shared
+//   memory and are combined through distributed shared memory after a cluster
+//   barrier (no workspace, no ticket, no global round trip).
+template <int REP, bool FUSED, bool CLUSTER>
+__global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams p) {
+  constexpr int kThreads = threads_for(REP);
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kPairs = kTile / 2 / kWarps;  // token pairs per warp per tile
   extern __shared__ __align__(128) unsigned char smem[];
   const Carve cv = carve(REP);
   __nv_bfloat16* sKV = (__nv_bfloat16*)(smem + cv.kv);
@@ -153,15 +178,22 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     return;
   }
   const size_t head0 = (size_t)b * p.Hq + g * REP;
-  if (len == 0) {  // empty sequence (standalone form only): zero output
+  if (!CLUSTER && len == 0) {  // empty sequence (standalone form only): zero output
     if (s == 0 && !FUSED)
-      for (int i = 0; i < REP; ++i) p.out_f32[(head0 + i) * kD + tid] = 0.f;
+      for (int e = tid; e < REP * kD; e += kThreads) p.out_f32[head0 * kD + e] = 0.f;
     return;
   }
-  const int n_act = (len + p.chunk - 1) / p.chunk;
-  if (s >= n_act) return;
-  const int t0 = s * p.chunk;
-  const int t_end = min(t0 + p.chunk, len);          // keys [t0, t_end)
+  int n_act = 1, t0, t_end;                          // keys [t0, t_end)
+  if (CLUSTER) {
+    const long long cl = gridDim.x;
+    t0 = (int)(((long long)len * s) / cl);
+    t_end = (int)(((long long)len * (s + 1)) / cl);
+  } else {
+    n_act = (len + p.chunk - 1) / p.chunk;
+    if (s >= n_act) return;
+    t0 = s * p.chunk;
+    t_end = min(t0 + p.chunk, len);
+  }
   const int n_tiles = (t_end - t0 + kTile - 1) / kTile;
   // in the fused form the current token `pos` is not read from the cache
   const int copy_end = FUSED ? min(t_end, pos) : t_end;
@@ -188,17 +220,20 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   if (FUSED) {
     const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
     const float* qkv = p.qkv + (size_t)b * qkv_w;
-    const float2 cs = p.rope[(size_t)pos * (kD / 2) + (tid & 63)];
+    // threads [0, 128) own one dim of every head vector; the rest only join the barriers
+    const bool dim_thread = tid < kD;
+    const int d = tid & (kD - 1);
+    const float2 cs = p.rope[(size_t)pos * (kD / 2) + (d & 63)];
     float xv[REP + 1];
 #pragma unroll
-    for (int i = 0; i < REP; ++i) xv[i] = qkv[(g * REP + i) * kD + tid];
-    xv[REP] = own_pos ? qkv[(p.Hq + g) * kD + tid] : 0.f;
-    const float vx = own_pos ? qkv[(p.Hq + p.Hkv + g) * kD + tid] : 0.f;
+    for (int i = 0; i < REP; ++i) xv[i] = dim_thread ? qkv[(g * REP + i) * kD + d] : 0.f;
+    xv[REP] = (own_pos && dim_thread) ? qkv[(p.Hq + g) * kD + d] : 0.f;
+    const float vx = (own_pos && dim_thread) ? qkv[(p.Hq + p.Hkv + g) * kD + d] : 0.f;
     float* red = sS;  // [4 warps][REP + 1] scratch before the first tile
 #pragma unroll
     for (int i = 0; i <= REP; ++i) {
       const float ss = warp_sum(xv[i] * xv[i]);
-      if (lane == 0) red[warp * (REP + 1) + i] = ss;
+      if (lane == 0 && dim_thread) red[warp * (REP + 1) + i] = ss;
     }
     __syncthreads();
     float y[REP + 1];
@@ -209,22 +244,26 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
       float n = xv[i] * inv;
       if (p.act_bf16) n = round_bf16(n);
       const __nv_bfloat16* w = i < REP ? p.q_norm : p.k_norm;
-      y[i] = __bfloat162float(w[tid]) * n;
+      y[i] = __bfloat162float(w[d]) * n;
       if (p.act_bf16) y[i] = round_bf16(y[i]);
-      if (i < REP) sQ[i * kD + tid] = y[i];
-      else s_x[tid] = y[i];
+      if (dim_thread) {
+        if (i < REP) sQ[i * kD + d] = y[i];
+        else s_x[d] = y[i];
+      }
     }
     __syncthreads();
     float r[REP + 1];
 #pragma unroll
     for (int i = 0; i <= REP; ++i) {
-      const float other = i < REP ? sQ[i * kD + (tid ^ 64)] : s_x[tid ^ 64];
-      r[i] = (tid < 64) ? (y[i] * cs.x - other * cs.y) : (y[i] * cs.x + other * cs.y);
+      const float other = i < REP ? sQ[i * kD + (d ^ 64)] : s_x[d ^ 64];
+      r[i] = (d < 64) ? (y[i] * cs.x - other * cs.y) : (y[i] * cs.x + other * cs.y);
     }
     __syncthreads();
+    if (dim_thread) {
 #pragma unroll
-    for (int i = 0; i < REP; ++i) sQ[i * kD + tid] = r[i] * p.scale_log2;
-    if (own_pos) {  // this split holds the current token: store k, v in the cache
+      for (int i = 0; i < REP; ++i) sQ[i * kD + d] = r[i] * p.scale_log2;
+    }
+    if (own_pos && dim_thread) {  // this split holds the current token: store k, v in the cache
       k_new = round_bf16(r[REP]);
       v_new = round_bf16(vx);
       const int lp = pos / p.page_size;
@@ -232,14 +271,13 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
       if (page < 0 || page >= p.n_pages) {
         if (tid == 0) set_error(p.err, QD_DEVERR_PAGE);
       } else {
-        const size_t off = (((size_t)page * p.Hkv + g) * p.page_size + (pos - lp * p.page_size)) * kD + tid;
+        const size_t off = (((size_t)page * p.Hkv + g) * p.page_size + (pos - lp * p.page_size)) * kD + d;
         p.k_pages[off] = __float2bfloat16_rn(k_new);
         p.v_pages[off] = __float2bfloat16_rn(v_new);
       }
     }
   } else {
-#pragma unroll
-    for (int i = 0; i < REP; ++i) sQ[i * kD + tid] = p.q[(head0 + i) * kD + tid] * p.scale_log2;
+    for (int e = tid; e < REP * kD; e += kThreads) sQ[e] = p.q[head0 * kD + e] * p.scale_log2;
   }
   if (tid < REP) {
     sRun[tid] = -INFINITY;
@@ -268,17 +306,18 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     if (!mbar_wait_bounded(&bars[st], (uint32_t)((it / kStages) & 1), p.err)) {
       for (int k = 1; k < kStages && it + k < n_tiles; ++k)
         mbar_wait_bounded(&bars[(it + k) % kStages], (uint32_t)(((it + k) / kStages) & 1), p.err);
-      return;
+      if (!CLUSTER) return;
+      break;  // cluster peers still expect this CTA at the cluster barriers (the error word is set)
     }
-    if (own_pos && pos >= ts && pos < ts + kTile) {
+    if (own_pos && pos >= ts && pos < ts + kTile && tid < kD) {
       sK[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(k_new);
       sV[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(v_new);
     }
     __syncthreads();
 
     // scores: lane = (token of a pair, 16-byte dim chunk); warp w owns pairs [8w, 8w + 8)
-#pragma unroll 2
-    for (int pi = warp * 8; pi < warp * 8 + 8; ++pi) {
+#pragma unroll
+    for (int pi = warp * kPairs; pi < warp * kPairs + kPairs; ++pi) {
       const int tt = 2 * pi + half;
       const bool ok = tt < nv;
       uint4 kw = make_uint4(0u, 0u, 0u, 0u);
@@ -321,14 +360,24 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     __syncthreads();
 
     // online softmax update per head (log2 domain)
-    for (int i = warp; i < REP; i += kThreads / 32) {
-      const float a0 = sS[i * kTile + lane], a1 = sS[i * kTile + lane + 32];
+    for (int i = warp; i < REP; i += kWarps) {
+      constexpr int kPer = kTile / 32;
+      float a[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) a[u] = sS[i * kTile + lane + 32 * u];
+      float mx = a[0];
+#pragma unroll
+      for (int u = 1; u < kPer; ++u) mx = fmaxf(mx, a[u]);
       const float m_old = sRun[i];
-      const float m_new = fmaxf(m_old, warp_max(fmaxf(a0, a1)));
-      const float e0 = exp2f(a0 - m_new), e1 = exp2f(a1 - m_new);
-      const float l = warp_sum(e0 + e1);
-      sS[i * kTile + lane] = e0;
-      sS[i * kTile + lane + 32] = e1;
+      const float m_new = fmaxf(m_old, warp_max(mx));
+      float sum = 0.f;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        a[u] = exp2f(a[u] - m_new);
+        sum += a[u];
+        sS[i * kTile + lane + 32 * u] = a[u];
+      }
+      const float l = warp_sum(sum);
       __syncwarp();
       if (lane == 0) {
         const float alpha = exp2f(m_old - m_new);   // 0 on the first tile
@@ -346,8 +395,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[i][e] *= alpha;
     }
-#pragma unroll 2
-    for (int pi = warp * 8; pi < warp * 8 + 8; ++pi) {
+#pragma unroll
+    for (int pi = warp * kPairs; pi < warp * kPairs + kPairs; ++pi) {
       const int tt = 2 * pi + half;
       if (tt < nv) {
         const uint4 vw = *(const uint4*)(sV + (size_t)tt * kD + dc * 8);
@@ -370,31 +419,71 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
 
   pdl_launch_dependents();  // all K/V of this split is in shared memory
 
-  // ---- reduce the two token halves and the four warps
+  // ---- reduce the two token halves, then the warps, element by element
 #pragma unroll
   for (int i = 0; i < REP; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] += __shfl_xor_sync(0xffffffffu, acc[i][e], 16);
-  float* sRed = (float*)sKV;  // [4 warps][REP][128] f32 (the ring is idle now)
+  constexpr int NE = REP * kD;          // elements of the [REP][128] output
+  float* sRed = (float*)sKV;            // [kWarps][REP][128] f32 (the ring is idle now)
   if (half == 0) {
 #pragma unroll
     for (int i = 0; i < REP; ++i)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sRed[(warp * REP + i) * kD + dc * 8 + e] = acc[i][e];
+      for (int e = 0; e < 8; ++e) sRed[warp * NE + i * kD + dc * 8 + e] = acc[i][e];
   }
   __syncthreads();
-  float o[REP];
+  constexpr int kEpt = NE >= kThreads ? NE / kThreads : 1;   // elements per thread
+  const int e0 = tid * kEpt;             // this thread's elements [e0, e0 + kEpt) (one head)
+  const bool elem_thread = e0 < NE;
+  const int hi = elem_thread ? e0 / kD : 0;
+  float o[kEpt];
 #pragma unroll
-  for (int i = 0; i < REP; ++i)
-    o[i] = (sRed[(0 * REP + i) * kD + tid] + sRed[(1 * REP + i) * kD + tid]) +
-           (sRed[(2 * REP + i) * kD + tid] + sRed[(3 * REP + i) * kD + tid]);
+  for (int j = 0; j < kEpt; ++j) {
+    float a = 0.f;
+    if (elem_thread) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) a += sRed[w * NE + e0 + j];
+    }
+    o[j] = a;
+  }
 
-  if (n_act == 1) {  // one split: already complete
+  if (CLUSTER && gridDim.x > 1) {
+    float* sPart = sRed + kWarps * NE;   // this CTA's unnormalised partial [NE]
+    if (elem_thread) {
 #pragma unroll
-    for (int i = 0; i < REP; ++i) {
-      const float r = o[i] / sRun[8 + i];
-      if (p.out_bf16) p.out_bf16[(head0 + i) * kD + tid] = __float2bfloat16_rn(r);
-      else p.out_f32[(head0 + i) * kD + tid] = r;
+      for (int j = 0; j < kEpt; ++j) sPart[e0 + j] = o[j];
+    }
+    cluster_sync();  // every CTA's (m, l, partial) is visible cluster-wide
+    const uint32_t cl = gridDim.x;
+    const int per = NE / (int)cl;        // output elements combined by this CTA
+    for (int e = tid; e < per; e += kThreads) {
+      const int el = s * per + e, i = el / kD;
+      float M = -INFINITY;
+      for (uint32_t r = 0; r < cl; ++r) M = fmaxf(M, ld_peer(&sRun[i], r));
+      float L = 0.f, O = 0.f;
+      for (uint32_t r = 0; r < cl; ++r) {
+        const float w = exp2f(ld_peer(&sRun[i], r) - M);
+        L = fmaf(w, ld_peer(&sRun[8 + i], r), L);
+        O = fmaf(w, ld_peer(&sPart[el], r), O);
+      }
+      const float res = O / L;
+      if (p.out_bf16) p.out_bf16[head0 * kD + el] = __float2bfloat16_rn(res);
+      else p.out_f32[head0 * kD + el] = res;
+    }
+    cluster_sync();  // peers may still be reading this CTA's shared memory
+    return;
+  }
+
+  if (n_act == 1) {  // one split (or a cluster of one): already complete
+    if (elem_thread) {
+      const float inv = 1.0f / sRun[8 + hi];
+#pragma unroll
+      for (int j = 0; j < kEpt; ++j) {
+        const float r = o[j] * inv;
+        if (p.out_bf16) p.out_bf16[head0 * kD + e0 + j] = __float2bfloat16_rn(r);
+        else p.out_f32[head0 * kD + e0 + j] = r;
+      }
     }
     return;
   }
@@ -402,8 +491,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   // ---- publish the partial, take a ticket; the last split combines
   const size_t slot0 = ((size_t)b * p.Hkv + g) * p.n_splits;
   const size_t slot = slot0 + s;
+  if (elem_thread) {
 #pragma unroll
-  for (int i = 0; i < REP; ++i) p.ws_acc[(slot * REP + i) * kD + tid] = o[i];
+    for (int j = 0; j < kEpt; ++j) p.ws_acc[slot * NE + e0 + j] = o[j];
+  }
   if (tid < REP) {
     p.ws_ml[(slot * REP + tid) * 2 + 0] = sRun[tid];
     p.ws_ml[(slot * REP + tid) * 2 + 1] = sRun[8 + tid];
@@ -416,7 +507,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
   __threadfence();
 
   // weights w[k][i] = exp2(m_k - M_i), sums l[k][i], totals L_i, all in shared memory
-  float* sW = (float*)sKV + 4 * REP * kD;       // after sRed: [kMaxSplits][REP]
+  float* sW = (float*)sKV + kWarps * NE;        // after sRed: [kMaxSplits][REP]
   float* sLk = sW + kMaxSplits * REP;           // [kMaxSplits][REP]
   float* sL = sLk + kMaxSplits * REP;           // [REP]
   for (int idx = tid; idx < n_act * REP; idx += kThreads) {
@@ -436,34 +527,33 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const AttnParams p) {
     sL[tid] = L;
   }
   __syncthreads();
-  // thread t accumulates elements [t*REP, t*REP + REP) of the [REP][128]
-  // partials (one head, REP adjacent dims); 16 splits of loads in flight
-  const int e0 = tid * REP, hi = e0 / kD;
-  float O[REP];
+  // this thread's kEpt elements of every split's partial; 16 splits of loads in flight
+  if (elem_thread) {
+    float O[kEpt];
 #pragma unroll
-  for (int j = 0; j < REP; ++j) O[j] = 0.f;
-  const float* accp = p.ws_acc + slot0 * REP * kD + e0;
-  for (int k0 = 0; k0 < n_act; k0 += 16) {
-    float v[16][REP];
+    for (int j = 0; j < kEpt; ++j) O[j] = 0.f;
+    const float* accp = p.ws_acc + slot0 * NE + e0;
+    for (int k0 = 0; k0 < n_act; k0 += 16) {
+      float v[16][kEpt];
 #pragma unroll
-    for (int u = 0; u < 16; ++u)
-      if (k0 + u < n_act) load_cg<REP>(accp + (size_t)(k0 + u) * REP * kD, v[u]);
+      for (int u = 0; u < 16; ++u)
+        if (k0 + u < n_act) load_cg<kEpt>(accp + (size_t)(k0 + u) * NE, v[u]);
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      if (k0 + u < n_act) {
-        const float w = sW[(k0 + u) * REP + hi];
+      for (int u = 0; u < 16; ++u) {
+        if (k0 + u < n_act) {
+          const float w = sW[(k0 + u) * REP + hi];
 #pragma unroll
-        for (int j = 0; j < REP; ++j) O[j] = fmaf(w, v[u][j], O[j]);
+          for (int j = 0; j < kEpt; ++j) O[j] = fmaf(w, v[u][j], O[j]);
+        }
       }
     }
-  }
-  const float invL = 1.0f / sL[hi];
+    const float invL = 1.0f / sL[hi];
 #pragma unroll
-  for (int j = 0; j < REP; ++j) {
-    const float r = O[j] * invL;
-    const size_t o = (head0 + hi) * kD + (e0 - hi * kD) + j;
-    if (p.out_bf16) p.out_bf16[o] = __float2bfloat16_rn(r);
-    else p.out_f32[o] = r;
+    for (int j = 0; j < kEpt; ++j) {
+      const float r = O[j] * invL;
+      if (p.out_bf16) p.out_bf16[head0 * kD + e0 + j] = __float2bfloat16_rn(r);
+      else p.out_f32[head0 * kD + e0 + j] = r;
+    }
   }
   if (tid == 0) p.ws_cnt[(size_t)b * p.Hkv + g] = 0;
 }
@@ -478,28 +568,71 @@ __global__ void rope_table_kernel(float2* table, int max_pos, int half, double t
   table[i] = make_float2((float)cs, (float)sn);
 }
 
-template <int REP, bool FUSED>
-cudaError_t launch_rep(const AttnParams& prm, const Launch& L) {
-  auto k = attn_kernel<REP, FUSED>;
+template <int REP, bool FUSED, bool CLUSTER>
+cudaError_t launch_rep(const AttnParams& prm, int cluster, const Launch& L) {
+  auto k = attn_kernel<REP, FUSED, CLUSTER>;
   const size_t smem = carve(REP).total;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    if (CLUSTER) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
+  if (CLUSTER) {
+    dim3 grid(cluster, prm.Hkv, prm.B);
+    return launch_ex_cluster(k, grid, dim3(threads_for(REP)), smem, cluster, L, prm);
+  }
   dim3 grid(prm.n_splits, prm.Hkv, prm.B);
-  return launch_ex(k, grid, dim3(kThreads), smem, L, prm);
+  return launch_ex(k, grid, dim3(threads_for(REP)), smem, L, prm);
+}
+
+// Cluster size for the fused step: the smallest power of two that gives about
+// one CTA per SM over batch x kv heads, at most 16 (8 if the device cannot
+// co-schedule clusters of 16 of this kernel).
+template <int REP, bool FUSED>
+int pick_cluster(int B, int Hkv, int max_cl) {
+  const int sms = dev_info().sm_count;
+  const int pairs = std::max(1, B * Hkv);
+  int cl = 1;
+  while (cl < std::min(16, max_cl) && pairs * cl * 2 <= sms) cl *= 2;
+  static int max_ok = 0;
+  if (max_ok == 0) {
+    auto k = attn_kernel<REP, FUSED, true>;
+    max_ok = 8;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)carve(REP).total) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1, 1);
+      cfg.blockDim = dim3(threads_for(REP));
+      cfg.dynamicSmemBytes = carve(REP).total;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 16;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n >= 1) max_ok = 16;
+    }
+    cudaGetLastError();
+  }
+  return std::min(cl, max_ok);
 }
 
 }  // namespace
 
-// Tokens per split: about two CTAs per SM at small batch, a single split per
-// sequence once batch x kv heads fills the GPU, never more than kMaxSplits.
+// Tokens per split: about one CTA per SM at small batch (fewer partials for
+// the combine), a single split per sequence once batch x kv heads fills the
+// GPU, never more than kMaxSplits.
 int attn_chunk(int B, int Hkv, int max_ctx) {
   const int sms = dev_info().sm_count;
   const int pairs = std::max(1, B * Hkv);
-  const int want = std::max(1, (2 * sms + pairs - 1) / pairs);
+  const int want = std::max(1, (sms + pairs - 1) / pairs);
   int chunk = (max_ctx + want - 1) / want;
   chunk = std::max(kTile, ((chunk + kTile - 1) / kTile) * kTile);
   while ((max_ctx + chunk - 1) / chunk > kMaxSplits) chunk += kTile;
@@ -551,9 +684,12 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   p.err = L.err;
   p.trig_late = L.trig_late;
   const bool fused = a.qkv != nullptr;
-#define QD_ATTN_CASE(R)                                                      \
-  case R:                                                                    \
-    return fused ? launch_rep<R, true>(p, L) : launch_rep<R, false>(p, L);
+  // the fused decode step splits each sequence across one thread block cluster;
+  // the standalone call keeps the workspace split (its workspace is the scratch)
+#define QD_ATTN_CASE(R)                                                                   \
+  case R:                                                                                 \
+    if (fused && a.use_cluster > 1) return launch_rep<R, true, true>(p, pick_cluster<R, true>(a.B, a.Hkv, a.use_cluster), L); \
+    return fused ? launch_rep<R, true, false>(p, 0, L) : launch_rep<R, false, false>(p, 0, L);
   switch (rep) {
     QD_ATTN_CASE(1)
     QD_ATTN_CASE(2)

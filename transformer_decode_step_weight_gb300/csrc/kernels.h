@@ -84,6 +84,7 @@ struct AttnArgs {
   void* workspace;
   size_t ws_bytes;
   int max_ctx;            // upper bound of keys per sequence (sizes the split grid)
+  int use_cluster;        // fused form: > 1 splits each sequence over a cluster of at most this many CTAs
 };
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx);
 int attn_chunk(int B, int Hkv, int max_ctx);
