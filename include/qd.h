@@ -86,7 +86,9 @@ int qd_version(void);
 /* W: bf16 [rows, cols]. x: bf16 [batch, cols] (x_is_f32 = 0) or f32            */
 /* [batch, cols] (x_is_f32 = 1; the kernel rounds x to bf16 first). y: f32      */
 /* [batch, rows]. Accumulation in f32, deterministic order.                   */
-/* Limits: cols % 8 == 0, 1 <= batch <= 8, rows >= 1.                          */
+/* batch <= 8: CUDA-core GEMV (cols % 8 == 0). 9 <= batch <= 64: the product is */
+/* a dense contraction and runs on the tcgen05 tensor cores ("qwen3-8b-rtx4080- */
+/* cutedsl" README, "Baseline tiled GEMM"); needs bf16 x and cols % 64 == 0.    */
 int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
                  float* y, int batch, cudaStream_t stream);
 
@@ -209,6 +211,8 @@ int qd_destroy_layer(qd_layer* layer);
 /* rope_table: from qd_rope_table_init with max_pos >= every position reached.  */
 /* logits: f32 [batch, vocab] device output. workspace: device scratch of        */
 /* qd_step_workspace_bytes(args) bytes, zero-filled before first use.           */
+/* batch <= 8 runs the GEMV path (BF16 or Q8_0; Q8_0 at batch 1); 9..64 (BF16)   */
+/* runs every projection as a tcgen05 GEMM over the batch (dims % 64 == 0).      */
 typedef struct {
   const qd_layer* const* layers;
   int n_layers;

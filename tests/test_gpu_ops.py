@@ -42,6 +42,31 @@ def test_gemv_bf16(cuda_lib, R, K, B):
         assert rel_max_abs(y[b].cpu().numpy(), ref) < GEMV_TOL
 
 
+@pytest.mark.parametrize("R,K,B", [(128, 64, 9), (300, 1024, 16), (4096, 4096, 64), (1000, 12288, 33),
+                                   (6144, 4096, 64), (151936, 4096, 64)])
+def test_gemm_bf16_tensor_cores(cuda_lib, R, K, B):
+    # 9 <= batch <= 64: the tcgen05 path (ragged last 128-row tile, batch below 64)
+    g = _gen(R * 7 + B)
+    W = (torch.randn((R, K), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    x = torch.randn((B, K), generator=g, device=DEV).to(torch.bfloat16)
+    y = api.gemv_bf16(W, x)
+    torch.cuda.synchronize()
+    Wb, xb = synth.bits_u16(W), synth.bits_u16(x)
+    rows = np.arange(R) if R <= 8192 else np.arange(0, R, 97)
+    for b in sorted({0, B // 2, B - 1}):
+        ref = oracle.gemv_bf16(Wb[rows], oracle.bf16_to_f64(xb[b]))
+        assert rel_max_abs(y[b].cpu().numpy()[rows], ref) < GEMV_TOL, b
+
+
+def test_gemm_bf16_tensor_cores_integer_exact(cuda_lib):
+    g = _gen(13)
+    W = torch.randint(-8, 9, (384, 512), generator=g, device=DEV).to(torch.bfloat16)
+    x = torch.randint(-8, 9, (24, 512), generator=g, device=DEV).to(torch.bfloat16)
+    y = api.gemv_bf16(W, x)
+    ref = x.double().cpu() @ W.double().cpu().T
+    assert torch.equal(y.cpu().double(), ref)
+
+
 def test_gemv_bf16_f32_input_rounds_to_bf16(cuda_lib):
     g = _gen(5)
     W = (torch.randn((700, 4096), generator=g, device=DEV) * 0.02).to(torch.bfloat16)

@@ -92,6 +92,54 @@ def test_small_bf16_batch_paged_teacher_forced(cuda_lib):
     assert api.check_device_error() == 0
 
 
+@pytest.mark.parametrize("batch", [12, 64])
+def test_batched_tensor_core_step_teacher_forced(cuda_lib, batch):
+    # 9..64 sequences: projections on tcgen05, paged KV through a random page table
+    mt = synth.make_model(synth.SMALL64, "bf16", 7, DEV, batch=batch, ctx=None, steps=3, paged=True)
+    om = oracle_model(mt)
+    check = sorted({0, batch // 3, batch - 1})
+    caches = {b: oracle_caches(mt, b, int(mt.seq_lens[b]) + 3) for b in check}
+    dec = api.Decoder(mt, max_steps=3)
+    assert dec.launches_per_step == 1 + 8 * 2 + 3
+    toks = {b: int(mt.start_tok[b]) for b in check}
+    for t in range(3):
+        dec.step()
+        torch.cuda.synchronize()
+        for b in check:
+            g = dec.logits[b].double().cpu().numpy()
+            ref = oracle.decode_token(om, toks[b], int(mt.seq_lens[b]) + t, caches[b][0], caches[b][1],
+                                      mode="bf16", act="bf16")
+            assert rel_max_abs(g, ref) < TOL["bf16"], (t, b)
+            toks[b] = int(dec.tok[b])
+            assert toks[b] == oracle.argmax_first(g)
+    assert api.check_device_error() == 0
+
+
+def test_qwen3_8b_batched_paged_layer(cuda_lib):
+    """The batched workload's shapes: 64 sequences, Qwen3-8B layer, 16-token pages through a
+    random page table, context uniform in [128, 4096]; sampled sequences checked whole."""
+    s = synth.QWEN3_8B
+    mt = synth.make_model(s, "bf16", 9, DEV, n_layers=1, batch=64, ctx=None, steps=1, paged=True)
+    om = oracle_model(mt)
+    dec = api.Decoder(mt, max_steps=1)
+    check = [0, 31, 63]
+    caches = {b: oracle_caches(mt, b, int(mt.seq_lens[b]) + 1) for b in check}
+    dec.step()
+    torch.cuda.synchronize()
+    res = dec.residual()
+    for b in check:
+        x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[b])]))
+        ref = oracle.layer_step(om.dims, om.layers[0], x0, caches[b][0][0], caches[b][1][0],
+                                int(mt.seq_lens[b]), mode="bf16", act="bf16")
+        assert rel_max_abs(res[b].double().cpu().numpy(), ref) < TOL["bf16"], b
+    rows = np.arange(0, s.vocab, 211)
+    for b in check:
+        lg = dec.logits[b].double().cpu().numpy()
+        assert rel_max_abs(lg[rows], oracle.lm_head_rows(om, res[b].double().cpu().numpy(), rows)) < TOL["bf16"]
+        assert int(dec.tok[b]) == oracle.argmax_first(lg)
+    assert api.check_device_error() == 0
+
+
 def test_graph_replay_is_bit_identical_to_eager(cuda_lib):
     runs = []
     for use_graph in (False, True):

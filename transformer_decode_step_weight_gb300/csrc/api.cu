@@ -11,6 +11,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -138,11 +139,19 @@ int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
                  cudaStream_t stream) {
   if (!W || !x || !y) return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: null pointer");
   if (rows < 1 || cols < 8) return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: rows=%d cols=%d", rows, cols);
+  if (!aligned16(W) || !aligned16(x) || !aligned16(y))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: pointers must be 16-byte aligned");
+  if (batch > 8) {  // a real contraction: tcgen05 tensor cores
+    if (x_is_f32 || !gemm_tc_supported(rows, cols, batch))
+      return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: batch %d needs bf16 x, cols %% 64 == 0 and batch <= 64", batch);
+    GemmTcArgs g;
+    g.W = W; g.X = x; g.R = rows; g.K = cols; g.B = batch; g.epi = EPI_STORE; g.y = y;
+    cudaError_t e = launch_gemm_tc(g, make_launch(stream, false));
+    return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_bf16 (tensor cores)");
+  }
   if (!gemv_bf16_supported(cols, batch))
     return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: cols=%d batch=%d (need cols%%8==0, cols<=32768, 1<=batch<=8)",
                 cols, batch);
-  if (!aligned16(W) || !aligned16(x) || !aligned16(y))
-    return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: pointers must be 16-byte aligned");
   GemvBf16Args a;
   a.W = W; a.R = rows; a.K = cols; a.batch = batch;
   a.pro = x_is_f32 ? PRO_X_F32 : PRO_X_BF16;
@@ -335,6 +344,7 @@ struct StepWs {
   float* qkv;       // [B, QKV]
   void* attn;       // [B, Hq*D] bf16 or f32
   float* gu;        // [B, 2F]
+  void* xn;         // bf16 [B, max(H, F)]: normed / SwiGLU activations (batched path)
   void* attn_ws;
   void* argmax_ws;
   size_t total;
@@ -353,6 +363,7 @@ StepWs step_ws_layout(const qd_step_args* a, void* base) {
   w.qkv = (float*)(p + off); off += al256((size_t)B * qkv * 4);
   w.attn = (void*)(p + off); off += al256((size_t)B * d.n_q_heads * d.head_dim * 4);
   w.gu = (float*)(p + off); off += al256((size_t)B * 2 * d.ffn * 4);
+  w.xn = (void*)(p + off); off += al256((size_t)B * std::max(d.hidden, d.ffn) * 2);
   w.attn_ws = (void*)(p + off);
   off += al256(attn_workspace_bytes(B, d.n_q_heads, d.n_kv_heads, a->max_pages * a->page_size));
   w.argmax_ws = (void*)(p + off); off += al256(argmax_workspace_bytes(B));
@@ -379,15 +390,18 @@ int validate_step(const qd_step_args* a) {
     if (!a->k_cache[i] || !a->v_cache[i] || !aligned16(a->k_cache[i]) || !aligned16(a->v_cache[i]))
       return fail(QD_ERR_INVALID_ARG, "qd_decode_step: cache %d null or unaligned", i);
   if (a->vocab < 1 || a->max_steps < 1) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: vocab/max_steps");
-  if (a->batch < 1 || a->batch > 8)
-    return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batch=%d (the GEMV step supports 1..8)", a->batch);
+  if (a->batch < 1 || a->batch > 64)
+    return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batch=%d (supported 1..64)", a->batch);
   if (d0.wtype == QD_W_Q8_0 && a->batch != 1)
     return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 step supports batch 1");
   if (d0.wtype == QD_W_BF16) {
     const int ks[3] = {d0.hidden, d0.n_q_heads * d0.head_dim, d0.ffn};
-    for (int k : ks)
-      if (!gemv_bf16_supported(k, a->batch))
+    for (int k : ks) {
+      if (a->batch <= 8 && !gemv_bf16_supported(k, a->batch))
         return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: GEMV K=%d with batch %d not supported", k, a->batch);
+      if (a->batch > 8 && !gemm_tc_supported(1, k, a->batch))
+        return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batched K=%d must be a multiple of 64", k);
+    }
   }
   int rc = check_attn_shape("qd_decode_step", a->batch, d0.n_q_heads, d0.n_kv_heads, d0.head_dim, a->page_size,
                             a->max_pages, a->n_pages);
@@ -412,7 +426,49 @@ int validate_step(const qd_step_args* a) {
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
 
+// Batched decode (9..64 sequences, BF16): every projection is a tcgen05 GEMM over
+// the batch; RMSNorm and SwiGLU write the bf16 GEMM operand in small row kernels.
+int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const StepWs w = step_ws_layout(a, a->workspace);
+  const Launch L = make_launch(stream, true);
+  const int B = a->batch;
+  const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int QKV = (Hq + 2 * Hkv) * D;
+  auto gemm = [&](const void* W, int R, int K, const void* X, int epi, float* y) {
+    GemmTcArgs g;
+    g.W = W; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
+    return launch_gemm_tc(g, L);
+  };
+  QD_TRY(launch_embed(a->embed, H, a->vocab, a->tok, B, w.res, L), "embed");
+  for (int li = 0; li < a->n_layers; ++li) {
+    const qd_layer* l = a->layers[li];
+    QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_in, B, H, d.rms_eps, w.xn, L), "rmsnorm");
+    QD_TRY(gemm(l->w.w_qkv, QKV, H, w.xn, EPI_STORE, w.qkv), "qkv gemm");
+    AttnArgs at = {};
+    at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
+    at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps; at.act_bf16 = 1;
+    at.pos = a->pos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = a->page_table;
+    at.B = B; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
+    at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D); at.out_bf16 = w.attn;
+    at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.use_cluster = 0;
+    QD_TRY(launch_attention(at, L), "attention");
+    QD_TRY(gemm(l->w.w_o, H, Hq * D, w.attn, EPI_RESID_ADD, w.res), "o gemm");
+    QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, B, H, d.rms_eps, w.xn, L), "rmsnorm");
+    QD_TRY(gemm(l->w.w_gu, 2 * F, H, w.xn, EPI_STORE, w.gu), "gu gemm");
+    QD_TRY(launch_swiglu_rows(w.gu, B, F, w.xn, L), "swiglu");
+    QD_TRY(gemm(l->w.w_down, H, F, w.xn, EPI_RESID_ADD, w.res), "down gemm");
+  }
+  QD_TRY(launch_rmsnorm_rows(w.res, a->final_norm, B, H, d.rms_eps, w.xn, L), "final rmsnorm");
+  QD_TRY(gemm(a->lm_head, a->vocab, H, w.xn, EPI_STORE, a->logits), "lm head gemm");
+  QD_TRY(launch_argmax_advance(a->logits, a->vocab, B, a->tok, a->pos, a->step, a->out_tokens, a->max_steps,
+                               w.argmax_ws, L),
+         "argmax");
+  return QD_OK;
+}
+
 int run_step(const qd_step_args* a, cudaStream_t stream) {
+  if (a->batch > 8) return run_step_tc(a, stream);
   const qd_layer_dims& d = a->layers[0]->dims;
   const StepWs w = step_ws_layout(a, a->workspace);
   const Launch L = make_launch(stream, true);
@@ -511,6 +567,7 @@ size_t qd_step_workspace_bytes(const qd_step_args* a) {
 
 int qd_step_launch_count(const qd_step_args* a) {
   if (!a || a->n_layers < 1) return 0;
+  if (a->batch > 8) return 1 + 8 * a->n_layers + 3;
   return 1 + 5 * a->n_layers + 2;
 }
 

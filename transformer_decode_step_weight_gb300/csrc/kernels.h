@@ -40,6 +40,22 @@ struct GemvBf16Args {
 bool gemv_bf16_supported(int K, int batch);
 cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L);
 
+// ----------------------------------------------------------------- batched GEMM (tcgen05)
+struct GemmTcArgs {
+  const void* W;          // bf16 [R, K]
+  const void* X;          // bf16 [B, K]
+  int R, K, B;            // B <= 64
+  int epi;                // GemvEpi
+  float* y;               // f32 [B, R]
+};
+bool gemm_tc_supported(int R, int K, int B);
+cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L);
+
+// row-wise helpers of the batched step
+cudaError_t launch_rmsnorm_rows(const float* x, const void* w, int B, int K, float eps, void* out_bf16,
+                                const Launch& L);
+cudaError_t launch_swiglu_rows(const float* gu, int B, int F, void* out_bf16, const Launch& L);
+
 // ----------------------------------------------------------------- GEMV Q8_0
 struct GemvQ8Args {
   const int8_t* qs;       // int8 [R, K]

@@ -129,6 +129,41 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_advance_kernel(const Ar
   }
 }
 
+// out[b, :] = bf16(w * bf16(x[b, :] * rsqrt(mean(x[b, :]^2) + eps))), Qwen cast order
+__global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* x, const __nv_bfloat16* w, int K, float eps,
+                                                           __nv_bfloat16* out) {
+  __shared__ float red[8];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x;
+  const float* xr = x + (size_t)b * K;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 4; i < K; i += blockDim.x * 4) {
+    const float4 v = *(const float4*)(xr + i);
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+  const float inv = 1.0f / sqrtf(tot / (float)K + eps);
+  for (int i = threadIdx.x; i < K; i += blockDim.x)
+    out[(size_t)b * K + i] = __float2bfloat16_rn(__bfloat162float(w[i]) * round_bf16(xr[i] * inv));
+}
+
+// out[b, j] = bf16(silu(g) * u) with g = gu[b, j], u = gu[b, F + j]
+__global__ void __launch_bounds__(256) swiglu_rows_kernel(const float* gu, int F, __nv_bfloat16* out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.y;
+  const float* row = gu + (size_t)b * 2 * F;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < F; j += gridDim.x * blockDim.x) {
+    const float g = row[j], u = row[F + j];
+    out[(size_t)b * F + j] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+  }
+}
+
 __global__ void paged_indices_kernel(const int32_t* pt, int B, int max_pages, int ps, int n,
                                      int32_t* idx) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -168,6 +203,17 @@ cudaError_t launch_embed(const void* embed, int H, int V, const int32_t* tok, in
   const int blocks = std::max(1, std::min(8, ceil_div(H, threads * 8)));
   return launch_ex(embed_kernel, dim3(blocks, B), dim3(threads), 0, L, (const __nv_bfloat16*)embed, H,
                    V, tok, res, L.err);
+}
+
+cudaError_t launch_rmsnorm_rows(const float* x, const void* w, int B, int K, float eps, void* out_bf16,
+                                const Launch& L) {
+  return launch_ex(rmsnorm_rows_kernel, dim3(B), dim3(256), 0, L, x, (const __nv_bfloat16*)w, K, eps,
+                   (__nv_bfloat16*)out_bf16);
+}
+
+cudaError_t launch_swiglu_rows(const float* gu, int B, int F, void* out_bf16, const Launch& L) {
+  const int blocks = std::max(1, std::min(32, ceil_div(F, 256)));
+  return launch_ex(swiglu_rows_kernel, dim3(blocks, B), dim3(256), 0, L, gu, F, (__nv_bfloat16*)out_bf16);
 }
 
 cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_tokens,

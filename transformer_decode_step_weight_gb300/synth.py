@@ -54,6 +54,8 @@ QWEN3_8B = Shape("qwen3-8b", 4096, 32, 8, 128, 12288, 36, 151936, False)
 # small shapes for fast parity cases (several tiles, ragged tails)
 TINY = Shape("tiny", 256, 4, 2, 128, 544, 2, 1000, True)
 SMALL = Shape("small", 512, 8, 2, 128, 1376, 3, 5003, False)
+# dims that are multiples of 64, as the batched (tensor-core) projections need
+SMALL64 = Shape("small64", 512, 8, 2, 128, 1408, 2, 2999, False)
 
 
 @dataclass
