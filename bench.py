@@ -33,7 +33,6 @@ import torch  # noqa: E402
 from transformer_decode_step_weight_gb300 import synth  # noqa: E402
 
 METRIC = "Qwen3-8B-shape decode tok/s @bs1; achieved HBM GB/s vs GB300 peak"
-RUN_LEN = 128          # greedy steps of one decode run (the workload)
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
 
 
@@ -43,16 +42,19 @@ def parse():
     ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qwen3-8b-bf16", choices=["qwen3-8b-bf16", "qwen3-0.6b"])
+    ap.add_argument("--workload", default="qwen3-8b-bf16",
+                    choices=["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-bf16-paged-b64"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--no-probe", action="store_true", help="skip the dominant-kernel event probe")
-    ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "attention"],
+    ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "attention", "gemm_tc"],
                     help="time one kernel alone on a full-size shape (profiling aid) instead of the step")
     ap.add_argument("--rows", type=int, default=24576)
     ap.add_argument("--cols", type=int, default=4096)
     ap.add_argument("--ctx", type=int, default=4224)
+    ap.add_argument("--batch", type=int, default=64, help="rows of x for --kernel gemm_tc")
+    ap.add_argument("--act", choices=["f32", "i8"], default="f32", help="Q8_0 activation lane")
     return ap.parse_args()
 
 
@@ -199,8 +201,12 @@ def run_ours(args, dist, rank, world, local):
     torch.cuda.set_device(dev)
     wl = synth.WORKLOADS[args.workload]
     s = wl.shape
-    mt = synth.make_model(s, wl.wtype, args.seed + rank, dev, ctx=wl.ctx, steps=RUN_LEN)
-    dec = api.Decoder(mt, max_steps=RUN_LEN, device=dev)
+    run_len = wl.steps
+    mt = synth.make_model(s, wl.wtype, args.seed + rank, dev, batch=wl.batch, ctx=None if wl.paged else wl.ctx,
+                          steps=run_len, paged=wl.paged)
+    lane = api.QD_ACT_I8 if args.act == "i8" else api.QD_ACT_F32
+    dec = api.Decoder(mt, max_steps=run_len, act=lane, device=dev)
+    lens = [int(v) for v in mt.seq_lens.cpu()]
     tok0, pos0 = dec.tok.clone(), dec.pos.clone()
 
     def reset():
@@ -228,7 +234,7 @@ def run_ours(args, dist, rank, world, local):
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for i in range(K):
-            if i and i % RUN_LEN == 0:
+            if i and i % run_len == 0:
                 reset()
             dec.replay()
         ev1.record(stream)
@@ -243,31 +249,35 @@ def run_ours(args, dist, rank, world, local):
     value = toks / (ms_max / 1e3)
     # algorithmic bytes of the timed steps
     wb = weight_bytes(s, wl.wtype)
-    step_bytes = [wb + kv_bytes(s, wl.ctx + (i % RUN_LEN)) for i in range(K)]
+    step_bytes = [wb + sum(kv_bytes(s, n + (i % run_len)) for n in lens) for i in range(K)]
     hbm_peak, peak_kind = peaks()
     step_gbs = sum(step_bytes) / (ms / 1e3) / 1e9
 
     # ---- dominant kernel: the BF16 GEMV, every launch of one token, events on its stream
-    roof = None if args.no_probe else dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind)
+    roof = None if (args.no_probe or wl.batch > 8 or wl.wtype != "bf16") else dominant_kernel_roofline(api, mt, s, stream, hbm_peak,
+                                                                                 peak_kind)
 
     # ---- end to end through the public API: per step H2D of the input token/position
     # from pinned memory, the step, D2H of the next token, host reads it
-    e2e = run_e2e(dec, stream, args.e2e_steps, reset, dist, world)
+    e2e = run_e2e(dec, stream, args.e2e_steps, reset, dist, world, run_len)
     launches = K * dec.launches_per_step
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(mt, s, wl)
+        cpu = cpu_baseline(mt, s, wl, lens[0])
 
     if rank == 0:
         out = {
             "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.wtype == "bf16" else "q8_0/f32",
+            "data": "synthetic",
             "config": {"workload": wl.name, "description": wl.description, "global_batch": dec.batch * world,
-                       "ctx_start": wl.ctx, "decode_run_steps": RUN_LEN, "parallelism": f"replicas x{world}",
+                       "q8_lane": args.act if wl.wtype == "q8_0" else None,
+                       "ctx_start": wl.ctx if not wl.paged else "uniform[128,4096]", "decode_run_steps": run_len,
+                       "parallelism": f"replicas x{world}",
                        "graph": "one CUDA graph per step, PDL between kernels",
-                       "l2": "inputs larger than L2 (15.1 GB of weights streamed per step)"},
+                       "l2": f"inputs larger than L2 ({wb / 1e9:.1f} GB of weights streamed per step)"},
             "roofline": roof,
             "step_roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                               "frac": round(step_gbs / hbm_peak, 4), "peak_kind": peak_kind,
@@ -315,38 +325,40 @@ def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "traffic": traffic}
 
 
-def run_e2e(dec, stream, steps, reset, dist, world):
+def run_e2e(dec, stream, steps, reset, dist, world, run_len):
+    """Host-driven loop through the public API: each step copies the input tokens and
+    positions from pinned host memory, replays the step, copies the next tokens back
+    and the host reads them before the next step."""
     if steps <= 0:
         return None
-    dev = dec.tok.device
-    h_in = torch.empty(2, dtype=torch.int32, pin_memory=True)
-    h_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    B = dec.batch
+    h_in = torch.empty((2, B), dtype=torch.int32, pin_memory=True)
+    h_out = torch.empty(B, dtype=torch.int32, pin_memory=True)
     with torch.cuda.stream(stream):
         reset()
     stream.synchronize()
-    h_in[0] = int(dec.tok[0])
-    h_in[1] = int(dec.pos[0])
+    h_in[0].copy_(dec.tok.cpu())
+    h_in[1].copy_(dec.pos.cpu())
     barrier(dist)
     t0 = time.perf_counter()
     for i in range(steps):
         with torch.cuda.stream(stream):
-            if i and i % RUN_LEN == 0:
+            if i and i % run_len == 0:
                 reset()
                 stream.synchronize()
-                h_in[0] = int(dec.tok[0])
-                h_in[1] = int(dec.pos[0])
-            dec.tok[:1].copy_(h_in[0:1], non_blocking=True)
-            dec.pos[:1].copy_(h_in[1:2], non_blocking=True)
+                h_in[0].copy_(dec.tok.cpu())
+                h_in[1].copy_(dec.pos.cpu())
+            dec.tok.copy_(h_in[0], non_blocking=True)
+            dec.pos.copy_(h_in[1], non_blocking=True)
             dec.replay()
-            h_out.copy_(dec.tok[:1], non_blocking=True)
+            h_out.copy_(dec.tok, non_blocking=True)
         stream.synchronize()
-        h_in[0] = int(h_out[0])
-        h_in[1] = h_in[1] + 1
+        h_in[0].copy_(h_out)
+        h_in[1] += 1
     dt = time.perf_counter() - t0
     dt = max_over_ranks(dist, dt)
-    del dev
-    return {"value": round(steps * dec.batch * world / dt, 3), "unit": "tok/s", "h2d_bytes_per_step": 8,
-            "d2h_bytes_per_step": 4, "steps": steps}
+    return {"value": round(steps * B * world / dt, 3), "unit": "tok/s", "h2d_bytes_per_step": 8 * B,
+            "d2h_bytes_per_step": 4 * B, "steps": steps}
 
 
 def _cores():
@@ -356,7 +368,7 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(mt, s, wl, n_layers_sample: int = 8):
+def cpu_baseline(mt, s, wl, ctx, n_layers_sample: int = 8):
     """The CPU oracle, as it stands, on a bounded sample: n full-size decoder layers
     (layer 0 of the model, at the workload's context) plus n/36 of the LM-head rows,
     scaled to one token."""
@@ -366,22 +378,27 @@ def cpu_baseline(mt, s, wl, n_layers_sample: int = 8):
     torch.set_num_threads(_cores())
     od = oracle_dims(s)
     ol = oracle_layer(mt.layers[0], mt.wtype)
-    ks, vs = oracle_caches(_OneLayer(mt), 0, wl.ctx + 1)
+    ks, vs = oracle_caches(_OneLayer(mt), 0, ctx + 1)
     x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[0])]))
     frac = n_layers_sample / s.n_layers
     rows = np.arange(0, s.vocab, int(round(1 / frac)))
-    lm_bits = synth.bits_u16(mt.lm_head[torch.as_tensor(rows, device=mt.lm_head.device)])
+    idx = torch.as_tensor(rows, device=mt.lm_head.device)
+    lm_bits = synth.bits_u16(mt.lm_head[idx]) if mt.lm_head_scales is None else None
+    mode, act = ("bf16", "bf16") if mt.wtype == "bf16" else ("f32", "f32")
     fn = synth.bits_u16(mt.final_norm)
     t0 = time.perf_counter()
     res = x0
     for _ in range(n_layers_sample):
-        res = oracle.layer_step(od, ol, x0, ks[0], vs[0], wl.ctx, mode="bf16", act="bf16")
-    xf = oracle.rmsnorm(res, oracle.bf16_to_f64(fn), s.rms_eps, "bf16")
-    oracle.gemv_bf16(lm_bits, xf)
+        res = oracle.layer_step(od, ol, x0, ks[0], vs[0], ctx, mode=mode, act=act)
+    xf = oracle.rmsnorm(res, oracle.bf16_to_f64(fn), s.rms_eps, mode)
+    if mt.lm_head_scales is None:
+        oracle.gemv_bf16(lm_bits, xf)
+    else:
+        oracle.gemv_q8_0(synth.host_i8(mt.lm_head[idx]), synth.bits_u16(mt.lm_head_scales[idx]), x=xf, act="f32")
     dt = time.perf_counter() - t0
     sec_per_tok = dt / frac
     return {"value": round(1.0 / sec_per_tok, 5), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
-            "sample": f"{n_layers_sample} of {s.n_layers} full-size decoder layers at context {wl.ctx} "
+            "sample": f"{n_layers_sample} of {s.n_layers} full-size decoder layers at context {ctx} "
                       f"plus {len(rows)} of {s.vocab} LM-head rows ({dt:.1f} s), scaled to one token"}
 
 
@@ -469,6 +486,12 @@ def run_kernel(args):
         lane = api.QD_ACT_I8 if args.kernel.endswith("i8") else api.QD_ACT_F32
         nbytes = R * K + R * (K // 32) * 2
         fn = lambda i: api.gemv_q8_0(qs[i % copies], ds[i % copies], x=x, act=lane, y=y, stream=stream)  # noqa: E731
+    elif args.kernel == "gemm_tc":
+        Ws = [(torch.randn((R, K), generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(copies)]
+        x = torch.randn((args.batch, K), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((args.batch, R), device=dev)
+        nbytes = R * K * 2
+        fn = lambda i: api.gemv_bf16(Ws[i % copies], x, y, stream=stream)  # noqa: E731
     else:
         s = synth.QWEN3_8B
         n = args.ctx

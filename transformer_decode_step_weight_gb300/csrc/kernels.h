@@ -104,6 +104,7 @@ struct AttnArgs {
 };
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx);
 int attn_chunk(int B, int Hkv, int max_ctx);
+cudaError_t launch_attention_mma(const AttnArgs& a, int chunk, size_t slots, const Launch& L);
 cudaError_t launch_attention(const AttnArgs& a, const Launch& L);
 // Static scratch of the allocation-free attention entry point: its capacity,
 // and its device address with the ticket counters of the shape's workspace
