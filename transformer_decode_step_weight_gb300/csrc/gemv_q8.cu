@@ -309,11 +309,340 @@ int pick_c(int K) {
   return 0;
 }
 
+// ---------------------------------------------------------------------------
+// Batch-1 Q8_0 GEMV on a TMA ring (same structure as the BF16 ring kernel): a
+// producer warp streams each stage's rows of int8 values and their fp16 scales
+// with two cp.async.bulk copies; eight consumer warps own 16-weight half-blocks
+// of every row with the activation slice (f32, or int8 + scale) in registers.
+constexpr int kConsQ = 256;
+constexpr int kRingQ = 96 * 1024;
+constexpr int kPhaseQ = 128;
+
+struct RingQ8Params {
+  const int8_t* qs;
+  const __half* d;
+  int R, K;
+  int rows_base, rows_extra;
+  int T, P, ns, stage_bytes, ring_bytes;
+  int pro;
+  const float* x;
+  const int8_t* xq;
+  const __half* xd;
+  const __nv_bfloat16* norm_w;
+  float eps;
+  int epi;
+  float* y;
+  int* err;
+  int trig_late;
+};
+
+QD_DEV void cons_sync_q() { asm volatile("bar.sync 1, %0;" ::"n"(kConsQ) : "memory"); }
+QD_DEV void mbar_arrive_q(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+template <int C, int LANE, int RPS>
+__global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const RingQ8Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = (uint64_t*)(smem + p.ring_bytes);
+  uint64_t* empty = full + 16;
+  float* red = (float*)(empty + 16);  // [kPhaseQ][wpg]
+  __shared__ float s_ss[kConsQ / 32];
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int K = p.K, KB = K / 32, KC = K / 16, ns = p.ns;
+  const int nrows = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
+  const int r0 = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
+  const int srows = p.P * RPS;
+  const int n_stages = (nrows + srows - 1) / srows;
+  const size_t qrow = (size_t)K, drow = (size_t)KB * 2;   // bytes per row of values / scales
+  const size_t dbase = (size_t)srows * qrow;               // scales follow the values in a stage
+
+  if (tid == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsQ / 32);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!p.trig_late) pdl_launch_dependents();
+
+  if (tid >= kConsQ) {  // ---- producer warp: weights only
+    if (lane == 0) {
+      for (int i = 0; i < n_stages; ++i) {
+        const int slot = i % ns;
+        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) return;
+        const int rows_i = min(srows, nrows - i * srows);
+        const size_t row = (size_t)r0 + (size_t)i * srows;
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)(rows_i * (qrow + drow)));
+        unsigned char* st = ring + (size_t)slot * p.stage_bytes;
+        bulk_g2s(st, p.qs + row * qrow, (uint32_t)(rows_i * qrow), &full[slot]);
+        bulk_g2s(st + dbase, (const unsigned char*)p.d + row * drow, (uint32_t)(rows_i * drow), &full[slot]);
+      }
+    }
+    pdl_launch_dependents();
+    return;
+  }
+
+  // ---- consumers: thread t of group g owns half-blocks ch[j] = j*T + t of every row
+  const int T = p.T;
+  const int g = tid / T, t = tid - g * T;
+  const int wpg = T >> 5, wig = t >> 5;
+  int ch[C];
+  bool cv[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) {
+    ch[j] = j * T + t;
+    cv[j] = ch[j] < KC;
+  }
+  pdl_wait();
+
+  float xf[C][16];
+  uint32_t xq[C][4];
+  float xd[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) xf[j][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) xq[j][e] = 0u;
+    xd[j] = 0.f;
+  }
+  if (p.pro == PRO_Q8_GIVEN) {
+#pragma unroll
+    for (int j = 0; j < C; ++j) {
+      if (!cv[j]) continue;
+      const uint4 a = *(const uint4*)(p.xq + (size_t)ch[j] * 16);
+      xq[j][0] = a.x; xq[j][1] = a.y; xq[j][2] = a.z; xq[j][3] = a.w;
+      xd[j] = __half2float(p.xd[ch[j] >> 1]);
+    }
+  } else {
+    if (p.pro == PRO_SWIGLU) {
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (!cv[j]) continue;
+        const float* gp = p.x + (size_t)ch[j] * 16;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 gg = *(const float4*)(gp + e), uu = *(const float4*)(gp + K + e);
+          xf[j][e] = silu(gg.x) * uu.x;
+          xf[j][e + 1] = silu(gg.y) * uu.y;
+          xf[j][e + 2] = silu(gg.z) * uu.z;
+          xf[j][e + 3] = silu(gg.w) * uu.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        if (!cv[j]) continue;
+        const float* xp = p.x + (size_t)ch[j] * 16;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 a = *(const float4*)(xp + e);
+          xf[j][e] = a.x; xf[j][e + 1] = a.y; xf[j][e + 2] = a.z; xf[j][e + 3] = a.w;
+        }
+      }
+      if (p.pro == PRO_RMSNORM) {
+        float ss = 0.f;
+        if (g == 0) {
+#pragma unroll
+          for (int j = 0; j < C; ++j)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ss = fmaf(xf[j][e], xf[j][e], ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) s_ss[tid >> 5] = ss;
+        cons_sync_q();
+        float tot = 0.f;
+        for (int i = 0; i < wpg; ++i) tot += s_ss[i];
+        const float inv = 1.0f / sqrtf(tot / (float)K + p.eps);
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+          if (!cv[j]) continue;
+#pragma unroll
+          for (int e = 0; e < 16; e += 8) {
+            const uint4 wn = *(const uint4*)(p.norm_w + (size_t)ch[j] * 16 + e);
+            const float nw[8] = {bf_lo(wn.x), bf_hi(wn.x), bf_lo(wn.y), bf_hi(wn.y),
+                                 bf_lo(wn.z), bf_hi(wn.z), bf_lo(wn.w), bf_hi(wn.w)};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) xf[j][e + k] = nw[k] * (xf[j][e + k] * inv);
+          }
+        }
+      }
+    }
+    if (LANE == 1) {  // re-quantise per 32-block; its halves sit in lanes t, t^1
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(xf[j][e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        const float dd = amax / 127.0f;
+        const float id = dd != 0.0f ? 1.0f / dd : 0.0f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t packed = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            int v = (int)roundf(xf[j][w * 4 + k] * id);
+            v = max(-127, min(127, v));
+            packed |= ((uint32_t)(v & 0xff)) << (8 * k);
+          }
+          xq[j][w] = packed;
+        }
+        xd[j] = __half2float(__float2half_rn(dd));
+      }
+    }
+  }
+
+  int ph_base = 0;
+  for (int i = 0; i < n_stages; ++i) {
+    const int slot = i % ns;
+    if (!mbar_wait_bounded(&full[slot], (uint32_t)((i / ns) & 1), p.err)) {
+      for (int k = 1; k < ns && i + k < n_stages; ++k)
+        mbar_wait_bounded(&full[(i + k) % ns], (uint32_t)(((i + k) / ns) & 1), p.err);
+      return;
+    }
+    if (i + 1 == n_stages) pdl_launch_dependents();
+    const int row0 = i * srows + g * RPS;
+    const unsigned char* st = ring + (size_t)slot * p.stage_bytes;
+    const int nv = min(RPS, nrows - row0);
+    uint4 wv[RPS][C];
+    float dw[RPS][C];
+#pragma unroll
+    for (int r = 0; r < RPS; ++r)
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        const bool ok = r < nv && cv[j];
+        const size_t lr = (size_t)(g * RPS + r);
+        wv[r][j] = ok ? *(const uint4*)(st + lr * qrow + (size_t)ch[j] * 16) : make_uint4(0u, 0u, 0u, 0u);
+        dw[r][j] = ok ? __half2float(*(const __half*)(st + dbase + lr * drow + (size_t)(ch[j] >> 1) * 2)) : 0.f;
+      }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_q(&empty[slot]);
+    float v[RPS];
+#pragma unroll
+    for (int r = 0; r < RPS; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < C; ++j) {
+        const uint32_t w4[4] = {wv[r][j].x, wv[r][j].y, wv[r][j].z, wv[r][j].w};
+        if (LANE == 0) {
+          float bs = 0.f, bs2 = 0.f;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            float f[4];
+            i8x4_to_f32(w4[w], f);
+            bs = fmaf(f[0], xf[j][w * 4], bs);
+            bs2 = fmaf(f[1], xf[j][w * 4 + 1], bs2);
+            bs = fmaf(f[2], xf[j][w * 4 + 2], bs);
+            bs2 = fmaf(f[3], xf[j][w * 4 + 3], bs2);
+          }
+          acc = fmaf(dw[r][j], bs + bs2, acc);
+        } else {
+          int dot = 0;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) dot = __dp4a((int)w4[w], (int)xq[j][w], dot);
+          acc = fmaf((float)dot, dw[r][j] * xd[j], acc);
+        }
+      }
+      v[r] = acc;
+    }
+    int rsel = 0;
+#pragma unroll
+    for (int L = 16, n = RPS; L >= 1; L >>= 1) {
+      if (n > 1) {
+        const int h = n / 2;
+        const bool up = (lane & L) != 0;
+#pragma unroll
+        for (int k = 0; k < h; ++k) {
+          const float send = up ? v[k] : v[k + h];
+          const float keep = up ? v[k + h] : v[k];
+          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, L);
+        }
+        if (up) rsel += h;
+        n = h;
+      } else {
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], L);
+      }
+    }
+    constexpr int kLowMask = 32 / RPS - 1;
+    if ((lane & kLowMask) == 0 && rsel < nv) red[(row0 + rsel - ph_base) * wpg + wig] = v[0];
+    const int done = min((i + 1) * srows, nrows);
+    if (done + srows - ph_base > kPhaseQ || i + 1 == n_stages) {
+      const int nph = done - ph_base;
+      cons_sync_q();
+      for (int r = tid; r < nph; r += kConsQ) {
+        float acc = 0.f;
+        for (int k = 0; k < wpg; ++k) acc += red[r * wpg + k];
+        float* yp = p.y + r0 + ph_base + r;
+        if (p.epi == EPI_RESID_ADD) *yp += acc;
+        else *yp = acc;
+      }
+      cons_sync_q();
+      ph_base = done;
+    }
+  }
+}
+
+template <int C, int LANE>
+cudaError_t launch_ring_q(const RingQ8Params& p, int grid, size_t smem, const Launch& L) {
+  constexpr int RPS = C == 1 ? 8 : C == 2 ? 4 : 2;
+  auto k = gemv_q8_ring_kernel<C, LANE, RPS>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         dev_info().max_smem_optin - 1024);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(k, dim3(grid), dim3(kConsQ + 32), smem, L, p);
+}
+
+int ring_q_c(int K) {
+  const int chunks = K / 16;
+  static const int opts[] = {1, 2, 3, 4};
+  for (int c : opts)
+    if (chunks <= c * kConsQ) return c;
+  return 0;
+}
+
 }  // namespace
 
 bool gemv_q8_supported(int K) { return K > 0 && K % 32 == 0 && pick_c(K) > 0; }
 
 cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
+  const bool aligned = (((uintptr_t)a.qs | (uintptr_t)a.d) & 15) == 0;
+  const int rc = (a.K % 256 == 0 && aligned) ? ring_q_c(a.K) : 0;
+  if (rc > 0) {
+    const int rps = rc == 1 ? 8 : rc == 2 ? 4 : 2;   // must match launch_ring_q
+    RingQ8Params p;
+    p.qs = a.qs; p.d = (const __half*)a.d; p.R = a.R; p.K = a.K;
+    const int grid = std::max(1, std::min(a.R, dev_info().sm_count));
+    p.rows_base = a.R / grid; p.rows_extra = a.R % grid;
+    p.T = std::min(kConsQ, ((ceil_div(a.K / 16, rc) + 31) / 32) * 32);
+    p.P = std::max(1, kConsQ / p.T);
+    const size_t row_bytes = (size_t)a.K + (size_t)a.K / 16;
+    p.stage_bytes = (int)((((size_t)p.P * rps * row_bytes) + 127) / 128 * 128);
+    p.ns = std::max(2, std::min(16, kRingQ / p.stage_bytes));
+    p.ring_bytes = p.ns * p.stage_bytes;
+    p.pro = a.pro; p.x = (const float*)a.x; p.xq = a.xq; p.xd = (const __half*)a.xd;
+    if (a.act == 1 && a.xq != nullptr) p.pro = PRO_Q8_GIVEN;
+    p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps; p.epi = a.epi; p.y = a.y;
+    p.err = L.err; p.trig_late = L.trig_late;
+    size_t smem = (size_t)p.ring_bytes + 32 * 8 + (size_t)kPhaseQ * (p.T / 32) * 4;
+    smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
+    if ((size_t)p.ns * p.stage_bytes <= (size_t)kRingQ * 2) {
+      switch (rc) {
+        case 1: return a.act == 1 ? launch_ring_q<1, 1>(p, grid, smem, L) : launch_ring_q<1, 0>(p, grid, smem, L);
+        case 2: return a.act == 1 ? launch_ring_q<2, 1>(p, grid, smem, L) : launch_ring_q<2, 0>(p, grid, smem, L);
+        case 3: return a.act == 1 ? launch_ring_q<3, 1>(p, grid, smem, L) : launch_ring_q<3, 0>(p, grid, smem, L);
+        default: return a.act == 1 ? launch_ring_q<4, 1>(p, grid, smem, L) : launch_ring_q<4, 0>(p, grid, smem, L);
+      }
+    }
+  }
   const int C = pick_c(a.K);
   const int KC = a.K / 16;
   const int T = std::min(kThreads, ((ceil_div(KC, C) + 31) / 32) * 32);
