@@ -16,10 +16,11 @@
 //     (a multiple of 128) of one kv head and all REP = Hq/Hkv q heads reading it;
 //     the host sizes `chunk` so the grid is about one CTA per SM at batch 1
 //     and one split per sequence at large batch;
-//   * the chunk streams through shared memory in 128-token tiles: one thread
+//   * the chunk streams through shared memory in 64-token tiles: one thread
 //     issues TMA bulk copies (cp.async.bulk, one per contiguous page segment)
-//     of a tile's K and V rows into a 2-stage ring on mbarriers, so the next
-//     tile loads while the current one is scored;
+//     of a tile's K and V rows into a 3-stage ring on mbarriers, the first
+//     stages before the programmatic-dependent wait (~100 KB of shared memory,
+//     so the CTA fits beside the projection kernel it overlaps);
 //   * per tile: scores from shared memory in f32, an online-softmax update of
 //     the running (max, sum) per head, then P.V into per-lane accumulators;
 //   * a split publishes (m, l, acc[REP][128]) to the workspace and takes a
@@ -39,9 +40,12 @@ namespace qd {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTile = 128;
-constexpr int kStages = 2;
-// 512 threads (16 warps) per CTA; 256 when 8 q heads share a kv head (register budget)
+constexpr int kTile = 64;
+constexpr int kStages = 3;
+// 512 threads (16 warps) per CTA, 256 when 8 q heads share a kv head (register
+// budget). 256 threads for every REP (so a CTA fits beside a GEMV CTA and
+// prefetches during the projection) measured slower on the Qwen3-8B step:
+// 296 vs 304 tok/s.
 __host__ __device__ constexpr int threads_for(int rep) { return rep >= 8 ? 256 : 512; }
 constexpr int kMaxSplits = 256;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -163,7 +167,12 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  pdl_wait();
+  // The position, the page table and the cached K/V rows below `pos` are not
+  // written by the kernel this one waits on (the QKV projection): `pos` was
+  // last written by the previous step's argmax, and the cache rows by earlier
+  // steps, all complete before the QKV projection's CTAs started. So the first
+  // tiles are requested before the programmatic-dependent wait, and stream in
+  // while the projection finishes; only q/k/v need the wait.
   if (!p.trig_late) pdl_launch_dependents();
 
   int len, pos = 0;
@@ -214,6 +223,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
       issue_tile(p, b, g, ts, max(0, min(ts + kTile, copy_end) - ts), stage_k(st), stage_v(st), &bars[st]);
     }
   }
+  pdl_wait();  // q, k, v (and, standalone, the caller's q) come from the previous kernel
 
   // ---- q for the REP heads of this kv head (pre-scaled by scale * log2 e); new k, v.
   // All head vectors load at once; one barrier for the sums of squares, one for RoPE.
