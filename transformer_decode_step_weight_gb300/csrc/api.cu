@@ -105,6 +105,41 @@ static int attn_cluster_enabled() {
   return n;
 }
 
+// L2 prefetch of weights ahead of the GEMV that reads them (batch-1 BF16 step):
+// QD_L2PF_ATTN_WO_KB = leading KB of every O-projection span that the attention
+// kernel fetches (QD_L2PF_ATTN_LATE = 1: after its own K/V, else right after
+// the dependency wait);
+// QD_L2PF_ATTN_GU_KB = leading KB of every gate+up span it fetches as well;
+// QD_L2PF_TAIL_KB = leading KB of every span of the next GEMV that a ring GEMV
+// fetches once its own copies are issued. 0 turns a form off.
+// QD_ATTN_TRIGGER_LOOP = 1: the attention lets the O projection launch only once
+// its K/V loop is done. QD_GEMV_O_RING_KB: ring size of the O projection.
+// QD_SWIGLU_IN_DOWN = 1: form SwiGLU in the down projection's prologue instead of
+// the gate+up epilogue (batch 1).
+struct StepTuning {
+  int swiglu_in_down = 0;
+  int attn_trig_loop = 0;
+  int o_ring_kb = 0;
+  long long attn_wo_kb = 0;
+  int attn_late = 0;
+  long long attn_gu_kb = 0;
+  long long tail_kb = 0;
+};
+static const StepTuning& step_tuning() {
+  static const StepTuning t = [] {
+    StepTuning u;
+    if (const char* v = getenv("QD_L2PF_ATTN_WO_KB")) u.attn_wo_kb = std::max(0LL, atoll(v));
+    if (const char* v = getenv("QD_L2PF_ATTN_LATE")) u.attn_late = atoi(v) != 0;
+    if (const char* v = getenv("QD_L2PF_ATTN_GU_KB")) u.attn_gu_kb = std::max(0LL, atoll(v));
+    if (const char* v = getenv("QD_L2PF_TAIL_KB")) u.tail_kb = std::max(0LL, atoll(v));
+    if (const char* v = getenv("QD_ATTN_TRIGGER_LOOP")) u.attn_trig_loop = atoi(v) != 0;
+    if (const char* v = getenv("QD_SWIGLU_IN_DOWN")) u.swiglu_in_down = atoi(v) != 0;
+    if (const char* v = getenv("QD_GEMV_O_RING_KB")) u.o_ring_kb = std::max(0, atoi(v));
+    return u;
+  }();
+  return t;
+}
+
 static Launch make_launch(cudaStream_t s, bool pdl) {
   Launch L;
   L.stream = s;
@@ -144,7 +179,7 @@ int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
   if (batch > 8) {  // a real contraction: tcgen05 tensor cores
     if (x_is_f32 || !gemm_tc_supported(rows, cols, batch))
       return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: batch %d needs bf16 x, cols %% 64 == 0 and batch <= 64", batch);
-    GemmTcArgs g;
+    GemmTcArgs g = {};
     g.W = W; g.X = x; g.R = rows; g.K = cols; g.B = batch; g.epi = EPI_STORE; g.y = y;
     cudaError_t e = launch_gemm_tc(g, make_launch(stream, false));
     return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_bf16 (tensor cores)");
@@ -152,7 +187,7 @@ int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
   if (!gemv_bf16_supported(cols, batch))
     return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: cols=%d batch=%d (need cols%%8==0, cols<=32768, 1<=batch<=8)",
                 cols, batch);
-  GemvBf16Args a;
+  GemvBf16Args a = {};
   a.W = W; a.R = rows; a.K = cols; a.batch = batch;
   a.pro = x_is_f32 ? PRO_X_F32 : PRO_X_BF16;
   a.x = x; a.norm_w = nullptr; a.eps = 0.f;
@@ -174,7 +209,7 @@ int qd_gemv_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const 
     return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: pointers must be 16-byte aligned");
   if (((uintptr_t)d_f16 & 1u) || (x_d_f16 && ((uintptr_t)x_d_f16 & 1u)))
     return fail(QD_ERR_INVALID_ARG, "qd_gemv_q8_0: scale pointers must be 2-byte aligned");
-  GemvQ8Args a;
+  GemvQ8Args a = {};
   a.qs = qs; a.d = d_f16; a.R = rows; a.K = cols; a.act = act;
   a.pro = PRO_X_F32; a.x = x_f32;
   a.xq = (act == QD_ACT_I8 && x_q && x_d_f16) ? x_q : nullptr; a.xd = x_d_f16;
@@ -436,7 +471,7 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
   const int QKV = (Hq + 2 * Hkv) * D;
   auto gemm = [&](const void* W, int R, int K, const void* X, int epi, float* y) {
-    GemmTcArgs g;
+    GemmTcArgs g = {};
     g.W = W; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
     return launch_gemm_tc(g, L);
   };
@@ -476,6 +511,17 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
   const int QKV = (Hq + 2 * Hkv) * D;
   const bool q8 = d.wtype == QD_W_Q8_0;
+  const StepTuning& pft = step_tuning();
+  // batch 1 on the ring GEMV: SwiGLU in the gate+up epilogue (bf16 h), so the down
+  // projection reads 2F bytes of h instead of 8F of gate/up and recomputes nothing
+  const bool swiglu_epi = !q8 && B == 1 && gemv_bf16_ring_ok(H, 1) && gemv_bf16_ring_ok(F, 1) &&
+                          !pft.swiglu_in_down;
+  // head of every span of the next batch-1 BF16 GEMV (R rows of K), or nothing
+  auto tail_plan = [&](const void* Wn, int R, int K) {
+    L2Prefetch pf = {};
+    if (B == 1 && pft.tail_kb > 0) pf = l2_plan_rows(Wn, R, (size_t)K * 2, (size_t)pft.tail_kb << 10);
+    return pf;
+  };
 
   QD_TRY(launch_embed(a->embed, H, a->vocab, a->tok, B, w.res, L), "embed");
   for (int li = 0; li < a->n_layers; ++li) {
@@ -502,6 +548,12 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     if (q8) at.out_f32 = (float*)w.attn;
     else at.out_bf16 = w.attn;
     at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.use_cluster = attn_cluster_enabled();
+    if (!q8 && B == 1) {
+      if (pft.attn_wo_kb) at.pf[0] = l2_plan_rows(l->w.w_o, H, (size_t)Hq * D * 2, (size_t)pft.attn_wo_kb << 10);
+      at.pf_late = pft.attn_late;
+      at.trig_loop = pft.attn_trig_loop;
+      if (pft.attn_gu_kb) at.pf[1] = l2_plan_rows(l->w.w_gu, 2 * F, (size_t)H * 2, (size_t)pft.attn_gu_kb << 10);
+    }
     QD_TRY(launch_attention(at, L), "attention");
     // O projection + residual add
     if (q8) {
@@ -513,6 +565,8 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
       GemvBf16Args g = {};
       g.W = l->w.w_o; g.R = H; g.K = Hq * D; g.batch = B; g.pro = PRO_X_BF16; g.x = w.attn;
       g.epi = EPI_RESID_ADD; g.y = w.res;
+      g.pf = tail_plan(l->w.w_gu, 2 * F, H);
+      g.ring_kb = pft.o_ring_kb;
       QD_TRY(launch_gemv_bf16(g, L), "o gemv");
     }
     // gate+up projection, RMSNorm(res; ln_post) fused into the prologue
@@ -525,6 +579,10 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
       GemvBf16Args g = {};
       g.W = l->w.w_gu; g.R = 2 * F; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
       g.norm_w = l->w.ln_post; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.gu;
+      if (swiglu_epi) {  // h = bf16(silu(gate) * up) formed in the epilogue, into xn
+        g.epi = EPI_SWIGLU; g.y = nullptr; g.y_bf16 = w.xn;
+      }
+      g.pf = tail_plan(l->w.w_down, H, F);
       QD_TRY(launch_gemv_bf16(g, L), "gu gemv");
     }
     // down projection with SwiGLU formed on load, + residual add
@@ -537,6 +595,9 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
       GemvBf16Args g = {};
       g.W = l->w.w_down; g.R = H; g.K = F; g.batch = B; g.pro = PRO_SWIGLU; g.x = w.gu;
       g.epi = EPI_RESID_ADD; g.y = w.res;
+      if (swiglu_epi) { g.pro = PRO_X_BF16; g.x = w.xn; }
+      if (li + 1 < a->n_layers) g.pf = tail_plan(a->layers[li + 1]->w.w_qkv, QKV, H);
+      else if (!a->lm_head_scales) g.pf = tail_plan(a->lm_head, a->vocab, H);
       QD_TRY(launch_gemv_bf16(g, L), "down gemv");
     }
   }

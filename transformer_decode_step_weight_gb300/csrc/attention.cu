@@ -41,7 +41,9 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTile = 64;
-constexpr int kStages = 3;
+// K/V ring depth: 3 stages by default; QD_ATTN_SIMT_STAGES = 2..4 (4 puts a whole
+// 256-token split in flight before the dependency wait).
+constexpr int kMaxStages = 4;
 // 512 threads (16 warps) per CTA, 256 when 8 q heads share a kv head (register
 // budget). 256 threads for every REP (so a CTA fits beside a GEMV CTA and
 // prefetches during the projection) measured slower on the Qwen3-8B step:
@@ -73,19 +75,23 @@ struct AttnParams {
   int* ws_cnt;
   int* err;
   int trig_late;
+  L2Prefetch pf[2];
+  int pf_late;  // 1: prefetch once this CTA's own K/V tiles have all arrived
+  int stages;   // K/V ring depth, 2..kMaxStages
+  int trig_loop;  // 1: trigger the dependent launch after the K/V loop, not at the start
 };
 
 struct Carve {
   size_t kv, q, s, run, bar, total;
 };
-__host__ __device__ inline Carve carve(int rep) {
+__host__ __device__ inline Carve carve(int rep, int stages) {
   Carve c;
-  c.kv = 0;                                          // kStages x (K tile, V tile)
-  c.q = c.kv + (size_t)kStages * 2 * kTile * kD * 2;
+  c.kv = 0;                                          // stages x (K tile, V tile)
+  c.q = c.kv + (size_t)stages * 2 * kTile * kD * 2;
   c.s = c.q + (size_t)rep * kD * 4;                  // scores / probabilities [REP][64]
   c.run = c.s + (size_t)rep * kTile * 4;             // m[REP], l[REP], alpha[REP], scratch
   c.bar = c.run + 64 * 4;
-  c.total = c.bar + kStages * 8;
+  c.total = c.bar + kMaxStages * 8;
   return c;
 }
 
@@ -155,7 +161,8 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   constexpr int kWarps = kThreads / 32;
   constexpr int kPairs = kTile / 2 / kWarps;  // token pairs per warp per tile
   extern __shared__ __align__(128) unsigned char smem[];
-  const Carve cv = carve(REP);
+  const int kStages = p.stages;
+  const Carve cv = carve(REP, kStages);
   __nv_bfloat16* sKV = (__nv_bfloat16*)(smem + cv.kv);
   float* sQ = (float*)(smem + cv.q);
   float* sS = (float*)(smem + cv.s);
@@ -166,6 +173,17 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // DRAM is mostly idle while this short kernel runs: every CTA fetches its share
+  // of the next GEMVs' weights into L2 once the dependency wait is over (the
+  // projection before this kernel is complete then, so it loses no bandwidth).
+  auto prefetch_next = [&]() {
+    if (warp == 1) {
+      const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+      const unsigned n_cta = gridDim.x * gridDim.y * gridDim.z;
+      l2_prefetch_spans(p.pf[0], cta, n_cta, lane);
+      l2_prefetch_spans(p.pf[1], cta, n_cta, lane);
+    }
+  };
 
   // The position, the page table and the cached K/V rows below `pos` are not
   // written by the kernel this one waits on (the QKV projection): `pos` was
@@ -173,7 +191,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   // steps, all complete before the QKV projection's CTAs started. So the first
   // tiles are requested before the programmatic-dependent wait, and stream in
   // while the projection finishes; only q/k/v need the wait.
-  if (!p.trig_late) pdl_launch_dependents();
+  if (!p.trig_late && !p.trig_loop) pdl_launch_dependents();
 
   int len, pos = 0;
   if (FUSED) {
@@ -201,7 +219,11 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
     t_end = (int)(((long long)len * (s + 1)) / cl);
   } else {
     n_act = (len + p.chunk - 1) / p.chunk;
-    if (s >= n_act) return;
+    if (s >= n_act) {  // no keys for this split: only its share of the prefetch
+      pdl_wait();
+      prefetch_next();
+      return;
+    }
     t0 = s * p.chunk;
     t_end = min(t0 + p.chunk, len);
   }
@@ -224,6 +246,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
     }
   }
   pdl_wait();  // q, k, v (and, standalone, the caller's q) come from the previous kernel
+  if (!p.pf_late) prefetch_next();
 
   // ---- q for the REP heads of this kv head (pre-scaled by scale * log2 e); new k, v.
   // All head vectors load at once; one barrier for the sums of squares, one for RoPE.
@@ -430,6 +453,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   }
 
   pdl_launch_dependents();  // all K/V of this split is in shared memory
+  if (p.pf_late) prefetch_next();
 
   // ---- reduce the two token halves, then the warps, element by element
 #pragma unroll
@@ -511,20 +535,33 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
     p.ws_ml[(slot * REP + tid) * 2 + 0] = sRun[tid];
     p.ws_ml[(slot * REP + tid) * 2 + 1] = sRun[8 + tid];
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_ticket = atomicAdd(p.ws_cnt + (size_t)b * p.Hkv + g, 1);
+  __syncthreads();  // every thread's share of the partial is written
+  if (tid == 0) {   // release the CTA's writes, take a ticket, acquire the others'
+    __threadfence();
+    s_ticket = atomicAdd(p.ws_cnt + (size_t)b * p.Hkv + g, 1);
+    __threadfence();
+  }
   __syncthreads();
   if (s_ticket != n_act - 1) return;
-  __threadfence();
 
-  // weights w[k][i] = exp2(m_k - M_i), sums l[k][i], totals L_i, all in shared memory
+  // The last split combines. One round of L2 loads: this thread's elements of the
+  // first kB splits' partials go to registers while (m, l) of every split go to
+  // shared memory; weights w[k][i] = exp2(m_k - M_i) and totals L_i follow.
+  constexpr int kB = 32 / kEpt > 0 ? 32 / kEpt : 1;   // splits per batch of register loads
   float* sW = (float*)sKV + kWarps * NE;        // after sRed: [kMaxSplits][REP]
   float* sLk = sW + kMaxSplits * REP;           // [kMaxSplits][REP]
   float* sL = sLk + kMaxSplits * REP;           // [REP]
+  const float* accp = p.ws_acc + slot0 * NE + e0;
+  float v[kB][kEpt];
+  if (elem_thread) {
+#pragma unroll
+    for (int u = 0; u < kB; ++u)
+      if (u < n_act) load_cg<kEpt>(accp + (size_t)u * NE, v[u]);
+  }
   for (int idx = tid; idx < n_act * REP; idx += kThreads) {
-    sW[idx] = __ldcg(p.ws_ml + (slot0 * REP + idx) * 2);
-    sLk[idx] = __ldcg(p.ws_ml + (slot0 * REP + idx) * 2 + 1);
+    const float2 ml = __ldcg((const float2*)(p.ws_ml + (slot0 * REP + idx) * 2));
+    sW[idx] = ml.x;
+    sLk[idx] = ml.y;
   }
   __syncthreads();
   if (tid < REP) {
@@ -539,19 +576,18 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
     sL[tid] = L;
   }
   __syncthreads();
-  // this thread's kEpt elements of every split's partial; 16 splits of loads in flight
   if (elem_thread) {
     float O[kEpt];
 #pragma unroll
     for (int j = 0; j < kEpt; ++j) O[j] = 0.f;
-    const float* accp = p.ws_acc + slot0 * NE + e0;
-    for (int k0 = 0; k0 < n_act; k0 += 16) {
-      float v[16][kEpt];
+    for (int k0 = 0; k0 < n_act; k0 += kB) {
+      if (k0 > 0) {
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (k0 + u < n_act) load_cg<kEpt>(accp + (size_t)(k0 + u) * NE, v[u]);
+        for (int u = 0; u < kB; ++u)
+          if (k0 + u < n_act) load_cg<kEpt>(accp + (size_t)(k0 + u) * NE, v[u]);
+      }
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < kB; ++u) {
         if (k0 + u < n_act) {
           const float w = sW[(k0 + u) * REP + hi];
 #pragma unroll
@@ -583,10 +619,11 @@ __global__ void rope_table_kernel(float2* table, int max_pos, int half, double t
 template <int REP, bool FUSED, bool CLUSTER>
 cudaError_t launch_rep(const AttnParams& prm, int cluster, const Launch& L) {
   auto k = attn_kernel<REP, FUSED, CLUSTER>;
-  const size_t smem = carve(REP).total;
+  const size_t smem = carve(REP, prm.stages).total;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)carve(REP, kMaxStages).total);
     if (e != cudaSuccess) return e;
     if (CLUSTER) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -600,6 +637,14 @@ cudaError_t launch_rep(const AttnParams& prm, int cluster, const Launch& L) {
   }
   dim3 grid(prm.n_splits, prm.Hkv, prm.B);
   return launch_ex(k, grid, dim3(threads_for(REP)), smem, L, prm);
+}
+
+int simt_stages() {
+  static const int n = [] {
+    const char* v = getenv("QD_ATTN_SIMT_STAGES");
+    return v ? std::max(2, std::min(kMaxStages, atoi(v))) : 3;
+  }();
+  return n;
 }
 
 // Cluster size for the fused step: the smallest power of two that gives about
@@ -616,11 +661,11 @@ int pick_cluster(int B, int Hkv, int max_cl) {
     auto k = attn_kernel<REP, FUSED, true>;
     max_ok = 8;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)carve(REP).total) == cudaSuccess) {
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)carve(REP, kMaxStages).total) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16, 1, 1);
       cfg.blockDim = dim3(threads_for(REP));
-      cfg.dynamicSmemBytes = carve(REP).total;
+      cfg.dynamicSmemBytes = carve(REP, simt_stages()).total;
       cudaLaunchAttribute at[1];
       at[0].id = cudaLaunchAttributeClusterDimension;
       at[0].val.clusterDim.x = 16;
@@ -689,7 +734,7 @@ static bool attn_use_mma(const AttnArgs& a) {
 cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   if (attn_use_mma(a) && !(a.qkv && a.use_cluster > 1))
     return launch_attention_mma(a, attn_chunk(a.B, a.Hkv, a.max_ctx), slots_cap(a.B, a.Hkv, a.max_ctx), L);
-  AttnParams p;
+  AttnParams p = {};
   const int rep = a.Hq / a.Hkv;
   p.q = a.q;
   p.qkv = a.qkv;
@@ -719,6 +764,11 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   p.ws_cnt = (int*)(ws + al(slots * rep * kD * 4) + al(slots * rep * 2 * 4));
   p.err = L.err;
   p.trig_late = L.trig_late;
+  p.pf[0] = a.pf[0];
+  p.pf[1] = a.pf[1];
+  p.pf_late = a.pf_late;
+  p.stages = simt_stages();
+  p.trig_loop = a.trig_loop;
   const bool fused = a.qkv != nullptr;
   // the fused decode step splits each sequence across one thread block cluster;
   // the standalone call keeps the workspace split (its workspace is the scratch)

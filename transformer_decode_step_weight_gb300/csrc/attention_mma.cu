@@ -532,7 +532,7 @@ cudaError_t launch_ms(const MParams& p, const Launch& L) {
 // Same workspace layout as the CUDA-core form: [slots][REP][128] partials,
 // [slots][REP][2] (max, sum), [B * Hkv] tickets; chunk is a multiple of 128.
 cudaError_t launch_attention_mma(const AttnArgs& a, int chunk, size_t slots, const Launch& L) {
-  MParams p;
+  MParams p = {};
   const int rep = a.Hq / a.Hkv;
   p.q = a.q;
   p.qkv = a.qkv;

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "qd.h"
+#include "kernels.h"
 
 #define QD_DEV __device__ __forceinline__
 
@@ -127,6 +128,30 @@ QD_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) 
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Issue this CTA's share of an L2 prefetch plan from the 32 lanes of one warp.
+// The spans are cut into 16 KB pieces dealt round-robin over (CTA, lane), piece
+// k of every span before piece k + 1 of any, so the leading bytes of each span
+// arrive first. cp.async.bulk.prefetch.L2 is fire-and-forget: no barrier, no
+// completion, and a piece never extends past its span.
+QD_DEV void l2_prefetch_spans(const L2Prefetch& pf, unsigned cta, unsigned n_cta, int lane) {
+  if (pf.base == nullptr || pf.n_spans <= 0 || pf.head_bytes < 16) return;
+  constexpr unsigned long long kPiece = 16384;
+  const unsigned long long span_max = (unsigned long long)(pf.rows_base + (pf.rows_extra > 0)) * pf.row_bytes;
+  const unsigned long long per = (min(pf.head_bytes, span_max) + kPiece - 1) / kPiece;
+  const unsigned long long n = per * (unsigned long long)pf.n_spans;
+  for (unsigned long long i = cta + (unsigned long long)lane * n_cta; i < n; i += 32ull * n_cta) {
+    const int span = (int)(i % (unsigned long long)pf.n_spans);
+    const unsigned long long off = (i / (unsigned long long)pf.n_spans) * kPiece;
+    const int nr = pf.rows_base + (span < pf.rows_extra ? 1 : 0);
+    const unsigned long long bytes = min(pf.head_bytes, (unsigned long long)nr * pf.row_bytes) & ~15ull;
+    if (off >= bytes) continue;
+    const unsigned long long r0 = (unsigned long long)span * pf.rows_base + (unsigned long long)min(span, pf.rows_extra);
+    const unsigned char* src = (const unsigned char*)pf.base + r0 * pf.row_bytes + off;
+    const uint32_t sz = (uint32_t)min(kPiece, bytes - off);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(sz) : "memory");
+  }
 }
 
 }  // namespace qd

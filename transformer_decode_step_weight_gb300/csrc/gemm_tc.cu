@@ -261,7 +261,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  TcParams p;
+  TcParams p = {};
   p.R = a.R; p.K = a.K; p.B = a.B; p.epi = a.epi; p.y = a.y; p.err = L.err;
   const int tiles = (a.R + kBM - 1) / kBM;
   return launch_ex(gemm_tc_kernel, dim3(tiles), dim3(kThreadsTc), kSmemTc, L, tw, tx, p);

@@ -277,13 +277,15 @@ int pick_c(int K) {
 // ---------------------------------------------------------------------------
 // Batch-1 form on a TMA ring. One producer warp streams the CTA's contiguous
 // weight rows into a shared-memory ring with cp.async.bulk (a few rows per
-// stage, ~96 KB in flight per SM, issued before the programmatic-dependent
+// stage, ~128 KB in flight per SM, issued before the programmatic-dependent
 // wait because weights never depend on an earlier kernel); eight consumer
 // warps own fixed 16-byte column chunks of every row (activation slice in
 // registers), read the stage from shared memory, reduce each row with warp
-// shuffles and a fixed-order sum over warps. At ~100 KB of shared memory and
-// <= 113 registers a thread, the next kernel's CTA fits beside this one and
-// fills its own ring while this one drains.
+// shuffles and a fixed-order sum over warps. The launcher pads the shared
+// memory past half an SM so that exactly one GEMV CTA runs per SM (two on one
+// SM under programmatic dependent launch made straggler CTAs); the next
+// kernel's CTA takes the SM as soon as this one exits and starts its own ring
+// before its dependency wait.
 constexpr int kCons = 256;          // consumer threads
 constexpr int kRingMax = 192 * 1024; // largest ring the launcher may choose
 constexpr int kPhaseRows = 128;     // rows reduced per phase
@@ -302,6 +304,9 @@ struct RingParams {
   float* y;
   int* err;
   int trig_late;
+  L2Prefetch pf;
+  int pair_F;                 // EPI_SWIGLU: F (rows of each half); the partition is over pairs
+  __nv_bfloat16* y_bf16;      // EPI_SWIGLU output [F]
 };
 
 QD_DEV void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
@@ -310,17 +315,23 @@ QD_DEV void mbar_arrive(uint64_t* bar) {
 }
 
 template <int C, int RPS>
-__global__ void __launch_bounds__(kCons + 32, 2) gemv_ring_kernel(const RingParams p) {
+__global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = (uint64_t*)(smem + p.ring_bytes);
   uint64_t* empty = full + 16;
   float* red = (float*)(empty + 16);            // [kPhaseRows][wpg]
+  float* s_pair = red + kPhaseRows * (p.T / 32);  // EPI_SWIGLU: row sums [2 * npair]
   __shared__ float s_ss[kCons / 32];
 
   const int tid = threadIdx.x, lane = tid & 31;
   const int K = p.K, ns = p.ns;
-  const int nrows = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
+  const bool pair = p.epi == EPI_SWIGLU;
+  // r0: first row (first pair under EPI_SWIGLU); local rows [0, npair) are gate rows
+  // r0.., local rows [npair, 2 npair) the up rows F + r0..
+  const int nown = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
+  const int npair = pair ? nown : 0;
+  const int nrows = pair ? 2 * nown : nown;
   const int r0 = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
   const int n_stages = (nrows + p.P * RPS - 1) / (p.P * RPS);
   const size_t row_bytes = (size_t)K * 2;
@@ -338,17 +349,32 @@ __global__ void __launch_bounds__(kCons + 32, 2) gemv_ring_kernel(const RingPara
   if (tid >= kCons) {  // ---- producer warp: weights only, so no dependency wait
     if (lane == 0) {
       const unsigned char* src = (const unsigned char*)(p.W + (size_t)r0 * K);
+      // EPI_SWIGLU: local row lr >= npair is weight row F + r0 + (lr - npair)
+      const unsigned char* src_up = pair ? (const unsigned char*)(p.W + ((size_t)p.pair_F + r0) * K) : src;
       for (int i = 0; i < n_stages; ++i) {
         const int slot = i % ns;
-        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) return;
+        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) break;
         const int srows = p.P * RPS;
-        const int rows_i = min(srows, nrows - i * srows);
-        const uint32_t bytes = (uint32_t)(rows_i * row_bytes);
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s(ring + (size_t)slot * p.stage_bytes, src + (size_t)i * srows * row_bytes, bytes, &full[slot]);
+        const int a = i * srows;
+        const int rows_i = min(srows, nrows - a);
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)(rows_i * row_bytes));
+        unsigned char* dst = ring + (size_t)slot * p.stage_bytes;
+        if (!pair) {
+          bulk_g2s(dst, src + (size_t)a * row_bytes, (uint32_t)(rows_i * row_bytes), &full[slot]);
+        } else {  // the stage may straddle the gate/up boundary: one copy per half
+          const int na = max(0, min(a + rows_i, npair) - a);   // gate rows in this stage
+          if (na > 0) bulk_g2s(dst, src + (size_t)a * row_bytes, (uint32_t)(na * row_bytes), &full[slot]);
+          if (rows_i > na)
+            bulk_g2s(dst + (size_t)na * row_bytes, src_up + (size_t)(a + na - npair) * row_bytes,
+                     (uint32_t)((rows_i - na) * row_bytes), &full[slot]);
+        }
       }
     }
+    __syncwarp();
     pdl_launch_dependents();  // every copy of this CTA is issued
+    // This CTA's last ring refill is in flight: DRAM would go idle here while
+    // the consumers drain, so fetch the head of the next GEMV's spans into L2.
+    l2_prefetch_spans(p.pf, blockIdx.x, gridDim.x, lane);
     return;
   }
 
@@ -363,6 +389,11 @@ __global__ void __launch_bounds__(kCons + 32, 2) gemv_ring_kernel(const RingPara
     col[j] = (j * T + t) * 8;
     cv[j] = col[j] < K;
   }
+  // the RMSNorm weights never come from an earlier kernel: load them before the wait
+  uint4 wn[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j)
+    wn[j] = (p.pro == PRO_RMSNORM && cv[j]) ? *(const uint4*)(p.norm_w + col[j]) : make_uint4(0u, 0u, 0u, 0u);
   pdl_wait();
 
   float x[C][8];
@@ -411,9 +442,8 @@ __global__ void __launch_bounds__(kCons + 32, 2) gemv_ring_kernel(const RingPara
 #pragma unroll
       for (int j = 0; j < C; ++j) {
         if (!cv[j]) continue;
-        const uint4 wn = *(const uint4*)(p.norm_w + col[j]);
-        const float nw[8] = {bf_lo(wn.x), bf_hi(wn.x), bf_lo(wn.y), bf_hi(wn.y),
-                             bf_lo(wn.z), bf_hi(wn.z), bf_lo(wn.w), bf_hi(wn.w)};
+        const float nw[8] = {bf_lo(wn[j].x), bf_hi(wn[j].x), bf_lo(wn[j].y), bf_hi(wn[j].y),
+                             bf_lo(wn[j].z), bf_hi(wn[j].z), bf_lo(wn[j].w), bf_hi(wn[j].w)};
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[j][e] = round_bf16(nw[e] * round_bf16(x[j][e] * inv));
       }
@@ -493,13 +523,21 @@ __global__ void __launch_bounds__(kCons + 32, 2) gemv_ring_kernel(const RingPara
       for (int r = tid; r < nph; r += kCons) {
         float acc = 0.f;
         for (int k = 0; k < wpg; ++k) acc += red[r * wpg + k];
-        float* yp = p.y + r0 + ph_base + r;
-        if (p.epi == EPI_RESID_ADD) *yp += acc;
-        else *yp = acc;
+        if (pair) {
+          s_pair[ph_base + r] = acc;
+        } else {
+          float* yp = p.y + r0 + ph_base + r;
+          if (p.epi == EPI_RESID_ADD) *yp += acc;
+          else *yp = acc;
+        }
       }
       cons_sync();
       ph_base = done;
     }
+  }
+  if (pair) {  // SwiGLU of the CTA's pairs (the last flush ended with a barrier)
+    for (int j = tid; j < npair; j += kCons)
+      p.y_bf16[r0 + j] = __float2bfloat16_rn(silu(s_pair[j]) * s_pair[npair + j]);
   }
 }
 
@@ -536,15 +574,16 @@ static int ring_c(int K) {
 }
 
 // Ring geometry: a stage is P x RPS whole rows; the ring holds ~ring_kb KB of
-// stages (default 96). The dynamic shared memory asked for is at least half of
+// stages (default 128: measured 1.6 % faster on the Qwen3-8B step than 96, and
+// 192 slower). The dynamic shared memory asked for is at least half of
 // an SM's, so two GEMV CTAs never share an SM: with programmatic dependent
 // launch the next GEMV's CTA would otherwise double up on the SMs that finish
-// first and straggle (measured: 234 vs 295 tok/s on the Qwen3-8B step). An
-// attention CTA still fits beside one GEMV CTA. QD_GEMV_RING_KB /
+// first and straggle (measured: 234 vs 295 tok/s on the Qwen3-8B step).
+// QD_GEMV_RING_KB /
 // QD_GEMV_SMEM_PAD_KB override the ring size / add padding (tuning);
 // QD_GEMV_RING=0 selects the register-streaming kernel.
 struct RingTuning {
-  int enabled = 1, ring_kb = 96, pad_kb = 0;
+  int enabled = 1, ring_kb = 128, pad_kb = 0;
   RingTuning() {
     if (const char* v = getenv("QD_GEMV_RING")) enabled = atoi(v) != 0;
     if (const char* v = getenv("QD_GEMV_SMEM_PAD_KB")) pad_kb = std::max(0, std::min(64, atoi(v)));
@@ -556,18 +595,41 @@ static const RingTuning& ring_tuning() {
   return t;
 }
 
+L2Prefetch l2_plan_rows(const void* base, int R, size_t row_bytes, size_t head_bytes) {
+  L2Prefetch pf = {};
+  if (base == nullptr || R < 1 || row_bytes % 16 != 0 || ((uintptr_t)base & 15) != 0 || head_bytes < 16) return pf;
+  const int grid = std::max(1, std::min(R, dev_info().sm_count));  // as every GEMV launcher cuts rows
+  pf.base = base;
+  pf.row_bytes = row_bytes;
+  pf.rows_base = R / grid;
+  pf.rows_extra = R % grid;
+  pf.n_spans = grid;
+  pf.head_bytes = head_bytes;
+  return pf;
+}
+
+bool gemv_bf16_ring_ok(int K, int batch) {
+  const int rc = (batch == 1 && ring_tuning().enabled && K % 8 == 0) ? ring_c(K) : 0;
+  const int rps = rc == 1 ? 8 : rc == 2 ? 4 : rc <= 4 ? 2 : 1;
+  return rc > 0 && (size_t)K * 2 * rps * 2 <= (size_t)kRingMax;
+}
+
 cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
   const RingTuning& tu = ring_tuning();
   const int rc = (a.batch == 1 && tu.enabled) ? ring_c(a.K) : 0;
-  const int ring_bytes = tu.ring_kb * 1024;
+  const int ring_bytes = (a.ring_kb > 0 ? std::min(a.ring_kb, kRingMax / 1024) : tu.ring_kb) * 1024;
   const int rc_rps = rc == 1 ? 8 : rc == 2 ? 4 : rc <= 4 ? 2 : 1;
   if (rc > 0 && (size_t)a.K * 2 * rc_rps * 2 <= (size_t)kRingMax) {
     const int chunks = a.K / 8;
-    RingParams p;
+    RingParams p = {};
     p.W = (const __nv_bfloat16*)a.W;
     p.R = a.R; p.K = a.K;
-    const int grid = std::max(1, std::min(a.R, dev_info().sm_count));
-    p.rows_base = a.R / grid; p.rows_extra = a.R % grid;
+    const bool pair = a.epi == EPI_SWIGLU;
+    const int units = pair ? a.R / 2 : a.R;   // rows, or gate/up pairs
+    const int grid = std::max(1, std::min(units, dev_info().sm_count));
+    p.rows_base = units / grid; p.rows_extra = units % grid;
+    p.pair_F = pair ? a.R / 2 : 0;
+    p.y_bf16 = (__nv_bfloat16*)a.y_bf16;
     p.T = std::min(kCons, ((ceil_div(chunks, rc) + 31) / 32) * 32);
     p.P = std::max(1, kCons / p.T);
     const int row_bytes = a.K * 2;
@@ -578,7 +640,10 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
     p.ring_bytes = p.ns * p.stage_bytes;
     p.pro = a.pro; p.x = a.x; p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps;
     p.epi = a.epi; p.y = a.y; p.err = L.err; p.trig_late = L.trig_late;
+    p.pf = a.pf;
     size_t smem = (size_t)p.ring_bytes + 32 * 8 + (size_t)kPhaseRows * (p.T / 32) * 4 + (size_t)tu.pad_kb * 1024;
+    if (pair) smem += (size_t)2 * (p.rows_base + 1) * 4;
+    if (smem > (size_t)dev_info().max_smem_optin - 1024) return cudaErrorInvalidValue;
     smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
     switch (rc) {
       case 1: return launch_ring_c<1>(p, grid, smem, L);
@@ -588,6 +653,7 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
       default: return launch_ring_c<6>(p, grid, smem, L);
     }
   }
+  if (a.epi == EPI_SWIGLU) return cudaErrorInvalidValue;  // the ring form only
   const int C = pick_c(a.K);
   const int chunks = a.K / 8;
   const int T = std::min(kThreads, ((ceil_div(chunks, C) + 31) / 32) * 32);
@@ -600,7 +666,7 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
   const int per_row = nb * wpg * (int)sizeof(float);
   const int phase_rows = std::max(1, std::min(rows_max, kSmemBudget / per_row));
 
-  GemvParams p;
+  GemvParams p = {};
   p.W = (const __nv_bfloat16*)a.W;
   p.R = a.R; p.K = a.K; p.batch = a.batch;
   p.rows_base = a.R / grid; p.rows_extra = a.R % grid;

@@ -397,6 +397,14 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
     ch[j] = j * T + t;
     cv[j] = ch[j] < KC;
   }
+  // the RMSNorm weights never come from an earlier kernel: load them before the wait
+  uint4 wn[C][2];
+#pragma unroll
+  for (int j = 0; j < C; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      wn[j][h] = (p.pro == PRO_RMSNORM && cv[j]) ? *(const uint4*)(p.norm_w + (size_t)ch[j] * 16 + h * 8)
+                                                 : make_uint4(0u, 0u, 0u, 0u);
   pdl_wait();
 
   float xf[C][16];
@@ -462,12 +470,12 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
         for (int j = 0; j < C; ++j) {
           if (!cv[j]) continue;
 #pragma unroll
-          for (int e = 0; e < 16; e += 8) {
-            const uint4 wn = *(const uint4*)(p.norm_w + (size_t)ch[j] * 16 + e);
-            const float nw[8] = {bf_lo(wn.x), bf_hi(wn.x), bf_lo(wn.y), bf_hi(wn.y),
-                                 bf_lo(wn.z), bf_hi(wn.z), bf_lo(wn.w), bf_hi(wn.w)};
+          for (int h = 0; h < 2; ++h) {
+            const uint4 w = wn[j][h];
+            const float nw[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                                 bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
 #pragma unroll
-            for (int k = 0; k < 8; ++k) xf[j][e + k] = nw[k] * (xf[j][e + k] * inv);
+            for (int k = 0; k < 8; ++k) xf[j][h * 8 + k] = nw[k] * (xf[j][h * 8 + k] * inv);
           }
         }
       }
@@ -618,7 +626,7 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
   const int rc = (a.K % 256 == 0 && aligned) ? ring_q_c(a.K) : 0;
   if (rc > 0) {
     const int rps = rc == 1 ? 8 : rc == 2 ? 4 : 2;   // must match launch_ring_q
-    RingQ8Params p;
+    RingQ8Params p = {};
     p.qs = a.qs; p.d = (const __half*)a.d; p.R = a.R; p.K = a.K;
     const int grid = std::max(1, std::min(a.R, dev_info().sm_count));
     p.rows_base = a.R / grid; p.rows_extra = a.R % grid;
@@ -652,7 +660,7 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
   const int wpg = T / 32;
   const int rows_max = ceil_div(a.R, grid);
   const int phase_rows = std::max(1, std::min(rows_max, kSmemBudget / (wpg * 4)));
-  Q8Params p;
+  Q8Params p = {};
   p.qs = a.qs;
   p.d = (const __half*)a.d;
   p.R = a.R; p.K = a.K;

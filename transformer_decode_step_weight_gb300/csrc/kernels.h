@@ -22,9 +22,29 @@ struct Launch {
   int* err;          // sticky device error word
 };
 
+// ----------------------------------------------------------------- L2 prefetch plan
+// Weights of a later GEMV, cut the way every GEMV cuts its rows over the grid
+// (span c = rows [c * rows_base + min(c, rows_extra), ...) is one CTA's), of
+// which the leading `head_bytes` of every span are fetched into L2 by a kernel
+// that runs before that GEMV and leaves DRAM idle part of its time. A hint
+// only: nothing waits on it and nothing depends on it for correctness.
+struct L2Prefetch {
+  const void* base;               // null: nothing to fetch
+  unsigned long long row_bytes;   // a multiple of 16
+  int rows_base, rows_extra, n_spans;
+  unsigned long long head_bytes;  // per span; >= the span's bytes fetches all of it
+};
+// The plan for an R-row matrix read by a GEMV (same partition as the GEMV
+// launchers); head_bytes = ~0 fetches the whole matrix. Null plan when the row
+// pitch or the base is not 16-byte aligned.
+L2Prefetch l2_plan_rows(const void* base, int R, size_t row_bytes, size_t head_bytes);
+
 // ----------------------------------------------------------------- GEMV bf16
 enum GemvPro { PRO_X_BF16 = 0, PRO_X_F32 = 1, PRO_RMSNORM = 2, PRO_SWIGLU = 3 };
-enum GemvEpi { EPI_STORE = 0, EPI_RESID_ADD = 1 };
+// EPI_SWIGLU (batch-1 ring form only): W holds [gate (F rows); up (F rows)] and the
+// output is h = bf16(silu(gate . x) * (up . x)) [F] in y_bf16. Each CTA takes the
+// same pair range of both halves, so gate_j and up_j meet in one CTA.
+enum GemvEpi { EPI_STORE = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2 };
 
 struct GemvBf16Args {
   const void* W;          // bf16 [R, K]
@@ -36,8 +56,14 @@ struct GemvBf16Args {
   float eps;
   int epi;                // GemvEpi
   float* y;               // f32 [batch, R]
+  L2Prefetch pf;          // batch-1 ring form: weights of the next GEMV, fetched once
+                          // this CTA's own copies are all issued (zero: none)
+  int ring_kb;            // batch-1 ring form: ring size in KB (0: the default)
+  void* y_bf16;           // EPI_SWIGLU: bf16 [R / 2]
 };
 bool gemv_bf16_supported(int K, int batch);
+// True when a batch-1 GEMV of K columns takes the ring form (EPI_SWIGLU needs it).
+bool gemv_bf16_ring_ok(int K, int batch);
 cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L);
 
 // ----------------------------------------------------------------- batched GEMM (tcgen05)
@@ -101,6 +127,12 @@ struct AttnArgs {
   size_t ws_bytes;
   int max_ctx;            // upper bound of keys per sequence (sizes the split grid)
   int use_cluster;        // fused form: > 1 splits each sequence over a cluster of at most this many CTAs
+  L2Prefetch pf[2];       // CUDA-core form: weights of the GEMVs that follow, fetched into L2
+                          // once the dependency wait is over (zero: none)
+  int pf_late;            // 1: only once the CTA's own K/V tiles have all arrived
+  int trig_loop;          // CUDA-core form: let the next kernel launch only once this
+                          // CTA's K/V loop is done (its weight prefetch then does not
+                          // compete with the K/V tiles); 0: at the start
 };
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx);
 int attn_chunk(int B, int Hkv, int max_ctx);

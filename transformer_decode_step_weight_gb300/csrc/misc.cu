@@ -181,7 +181,7 @@ size_t argmax_workspace_bytes(int B) {
 cudaError_t launch_argmax_advance(const float* logits, int V, int B, int32_t* tok, int32_t* pos,
                                   int32_t* step, int32_t* out_tokens, int max_steps, void* ws,
                                   const Launch& L) {
-  ArgmaxParams p;
+  ArgmaxParams p = {};
   p.logits = logits;
   p.V = V;
   p.B = B;
