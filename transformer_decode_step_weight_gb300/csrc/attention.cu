@@ -79,19 +79,23 @@ struct AttnParams {
   int pf_late;  // 1: prefetch once this CTA's own K/V tiles have all arrived
   int stages;   // K/V ring depth, 2..kMaxStages
   int trig_loop;  // 1: trigger the dependent launch after the K/V loop, not at the start
+  const __nv_bfloat16* k_next;  // the next layer's caches: this split's rows go to L2
+  const __nv_bfloat16* v_next;
+  int kv_pf;                    // 0 off, 1 evict-normal, 2 evict-last
 };
 
 struct Carve {
-  size_t kv, q, s, run, bar, total;
+  size_t kv, q, s, run, wm, bar, total;
 };
 __host__ __device__ inline Carve carve(int rep, int stages) {
   Carve c;
   c.kv = 0;                                          // stages x (K tile, V tile)
   c.q = c.kv + (size_t)stages * 2 * kTile * kD * 2;
-  c.s = c.q + (size_t)rep * kD * 4;                  // scores / probabilities [REP][64]
-  c.run = c.s + (size_t)rep * kTile * 4;             // m[REP], l[REP], alpha[REP], scratch
-  c.bar = c.run + 64 * 4;
-  c.total = c.bar + kMaxStages * 8;
+  c.s = c.q + (size_t)rep * kD * 4;                  // per-warp probabilities, REP x 64 floats in all
+  c.run = c.s + (size_t)rep * kTile * 4;             // m[REP], l[REP], scratch
+  c.wm = c.run + 64 * 4;                             // per-warp maxima / sums [2][16 warps][8]
+  c.bar = c.wm + 2 * 16 * 8 * 4;                     // full[kMaxStages], empty[kMaxStages]
+  c.total = c.bar + 2 * kMaxStages * 8;
   return c;
 }
 
@@ -132,6 +136,24 @@ QD_DEV void issue_tile(const AttnParams& p, int b, int g, int t, int n, __nv_bfl
     bulk_g2s(sK + (size_t)(t - t0) * kD, p.k_pages + off, bytes, bar);
     bulk_g2s(sV + (size_t)(t - t0) * kD, p.v_pages + off, bytes, bar);
     t = seg_end;
+  }
+}
+
+// Fetch cached rows [t0, t1) of kv head g of sequence b of another layer's
+// caches (same shape as this layer's) into L2: one page segment per lane.
+QD_DEV void prefetch_kv_rows(const AttnParams& p, const __nv_bfloat16* kc, const __nv_bfloat16* vc, int b, int g,
+                             int t0, int t1, int lane, uint64_t pol) {
+  if (t1 <= t0) return;
+  const int ps = p.page_size;
+  const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
+  for (int lp = t0 / ps + lane; lp <= (t1 - 1) / ps; lp += 32) {
+    const int page = pt[lp];
+    if (page < 0 || page >= p.n_pages) continue;
+    const int a = max(t0, lp * ps), e = min(t1, (lp + 1) * ps);
+    const size_t off = (((size_t)page * p.Hkv + g) * ps + (a - lp * ps)) * kD;
+    const uint32_t bytes = (uint32_t)(e - a) * kD * 2;
+    l2_prefetch_hint(kc + off, bytes, pol);
+    l2_prefetch_hint(vc + off, bytes, pol);
   }
 }
 
@@ -234,8 +256,12 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   auto stage_k = [&](int st) { return sKV + (size_t)st * 2 * kTile * kD; };
   auto stage_v = [&](int st) { return sKV + (size_t)st * 2 * kTile * kD + kTile * kD; };
 
+  uint64_t* empty = bars + kMaxStages;  // a stage is free once every warp has read it
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&bars[st], 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&bars[st], 1);
+      mbar_init(&empty[st], kWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -245,20 +271,30 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
       issue_tile(p, b, g, ts, max(0, min(ts + kTile, copy_end) - ts), stage_k(st), stage_v(st), &bars[st]);
     }
   }
+  // The RoPE row, the QK-norm weights and the cache page of the current token
+  // do not come from the previous kernel either: load them before the wait.
+  float k_new = 0.f, v_new = 0.f;
+  const bool own_pos = FUSED && pos >= t0 && pos < t_end;
+  const int d = tid & (kD - 1);
+  float2 cs = make_float2(0.f, 0.f);
+  float wq = 0.f, wk = 0.f;
+  int own_page = -1;
+  if (FUSED) {
+    cs = p.rope[(size_t)pos * (kD / 2) + (d & 63)];
+    wq = __bfloat162float(p.q_norm[d]);
+    wk = __bfloat162float(p.k_norm[d]);
+    if (own_pos) own_page = p.page_table[(size_t)b * p.max_pages + pos / p.page_size];
+  }
   pdl_wait();  // q, k, v (and, standalone, the caller's q) come from the previous kernel
   if (!p.pf_late) prefetch_next();
 
   // ---- q for the REP heads of this kv head (pre-scaled by scale * log2 e); new k, v.
   // All head vectors load at once; one barrier for the sums of squares, one for RoPE.
-  float k_new = 0.f, v_new = 0.f;
-  const bool own_pos = FUSED && pos >= t0 && pos < t_end;
   if (FUSED) {
     const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
     const float* qkv = p.qkv + (size_t)b * qkv_w;
     // threads [0, 128) own one dim of every head vector; the rest only join the barriers
     const bool dim_thread = tid < kD;
-    const int d = tid & (kD - 1);
-    const float2 cs = p.rope[(size_t)pos * (kD / 2) + (d & 63)];
     float xv[REP + 1];
 #pragma unroll
     for (int i = 0; i < REP; ++i) xv[i] = dim_thread ? qkv[(g * REP + i) * kD + d] : 0.f;
@@ -278,8 +314,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
       const float inv = 1.0f / sqrtf(tot / (float)kD + p.eps);
       float n = xv[i] * inv;
       if (p.act_bf16) n = round_bf16(n);
-      const __nv_bfloat16* w = i < REP ? p.q_norm : p.k_norm;
-      y[i] = __bfloat162float(w[d]) * n;
+      y[i] = (i < REP ? wq : wk) * n;
       if (p.act_bf16) y[i] = round_bf16(y[i]);
       if (dim_thread) {
         if (i < REP) sQ[i * kD + d] = y[i];
@@ -302,7 +337,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
       k_new = round_bf16(r[REP]);
       v_new = round_bf16(vx);
       const int lp = pos / p.page_size;
-      const int page = p.page_table[(size_t)b * p.max_pages + lp];
+      const int page = own_page;
       if (page < 0 || page >= p.n_pages) {
         if (tid == 0) set_error(p.err, QD_DEVERR_PAGE);
       } else {
@@ -314,12 +349,14 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   } else {
     for (int e = tid; e < REP * kD; e += kThreads) sQ[e] = p.q[head0 * kD + e] * p.scale_log2;
   }
-  if (tid < REP) {
-    sRun[tid] = -INFINITY;
-    sRun[8 + tid] = 0.f;
-  }
   __syncthreads();
 
+  // ---- K/V loop. Each warp owns kPairs token pairs of every tile from score to
+  // P.V: lane = (token of a pair, 16-byte chunk of the head dim). Per tile one
+  // CTA barrier publishes the per-warp maxima; every warp then forms the same
+  // running max per head and rescales only its own accumulators and partial
+  // sums. A stage is handed back through its `empty` barrier (one arrival per
+  // warp), so no second CTA barrier is needed per tile.
   const int half = lane >> 4, dc = lane & 15;
   float qr[REP][8];
 #pragma unroll
@@ -331,6 +368,22 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   for (int i = 0; i < REP; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+  float m_run[REP];                      // identical in every lane of every warp
+#pragma unroll
+  for (int i = 0; i < REP; ++i) m_run[i] = -INFINITY;
+  float l_hold = 0.f;                    // holder lanes: sum of p of head hsel over this lane's tokens
+  constexpr int kTokW = 2 * kPairs;      // tokens per warp per tile
+  float* sP = sS + warp * REP * kTokW;   // this warp's probabilities [REP][kTokW]
+  float* sWm = (float*)(smem + cv.wm);   // [2][16][8]
+  constexpr int kHoldMask = 16 / REP - 1;
+  const bool holder = (dc & kHoldMask) == 0;
+  // head whose dot a holder lane ends with (fixed by the lane's position in the butterfly)
+  int hsel = 0;
+#pragma unroll
+  for (int L = 8, n = REP; L >= 1 && n > 1; L >>= 1) {
+    n /= 2;
+    if (lane & L) hsel += n;
+  }
 
   for (int it = 0; it < n_tiles; ++it) {
     const int st = it % kStages;
@@ -338,22 +391,21 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
     const int nv = min(kTile, t_end - ts);
     __nv_bfloat16* sK = stage_k(st);
     __nv_bfloat16* sV = stage_v(st);
-    if (!mbar_wait_bounded(&bars[st], (uint32_t)((it / kStages) & 1), p.err)) {
-      for (int k = 1; k < kStages && it + k < n_tiles; ++k)
-        mbar_wait_bounded(&bars[(it + k) % kStages], (uint32_t)(((it + k) / kStages) & 1), p.err);
-      if (!CLUSTER) return;
-      break;  // cluster peers still expect this CTA at the cluster barriers (the error word is set)
+    const bool got = mbar_wait_bounded(&bars[st], (uint32_t)((it / kStages) & 1), p.err);
+    if (own_pos && pos >= ts && pos < ts + kTile) {  // CTA-uniform: the current token's row
+      if (tid < kD) {
+        sK[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(k_new);
+        sV[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(v_new);
+      }
+      __syncthreads();
     }
-    if (own_pos && pos >= ts && pos < ts + kTile && tid < kD) {
-      sK[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(k_new);
-      sV[(size_t)(pos - ts) * kD + tid] = __float2bfloat16_rn(v_new);
-    }
-    __syncthreads();
 
-    // scores: lane = (token of a pair, 16-byte dim chunk); warp w owns pairs [8w, 8w + 8)
+    // scores of this warp's tokens; after the transposed butterfly over the 16
+    // lanes of a token, holder lane (dc) has the full dot of head hsel
+    float sc[kPairs];
 #pragma unroll
-    for (int pi = warp * kPairs; pi < warp * kPairs + kPairs; ++pi) {
-      const int tt = 2 * pi + half;
+    for (int q = 0; q < kPairs; ++q) {
+      const int tt = 2 * (warp * kPairs + q) + half;
       const bool ok = tt < nv;
       uint4 kw = make_uint4(0u, 0u, 0u, 0u);
       if (ok) kw = *(const uint4*)(sK + (size_t)tt * kD + dc * 8);
@@ -370,9 +422,6 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
         }
         v[i] = a + c;
       }
-      // transposed butterfly over the 16 lanes of this token: afterwards lane
-      // (dc) holds the full dot of head hsel(dc)
-      int hsel = 0;
 #pragma unroll
       for (int L = 8, n = REP; L >= 1; L >>= 1) {
         if (n > 1) {
@@ -384,76 +433,107 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
             const float keep = up ? v[k + h] : v[k];
             v[k] = keep + __shfl_xor_sync(0xffffffffu, send, L);
           }
-          if (up) hsel += h;
           n = h;
         } else {
           v[0] += __shfl_xor_sync(0xffffffffu, v[0], L);
         }
       }
-      if ((dc & (16 / REP - 1)) == 0) sS[hsel * kTile + tt] = ok ? v[0] : -INFINITY;
+      sc[q] = ok ? v[0] : -INFINITY;
     }
-    __syncthreads();
-
-    // online softmax update per head (log2 domain)
-    for (int i = warp; i < REP; i += kWarps) {
-      constexpr int kPer = kTile / 32;
-      float a[kPer];
+    // this warp's maximum per head -> shared memory (buffer it & 1)
+    float mx = sc[0];
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) a[u] = sS[i * kTile + lane + 32 * u];
-      float mx = a[0];
-#pragma unroll
-      for (int u = 1; u < kPer; ++u) mx = fmaxf(mx, a[u]);
-      const float m_old = sRun[i];
-      const float m_new = fmaxf(m_old, warp_max(mx));
-      float sum = 0.f;
-#pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        a[u] = exp2f(a[u] - m_new);
-        sum += a[u];
-        sS[i * kTile + lane + 32 * u] = a[u];
-      }
-      const float l = warp_sum(sum);
-      __syncwarp();
-      if (lane == 0) {
-        const float alpha = exp2f(m_old - m_new);   // 0 on the first tile
-        sRun[16 + i] = alpha;
-        sRun[8 + i] = sRun[8 + i] * alpha + l;
-        sRun[i] = m_new;
-      }
+    for (int q = 1; q < kPairs; ++q) mx = fmaxf(mx, sc[q]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    float* wmb = sWm + (it & 1) * 16 * 8;
+    if (holder && half == 0) wmb[warp * 8 + hsel] = mx;
+    if (!__syncthreads_and(got)) {  // a K/V copy never arrived: drain, leave together
+      for (int k = 1; k < kStages && it + k < n_tiles; ++k)
+        mbar_wait_bounded(&bars[(it + k) % kStages], (uint32_t)(((it + k) / kStages) & 1), p.err);
+      if (!CLUSTER) return;
+      break;  // cluster peers still expect this CTA at the cluster barriers (the error word is set)
     }
-    __syncthreads();
-
-    // P . V with the running accumulators rescaled
+    // running max over all warps: lane j < REP reduces head j, then broadcast
+    float mh = -INFINITY;
+    if (lane < REP) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) mh = fmaxf(mh, wmb[w * 8 + lane]);
+    }
+    float alpha[REP];
 #pragma unroll
     for (int i = 0; i < REP; ++i) {
-      const float alpha = sRun[16 + i];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[i][e] *= alpha;
+      const float m_new = fmaxf(m_run[i], __shfl_sync(0xffffffffu, mh, i));
+      alpha[i] = exp2f(m_run[i] - m_new);   // 0 on the first tile
+      m_run[i] = m_new;
     }
+    // probabilities of this warp's tokens (holder lanes), partial sums, P.V
+    float m_h = m_run[0], a_h = alpha[0];
 #pragma unroll
-    for (int pi = warp * kPairs; pi < warp * kPairs + kPairs; ++pi) {
-      const int tt = 2 * pi + half;
+    for (int i = 1; i < REP; ++i)
+      if (hsel == i) { m_h = m_run[i]; a_h = alpha[i]; }
+    l_hold *= a_h;
+#pragma unroll
+    for (int q = 0; q < kPairs; ++q) {
+      const float pp = exp2f(sc[q] - m_h);   // 0 for masked tokens
+      if (holder) {
+        l_hold += pp;
+        sP[hsel * kTokW + 2 * q + half] = pp;
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < REP; ++i)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[i][e] *= alpha[i];
+#pragma unroll
+    for (int q = 0; q < kPairs; ++q) {
+      const int tt = 2 * (warp * kPairs + q) + half;
       if (tt < nv) {
         const uint4 vw = *(const uint4*)(sV + (size_t)tt * kD + dc * 8);
         const float vf[8] = {bf_lo(vw.x), bf_hi(vw.x), bf_lo(vw.y), bf_hi(vw.y),
                              bf_lo(vw.z), bf_hi(vw.z), bf_lo(vw.w), bf_hi(vw.w)};
 #pragma unroll
         for (int i = 0; i < REP; ++i) {
-          const float pp = sS[i * kTile + tt];
+          const float pp = sP[i * kTokW + 2 * q + half];
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(pp, vf[e], acc[i][e]);
         }
       }
     }
-    __syncthreads();  // the stage and the probabilities are free again
+    __syncwarp();                          // this warp is done with the stage and sP
+    if (lane == 0) mbar_arrive(&empty[st]);
     if (tid == 0 && it + kStages < n_tiles) {
-      const int tn = t0 + (it + kStages) * kTile;
-      issue_tile(p, b, g, tn, max(0, min(tn + kTile, copy_end) - tn), sK, sV, &bars[st]);
+      if (mbar_wait_bounded(&empty[st], (uint32_t)((it / kStages) & 1), p.err)) {
+        const int tn = t0 + (it + kStages) * kTile;
+        issue_tile(p, b, g, tn, max(0, min(tn + kTile, copy_end) - tn), sK, sV, &bars[st]);
+      }
+    }
+  }
+  // per-head totals: m (same everywhere) and l summed over holder lanes and warps
+  {
+    float lw = l_hold + __shfl_xor_sync(0xffffffffu, l_hold, 16);
+    float* wl = sWm + (n_tiles & 1) * 16 * 8;   // the buffer no warp can still be reading
+    if (holder && half == 0) wl[warp * 8 + hsel] = lw;
+    __syncthreads();
+    if (tid < REP) {
+      float L = 0.f;
+      for (int w = 0; w < kWarps; ++w) L += wl[w * 8 + tid];
+      float m = m_run[0];
+#pragma unroll
+      for (int i = 1; i < REP; ++i)
+        if (tid == i) m = m_run[i];
+      sRun[tid] = m;
+      sRun[8 + tid] = L;
     }
   }
 
   pdl_launch_dependents();  // all K/V of this split is in shared memory
   if (p.pf_late) prefetch_next();
+  // DRAM idles while the splits publish and combine: bring the next layer's
+  // rows of this split into L2 for its attention
+  if (p.kv_pf && p.k_next && warp == 2)
+    prefetch_kv_rows(p, p.k_next, p.v_next, b, g, t0, copy_end, lane,
+                     p.kv_pf == 2 ? policy_evict_last() : policy_evict_normal());
 
   // ---- reduce the two token halves, then the warps, element by element
 #pragma unroll
@@ -769,6 +849,9 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   p.pf_late = a.pf_late;
   p.stages = simt_stages();
   p.trig_loop = a.trig_loop;
+  p.k_next = (const __nv_bfloat16*)a.k_next;
+  p.v_next = (const __nv_bfloat16*)a.v_next;
+  p.kv_pf = a.kv_pf;
   const bool fused = a.qkv != nullptr;
   // the fused decode step splits each sequence across one thread block cluster;
   // the standalone call keeps the workspace split (its workspace is the scratch)

@@ -22,6 +22,19 @@ QD_DEV uint64_t policy_evict_first() {
   return pol;
 }
 
+// L2 policies for data kept until a later kernel reads it (evict_last) or for
+// the default priority (evict_normal).
+QD_DEV uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+QD_DEV uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // 128-bit streaming load through the non-coherent path without L1 allocation.
 QD_DEV uint4 ld_stream(const void* p, uint64_t pol) {
   uint4 v;
@@ -85,6 +98,10 @@ QD_DEV void mbar_init(uint64_t* bar, uint32_t count) {
 }
 QD_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
+QD_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 QD_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
@@ -119,6 +136,22 @@ QD_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, int* err) {
   }
   set_error(err, QD_DEVERR_TIMEOUT);
   return false;
+}
+
+// Global -> shared bulk copy with an L2 cache policy (same alignment rules).
+QD_DEV void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// Fetch [src, src + bytes) into L2 with a cache policy; fire and forget.
+// src 16-byte aligned, bytes a multiple of 16.
+QD_DEV void l2_prefetch_hint(const void* src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(pol)
+               : "memory");
 }
 
 // Global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.

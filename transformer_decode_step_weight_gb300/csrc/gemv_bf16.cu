@@ -307,12 +307,10 @@ struct RingParams {
   L2Prefetch pf;
   int pair_F;                 // EPI_SWIGLU: F (rows of each half); the partition is over pairs
   __nv_bfloat16* y_bf16;      // EPI_SWIGLU output [F]
+  int w_evict_first;          // weight copies marked evict-first in L2
 };
 
 QD_DEV void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
-QD_DEV void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 template <int C, int RPS>
 __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingParams p) {
@@ -351,6 +349,11 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingPara
       const unsigned char* src = (const unsigned char*)(p.W + (size_t)r0 * K);
       // EPI_SWIGLU: local row lr >= npair is weight row F + r0 + (lr - npair)
       const unsigned char* src_up = pair ? (const unsigned char*)(p.W + ((size_t)p.pair_F + r0) * K) : src;
+      const uint64_t pol = policy_evict_first();
+      auto copy = [&](void* d, const void* g, uint32_t n, uint64_t* bar) {
+        if (p.w_evict_first) bulk_g2s_hint(d, g, n, bar, pol);
+        else bulk_g2s(d, g, n, bar);
+      };
       for (int i = 0; i < n_stages; ++i) {
         const int slot = i % ns;
         if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) break;
@@ -360,12 +363,12 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingPara
         mbar_arrive_expect_tx(&full[slot], (uint32_t)(rows_i * row_bytes));
         unsigned char* dst = ring + (size_t)slot * p.stage_bytes;
         if (!pair) {
-          bulk_g2s(dst, src + (size_t)a * row_bytes, (uint32_t)(rows_i * row_bytes), &full[slot]);
+          copy(dst, src + (size_t)a * row_bytes, (uint32_t)(rows_i * row_bytes), &full[slot]);
         } else {  // the stage may straddle the gate/up boundary: one copy per half
           const int na = max(0, min(a + rows_i, npair) - a);   // gate rows in this stage
-          if (na > 0) bulk_g2s(dst, src + (size_t)a * row_bytes, (uint32_t)(na * row_bytes), &full[slot]);
+          if (na > 0) copy(dst, src + (size_t)a * row_bytes, (uint32_t)(na * row_bytes), &full[slot]);
           if (rows_i > na)
-            bulk_g2s(dst + (size_t)na * row_bytes, src_up + (size_t)(a + na - npair) * row_bytes,
+            copy(dst + (size_t)na * row_bytes, src_up + (size_t)(a + na - npair) * row_bytes,
                      (uint32_t)((rows_i - na) * row_bytes), &full[slot]);
         }
       }
@@ -641,6 +644,7 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
     p.pro = a.pro; p.x = a.x; p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps;
     p.epi = a.epi; p.y = a.y; p.err = L.err; p.trig_late = L.trig_late;
     p.pf = a.pf;
+    p.w_evict_first = a.w_evict_first;
     size_t smem = (size_t)p.ring_bytes + 32 * 8 + (size_t)kPhaseRows * (p.T / 32) * 4 + (size_t)tu.pad_kb * 1024;
     if (pair) smem += (size_t)2 * (p.rows_base + 1) * 4;
     if (smem > (size_t)dev_info().max_smem_optin - 1024) return cudaErrorInvalidValue;

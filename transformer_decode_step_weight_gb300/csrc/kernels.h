@@ -60,6 +60,7 @@ struct GemvBf16Args {
                           // this CTA's own copies are all issued (zero: none)
   int ring_kb;            // batch-1 ring form: ring size in KB (0: the default)
   void* y_bf16;           // EPI_SWIGLU: bf16 [R / 2]
+  int w_evict_first;      // batch-1 ring form: weight copies marked evict-first in L2
 };
 bool gemv_bf16_supported(int K, int batch);
 // True when a batch-1 GEMV of K columns takes the ring form (EPI_SWIGLU needs it).
@@ -130,6 +131,9 @@ struct AttnArgs {
   L2Prefetch pf[2];       // CUDA-core form: weights of the GEMVs that follow, fetched into L2
                           // once the dependency wait is over (zero: none)
   int pf_late;            // 1: only once the CTA's own K/V tiles have all arrived
+  const void* k_next;     // CUDA-core fused form: the next layer's caches (same shape);
+  const void* v_next;     // each CTA fetches its split's cached rows of them into L2
+  int kv_pf;              // 0 off, 1 evict-normal, 2 evict-last prefetch of k/v_next
   int trig_loop;          // CUDA-core form: let the next kernel launch only once this
                           // CTA's K/V loop is done (its weight prefetch then does not
                           // compete with the K/V tiles); 0: at the start
