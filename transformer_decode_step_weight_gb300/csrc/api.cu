@@ -391,6 +391,9 @@ struct StepWs {
   void* xn;         // bf16 [B, max(H, F)]: normed / SwiGLU activations (batched path)
   void* attn_ws;
   void* argmax_ws;
+  int* claims;      // [5 L + 1][2] row-claim counters of the batch-1 GEMVs (zero between launches)
+  void* gemm_ws;    // batched path: split-K partials and tickets (one GEMM at a time)
+  size_t gemm_ws_bytes;
   size_t total;
 };
 
@@ -411,6 +414,15 @@ StepWs step_ws_layout(const qd_step_args* a, void* base) {
   w.attn_ws = (void*)(p + off);
   off += al256(attn_workspace_bytes(B, d.n_q_heads, d.n_kv_heads, a->max_pages * a->page_size));
   w.argmax_ws = (void*)(p + off); off += al256(argmax_workspace_bytes(B));
+  w.claims = (int*)(p + off); off += al256((size_t)(5 * a->n_layers + 1) * 2 * sizeof(int));
+  w.gemm_ws = (void*)(p + off);
+  w.gemm_ws_bytes = 0;
+  if (B > 8) {  // the batched step runs its projections as split-K tcgen05 GEMMs
+    const int shapes[5][2] = {{(int)qkv, d.hidden}, {d.hidden, d.n_q_heads * d.head_dim}, {2 * d.ffn, d.hidden},
+                              {d.hidden, d.ffn}, {a->vocab, d.hidden}};
+    for (const auto& sh : shapes) w.gemm_ws_bytes = std::max(w.gemm_ws_bytes, gemm_tc_workspace_bytes(sh[0], sh[1]));
+  }
+  off += al256(w.gemm_ws_bytes);
   w.total = off;
   return w;
 }
@@ -482,6 +494,7 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   auto gemm = [&](const void* W, int R, int K, const void* X, int epi, float* y) {
     GemmTcArgs g = {};
     g.W = W; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
+    g.ws = w.gemm_ws; g.ws_bytes = w.gemm_ws_bytes;
     return launch_gemm_tc(g, L);
   };
   QD_TRY(launch_embed(a->embed, H, a->vocab, a->tok, B, w.res, L), "embed");
@@ -523,8 +536,10 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   const StepTuning& pft = step_tuning();
   // batch 1 on the ring GEMV: SwiGLU in the gate+up epilogue (bf16 h), so the down
   // projection reads 2F bytes of h instead of 8F of gate/up and recomputes nothing
-  const bool swiglu_epi = !q8 && B == 1 && gemv_bf16_ring_ok(H, 1) && gemv_bf16_ring_ok(F, 1) &&
+  const bool swiglu_epi = !q8 && B == 1 && gemv_bf16_swiglu_ok(H) && gemv_bf16_ring_ok(F, 1) &&
                           !pft.swiglu_in_down;
+  // each batch-1 GEMV launch of the step owns a pair of row-claim counters
+  auto claim = [&](int li, int k) { return B == 1 ? w.claims + 2 * (5 * li + k) : nullptr; };
   // head of every span of the next batch-1 BF16 GEMV (R rows of K), or nothing
   auto tail_plan = [&](const void* Wn, int R, int K) {
     L2Prefetch pf = {};
@@ -544,6 +559,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 0);
       g.W = l->w.w_qkv; g.R = QKV; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
       g.norm_w = l->w.ln_in; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.qkv;
       QD_TRY(launch_gemv_bf16(g, L), "qkv gemv");
@@ -580,6 +596,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 1);
       g.W = l->w.w_o; g.R = H; g.K = Hq * D; g.batch = B; g.pro = PRO_X_BF16; g.x = w.attn;
       g.epi = EPI_RESID_ADD; g.y = w.res;
       g.pf = tail_plan(l->w.w_gu, 2 * F, H);
@@ -595,6 +612,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 2);
       g.W = l->w.w_gu; g.R = 2 * F; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
       g.norm_w = l->w.ln_post; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.gu;
       if (swiglu_epi) {  // h = bf16(silu(gate) * up) formed in the epilogue, into xn
@@ -612,6 +630,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 3);
       g.W = l->w.w_down; g.R = H; g.K = F; g.batch = B; g.pro = PRO_SWIGLU; g.x = w.gu;
       g.epi = EPI_RESID_ADD; g.y = w.res;
       if (swiglu_epi) { g.pro = PRO_X_BF16; g.x = w.xn; }
@@ -629,6 +648,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   } else {
     GemvBf16Args g = {};
     g.w_evict_first = pft.w_evict_first;
+    g.claim = claim(a->n_layers, 0);
     g.W = a->lm_head; g.R = a->vocab; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
     g.norm_w = a->final_norm; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = a->logits;
     QD_TRY(launch_gemv_bf16(g, L), "lm head");

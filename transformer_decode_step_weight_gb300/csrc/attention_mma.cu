@@ -140,24 +140,12 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  pdl_wait();
   if (!p.trig_late) pdl_launch_dependents();
 
-  // issue every independent load first: the position (or length) and this
-  // thread's dim of the q heads (and of the new k, v)
+  // The position (or length), the page table and the cached rows below it are
+  // final before this kernel starts (only q, k, v come from the kernel it waits
+  // on), so the first K/V tiles are requested before the dependency wait.
   const int pv_raw = FUSED ? p.pos[b] : p.seq_lens[b];
-  const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
-  float xq[REP], xk = 0.f, xvv = 0.f;
-  if (FUSED) {
-    const float* qkv = p.qkv + (size_t)b * qkv_w;
-#pragma unroll
-    for (int i = 0; i < REP; ++i) xq[i] = qkv[(g * REP + i) * kD + tid];
-    xk = qkv[(p.Hq + g) * kD + tid];
-    xvv = qkv[(p.Hq + p.Hkv + g) * kD + tid];
-  } else {
-#pragma unroll
-    for (int i = 0; i < REP; ++i) xq[i] = p.q[((size_t)b * p.Hq + g * REP + i) * kD + tid];
-  }
   int len, pos = 0;
   if (FUSED) {
     pos = pv_raw;
@@ -173,6 +161,7 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
   }
   const size_t head0 = (size_t)b * p.Hq + g * REP;
   if (len == 0) {  // empty sequence (standalone form only): zero output
+    pdl_wait();
     if (s == 0 && !FUSED)
       for (int e = tid; e < REP * kD; e += kTh) p.out_f32[head0 * kD + e] = 0.f;
     return;
@@ -183,16 +172,28 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
   const int t_end = min(t0 + p.chunk, len);
   const int n_tiles = (t_end - t0 + kT - 1) / kT;
   const int skip_tok = FUSED ? pos : -1;   // the current token comes from registers
-
   const uint32_t ring_u = smem_u32(ring);
   auto tileK = [&](int st) { return ring_u + (uint32_t)(st * 2 * kTileBytes); };
   auto tileV = [&](int st) { return ring_u + (uint32_t)(st * 2 * kTileBytes + kTileBytes); };
 
-  // ---- start streaming the first tiles, then build q (and the new k, v) meanwhile
+  // ---- start streaming the first tiles, then wait for and build q (and the new k, v)
 #pragma unroll
   for (int st = 0; st < kSt - 1; ++st) {
     if (st < n_tiles) load_tile(p, b, g, t0 + st * kT, t_end, skip_tok, tileK(st), tileV(st));
     cp_async_commit();
+  }
+  pdl_wait();
+  const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
+  float xq[REP], xk = 0.f, xvv = 0.f;
+  if (FUSED) {
+    const float* qkv = p.qkv + (size_t)b * qkv_w;
+#pragma unroll
+    for (int i = 0; i < REP; ++i) xq[i] = qkv[(g * REP + i) * kD + tid];
+    xk = qkv[(p.Hq + g) * kD + tid];
+    xvv = qkv[(p.Hq + p.Hkv + g) * kD + tid];
+  } else {
+#pragma unroll
+    for (int i = 0; i < REP; ++i) xq[i] = p.q[((size_t)b * p.Hq + g * REP + i) * kD + tid];
   }
 
   float k_new = 0.f, v_new = 0.f;

@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 namespace qd {
@@ -36,12 +37,16 @@ constexpr int kStagesTc = 6;
 constexpr int kTileA = kBM * kBK * 2;    // 16 KB
 constexpr int kTileB = kBN * kBK * 2;    // 8 KB
 constexpr int kThreadsTc = 128;
+constexpr int kMaxSplits = 4;   // K splits of one tile (partials summed in registers)
 
 struct TcParams {
   int R, K, B;
   int epi;        // EPI_STORE / EPI_RESID_ADD
   float* y;       // [B, R]
   int* err;
+  int splits;     // K splits (grid y); > 1: partials through part / cnt
+  float* part;    // [tiles][splits][kBN][kBM] f32 partial tiles
+  int* cnt;       // [tiles] tickets, zero between launches
 };
 
 // --- tcgen05 / TMA wrappers -------------------------------------------------
@@ -135,7 +140,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * kBM;
-  const int n_k = p.K / kBK;
+  // this CTA's K blocks [kb0, kb0 + n_k) of split blockIdx.y
+  const int n_kt = p.K / kBK;
+  const int kb0 = (int)(((long long)n_kt * blockIdx.y) / p.splits);
+  const int n_k = (int)(((long long)n_kt * (blockIdx.y + 1)) / p.splits) - kb0;
+  __shared__ int s_ticket;
 
   if (tid == 0) {
     for (int i = 0; i < kStagesTc; ++i) {
@@ -158,10 +167,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int pre = min(kStagesTc, n_k);
     for (int i = 0; i < pre; ++i) {
       mbar_arrive_expect_tx(&full[i], kTileA + kTileB);
-      tma_load_2d(sA + i * kTileA, &tmW, i * kBK, row0, &full[i]);
+      tma_load_2d(sA + i * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[i]);
     }
     pdl_wait();
-    for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * kTileB, &tmX, i * kBK, 0, &full[i]);
+    for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[i]);
     for (int i = pre; i < n_k; ++i) {
       const int s = i % kStagesTc;
       if (!mbar_wait_bounded(&empty[s], (uint32_t)(((i / kStagesTc) - 1) & 1), p.err)) {
@@ -169,8 +178,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         break;
       }
       mbar_arrive_expect_tx(&full[s], kTileA + kTileB);
-      tma_load_2d(sA + s * kTileA, &tmW, i * kBK, row0, &full[s]);
-      tma_load_2d(sB + s * kTileB, &tmX, i * kBK, 0, &full[s]);
+      tma_load_2d(sA + s * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[s]);
+      tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -194,8 +203,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_after();
   float v[64];
   tmem_ld_32x64(tmem + ((uint32_t)(warp * 32) << 16), v);
-  const int r = row0 + warp * 32 + lane;
-  if (ok && !s_abort && r < p.R) {
+  const int rl = warp * 32 + lane;          // this thread's row of the tile
+  const int r = row0 + rl;
+  bool write = ok && !s_abort;
+  if (p.splits > 1) {
+    // publish this split's partial tile [kBM rows][kBN tokens] (a thread's row is
+    // 256 contiguous bytes), take a ticket; the last split of the tile adds every
+    // partial in split order, 16 tokens at a time with all splits' loads in flight
+    const size_t tile = blockIdx.x;
+    float4* part = (float4*)(p.part + (tile * p.splits + blockIdx.y) * (size_t)(kBN * kBM) + (size_t)rl * kBN);
+#pragma unroll
+    for (int q = 0; q < kBN / 4; ++q) part[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      s_ticket = atomicAdd(p.cnt + tile, 1);
+      __threadfence();
+    }
+    __syncthreads();
+    if (s_ticket == p.splits - 1 && write && r < p.R) {
+      const float4* base = (const float4*)(p.part + tile * p.splits * (size_t)(kBN * kBM) + (size_t)rl * kBN);
+      constexpr size_t kSplitStride = (size_t)kBN * kBM / 4;   // float4s per partial tile
+#pragma unroll 1
+      for (int c = 0; c < kBN / 16; ++c) {
+        float4 t[kMaxSplits][4];
+#pragma unroll
+        for (int sp = 0; sp < kMaxSplits; ++sp)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            t[sp][q] = sp < p.splits ? __ldcg(base + sp * kSplitStride + c * 4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float4 a = t[0][q];
+#pragma unroll
+          for (int sp = 1; sp < kMaxSplits; ++sp) {
+            if (sp < p.splits) {
+              a.x += t[sp][q].x; a.y += t[sp][q].y; a.z += t[sp][q].z; a.w += t[sp][q].w;
+            }
+          }
+          const float o[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int n = c * 16 + q * 4 + e;
+            if (n < p.B) {
+              float* yp = p.y + (size_t)n * p.R + r;
+              if (p.epi == EPI_RESID_ADD) *yp += o[e];
+              else *yp = o[e];
+            }
+          }
+        }
+      }
+    }
+    if (s_ticket == p.splits - 1 && tid == 0) p.cnt[tile] = 0;
+    write = false;  // the tile's output is written above (or by another split)
+  }
+  if (write && r < p.R) {
 #pragma unroll
     for (int n = 0; n < kBN; ++n) {
       if (n < p.B) {
@@ -247,6 +310,47 @@ constexpr size_t kSmemTc = 1024 + (size_t)kStagesTc * (kTileA + kTileB) + (2 * k
 
 bool gemm_tc_supported(int R, int K, int B) { return R >= 1 && K >= kBK && K % kBK == 0 && B >= 1 && B <= kBN; }
 
+// K splits for an R x K launch, chosen to keep every SM streaming to the end.
+// With s splits the tiles x s CTAs run in ceil(tiles x s / SMs) rounds of 1/s of
+// a tile's weight bytes each; every split adds a 32 KB partial tile written and
+// read back (mostly through L2, counted at half weight). At least 8 K blocks per
+// CTA, at most kMaxSplits. QD_GEMM_SPLITS forces a count.
+// Split-K workspace: a fixed block of tile tickets first (the same place for every
+// launch that shares the workspace, so one launch's partials never land on
+// another's tickets), then the partial tiles.
+constexpr int kMaxSplitTiles = 4096;
+constexpr size_t kTicketBytes = (size_t)kMaxSplitTiles * sizeof(int);
+
+int gemm_tc_splits(int R, int K) {
+  if (R < 1 || K < kBK) return 1;
+  const int tiles = (R + kBM - 1) / kBM, n_kt = K / kBK, sms = dev_info().sm_count;
+  if (tiles > kMaxSplitTiles) return 1;
+  static const int forced = [] {
+    const char* v = getenv("QD_GEMM_SPLITS");
+    return v ? atoi(v) : 0;
+  }();
+  if (forced > 0) return std::max(1, std::min(std::min(forced, kMaxSplits), n_kt));
+  if (tiles >= sms) return 1;  // the tiles alone fill the GPU (measured: splitting them was slower)
+  int best = 1;
+  double best_t = (double)((tiles + sms - 1) / sms);
+  const double tile_bytes = (double)kBM * K * 2;
+  for (int sp = 2; sp <= kMaxSplits && n_kt / sp >= 8; ++sp) {
+    const double t = (double)((tiles * sp + sms - 1) / sms) / sp + 0.5 * sp * 65536.0 / tile_bytes;
+    if (t < best_t) {
+      best_t = t;
+      best = sp;
+    }
+  }
+  return best;
+}
+
+size_t gemm_tc_workspace_bytes(int R, int K) {
+  const int sp = gemm_tc_splits(R, K);
+  if (sp <= 1) return 0;
+  const size_t tiles = (size_t)(R + kBM - 1) / kBM;
+  return kTicketBytes + tiles * sp * kBN * kBM * sizeof(float);
+}
+
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   if (!gemm_tc_supported(a.R, a.K, a.B)) return cudaErrorInvalidValue;
   CUtensorMap tw, tx;
@@ -264,7 +368,14 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   TcParams p = {};
   p.R = a.R; p.K = a.K; p.B = a.B; p.epi = a.epi; p.y = a.y; p.err = L.err;
   const int tiles = (a.R + kBM - 1) / kBM;
-  return launch_ex(gemm_tc_kernel, dim3(tiles), dim3(kThreadsTc), kSmemTc, L, tw, tx, p);
+  p.splits = 1;
+  const size_t need = gemm_tc_workspace_bytes(a.R, a.K);
+  if (a.ws && need > 0 && a.ws_bytes >= need) {
+    p.splits = gemm_tc_splits(a.R, a.K);
+    p.cnt = (int*)a.ws;
+    p.part = (float*)((unsigned char*)a.ws + kTicketBytes);
+  }
+  return launch_ex(gemm_tc_kernel, dim3(tiles, p.splits), dim3(kThreadsTc), kSmemTc, L, tw, tx, p);
 }
 
 }  // namespace qd

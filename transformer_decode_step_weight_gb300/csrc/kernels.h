@@ -61,10 +61,15 @@ struct GemvBf16Args {
   int ring_kb;            // batch-1 ring form: ring size in KB (0: the default)
   void* y_bf16;           // EPI_SWIGLU: bf16 [R / 2]
   int w_evict_first;      // batch-1 ring form: weight copies marked evict-first in L2
+  int* claim;             // batch-1 ring form: two ints, zero before the launch and left
+                          // zero after it; part of the rows is then claimed by whichever
+                          // CTA is free (null: static split of the rows)
 };
 bool gemv_bf16_supported(int K, int batch);
-// True when a batch-1 GEMV of K columns takes the ring form (EPI_SWIGLU needs it).
+// True when a batch-1 GEMV of K columns takes the ring form, and when that form
+// can also take EPI_SWIGLU.
 bool gemv_bf16_ring_ok(int K, int batch);
+bool gemv_bf16_swiglu_ok(int K);
 cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L);
 
 // ----------------------------------------------------------------- batched GEMM (tcgen05)
@@ -74,8 +79,13 @@ struct GemmTcArgs {
   int R, K, B;            // B <= 64
   int epi;                // GemvEpi
   float* y;               // f32 [B, R]
+  void* ws;               // split-K partials and tile tickets (zero-filled before first use,
+  size_t ws_bytes;        // left so); null: no split
 };
 bool gemm_tc_supported(int R, int K, int B);
+// K splits a launch of this shape takes, and the workspace they need.
+int gemm_tc_splits(int R, int K);
+size_t gemm_tc_workspace_bytes(int R, int K);
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L);
 
 // row-wise helpers of the batched step

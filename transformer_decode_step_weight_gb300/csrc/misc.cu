@@ -129,27 +129,60 @@ __global__ void __launch_bounds__(kArgmaxThreads) argmax_advance_kernel(const Ar
   }
 }
 
-// out[b, :] = bf16(w * bf16(x[b, :] * rsqrt(mean(x[b, :]^2) + eps))), Qwen cast order
+// out[b, :] = bf16(w * bf16(x[b, :] * rsqrt(mean(x[b, :]^2) + eps))), Qwen cast order.
+// One CTA per row; each thread keeps CPT 8-element chunks of the row in registers
+// (one pass over x), the weights are loaded before the dependency wait.
+template <int CPT>
 __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* x, const __nv_bfloat16* w, int K, float eps,
                                                            __nv_bfloat16* out) {
   __shared__ float red[8];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  uint4 wv[CPT];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int i = (c * 256 + tid) * 8;
+    wv[c] = i < K ? *(const uint4*)(w + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
   pdl_wait();
   pdl_launch_dependents();
-  const int b = blockIdx.x;
   const float* xr = x + (size_t)b * K;
+  float xv[CPT][8];
   float ss = 0.f;
-  for (int i = threadIdx.x * 4; i < K; i += blockDim.x * 4) {
-    const float4 v = *(const float4*)(xr + i);
-    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int i = (c * 256 + tid) * 8;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), d = a;
+    if (i < K) {
+      a = *(const float4*)(xr + i);
+      d = *(const float4*)(xr + i + 4);
+    }
+    xv[c][0] = a.x; xv[c][1] = a.y; xv[c][2] = a.z; xv[c][3] = a.w;
+    xv[c][4] = d.x; xv[c][5] = d.y; xv[c][6] = d.z; xv[c][7] = d.w;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(xv[c][e], xv[c][e], ss);
   }
   ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
   __syncthreads();
   float tot = 0.f;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += red[i];
   const float inv = 1.0f / sqrtf(tot / (float)K + eps);
-  for (int i = threadIdx.x; i < K; i += blockDim.x)
-    out[(size_t)b * K + i] = __float2bfloat16_rn(__bfloat162float(w[i]) * round_bf16(xr[i] * inv));
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int i = (c * 256 + tid) * 8;
+    if (i >= K) continue;
+    const float wf[8] = {bf_lo(wv[c].x), bf_hi(wv[c].x), bf_lo(wv[c].y), bf_hi(wv[c].y),
+                         bf_lo(wv[c].z), bf_hi(wv[c].z), bf_lo(wv[c].w), bf_hi(wv[c].w)};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16 lo = __float2bfloat16_rn(wf[2 * e] * round_bf16(xv[c][2 * e] * inv));
+      const __nv_bfloat16 hi = __float2bfloat16_rn(wf[2 * e + 1] * round_bf16(xv[c][2 * e + 1] * inv));
+      o[e] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+    }
+    *(uint4*)(out + (size_t)b * K + i) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // out[b, j] = bf16(silu(g) * u) with g = gu[b, j], u = gu[b, F + j]
@@ -207,8 +240,17 @@ cudaError_t launch_embed(const void* embed, int H, int V, const int32_t* tok, in
 
 cudaError_t launch_rmsnorm_rows(const float* x, const void* w, int B, int K, float eps, void* out_bf16,
                                 const Launch& L) {
-  return launch_ex(rmsnorm_rows_kernel, dim3(B), dim3(256), 0, L, x, (const __nv_bfloat16*)w, K, eps,
-                   (__nv_bfloat16*)out_bf16);
+  if (K % 8 != 0) return cudaErrorInvalidValue;
+  const int cpt = ceil_div(K / 8, 256);
+  const __nv_bfloat16* wb = (const __nv_bfloat16*)w;
+  __nv_bfloat16* ob = (__nv_bfloat16*)out_bf16;
+  switch (cpt) {
+    case 1: return launch_ex(rmsnorm_rows_kernel<1>, dim3(B), dim3(256), 0, L, x, wb, K, eps, ob);
+    case 2: return launch_ex(rmsnorm_rows_kernel<2>, dim3(B), dim3(256), 0, L, x, wb, K, eps, ob);
+    case 3: return launch_ex(rmsnorm_rows_kernel<3>, dim3(B), dim3(256), 0, L, x, wb, K, eps, ob);
+    case 4: return launch_ex(rmsnorm_rows_kernel<4>, dim3(B), dim3(256), 0, L, x, wb, K, eps, ob);
+    default: return cudaErrorInvalidValue;  // rows above 8192 are not a decode-step shape here
+  }
 }
 
 cudaError_t launch_swiglu_rows(const float* gu, int B, int F, void* out_bf16, const Launch& L) {
