@@ -206,14 +206,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int rl = warp * 32 + lane;          // this thread's row of the tile
   const int r = row0 + rl;
   bool write = ok && !s_abort;
-  if (p.splits > 1) {
-    // publish this split's partial tile [kBM rows][kBN tokens] (a thread's row is
-    // 256 contiguous bytes), take a ticket; the last split of the tile adds every
-    // partial in split order, 16 tokens at a time with all splits' loads in flight
-    const size_t tile = blockIdx.x;
-    float4* part = (float4*)(p.part + (tile * p.splits + blockIdx.y) * (size_t)(kBN * kBM) + (size_t)rl * kBN);
+  // y[n0 + j, r] (+)= o[j] for 16 tokens; the residual values are all loaded
+  // before any store, so the 16 read-modify-writes overlap instead of queueing
+  auto store_rows = [&](int n0, const float* o) {
+    float old[16];
+    if (p.epi == EPI_RESID_ADD) {
 #pragma unroll
-    for (int q = 0; q < kBN / 4; ++q) part[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int j = 0; j < 16; ++j) old[j] = n0 + j < p.B ? p.y[(size_t)(n0 + j) * p.R + r] : 0.f;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) old[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (n0 + j < p.B) p.y[(size_t)(n0 + j) * p.R + r] = p.epi == EPI_RESID_ADD ? old[j] + o[j] : o[j];
+  };
+  if (p.splits > 1) {
+    // publish this split's partial tile [kBN tokens][kBM rows] (each warp access
+    // one 128-byte line), take a ticket; the last split of the tile adds every
+    // partial in split order, 16 tokens at a time with all their loads (and the
+    // residual's) in flight together
+    const size_t tile = blockIdx.x;
+    float* part = p.part + (tile * p.splits + blockIdx.y) * (size_t)(kBN * kBM);
+#pragma unroll
+    for (int n = 0; n < kBN; ++n) part[(size_t)n * kBM + rl] = v[n];
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -223,35 +239,26 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
     __syncthreads();
     if (s_ticket == p.splits - 1 && write && r < p.R) {
-      const float4* base = (const float4*)(p.part + tile * p.splits * (size_t)(kBN * kBM) + (size_t)rl * kBN);
-      constexpr size_t kSplitStride = (size_t)kBN * kBM / 4;   // float4s per partial tile
+      const float* base = p.part + tile * p.splits * (size_t)(kBN * kBM) + rl;
+      const bool radd = p.epi == EPI_RESID_ADD;
 #pragma unroll 1
       for (int c = 0; c < kBN / 16; ++c) {
-        float4 t[kMaxSplits][4];
+        float t[kMaxSplits][16], yo[16];
 #pragma unroll
         for (int sp = 0; sp < kMaxSplits; ++sp)
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            t[sp][q] = sp < p.splits ? __ldcg(base + sp * kSplitStride + c * 4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < 16; ++j)
+            t[sp][j] = sp < p.splits ? __ldcg(base + ((size_t)sp * kBN + c * 16 + j) * kBM) : 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float4 a = t[0][q];
+        for (int j = 0; j < 16; ++j)
+          yo[j] = (radd && c * 16 + j < p.B) ? p.y[(size_t)(c * 16 + j) * p.R + r] : 0.f;
 #pragma unroll
-          for (int sp = 1; sp < kMaxSplits; ++sp) {
-            if (sp < p.splits) {
-              a.x += t[sp][q].x; a.y += t[sp][q].y; a.z += t[sp][q].z; a.w += t[sp][q].w;
-            }
-          }
-          const float o[4] = {a.x, a.y, a.z, a.w};
+        for (int j = 0; j < 16; ++j) {
+          float a = t[0][j];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int n = c * 16 + q * 4 + e;
-            if (n < p.B) {
-              float* yp = p.y + (size_t)n * p.R + r;
-              if (p.epi == EPI_RESID_ADD) *yp += o[e];
-              else *yp = o[e];
-            }
-          }
+          for (int sp = 1; sp < kMaxSplits; ++sp)
+            if (sp < p.splits) a += t[sp][j];
+          if (c * 16 + j < p.B) p.y[(size_t)(c * 16 + j) * p.R + r] = radd ? yo[j] + a : a;
         }
       }
     }
@@ -260,13 +267,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   }
   if (write && r < p.R) {
 #pragma unroll
-    for (int n = 0; n < kBN; ++n) {
-      if (n < p.B) {
-        float* yp = p.y + (size_t)n * p.R + r;
-        if (p.epi == EPI_RESID_ADD) *yp += v[n];
-        else *yp = v[n];
-      }
-    }
+    for (int c = 0; c < kBN / 16; ++c) store_rows(c * 16, v + c * 16);
   }
   tc_fence_before();
   __syncthreads();
