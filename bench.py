@@ -48,12 +48,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--no-probe", action="store_true", help="skip the dominant-kernel event probe")
-    ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "attention", "gemm_tc"],
+    ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "attention", "attention_batched",
+                                         "gemm_tc"],
                     help="time one kernel alone on a full-size shape (profiling aid) instead of the step")
     ap.add_argument("--rows", type=int, default=24576)
     ap.add_argument("--cols", type=int, default=4096)
     ap.add_argument("--ctx", type=int, default=4224)
-    ap.add_argument("--batch", type=int, default=64, help="rows of x for --kernel gemm_tc")
+    ap.add_argument("--batch", type=int, default=64,
+                    help="rows of x for --kernel gemm_tc; sequences for --kernel attention_batched")
     ap.add_argument("--act", choices=["f32", "i8"], default="f32", help="Q8_0 activation lane")
     return ap.parse_args()
 
@@ -492,6 +494,28 @@ def run_kernel(args):
         y = torch.empty((args.batch, R), device=dev)
         nbytes = R * K * 2
         fn = lambda i: api.gemv_bf16(Ws[i % copies], x, y, stream=stream)  # noqa: E731
+    elif args.kernel == "attention_batched":
+        # the batched workload's cache: `batch` sequences of 128..ctx tokens in 16-token
+        # pages through a seeded random page table
+        s = synth.QWEN3_8B
+        B, ps = args.batch, 16
+        lens = torch.randint(128, args.ctx + 1, (B,), generator=g, device=dev, dtype=torch.int64).to(torch.int32)
+        per = [-(-int(v) // ps) for v in lens.cpu()]
+        n_phys = sum(per)
+        perm = torch.randperm(n_phys, generator=g, device=dev).to(torch.int32)
+        pt = torch.zeros((B, max(per)), dtype=torch.int32, device=dev)
+        off = 0
+        for bi, npg in enumerate(per):
+            pt[bi, :npg] = perm[off:off + npg]
+            off += npg
+        kp = torch.randn((n_phys, s.n_kv_heads, ps, 128), generator=g, device=dev).to(torch.bfloat16)
+        vp = torch.randn((n_phys, s.n_kv_heads, ps, 128), generator=g, device=dev).to(torch.bfloat16)
+        q = torch.randn((B, s.n_q_heads, 128), generator=g, device=dev)
+        out = torch.empty_like(q)
+        ws = torch.zeros(api.attn_workspace_bytes(B, s.n_q_heads, s.n_kv_heads, max(per) * ps), dtype=torch.uint8,
+                         device=dev)
+        nbytes = int(lens.sum()) * s.n_kv_heads * 128 * 2 * 2
+        fn = lambda i: api.attn_decode_paged(q, kp, vp, pt, lens, 0.0884, out=out, workspace=ws, stream=stream)  # noqa
     else:
         s = synth.QWEN3_8B
         n = args.ctx

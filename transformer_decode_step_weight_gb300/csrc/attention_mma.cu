@@ -26,6 +26,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 
 namespace qd {
 namespace {
@@ -94,6 +95,13 @@ QD_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : 
 
 // byte offset of (row r, 16-byte chunk c) in a swizzled 256-byte-row tile
 QD_DEV uint32_t swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
+// the TMA form keeps each 128-byte half of the rows in its own 8 KB block, in
+// the 128-byte swizzle the copy engine writes (chunk c of row r at c ^ (r & 7))
+QD_DEV uint32_t swz_tma(int r, int c) {
+  return (uint32_t)((c >> 3) * (kT * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+template <bool TMA>
+QD_DEV uint32_t swz_t(int r, int c) { return TMA ? swz_tma(r, c) : swz(r, c); }
 
 // Issue the cp.async copies of one tile's K and V rows [t, t + kT) (rows at or
 // past t_valid_end are zero-filled, rows of the current token are skipped and
@@ -123,9 +131,57 @@ QD_DEV void load_tile(const MParams& p, int b, int g, int t, int t_valid_end, in
   }
 }
 
-template <int REP, bool FUSED, int kSt>
-__global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+QD_DEV void tma_box(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Issue the TMA copies of one tile's K and V rows [t, t + kT) as 16-row page
+// segments (two 64-column boxes each) onto `bar`; segments at or past
+// t_valid_end are not copied. The page size is a multiple of 16, so a segment
+// never crosses a page. Returns nothing; the expected bytes are set here.
+QD_DEV void load_tile_tma(const MParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int b, int g, int t,
+                          int t_valid_end, uint32_t sK, uint32_t sV, uint64_t* bar) {
+  const int ps = p.page_size;
+  const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
+  int nseg = 0;
+  int rows[kT / 16];
+#pragma unroll
+  for (int k = 0; k < kT / 16; ++k) {
+    const int tok = t + 16 * k;
+    rows[k] = -1;
+    if (tok < t_valid_end) {
+      const int lp = tok / ps;
+      int page = pt[lp];
+      if (page < 0 || page >= p.n_pages) {
+        set_error(p.err, QD_DEVERR_PAGE);
+        page = 0;
+      }
+      rows[k] = (page * p.Hkv + g) * ps + (tok - lp * ps);
+      ++nseg;
+    }
+  }
+  mbar_arrive_expect_tx(bar, (uint32_t)nseg * 4 * 16 * 128);
+#pragma unroll
+  for (int k = 0; k < kT / 16; ++k) {
+    if (rows[k] < 0) continue;
+    const uint32_t dk = sK + k * 16 * 128, dv = sV + k * 16 * 128;
+    tma_box(dk, tmK, 0, rows[k], bar);
+    tma_box(dk + kT * 128, tmK, 64, rows[k], bar);
+    tma_box(dv, tmV, 0, rows[k], bar);
+    tma_box(dv + kT * 128, tmV, 64, rows[k], bar);
+  }
+}
+
+template <int REP, bool FUSED, int kSt, bool TMA>
+__global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                       const __grid_constant__ CUtensorMap tmV, const MParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // 1024-byte alignment for the swizzled TMA boxes
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* ring = smem;                                         // kSt x (K, V) tiles
   __nv_bfloat16* sQh = (__nv_bfloat16*)(smem + kSt * 2 * kTileBytes);  // [8][128]
   __nv_bfloat16* sQl = sQh + kHP * kD;
@@ -134,6 +190,7 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
   float* sM = sQf + REP * kD;                                          // [kW][8]
   float* sL = sM + kW * kHP;                                           // [kW][8]
   float* sRed = sL + kW * kHP;                                         // scratch [4][REP + 1]
+  uint64_t* bars = (uint64_t*)(((uintptr_t)(sRed + 4 * 9) + 7) & ~(uintptr_t)7);  // TMA: full[kSt]
   __shared__ int s_ticket;
   __shared__ float s_x[kD];
 
@@ -177,10 +234,20 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
   auto tileV = [&](int st) { return ring_u + (uint32_t)(st * 2 * kTileBytes + kTileBytes); };
 
   // ---- start streaming the first tiles, then wait for and build q (and the new k, v)
+  if constexpr (TMA) {
+    if (tid == 0) {
+      for (int st = 0; st < kSt; ++st) mbar_init(&bars[st], 1);
+      fence_mbar_init();
+      for (int st = 0; st < kSt - 1 && st < n_tiles; ++st)
+        load_tile_tma(p, &tmK, &tmV, b, g, t0 + st * kT, t_end, tileK(st), tileV(st), &bars[st]);
+    }
+    __syncthreads();  // the barriers are initialised before anyone waits on them
+  } else {
 #pragma unroll
-  for (int st = 0; st < kSt - 1; ++st) {
-    if (st < n_tiles) load_tile(p, b, g, t0 + st * kT, t_end, skip_tok, tileK(st), tileV(st));
-    cp_async_commit();
+    for (int st = 0; st < kSt - 1; ++st) {
+      if (st < n_tiles) load_tile(p, b, g, t0 + st * kT, t_end, skip_tok, tileK(st), tileV(st));
+      cp_async_commit();
+    }
   }
   pdl_wait();
   const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
@@ -288,17 +355,39 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
 
   for (int it = 0; it < n_tiles; ++it) {
     const int st = it % kSt;
-    {  // keep kSt - 1 tiles in flight
-      const int nt = it + kSt - 1;
-      if (nt < n_tiles) load_tile(p, b, g, t0 + nt * kT, t_end, skip_tok, tileK(nt % kSt), tileV(nt % kSt));
-      cp_async_commit();
-    }
-    cp_async_wait<kSt - 1>();
-    __syncthreads();  // every thread's copies of this tile have landed
     const int ts = t0 + it * kT;
+    if constexpr (TMA) {
+      const int nt = it + kSt - 1;   // keep kSt - 1 tiles in flight
+      if (tid == 0 && nt < n_tiles) {
+        fence_proxy_async_smem();    // the stage's earlier reads come before the copies
+        load_tile_tma(p, &tmK, &tmV, b, g, t0 + nt * kT, t_end, tileK(nt % kSt), tileV(nt % kSt), &bars[nt % kSt]);
+      }
+      const bool got = mbar_wait_bounded(&bars[st], (uint32_t)((it / kSt) & 1), p.err);
+      if (ts + kT > t_end) {  // rows past the sequence: whole 16-row boxes may hold any bits
+        const int nv = max(0, t_end - ts);
+        unsigned char* sVg = ring + st * 2 * kTileBytes + kTileBytes;
+        for (int e = tid; e < (kT - nv) * 16; e += kTh) {
+          const int r = nv + (e >> 4), c = e & 15;
+          *(uint4*)(sVg + swz_tma(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (!__syncthreads_and(got)) {  // a copy never arrived: let the others land, then leave
+        for (int k = 1; k < kSt && it + k < n_tiles; ++k)
+          mbar_wait_bounded(&bars[(it + k) % kSt], (uint32_t)(((it + k) / kSt) & 1), p.err);
+        return;
+      }
+    } else {
+      {  // keep kSt - 1 tiles in flight
+        const int nt = it + kSt - 1;
+        if (nt < n_tiles) load_tile(p, b, g, t0 + nt * kT, t_end, skip_tok, tileK(nt % kSt), tileV(nt % kSt));
+        cp_async_commit();
+      }
+      cp_async_wait<kSt - 1>();
+      __syncthreads();  // every thread's copies of this tile have landed
+    }
     if (own_pos && pos >= ts && pos < ts + kT) {  // the current token's row, swizzled like the copies
       const int r = pos - ts;
-      const uint32_t o16 = swz(r, tid >> 3) + (uint32_t)((tid & 7) * 2);
+      const uint32_t o16 = swz_t<TMA>(r, tid >> 3) + (uint32_t)((tid & 7) * 2);
       *(__nv_bfloat16*)(ring + st * 2 * kTileBytes + o16) = __float2bfloat16_rn(k_new);
       *(__nv_bfloat16*)(ring + st * 2 * kTileBytes + kTileBytes + o16) = __float2bfloat16_rn(v_new);
       __syncthreads();
@@ -310,7 +399,7 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t a[4];
-      ldsm_x4(a, sK + swz(warp * 16 + rA, 2 * ks + cA));
+      ldsm_x4(a, sK + swz_t<TMA>(warp * 16 + rA, 2 * ks + cA));
       mma16816(sc, a, qh[ks][0], qh[ks][1]);
       mma16816(sl, a, ql[ks][0], ql[ks][1]);
     }
@@ -374,14 +463,14 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t a[4];
-      ldsm_x4_t(a, sV + swz(warp * 16 + rV, 2 * mt + cV));
+      ldsm_x4_t(a, sV + swz_t<TMA>(warp * 16 + rV, 2 * mt + cV));
       mma16816(o[mt], a, pb0h, pb1h);
       mma16816(o[mt], a, pb0l, pb1l);
     }
     __syncwarp();
     __syncthreads();  // the stage is refilled by the next iteration's copies
   }
-  cp_async_wait<0>();
+  if constexpr (!TMA) cp_async_wait<0>();
   pdl_launch_dependents();
 
   // ---- merge the four warps: O^T fragments -> [warp][head][dim] f32 (ring is idle now)
@@ -497,21 +586,50 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const MParams p) {
 }
 
 constexpr size_t smem_bytes(int rep, int kSt) {
-  return (size_t)kSt * 2 * kTileBytes + 2 * kHP * kD * 2 + (size_t)kW * 2 * kHP * 16 * 2 + (size_t)rep * kD * 4 +
-         2 * kW * kHP * 4 + 4 * 9 * 4 + 64;
+  return 1024 + (size_t)kSt * 2 * kTileBytes + 2 * kHP * kD * 2 + (size_t)kW * 2 * kHP * 16 * 2 +
+         (size_t)rep * kD * 4 + 2 * kW * kHP * 4 + 4 * 9 * 4 + 64 + (size_t)kSt * 8;
+}
+
+// QD_ATTN_TMA=0 keeps the cp.async loads on every page size.
+bool tma_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("QD_ATTN_TMA");
+    return v == nullptr || atoi(v) != 0;
+  }();
+  return on;
 }
 
 template <int REP, bool FUSED, int ST>
 cudaError_t launch_m(const MParams& p, const Launch& L) {
-  auto k = attn_mma_kernel<REP, FUSED, ST>;
+  // TMA boxes need 16-row page segments; other page sizes take the cp.async form
+  alignas(64) CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  bool tma = p.page_size % 16 == 0 && tma_enabled();
+  if (tma) {
+    const uint64_t rows = (uint64_t)p.n_pages * p.Hkv * p.page_size;
+    tma = encode_tmap_bf16_2d(&tk, p.k_pages, rows, kD, 16) == cudaSuccess &&
+          encode_tmap_bf16_2d(&tv, p.v_pages, rows, kD, 16) == cudaSuccess;
+  }
   const size_t smem = smem_bytes(REP, ST);
+  if (tma) {
+    auto k = attn_mma_kernel<REP, FUSED, ST, true>;
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    return launch_ex(k, dim3(p.n_splits, p.Hkv, p.B), dim3(kTh), smem, L, tk, tv, p);
+  }
+  auto k = attn_mma_kernel<REP, FUSED, ST, false>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(k, dim3(p.n_splits, p.Hkv, p.B), dim3(kTh), smem, L, p);
+  return launch_ex(k, dim3(p.n_splits, p.Hkv, p.B), dim3(kTh), smem, L, tk, tv, p);
 }
 
 // 2-stage ring by default: ~74 KB of shared memory leaves room on the SM for

@@ -2,6 +2,7 @@
 // programmatic-dependent-launch controls, bf16 widening, reductions.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -137,6 +138,20 @@ QD_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, int* err) {
   set_error(err, QD_DEVERR_TIMEOUT);
   return false;
 }
+
+// 2D tiled TMA load of the box at (x, y) of a tensor map into shared memory,
+// completing on `bar`; x times the element size must be a multiple of 16 bytes.
+QD_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before its
+// later async-proxy (TMA) ones.
+QD_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Global -> shared bulk copy with an L2 cache policy (same alignment rules).
 QD_DEV void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {

@@ -92,14 +92,6 @@ QD_DEV void mma_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
-QD_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // 32 TMEM lanes x 64 columns of 32 bits for this warp.
 QD_DEV void tmem_ld_32x64(uint32_t taddr, float* v) {
   uint32_t r[64];
@@ -308,6 +300,10 @@ cudaError_t encode_rowmajor_bf16(CUtensorMap* m, const void* base, uint64_t rows
 constexpr size_t kSmemTc = 1024 + (size_t)kStagesTc * (kTileA + kTileB) + (2 * kStagesTc + 1) * 8 + 16;
 
 }  // namespace
+
+cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return encode_rowmajor_bf16((CUtensorMap*)map, base, rows, cols, box_rows);
+}
 
 bool gemm_tc_supported(int R, int K, int B) { return R >= 1 && K >= kBK && K % kBK == 0 && B >= 1 && B <= kBN; }
 

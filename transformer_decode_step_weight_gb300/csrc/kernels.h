@@ -83,6 +83,9 @@ struct GemmTcArgs {
   size_t ws_bytes;        // left so); null: no split
 };
 bool gemm_tc_supported(int R, int K, int B);
+// Tensor map (CUtensorMap, 128-byte aligned storage of 128 bytes) of a row-major
+// bf16 [rows, cols] matrix: boxes of box_rows x 64 columns, 128-byte swizzle.
+cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 // K splits a launch of this shape takes, and the workspace they need.
 int gemm_tc_splits(int R, int K);
 size_t gemm_tc_workspace_bytes(int R, int K);
