@@ -33,7 +33,9 @@ namespace {
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBN = 64;         // tokens (MMA N, TMEM columns)
 constexpr int kBK = 64;         // K elements per stage (128 bytes of bf16)
-constexpr int kStagesTc = 6;
+// Ring depth: 6 stages (one CTA per SM) when the CTAs fit in one wave, else 3
+// (~74 KB, two or three CTAs per SM, so a grid of up to twice the SM count still
+// runs in one wave). QD_GEMM_STAGES = 3 or 6 forces one.
 constexpr int kTileA = kBM * kBK * 2;    // 16 KB
 constexpr int kTileB = kBN * kBK * 2;    // 8 KB
 constexpr int kThreadsTc = 128;
@@ -116,6 +118,7 @@ QD_DEV void tmem_ld_32x64(uint32_t taddr, float* v) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+template <int kStagesTc>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const TcParams p) {
@@ -297,7 +300,19 @@ cudaError_t encode_rowmajor_bf16(CUtensorMap* m, const void* base, uint64_t rows
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-constexpr size_t kSmemTc = 1024 + (size_t)kStagesTc * (kTileA + kTileB) + (2 * kStagesTc + 1) * 8 + 16;
+constexpr size_t smem_tc(int st) { return 1024 + (size_t)st * (kTileA + kTileB) + (2 * st + 1) * 8 + 16; }
+
+template <int ST>
+cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int tiles, const Launch& L) {
+  auto k = gemm_tc_kernel<ST>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tc(ST));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(k, dim3(tiles, p.splits), dim3(kThreadsTc), smem_tc(ST), L, tw, tx, p);
+}
 
 }  // namespace
 
@@ -356,12 +371,6 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   // X has B rows; the 64-row box reads zeros past them
   e = encode_rowmajor_bf16(&tx, a.X, (uint64_t)a.B, (uint64_t)a.K, kBN);
   if (e != cudaSuccess) return e;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   TcParams p = {};
   p.R = a.R; p.K = a.K; p.B = a.B; p.epi = a.epi; p.y = a.y; p.err = L.err;
   const int tiles = (a.R + kBM - 1) / kBM;
@@ -372,7 +381,12 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
     p.cnt = (int*)a.ws;
     p.part = (float*)((unsigned char*)a.ws + kTicketBytes);
   }
-  return launch_ex(gemm_tc_kernel, dim3(tiles, p.splits), dim3(kThreadsTc), kSmemTc, L, tw, tx, p);
+  static const int forced = [] {
+    const char* v = getenv("QD_GEMM_STAGES");
+    return v ? atoi(v) : 0;
+  }();
+  const bool deep = forced == 6 || (forced != 3 && (long long)tiles * p.splits <= dev_info().sm_count);
+  return deep ? launch_tc<6>(tw, tx, p, tiles, L) : launch_tc<3>(tw, tx, p, tiles, L);
 }
 
 }  // namespace qd
