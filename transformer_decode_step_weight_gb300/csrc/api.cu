@@ -121,7 +121,13 @@ static int attn_cluster_enabled() {
 // step). QD_W_EVICT_FIRST (default 1) marks GEMV weight copies evict-first in L2,
 // so the streamed weights do not push activations and caches out (measured
 // 1.7 % faster on the Qwen3-8B step).
+// QD_KV_PF_QKV = 1: the QKV GEMV fetches the layer's whole K/V cache into L2 as it
+// starts, for the attention that follows it (batch 1, one page per sequence).
+// QD_GEMV_DOWN_RING_KB / QD_GEMV_QKV_RING_KB: ring size of the down / QKV projection.
 struct StepTuning {
+  int down_ring_kb = 0;
+  int qkv_ring_kb = 0;
+  int kv_pf_qkv = 0;
   int kv_pf = 0;
   int w_evict_first = 1;
   int swiglu_in_down = 0;
@@ -142,6 +148,9 @@ static const StepTuning& step_tuning() {
     if (const char* v = getenv("QD_ATTN_TRIGGER_LOOP")) u.attn_trig_loop = atoi(v) != 0;
     if (const char* v = getenv("QD_SWIGLU_IN_DOWN")) u.swiglu_in_down = atoi(v) != 0;
     if (const char* v = getenv("QD_KV_PF")) u.kv_pf = std::max(0, std::min(2, atoi(v)));
+    if (const char* v = getenv("QD_KV_PF_QKV")) u.kv_pf_qkv = atoi(v) != 0;
+    if (const char* v = getenv("QD_GEMV_DOWN_RING_KB")) u.down_ring_kb = std::max(0, atoi(v));
+    if (const char* v = getenv("QD_GEMV_QKV_RING_KB")) u.qkv_ring_kb = std::max(0, atoi(v));
     if (const char* v = getenv("QD_W_EVICT_FIRST")) u.w_evict_first = atoi(v) != 0;
     if (const char* v = getenv("QD_GEMV_O_RING_KB")) u.o_ring_kb = std::max(0, atoi(v));
     return u;
@@ -538,6 +547,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   // projection reads 2F bytes of h instead of 8F of gate/up and recomputes nothing
   const bool swiglu_epi = !q8 && B == 1 && gemv_bf16_swiglu_ok(H) && gemv_bf16_ring_ok(F, 1) &&
                           !pft.swiglu_in_down;
+  const bool q8_swiglu_epi = q8 && B == 1 && gemv_q8_swiglu_ok(H) && gemv_q8_supported(F) && !pft.swiglu_in_down;
   // each batch-1 GEMV launch of the step owns a pair of row-claim counters
   auto claim = [&](int li, int k) { return B == 1 ? w.claims + 2 * (5 * li + k) : nullptr; };
   // head of every span of the next batch-1 BF16 GEMV (R rows of K), or nothing
@@ -553,6 +563,8 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     // QKV projection, RMSNorm(res; ln_in) fused into the prologue
     if (q8) {
       GemvQ8Args g = {};
+      g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 0);
       g.qs = (const int8_t*)l->w.w_qkv; g.d = l->w.s_qkv; g.R = QKV; g.K = H; g.act = d.act;
       g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = l->w.ln_in; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.qkv;
       QD_TRY(launch_gemv_q8(g, L), "qkv gemv q8");
@@ -560,6 +572,12 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
       g.claim = claim(li, 0);
+      g.ring_kb = pft.qkv_ring_kb;
+      if (pft.kv_pf_qkv && B == 1) {  // this layer's caches: Hkv "rows" of page_size tokens per page
+        const size_t rb = (size_t)a->page_size * D * 2;
+        g.pf_head[0] = l2_plan_rows(a->k_cache[li], a->n_pages * Hkv, rb, ~(size_t)0);
+        g.pf_head[1] = l2_plan_rows(a->v_cache[li], a->n_pages * Hkv, rb, ~(size_t)0);
+      }
       g.W = l->w.w_qkv; g.R = QKV; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
       g.norm_w = l->w.ln_in; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.qkv;
       QD_TRY(launch_gemv_bf16(g, L), "qkv gemv");
@@ -590,6 +608,8 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     // O projection + residual add
     if (q8) {
       GemvQ8Args g = {};
+      g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 1);
       g.qs = (const int8_t*)l->w.w_o; g.d = l->w.s_o; g.R = H; g.K = Hq * D; g.act = d.act;
       g.pro = PRO_X_F32; g.x = w.attn; g.epi = EPI_RESID_ADD; g.y = w.res;
       QD_TRY(launch_gemv_q8(g, L), "o gemv q8");
@@ -606,8 +626,11 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     // gate+up projection, RMSNorm(res; ln_post) fused into the prologue
     if (q8) {
       GemvQ8Args g = {};
+      g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 2);
       g.qs = (const int8_t*)l->w.w_gu; g.d = l->w.s_gu; g.R = 2 * F; g.K = H; g.act = d.act;
       g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = l->w.ln_post; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.gu;
+      if (q8_swiglu_epi) g.epi = EPI_SWIGLU;  // y = f32 silu(gate) * up [F]
       QD_TRY(launch_gemv_q8(g, L), "gu gemv q8");
     } else {
       GemvBf16Args g = {};
@@ -624,13 +647,17 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     // down projection with SwiGLU formed on load, + residual add
     if (q8) {
       GemvQ8Args g = {};
+      g.w_evict_first = pft.w_evict_first;
+      g.claim = claim(li, 3);
       g.qs = (const int8_t*)l->w.w_down; g.d = l->w.s_down; g.R = H; g.K = F; g.act = d.act;
       g.pro = PRO_SWIGLU; g.x = w.gu; g.epi = EPI_RESID_ADD; g.y = w.res;
+      if (q8_swiglu_epi) g.pro = PRO_X_F32;  // the gate+up epilogue already formed silu(g) * u
       QD_TRY(launch_gemv_q8(g, L), "down gemv q8");
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
       g.claim = claim(li, 3);
+      g.ring_kb = pft.down_ring_kb;
       g.W = l->w.w_down; g.R = H; g.K = F; g.batch = B; g.pro = PRO_SWIGLU; g.x = w.gu;
       g.epi = EPI_RESID_ADD; g.y = w.res;
       if (swiglu_epi) { g.pro = PRO_X_BF16; g.x = w.xn; }
@@ -642,6 +669,8 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   // final RMSNorm + LM head
   if (a->lm_head_scales) {
     GemvQ8Args g = {};
+    g.w_evict_first = pft.w_evict_first;
+    g.claim = claim(a->n_layers, 0);
     g.qs = (const int8_t*)a->lm_head; g.d = a->lm_head_scales; g.R = a->vocab; g.K = H; g.act = a->lm_act;
     g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = a->final_norm; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = a->logits;
     QD_TRY(launch_gemv_q8(g, L), "lm head q8");

@@ -827,7 +827,10 @@ static bool attn_use_mma(const AttnArgs& a) {
 
 cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   if (attn_use_mma(a) && !(a.qkv && a.use_cluster > 1))
-    return launch_attention_mma(a, attn_chunk_mma(a.max_ctx), slots_cap(a.B, a.Hkv, a.max_ctx), L);
+    return launch_attention_mma(a,
+                                (long long)a.B * a.Hkv >= dev_info().sm_count ? attn_chunk_mma(a.max_ctx)
+                                                                               : attn_chunk(a.B, a.Hkv, a.max_ctx),
+                                slots_cap(a.B, a.Hkv, a.max_ctx), L);
   AttnParams p = {};
   const int rep = a.Hq / a.Hkv;
   p.q = a.q;

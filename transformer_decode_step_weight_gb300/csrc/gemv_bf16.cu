@@ -308,6 +308,7 @@ struct RingParams {
   int pair_F;                 // EPI_SWIGLU: F (rows of each half); the partition is over pairs
   __nv_bfloat16* y_bf16;      // EPI_SWIGLU output [F]
   int w_evict_first;          // weight copies marked evict-first in L2
+  L2Prefetch pf_head[2];      // fetched into L2 as the kernel starts
   int* claim;                 // null: static partition; else [claim, done] counters (zero at launch)
   int static_per_cta;         // units each CTA streams before claiming from the pool
 };
@@ -361,6 +362,9 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingPara
   if (!p.trig_late) pdl_launch_dependents();
 
   if (tid >= kCons) {  // ---- producer warp: weights only, so no dependency wait
+    // data a later kernel reads soon (e.g. the attention's cached K/V): into L2 first
+    l2_prefetch_spans(p.pf_head[0], blockIdx.x, gridDim.x, lane);
+    l2_prefetch_spans(p.pf_head[1], blockIdx.x, gridDim.x, lane);
     if (lane == 0) {
       const unsigned char* W = (const unsigned char*)p.W;
       const uint64_t pol = policy_evict_first();
@@ -713,6 +717,8 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
     p.pro = a.pro; p.x = a.x; p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps;
     p.epi = a.epi; p.y = a.y; p.err = L.err; p.trig_late = L.trig_late;
     p.pf = a.pf;
+    p.pf_head[0] = a.pf_head[0];
+    p.pf_head[1] = a.pf_head[1];
     p.w_evict_first = a.w_evict_first;
     if (a.claim && tu.dyn_pct > 0) {  // static share, then claimed chunks
       p.claim = a.claim;

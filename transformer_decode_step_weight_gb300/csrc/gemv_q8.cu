@@ -22,6 +22,7 @@
 #include "launch.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace qd {
 namespace {
@@ -334,6 +335,10 @@ struct RingQ8Params {
   float* y;
   int* err;
   int trig_late;
+  int pair_F;            // EPI_SWIGLU: rows of each half; units are (gate j, up F + j) pairs
+  int w_evict_first;
+  int* claim;            // null: static split; else [claim, done] counters
+  int static_per_cta;
 };
 
 QD_DEV void cons_sync_q() { asm volatile("bar.sync 1, %0;" ::"n"(kConsQ) : "memory"); }
@@ -347,15 +352,32 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
   unsigned char* ring = smem;
   uint64_t* full = (uint64_t*)(smem + p.ring_bytes);
   uint64_t* empty = full + 16;
-  float* red = (float*)(empty + 16);  // [kPhaseQ][wpg]
+  int* st_u0 = (int*)(empty + 16);              // [16] first unit of each stage's chunk
+  int* st_n = st_u0 + 16;                       // [16] units in it (0: no more work)
+  float* red = (float*)(st_n + 16);             // [kPhaseQ][wpg]
+  float* rsum = red + kPhaseQ * (p.T / 32);     // [kPhaseQ] EPI_SWIGLU: gate/up sums by pair slot
+  int* rid = (int*)(rsum + kPhaseQ);            // [kPhaseQ] destination of each phase row
+  int* pid = rid + kPhaseQ;                     // [kPhaseQ / 2] EPI_SWIGLU: pair of each pair slot
   __shared__ float s_ss[kConsQ / 32];
 
   const int tid = threadIdx.x, lane = tid & 31;
   const int K = p.K, KB = K / 32, KC = K / 16, ns = p.ns;
-  const int nrows = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
-  const int r0 = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
+  const bool pair = p.epi == EPI_SWIGLU;
+  // units: rows, or under EPI_SWIGLU (gate row j, up row F + j) pairs; static share
+  // first, then (with a claim counter) stages of the pool [pool0, units)
+  const int upr = pair ? 2 : 1;
   const int srows = p.P * RPS;
-  const int n_stages = (nrows + srows - 1) / srows;
+  const int cu = srows / upr;
+  const int units = pair ? p.pair_F : p.R;
+  int u_s, n_s;
+  if (p.claim) {
+    u_s = (int)blockIdx.x * p.static_per_cta;
+    n_s = p.static_per_cta;
+  } else {
+    n_s = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
+    u_s = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
+  }
+  const int pool0 = p.claim ? p.static_per_cta * (int)gridDim.x : units;
   const size_t qrow = (size_t)K, drow = (size_t)KB * 2;   // bytes per row of values / scales
   const size_t dbase = (size_t)srows * qrow;               // scales follow the values in a stage
 
@@ -371,17 +393,63 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
 
   if (tid >= kConsQ) {  // ---- producer warp: weights only
     if (lane == 0) {
-      for (int i = 0; i < n_stages; ++i) {
+      const uint64_t pol = policy_evict_first();
+      auto copy = [&](void* d, const void* g, uint32_t n, uint64_t* bar) {
+        if (p.w_evict_first) bulk_g2s_hint(d, g, n, bar, pol);
+        else bulk_g2s(d, g, n, bar);
+      };
+      const unsigned char* Q = (const unsigned char*)p.qs;
+      const unsigned char* D = (const unsigned char*)p.d;
+      int u = u_s;
+      const int u_end = u_s + n_s;
+      int next = p.claim ? pool0 + atomicAdd(p.claim, cu) : units;  // claimed one chunk ahead
+      bool ok = true;
+      int i = 0;
+      for (;; ++i) {
+        int c0, cn;
+        if (u < u_end) {
+          c0 = u;
+          cn = min(cu, u_end - u);
+          u += cn;
+        } else {
+          if (next >= units) break;
+          c0 = next;
+          cn = min(cu, units - c0);
+          next = pool0 + atomicAdd(p.claim, cu);
+        }
         const int slot = i % ns;
-        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) return;
-        const int rows_i = min(srows, nrows - i * srows);
-        const size_t row = (size_t)r0 + (size_t)i * srows;
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)(rows_i * (qrow + drow)));
+        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) {
+          ok = false;
+          break;
+        }
+        st_u0[slot] = c0;
+        st_n[slot] = cn;
         unsigned char* st = ring + (size_t)slot * p.stage_bytes;
-        bulk_g2s(st, p.qs + row * qrow, (uint32_t)(rows_i * qrow), &full[slot]);
-        bulk_g2s(st + dbase, (const unsigned char*)p.d + row * drow, (uint32_t)(rows_i * drow), &full[slot]);
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)((size_t)cn * upr * (qrow + drow)));
+        copy(st, Q + (size_t)c0 * qrow, (uint32_t)(cn * qrow), &full[slot]);
+        copy(st + dbase, D + (size_t)c0 * drow, (uint32_t)(cn * drow), &full[slot]);
+        if (pair) {
+          const size_t up = (size_t)p.pair_F + c0;
+          copy(st + (size_t)cn * qrow, Q + up * qrow, (uint32_t)(cn * qrow), &full[slot]);
+          copy(st + dbase + (size_t)cn * drow, D + up * drow, (uint32_t)(cn * drow), &full[slot]);
+        }
+      }
+      if (ok) {  // end marker: a stage of no units
+        const int slot = i % ns;
+        if (i < ns || mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) {
+          st_n[slot] = 0;
+          mbar_arrive_q(&full[slot]);
+        }
+      }
+      if (p.claim) {  // the last producer to stop claiming resets the counters
+        __threadfence();
+        if (atomicAdd(p.claim + 1, 1) == (int)gridDim.x - 1) {
+          atomicExch(p.claim, 0);
+          atomicExch(p.claim + 1, 0);
+        }
       }
     }
+    __syncwarp();
     pdl_launch_dependents();
     return;
   }
@@ -505,18 +573,41 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
     }
   }
 
-  int ph_base = 0;
-  for (int i = 0; i < n_stages; ++i) {
+  int ph_n = 0, pp_n = 0;  // rows and (EPI_SWIGLU) pairs of the current phase
+  auto flush = [&]() {
+    cons_sync_q();
+    for (int r = tid; r < ph_n; r += kConsQ) {
+      float acc = 0.f;
+      for (int k = 0; k < wpg; ++k) acc += red[r * wpg + k];
+      if (pair) {
+        rsum[rid[r]] = acc;
+      } else {
+        float* yp = p.y + rid[r];
+        if (p.epi == EPI_RESID_ADD) *yp += acc;
+        else *yp = acc;
+      }
+    }
+    cons_sync_q();
+    if (pair) {  // SwiGLU of the phase's pairs (f32, the value the down projection quantises)
+      for (int q = tid; q < pp_n; q += kConsQ) p.y[pid[q]] = silu(rsum[2 * q]) * rsum[2 * q + 1];
+      cons_sync_q();
+    }
+    ph_n = 0;
+    pp_n = 0;
+  };
+  for (int i = 0;; ++i) {
     const int slot = i % ns;
     if (!mbar_wait_bounded(&full[slot], (uint32_t)((i / ns) & 1), p.err)) {
-      for (int k = 1; k < ns && i + k < n_stages; ++k)
+      for (int k = 1; k < ns; ++k)  // let copies still in flight land before the CTA leaves
         mbar_wait_bounded(&full[(i + k) % ns], (uint32_t)(((i + k) / ns) & 1), p.err);
       return;
     }
-    if (i + 1 == n_stages) pdl_launch_dependents();
-    const int row0 = i * srows + g * RPS;
+    const int c0 = st_u0[slot], cn = st_n[slot];
+    if (cn == 0) break;
+    const int svalid = cn * upr;                        // valid rows of the stage
+    const int row0 = g * RPS;                           // this group's first row of the stage
     const unsigned char* st = ring + (size_t)slot * p.stage_bytes;
-    const int nv = min(RPS, nrows - row0);
+    const int nv = min(RPS, svalid - row0);
     uint4 wv[RPS][C];
     float dw[RPS][C];
 #pragma unroll
@@ -524,7 +615,7 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
 #pragma unroll
       for (int j = 0; j < C; ++j) {
         const bool ok = r < nv && cv[j];
-        const size_t lr = (size_t)(g * RPS + r);
+        const size_t lr = (size_t)(row0 + r);
         wv[r][j] = ok ? *(const uint4*)(st + lr * qrow + (size_t)ch[j] * 16) : make_uint4(0u, 0u, 0u, 0u);
         dw[r][j] = ok ? __half2float(*(const __half*)(st + dbase + lr * drow + (size_t)(ch[j] >> 1) * 2)) : 0.f;
       }
@@ -577,22 +668,23 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
       }
     }
     constexpr int kLowMask = 32 / RPS - 1;
-    if ((lane & kLowMask) == 0 && rsel < nv) red[(row0 + rsel - ph_base) * wpg + wig] = v[0];
-    const int done = min((i + 1) * srows, nrows);
-    if (done + srows - ph_base > kPhaseQ || i + 1 == n_stages) {
-      const int nph = done - ph_base;
-      cons_sync_q();
-      for (int r = tid; r < nph; r += kConsQ) {
-        float acc = 0.f;
-        for (int k = 0; k < wpg; ++k) acc += red[r * wpg + k];
-        float* yp = p.y + r0 + ph_base + r;
-        if (p.epi == EPI_RESID_ADD) *yp += acc;
-        else *yp = acc;
+    if ((lane & kLowMask) == 0 && rsel < nv) red[(ph_n + row0 + rsel) * wpg + wig] = v[0];
+    if (tid < svalid) {  // destinations of the stage's rows
+      if (pair) {
+        const bool up_row = tid >= cn;
+        const int q = up_row ? tid - cn : tid;
+        rid[ph_n + tid] = 2 * (pp_n + q) + (up_row ? 1 : 0);
+        if (!up_row) pid[pp_n + q] = c0 + q;
+      } else {
+        rid[ph_n + tid] = c0 + tid;
       }
-      cons_sync_q();
-      ph_base = done;
     }
+    ph_n += svalid;
+    pp_n += pair ? cn : 0;
+    if (ph_n + srows > kPhaseQ) flush();  // the next stage might not fit
   }
+  if (p.trig_late) pdl_launch_dependents();
+  flush();
 }
 
 template <int C, int LANE>
@@ -609,6 +701,15 @@ cudaError_t launch_ring_q(const RingQ8Params& p, int grid, size_t smem, const La
   return launch_ex(k, dim3(grid), dim3(kConsQ + 32), smem, L, p);
 }
 
+// percent of a step GEMV's units claimed from the shared pool (QD_GEMV_DYN_PCT, as the BF16 ring)
+int q8_dyn_pct() {
+  static const int v = [] {
+    const char* e = getenv("QD_GEMV_DYN_PCT");
+    return e ? std::max(0, std::min(100, atoi(e))) : 15;
+  }();
+  return v;
+}
+
 int ring_q_c(int K) {
   const int chunks = K / 16;
   static const int opts[] = {1, 2, 3, 4};
@@ -621,6 +722,11 @@ int ring_q_c(int K) {
 
 bool gemv_q8_supported(int K) { return K > 0 && K % 32 == 0 && pick_c(K) > 0; }
 
+bool gemv_q8_swiglu_ok(int K) {
+  const int rc = K % 256 == 0 ? ring_q_c(K) : 0;
+  return rc >= 1;  // every ring form has RPS >= 2, so a stage holds whole gate/up pairs
+}
+
 cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
   const bool aligned = (((uintptr_t)a.qs | (uintptr_t)a.d) & 15) == 0;
   const int rc = (a.K % 256 == 0 && aligned) ? ring_q_c(a.K) : 0;
@@ -628,8 +734,18 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
     const int rps = rc == 1 ? 8 : rc == 2 ? 4 : 2;   // must match launch_ring_q
     RingQ8Params p = {};
     p.qs = a.qs; p.d = (const __half*)a.d; p.R = a.R; p.K = a.K;
-    const int grid = std::max(1, std::min(a.R, dev_info().sm_count));
-    p.rows_base = a.R / grid; p.rows_extra = a.R % grid;
+    const bool pair = a.epi == EPI_SWIGLU;
+    const int units = pair ? a.R / 2 : a.R;   // rows, or gate/up pairs
+    const int grid = std::max(1, std::min(units, dev_info().sm_count));
+    p.rows_base = units / grid; p.rows_extra = units % grid;
+    p.pair_F = pair ? a.R / 2 : 0;
+    if (pair && (std::max(1, kConsQ / std::min(kConsQ, ((ceil_div(a.K / 16, rc) + 31) / 32) * 32)) * rps) % 2 != 0)
+      return cudaErrorInvalidValue;  // a stage holds whole pairs
+    p.w_evict_first = a.w_evict_first;
+    if (a.claim && q8_dyn_pct() > 0) {
+      p.claim = a.claim;
+      p.static_per_cta = (int)(((long long)units * (100 - q8_dyn_pct())) / (100LL * grid));
+    }
     p.T = std::min(kConsQ, ((ceil_div(a.K / 16, rc) + 31) / 32) * 32);
     p.P = std::max(1, kConsQ / p.T);
     const size_t row_bytes = (size_t)a.K + (size_t)a.K / 16;
@@ -640,7 +756,8 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
     if (a.act == 1 && a.xq != nullptr) p.pro = PRO_Q8_GIVEN;
     p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps; p.epi = a.epi; p.y = a.y;
     p.err = L.err; p.trig_late = L.trig_late;
-    size_t smem = (size_t)p.ring_bytes + 32 * 8 + (size_t)kPhaseQ * (p.T / 32) * 4;
+    size_t smem = (size_t)p.ring_bytes + 32 * 8 + 32 * 4 + (size_t)kPhaseQ * (p.T / 32) * 4 +
+                  (size_t)kPhaseQ * 4 * 2 + (size_t)kPhaseQ / 2 * 4;
     smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
     if ((size_t)p.ns * p.stage_bytes <= (size_t)kRingQ * 2) {
       switch (rc) {
@@ -651,6 +768,7 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
       }
     }
   }
+  if (a.epi == EPI_SWIGLU) return cudaErrorInvalidValue;  // the ring form only
   const int C = pick_c(a.K);
   const int KC = a.K / 16;
   const int T = std::min(kThreads, ((ceil_div(KC, C) + 31) / 32) * 32);

@@ -61,6 +61,7 @@ struct GemvBf16Args {
   int ring_kb;            // batch-1 ring form: ring size in KB (0: the default)
   void* y_bf16;           // EPI_SWIGLU: bf16 [R / 2]
   int w_evict_first;      // batch-1 ring form: weight copies marked evict-first in L2
+  L2Prefetch pf_head[2];  // batch-1 ring form: fetched into L2 as the kernel starts (zero: none)
   int* claim;             // batch-1 ring form: two ints, zero before the launch and left
                           // zero after it; part of the rows is then claimed by whichever
                           // CTA is free (null: static split of the rows)
@@ -108,10 +109,14 @@ struct GemvQ8Args {
   const void* xd;         // f16 [K/32]
   const void* norm_w;
   float eps;
-  int epi;
+  int epi;               // GemvEpi; EPI_SWIGLU (ring form): y = f32 silu(gate) * up [R / 2]
   float* y;
+  int w_evict_first;      // ring form: weight copies marked evict-first in L2
+  int* claim;             // ring form: two zero ints; part of the rows is claimed by free CTAs
 };
 bool gemv_q8_supported(int K);
+// True when a Q8_0 GEMV of K columns takes the ring form and can take EPI_SWIGLU.
+bool gemv_q8_swiglu_ok(int K);
 cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L);
 cudaError_t launch_quantize_q8(const float* x, int n, int8_t* xq, void* xd, const Launch& L);
 cudaError_t launch_q8_block_dots(const int8_t* qs, int R, int K, const int8_t* xq, int32_t* dots,
