@@ -203,6 +203,28 @@ def test_attention_parity(cuda_lib, B, hq, hkv, lens, ps, paged):
     assert api.check_device_error() == 0
 
 
+@pytest.mark.parametrize("ps,with_empty", [(16, False), (32, True), (8, False)])
+def test_attention_parity_tensor_core_form(cuda_lib, ps, with_empty):
+    """20 sequences x 8 kv heads (at least one CTA per SM) take the tensor-core form:
+    1024-token splits, K/V by 2D TMA when the page size is a multiple of 16 (16, 32),
+    by 16-byte cp.async otherwise (8). Lengths cross split, tile and page edges."""
+    g = torch.Generator().manual_seed(ps)
+    lens = [int(v) for v in torch.randint(1, 2600, (20,), generator=g)]
+    lens[3], lens[7], lens[11] = 1024, 1025, 63
+    if with_empty:
+        lens[5] = 0
+    q, kp, vp, pt, sl = _attn_case(20, 32, 8, lens, ps, 900 + ps, True)
+    out = api.attn_decode_paged(q, kp, vp, pt, sl, 1 / math.sqrt(128))
+    ref = _attn_ref(q, kp, vp, pt, lens)
+    got = out.cpu().numpy()
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert np.all(got[b] == 0)
+        else:
+            assert rel_max_abs(got[b], ref[b]) < 1e-5, (b, n)
+    assert api.check_device_error() == 0
+
+
 def test_attention_page_permutation_is_bitwise_invariant(cuda_lib):
     # same logical cache through a permuted page table == identity table over permuted data
     lens = [300, 77]
