@@ -272,7 +272,7 @@ def run_ours(args, dist, rank, world, local):
         out = {
             "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.wtype == "bf16" else "q8_0/f32",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.wtype == "bf16" else ("q8_0/i8" if args.act == "i8" else "q8_0/f32"),
             "data": "synthetic",
             "config": {"workload": wl.name, "description": wl.description, "global_batch": dec.batch * world,
                        "q8_lane": args.act if wl.wtype == "q8_0" else None,
