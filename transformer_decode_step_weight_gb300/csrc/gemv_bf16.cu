@@ -720,7 +720,10 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
     p.pf_head[0] = a.pf_head[0];
     p.pf_head[1] = a.pf_head[1];
     p.w_evict_first = a.w_evict_first;
-    if (a.claim && tu.dyn_pct > 0) {  // static share, then claimed chunks
+    // static share, then claimed chunks -- only when a chunk (one stage) is small
+    // against a CTA's share: with a few stages per CTA, whoever wins a pooled chunk
+    // does much more than the rest (measured slower on Qwen3-0.6B shapes)
+    if (a.claim && tu.dyn_pct > 0 && units / grid >= 8 * ((p.P * rps) / (pair ? 2 : 1))) {
       p.claim = a.claim;
       p.static_per_cta = (int)(((long long)units * (100 - tu.dyn_pct)) / (100LL * grid));
     }

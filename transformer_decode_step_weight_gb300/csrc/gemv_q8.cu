@@ -742,7 +742,9 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
     if (pair && (std::max(1, kConsQ / std::min(kConsQ, ((ceil_div(a.K / 16, rc) + 31) / 32) * 32)) * rps) % 2 != 0)
       return cudaErrorInvalidValue;  // a stage holds whole pairs
     p.w_evict_first = a.w_evict_first;
-    if (a.claim && q8_dyn_pct() > 0) {
+    const int cu_q = (std::max(1, kConsQ / std::min(kConsQ, ((ceil_div(a.K / 16, rc) + 31) / 32) * 32)) * rps) /
+                     (pair ? 2 : 1);
+    if (a.claim && q8_dyn_pct() > 0 && units / grid >= 8 * cu_q) {  // as the BF16 ring: small chunks only
       p.claim = a.claim;
       p.static_per_cta = (int)(((long long)units * (100 - q8_dyn_pct())) / (100LL * grid));
     }
