@@ -255,6 +255,10 @@ def run_ours(args, dist, rank, world, local):
     hbm_peak, peak_kind = peaks()
     step_gbs = sum(step_bytes) / (ms / 1e3) / 1e9
 
+    # ---- a pure-read streaming peak on this GPU (a 4 GiB reduction), for the third
+    # denominator of the step's fraction (the others: the measured copy peak, 8 TB/s)
+    read_peak = measure_read_peak(dev, stream)
+
     # ---- dominant kernel: the BF16 GEMV, every launch of one token, events on its stream
     roof = None if (args.no_probe or wl.batch > 8 or wl.wtype != "bf16") else dominant_kernel_roofline(api, mt, s, stream, hbm_peak,
                                                                                  peak_kind)
@@ -283,11 +287,36 @@ def run_ours(args, dist, rank, world, local):
             "roofline": roof,
             "step_roofline": {"bound": "hbm", "achieved": round(step_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                               "frac": round(step_gbs / hbm_peak, 4), "peak_kind": peak_kind,
+                              "frac_of_nominal_8tbs": round(step_gbs / 8000.0, 4),
+                              "read_peak_gbs": read_peak,
+                              "frac_of_read_peak": round(step_gbs / read_peak, 4) if read_peak else None,
                               "bytes_per_step": int(sum(step_bytes) / K)},
             "e2e": e2e, "gpu_launches": launches, "clocks": clk, "cpu_baseline": cpu,
         }
         print(json.dumps(out), flush=True)
     dec.close()
+
+
+def measure_read_peak(dev, stream, gib=4, reps=5):
+    """Pure-read HBM bandwidth: best of `reps` sums over a `gib` GiB f32 buffer (read once
+    per sum, far larger than L2), timed with CUDA events on `stream`. None if it cannot run."""
+    try:
+        buf = torch.ones(gib * (1 << 28), dtype=torch.float32, device=dev)
+        best = None
+        with torch.cuda.stream(stream):
+            buf.sum()
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                buf.sum()
+                e1.record(stream)
+                e1.synchronize()
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None or ms < best else best
+        del buf
+        return round(gib * (1 << 30) / (best / 1e3) / 1e9, 1)
+    except Exception:
+        return None
 
 
 def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):

@@ -819,6 +819,19 @@ static int attn_chunk_mma(int max_ctx) {
   return chunk;
 }
 
+// Tensor-core form at small batch (forced by QD_ATTN_IMPL=mma): the CUDA-core form's
+// split, or QD_ATTN_MMA_SMALL_CHUNK tokens (a multiple of 64).
+static int attn_chunk_mma_small(const AttnArgs& a) {
+  static const int forced = [] {
+    const char* v = getenv("QD_ATTN_MMA_SMALL_CHUNK");
+    return v ? atoi(v) : 0;
+  }();
+  if (forced <= 0) return attn_chunk(a.B, a.Hkv, a.max_ctx);
+  int chunk = std::max(kTile, (forced / kTile) * kTile);
+  while ((a.max_ctx + chunk - 1) / chunk > kMaxSplits) chunk += kTile;
+  return chunk;
+}
+
 static bool attn_use_mma(const AttnArgs& a) {
   const int f = attn_impl_forced();
   if (f) return f == 2;
@@ -829,7 +842,7 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   if (attn_use_mma(a) && !(a.qkv && a.use_cluster > 1))
     return launch_attention_mma(a,
                                 (long long)a.B * a.Hkv >= dev_info().sm_count ? attn_chunk_mma(a.max_ctx)
-                                                                               : attn_chunk(a.B, a.Hkv, a.max_ctx),
+                                                                               : attn_chunk_mma_small(a),
                                 slots_cap(a.B, a.Hkv, a.max_ctx), L);
   AttnParams p = {};
   const int rep = a.Hq / a.Hkv;
