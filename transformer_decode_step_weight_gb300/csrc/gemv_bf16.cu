@@ -308,9 +308,6 @@ struct RingParams {
   int pair_F;                 // EPI_SWIGLU: F (rows of each half); the partition is over pairs
   __nv_bfloat16* y_bf16;      // EPI_SWIGLU output [F]
   int w_evict_first;          // weight copies marked evict-first in L2
-  L2Prefetch pf_head[2];      // fetched into L2 as the kernel starts
-  int* claim;                 // null: static partition; else [claim, done] counters (zero at launch)
-  int static_per_cta;         // units each CTA streams before claiming from the pool
 };
 
 QD_DEV void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
@@ -321,34 +318,20 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingPara
   unsigned char* ring = smem;
   uint64_t* full = (uint64_t*)(smem + p.ring_bytes);
   uint64_t* empty = full + 16;
-  int* st_u0 = (int*)(empty + 16);              // [16] first unit of each stage's chunk
-  int* st_n = st_u0 + 16;                       // [16] units in it (0: no more work)
-  float* red = (float*)(st_n + 16);             // [kPhaseRows][wpg] per-warp row partials
-  float* rsum = red + kPhaseRows * (p.T / 32);  // [kPhaseRows] EPI_SWIGLU: gate/up sums by pair slot
-  int* rid = (int*)(rsum + kPhaseRows);         // [kPhaseRows] destination of each phase row
-  int* pid = rid + kPhaseRows;                  // [kPhaseRows / 2] EPI_SWIGLU: pair of each pair slot
+  float* red = (float*)(empty + 16);            // [kPhaseRows][wpg]
+  float* s_pair = red + kPhaseRows * (p.T / 32);  // EPI_SWIGLU: row sums [2 * npair]
   __shared__ float s_ss[kCons / 32];
 
   const int tid = threadIdx.x, lane = tid & 31;
   const int K = p.K, ns = p.ns;
   const bool pair = p.epi == EPI_SWIGLU;
-  // A unit is a weight row, or under EPI_SWIGLU a (gate row j, up row F + j) pair;
-  // a stage holds cu units. Each CTA streams its static share first; with a claim
-  // counter the remaining units [pool0, units) are taken one stage at a time by
-  // whichever CTA gets there first, which evens out CTAs that DRAM serves slower.
-  const int upr = pair ? 2 : 1;
-  const int stage_rows = p.P * RPS;
-  const int cu = stage_rows / upr;
-  const int units = pair ? p.pair_F : p.R;
-  int u_s, n_s;
-  if (p.claim) {
-    u_s = (int)blockIdx.x * p.static_per_cta;
-    n_s = p.static_per_cta;
-  } else {
-    n_s = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
-    u_s = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
-  }
-  const int pool0 = p.claim ? p.static_per_cta * (int)gridDim.x : units;
+  // r0: first row (first pair under EPI_SWIGLU); local rows [0, npair) are gate rows
+  // r0.., local rows [npair, 2 npair) the up rows F + r0..
+  const int nown = p.rows_base + ((int)blockIdx.x < p.rows_extra ? 1 : 0);
+  const int npair = pair ? nown : 0;
+  const int nrows = pair ? 2 * nown : nown;
+  const int r0 = (int)blockIdx.x * p.rows_base + min((int)blockIdx.x, p.rows_extra);
+  const int n_stages = (nrows + p.P * RPS - 1) / (p.P * RPS);
   const size_t row_bytes = (size_t)K * 2;
 
   if (tid == 0) {
@@ -362,61 +345,31 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingPara
   if (!p.trig_late) pdl_launch_dependents();
 
   if (tid >= kCons) {  // ---- producer warp: weights only, so no dependency wait
-    // data a later kernel reads soon (e.g. the attention's cached K/V): into L2 first
-    l2_prefetch_spans(p.pf_head[0], blockIdx.x, gridDim.x, lane);
-    l2_prefetch_spans(p.pf_head[1], blockIdx.x, gridDim.x, lane);
     if (lane == 0) {
-      const unsigned char* W = (const unsigned char*)p.W;
+      const unsigned char* src = (const unsigned char*)(p.W + (size_t)r0 * K);
+      // EPI_SWIGLU: local row lr >= npair is weight row F + r0 + (lr - npair)
+      const unsigned char* src_up = pair ? (const unsigned char*)(p.W + ((size_t)p.pair_F + r0) * K) : src;
       const uint64_t pol = policy_evict_first();
       auto copy = [&](void* d, const void* g, uint32_t n, uint64_t* bar) {
         if (p.w_evict_first) bulk_g2s_hint(d, g, n, bar, pol);
         else bulk_g2s(d, g, n, bar);
       };
-      int u = u_s;
-      const int u_end = u_s + n_s;
-      // the next pooled chunk is claimed one chunk ahead, so the atomic's round
-      // trip overlaps the wait for a free stage
-      int next = p.claim ? pool0 + atomicAdd(p.claim, cu) : units;
-      bool ok = true;
-      int i = 0;
-      for (;; ++i) {
-        int c0, cn;
-        if (u < u_end) {
-          c0 = u;
-          cn = min(cu, u_end - u);
-          u += cn;
-        } else {
-          if (next >= units) break;
-          c0 = next;
-          cn = min(cu, units - c0);
-          next = pool0 + atomicAdd(p.claim, cu);
-        }
+      for (int i = 0; i < n_stages; ++i) {
         const int slot = i % ns;
-        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) {
-          ok = false;
-          break;
-        }
-        st_u0[slot] = c0;
-        st_n[slot] = cn;
+        if (i >= ns && !mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) break;
+        const int srows = p.P * RPS;
+        const int a = i * srows;
+        const int rows_i = min(srows, nrows - a);
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)(rows_i * row_bytes));
         unsigned char* dst = ring + (size_t)slot * p.stage_bytes;
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)((size_t)cn * upr * row_bytes));
-        copy(dst, W + (size_t)c0 * row_bytes, (uint32_t)(cn * row_bytes), &full[slot]);
-        if (pair)
-          copy(dst + (size_t)cn * row_bytes, W + ((size_t)p.pair_F + c0) * row_bytes, (uint32_t)(cn * row_bytes),
-               &full[slot]);
-      }
-      if (ok) {  // end marker: a stage of no units
-        const int slot = i % ns;
-        if (i < ns || mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) {
-          st_n[slot] = 0;
-          mbar_arrive(&full[slot]);
-        }
-      }
-      if (p.claim) {  // the last producer to stop claiming resets the counters for the next launch
-        __threadfence();
-        if (atomicAdd(p.claim + 1, 1) == (int)gridDim.x - 1) {
-          atomicExch(p.claim, 0);
-          atomicExch(p.claim + 1, 0);
+        if (!pair) {
+          copy(dst, src + (size_t)a * row_bytes, (uint32_t)(rows_i * row_bytes), &full[slot]);
+        } else {  // the stage may straddle the gate/up boundary: one copy per half
+          const int na = max(0, min(a + rows_i, npair) - a);   // gate rows in this stage
+          if (na > 0) copy(dst, src + (size_t)a * row_bytes, (uint32_t)(na * row_bytes), &full[slot]);
+          if (rows_i > na)
+            copy(dst + (size_t)na * row_bytes, src_up + (size_t)(a + na - npair) * row_bytes,
+                     (uint32_t)((rows_i - na) * row_bytes), &full[slot]);
         }
       }
     }
@@ -513,45 +466,20 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingPara
     }
   }
 
-  // stage = P groups x RPS rows; group g owns rows [g*RPS, g*RPS + RPS) of every stage.
-  // A phase collects up to kPhaseRows rows (their per-warp partials in red and
-  // their destinations in rid) before one reduction over the warps.
-  int ph_n = 0, pp_n = 0;  // rows and (EPI_SWIGLU) pairs of the current phase
-  auto flush = [&]() {
-    cons_sync();
-    for (int r = tid; r < ph_n; r += kCons) {
-      float acc = 0.f;
-      for (int k = 0; k < wpg; ++k) acc += red[r * wpg + k];
-      if (pair) {
-        rsum[rid[r]] = acc;
-      } else {
-        float* yp = p.y + rid[r];
-        if (p.epi == EPI_RESID_ADD) *yp += acc;
-        else *yp = acc;
-      }
-    }
-    cons_sync();
-    if (pair) {  // SwiGLU of the phase's pairs
-      for (int q = tid; q < pp_n; q += kCons)
-        p.y_bf16[pid[q]] = __float2bfloat16_rn(silu(rsum[2 * q]) * rsum[2 * q + 1]);
-      cons_sync();
-    }
-    ph_n = 0;
-    pp_n = 0;
-  };
-  for (int i = 0;; ++i) {
+  // stage = P groups x RPS rows; group g owns rows [g*RPS, g*RPS + RPS) of every stage
+  const int stage_rows = P * RPS;
+  int ph_base = 0;  // first local row of the current reduction phase
+  for (int i = 0; i < n_stages; ++i) {
     const int slot = i % ns;
     if (!mbar_wait_bounded(&full[slot], (uint32_t)((i / ns) & 1), p.err)) {
-      for (int k = 1; k < ns; ++k)  // let copies still in flight land before the CTA leaves
+      for (int k = 1; k < ns && i + k < n_stages; ++k)
         mbar_wait_bounded(&full[(i + k) % ns], (uint32_t)(((i + k) / ns) & 1), p.err);
       return;
     }
-    const int c0 = st_u0[slot], cn = st_n[slot];
-    if (cn == 0) break;
-    const int srows = cn * upr;                         // valid rows of the stage
-    const int row0 = g * RPS;                           // this group's first row of the stage
-    const unsigned char* base = ring + (size_t)slot * p.stage_bytes + (size_t)row0 * row_bytes;
-    const int nv = min(RPS, srows - row0);              // valid rows of the group (may be <= 0)
+    if (i + 1 == n_stages) pdl_launch_dependents();
+    const int row0 = i * stage_rows + g * RPS;          // local row of this group's first row
+    const unsigned char* base = ring + (size_t)slot * p.stage_bytes + (size_t)g * RPS * row_bytes;
+    const int nv = min(RPS, nrows - row0);              // valid rows of the group (may be <= 0)
     uint4 w[RPS][C];
 #pragma unroll
     for (int r = 0; r < RPS; ++r)
@@ -589,23 +517,31 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_ring_kernel(const RingPara
       }
     }
     constexpr int kLowMask = 32 / RPS - 1;              // lanes below the halving levels
-    if ((lane & kLowMask) == 0 && rsel < nv) red[(ph_n + row0 + rsel) * wpg + wig] = v[0];
-    if (tid < srows) {  // destinations of the stage's rows
-      if (pair) {
-        const bool up_row = tid >= cn;
-        const int q = up_row ? tid - cn : tid;
-        rid[ph_n + tid] = 2 * (pp_n + q) + (up_row ? 1 : 0);
-        if (!up_row) pid[pp_n + q] = c0 + q;
-      } else {
-        rid[ph_n + tid] = c0 + tid;
+    if ((lane & kLowMask) == 0 && rsel < nv)
+      red[(row0 + rsel - ph_base) * wpg + wig] = v[0];
+    const int done = min((i + 1) * stage_rows, nrows);
+    if (done + stage_rows - ph_base > kPhaseRows || i + 1 == n_stages) {  // the next stage would not fit
+      const int nph = done - ph_base;
+      cons_sync();
+      for (int r = tid; r < nph; r += kCons) {
+        float acc = 0.f;
+        for (int k = 0; k < wpg; ++k) acc += red[r * wpg + k];
+        if (pair) {
+          s_pair[ph_base + r] = acc;
+        } else {
+          float* yp = p.y + r0 + ph_base + r;
+          if (p.epi == EPI_RESID_ADD) *yp += acc;
+          else *yp = acc;
+        }
       }
+      cons_sync();
+      ph_base = done;
     }
-    ph_n += srows;
-    pp_n += pair ? cn : 0;
-    if (ph_n + stage_rows > kPhaseRows) flush();  // the next stage might not fit
   }
-  if (p.trig_late) pdl_launch_dependents();
-  flush();
+  if (pair) {  // SwiGLU of the CTA's pairs (the last flush ended with a barrier)
+    for (int j = tid; j < npair; j += kCons)
+      p.y_bf16[r0 + j] = __float2bfloat16_rn(silu(s_pair[j]) * s_pair[npair + j]);
+  }
 }
 
 template <int C>
@@ -649,12 +585,9 @@ static int ring_c(int K) {
 // QD_GEMV_RING_KB /
 // QD_GEMV_SMEM_PAD_KB override the ring size / add padding (tuning);
 // QD_GEMV_RING=0 selects the register-streaming kernel.
-// QD_GEMV_DYN_PCT: percent of the units claimed from a shared pool (when the
-// caller gives a claim counter) instead of being split statically.
 struct RingTuning {
-  int enabled = 1, ring_kb = 128, pad_kb = 0, dyn_pct = 15;
+  int enabled = 1, ring_kb = 128, pad_kb = 0;
   RingTuning() {
-    if (const char* v = getenv("QD_GEMV_DYN_PCT")) dyn_pct = std::max(0, std::min(100, atoi(v)));
     if (const char* v = getenv("QD_GEMV_RING")) enabled = atoi(v) != 0;
     if (const char* v = getenv("QD_GEMV_SMEM_PAD_KB")) pad_kb = std::max(0, std::min(64, atoi(v)));
     if (const char* v = getenv("QD_GEMV_RING_KB")) ring_kb = std::max(16, std::min(kRingMax / 1024, atoi(v)));
@@ -711,24 +644,14 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
     const int rps = rc == 1 ? 8 : rc == 2 ? 4 : rc <= 4 ? 2 : 1;     // must match launch_ring_c
     p.rps = rps;
     p.stage_bytes = ((p.P * rps * row_bytes + 127) / 128) * 128;
-    if (pair && (p.P * rps) % 2 != 0) return cudaErrorInvalidValue;  // a stage holds whole pairs
     p.ns = std::max(2, std::min(16, ring_bytes / p.stage_bytes));
     p.ring_bytes = p.ns * p.stage_bytes;
     p.pro = a.pro; p.x = a.x; p.norm_w = (const __nv_bfloat16*)a.norm_w; p.eps = a.eps;
     p.epi = a.epi; p.y = a.y; p.err = L.err; p.trig_late = L.trig_late;
     p.pf = a.pf;
-    p.pf_head[0] = a.pf_head[0];
-    p.pf_head[1] = a.pf_head[1];
     p.w_evict_first = a.w_evict_first;
-    // static share, then claimed chunks -- only when a chunk (one stage) is small
-    // against a CTA's share: with a few stages per CTA, whoever wins a pooled chunk
-    // does much more than the rest (measured slower on Qwen3-0.6B shapes)
-    if (a.claim && tu.dyn_pct > 0 && units / grid >= 8 * ((p.P * rps) / (pair ? 2 : 1))) {
-      p.claim = a.claim;
-      p.static_per_cta = (int)(((long long)units * (100 - tu.dyn_pct)) / (100LL * grid));
-    }
-    size_t smem = (size_t)p.ring_bytes + 32 * 8 + 32 * 4 + (size_t)kPhaseRows * (p.T / 32) * 4 +
-                  (size_t)kPhaseRows * 4 * 2 + (size_t)kPhaseRows / 2 * 4 + (size_t)tu.pad_kb * 1024;
+    size_t smem = (size_t)p.ring_bytes + 32 * 8 + (size_t)kPhaseRows * (p.T / 32) * 4 + (size_t)tu.pad_kb * 1024;
+    if (pair) smem += (size_t)2 * (p.rows_base + 1) * 4;
     if (smem > (size_t)dev_info().max_smem_optin - 1024) return cudaErrorInvalidValue;
     smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
     switch (rc) {

@@ -434,6 +434,10 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
           copy(st + dbase + (size_t)cn * drow, D + up * drow, (uint32_t)(cn * drow), &full[slot]);
         }
       }
+      // Every copy of this CTA is issued: let the next kernel launch now (its weight
+      // stream starts before its dependency wait). The end marker below may have to
+      // wait for a free stage, and the trigger must not wait with it.
+      pdl_launch_dependents();
       if (ok) {  // end marker: a stage of no units
         const int slot = i % ns;
         if (i < ns || mbar_wait_bounded(&empty[slot], (uint32_t)(((i / ns) - 1) & 1), p.err)) {
