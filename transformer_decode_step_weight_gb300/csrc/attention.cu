@@ -44,11 +44,10 @@ constexpr int kTile = 64;
 // K/V ring depth: 3 stages by default; QD_ATTN_SIMT_STAGES = 2..4 (4 puts a whole
 // 256-token split in flight before the dependency wait).
 constexpr int kMaxStages = 4;
-// 512 threads (16 warps) per CTA, 256 when 8 q heads share a kv head (register
-// budget). 256 threads for every REP (so a CTA fits beside a GEMV CTA and
-// prefetches during the projection) measured slower on the Qwen3-8B step:
-// 296 vs 304 tok/s.
-__host__ __device__ constexpr int threads_for(int rep) { return rep >= 8 ? 256 : 512; }
+// 256 threads (8 warps) per CTA, with about two CTAs per SM (attn_chunk): on the
+// Qwen3-8B step 338.0 vs 335.3 tok/s against 512 threads and one CTA per SM, on
+// Qwen3-0.6B 1447 vs 1281 (same box).
+__host__ __device__ constexpr int threads_for(int rep) { return 256; }
 constexpr int kMaxSplits = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -763,13 +762,14 @@ int pick_cluster(int B, int Hkv, int max_cl) {
 
 }  // namespace
 
-// Tokens per split: about one CTA per SM at small batch (fewer partials for
-// the combine), a single split per sequence once batch x kv heads fills the
-// GPU, never more than kMaxSplits.
+// Tokens per split: about two CTAs per SM at small batch (256-thread CTAs, two fit
+// on an SM; fewer partials for the combine than more splits would give), a single
+// split per sequence once batch x kv heads fills the GPU twice, never more than
+// kMaxSplits.
 int attn_chunk(int B, int Hkv, int max_ctx) {
   const int sms = dev_info().sm_count;
   const int pairs = std::max(1, B * Hkv);
-  const int want = std::max(1, (sms + pairs - 1) / pairs);
+  const int want = std::max(1, (2 * sms + pairs - 1) / pairs);
   int chunk = (max_ctx + want - 1) / want;
   chunk = std::max(kTile, ((chunk + kTile - 1) / kTile) * kTile);
   while ((max_ctx + chunk - 1) / chunk > kMaxSplits) chunk += kTile;
