@@ -123,13 +123,10 @@ static int attn_cluster_enabled() {
 // step). QD_W_EVICT_FIRST (default 1) marks GEMV weight copies evict-first in L2,
 // so the streamed weights do not push activations and caches out (measured
 // 1.7 % faster on the Qwen3-8B step).
-// QD_KV_PF_QKV = 1: the QKV GEMV fetches the layer's whole K/V cache into L2 as it
-// starts, for the attention that follows it (batch 1, one page per sequence).
 // QD_GEMV_DOWN_RING_KB / QD_GEMV_QKV_RING_KB: ring size of the down / QKV projection.
 struct StepTuning {
   int down_ring_kb = 0;
   int qkv_ring_kb = 0;
-  int kv_pf_qkv = 0;
   int kv_pf = 0;
   int w_evict_first = 1;
   int swiglu_in_down = 0;
@@ -150,7 +147,6 @@ static const StepTuning& step_tuning() {
     if (const char* v = getenv("QD_ATTN_TRIGGER_LOOP")) u.attn_trig_loop = atoi(v) != 0;
     if (const char* v = getenv("QD_SWIGLU_IN_DOWN")) u.swiglu_in_down = atoi(v) != 0;
     if (const char* v = getenv("QD_KV_PF")) u.kv_pf = std::max(0, std::min(2, atoi(v)));
-    if (const char* v = getenv("QD_KV_PF_QKV")) u.kv_pf_qkv = atoi(v) != 0;
     if (const char* v = getenv("QD_GEMV_DOWN_RING_KB")) u.down_ring_kb = std::max(0, atoi(v));
     if (const char* v = getenv("QD_GEMV_QKV_RING_KB")) u.qkv_ring_kb = std::max(0, atoi(v));
     if (const char* v = getenv("QD_W_EVICT_FIRST")) u.w_evict_first = atoi(v) != 0;
@@ -402,7 +398,7 @@ struct StepWs {
   void* xn;         // bf16 [B, max(H, F)]: normed / SwiGLU activations (batched path)
   void* attn_ws;
   void* argmax_ws;
-  int* claims;      // [5 L + 1][2] row-claim counters of the batch-1 GEMVs (zero between launches)
+  int* claims;      // [5 L + 1][2] row-claim counters of the batch-1 Q8_0 GEMVs (zero between launches)
   void* gemm_ws;    // batched path: split-K partials and tickets (one GEMM at a time)
   size_t gemm_ws_bytes;
   size_t total;
@@ -550,7 +546,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   const bool swiglu_epi = !q8 && B == 1 && gemv_bf16_swiglu_ok(H) && gemv_bf16_ring_ok(F, 1) &&
                           !pft.swiglu_in_down;
   const bool q8_swiglu_epi = q8 && B == 1 && gemv_q8_swiglu_ok(H) && gemv_q8_supported(F) && !pft.swiglu_in_down;
-  // each batch-1 GEMV launch of the step owns a pair of row-claim counters
+  // each batch-1 Q8_0 GEMV launch of the step owns a pair of row-claim counters
   auto claim = [&](int li, int k) { return B == 1 ? w.claims + 2 * (5 * li + k) : nullptr; };
   // head of every span of the next batch-1 BF16 GEMV (R rows of K), or nothing
   auto tail_plan = [&](const void* Wn, int R, int K) {
@@ -573,13 +569,7 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
-      g.claim = claim(li, 0);
       g.ring_kb = pft.qkv_ring_kb;
-      if (pft.kv_pf_qkv && B == 1) {  // this layer's caches: Hkv "rows" of page_size tokens per page
-        const size_t rb = (size_t)a->page_size * D * 2;
-        g.pf_head[0] = l2_plan_rows(a->k_cache[li], a->n_pages * Hkv, rb, ~(size_t)0);
-        g.pf_head[1] = l2_plan_rows(a->v_cache[li], a->n_pages * Hkv, rb, ~(size_t)0);
-      }
       g.W = l->w.w_qkv; g.R = QKV; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
       g.norm_w = l->w.ln_in; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.qkv;
       QD_TRY(launch_gemv_bf16(g, L), "qkv gemv");
@@ -618,7 +608,6 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
-      g.claim = claim(li, 1);
       g.W = l->w.w_o; g.R = H; g.K = Hq * D; g.batch = B; g.pro = PRO_X_BF16; g.x = w.attn;
       g.epi = EPI_RESID_ADD; g.y = w.res;
       g.pf = tail_plan(l->w.w_gu, 2 * F, H);
@@ -637,7 +626,6 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
-      g.claim = claim(li, 2);
       g.W = l->w.w_gu; g.R = 2 * F; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
       g.norm_w = l->w.ln_post; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = w.gu;
       if (swiglu_epi) {  // h = bf16(silu(gate) * up) formed in the epilogue, into xn
@@ -658,7 +646,6 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
     } else {
       GemvBf16Args g = {};
       g.w_evict_first = pft.w_evict_first;
-      g.claim = claim(li, 3);
       g.ring_kb = pft.down_ring_kb;
       g.W = l->w.w_down; g.R = H; g.K = F; g.batch = B; g.pro = PRO_SWIGLU; g.x = w.gu;
       g.epi = EPI_RESID_ADD; g.y = w.res;
@@ -679,7 +666,6 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   } else {
     GemvBf16Args g = {};
     g.w_evict_first = pft.w_evict_first;
-    g.claim = claim(a->n_layers, 0);
     g.W = a->lm_head; g.R = a->vocab; g.K = H; g.batch = B; g.pro = PRO_RMSNORM; g.x = w.res;
     g.norm_w = a->final_norm; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = a->logits;
     QD_TRY(launch_gemv_bf16(g, L), "lm head");

@@ -61,10 +61,6 @@ struct GemvBf16Args {
   int ring_kb;            // batch-1 ring form: ring size in KB (0: the default)
   void* y_bf16;           // EPI_SWIGLU: bf16 [R / 2]
   int w_evict_first;      // batch-1 ring form: weight copies marked evict-first in L2
-  L2Prefetch pf_head[2];  // batch-1 ring form: fetched into L2 as the kernel starts (zero: none)
-  int* claim;             // batch-1 ring form: two ints, zero before the launch and left
-                          // zero after it; part of the rows is then claimed by whichever
-                          // CTA is free (null: static split of the rows)
 };
 bool gemv_bf16_supported(int K, int batch);
 // True when a batch-1 GEMV of K columns takes the ring form, and when that form
