@@ -30,7 +30,9 @@ Readings where those pages are silent (each also listed in the design notes):
     h // (Hq / Hkv).
   * SwiGLU: silu(g) * u with silu(g) = g / (1 + exp(-g)); the concatenated
     gate+up matrix holds the F gate rows first, then the F up rows.
-  * Q8_0: per row, K/32 blocks, w = f32(d) * q with q int8 and d fp16.
+  * Q8_0: per row, K/32 blocks, w = f32(d) * q with q int8 and d fp16. The
+    batched (tensor-core) step widens each weight to bf16 first:
+    w = bf16(f32(d) * q), one round-to-nearest-even of the exact product.
     Activation re-quantisation per 32-block: amax = max|x|, d = amax / 127,
     id = 1 / d (0 when d == 0), q = round-half-away-from-zero(x * id), all in
     IEEE binary32, d stored as fp16 (round to nearest even).
@@ -202,6 +204,17 @@ def q8_0_dequant(qs, d_bits) -> np.ndarray:
     return (qs.reshape(r, k // QK8_0, QK8_0) * d[:, :, None]).reshape(r, k)
 
 
+def q8_0_widen_bf16(qs, d_bits) -> np.ndarray:
+    """Each Q8_0 weight rounded once to bfloat16: W[r, k] = bf16(f32(d[r, k // 32]) * q[r, k]).
+
+    The batched projections run on bf16 tensor cores, so each weight is widened
+    to bf16 before the contraction. q has at most 8 significant bits and d (fp16)
+    at most 11, so the product is exact in binary32 and in float64; the one
+    rounding is round-to-nearest-even of the exact product.
+    """
+    return round_bf16(q8_0_dequant(qs, d_bits))
+
+
 def q8_0_quantize(x_f32):
     """Per-32-block int8 re-quantisation of a binary32 activation vector.
 
@@ -239,6 +252,8 @@ def gemv_q8_0(qs, d_bits, x=None, xq=None, xd_bits=None, act: str = "f32",
 
     act == "f32": y_r = sum_b f32(d_rb) * sum_i q_rbi * x_bi   (dequantising lane)
     act == "i8":  y_r = sum_b f32(d_rb) * f32(dx_b) * sum_i q_rbi * xq_bi  (dp4a lane)
+    act == "w_bf16": y_r = sum_k bf16(f32(d_rb) * q_rk) * x_k  (tensor-core lane of the
+                  batched step: weights widened to bf16, x the bf16 activation)
     """
     qs = np.asarray(qs, dtype=np.int8)
     r, k = qs.shape
@@ -254,6 +269,11 @@ def gemv_q8_0(qs, d_bits, x=None, xq=None, xd_bits=None, act: str = "f32",
             dots = q8_0_block_dots(qs[r0:r0 + row_chunk], xq).astype(np.float64)
             dw = f16_to_f64(np.asarray(d_bits)[r0:r0 + row_chunk])
             y[r0:r0 + row_chunk] = (dots * dw * dx[None, :]).sum(axis=1)
+    elif act == "w_bf16":
+        x = np.asarray(x, dtype=np.float64)
+        for r0 in range(0, r, row_chunk):
+            y[r0:r0 + row_chunk] = q8_0_widen_bf16(qs[r0:r0 + row_chunk],
+                                                   np.asarray(d_bits)[r0:r0 + row_chunk]) @ x
     else:
         raise ValueError(act)
     return y
@@ -346,6 +366,7 @@ def _project(w, s, x, act: str, mode: str):
     act == "bf16": W bf16, x already in its storage precision.
     act == "f32":  Q8_0 dequantising lane (x binary32).
     act == "i8":   Q8_0 dp4a lane: x re-quantised per 32-block first.
+    act == "w_bf16": Q8_0 weights widened to bf16, x bf16 (batched tensor-core step).
     """
     if act == "bf16":
         return gemv_bf16(w, x)
@@ -354,6 +375,8 @@ def _project(w, s, x, act: str, mode: str):
     if act == "i8":
         xq, xd = q8_0_quantize(np.asarray(x, dtype=np.float64).astype(np.float32))
         return gemv_q8_0(w, s, xq=xq, xd_bits=xd, act="i8")
+    if act == "w_bf16":
+        return gemv_q8_0(w, s, x=x, act="w_bf16")
     raise ValueError(act)
 
 

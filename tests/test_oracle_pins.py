@@ -273,6 +273,68 @@ def test_q8_0_lanes_brute_force_and_unit_scale_exact():
     assert dots[2, 1] == sum(int(qs[2, 32 + i]) * int(xq[32 + i]) for i in range(32))
 
 
+def _golden_widen():
+    rows = []
+    with open(os.path.join(GOLDEN, "q8_0_widen_bf16_hand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                q, d, w = line.split()
+                rows.append((int(q), int(d, 16), int(w, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("q,d,w", _golden_widen())
+def test_q8_0_widen_bf16_hand_cases(q, d, w):
+    got = oracle.f64_to_bf16_bits(oracle.q8_0_widen_bf16(np.full((1, 32), q, dtype=np.int8),
+                                                         np.array([[d]], dtype=np.uint16)))
+    assert np.all(got == w), (hex(int(got[0, 0])), hex(w))
+
+
+def _bf16_rne_exact(v):
+    """Round a Fraction to 8 significant bits, ties to even, in exact rational arithmetic."""
+    from fractions import Fraction
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    scale = Fraction(2) ** (7 - e)          # a * scale lies in [128, 256)
+    m = a * scale
+    lo = m.numerator // m.denominator
+    rem = m - lo
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2 == 1):
+        lo += 1
+    return (lo / scale) * (1 if v > 0 else -1)
+
+
+def test_q8_0_widened_lane_brute_force_and_power_of_two_scales():
+    from fractions import Fraction
+    rng = np.random.default_rng(12)
+    R, K = 5, 96
+    qs = rng.integers(-128, 128, size=(R, K)).astype(np.int8)
+    d = (np.abs(rng.standard_normal((R, K // 32))) * 0.01).astype(np.float16).view(np.uint16)
+    x = rng.integers(-8, 9, size=K).astype(np.float64)
+    y = oracle.gemv_q8_0(qs, d, x=x, act="w_bf16")
+    rounded = 0
+    for r in range(R):
+        tot = Fraction(0)
+        for k in range(K):
+            exact = Fraction(float(d[r, k // 32].view(np.float16))) * int(qs[r, k])
+            w = _bf16_rne_exact(exact)
+            rounded += w != exact
+            tot += w * int(x[k])
+        assert y[r] == pytest.approx(float(tot), rel=1e-13, abs=1e-13)
+    assert rounded > R * K // 2        # the random scales do make most weights round
+    # power-of-two scales: widening is exact, so the lane equals the dequantising lane
+    p2 = np.array([0x3C00, 0x3800, 0x4000], dtype=np.uint16)[rng.integers(0, 3, (R, K // 32))]
+    np.testing.assert_array_equal(oracle.gemv_q8_0(qs, p2, x=x, act="w_bf16"),
+                                  oracle.gemv_q8_0(qs, p2, x=x, act="f32"))
+
+
 def test_q8_0_dequant_layout():
     qs = np.arange(-32, 32, dtype=np.int8).reshape(1, 64)
     d = np.array([[0x3C00, 0x4000]], dtype=np.uint16)      # 1.0, 2.0
