@@ -43,21 +43,32 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3-8b-bf16",
-                    choices=["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-bf16-paged-b64"])
+                    choices=["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-bf16-paged-b64",
+                             "qwen3-8b-q8_0-paged-b64"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--no-probe", action="store_true", help="skip the dominant-kernel event probe")
     ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "attention", "attention_batched",
-                                         "gemm_tc"],
+                                         "gemm_tc", "gemm_q8"],
                     help="time one kernel alone on a full-size shape (profiling aid) instead of the step")
     ap.add_argument("--rows", type=int, default=24576)
     ap.add_argument("--cols", type=int, default=4096)
     ap.add_argument("--ctx", type=int, default=4224)
     ap.add_argument("--batch", type=int, default=64,
                     help="rows of x for --kernel gemm_tc; sequences for --kernel attention_batched")
-    ap.add_argument("--act", choices=["f32", "i8"], default="f32", help="Q8_0 activation lane")
+    ap.add_argument("--act", choices=["f32", "i8"], default="f32", help="Q8_0 activation lane (batch 1)")
+    ap.add_argument("--deq", type=int, choices=[0, 1, 2],
+                    help="Q8_0 lanes by level: 0 = dp4a everywhere, 1 = dp4a in the layers and f32 activations for "
+                         "the LM head, 2 = f32 activations everywhere (overrides --act)")
     return ap.parse_args()
+
+
+def q8_lanes(args):
+    """(layer lane, LM-head lane) names of the Q8_0 batch-1 GEMVs."""
+    if args.deq is not None:
+        return ("i8", "i8") if args.deq == 0 else (("i8", "f32") if args.deq == 1 else ("f32", "f32"))
+    return args.act, args.act
 
 
 def dist_setup(args):
@@ -206,8 +217,10 @@ def run_ours(args, dist, rank, world, local):
     run_len = wl.steps
     mt = synth.make_model(s, wl.wtype, args.seed + rank, dev, batch=wl.batch, ctx=None if wl.paged else wl.ctx,
                           steps=run_len, paged=wl.paged)
-    lane = api.QD_ACT_I8 if args.act == "i8" else api.QD_ACT_F32
-    dec = api.Decoder(mt, max_steps=run_len, act=lane, device=dev)
+    act, lm_act = q8_lanes(args)
+    lane = api.QD_ACT_I8 if act == "i8" else api.QD_ACT_F32
+    lm_lane = api.QD_ACT_I8 if lm_act == "i8" else api.QD_ACT_F32
+    dec = api.Decoder(mt, max_steps=run_len, act=lane, lm_act=lm_lane, device=dev)
     lens = [int(v) for v in mt.seq_lens.cpu()]
     tok0, pos0 = dec.tok.clone(), dec.pos.clone()
 
@@ -276,10 +289,10 @@ def run_ours(args, dist, rank, world, local):
         out = {
             "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms_max / K, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.wtype == "bf16" else ("q8_0/i8" if args.act == "i8" else "q8_0/f32"),
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(wl, act, lm_act),
             "data": "synthetic",
             "config": {"workload": wl.name, "description": wl.description, "global_batch": dec.batch * world,
-                       "q8_lane": args.act if wl.wtype == "q8_0" else None,
+                       "q8_lane": q8_lane_label(wl, act, lm_act),
                        "ctx_start": wl.ctx if not wl.paged else "uniform[128,4096]", "decode_run_steps": run_len,
                        "parallelism": f"replicas x{world}",
                        "graph": "one CUDA graph per step, PDL between kernels",
@@ -295,6 +308,23 @@ def run_ours(args, dist, rank, world, local):
         }
         print(json.dumps(out), flush=True)
     dec.close()
+
+
+def dtype_label(wl, act, lm_act):
+    """The arithmetic the step computes in: bf16 MMA / FMA, or the Q8_0 lanes."""
+    if wl.wtype == "bf16":
+        return "bf16"
+    if wl.batch > 1:
+        return "q8_0->bf16"          # weights widened on chip, bf16 tensor-core MMA
+    return f"q8_0/{act}" if act == lm_act else f"q8_0/{act}+head_{lm_act}"
+
+
+def q8_lane_label(wl, act, lm_act):
+    if wl.wtype != "q8_0":
+        return None
+    if wl.batch > 1:
+        return "weights widened to bf16 on chip (tensor cores)"
+    return act if act == lm_act else f"{act} (LM head {lm_act})"
 
 
 def measure_read_peak(dev, stream, gib=4, reps=5):
@@ -415,7 +445,10 @@ def cpu_baseline(mt, s, wl, ctx, n_layers_sample: int = 8):
     rows = np.arange(0, s.vocab, int(round(1 / frac)))
     idx = torch.as_tensor(rows, device=mt.lm_head.device)
     lm_bits = synth.bits_u16(mt.lm_head[idx]) if mt.lm_head_scales is None else None
-    mode, act = ("bf16", "bf16") if mt.wtype == "bf16" else ("f32", "f32")
+    if mt.wtype == "bf16":
+        mode, act = "bf16", "bf16"
+    else:  # the Q8_0 lane the GPU step runs at this batch
+        mode, act = ("bf16", "w_bf16") if wl.batch > 1 else ("f32", "f32")
     fn = synth.bits_u16(mt.final_norm)
     t0 = time.perf_counter()
     res = x0
@@ -425,7 +458,7 @@ def cpu_baseline(mt, s, wl, ctx, n_layers_sample: int = 8):
     if mt.lm_head_scales is None:
         oracle.gemv_bf16(lm_bits, xf)
     else:
-        oracle.gemv_q8_0(synth.host_i8(mt.lm_head[idx]), synth.bits_u16(mt.lm_head_scales[idx]), x=xf, act="f32")
+        oracle.gemv_q8_0(synth.host_i8(mt.lm_head[idx]), synth.bits_u16(mt.lm_head_scales[idx]), x=xf, act=act)
     dt = time.perf_counter() - t0
     sec_per_tok = dt / frac
     return {"value": round(1.0 / sec_per_tok, 5), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
@@ -462,13 +495,23 @@ def run_reference(args, dist, rank, world, local):
     ks, vs = oracle_caches(mt, 0, wl.ctx + 1)
     x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[0])]))
     rows = np.arange(0, s.vocab, s.n_layers)
-    lm_bits = synth.bits_u16(mt.lm_head[torch.as_tensor(rows, device=mt.lm_head.device)])
+    idx = torch.as_tensor(rows, device=mt.lm_head.device)
+    if wl.wtype == "bf16":
+        mode, act = "bf16", "bf16"
+        lm, lms = synth.bits_u16(mt.lm_head[idx]), None
+    else:  # the Q8_0 lane the GPU step runs at the workload's batch
+        mode, act = ("bf16", "w_bf16") if wl.batch > 1 else ("f32", q8_lanes(args)[0])
+        lm, lms = synth.host_i8(mt.lm_head[idx]), synth.bits_u16(mt.lm_head_scales[idx])
     fn = oracle.bf16_to_f64(synth.bits_u16(mt.final_norm))
     del mt
 
     def one():
-        r = oracle.layer_step(od, ol, x0, ks[0], vs[0], wl.ctx, mode="bf16", act="bf16")
-        oracle.gemv_bf16(lm_bits, oracle.rmsnorm(r, fn, s.rms_eps, "bf16"))
+        r = oracle.layer_step(od, ol, x0, ks[0], vs[0], wl.ctx, mode=mode, act=act)
+        xf = oracle.rmsnorm(r, fn, s.rms_eps, mode)
+        if lms is None:
+            oracle.gemv_bf16(lm, xf)
+        else:
+            oracle._project(lm, lms, xf, act, mode)
 
     for _ in range(args.warmup):
         one()
@@ -523,6 +566,17 @@ def run_kernel(args):
         y = torch.empty((args.batch, R), device=dev)
         nbytes = R * K * 2
         fn = lambda i: api.gemv_bf16(Ws[i % copies], x, y, stream=stream)  # noqa: E731
+    elif args.kernel == "gemm_q8":
+        qs = [torch.randint(-127, 128, (R, K), generator=g, device=dev, dtype=torch.int16).to(torch.int8)
+              for _ in range(copies)]
+        ds = [(torch.randn((R, K // 32), generator=g, device=dev).abs() * 0.002).to(torch.float16)
+              for _ in range(copies)]
+        x = torch.randn((args.batch, K), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((args.batch, R), device=dev)
+        nb = api.gemm_workspace_bytes(R, K)
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=dev) if nb else None
+        nbytes = R * K + R * (K // 32) * 2
+        fn = lambda i: api.gemm_q8_0(qs[i % copies], ds[i % copies], x, y=y, workspace=ws, stream=stream)  # noqa
     elif args.kernel == "attention_batched":
         # the batched workload's cache: `batch` sequences of 128..ctx tokens in 16-token
         # pages through a seeded random page table

@@ -103,6 +103,23 @@ int qd_gemv_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols,
                  const float* x_f32, const int8_t* x_q, const void* x_d_f16,
                  qd_act act, float* y, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Batched Q8_0 projection on the tcgen05 tensor cores ("qwen3-8b-rtx4080-     */
+/* cutedsl" README, "Baseline tiled GEMM"; Q8_0 blocks per [EQ-SPEED]):          */
+/*   y[b, r] = sum_c bf16(f32(d[r, c/32]) * qs[r, c]) * x[b, c]                  */
+/* Each weight is widened on chip to bf16 (the product is exact in binary32,     */
+/* then one round to nearest even) and the contraction runs as bf16 MMA with f32 */
+/* accumulation. qs: int8 [rows, cols]; d: f16 [rows, cols/32]; x: bf16          */
+/* [batch, cols]; y: f32 [batch, rows]. workspace: NULL (no K split) or device   */
+/* scratch of qd_gemm_workspace_bytes(rows, cols, QD_W_Q8_0) bytes, zero-filled  */
+/* before its first use (each call leaves it zero-filled); with it, grids that   */
+/* do not fill the SMs split K and sum the partials in split order.              */
+/* Limits: cols % 256 == 0, 1 <= batch <= 64, every pointer 16-byte aligned.     */
+size_t qd_gemm_workspace_bytes(int rows, int cols, qd_wtype wtype);
+int qd_gemm_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const void* x_bf16,
+                 int batch, float* y, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
 /* Activation re-quantisation per 32-block ([EQ-SPEED] item 3): amax = max|x|,  */
 /* d = amax / 127, q = round-half-away(x * (1/d)) in IEEE binary32 (0 if d = 0), */
 /* d stored as f16 (round to nearest even). x: f32 [n]; x_q: int8 [n];            */
@@ -211,8 +228,11 @@ int qd_destroy_layer(qd_layer* layer);
 /* rope_table: from qd_rope_table_init with max_pos >= every position reached.  */
 /* logits: f32 [batch, vocab] device output. workspace: device scratch of        */
 /* qd_step_workspace_bytes(args) bytes, zero-filled before first use.           */
-/* batch <= 8 runs the GEMV path (BF16 or Q8_0; Q8_0 at batch 1); 9..64 (BF16)   */
-/* runs every projection as a tcgen05 GEMM over the batch (dims % 64 == 0).      */
+/* BF16 layers: batch <= 8 runs the GEMV path; 9..64 runs every projection as a  */
+/* tcgen05 GEMM over the batch (dims % 64 == 0). Q8_0 layers: batch 1 runs the   */
+/* Q8_0 GEMV lanes (act, lm_act); 2..64 runs the tcgen05 GEMMs with the weights  */
+/* widened to bf16 as in qd_gemm_q8_0 (act and lm_act unused; dims % 256 == 0,   */
+/* scales 16-byte aligned).                                                     */
 typedef struct {
   const qd_layer* const* layers;
   int n_layers;

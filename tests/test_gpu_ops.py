@@ -146,6 +146,53 @@ def test_gemv_q8_0_unit_scales_integer_exact(cuda_lib):
     assert torch.equal(y.cpu().double(), ref)
 
 
+@pytest.mark.parametrize("R,K,B,split", [(128, 256, 2, False), (300, 768, 17, False), (1000, 1536, 64, True),
+                                         (6144, 4096, 64, True), (4096, 12288, 64, True),
+                                         (151936, 4096, 64, False)])
+def test_gemm_q8_0_tensor_cores(cuda_lib, R, K, B, split):
+    # Q8_0 weights widened to bf16 on chip: ragged last 128-row tile, batch below 64,
+    # K split across CTAs (partials summed in split order) where the grid is small
+    qs, d = _q8(R, K, R + 5)
+    x = torch.randn((B, K), generator=_gen(K + 5), device=DEV).to(torch.bfloat16)
+    ws = None
+    if split:
+        nbytes = api.gemm_workspace_bytes(R, K)
+        assert nbytes > 0
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    y = api.gemm_q8_0(qs, d, x, workspace=ws)
+    y2 = api.gemm_q8_0(qs, d, x, workspace=ws)   # the first call left its tickets at zero
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    qh, dh, xb = synth.host_i8(qs), synth.bits_u16(d), synth.bits_u16(x)
+    rows = np.arange(R) if R <= 8192 else np.arange(0, R, 97)
+    for b in sorted({0, B // 2, B - 1}):
+        ref = oracle.gemv_q8_0(qh[rows], dh[rows], x=oracle.bf16_to_f64(xb[b]), act="w_bf16")
+        assert rel_max_abs(y[b].cpu().numpy()[rows], ref) < GEMV_TOL, b
+    assert api.check_device_error() == 0
+
+
+def test_gemm_q8_0_widening_bit_exact(cuda_lib):
+    # one-hot activations pick single widened weights, y[b, r] = bf16(f32(d[r, c_b / 32]) * q[r, c_b])
+    # exactly: this pins the swizzled placement and the scale of each column position
+    R, K, B = 200, 256, 64
+    qs, d = _q8(R, K, 77)
+    cols = np.arange(B) * 4 + np.arange(B) // 16       # all four K tiles, every 16-byte chunk
+    x = torch.zeros((B, K), dtype=torch.bfloat16, device=DEV)
+    x[torch.arange(B, device=DEV), torch.tensor(cols, device=DEV)] = 1.0
+    y = api.gemm_q8_0(qs, d, x)
+    W = oracle.q8_0_widen_bf16(synth.host_i8(qs), synth.bits_u16(d))
+    np.testing.assert_array_equal(y.cpu().numpy().astype(np.float64), W[:, cols].T)
+
+
+def test_gemm_q8_0_unit_scales_integer_exact(cuda_lib):
+    qs, _ = _q8(384, 512, 21)
+    d = torch.ones((384, 16), dtype=torch.float16, device=DEV)
+    x = torch.randint(-8, 9, (24, 512), generator=_gen(22), device=DEV).to(torch.bfloat16)
+    y = api.gemm_q8_0(qs, d, x)
+    ref = x.double().cpu() @ qs.double().cpu().T
+    assert torch.equal(y.cpu().double(), ref)
+
+
 # ---------------------------------------------------------------- attention
 
 

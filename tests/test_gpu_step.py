@@ -18,7 +18,7 @@ from transformer_decode_step_weight_gb300 import api, synth
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-TOL = {"bf16": 2e-2, "f32": 5e-3, "i8": 2e-2}
+TOL = {"bf16": 2e-2, "f32": 5e-3, "i8": 2e-2, "w_bf16": 2e-2}
 
 
 def teacher_forced(dec, mt, steps, mode, act, lm_act=None, b=0, log=None):
@@ -63,12 +63,16 @@ def test_tiny_bf16_model_teacher_forced(cuda_lib):
     assert int(dec.pos[0]) == 32 and int(dec.step_ctr[0]) == 12
 
 
-@pytest.mark.parametrize("act,lane", [("f32", api.QD_ACT_F32), ("i8", api.QD_ACT_I8)])
-def test_tiny_q8_model_teacher_forced(cuda_lib, act, lane):
+@pytest.mark.parametrize("act,lane,lm_act,lm_lane", [("f32", api.QD_ACT_F32, None, None),
+                                                     ("i8", api.QD_ACT_I8, None, None),
+                                                     ("i8", api.QD_ACT_I8, "f32", api.QD_ACT_F32)])
+def test_tiny_q8_model_teacher_forced(cuda_lib, act, lane, lm_act, lm_lane):
+    # deq = 2 (f32 activations everywhere), 0 (dp4a everywhere) and 1 (dp4a in the
+    # layers, the LM head on f32 activations)
     mt = synth.make_model(synth.TINY, "q8_0", 2, DEV, ctx=40, steps=8)
-    dec = api.Decoder(mt, max_steps=8, act=lane)
+    dec = api.Decoder(mt, max_steps=8, act=lane, lm_act=lm_lane)
     st = {}
-    teacher_forced(dec, mt, 8, "f32", act, log=st)
+    teacher_forced(dec, mt, 8, "f32", act, lm_act=lm_act, log=st)
     assert st["strict"] >= 7
 
 
@@ -115,11 +119,36 @@ def test_batched_tensor_core_step_teacher_forced(cuda_lib, batch):
     assert api.check_device_error() == 0
 
 
-def test_qwen3_8b_batched_paged_layer(cuda_lib):
+@pytest.mark.parametrize("batch", [3, 16])
+def test_batched_q8_step_teacher_forced(cuda_lib, batch):
+    # Q8_0 weights (LM head too) at batch > 1: every projection a tcgen05 GEMM with the
+    # weights widened to bf16 on chip; paged KV through a random page table
+    mt = synth.make_model(synth.SMALL256, "q8_0", 8, DEV, batch=batch, ctx=None, steps=3, paged=True)
+    om = oracle_model(mt)
+    check = sorted({0, batch // 2, batch - 1})
+    caches = {b: oracle_caches(mt, b, int(mt.seq_lens[b]) + 3) for b in check}
+    dec = api.Decoder(mt, max_steps=3)
+    assert dec.launches_per_step == 1 + 8 * 2 + 3
+    toks = {b: int(mt.start_tok[b]) for b in check}
+    for t in range(3):
+        dec.step()
+        torch.cuda.synchronize()
+        for b in check:
+            g = dec.logits[b].double().cpu().numpy()
+            ref = oracle.decode_token(om, toks[b], int(mt.seq_lens[b]) + t, caches[b][0], caches[b][1],
+                                      mode="bf16", act="w_bf16")
+            assert rel_max_abs(g, ref) < TOL["w_bf16"], (t, b)
+            toks[b] = int(dec.tok[b])
+            assert toks[b] == oracle.argmax_first(g)
+    assert api.check_device_error() == 0
+
+
+@pytest.mark.parametrize("wtype,act", [("bf16", "bf16"), ("q8_0", "w_bf16")])
+def test_qwen3_8b_batched_paged_layer(cuda_lib, wtype, act):
     """The batched workload's shapes: 64 sequences, Qwen3-8B layer, 16-token pages through a
     random page table, context uniform in [128, 4096]; sampled sequences checked whole."""
     s = synth.QWEN3_8B
-    mt = synth.make_model(s, "bf16", 9, DEV, n_layers=1, batch=64, ctx=None, steps=1, paged=True)
+    mt = synth.make_model(s, wtype, 9, DEV, n_layers=1, batch=64, ctx=None, steps=1, paged=True)
     om = oracle_model(mt)
     dec = api.Decoder(mt, max_steps=1)
     check = [0, 31, 63]
@@ -130,12 +159,13 @@ def test_qwen3_8b_batched_paged_layer(cuda_lib):
     for b in check:
         x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[b])]))
         ref = oracle.layer_step(om.dims, om.layers[0], x0, caches[b][0][0], caches[b][1][0],
-                                int(mt.seq_lens[b]), mode="bf16", act="bf16")
-        assert rel_max_abs(res[b].double().cpu().numpy(), ref) < TOL["bf16"], b
+                                int(mt.seq_lens[b]), mode="bf16", act=act)
+        assert rel_max_abs(res[b].double().cpu().numpy(), ref) < TOL[act], b
     rows = np.arange(0, s.vocab, 211)
     for b in check:
         lg = dec.logits[b].double().cpu().numpy()
-        assert rel_max_abs(lg[rows], oracle.lm_head_rows(om, res[b].double().cpu().numpy(), rows)) < TOL["bf16"]
+        ref = oracle.lm_head_rows(om, res[b].double().cpu().numpy(), rows, act=act)
+        assert rel_max_abs(lg[rows], ref) < TOL[act]
         assert int(dec.tok[b]) == oracle.argmax_first(lg)
     assert api.check_device_error() == 0
 

@@ -57,6 +57,8 @@ _SIGS = {
     "qd_gemv_bf16": (_i, [_vp, _i, _i, _vp, _i, _vp, _i, _vp]),
     "qd_gemv_q8_0": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _i, _vp, _vp]),
     "qd_quantize_q8_0": (_i, [_vp, _i, _vp, _vp, _vp]),
+    "qd_gemm_workspace_bytes": (_sz, [_i, _i, _i]),
+    "qd_gemm_q8_0": (_i, [_vp, _vp, _i, _i, _vp, _i, _vp, _vp, _sz, _vp]),
     "qd_attn_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "qd_attn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
     "qd_attn_decode_paged_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp]),
@@ -138,6 +140,21 @@ def gemv_q8_0(qs, d, x=None, xq=None, xd=None, act=QD_ACT_F32, y=None, stream=No
     if y is None:
         y = torch.empty(R, dtype=torch.float32, device=qs.device)
     _check(lib().qd_gemv_q8_0(_p(qs), _p(d), R, K, _p(x), _p(xq), _p(xd), act, _p(y), _stream(stream)))
+    return y
+
+
+def gemm_workspace_bytes(rows, cols, wtype=QD_W_Q8_0):
+    return int(lib().qd_gemm_workspace_bytes(rows, cols, wtype))
+
+
+def gemm_q8_0(qs, d, x, y=None, workspace=None, stream=None):
+    """y[b] = bf16(f32(d) * qs) @ x[b] on the tensor cores; x bf16 [B, K] -> f32 [B, R]."""
+    R, K = qs.shape
+    B = x.shape[0]
+    if y is None:
+        y = torch.empty((B, R), dtype=torch.float32, device=qs.device)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().qd_gemm_q8_0(_p(qs), _p(d), R, K, _p(x), B, _p(y), _p(workspace), nbytes, _stream(stream)))
     return y
 
 

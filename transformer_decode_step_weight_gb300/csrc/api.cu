@@ -234,6 +234,29 @@ int qd_gemv_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const 
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_q8_0");
 }
 
+size_t qd_gemm_workspace_bytes(int rows, int cols, qd_wtype wtype) {
+  if (rows < 1 || cols < 1) return 0;
+  return gemm_tc_workspace_bytes(rows, cols, wtype == QD_W_Q8_0);
+}
+
+int qd_gemm_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const void* x_bf16, int batch, float* y,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!qs || !d_f16 || !x_bf16 || !y) return fail(QD_ERR_INVALID_ARG, "qd_gemm_q8_0: null pointer");
+  if (rows < 1 || cols < 32 || cols % 32 || batch < 1)
+    return fail(QD_ERR_INVALID_ARG, "qd_gemm_q8_0: rows=%d cols=%d batch=%d", rows, cols, batch);
+  if (!gemm_tc_q8_supported(rows, cols, batch))
+    return fail(QD_ERR_UNSUPPORTED, "qd_gemm_q8_0: need cols %% 256 == 0 and batch <= 64 (cols=%d batch=%d)", cols,
+                batch);
+  if (!aligned16(qs) || !aligned16(d_f16) || !aligned16(x_bf16) || !aligned16(y) ||
+      (workspace && !aligned16(workspace)))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemm_q8_0: pointers must be 16-byte aligned");
+  GemmTcArgs g = {};
+  g.W = qs; g.S = d_f16; g.X = x_bf16; g.R = rows; g.K = cols; g.B = batch; g.epi = EPI_STORE; g.y = y;
+  g.ws = workspace; g.ws_bytes = workspace ? workspace_bytes : 0;
+  cudaError_t e = launch_gemm_tc(g, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemm_q8_0");
+}
+
 int qd_quantize_q8_0(const float* x, int n, int8_t* x_q, void* x_d_f16, cudaStream_t stream) {
   if (!x || !x_q || !x_d_f16) return fail(QD_ERR_INVALID_ARG, "qd_quantize_q8_0: null pointer");
   if (n < 0 || n % 32) return fail(QD_ERR_INVALID_ARG, "qd_quantize_q8_0: n=%d must be a multiple of 32", n);
@@ -406,6 +429,12 @@ struct StepWs {
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// The tensor-core step: BF16 models from batch 9, Q8_0 models from batch 2 (the
+// Q8_0 GEMV lanes take one activation vector).
+bool tc_step(const qd_step_args* a) {
+  return a->batch > 8 || (a->layers[0]->dims.wtype == QD_W_Q8_0 && a->batch > 1);
+}
+
 StepWs step_ws_layout(const qd_step_args* a, void* base) {
   const qd_layer_dims& d = a->layers[0]->dims;
   const int B = a->batch;
@@ -424,10 +453,12 @@ StepWs step_ws_layout(const qd_step_args* a, void* base) {
   w.claims = (int*)(p + off); off += al256((size_t)(5 * a->n_layers + 1) * 2 * sizeof(int));
   w.gemm_ws = (void*)(p + off);
   w.gemm_ws_bytes = 0;
-  if (B > 8) {  // the batched step runs its projections as split-K tcgen05 GEMMs
-    const int shapes[5][2] = {{(int)qkv, d.hidden}, {d.hidden, d.n_q_heads * d.head_dim}, {2 * d.ffn, d.hidden},
-                              {d.hidden, d.ffn}, {a->vocab, d.hidden}};
-    for (const auto& sh : shapes) w.gemm_ws_bytes = std::max(w.gemm_ws_bytes, gemm_tc_workspace_bytes(sh[0], sh[1]));
+  if (tc_step(a)) {  // the batched step runs its projections as split-K tcgen05 GEMMs
+    const bool q8 = d.wtype == QD_W_Q8_0, q8_head = a->lm_head_scales != nullptr;
+    const int shapes[5][3] = {{(int)qkv, d.hidden, q8}, {d.hidden, d.n_q_heads * d.head_dim, q8},
+                              {2 * d.ffn, d.hidden, q8}, {d.hidden, d.ffn, q8}, {a->vocab, d.hidden, q8_head}};
+    for (const auto& sh : shapes)
+      w.gemm_ws_bytes = std::max(w.gemm_ws_bytes, gemm_tc_workspace_bytes(sh[0], sh[1], sh[2] != 0));
   }
   off += al256(w.gemm_ws_bytes);
   w.total = off;
@@ -455,8 +486,12 @@ int validate_step(const qd_step_args* a) {
   if (a->vocab < 1 || a->max_steps < 1) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: vocab/max_steps");
   if (a->batch < 1 || a->batch > 64)
     return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batch=%d (supported 1..64)", a->batch);
-  if (d0.wtype == QD_W_Q8_0 && a->batch != 1)
-    return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 step supports batch 1");
+  if (d0.wtype == QD_W_Q8_0 && a->batch > 1) {
+    const int ks[3] = {d0.hidden, d0.n_q_heads * d0.head_dim, d0.ffn};
+    for (int k : ks)
+      if (!gemm_tc_q8_supported(1, k, a->batch))
+        return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batched Q8_0 K=%d must be a multiple of 256", k);
+  }
   if (d0.wtype == QD_W_BF16) {
     const int ks[3] = {d0.hidden, d0.n_q_heads * d0.head_dim, d0.ffn};
     for (int k : ks) {
@@ -473,8 +508,17 @@ int validate_step(const qd_step_args* a) {
   const bool q8_head = a->lm_head_scales != nullptr;
   if (q8_head) {
     if (!gemv_q8_supported(d0.hidden)) return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 head dims");
-    if (a->batch != 1) return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 LM head supports batch 1");
+    if (a->batch > 1 && !tc_step(a))
+      return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: a Q8_0 LM head over BF16 layers needs batch 1 or 9..64");
+    if (a->batch > 1 && (!gemm_tc_q8_supported(a->vocab, d0.hidden, a->batch) || !aligned16(a->lm_head_scales)))
+      return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batched Q8_0 LM head needs hidden %% 256 == 0");
   }
+  if (d0.wtype == QD_W_Q8_0 && a->batch > 1)
+    for (int i = 0; i < a->n_layers; ++i) {
+      const qd_layer_weights& lw = a->layers[i]->w;
+      if (!aligned16(lw.s_qkv) || !aligned16(lw.s_o) || !aligned16(lw.s_gu) || !aligned16(lw.s_down))
+        return fail(QD_ERR_INVALID_ARG, "qd_decode_step: batched Q8_0 scales must be 16-byte aligned");
+    }
   if (!aligned16(a->embed) || !aligned16(a->lm_head) || !aligned16(a->logits) || !aligned16(a->workspace))
     return fail(QD_ERR_INVALID_ARG, "qd_decode_step: pointers must be 16-byte aligned");
   const StepWs w = step_ws_layout(a, a->workspace);
@@ -489,18 +533,21 @@ int validate_step(const qd_step_args* a) {
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
 
-// Batched decode (9..64 sequences, BF16): every projection is a tcgen05 GEMM over
-// the batch; RMSNorm and SwiGLU write the bf16 GEMM operand in small row kernels.
+// Batched decode (BF16: 9..64 sequences; Q8_0: 2..64): every projection is a
+// tcgen05 GEMM over the batch (Q8_0 weights widened to bf16 on chip); RMSNorm and
+// SwiGLU write the bf16 GEMM operand in small row kernels.
 int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   const qd_layer_dims& d = a->layers[0]->dims;
+  const bool q8 = d.wtype == QD_W_Q8_0;
   const StepWs w = step_ws_layout(a, a->workspace);
   const Launch L = make_launch(stream, true);
   const int B = a->batch;
   const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
   const int QKV = (Hq + 2 * Hkv) * D;
-  auto gemm = [&](const void* W, int R, int K, const void* X, int epi, float* y) {
+  // S: the Q8_0 scales of W, or null for bf16 W
+  auto gemm = [&](const void* W, const void* S, int R, int K, const void* X, int epi, float* y) {
     GemmTcArgs g = {};
-    g.W = W; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
+    g.W = W; g.S = S; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
     g.ws = w.gemm_ws; g.ws_bytes = w.gemm_ws_bytes;
     return launch_gemm_tc(g, L);
   };
@@ -508,7 +555,7 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   for (int li = 0; li < a->n_layers; ++li) {
     const qd_layer* l = a->layers[li];
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_in, B, H, d.rms_eps, w.xn, L), "rmsnorm");
-    QD_TRY(gemm(l->w.w_qkv, QKV, H, w.xn, EPI_STORE, w.qkv), "qkv gemm");
+    QD_TRY(gemm(l->w.w_qkv, q8 ? l->w.s_qkv : nullptr, QKV, H, w.xn, EPI_STORE, w.qkv), "qkv gemm");
     AttnArgs at = {};
     at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
     at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps; at.act_bf16 = 1;
@@ -517,14 +564,14 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
     at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D); at.out_bf16 = w.attn;
     at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.use_cluster = 0;
     QD_TRY(launch_attention(at, L), "attention");
-    QD_TRY(gemm(l->w.w_o, H, Hq * D, w.attn, EPI_RESID_ADD, w.res), "o gemm");
+    QD_TRY(gemm(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, EPI_RESID_ADD, w.res), "o gemm");
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, B, H, d.rms_eps, w.xn, L), "rmsnorm");
-    QD_TRY(gemm(l->w.w_gu, 2 * F, H, w.xn, EPI_STORE, w.gu), "gu gemm");
+    QD_TRY(gemm(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, EPI_STORE, w.gu), "gu gemm");
     QD_TRY(launch_swiglu_rows(w.gu, B, F, w.xn, L), "swiglu");
-    QD_TRY(gemm(l->w.w_down, H, F, w.xn, EPI_RESID_ADD, w.res), "down gemm");
+    QD_TRY(gemm(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, EPI_RESID_ADD, w.res), "down gemm");
   }
   QD_TRY(launch_rmsnorm_rows(w.res, a->final_norm, B, H, d.rms_eps, w.xn, L), "final rmsnorm");
-  QD_TRY(gemm(a->lm_head, a->vocab, H, w.xn, EPI_STORE, a->logits), "lm head gemm");
+  QD_TRY(gemm(a->lm_head, a->lm_head_scales, a->vocab, H, w.xn, EPI_STORE, a->logits), "lm head gemm");
   QD_TRY(launch_argmax_advance(a->logits, a->vocab, B, a->tok, a->pos, a->step, a->out_tokens, a->max_steps,
                                w.argmax_ws, L),
          "argmax");
@@ -532,7 +579,7 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
 }
 
 int run_step(const qd_step_args* a, cudaStream_t stream) {
-  if (a->batch > 8) return run_step_tc(a, stream);
+  if (tc_step(a)) return run_step_tc(a, stream);
   const qd_layer_dims& d = a->layers[0]->dims;
   const StepWs w = step_ws_layout(a, a->workspace);
   const Launch L = make_launch(stream, true);
@@ -685,7 +732,7 @@ size_t qd_step_workspace_bytes(const qd_step_args* a) {
 
 int qd_step_launch_count(const qd_step_args* a) {
   if (!a || a->n_layers < 1) return 0;
-  if (a->batch > 8) return 1 + 8 * a->n_layers + 3;
+  if (tc_step(a)) return 1 + 8 * a->n_layers + 3;
   return 1 + 5 * a->n_layers + 2;
 }
 

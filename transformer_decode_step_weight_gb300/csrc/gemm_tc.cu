@@ -16,6 +16,12 @@
 //     each stage back to the producer; a final commit releases the epilogue;
 //   * the four warps read their 32 TMEM lanes each (tcgen05.ld 32x32b.x64) and
 //     store y or add it to the residual stream.
+// Q8_0 weights (int8 values, an fp16 scale per 32 of a row; "emit_qwen38_generate"
+// rustdoc, "Where the speed comes from") take the same MMA: the producer streams the
+// int8 tile [128 x 64 B] and its scales with TMA, and eight converter warps widen
+// each weight to bf16(f32(d) * q) (exact product, one round to nearest even) into
+// the swizzled A tile the MMA reads. The tensor cores' int8 rate on this part is
+// far below their bf16 rate, so the int8 values are not fed to them directly.
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -38,7 +44,11 @@ constexpr int kBK = 64;         // K elements per stage (128 bytes of bf16)
 // runs in one wave). QD_GEMM_STAGES = 3 or 6 forces one.
 constexpr int kTileA = kBM * kBK * 2;    // 16 KB
 constexpr int kTileB = kBN * kBK * 2;    // 8 KB
+constexpr int kTileQ = kBM * kBK;        // 8 KB: int8 values of a Q8_0 tile
+constexpr int kTileS = kBM * 16;         // 2 KB: 8 fp16 scales (256 columns) per row
 constexpr int kThreadsTc = 128;
+constexpr int kConvWarps = 8;            // Q8_0: warps 4..11 widen int8 -> bf16
+constexpr int kThreadsQ8 = kThreadsTc + 32 * kConvWarps;
 constexpr int kMaxSplits = 4;   // K splits of one tile (partials summed in registers)
 
 struct TcParams {
@@ -118,18 +128,68 @@ QD_DEV void tmem_ld_32x64(uint32_t taddr, float* v) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int kStagesTc>
-__global__ void __launch_bounds__(kThreadsTc, 1)
+// Eight Q8_0 weights (two 32-bit words of int8) -> four bf16 pairs, each
+// bf16(f32(d) * q). q + 128 is placed in the low mantissa bits of 2^23 and the
+// bias subtracted, which gives q exactly; q * d is exact in binary32 (8 by 11
+// significant bits), so the pack's round to nearest even is the only rounding.
+QD_DEV uint32_t bf16x2_bits(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+QD_DEV uint4 widen8_q8(uint32_t w0, uint32_t w1, float d) {
+  uint32_t o[4];
+  const uint32_t u[2] = {w0 ^ 0x80808080u, w1 ^ 0x80808080u};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float f[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      f[b] = (__uint_as_float(__byte_perm(u[h], 0x4B000000u, 0x7540u + b)) - 8388736.0f) * d;
+    o[2 * h] = bf16x2_bits(f[0], f[1]);
+    o[2 * h + 1] = bf16x2_bits(f[2], f[3]);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Ring depths of the Q8_0 form (one CTA per SM, ~216 KB of shared memory). The
+// converters work as kConvGroups groups of two warps, group g widening K steps
+// g, g + kConvGroups, ...: a single step's widening is a chain of loads, math,
+// stores and a proxy fence whose latency one group alone cannot hide, so several
+// steps are widened at once. The A ring holds those steps plus the MMA's; the
+// int8 ring carries the HBM stream (about 68 KB in flight per SM); X comes from L2.
+constexpr int kConvGroups = kConvWarps / 2;
+constexpr int kQSt = 8;    // int8 + scale tiles
+constexpr int kBSt = 5;    // X tiles
+constexpr int kASt = 6;    // widened bf16 A tiles
+
+// Bounded wait for the last copy issued to each slot of a ring (a CTA never
+// exits with a TMA copy still landing in its shared memory).
+QD_DEV void drain_ring(uint64_t* full, int slots, int issued, int* err) {
+  for (int i = max(0, issued - slots); i < issued; ++i) mbar_wait_bounded(&full[i % slots], (uint32_t)((i / slots) & 1), err);
+}
+
+template <int kStagesTc, bool kQ8>
+__global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStagesTc <= 3) ? 3 : 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmS, const TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char* sA = smem;                                   // [stages][128 x 128 B]
-  unsigned char* sB = smem + kStagesTc * kTileA;              // [stages][64 x 128 B]
-  uint64_t* full = (uint64_t*)(sB + kStagesTc * kTileB);
-  uint64_t* empty = full + kStagesTc;
-  uint64_t* done = empty + kStagesTc;
+  constexpr int nA = kQ8 ? kASt : kStagesTc;  // A tiles (bf16 W, or widened Q8_0)
+  constexpr int nB = kQ8 ? kBSt : kStagesTc;  // X tiles
+  constexpr int nQ = kQ8 ? kQSt : 0;          // int8 + scale tiles
+  unsigned char* sA = smem;                   // [nA][128 x 128 B]
+  unsigned char* sB = sA + nA * kTileA;       // [nB][64 x 128 B]
+  unsigned char* sQ = sB + nB * kTileB;       // [nQ][128 x 64 B]
+  unsigned char* sS = sQ + nQ * kTileQ;       // [nQ][128 x 16 B]
+  // bf16 form: full/empty per stage cover both A and B tiles
+  uint64_t* full = (uint64_t*)(sS + nQ * kTileS);   // [nA] A+B landed / [nB] X landed (Q8_0)
+  uint64_t* empty = full + nB;                      // [nB] stage read by the MMA
+  uint64_t* qfull = empty + nB;                     // [nQ] int8 + scales landed
+  uint64_t* qempty = qfull + nQ;                    // [nQ] int8 tile read by the converters
+  uint64_t* conv = qempty + nQ;                     // [nA] A tile widened (Q8_0)
+  uint64_t* aempty = conv + (kQ8 ? nA : 0);         // [nA] A tile read by the MMA (Q8_0)
+  uint64_t* done = aempty + (kQ8 ? nA : 0);
   uint32_t* tmem_slot = (uint32_t*)(done + 1);
   __shared__ int s_abort;
 
@@ -142,10 +202,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __shared__ int s_ticket;
 
   if (tid == 0) {
-    for (int i = 0; i < kStagesTc; ++i) {
+    for (int i = 0; i < nB; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
+    for (int i = 0; i < nQ; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 2);  // the two warps of the step's converter group
+    }
+    if (kQ8)
+      for (int i = 0; i < nA; ++i) {
+        mbar_init(&conv[i], 2);
+        mbar_init(&aempty[i], 1);
+      }
     mbar_init(done, 1);
     fence_mbar_init();
     s_abort = 0;
@@ -157,50 +226,142 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer: W tiles need no dependency; X (this step's activations) does
-    const int pre = min(kStagesTc, n_k);
-    for (int i = 0; i < pre; ++i) {
-      mbar_arrive_expect_tx(&full[i], kTileA + kTileB);
-      tma_load_2d(sA + i * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[i]);
-    }
-    pdl_wait();
-    for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[i]);
-    for (int i = pre; i < n_k; ++i) {
-      const int s = i % kStagesTc;
-      if (!mbar_wait_bounded(&empty[s], (uint32_t)(((i / kStagesTc) - 1) & 1), p.err)) {
-        s_abort = 1;
-        break;
-      }
-      mbar_arrive_expect_tx(&full[s], kTileA + kTileB);
-      tma_load_2d(sA + s * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[s]);
-      tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[s]);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    for (int i = 0; i < n_k; ++i) {
-      const int s = i % kStagesTc;
-      if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kStagesTc) & 1), p.err)) break;
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(sA + s * kTileA), b0 = smem_u32(sB + s * kTileB);
+  auto mma_stage = [&](uint32_t a0, uint32_t b0, int i) {
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), (i | kk) != 0);
-      mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), (i | kk) != 0);
+  };
+
+  if constexpr (!kQ8) {
+    if (warp == 0 && lane == 0) {
+      // ---- producer: W tiles need no dependency; X (this step's activations) does
+      const int pre = min(kStagesTc, n_k);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], kTileA + kTileB);
+        tma_load_2d(sA + i * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[i]);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[i]);
+      int issued = pre;
+      for (int i = pre; i < n_k; ++i) {
+        const int s = i % kStagesTc;
+        if (!mbar_wait_bounded(&empty[s], (uint32_t)(((i / kStagesTc) - 1) & 1), p.err)) {
+          s_abort = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kTileA + kTileB);
+        tma_load_2d(sA + s * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[s]);
+        tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[s]);
+        issued = i + 1;
+      }
+      drain_ring(full, kStagesTc, issued, p.err);
+    } else if (warp == 1 && lane == 0) {
+      // ---- MMA issuer
+      for (int i = 0; i < n_k; ++i) {
+        const int s = i % kStagesTc;
+        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kStagesTc) & 1), p.err)) break;
+        tc_fence_after();
+        mma_stage(smem_u32(sA + s * kTileA), smem_u32(sB + s * kTileB), i);
+        mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+      }
+      mma_commit(done);         // D complete (also arrives after an early exit)
     }
-    mma_commit(done);         // D complete (also arrives after an early exit)
+  } else {
+    if (warp == 0 && lane == 0) {
+      // ---- weight producer: int8 tiles and their scales (no dependency on the
+      // previous kernel), as far ahead as the int8 ring allows
+      int issued = 0;
+      for (int i = 0; i < n_k; ++i) {
+        const int s = i % kQSt;
+        if (i >= kQSt && !mbar_wait_bounded(&qempty[s], (uint32_t)(((i / kQSt) - 1) & 1), p.err)) {
+          s_abort = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&qfull[s], kTileQ + kTileS);
+        tma_load_2d(sQ + s * kTileQ, &tmW, (kb0 + i) * kBK, row0, &qfull[s]);
+        tma_load_2d(sS + s * kTileS, &tmS, ((kb0 + i) >> 2) * 8, row0, &qfull[s]);  // 16-byte aligned x
+        issued = i + 1;
+      }
+      drain_ring(qfull, kQSt, issued, p.err);
+    } else if (warp == 2 && lane == 0) {
+      // ---- activation producer: this step's X tiles (from L2)
+      pdl_wait();
+      int issued = 0;
+      for (int i = 0; i < n_k; ++i) {
+        const int s = i % kBSt;
+        if (i >= kBSt && !mbar_wait_bounded(&empty[s], (uint32_t)(((i / kBSt) - 1) & 1), p.err)) {
+          s_abort = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kTileB);
+        tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[s]);
+        issued = i + 1;
+      }
+      drain_ring(full, kBSt, issued, p.err);
+    } else if (warp == 1 && lane == 0) {
+      // ---- MMA issuer
+      for (int i = 0; i < n_k; ++i) {
+        const int sa = i % kASt, sb = i % kBSt;
+        if (!mbar_wait_bounded(&full[sb], (uint32_t)((i / kBSt) & 1), p.err)) break;
+        if (!mbar_wait_bounded(&conv[sa], (uint32_t)((i / kASt) & 1), p.err)) break;
+        tc_fence_after();
+        mma_stage(smem_u32(sA + sa * kTileA), smem_u32(sB + sb * kTileB), i);
+        mma_commit(&aempty[sa]);
+        mma_commit(&empty[sb]);
+      }
+      mma_commit(done);
+    } else if (warp >= 4) {
+      // ---- converters: int8 tile + scales -> bf16 A tile in the 128-byte-swizzle
+      // layout TMA would have written (16-byte chunk c of row r at chunk c ^ (r & 7)).
+      // In a group, thread t (0..63) takes 16 int8 of a row per item: rows t / 4 + 16 j
+      // (j < 8), chunk t % 4, so a warp reads 512 contiguous bytes per j and its
+      // swizzled stores hit distinct banks. All eight items are loaded before the
+      // int8 slot is released, then widened and stored.
+      const int grp = (warp - 4) >> 1;
+      const int t = ((warp - 4) & 1) * 32 + lane;
+      for (int i = grp; i < n_k; i += kConvGroups) {
+        const int sq = i % kQSt, sa = i % kASt;
+        if (!mbar_wait_bounded(&qfull[sq], (uint32_t)((i / kQSt) & 1), p.err)) break;
+        if (i >= kASt && !mbar_wait_bounded(&aempty[sa], (uint32_t)(((i / kASt) - 1) & 1), p.err)) break;
+        const int kt = kb0 + i;
+        const unsigned char* q = sQ + sq * kTileQ;
+        const __half* sc = (const __half*)(sS + sq * kTileS);
+        const int c = t & 3, r0 = t >> 2;
+        uint4 w[8];
+        float d[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int row = r0 + 16 * j;
+          w[j] = *(const uint4*)(q + row * kBK + c * 16);
+          d[j] = __half2float(sc[row * 8 + (kt & 3) * 2 + (c >> 1)]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[sq]);
+        unsigned char* a = sA + sa * kTileA;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int row = r0 + 16 * j, sw = row & 7;
+          *(uint4*)(a + row * 128 + (((2 * c) ^ sw) << 4)) = widen8_q8(w[j].x, w[j].y, d[j]);
+          *(uint4*)(a + row * 128 + (((2 * c + 1) ^ sw) << 4)) = widen8_q8(w[j].z, w[j].w, d[j]);
+        }
+        fence_proxy_async_smem();  // the generic-proxy stores before the MMA's reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[sa]);
+      }
+    }
   }
   __syncwarp();
 
-  // ---- epilogue: warp w owns TMEM lanes [32w, 32w + 32) = rows row0 + 32w + lane
+  // ---- epilogue: warp w < 4 owns TMEM lanes [32w, 32w + 32) = rows row0 + 32w + lane
   pdl_wait();
-  const bool ok = mbar_wait_bounded(done, 0, p.err);
+  const bool rows_here = !kQ8 || warp < 4;
+  const bool ok = rows_here ? mbar_wait_bounded(done, 0, p.err) : true;
   tc_fence_after();
   float v[64];
-  tmem_ld_32x64(tmem + ((uint32_t)(warp * 32) << 16), v);
+  if (rows_here) tmem_ld_32x64(tmem + ((uint32_t)(warp * 32) << 16), v);
   const int rl = warp * 32 + lane;          // this thread's row of the tile
   const int r = row0 + rl;
-  bool write = ok && !s_abort;
+  bool write = rows_here && ok && !s_abort;
   // y[n0 + j, r] (+)= o[j] for 16 tokens; the residual values are all loaded
   // before any store, so the 16 read-modify-writes overlap instead of queueing
   auto store_rows = [&](int n0, const float* o) {
@@ -223,8 +384,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // residual's) in flight together
     const size_t tile = blockIdx.x;
     float* part = p.part + (tile * p.splits + blockIdx.y) * (size_t)(kBN * kBM);
+    if (rows_here) {
 #pragma unroll
-    for (int n = 0; n < kBN; ++n) part[(size_t)n * kBM + rl] = v[n];
+      for (int n = 0; n < kBN; ++n) part[(size_t)n * kBM + rl] = v[n];
+    }
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -285,33 +448,45 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 [rows, cols] matrix, box of box_rows x 64 columns, 128-byte swizzle.
-cudaError_t encode_rowmajor_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                                 uint32_t box_rows) {
+// Row-major [rows, cols] matrix of elem-byte elements, box of box_rows x box_cols.
+cudaError_t encode_rowmajor(CUtensorMap* m, CUtensorMapDataType dt, int elem, const void* base, uint64_t rows,
+                            uint64_t cols, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint64_t strides[1] = {cols * elem};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-constexpr size_t smem_tc(int st) { return 1024 + (size_t)st * (kTileA + kTileB) + (2 * st + 1) * 8 + 16; }
+// Row-major bf16 [rows, cols] matrix, box of box_rows x 64 columns, 128-byte swizzle.
+cudaError_t encode_rowmajor_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                                 uint32_t box_rows) {
+  return encode_rowmajor(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, kBK, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+}
 
-template <int ST>
-cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, int tiles, const Launch& L) {
-  auto k = gemm_tc_kernel<ST>;
+constexpr size_t smem_tc(int st, bool q8) {
+  return q8 ? 1024 + (size_t)kASt * kTileA + (size_t)kBSt * kTileB + (size_t)kQSt * (kTileQ + kTileS) +
+                  (2 * kBSt + 2 * kQSt + 2 * kASt + 1) * 8 + 16
+            : 1024 + (size_t)st * (kTileA + kTileB) + (2 * st + 1) * 8 + 16;
+}
+
+template <int ST, bool Q8>
+cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts, const TcParams& p,
+                      int tiles, const Launch& L) {
+  auto k = gemm_tc_kernel<ST, Q8>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tc(ST));
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tc(ST, Q8));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(k, dim3(tiles, p.splits), dim3(kThreadsTc), smem_tc(ST), L, tw, tx, p);
+  return launch_ex(k, dim3(tiles, p.splits), dim3(Q8 ? kThreadsQ8 : kThreadsTc), smem_tc(ST, Q8), L, tw, tx, ts,
+                   p);
 }
 
 }  // namespace
@@ -321,6 +496,10 @@ cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint
 }
 
 bool gemm_tc_supported(int R, int K, int B) { return R >= 1 && K >= kBK && K % kBK == 0 && B >= 1 && B <= kBN; }
+
+// Q8_0 weights: the scale rows are read as 16-byte TMA boxes (256 columns), so
+// their stride K/32 x 2 bytes must be a multiple of 16.
+bool gemm_tc_q8_supported(int R, int K, int B) { return gemm_tc_supported(R, K, B) && K % 256 == 0; }
 
 // K splits for an R x K launch, chosen to keep every SM streaming to the end.
 // With s splits the tiles x s CTAs run in ceil(tiles x s / SMs) rounds of 1/s of
@@ -333,7 +512,7 @@ bool gemm_tc_supported(int R, int K, int B) { return R >= 1 && K >= kBK && K % k
 constexpr int kMaxSplitTiles = 4096;
 constexpr size_t kTicketBytes = (size_t)kMaxSplitTiles * sizeof(int);
 
-int gemm_tc_splits(int R, int K) {
+int gemm_tc_splits(int R, int K, bool q8) {
   if (R < 1 || K < kBK) return 1;
   const int tiles = (R + kBM - 1) / kBM, n_kt = K / kBK, sms = dev_info().sm_count;
   if (tiles > kMaxSplitTiles) return 1;
@@ -342,10 +521,12 @@ int gemm_tc_splits(int R, int K) {
     return v ? atoi(v) : 0;
   }();
   if (forced > 0) return std::max(1, std::min(std::min(forced, kMaxSplits), n_kt));
-  if (tiles >= sms) return 1;  // the tiles alone fill the GPU (measured: splitting them was slower)
+  // bf16: two or three CTAs per SM, so tiles that fill the SMs are not split (measured
+  // slower); Q8_0 runs one CTA per SM, where splitting evens out a partial last wave
+  if (tiles >= sms && !q8) return 1;
   int best = 1;
   double best_t = (double)((tiles + sms - 1) / sms);
-  const double tile_bytes = (double)kBM * K * 2;
+  const double tile_bytes = (double)kBM * K * (q8 ? 34.0 / 32.0 : 2.0);
   for (int sp = 2; sp <= kMaxSplits && n_kt / sp >= 8; ++sp) {
     const double t = (double)((tiles * sp + sms - 1) / sms) / sp + 0.5 * sp * 65536.0 / tile_bytes;
     if (t < best_t) {
@@ -356,17 +537,30 @@ int gemm_tc_splits(int R, int K) {
   return best;
 }
 
-size_t gemm_tc_workspace_bytes(int R, int K) {
-  const int sp = gemm_tc_splits(R, K);
+size_t gemm_tc_workspace_bytes(int R, int K, bool q8) {
+  const int sp = gemm_tc_splits(R, K, q8);
   if (sp <= 1) return 0;
   const size_t tiles = (size_t)(R + kBM - 1) / kBM;
   return kTicketBytes + tiles * sp * kBN * kBM * sizeof(float);
 }
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
-  if (!gemm_tc_supported(a.R, a.K, a.B)) return cudaErrorInvalidValue;
-  CUtensorMap tw, tx;
-  cudaError_t e = encode_rowmajor_bf16(&tw, a.W, (uint64_t)a.R, (uint64_t)a.K, kBM);
+  const bool q8 = a.S != nullptr;
+  if (!(q8 ? gemm_tc_q8_supported(a.R, a.K, a.B) : gemm_tc_supported(a.R, a.K, a.B))) return cudaErrorInvalidValue;
+  CUtensorMap tw, tx, ts;
+  cudaError_t e;
+  if (q8) {
+    // int8 [R, K] in 128 x 64-byte boxes; fp16 scales [R, K/32] in 128 x 8 boxes;
+    // rows past R read as zeros
+    e = encode_rowmajor(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.W, (uint64_t)a.R, (uint64_t)a.K, kBK, kBM,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    e = encode_rowmajor(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.S, (uint64_t)a.R, (uint64_t)a.K / 32, 8, kBM,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    e = encode_rowmajor_bf16(&tw, a.W, (uint64_t)a.R, (uint64_t)a.K, kBM);
+    ts = tw;  // unused
+  }
   if (e != cudaSuccess) return e;
   // X has B rows; the 64-row box reads zeros past them
   e = encode_rowmajor_bf16(&tx, a.X, (uint64_t)a.B, (uint64_t)a.K, kBN);
@@ -375,18 +569,20 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   p.R = a.R; p.K = a.K; p.B = a.B; p.epi = a.epi; p.y = a.y; p.err = L.err;
   const int tiles = (a.R + kBM - 1) / kBM;
   p.splits = 1;
-  const size_t need = gemm_tc_workspace_bytes(a.R, a.K);
+  const size_t need = gemm_tc_workspace_bytes(a.R, a.K, q8);
   if (a.ws && need > 0 && a.ws_bytes >= need) {
-    p.splits = gemm_tc_splits(a.R, a.K);
+    p.splits = gemm_tc_splits(a.R, a.K, q8);
     p.cnt = (int*)a.ws;
     p.part = (float*)((unsigned char*)a.ws + kTicketBytes);
   }
+  // Q8_0: one 384-thread CTA per SM with its own ring depths
+  if (q8) return launch_tc<kASt, true>(tw, tx, ts, p, tiles, L);
   static const int forced = [] {
     const char* v = getenv("QD_GEMM_STAGES");
     return v ? atoi(v) : 0;
   }();
   const bool deep = forced == 6 || (forced != 3 && (long long)tiles * p.splits <= dev_info().sm_count);
-  return deep ? launch_tc<6>(tw, tx, p, tiles, L) : launch_tc<3>(tw, tx, p, tiles, L);
+  return deep ? launch_tc<6, false>(tw, tx, ts, p, tiles, L) : launch_tc<3, false>(tw, tx, ts, p, tiles, L);
 }
 
 }  // namespace qd

@@ -71,7 +71,8 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L);
 
 // ----------------------------------------------------------------- batched GEMM (tcgen05)
 struct GemmTcArgs {
-  const void* W;          // bf16 [R, K]
+  const void* W;          // bf16 [R, K], or Q8_0 int8 values [R, K] when S is set
+  const void* S;          // Q8_0 fp16 scales [R, K/32], or null (bf16 W)
   const void* X;          // bf16 [B, K]
   int R, K, B;            // B <= 64
   int epi;                // GemvEpi
@@ -80,12 +81,13 @@ struct GemmTcArgs {
   size_t ws_bytes;        // left so); null: no split
 };
 bool gemm_tc_supported(int R, int K, int B);
+bool gemm_tc_q8_supported(int R, int K, int B);
 // Tensor map (CUtensorMap, 128-byte aligned storage of 128 bytes) of a row-major
 // bf16 [rows, cols] matrix: boxes of box_rows x 64 columns, 128-byte swizzle.
 cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 // K splits a launch of this shape takes, and the workspace they need.
-int gemm_tc_splits(int R, int K);
-size_t gemm_tc_workspace_bytes(int R, int K);
+int gemm_tc_splits(int R, int K, bool q8 = false);
+size_t gemm_tc_workspace_bytes(int R, int K, bool q8 = false);
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L);
 
 // row-wise helpers of the batched step

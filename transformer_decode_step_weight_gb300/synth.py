@@ -56,6 +56,8 @@ TINY = Shape("tiny", 256, 4, 2, 128, 544, 2, 1000, True)
 SMALL = Shape("small", 512, 8, 2, 128, 1376, 3, 5003, False)
 # dims that are multiples of 64, as the batched (tensor-core) projections need
 SMALL64 = Shape("small64", 512, 8, 2, 128, 1408, 2, 2999, False)
+# dims that are multiples of 256, as the batched Q8_0 projections need
+SMALL256 = Shape("small256", 512, 4, 2, 128, 1536, 2, 3001, False)
 
 
 @dataclass
@@ -93,6 +95,9 @@ WORKLOADS = {
     "qwen3-8b-bf16-paged-b64": Workload(
         "qwen3-8b-bf16-paged-b64", QWEN3_8B, "bf16", ctx=4096, steps=64, batch=64, paged=True,
         description="64 sequences, context uniform in [128, 4096], 16-token pages, random page table"),
+    "qwen3-8b-q8_0-paged-b64": Workload(
+        "qwen3-8b-q8_0-paged-b64", QWEN3_8B, "q8_0", ctx=4096, steps=64, batch=64, paged=True,
+        description="Q8_0 weights (LM head too), 64 sequences, context uniform in [128, 4096], 16-token pages"),
 }
 
 
