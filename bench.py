@@ -511,7 +511,7 @@ def run_reference(args, dist, rank, world, local):
         if lms is None:
             oracle.gemv_bf16(lm, xf)
         else:
-            oracle._project(lm, lms, xf, act, mode)
+            oracle.project(lm, lms, xf, act)
 
     for _ in range(args.warmup):
         one()

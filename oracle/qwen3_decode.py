@@ -360,7 +360,7 @@ class LayerWeights:
     s_down: np.ndarray | None = None
 
 
-def _project(w, s, x, act: str, mode: str):
+def project(w, s, x, act: str):
     """One weight-streaming projection for either storage format.
 
     act == "bf16": W bf16, x already in its storage precision.
@@ -396,7 +396,7 @@ def layer_step(dims: Dims, lw: LayerWeights, res, k_cache, v_cache, pos: int,
     H, D, hq, hkv, F = dims.hidden, dims.head_dim, dims.n_q_heads, dims.n_kv_heads, dims.ffn
     res = np.asarray(res, dtype=np.float64).copy()
     xn = rmsnorm(res, bf16_to_f64(lw.ln_in), dims.rms_eps, mode)
-    qkv = _project(lw.w_qkv, lw.s_qkv, xn, act, mode)
+    qkv = project(lw.w_qkv, lw.s_qkv, xn, act)
     q = qkv[:hq * D].reshape(hq, D)
     k = qkv[hq * D:(hq + hkv) * D].reshape(hkv, D)
     v = qkv[(hq + hkv) * D:].reshape(hkv, D)
@@ -408,11 +408,11 @@ def layer_step(dims: Dims, lw: LayerWeights, res, k_cache, v_cache, pos: int,
     v_cache[:, pos, :] = kv_rnd(v)
     o = gqa_attention(q, k_cache[:, :pos + 1, :], v_cache[:, :pos + 1, :])
     o = rnd(o.reshape(-1))
-    res = res + _project(lw.w_o, lw.s_o, o, act, mode)
+    res = res + project(lw.w_o, lw.s_o, o, act)
     xn2 = rmsnorm(res, bf16_to_f64(lw.ln_post), dims.rms_eps, mode)
-    gu = _project(lw.w_gu, lw.s_gu, xn2, act, mode)
+    gu = project(lw.w_gu, lw.s_gu, xn2, act)
     a = rnd(silu(gu[:F]) * gu[F:])
-    res = res + _project(lw.w_down, lw.s_down, a, act, mode)
+    res = res + project(lw.w_down, lw.s_down, a, act)
     if trace is not None:
         trace.update(q=q, k=k, v=v, attn=o, xn=xn, xn2=xn2, gu=gu)
     return res
@@ -449,7 +449,7 @@ def decode_token(model: Model, tok: int, pos: int, k_caches, v_caches,
         residual_trace.append(res.copy())
     xf = rmsnorm(res, bf16_to_f64(model.final_norm), d.rms_eps, mode)
     lm_act = act if lm_act is None else lm_act
-    return _project(model.lm_head, model.lm_head_scales, xf, lm_act, mode)
+    return project(model.lm_head, model.lm_head_scales, xf, lm_act)
 
 
 def lm_head_rows(model: Model, final_res, rows, mode: str = "bf16", act: str = "bf16"):
@@ -459,4 +459,4 @@ def lm_head_rows(model: Model, final_res, rows, mode: str = "bf16", act: str = "
                  d.rms_eps, mode)
     rows = np.asarray(rows)
     s = None if model.lm_head_scales is None else np.asarray(model.lm_head_scales)[rows]
-    return _project(np.asarray(model.lm_head)[rows], s, xf, act, mode)
+    return project(np.asarray(model.lm_head)[rows], s, xf, act)

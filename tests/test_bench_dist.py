@@ -67,9 +67,34 @@ def test_weight_byte_accounting_matches_the_shapes():
     assert abs(q8 / wb - 1.0625 / 2) < 1e-3
 
 
-@pytest.mark.parametrize("name", ["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-bf16-paged-b64"])
+@pytest.mark.parametrize("name", ["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-bf16-paged-b64",
+                                  "qwen3-8b-q8_0-paged-b64"])
 def test_workloads_are_the_named_shapes(name):
     from transformer_decode_step_weight_gb300 import synth
     wl = synth.WORKLOADS[name]
     assert wl.shape.head_dim == 128 and wl.shape.vocab == 151936
     assert wl.shape.n_q_heads % wl.shape.n_kv_heads == 0
+
+
+@pytest.mark.parametrize("deq,act,want", [(None, "f32", ("f32", "f32")), (None, "i8", ("i8", "i8")),
+                                          (0, "f32", ("i8", "i8")), (1, "f32", ("i8", "f32")),
+                                          (2, "i8", ("f32", "f32"))])
+def test_q8_deq_levels_pick_the_lanes(deq, act, want):
+    # deq 0: dp4a everywhere; 1: dp4a in the layers, f32 activations for the LM head;
+    # 2: f32 activations everywhere; without --deq, --act sets both
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.q8_lanes(types.SimpleNamespace(deq=deq, act=act)) == want
+
+
+def test_dtype_labels_name_the_arithmetic():
+    sys.path.insert(0, ROOT)
+    import bench
+    from transformer_decode_step_weight_gb300 import synth
+    wl = synth.WORKLOADS
+    assert bench.dtype_label(wl["qwen3-8b-bf16"], "f32", "f32") == "bf16"
+    assert bench.dtype_label(wl["qwen3-8b-q8_0"], "i8", "i8") == "q8_0/i8"
+    assert bench.dtype_label(wl["qwen3-8b-q8_0"], "i8", "f32") == "q8_0/i8+head_f32"
+    assert bench.dtype_label(wl["qwen3-8b-q8_0-paged-b64"], "f32", "f32") == "q8_0->bf16"
+    assert bench.q8_lane_label(wl["qwen3-8b-bf16-paged-b64"], "f32", "f32") is None
