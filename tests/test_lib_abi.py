@@ -66,6 +66,15 @@ def test_host_validation_without_gpu(lib):
     d.n_q_heads = 12
     assert lib.qd_create_layer(C.byref(d), C.byref(w), C.byref(h)) == -1      # Hq % Hkv != 0
     assert lib.qd_decode_step(None, None) == -1
+    # the batched Q8_0 GEMM: null pointers, cols not a multiple of 32, and cols that are a
+    # multiple of 32 but not of 256 (its scale boxes) are refused before any launch;
+    # the non-null pointers below are never dereferenced
+    fake = C.c_void_p(1 << 20)
+    assert lib.qd_gemm_q8_0(None, None, 128, 256, None, 2, None, None, 0, None) == -1
+    assert lib.qd_gemm_q8_0(fake, fake, 128, 300, fake, 2, fake, None, 0, None) == -1
+    assert lib.qd_gemm_q8_0(fake, fake, 128, 288, fake, 2, fake, None, 0, None) == -2
+    assert b"256" in lib.qd_last_error()
+    assert lib.qd_gemm_q8_0(fake, fake, 128, 256, fake, 65, fake, None, 0, None) == -2   # batch > 64
     # workspace sizing is pure host arithmetic
     assert lib.qd_attn_workspace_bytes(1, 32, 8, 4224) > 0
     assert lib.qd_attn_workspace_bytes(0, 32, 8, 4224) == 0
