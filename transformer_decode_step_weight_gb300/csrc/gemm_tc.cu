@@ -17,11 +17,13 @@
 //   * the four warps read their 32 TMEM lanes each (tcgen05.ld 32x32b.x64) and
 //     store y or add it to the residual stream.
 // Q8_0 weights (int8 values, an fp16 scale per 32 of a row; "emit_qwen38_generate"
-// rustdoc, "Where the speed comes from") take the same MMA: the producer streams the
-// int8 tile [128 x 64 B] and its scales with TMA, and eight converter warps widen
-// each weight to bf16(f32(d) * q) (exact product, one round to nearest even) into
-// the swizzled A tile the MMA reads. The tensor cores' int8 rate on this part is
-// far below their bf16 rate, so the int8 values are not fed to them directly.
+// rustdoc, "Where the speed comes from") take the same MMA and epilogue in a
+// 384-thread form: warp 0 streams the int8 tiles [128 x 64 B] and their scale boxes
+// with TMA, warp 2 the X tiles, and four groups of two converter warps widen each
+// weight to bf16(f32(d) * q) (exact product, one round to nearest even) into the
+// swizzled A tile the MMA reads, each group a different K step. The tensor cores'
+// int8 rate on this part is far below their bf16 rate, so the int8 values are not
+// fed to them directly.
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -39,9 +41,10 @@ namespace {
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBN = 64;         // tokens (MMA N, TMEM columns)
 constexpr int kBK = 64;         // K elements per stage (128 bytes of bf16)
-// Ring depth: 6 stages (one CTA per SM) when the CTAs fit in one wave, else 3
+// bf16 ring depth: 6 stages (one CTA per SM) when the CTAs fit in one wave, else 3
 // (~74 KB, two or three CTAs per SM, so a grid of up to twice the SM count still
-// runs in one wave). QD_GEMM_STAGES = 3 or 6 forces one.
+// runs in one wave). QD_GEMM_STAGES = 3 or 6 forces one. The Q8_0 form's rings
+// are set below (kQSt, kBSt, kASt).
 constexpr int kTileA = kBM * kBK * 2;    // 16 KB
 constexpr int kTileB = kBN * kBK * 2;    // 8 KB
 constexpr int kTileQ = kBM * kBK;        // 8 KB: int8 values of a Q8_0 tile
