@@ -281,13 +281,20 @@ int qd_step_launch_count(const qd_step_args* args);
 
 /* ------------------------------------------------------------------------ */
 /* Test-only exports (make the bit-exactness claims directly checkable).      */
-/* dots[r, b] = sum_i qs[r, 32b+i] * x_q[32b+i] as int32, [rows, cols/32].       */
-int qd_debug_q8_block_dots(const int8_t* qs, int rows, int cols, const int8_t* x_q,
-                           int32_t* dots, cudaStream_t stream);
+/* qd_debug_q8_block_dots runs the production Q8_0 GEMV of the i8 lane          */
+/* (qd_gemv_q8_0 with act = QD_ACT_I8 and x_q, x_d given: the same dispatch and  */
+/* kernels as the decode step's Q8_0 GEMVs) in a form that also stores each      */
+/* int32 block dot it forms: dots[r, b] = sum_i qs[r, 32b+i] * x_q[32b+i],        */
+/* int32 [rows, cols/32]; y: f32 [rows], the GEMV result.                        */
+int qd_debug_q8_block_dots(const int8_t* qs, const void* d_f16, int rows, int cols, const int8_t* x_q,
+                           const void* x_d_f16, int32_t* dots, float* y, cudaStream_t stream);
 /* idx[b, t] = page_table[b*max_pages + t/page_size]*page_size + t%page_size for */
-/* t < n_tokens (the physical token slot the attention kernel reads).           */
+/* t < n_tokens: the physical token slot the attention kernels read, through    */
+/* the same device function they use. A page id outside [0, n_pages) gives      */
+/* idx = -1 and sets QD_DEVERR_PAGE (the attention kernels read page 0 there).  */
 int qd_debug_paged_indices(const int32_t* page_table, int batch, int max_pages,
-                           int page_size, int n_tokens, int32_t* idx, cudaStream_t stream);
+                           int page_size, int n_pages, int n_tokens, int32_t* idx,
+                           cudaStream_t stream);
 
 #ifdef __cplusplus
 }

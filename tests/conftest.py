@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -21,3 +22,20 @@ def cuda_lib():
         pytest.skip("no CUDA device")
     from transformer_decode_step_weight_gb300 import api
     return api.lib()
+
+
+# Measured parity figures (errors, agreement counts) recorded by the GPU tests;
+# written as JSON to $QD_PARITY_LOG at the end of the session when that is set.
+_PARITY = {}
+
+
+@pytest.fixture(scope="session")
+def parity_log():
+    return _PARITY
+
+
+def pytest_sessionfinish(session, exitstatus):
+    path = os.environ.get("QD_PARITY_LOG")
+    if path and _PARITY:
+        with open(path, "w") as f:
+            json.dump(_PARITY, f, indent=1, sort_keys=True)

@@ -1,4 +1,5 @@
-"""Test-side glue: host copies of the seeded tensors in the oracle's form."""
+"""Test-side glue: host copies of the seeded tensors in the oracle's form, and the
+teacher-forced comparison of a GPU decode run with the oracle."""
 from __future__ import annotations
 
 import numpy as np
@@ -55,3 +56,59 @@ def rel_max_abs(got, ref) -> float:
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-300))
+
+
+# Relative max-abs error limits on logits / hidden states: BF16 path, f32-activation
+# Q8_0 lane, dp4a lane, and the batched Q8_0 path (tensor cores, weights widened).
+TOL = {"bf16": 2e-2, "f32": 5e-3, "i8": 2e-2, "w_bf16": 2e-2}
+
+
+def teacher_forced(dec, mt, steps, lanes, b=0, log=None):
+    """Run `steps` eager GPU decode steps of sequence b; check each against the oracle.
+
+    Protocol for greedy tokens (teacher-forced): the oracle follows the GPU's own
+    token stream. ``lanes`` is a list of (mode, act, lm_act, tol) oracle lanes the GPU
+    logits are held to, each with its own caches. At every step the logits must be
+    within the lane's relative max-abs tolerance, the GPU token must be the argmax of
+    the GPU logits, and it must equal the oracle's argmax unless the oracle's top-1 /
+    top-2 gap is below 4x the step's max-abs logit error (a near tie, logged). The
+    first lane decides the token agreement figures. Returns the log dict.
+    """
+    import torch
+
+    from transformer_decode_step_weight_gb300 import api
+    import oracle
+
+    om = oracle_model(mt)
+    pos0 = int(mt.seq_lens[b])
+    caches = [oracle_caches(mt, b, pos0 + steps) for _ in lanes]
+    tok = int(mt.start_tok[b])
+    st = {"steps": steps, "strict": 0, "near_ties": [], "worst_rel_err": [0.0] * len(lanes),
+          "lanes": [f"{m}/{a}/{la or a}" for m, a, la, _ in lanes]}
+    for t in range(steps):
+        dec.step()
+        torch.cuda.synchronize()
+        g = dec.logits[b].double().cpu().numpy()
+        gtok = int(dec.tok[b])
+        assert gtok == oracle.argmax_first(g), t
+        assert int(dec.out_tokens[b, t]) == gtok
+        for li, (mode, act, lm_act, tol) in enumerate(lanes):
+            ref = oracle.decode_token(om, tok, pos0 + t, caches[li][0], caches[li][1], mode=mode, act=act,
+                                      lm_act=lm_act)
+            err = rel_max_abs(g, ref)
+            st["worst_rel_err"][li] = max(st["worst_rel_err"][li], err)
+            assert err < tol, (t, li, err)
+            otok = oracle.argmax_first(ref)
+            if gtok != otok:
+                top = np.sort(ref)[-2:]
+                gap = float(top[1] - top[0])
+                assert gap < 4 * np.max(np.abs(g - ref)), (t, li, gtok, otok, gap)
+                if li == 0:
+                    st["near_ties"].append({"step": t, "gpu": gtok, "oracle": otok, "gap": gap})
+            elif li == 0:
+                st["strict"] += 1
+        tok = gtok
+    assert api.check_device_error() == 0
+    if log is not None:
+        log.update(st)
+    return st

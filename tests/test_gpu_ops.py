@@ -104,14 +104,23 @@ def test_quantize_q8_0_bit_exact(cuda_lib):
     assert np.array_equal(synth.bits_u16(xd), rd)
 
 
-@pytest.mark.parametrize("R,K", [(33, 64), (1000, 1024), (4096, 4096), (3000, 12288)])
+@pytest.mark.parametrize("R,K", [(33, 64), (513, 96), (1000, 1024), (4096, 4096), (3000, 12288), (6144, 4096)])
 def test_q8_block_dots_bit_exact(cuda_lib, R, K):
-    qs, _ = _q8(R, K, R)
+    # the production i8-lane GEMV stores the int32 block dots it forms (K % 256 == 0:
+    # the TMA-ring form the decode step runs; otherwise the register-streaming form)
+    qs, d = _q8(R, K, R)
     x = torch.randn(K, generator=_gen(K), device=DEV)
-    xq, _ = api.quantize_q8_0(x)
-    dots = api.debug_q8_block_dots(qs, xq)
+    xq, xd = api.quantize_q8_0(x)
+    dots, y = api.debug_q8_block_dots(qs, d, xq, xd)
+    torch.cuda.synchronize()
     ref = oracle.q8_0_block_dots(synth.host_i8(qs), synth.host_i8(xq))
     assert np.array_equal(dots.cpu().numpy().astype(np.int64), ref)
+    yref = oracle.gemv_q8_0(synth.host_i8(qs), synth.bits_u16(d), xq=synth.host_i8(xq), xd_bits=synth.bits_u16(xd),
+                            act="i8")
+    assert rel_max_abs(y.cpu().numpy(), yref) < GEMV_TOL
+    # the same launch without the dump gives the same bits
+    y2 = api.gemv_q8_0(qs, d, xq=xq, xd=xd, act=api.QD_ACT_I8)
+    assert torch.equal(y, y2)
 
 
 @pytest.mark.parametrize("R,K", [(37, 64), (1000, 1024), (6144, 4096), (4096, 12288), (151936, 1024)])
@@ -149,9 +158,11 @@ def test_gemv_q8_0_unit_scales_integer_exact(cuda_lib):
 @pytest.mark.parametrize("R,K,B,split", [(128, 256, 2, False), (300, 768, 17, False), (1000, 1536, 64, True),
                                          (6144, 4096, 64, True), (4096, 12288, 64, True),
                                          (151936, 4096, 64, False)])
-def test_gemm_q8_0_tensor_cores(cuda_lib, R, K, B, split):
+def test_gemm_q8_0_tensor_cores(cuda_lib, R, K, B, split, parity_log):
     # Q8_0 weights widened to bf16 on chip: ragged last 128-row tile, batch below 64,
-    # K split across CTAs (partials summed in split order) where the grid is small
+    # K split across CTAs (partials summed in split order) where the grid is small.
+    # Held to the widened-weight lane element by element and to the pages' Q8_0
+    # definition w = f32(d) q at the bf16 path's tolerance (the widening error).
     qs, d = _q8(R, K, R + 5)
     x = torch.randn((B, K), generator=_gen(K + 5), device=DEV).to(torch.bfloat16)
     ws = None
@@ -165,9 +176,15 @@ def test_gemm_q8_0_tensor_cores(cuda_lib, R, K, B, split):
     assert torch.equal(y, y2)
     qh, dh, xb = synth.host_i8(qs), synth.bits_u16(d), synth.bits_u16(x)
     rows = np.arange(R) if R <= 8192 else np.arange(0, R, 97)
+    worst = 0.0
     for b in sorted({0, B // 2, B - 1}):
         ref = oracle.gemv_q8_0(qh[rows], dh[rows], x=oracle.bf16_to_f64(xb[b]), act="w_bf16")
         assert rel_max_abs(y[b].cpu().numpy()[rows], ref) < GEMV_TOL, b
+        ref = oracle.gemv_q8_0(qh[rows], dh[rows], x=oracle.bf16_to_f64(xb[b]), act="f32")
+        err = rel_max_abs(y[b].cpu().numpy()[rows], ref)
+        worst = max(worst, err)
+        assert err < 2e-2, (b, err)
+    parity_log[f"gemm_q8_0_vs_q8_0_definition/{R}x{K}x{B}"] = worst
     assert api.check_device_error() == 0
 
 
@@ -301,12 +318,23 @@ def test_attention_is_deterministic(cuda_lib):
 
 
 def test_paged_indices_bit_exact(cuda_lib):
+    # through the page-table lookup the attention kernels use
     g = _gen(11)
     pt = torch.randperm(40, generator=g, device=DEV).to(torch.int32).reshape(4, 10)
-    idx = api.debug_paged_indices(pt, 16, 150)
+    idx = api.debug_paged_indices(pt, 16, 150, n_pages=40)
     ptn = pt.cpu().numpy()
     ref = np.array([[oracle.paged_token_index(ptn[b], t, 16) for t in range(150)] for b in range(4)])
     assert np.array_equal(idx.cpu().numpy(), ref)
+    for ps in (1, 7, 32):
+        idx = api.debug_paged_indices(pt, ps, 10 * ps, n_pages=40)
+        ref = np.array([[oracle.paged_token_index(ptn[b], t, ps) for t in range(10 * ps)] for b in range(4)])
+        assert np.array_equal(idx.cpu().numpy(), ref), ps
+    assert api.check_device_error() == 0
+    # an id outside the cache is not followed: -1 there and the page error bit
+    pt[1, 2] = 40
+    idx = api.debug_paged_indices(pt, 16, 150, n_pages=40).cpu().numpy()
+    assert np.all(idx[1, 32:48] == -1) and np.all(idx[1, :32] >= 0) and np.all(idx[1, 48:] >= 0)
+    assert api.check_device_error() == 1
 
 
 def test_rope_table_matches_definition(cuda_lib):

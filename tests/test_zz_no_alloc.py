@@ -16,8 +16,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from helpers import rel_max_abs
-from transformer_decode_step_weight_gb300 import api
+from transformer_decode_step_weight_gb300 import api, synth
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -53,6 +54,36 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(cuda_lib):
         torch.cuda.synchronize()
         for b in range(len(lens)):
             assert rel_max_abs(got[b].cpu().numpy(), ref[b].cpu().numpy()) < TOL, (seed, b)
+            assert rel_max_abs(got[b].cpu().numpy(), _oracle_attention(q, kp, vp, pt, lens, b, scale)) < TOL
+    assert api.check_device_error() == 0
+
+
+def _oracle_attention(q, kp, vp, pt, lens, b, scale):
+    """The oracle's GQA attention of sequence b over its gathered pages."""
+    n = lens[b]
+    k = oracle.bf16_to_f64(oracle.gather_paged(synth.bits_u16(kp), pt[b].cpu().numpy(), n))
+    v = oracle.bf16_to_f64(oracle.gather_paged(synth.bits_u16(vp), pt[b].cpu().numpy(), n))
+    return oracle.gqa_attention(q[b].double().cpu().numpy(), k, v, scale)
+
+
+def test_noalloc_tensor_core_form_matches_workspace_and_oracle(cuda_lib):
+    # batch x kv heads at or above the SM count: the tensor-core attention runs on the
+    # static scratch (its tickets cleared by the call). Two calls in a row.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B = -(-sms // 8) + 5
+    scale = 1 / math.sqrt(128)
+    for seed in (3, 4):
+        rng = np.random.default_rng(seed)
+        lens = [int(v) for v in rng.integers(1, 300, B)]
+        q, kp, vp, pt, sl = _case(seed, lens)
+        assert api.attn_workspace_bytes(B, 32, 8, pt.shape[1] * 16) <= 8 << 20
+        ref = api.attn_decode_paged(q, kp, vp, pt, sl, scale)
+        got = api.attn_decode_paged_noalloc(q, kp, vp, pt, sl, scale)
+        torch.cuda.synchronize()
+        for b in range(B):
+            assert rel_max_abs(got[b].cpu().numpy(), ref[b].cpu().numpy()) < TOL, (seed, b)
+        for b in (0, B // 2, B - 1):
+            assert rel_max_abs(got[b].cpu().numpy(), _oracle_attention(q, kp, vp, pt, lens, b, scale)) < TOL
     assert api.check_device_error() == 0
 
 

@@ -74,8 +74,8 @@ _SIGS = {
     "qd_graph_launch": (_i, [_vp, _vp]),
     "qd_graph_destroy": (_i, [_vp]),
     "qd_check_device_error": (_i, [_vp, C.POINTER(_i)]),
-    "qd_debug_q8_block_dots": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
-    "qd_debug_paged_indices": (_i, [_vp, _i, _i, _i, _i, _vp, _vp]),
+    "qd_debug_q8_block_dots": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "qd_debug_paged_indices": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
 }
 
 _lib = None
@@ -218,17 +218,21 @@ def check_device_error(stream=None) -> int:
     return bits.value
 
 
-def debug_q8_block_dots(qs, xq, stream=None):
+def debug_q8_block_dots(qs, d, xq, xd, stream=None):
+    """(int32 block dots [R, K/32], f32 y [R]) of the production i8-lane Q8_0 GEMV."""
     R, K = qs.shape
     dots = torch.empty((R, K // 32), dtype=torch.int32, device=qs.device)
-    _check(lib().qd_debug_q8_block_dots(_p(qs), R, K, _p(xq), _p(dots), _stream(stream)))
-    return dots
+    y = torch.empty(R, dtype=torch.float32, device=qs.device)
+    _check(lib().qd_debug_q8_block_dots(_p(qs), _p(d), R, K, _p(xq), _p(xd), _p(dots), _p(y), _stream(stream)))
+    return dots, y
 
 
-def debug_paged_indices(page_table, page_size, n_tokens, stream=None):
+def debug_paged_indices(page_table, page_size, n_tokens, n_pages=None, stream=None):
     B, max_pages = page_table.shape
+    if n_pages is None:
+        n_pages = max_pages * B
     idx = torch.empty((B, n_tokens), dtype=torch.int32, device=page_table.device)
-    _check(lib().qd_debug_paged_indices(_p(page_table), B, max_pages, page_size, n_tokens, _p(idx),
+    _check(lib().qd_debug_paged_indices(_p(page_table), B, max_pages, page_size, n_pages, n_tokens, _p(idx),
                                         _stream(stream)))
     return idx
 

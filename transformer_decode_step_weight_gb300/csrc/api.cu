@@ -809,21 +809,29 @@ int qd_check_device_error(cudaStream_t stream, int* bits) {
 }
 
 // ------------------------------------------------------------------ test exports
-int qd_debug_q8_block_dots(const int8_t* qs, int rows, int cols, const int8_t* x_q, int32_t* dots,
-                           cudaStream_t stream) {
-  if (!qs || !x_q || !dots || rows < 1 || cols < 32 || cols % 32)
+int qd_debug_q8_block_dots(const int8_t* qs, const void* d_f16, int rows, int cols, const int8_t* x_q,
+                           const void* x_d_f16, int32_t* dots, float* y, cudaStream_t stream) {
+  if (!qs || !d_f16 || !x_q || !x_d_f16 || !dots || !y || rows < 1 || cols < 32 || cols % 32)
     return fail(QD_ERR_INVALID_ARG, "qd_debug_q8_block_dots: bad arguments");
-  if (!aligned16(qs) || !aligned16(x_q)) return fail(QD_ERR_INVALID_ARG, "qd_debug_q8_block_dots: alignment");
-  cudaError_t e = launch_q8_block_dots(qs, rows, cols, x_q, dots, make_launch(stream, false));
+  if (!gemv_q8_supported(cols)) return fail(QD_ERR_UNSUPPORTED, "qd_debug_q8_block_dots: cols=%d too large", cols);
+  if (!aligned16(qs) || !aligned16(x_q) || !aligned16(y) || ((uintptr_t)d_f16 & 1u) || ((uintptr_t)x_d_f16 & 1u))
+    return fail(QD_ERR_INVALID_ARG, "qd_debug_q8_block_dots: alignment");
+  // the production i8-lane GEMV (the same dispatch as qd_gemv_q8_0), storing its block dots
+  GemvQ8Args a = {};
+  a.qs = qs; a.d = d_f16; a.R = rows; a.K = cols; a.act = QD_ACT_I8;
+  a.pro = PRO_X_F32; a.x = nullptr; a.xq = x_q; a.xd = x_d_f16;
+  a.epi = EPI_STORE; a.y = y; a.dots = dots;
+  cudaError_t e = launch_gemv_q8(a, make_launch(stream, false));
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_debug_q8_block_dots");
 }
 
-int qd_debug_paged_indices(const int32_t* page_table, int batch, int max_pages, int page_size, int n_tokens,
-                           int32_t* idx, cudaStream_t stream) {
-  if (!page_table || !idx || batch < 1 || max_pages < 1 || page_size < 1 || n_tokens < 0 ||
+int qd_debug_paged_indices(const int32_t* page_table, int batch, int max_pages, int page_size, int n_pages,
+                           int n_tokens, int32_t* idx, cudaStream_t stream) {
+  if (!page_table || !idx || batch < 1 || max_pages < 1 || page_size < 1 || n_pages < 1 || n_tokens < 0 ||
       (long long)n_tokens > (long long)max_pages * page_size)
     return fail(QD_ERR_INVALID_ARG, "qd_debug_paged_indices: bad arguments");
-  cudaError_t e = launch_paged_indices(page_table, batch, max_pages, page_size, n_tokens, idx, stream);
+  cudaError_t e = launch_paged_indices(page_table, batch, max_pages, page_size, n_pages, n_tokens, idx,
+                                       make_launch(stream, false));
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_debug_paged_indices");
 }
 

@@ -123,14 +123,10 @@ QD_DEV void issue_tile(const AttnParams& p, int b, int g, int t, int n, __nv_bfl
   const int ps = p.page_size;
   const int t0 = t, end = t + n;
   while (t < end) {
-    const int lp = t / ps;
-    int page = pt[lp];
-    if (page < 0 || page >= p.n_pages) {
-      set_error(p.err, QD_DEVERR_PAGE);
-      page = 0;
-    }
-    const int seg_end = min(end, (lp + 1) * ps);
-    const size_t off = (((size_t)page * p.Hkv + g) * ps + (t - lp * ps)) * kD;
+    const PagedSlot ps_t = paged_slot(pt, t, ps, p.n_pages);
+    if (!ps_t.ok) set_error(p.err, QD_DEVERR_PAGE);
+    const int seg_end = min(end, t + (ps - ps_t.slot));
+    const size_t off = (((size_t)ps_t.page * p.Hkv + g) * ps + ps_t.slot) * kD;
     const uint32_t bytes = (uint32_t)(seg_end - t) * kD * 2;
     bulk_g2s(sK + (size_t)(t - t0) * kD, p.k_pages + off, bytes, bar);
     bulk_g2s(sV + (size_t)(t - t0) * kD, p.v_pages + off, bytes, bar);
@@ -277,12 +273,12 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   const int d = tid & (kD - 1);
   float2 cs = make_float2(0.f, 0.f);
   float wq = 0.f, wk = 0.f;
-  int own_page = -1;
+  PagedSlot own = {0, 0, false};
   if (FUSED) {
     cs = p.rope[(size_t)pos * (kD / 2) + (d & 63)];
     wq = __bfloat162float(p.q_norm[d]);
     wk = __bfloat162float(p.k_norm[d]);
-    if (own_pos) own_page = p.page_table[(size_t)b * p.max_pages + pos / p.page_size];
+    if (own_pos) own = paged_slot(p.page_table + (size_t)b * p.max_pages, pos, p.page_size, p.n_pages);
   }
   pdl_wait();  // q, k, v (and, standalone, the caller's q) come from the previous kernel
   if (!p.pf_late) prefetch_next();
@@ -335,12 +331,10 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
     if (own_pos && dim_thread) {  // this split holds the current token: store k, v in the cache
       k_new = round_bf16(r[REP]);
       v_new = round_bf16(vx);
-      const int lp = pos / p.page_size;
-      const int page = own_page;
-      if (page < 0 || page >= p.n_pages) {
+      if (!own.ok) {
         if (tid == 0) set_error(p.err, QD_DEVERR_PAGE);
       } else {
-        const size_t off = (((size_t)page * p.Hkv + g) * p.page_size + (pos - lp * p.page_size)) * kD + d;
+        const size_t off = (((size_t)own.page * p.Hkv + g) * p.page_size + own.slot) * kD + d;
         p.k_pages[off] = __float2bfloat16_rn(k_new);
         p.v_pages[off] = __float2bfloat16_rn(v_new);
       }

@@ -118,13 +118,9 @@ QD_DEV void load_tile(const MParams& p, int b, int g, int t, int t_valid_end, in
     const bool ok = tok < t_valid_end && tok != skip_tok;
     size_t off = 0;
     if (ok) {
-      const int lp = tok / ps;
-      int page = pt[lp];
-      if (page < 0 || page >= p.n_pages) {
-        set_error(p.err, QD_DEVERR_PAGE);
-        page = 0;
-      }
-      off = (((size_t)page * p.Hkv + g) * ps + (tok - lp * ps)) * kD + c * 8;
+      const PagedSlot sl = paged_slot(pt, tok, ps, p.n_pages);
+      if (!sl.ok) set_error(p.err, QD_DEVERR_PAGE);
+      off = (((size_t)sl.page * p.Hkv + g) * ps + sl.slot) * kD + c * 8;
     }
     cp_async16(sK + swz(r, c), p.k_pages + off, ok ? 16 : 0);
     cp_async16(sV + swz(r, c), p.v_pages + off, ok ? 16 : 0);
@@ -154,13 +150,9 @@ QD_DEV void load_tile_tma(const MParams& p, const CUtensorMap* tmK, const CUtens
     const int tok = t + 16 * k;
     rows[k] = -1;
     if (tok < t_valid_end) {
-      const int lp = tok / ps;
-      int page = pt[lp];
-      if (page < 0 || page >= p.n_pages) {
-        set_error(p.err, QD_DEVERR_PAGE);
-        page = 0;
-      }
-      rows[k] = (page * p.Hkv + g) * ps + (tok - lp * ps);
+      const PagedSlot sl = paged_slot(pt, tok, ps, p.n_pages);
+      if (!sl.ok) set_error(p.err, QD_DEVERR_PAGE);
+      rows[k] = (sl.page * p.Hkv + g) * ps + sl.slot;
       ++nseg;
     }
   }
@@ -304,12 +296,11 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
     if (own_pos) {
       k_new = round_bf16(r[REP]);
       v_new = round_bf16(vx);
-      const int lp = pos / p.page_size;
-      const int page = p.page_table[(size_t)b * p.max_pages + lp];
-      if (page < 0 || page >= p.n_pages) {
+      const PagedSlot own = paged_slot(p.page_table + (size_t)b * p.max_pages, pos, p.page_size, p.n_pages);
+      if (!own.ok) {
         if (tid == 0) set_error(p.err, QD_DEVERR_PAGE);
       } else {
-        const size_t off = (((size_t)page * p.Hkv + g) * p.page_size + (pos - lp * p.page_size)) * kD + tid;
+        const size_t off = (((size_t)own.page * p.Hkv + g) * p.page_size + own.slot) * kD + tid;
         p.k_pages_w[off] = __float2bfloat16_rn(k_new);
         p.v_pages_w[off] = __float2bfloat16_rn(v_new);
       }

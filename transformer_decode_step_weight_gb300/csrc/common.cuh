@@ -81,6 +81,23 @@ QD_DEV float warp_max(float v) {
   return v;
 }
 
+// Physical place of logical token t of a sequence in a paged K/V cache: the
+// page-table row pt_row names the page of logical page t / ps, and the token
+// sits in slot t % ps of it. Every kernel that reads or writes the cache through
+// a page table, and the test export of the gather indices, go through this
+// function. A page id outside [0, n_pages) is not followed: ok is false and the
+// page is 0 (callers set QD_DEVERR_PAGE).
+struct PagedSlot {
+  int page, slot;
+  bool ok;
+};
+QD_DEV PagedSlot paged_slot(const int32_t* pt_row, int t, int ps, int n_pages) {
+  const int lp = t / ps;
+  const int page = pt_row[lp];
+  const bool ok = page >= 0 && page < n_pages;
+  return PagedSlot{ok ? page : 0, t - lp * ps, ok};
+}
+
 // Sticky device error word (bits QD_DEVERR_*), one per process.
 QD_DEV void set_error(int* err, int bit) {
   if (err) atomicOr(err, bit);

@@ -262,7 +262,10 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
       // ---- MMA issuer
       for (int i = 0; i < n_k; ++i) {
         const int s = i % kStagesTc;
-        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kStagesTc) & 1), p.err)) break;
+        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / kStagesTc) & 1), p.err)) {
+          s_abort = 1;  // D holds a partial sum: the epilogue must not store it
+          break;
+        }
         tc_fence_after();
         mma_stage(smem_u32(sA + s * kTileA), smem_u32(sB + s * kTileB), i);
         mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
@@ -305,8 +308,11 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
       // ---- MMA issuer
       for (int i = 0; i < n_k; ++i) {
         const int sa = i % kASt, sb = i % kBSt;
-        if (!mbar_wait_bounded(&full[sb], (uint32_t)((i / kBSt) & 1), p.err)) break;
-        if (!mbar_wait_bounded(&conv[sa], (uint32_t)((i / kASt) & 1), p.err)) break;
+        if (!mbar_wait_bounded(&full[sb], (uint32_t)((i / kBSt) & 1), p.err) ||
+            !mbar_wait_bounded(&conv[sa], (uint32_t)((i / kASt) & 1), p.err)) {
+          s_abort = 1;
+          break;
+        }
         tc_fence_after();
         mma_stage(smem_u32(sA + sa * kTileA), smem_u32(sB + sb * kTileB), i);
         mma_commit(&aempty[sa]);
@@ -324,8 +330,11 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
       const int t = ((warp - 4) & 1) * 32 + lane;
       for (int i = grp; i < n_k; i += kConvGroups) {
         const int sq = i % kQSt, sa = i % kASt;
-        if (!mbar_wait_bounded(&qfull[sq], (uint32_t)((i / kQSt) & 1), p.err)) break;
-        if (i >= kASt && !mbar_wait_bounded(&aempty[sa], (uint32_t)(((i / kASt) - 1) & 1), p.err)) break;
+        if (!mbar_wait_bounded(&qfull[sq], (uint32_t)((i / kQSt) & 1), p.err) ||
+            (i >= kASt && !mbar_wait_bounded(&aempty[sa], (uint32_t)(((i / kASt) - 1) & 1), p.err))) {
+          s_abort = 1;
+          break;
+        }
         const int kt = kb0 + i;
         const unsigned char* q = sQ + sq * kTileQ;
         const __half* sc = (const __half*)(sS + sq * kTileS);
@@ -354,6 +363,8 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
     }
   }
   __syncwarp();
+  // every role has left its loop: an abort flag set by any of them is visible below
+  __syncthreads();
 
   // ---- epilogue: warp w < 4 owns TMEM lanes [32w, 32w + 32) = rows row0 + 32w + lane
   pdl_wait();

@@ -44,6 +44,7 @@ struct Q8Params {
   float eps;
   int epi;
   float* y;
+  int32_t* dots;   // DUMP: the int32 block dots [R, K/32] this launch forms (i8 lane)
 };
 
 QD_DEV uint16_t ld_stream_u16(const void* p) {
@@ -63,10 +64,22 @@ QD_DEV void i8x4_to_f32(uint32_t w, float* f) {
 
 QD_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// Exact int32 dot of a 16-weight half-block with the matching 16 int8 activation
+// codes (four dp4a steps). Both GEMV forms use it; the two halves of a 32-block
+// sit in adjacent lanes, so the block dot is this value plus the neighbour's.
+QD_DEV int q8_half_dot(const uint32_t (&w)[4], const uint32_t (&x)[4]) {
+  int acc = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc = __dp4a((int)w[k], (int)x[k], acc);
+  return acc;
+}
+
 // Prologue that takes an already quantised activation (int8 + f16 scales).
 constexpr int PRO_Q8_GIVEN = 16;
 
-template <int C, int LANE, int U>
+// DUMP: the i8 lane also stores each int32 block dot it forms (the test export
+// of the bit-exact block dots runs the production kernel this way).
+template <int C, int LANE, int U, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 1) gemv_q8_kernel(const Q8Params p) {
   extern __shared__ float red[];
   __shared__ float s_ss[kThreads / 32];
@@ -237,9 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_q8_kernel(const Q8Params p) 
               }
               s = fmaf(dw, bs, s);
             } else {
-              int acc = 0;
-#pragma unroll
-              for (int w = 0; w < 4; ++w) acc = __dp4a((int)wv[w], (int)xq[j][w], acc);
+              const int acc = q8_half_dot(wv, xq[j]);
+              if (DUMP) {
+                const int other = __shfl_xor_sync(0xffffffffu, acc, 1);
+                if ((t & 1) == 0 && cv[j]) p.dots[(size_t)(r0 + ph0 + lr) * KB + (ch[j] >> 1)] = acc + other;
+              }
               s = fmaf((float)acc, dw * xd[j], s);
             }
           }
@@ -275,24 +290,10 @@ __global__ void quantize_q8_kernel(const float* x, int n, int8_t* xq, __half* xd
   if (lane == 0) xd[blk] = __float2half_rn(d);
 }
 
-__global__ void q8_block_dots_kernel(const int8_t* qs, int R, int K, const int8_t* xq, int32_t* dots) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int KB = K / 32;
-  if (i >= (long long)R * KB) return;
-  const long long r = i / KB;
-  const int b = (int)(i % KB);
-  const int* w = (const int*)(qs + r * K + (size_t)b * 32);
-  const int* a = (const int*)(xq + (size_t)b * 32);
-  int acc = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) acc = __dp4a(w[k], a[k], acc);
-  dots[i] = acc;
-}
-
-template <int C, int LANE>
+template <int C, int LANE, bool DUMP = false>
 cudaError_t launch_cl(const Q8Params& p, int grid, int threads, size_t smem, const Launch& L) {
   constexpr int U = 8 / C;
-  auto k = gemv_q8_kernel<C, LANE, U>;
+  auto k = gemv_q8_kernel<C, LANE, U, DUMP>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
@@ -339,6 +340,7 @@ struct RingQ8Params {
   int w_evict_first;
   int* claim;            // null: static split; else [claim, done] counters
   int static_per_cta;
+  int32_t* dots;         // DUMP: the int32 block dots [R, K/32] this launch forms (i8 lane)
 };
 
 QD_DEV void cons_sync_q() { asm volatile("bar.sync 1, %0;" ::"n"(kConsQ) : "memory"); }
@@ -346,7 +348,7 @@ QD_DEV void mbar_arrive_q(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-template <int C, int LANE, int RPS>
+template <int C, int LANE, int RPS, bool DUMP>
 __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const RingQ8Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
@@ -645,9 +647,11 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
           }
           acc = fmaf(dw[r][j], bs + bs2, acc);
         } else {
-          int dot = 0;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) dot = __dp4a((int)w4[w], (int)xq[j][w], dot);
+          const int dot = q8_half_dot(w4, xq[j]);
+          if (DUMP) {  // rows are units here (EPI_STORE): stage unit c0 + local row
+            const int other = __shfl_xor_sync(0xffffffffu, dot, 1);
+            if ((t & 1) == 0 && r < nv && cv[j]) p.dots[(size_t)(c0 + row0 + r) * KB + (ch[j] >> 1)] = dot + other;
+          }
           acc = fmaf((float)dot, dw[r][j] * xd[j], acc);
         }
       }
@@ -691,10 +695,10 @@ __global__ void __launch_bounds__(kConsQ + 32, 1) gemv_q8_ring_kernel(const Ring
   flush();
 }
 
-template <int C, int LANE>
+template <int C, int LANE, bool DUMP = false>
 cudaError_t launch_ring_q(const RingQ8Params& p, int grid, size_t smem, const Launch& L) {
   constexpr int RPS = C == 1 ? 8 : C == 2 ? 4 : 2;
-  auto k = gemv_q8_ring_kernel<C, LANE, RPS>;
+  auto k = gemv_q8_ring_kernel<C, LANE, RPS, DUMP>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -732,6 +736,7 @@ bool gemv_q8_swiglu_ok(int K) {
 }
 
 cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
+  if (a.dots && (a.act != 1 || a.epi != EPI_STORE)) return cudaErrorInvalidValue;  // i8 lane, plain rows
   const bool aligned = (((uintptr_t)a.qs | (uintptr_t)a.d) & 15) == 0;
   const int rc = (a.K % 256 == 0 && aligned) ? ring_q_c(a.K) : 0;
   if (rc > 0) {
@@ -765,7 +770,16 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
     size_t smem = (size_t)p.ring_bytes + 32 * 8 + 32 * 4 + (size_t)kPhaseQ * (p.T / 32) * 4 +
                   (size_t)kPhaseQ * 4 * 2 + (size_t)kPhaseQ / 2 * 4;
     smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
+    p.dots = a.dots;
     if ((size_t)p.ns * p.stage_bytes <= (size_t)kRingQ * 2) {
+      if (a.dots) {
+        switch (rc) {
+          case 1: return launch_ring_q<1, 1, true>(p, grid, smem, L);
+          case 2: return launch_ring_q<2, 1, true>(p, grid, smem, L);
+          case 3: return launch_ring_q<3, 1, true>(p, grid, smem, L);
+          default: return launch_ring_q<4, 1, true>(p, grid, smem, L);
+        }
+      }
       switch (rc) {
         case 1: return a.act == 1 ? launch_ring_q<1, 1>(p, grid, smem, L) : launch_ring_q<1, 0>(p, grid, smem, L);
         case 2: return a.act == 1 ? launch_ring_q<2, 1>(p, grid, smem, L) : launch_ring_q<2, 0>(p, grid, smem, L);
@@ -794,7 +808,15 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
   p.xq = a.xq; p.xd = (const __half*)a.xd;
   if (a.act == 1 && a.xq != nullptr) p.pro = PRO_Q8_GIVEN;
   p.epi = a.epi; p.y = a.y;
+  p.dots = a.dots;
   const size_t smem = (size_t)phase_rows * wpg * 4;
+  if (a.dots) {
+    switch (C) {
+      case 1: return launch_cl<1, 1, true>(p, grid, threads, smem, L);
+      case 2: return launch_cl<2, 1, true>(p, grid, threads, smem, L);
+      default: return launch_cl<4, 1, true>(p, grid, threads, smem, L);
+    }
+  }
   switch (C) {
     case 1: return a.act == 1 ? launch_cl<1, 1>(p, grid, threads, smem, L) : launch_cl<1, 0>(p, grid, threads, smem, L);
     case 2: return a.act == 1 ? launch_cl<2, 1>(p, grid, threads, smem, L) : launch_cl<2, 0>(p, grid, threads, smem, L);
@@ -807,14 +829,6 @@ cudaError_t launch_quantize_q8(const float* x, int n, int8_t* xq, void* xd, cons
   const int blocks = ceil_div((long long)n, threads);
   if (blocks == 0) return cudaSuccess;
   return launch_ex(quantize_q8_kernel, dim3(blocks), dim3(threads), 0, L, x, n, xq, (__half*)xd);
-}
-
-cudaError_t launch_q8_block_dots(const int8_t* qs, int R, int K, const int8_t* xq, int32_t* dots,
-                                 const Launch& L) {
-  const long long n = (long long)R * (K / 32);
-  if (n == 0) return cudaSuccess;
-  q8_block_dots_kernel<<<(int)((n + 255) / 256), 256, 0, L.stream>>>(qs, R, K, xq, dots);
-  return cudaGetLastError();
 }
 
 }  // namespace qd

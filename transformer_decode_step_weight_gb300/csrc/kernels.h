@@ -111,14 +111,14 @@ struct GemvQ8Args {
   float* y;
   int w_evict_first;      // ring form: weight copies marked evict-first in L2
   int* claim;             // ring form: two zero ints; part of the rows is claimed by free CTAs
+  int32_t* dots;          // i8 lane, EPI_STORE: also store the int32 block dots [R, K/32] the
+                          // launch forms (test export of their bit-exactness); null: none
 };
 bool gemv_q8_supported(int K);
 // True when a Q8_0 GEMV of K columns takes the ring form and can take EPI_SWIGLU.
 bool gemv_q8_swiglu_ok(int K);
 cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L);
 cudaError_t launch_quantize_q8(const float* x, int n, int8_t* xq, void* xd, const Launch& L);
-cudaError_t launch_q8_block_dots(const int8_t* qs, int R, int K, const int8_t* xq, int32_t* dots,
-                                 const Launch& L);
 
 // ----------------------------------------------------------------- attention
 struct AttnArgs {
@@ -172,7 +172,7 @@ cudaError_t launch_argmax_advance(const float* logits, int V, int B, int32_t* to
                                   const Launch& L);
 cudaError_t launch_embed(const void* embed, int H, int V, const int32_t* tok, int B, float* res,
                          const Launch& L);
-cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_tokens,
-                                 int32_t* idx, cudaStream_t s);
+cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_pages, int n_tokens,
+                                 int32_t* idx, const Launch& L);
 
 }  // namespace qd

@@ -197,12 +197,16 @@ __global__ void __launch_bounds__(256) swiglu_rows_kernel(const float* gu, int F
   }
 }
 
-__global__ void paged_indices_kernel(const int32_t* pt, int B, int max_pages, int ps, int n,
-                                     int32_t* idx) {
+// The physical token slot of logical token t, through the attention kernels' own
+// page-table lookup (paged_slot); -1 and QD_DEVERR_PAGE for an id out of range.
+__global__ void paged_indices_kernel(const int32_t* pt, int B, int max_pages, int ps, int n_pages, int n,
+                                     int32_t* idx, int* err) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)B * n) return;
   const int b = (int)(i / n), t = (int)(i % n);
-  idx[i] = pt[(size_t)b * max_pages + t / ps] * ps + t % ps;
+  const PagedSlot sl = paged_slot(pt + (size_t)b * max_pages, t, ps, n_pages);
+  if (!sl.ok) set_error(err, QD_DEVERR_PAGE);
+  idx[i] = sl.ok ? sl.page * ps + sl.slot : -1;
 }
 
 }  // namespace
@@ -258,12 +262,12 @@ cudaError_t launch_swiglu_rows(const float* gu, int B, int F, void* out_bf16, co
   return launch_ex(swiglu_rows_kernel, dim3(blocks, B), dim3(256), 0, L, gu, F, (__nv_bfloat16*)out_bf16);
 }
 
-cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_tokens,
-                                 int32_t* idx, cudaStream_t s) {
+cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_pages, int n_tokens,
+                                 int32_t* idx, const Launch& L) {
   const long long n = (long long)B * n_tokens;
   if (n == 0) return cudaSuccess;
-  paged_indices_kernel<<<(int)((n + 255) / 256), 256, 0, s>>>(pt, B, max_pages, ps, n_tokens, idx);
-  return cudaGetLastError();
+  return launch_ex(paged_indices_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, L, pt, B, max_pages, ps,
+                   n_pages, n_tokens, idx, L.err);
 }
 
 }  // namespace qd
