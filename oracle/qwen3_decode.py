@@ -39,6 +39,14 @@ Readings where those pages are silent (each also listed in the design notes):
   * Argmax: the lowest index among equal maxima; NaN never wins; an all-NaN
     row gives index 0.
 
+Accumulation. Every product-sum (the projections) is accumulated in float64
+(``acc="f64"``, the default). ``acc="f32"`` evaluates the same sums in IEEE
+binary32 instead (operands widened exactly, the library's own summation order).
+It is not a model of any kernel: it is a second, equally valid evaluation of the
+same rounded computation, used to measure how far a deep bf16 model's outputs move
+under ulp-level differences in accumulation alone (the floor any implementation
+that does not accumulate in float64 sits on).
+
 Precision modes. ``exact`` computes every step in float64 with no rounding
 (used by the closed-form pins). ``bf16`` additionally rounds to bfloat16 at the
 points where the bf16 decode step stores a value in bf16: the two RMSNorm
@@ -178,14 +186,24 @@ def gemv(w, x) -> np.ndarray:
     return np.asarray(w, dtype=np.float64) @ np.asarray(x, dtype=np.float64)
 
 
-def gemv_bf16(w_bits, x, row_chunk: int = 8192) -> np.ndarray:
+def _matvec(w, x, acc: str):
+    """w @ x with float64 accumulation, or in binary32 (w and x rounded to binary32
+    first; exact for bf16 / Q8_0 weights and for bf16 or binary32 activations)."""
+    if acc == "f64":
+        return w @ x
+    if acc == "f32":
+        return (np.asarray(w, dtype=np.float32) @ np.asarray(x, dtype=np.float32)).astype(np.float64)
+    raise ValueError(acc)
+
+
+def gemv_bf16(w_bits, x, row_chunk: int = 8192, acc: str = "f64") -> np.ndarray:
     """y = W x with W given as bf16 bits [R, K]; widened a block of rows at a time."""
     w_bits = np.asarray(w_bits)
     x = np.asarray(x, dtype=np.float64)
     r = w_bits.shape[0]
     y = np.empty(r, dtype=np.float64)
     for r0 in range(0, r, row_chunk):
-        y[r0:r0 + row_chunk] = bf16_to_f64(w_bits[r0:r0 + row_chunk]) @ x
+        y[r0:r0 + row_chunk] = _matvec(bf16_to_f64(w_bits[r0:r0 + row_chunk]), x, acc)
     return y
 
 
@@ -247,7 +265,7 @@ def q8_0_block_dots(qs, xq) -> np.ndarray:
 
 
 def gemv_q8_0(qs, d_bits, x=None, xq=None, xd_bits=None, act: str = "f32",
-              row_chunk: int = 8192) -> np.ndarray:
+              row_chunk: int = 8192, acc: str = "f64") -> np.ndarray:
     """Q8_0 GEMV, both lanes of the "emit_qwen38_generate" rustdoc's ``deq`` knob.
 
     act == "f32": y_r = sum_b f32(d_rb) * sum_i q_rbi * x_bi   (dequantising lane)
@@ -261,19 +279,20 @@ def gemv_q8_0(qs, d_bits, x=None, xq=None, xd_bits=None, act: str = "f32",
     if act == "f32":
         x = np.asarray(x, dtype=np.float64)
         for r0 in range(0, r, row_chunk):
-            y[r0:r0 + row_chunk] = q8_0_dequant(qs[r0:r0 + row_chunk],
-                                                np.asarray(d_bits)[r0:r0 + row_chunk]) @ x
+            y[r0:r0 + row_chunk] = _matvec(q8_0_dequant(qs[r0:r0 + row_chunk],
+                                                        np.asarray(d_bits)[r0:r0 + row_chunk]), x, acc)
     elif act == "i8":
         dx = f16_to_f64(xd_bits)
+        ft = np.float64 if acc == "f64" else np.float32
         for r0 in range(0, r, row_chunk):
-            dots = q8_0_block_dots(qs[r0:r0 + row_chunk], xq).astype(np.float64)
-            dw = f16_to_f64(np.asarray(d_bits)[r0:r0 + row_chunk])
-            y[r0:r0 + row_chunk] = (dots * dw * dx[None, :]).sum(axis=1)
+            dots = q8_0_block_dots(qs[r0:r0 + row_chunk], xq).astype(ft)
+            dw = f16_to_f64(np.asarray(d_bits)[r0:r0 + row_chunk]).astype(ft)
+            y[r0:r0 + row_chunk] = (dots * dw * dx.astype(ft)[None, :]).sum(axis=1, dtype=ft)
     elif act == "w_bf16":
         x = np.asarray(x, dtype=np.float64)
         for r0 in range(0, r, row_chunk):
-            y[r0:r0 + row_chunk] = q8_0_widen_bf16(qs[r0:r0 + row_chunk],
-                                                   np.asarray(d_bits)[r0:r0 + row_chunk]) @ x
+            y[r0:r0 + row_chunk] = _matvec(q8_0_widen_bf16(qs[r0:r0 + row_chunk],
+                                                           np.asarray(d_bits)[r0:r0 + row_chunk]), x, acc)
     else:
         raise ValueError(act)
     return y
@@ -360,7 +379,7 @@ class LayerWeights:
     s_down: np.ndarray | None = None
 
 
-def project(w, s, x, act: str):
+def project(w, s, x, act: str, acc: str = "f64"):
     """One weight-streaming projection for either storage format.
 
     act == "bf16": W bf16, x already in its storage precision.
@@ -369,19 +388,19 @@ def project(w, s, x, act: str):
     act == "w_bf16": Q8_0 weights widened to bf16, x bf16 (batched tensor-core step).
     """
     if act == "bf16":
-        return gemv_bf16(w, x)
+        return gemv_bf16(w, x, acc=acc)
     if act == "f32":
-        return gemv_q8_0(w, s, x=x, act="f32")
+        return gemv_q8_0(w, s, x=x, act="f32", acc=acc)
     if act == "i8":
         xq, xd = q8_0_quantize(np.asarray(x, dtype=np.float64).astype(np.float32))
-        return gemv_q8_0(w, s, xq=xq, xd_bits=xd, act="i8")
+        return gemv_q8_0(w, s, xq=xq, xd_bits=xd, act="i8", acc=acc)
     if act == "w_bf16":
-        return gemv_q8_0(w, s, x=x, act="w_bf16")
+        return gemv_q8_0(w, s, x=x, act="w_bf16", acc=acc)
     raise ValueError(act)
 
 
 def layer_step(dims: Dims, lw: LayerWeights, res, k_cache, v_cache, pos: int,
-               mode: str = "bf16", act: str = "bf16", trace: dict | None = None):
+               mode: str = "bf16", act: str = "bf16", trace: dict | None = None, acc: str = "f64"):
     """One decoder layer for one token at position ``pos``.
 
     Pipeline order from "GPU Kernel Lab" README, "Decode integration":
@@ -396,7 +415,7 @@ def layer_step(dims: Dims, lw: LayerWeights, res, k_cache, v_cache, pos: int,
     H, D, hq, hkv, F = dims.hidden, dims.head_dim, dims.n_q_heads, dims.n_kv_heads, dims.ffn
     res = np.asarray(res, dtype=np.float64).copy()
     xn = rmsnorm(res, bf16_to_f64(lw.ln_in), dims.rms_eps, mode)
-    qkv = project(lw.w_qkv, lw.s_qkv, xn, act)
+    qkv = project(lw.w_qkv, lw.s_qkv, xn, act, acc)
     q = qkv[:hq * D].reshape(hq, D)
     k = qkv[hq * D:(hq + hkv) * D].reshape(hkv, D)
     v = qkv[(hq + hkv) * D:].reshape(hkv, D)
@@ -408,11 +427,11 @@ def layer_step(dims: Dims, lw: LayerWeights, res, k_cache, v_cache, pos: int,
     v_cache[:, pos, :] = kv_rnd(v)
     o = gqa_attention(q, k_cache[:, :pos + 1, :], v_cache[:, :pos + 1, :])
     o = rnd(o.reshape(-1))
-    res = res + project(lw.w_o, lw.s_o, o, act)
+    res = res + project(lw.w_o, lw.s_o, o, act, acc)
     xn2 = rmsnorm(res, bf16_to_f64(lw.ln_post), dims.rms_eps, mode)
-    gu = project(lw.w_gu, lw.s_gu, xn2, act)
+    gu = project(lw.w_gu, lw.s_gu, xn2, act, acc)
     a = rnd(silu(gu[:F]) * gu[F:])
-    res = res + project(lw.w_down, lw.s_down, a, act)
+    res = res + project(lw.w_down, lw.s_down, a, act, acc)
     if trace is not None:
         trace.update(q=q, k=k, v=v, attn=o, xn=xn, xn2=xn2, gu=gu)
     return res
@@ -431,7 +450,7 @@ class Model:
 
 def decode_token(model: Model, tok: int, pos: int, k_caches, v_caches,
                  mode: str = "bf16", act: str = "bf16", lm_act: str | None = None,
-                 residual_trace: list | None = None):
+                 residual_trace: list | None = None, acc: str = "f64"):
     """Logits for one token at position ``pos``; the caches gain slot ``pos``.
 
     "GPU Kernel Lab" README, "Decode integration": embedding row of the token
@@ -444,12 +463,12 @@ def decode_token(model: Model, tok: int, pos: int, k_caches, v_caches,
     for li, lw in enumerate(model.layers):
         if residual_trace is not None:
             residual_trace.append(res.copy())
-        res = layer_step(d, lw, res, k_caches[li], v_caches[li], pos, mode, act)
+        res = layer_step(d, lw, res, k_caches[li], v_caches[li], pos, mode, act, acc=acc)
     if residual_trace is not None:
         residual_trace.append(res.copy())
     xf = rmsnorm(res, bf16_to_f64(model.final_norm), d.rms_eps, mode)
     lm_act = act if lm_act is None else lm_act
-    return project(model.lm_head, model.lm_head_scales, xf, lm_act)
+    return project(model.lm_head, model.lm_head_scales, xf, lm_act, acc)
 
 
 def lm_head_rows(model: Model, final_res, rows, mode: str = "bf16", act: str = "bf16"):

@@ -63,7 +63,7 @@ def rel_max_abs(got, ref) -> float:
 TOL = {"bf16": 2e-2, "f32": 5e-3, "i8": 2e-2, "w_bf16": 2e-2}
 
 
-def teacher_forced(dec, mt, steps, lanes, b=0, log=None):
+def teacher_forced(dec, mt, steps, lanes, b=0, floor_factor=None, lm_resync=False):
     """Run `steps` eager GPU decode steps of sequence b; check each against the oracle.
 
     Protocol for greedy tokens (teacher-forced): the oracle follows the GPU's own
@@ -72,8 +72,19 @@ def teacher_forced(dec, mt, steps, lanes, b=0, log=None):
     within the lane's relative max-abs tolerance, the GPU token must be the argmax of
     the GPU logits, and it must equal the oracle's argmax unless the oracle's top-1 /
     top-2 gap is below 4x the step's max-abs logit error (a near tie, logged). The
-    first lane decides the token agreement figures. Returns the log dict.
+    first lane decides the token agreement figures.
+
+    floor_factor: the end-to-end limit of lane 0 becomes max(tol, floor_factor x the
+    oracle's own drift), the drift being how far the oracle's logits of step 0 move
+    when its sums are accumulated in binary32 instead of float64 (``acc="f32"``). In a
+    deep model of bf16-rounded activations, ulp-level differences flip roundings that
+    the following layers amplify; this measures that floor for the model at hand.
+    lm_resync: at step 0 also hold the GPU logits to the oracle's LM head applied to
+    the GPU's own final hidden state (every row), at the lane's tolerance.
+    Returns the log dict.
     """
+    import copy
+
     import torch
 
     from transformer_decode_step_weight_gb300 import api
@@ -83,6 +94,7 @@ def teacher_forced(dec, mt, steps, lanes, b=0, log=None):
     pos0 = int(mt.seq_lens[b])
     caches = [oracle_caches(mt, b, pos0 + steps) for _ in lanes]
     tok = int(mt.start_tok[b])
+    tols = [ln[3] for ln in lanes]
     st = {"steps": steps, "strict": 0, "near_ties": [], "worst_rel_err": [0.0] * len(lanes),
           "lanes": [f"{m}/{a}/{la or a}" for m, a, la, _ in lanes]}
     for t in range(steps):
@@ -92,12 +104,25 @@ def teacher_forced(dec, mt, steps, lanes, b=0, log=None):
         gtok = int(dec.tok[b])
         assert gtok == oracle.argmax_first(g), t
         assert int(dec.out_tokens[b, t]) == gtok
-        for li, (mode, act, lm_act, tol) in enumerate(lanes):
+        for li, (mode, act, lm_act, _) in enumerate(lanes):
+            if t == 0 and li == 0 and floor_factor is not None:
+                kc, vc = copy.deepcopy(caches[0][0]), copy.deepcopy(caches[0][1])
+                r32 = oracle.decode_token(om, tok, pos0, kc, vc, mode=mode, act=act, lm_act=lm_act, acc="f32")
             ref = oracle.decode_token(om, tok, pos0 + t, caches[li][0], caches[li][1], mode=mode, act=act,
                                       lm_act=lm_act)
+            if t == 0 and li == 0 and floor_factor is not None:
+                st["floor"] = rel_max_abs(r32, ref)
+                tols[0] = max(tols[0], floor_factor * st["floor"])
+                st["tol"] = tols[0]
+            if t == 0 and li == 0 and lm_resync:
+                xf = oracle.rmsnorm(dec.residual()[b].double().cpu().numpy(), oracle.bf16_to_f64(om.final_norm),
+                                    om.dims.rms_eps, mode)
+                lm_ref = oracle.project(om.lm_head, om.lm_head_scales, xf, lm_act or act)
+                st["lm_head_resync_err"] = rel_max_abs(g, lm_ref)
+                assert st["lm_head_resync_err"] < lanes[0][3], st["lm_head_resync_err"]
             err = rel_max_abs(g, ref)
             st["worst_rel_err"][li] = max(st["worst_rel_err"][li], err)
-            assert err < tol, (t, li, err)
+            assert err < tols[li], (t, li, err, tols[li])
             otok = oracle.argmax_first(ref)
             if gtok != otok:
                 top = np.sort(ref)[-2:]
@@ -109,6 +134,49 @@ def teacher_forced(dec, mt, steps, lanes, b=0, log=None):
                 st["strict"] += 1
         tok = gtok
     assert api.check_device_error() == 0
-    if log is not None:
-        log.update(st)
     return st
+
+
+def per_layer_resync(mt, lane, mode, act, tol, b=0):
+    """Step 0 of a contiguous-cache model one layer at a time, on the GPU's own inputs.
+
+    The GPU's residual after l layers comes from a decoder over the first l layers of
+    the same tensors (the step is deterministic, so layer l - 1 sees the same input
+    inside every prefix); the oracle applies layer l - 1 to the GPU's residual after
+    l - 1 layers. Each layer's output and the K/V row it writes to the cache are held
+    to `tol`, so rounding differences do not compound across layers here. Returns the
+    worst error of each.
+    """
+    import dataclasses
+
+    import torch
+
+    from transformer_decode_step_weight_gb300 import api
+    import oracle
+
+    om = oracle_model(mt)
+    pos = int(mt.seq_lens[b])
+    ks, vs = oracle_caches(mt, b, pos + 1)
+    x = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[b])]))
+    worst = {"layer": 0.0, "kv": 0.0}
+    for li in range(len(mt.layers)):
+        sub = dataclasses.replace(mt, layers=mt.layers[:li + 1], k_cache=mt.k_cache[:li + 1],
+                                  v_cache=mt.v_cache[:li + 1])
+        dec = api.Decoder(sub, max_steps=1, act=lane)
+        dec.step()
+        torch.cuda.synchronize()
+        got = dec.residual()[b].double().cpu().numpy()
+        dec.close()
+        ref = oracle.layer_step(om.dims, om.layers[li], x, ks[li], vs[li], pos, mode=mode, act=act)
+        err = rel_max_abs(got, ref)
+        worst["layer"] = max(worst["layer"], err)
+        assert err < tol, (li, err)
+        page = int(mt.page_table[b, pos // mt.page_size])
+        slot = pos % mt.page_size
+        for cache, ref_c in ((mt.k_cache[li], ks[li]), (mt.v_cache[li], vs[li])):
+            row = oracle.bf16_to_f64(synth.bits_u16(cache[page, :, slot, :]))
+            e = rel_max_abs(row, ref_c[:, pos])
+            worst["kv"] = max(worst["kv"], e)
+            assert e < tol, (li, e)
+        x = got
+    return worst

@@ -5,10 +5,20 @@ tokens with logits within tolerance ("GPU Kernel Lab" README, "Measured final
 results": the decode path is gated on argmax agreement with the reference over a
 whole decode run). These tests run the full models of the benchmark workloads (36
 layers at context 4096 for BF16, 36 Q8_0 layers at context 2048 on both activation
-lanes, 28 layers for Qwen3-0.6B in test_gpu_step) for several greedy steps through
-the C ABI, teacher-forced (helpers.teacher_forced): logits of every step within the
-relative max-abs tolerance, the GPU token the oracle's argmax except at logged near
-ties. The oracle takes several seconds per 8B token on the host cores.
+lanes; 28 layers of Qwen3-0.6B in test_gpu_step) through the C ABI:
+
+  * every layer on the GPU's own input against the oracle's layer (no compounding),
+    and the K/V row each layer writes (helpers.per_layer_resync);
+  * the LM head on the GPU's own final hidden state, every row;
+  * several greedy steps end to end, teacher-forced (helpers.teacher_forced): the GPU
+    token is the oracle's argmax except at logged near ties, and the logits are within
+    max(tolerance, 3 x the oracle's own accumulation drift). In a random-weight model
+    of 36 bf16-rounded layers, ulp-level differences flip roundings that later layers
+    amplify: merely accumulating the oracle's sums in binary32 instead of float64
+    moves its Qwen3-8B logits by about 1.6e-2, so the end-to-end limit is set from
+    that floor, measured in the test.
+
+The oracle takes several seconds per 8B token on the host cores.
 """
 import gc
 
@@ -34,8 +44,10 @@ def _free(*objs):
 def test_qwen3_8b_bf16_model_teacher_forced(cuda_lib, parity_log):
     steps = 8
     mt = synth.make_model(synth.QWEN3_8B, "bf16", 0, DEV, ctx=4096, steps=steps)
+    layers = per_layer_resync(mt, api.QD_ACT_F32, "bf16", "bf16", tol=1e-2)
     dec = api.Decoder(mt, max_steps=steps)
-    st = teacher_forced(dec, mt, steps, [("bf16", "bf16", None, TOL["bf16"])])
+    st = teacher_forced(dec, mt, steps, [("bf16", "bf16", None, TOL["bf16"])], floor_factor=3.0, lm_resync=True)
+    st["per_layer_worst"] = layers
     parity_log["qwen3_8b_bf16_model"] = st
     # near ties are accepted by the protocol and logged; a systematic mismatch is not
     assert st["strict"] >= steps // 2
@@ -49,8 +61,10 @@ def test_qwen3_8b_q8_0_model_teacher_forced(cuda_lib, parity_log):
     steps = 6
     mt = synth.make_model(synth.QWEN3_8B, "q8_0", 1, DEV, ctx=2048, steps=steps)
     for act, lane in (("f32", api.QD_ACT_F32), ("i8", api.QD_ACT_I8)):
+        layers = per_layer_resync(mt, lane, "f32", act, tol=TOL[act])
         dec = api.Decoder(mt, max_steps=steps, act=lane)
-        st = teacher_forced(dec, mt, steps, [("f32", act, None, TOL[act])])
+        st = teacher_forced(dec, mt, steps, [("f32", act, None, TOL[act])], floor_factor=3.0, lm_resync=True)
+        st["per_layer_worst"] = layers
         parity_log[f"qwen3_8b_q8_0_model/{act}"] = st
         assert st["strict"] >= steps // 2, act
         _free(dec)

@@ -217,3 +217,41 @@ def test_layer_rounds_the_swiglu_product_q8_0_f32_lane():
     out = oracle.layer_step(oracle.Dims(H, HQ, HKV, D, F, rms_eps=0.0), lq, ones(H), kc, vc, pos=3,
                             mode="f32", act="f32")
     assert out[0] == 41 + 2**-17
+
+
+# ---------------------------------------------------------------- accumulation precision
+
+
+def test_f32_accumulation_exact_on_integers_and_within_the_summation_bound():
+    rng = np.random.default_rng(31)
+    # small integers: every partial sum is exact in binary32, so both accumulations agree
+    w = rng.integers(-8, 9, size=(40, 512)).astype(np.float64)
+    x = rng.integers(-8, 9, size=512).astype(np.float64)
+    bits = oracle.f64_to_bf16_bits(w)
+    np.testing.assert_array_equal(oracle.gemv_bf16(bits, x, acc="f32"), oracle.gemv_bf16(bits, x))
+    ones = np.full((40, 16), 0x3C00, dtype=np.uint16)
+    qs = rng.integers(-127, 128, size=(40, 512)).astype(np.int8)
+    np.testing.assert_array_equal(oracle.gemv_q8_0(qs, ones, x=x, act="f32", acc="f32"),
+                                  oracle.gemv_q8_0(qs, ones, x=x, act="f32"))
+    # random bf16 operands: |y32 - y64| <= gamma_(K+1) * sum |w| |x| for any summation
+    # order (the classical bound, u = 2^-24), and binary32 is really what is used
+    K = 4096
+    wb = oracle.f64_to_bf16_bits(rng.standard_normal((64, K)) * 0.02)
+    xb = oracle.round_bf16(rng.standard_normal(K))
+    y64, y32 = oracle.gemv_bf16(wb, xb), oracle.gemv_bf16(wb, xb, acc="f32")
+    u = 2.0 ** -24
+    gamma = (K + 1) * u / (1 - (K + 1) * u)
+    bound = gamma * (np.abs(oracle.bf16_to_f64(wb)) @ np.abs(xb))
+    assert np.all(np.abs(y32 - y64) <= bound)
+    assert np.any(y32 != y64)
+    np.testing.assert_array_equal(y32, y32.astype(np.float32).astype(np.float64))
+    # the dp4a lane: exact integer dots scaled and summed in binary32
+    xq, xd = oracle.q8_0_quantize(rng.standard_normal(K).astype(np.float32))
+    d = (np.abs(rng.standard_normal((64, K // 32))) * 0.002).astype(np.float16).view(np.uint16)
+    q = rng.integers(-127, 128, size=(64, K)).astype(np.int8)
+    a64 = oracle.gemv_q8_0(q, d, xq=xq, xd_bits=xd, act="i8")
+    a32 = oracle.gemv_q8_0(q, d, xq=xq, xd_bits=xd, act="i8", acc="f32")
+    terms = np.abs(oracle.q8_0_block_dots(q, xq) * oracle.f16_to_f64(d) * oracle.f16_to_f64(xd)[None, :]).sum(axis=1)
+    nb = K // 32
+    assert np.all(np.abs(a32 - a64) <= (nb + 3) * u / (1 - (nb + 3) * u) * terms)
+    assert np.any(a32 != a64)

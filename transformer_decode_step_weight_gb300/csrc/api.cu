@@ -424,6 +424,7 @@ struct StepWs {
   int* claims;      // [5 L + 1][2] row-claim counters of the batch-1 Q8_0 GEMVs (zero between launches)
   void* gemm_ws;    // batched path: split-K partials and tickets (one GEMM at a time)
   size_t gemm_ws_bytes;
+  void* stream_ws;  // batch-1 BF16: the persistent step kernel's partials, counters, candidates
   size_t total;
 };
 
@@ -461,8 +462,44 @@ StepWs step_ws_layout(const qd_step_args* a, void* base) {
       w.gemm_ws_bytes = std::max(w.gemm_ws_bytes, gemm_tc_workspace_bytes(sh[0], sh[1], sh[2] != 0));
   }
   off += al256(w.gemm_ws_bytes);
+  w.stream_ws = (void*)(p + off);
+  if (a->batch == 1 && d.wtype == QD_W_BF16) off += al256(stream_ws_bytes(a->n_layers, d.n_q_heads, d.n_kv_heads));
   w.total = off;
   return w;
+}
+
+// QD_STEP_PATH (read on every call): "persistent" runs a batch-1 BF16 step as the
+// one persistent step kernel (step_stream.cu) when its shape allows; anything else
+// keeps the one-kernel-per-operation path.
+bool step_kernels_forced() {
+  const char* v = getenv("QD_STEP_PATH");
+  return !(v && strcmp(v, "persistent") == 0);
+}
+
+// The persistent batch-1 step (step_stream.cu): its arguments, and whether it takes
+// this step.
+bool stream_args(const qd_step_args* a, const StepWs& w, std::vector<StreamLayerPtrs>& lp, StreamStepArgs& s) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  if (a->batch != 1 || d.wtype != QD_W_BF16 || a->lm_head_scales || a->n_layers > kStreamMaxLayers) return false;
+  lp.resize(a->n_layers);
+  for (int i = 0; i < a->n_layers; ++i) {
+    const qd_layer_weights& lw = a->layers[i]->w;
+    lp[i] = StreamLayerPtrs{lw.w_qkv, lw.w_o, lw.w_gu, lw.w_down, lw.ln_in, lw.ln_post, lw.q_norm, lw.k_norm,
+                            a->k_cache[i], a->v_cache[i]};
+  }
+  s = StreamStepArgs{};
+  s.layers = lp.data();
+  s.n_layers = a->n_layers;
+  s.H = d.hidden; s.Hq = d.n_q_heads; s.Hkv = d.n_kv_heads; s.F = d.ffn; s.V = a->vocab;
+  s.eps = d.rms_eps;
+  s.embed = a->embed; s.final_norm = a->final_norm; s.lm_head = a->lm_head;
+  s.page_table = a->page_table; s.page_size = a->page_size; s.max_pages = a->max_pages; s.n_pages = a->n_pages;
+  s.rope = a->rope_table; s.rope_max_pos = a->rope_max_pos;
+  s.tok = a->tok; s.pos = a->pos; s.step = a->step; s.out_tokens = a->out_tokens; s.max_steps = a->max_steps;
+  s.logits = a->logits;
+  s.res = w.res; s.qkv = w.qkv; s.attn = w.attn; s.h = w.xn;
+  s.ws = w.stream_ws;
+  return stream_step_supported(s);
 }
 
 int validate_step(const qd_step_args* a) {
@@ -582,6 +619,14 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   if (tc_step(a)) return run_step_tc(a, stream);
   const qd_layer_dims& d = a->layers[0]->dims;
   const StepWs w = step_ws_layout(a, a->workspace);
+  if (!step_kernels_forced()) {
+    std::vector<StreamLayerPtrs> lp;
+    StreamStepArgs sa;
+    if (stream_args(a, w, lp, sa)) {
+      QD_TRY(launch_stream_step(sa, make_launch(stream, false)), "persistent step");
+      return QD_OK;
+    }
+  }
   const Launch L = make_launch(stream, true);
   const int B = a->batch;
   const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
@@ -731,8 +776,13 @@ size_t qd_step_workspace_bytes(const qd_step_args* a) {
 }
 
 int qd_step_launch_count(const qd_step_args* a) {
-  if (!a || a->n_layers < 1) return 0;
+  if (!a || a->n_layers < 1 || !a->layers || !a->layers[0]) return 0;
   if (tc_step(a)) return 1 + 8 * a->n_layers + 3;
+  if (!step_kernels_forced()) {
+    std::vector<StreamLayerPtrs> lp;
+    StreamStepArgs sa;
+    if (stream_args(a, step_ws_layout(a, a->workspace), lp, sa)) return 1;
+  }
   return 1 + 5 * a->n_layers + 2;
 }
 

@@ -165,6 +165,39 @@ size_t attn_noalloc_scratch_bytes();
 cudaError_t attn_noalloc_scratch(int B, int Hq, int Hkv, int max_ctx, void** ptr, cudaStream_t stream);
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float theta, cudaStream_t s);
 
+// ----------------------------------------------------------------- persistent batch-1 step
+// The whole decode step of a BF16 model at batch 1 as one cooperative kernel
+// (step_stream.cu). res / qkv / attn / h are the step workspace's activation
+// buffers (f32 [H], f32 [QKV], bf16 [Hq D], bf16 [F]); ws is its own zero-filled
+// scratch of stream_ws_bytes() (split partials, phase counters, argmax candidates),
+// which every launch leaves zero-filled again unless a wait timed out.
+constexpr int kStreamMaxLayers = 64;
+struct StreamLayerPtrs {
+  const void *w_qkv, *w_o, *w_gu, *w_down, *ln_in, *ln_post, *q_norm, *k_norm;
+  void *k_cache, *v_cache;
+};
+struct StreamStepArgs {
+  const StreamLayerPtrs* layers;  // host array [n_layers]
+  int n_layers, H, Hq, Hkv, F, V;
+  float eps;
+  const void *embed, *final_norm, *lm_head;
+  const int32_t* page_table;
+  int page_size, max_pages, n_pages;
+  const float* rope;
+  int rope_max_pos;
+  int32_t *tok, *pos, *step, *out_tokens;
+  int max_steps;
+  float* logits;
+  float* res;
+  float* qkv;
+  void* attn;
+  void* h;
+  void* ws;
+};
+size_t stream_ws_bytes(int n_layers, int Hq, int Hkv);
+bool stream_step_supported(const StreamStepArgs& a);
+cudaError_t launch_stream_step(const StreamStepArgs& a, const Launch& L);
+
 // ----------------------------------------------------------------- misc
 size_t argmax_workspace_bytes(int B);
 cudaError_t launch_argmax_advance(const float* logits, int V, int B, int32_t* tok, int32_t* pos,
