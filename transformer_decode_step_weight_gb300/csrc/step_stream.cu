@@ -57,7 +57,10 @@ constexpr int kST = kCT + 32;           // plus the producer warp
 #define QD_STREAM_STAGES 4
 #endif
 #ifndef QD_STREAM_PF_AHEAD
-#define QD_STREAM_PF_AHEAD 6
+#define QD_STREAM_PF_AHEAD 4
+#endif
+#ifndef QD_STREAM_PF_STALL
+#define QD_STREAM_PF_STALL 12
 #endif
 constexpr int kStageB = QD_STREAM_STAGE_KB * 1024;  // bytes per ring stage
 constexpr int kNSt = QD_STREAM_STAGES;              // ring stages
@@ -66,7 +69,9 @@ constexpr int kTokS = kStageB / (kD * 2 * 2);  // K/V tokens per stage (96)
 constexpr int kFlush = 128;             // rows per reduction window
 constexpr int kMaxSplit = 64;           // attention splits per kv head
 constexpr int kMaxPair = 256;           // gate/up pairs per CTA
-constexpr int kPfAhead = QD_STREAM_PF_AHEAD;  // stages the L2 fetch runs ahead of the ring
+constexpr int kMaxOwnRows = 256;        // residual rows per CTA (kept in shared memory)
+constexpr int kPfAhead = QD_STREAM_PF_AHEAD;  // stages the L2 read-ahead leads the copies by
+constexpr int kPfStall = QD_STREAM_PF_STALL;  // ... and how far it may run on while stalled
 constexpr int kHP = 8;                  // q heads padded to the MMA N
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -75,7 +80,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // set by qd_stream_trace_set. The product build compiles none of this.
 #ifdef QD_STREAM_TRACE
 __device__ unsigned long long* g_stream_trace = nullptr;
-constexpr int kTraceStride = 1024;  // events per CTA
+constexpr int kTraceStride = 4096;  // events per CTA
 #define STRACE(ev)                                                                      \
   do {                                                                                \
     if (g_stream_trace) g_stream_trace[(size_t)blockIdx.x * kTraceStride + (ev)] = global_ns(); \
@@ -136,7 +141,8 @@ struct Carve {
   static constexpr size_t ml = pbuf + (size_t)kCW * 2 * kHP * 16 * 2;  // [2][kCW][8] f32
   static constexpr size_t ared = ml + 2 * kCW * kHP * 4;               // [4][9] f32 + [128] f32
   static constexpr size_t obuf = ared + 64 * 4 + kD * 4;               // [kCW][4][128] f32 (q staging first)
-  static constexpr size_t total = obuf + (size_t)kCW * 4 * kD * 4;
+  static constexpr size_t resown = obuf + (size_t)kCW * 4 * kD * 4;  // [kMaxOwnRows] f32
+  static constexpr size_t total = resown + (size_t)kMaxOwnRows * 4;
 };
 constexpr size_t kSmemBytes = Carve::total + 1024;  // + alignment slack of the ring
 
@@ -156,6 +162,7 @@ struct Smem {
   float* ared;
   float* sx;
   float* obuf;
+  float* resown;  // this CTA's rows of the residual (the rows its O and down phases own)
 };
 
 // ---------------------------------------------------------------- sync primitives
@@ -172,6 +179,14 @@ QD_DEV bool cbar_and(bool v) {
       : "r"((uint32_t)v), "n"(kCT)
       : "memory");
   return r != 0;
+}
+QD_DEV void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+QD_DEV int atom_acq_rel_add(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 QD_DEV int ld_acquire(const int* p) {
   int v;
@@ -411,21 +426,10 @@ QD_DEV void prefetch_stage(const SParams& p, const Ctx& x, const Cursor& c) {
   }
 }
 
-// producer-side wait: bounded, and it stops early once the consumers have aborted
-QD_DEV bool prod_wait(uint64_t* bar, uint32_t parity, volatile int* s_abort, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (int i = 0; i < (1 << 24); ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63) {
-      if (*s_abort) return false;
-      if (global_ns() - t0 > 1000000000ull) break;
-    }
-  }
-  set_error(err, QD_DEVERR_TIMEOUT);
-  return false;
-}
-
+// The producer runs the L2 read-ahead kPfAhead stages ahead of its copies while
+// the stream flows, and up to kPfStall stages ahead while it waits for a free ring
+// slot (the consumers are stalled on a dependency): HBM then keeps fetching the
+// coming weights into L2, and the ring refills from L2 once the consumers resume.
 QD_DEV void producer(const SParams& p, const STmaps& tm, const Ctx& x, const Smem& S, volatile int* s_abort) {
   const uint64_t pol = policy_evict_first();
   Cursor cp, pf;
@@ -434,26 +438,52 @@ QD_DEV void producer(const SParams& p, const STmaps& tm, const Ctx& x, const Sme
   cp.it = pf.it = get_item(p, x, 0);
   cur_settle(p, x, cp);
   cur_settle(p, x, pf);
-  for (int i = 0; i < kPfAhead && pf.it.kind != IT_END; ++i) {
+  int ahead = 0;  // stages the read-ahead cursor is in front of the copy cursor
+  auto pf_step = [&]() {
     prefetch_stage(p, x, pf);
     ++pf.k;
     cur_settle(p, x, pf);
-  }
+    ++ahead;
+  };
+  while (ahead < kPfAhead && pf.it.kind != IT_END) pf_step();
   int issued = 0;
+  bool ok = true;
   while (cp.it.kind != IT_END) {
     const int slot = issued % kNSt;
-    if (issued >= kNSt && !prod_wait(&S.empty[slot], (uint32_t)(((issued / kNSt) - 1) & 1), s_abort, p.err)) break;
-    if (*s_abort) break;
+    if (issued >= kNSt) {
+      uint64_t* bar = &S.empty[slot];
+      const uint32_t parity = (uint32_t)(((issued / kNSt) - 1) & 1);
+      if (!mbar_try_wait(bar, parity)) {
+        const uint64_t t0 = global_ns();
+        bool got = false;
+        for (int i = 0; i < (1 << 24); ++i) {
+          if (mbar_try_wait(bar, parity)) {
+            got = true;
+            break;
+          }
+          if (ahead < kPfStall && pf.it.kind != IT_END) pf_step();
+          if ((i & 63) == 63 && (*s_abort || global_ns() - t0 > 1000000000ull)) break;
+        }
+        if (!got) {
+          if (!*s_abort) set_error(p.err, QD_DEVERR_TIMEOUT);
+          ok = false;
+        }
+      }
+    }
+    if (!ok || *s_abort) break;
     if (cp.k == 0) STRACE(512 + cp.idx);
+    if (cp.it.kind == IT_KV && cp.k < 4) STRACE(3000 + 10 * cp.it.layer + cp.k);
     issue_stage(p, tm, x, cp, S.ring + (size_t)slot * kStageB, &S.full[slot], pol);
     ++issued;
     ++cp.k;
     cur_settle(p, x, cp);
-    if (pf.it.kind != IT_END) {
-      prefetch_stage(p, x, pf);
+    if (ahead > 0) {
+      --ahead;
+    } else if (pf.it.kind != IT_END) {  // the read-ahead fell level: move it along without fetching
       ++pf.k;
       cur_settle(p, x, pf);
     }
+    while (ahead < kPfAhead && pf.it.kind != IT_END) pf_step();
   }
   // a CTA never exits with a copy still landing in its shared memory
   for (int i = max(0, issued - kNSt); i < issued; ++i)
@@ -472,11 +502,27 @@ QD_DEV float dot8(const uint4& w, const float* x) {
   return a + b;
 }
 QD_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+QD_DEV uint32_t bf16x2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
+  return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
+
+// Consumers: wait until *cnt >= target (thread 0 polls, the others wait at the
+// consumer barrier). False on a timeout or an abort, which then ends this CTA too.
+QD_DEV bool cwait(const int* cnt, int target, const Smem& S, int* abort_w, int* err, volatile int* s_abort) {
+  if (cnt == nullptr) return true;
+  if (threadIdx.x == 0) S.misc_i[1] = wait_count(cnt, target, abort_w, err) ? 1 : 0;
+  cbar();
+  const bool r = S.misc_i[1] != 0;
+  if (!r && threadIdx.x == 0) *s_abort = 1;
+  return r;
+}
 
 enum { P_NORM_RES = 0, P_NORM_EMB = 1, P_BF16 = 2 };
 enum { E_STORE = 0, E_RES = 1, E_PAIR = 2, E_LM = 3 };
 
 struct GemvJob {
+  const int* wait_cnt;       // dependency: *wait_cnt >= wait_target before the activation is read
+  int wait_target;
   int K;
   int pro;
   const __nv_bfloat16* xb;   // P_NORM_EMB: embedding row; P_BF16: activation
@@ -484,6 +530,7 @@ struct GemvJob {
   int epi;
   float* y;                  // E_STORE / E_LM
   const __nv_bfloat16* emb;  // E_RES: residual base from this embedding row (first layer's O)
+  int trace_ev;              // profiling build: the event stamped once the wait is over
 };
 
 struct Cand {
@@ -501,7 +548,7 @@ QD_DEV int c_of(int K) {
 // reduction windows, epilogue. Returns false on an abort.
 template <int C>
 QD_DEV bool gemv_item(const SParams& p, const Item& it, const GemvJob& J, const Smem& S, int& gs, Cand& best,
-                      volatile int* s_abort) {
+                      volatile int* s_abort, int* abort_w) {
   constexpr int RB = C == 1 ? 8 : C == 2 ? 4 : 2;   // rows per register batch
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = J.K;
@@ -525,6 +572,13 @@ QD_DEV bool gemv_item(const SParams& p, const Item& it, const GemvJob& J, const 
   for (int j = 0; j < C; ++j)
 #pragma unroll
     for (int e = 0; e < 8; ++e) xv[j][e] = 0.f;
+  // the RMSNorm weights do not depend on the earlier phases: load them before the wait
+  uint4 wn[C];
+#pragma unroll
+  for (int j = 0; j < C; ++j)
+    wn[j] = (J.pro != P_BF16 && cv[j]) ? *(const uint4*)(J.nw + col[j]) : make_uint4(0u, 0u, 0u, 0u);
+  if (!cwait(J.wait_cnt, J.wait_target, S, abort_w, p.err, s_abort)) return false;
+  if (tid == 0) STRACE(J.trace_ev);
   if (J.pro == P_BF16) {
 #pragma unroll
     for (int j = 0; j < C; ++j) {
@@ -534,10 +588,8 @@ QD_DEV bool gemv_item(const SParams& p, const Item& it, const GemvJob& J, const 
       xv[j][4] = bf_lo(v.z); xv[j][5] = bf_hi(v.z); xv[j][6] = bf_lo(v.w); xv[j][7] = bf_hi(v.w);
     }
   } else {
-    uint4 wn[C];
 #pragma unroll
     for (int j = 0; j < C; ++j) {
-      wn[j] = cv[j] ? *(const uint4*)(J.nw + col[j]) : make_uint4(0u, 0u, 0u, 0u);
       if (!cv[j]) continue;
       if (J.pro == P_NORM_EMB) {
         const uint4 v = *(const uint4*)(J.xb + col[j]);
@@ -570,17 +622,18 @@ QD_DEV bool gemv_item(const SParams& p, const Item& it, const GemvJob& J, const 
 #pragma unroll
       for (int e = 0; e < 8; ++e) xv[j][e] = cv[j] ? round_bf16(nw[e] * round_bf16(xv[j][e] * inv)) : 0.f;
     }
-    cbar();  // misc_f is reused below
+    // (misc_f is written again only after the flush barriers that end this item)
   }
 
   // ---- reduction windows
   auto epilogue = [&](int lr, float s) {
     if (J.epi == E_STORE) {
       J.y[it.r0 + lr] = s;
-    } else if (J.epi == E_RES) {
+    } else if (J.epi == E_RES) {  // this CTA owns these rows of the residual: its copy is in smem
       const int r = it.r0 + lr;
-      const float base = J.emb ? __bfloat162float(J.emb[r]) : __ldcg(p.res + r);
-      p.res[r] = base + s;
+      const float v = (J.emb ? __bfloat162float(J.emb[r]) : S.resown[lr]) + s;
+      p.res[r] = v;
+      S.resown[lr] = v;
     } else if (J.epi == E_PAIR) {
       S.pair[lr] = s;
     } else {
@@ -615,6 +668,7 @@ QD_DEV bool gemv_item(const SParams& p, const Item& it, const GemvJob& J, const 
       if (tid == 0) *s_abort = 1;
       return false;
     }
+    if (k == 0 && tid == 0) STRACE(1024 + J.trace_ev);
     const unsigned char* st = S.ring + (size_t)slot * kStageB;
     if (in_grp) {
       for (int b0 = 0; b0 < nr; b0 += P * RB) {
@@ -663,6 +717,7 @@ QD_DEV bool gemv_item(const SParams& p, const Item& it, const GemvJob& J, const 
     if (lane == 0) mbar_arrive(&S.empty[slot]);
     ++gs;
   }
+  if (tid == 0) STRACE(1536 + J.trace_ev);
   flush(wbase, it.n1 + it.n2 - wbase);
   if (J.epi == E_PAIR) {  // h = bf16(silu(gate) * up) of this CTA's pairs
     for (int j = tid; j < it.n1; j += kCT)
@@ -672,13 +727,13 @@ QD_DEV bool gemv_item(const SParams& p, const Item& it, const GemvJob& J, const 
 }
 
 QD_DEV bool run_gemv(const SParams& p, const Item& it, const GemvJob& J, const Smem& S, int& gs, Cand& best,
-                     volatile int* s_abort) {
+                     volatile int* s_abort, int* abort_w) {
   switch (c_of(J.K)) {
-    case 1: return gemv_item<1>(p, it, J, S, gs, best, s_abort);
-    case 2: return gemv_item<2>(p, it, J, S, gs, best, s_abort);
-    case 3: return gemv_item<3>(p, it, J, S, gs, best, s_abort);
-    case 4: return gemv_item<4>(p, it, J, S, gs, best, s_abort);
-    default: return gemv_item<6>(p, it, J, S, gs, best, s_abort);
+    case 1: return gemv_item<1>(p, it, J, S, gs, best, s_abort, abort_w);
+    case 2: return gemv_item<2>(p, it, J, S, gs, best, s_abort, abort_w);
+    case 3: return gemv_item<3>(p, it, J, S, gs, best, s_abort, abort_w);
+    case 4: return gemv_item<4>(p, it, J, S, gs, best, s_abort, abort_w);
+    default: return gemv_item<6>(p, it, J, S, gs, best, s_abort, abort_w);
   }
 }
 
@@ -718,64 +773,76 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
   const int g = it.g;
   const SLayer& Ly = p.L[it.layer];
   const bool own_pos = pos >= it.t0 && pos < it.t1;
-  // ---- q (pre-scaled by scale * log2 e) as bf16 hi + lo, heads padded to 8; new k, v
-  float k_new = 0.f, v_new = 0.f;
+  // ---- q (pre-scaled by scale * log2 e) as bf16 hi + lo, heads padded to 8; new k, v.
+  // One warp per head vector (lane l holds dims 4l .. 4l + 3): the RMSNorm is a warp
+  // reduction and RoPE's partner dim d ^ 64 sits in lane l ^ 16, so no CTA barrier is
+  // needed until the vectors are in shared memory.
+  float* s_knew = S.obuf;          // [128] bf16-valued new k (the split holding pos)
+  float* s_vnew = S.obuf + kD;     // [128] new v
   {
-    const int d = tid & (kD - 1);
-    const bool dim_t = tid < kD;
-    const float* qkv = p.qkv;
-    float xv[kHP + 1];
-#pragma unroll
-    for (int i = 0; i < kHP; ++i) xv[i] = (dim_t && i < REP) ? __ldcg(qkv + (g * REP + i) * kD + d) : 0.f;
-    xv[kHP] = (dim_t && own_pos) ? __ldcg(qkv + (p.Hq + g) * kD + d) : 0.f;
-    const float vx = (dim_t && own_pos) ? __ldcg(qkv + (p.Hq + p.Hkv + g) * kD + d) : 0.f;
-    const float2 cs = p.rope[(size_t)pos * (kD / 2) + (d & 63)];
-    const float wq = __bfloat162float(Ly.q_norm[d]), wk = __bfloat162float(Ly.k_norm[d]);
-#pragma unroll
-    for (int i = 0; i <= kHP; ++i) {
-      const float ss = warp_sum(xv[i] * xv[i]);
-      if (lane == 0 && dim_t) S.ared[warp * (kHP + 1) + i] = ss;
+    const int d0 = lane * 4;
+    // the RoPE row and the QK-norm weights do not depend on the projection: load
+    // them before waiting for it
+    const float4 c01 = *(const float4*)(p.rope + (size_t)pos * (kD / 2) + (d0 & 63));
+    const float4 c23 = *(const float4*)(p.rope + (size_t)pos * (kD / 2) + (d0 & 63) + 2);
+    const float cs_c[4] = {c01.x, c01.z, c23.x, c23.z}, cs_s[4] = {c01.y, c01.w, c23.y, c23.w};
+    const uint2 wqb = *(const uint2*)(Ly.q_norm + d0), wkb = *(const uint2*)(Ly.k_norm + d0);
+    const float wq[4] = {bf_lo(wqb.x), bf_hi(wqb.x), bf_lo(wqb.y), bf_hi(wqb.y)};
+    const float wk[4] = {bf_lo(wkb.x), bf_hi(wkb.x), bf_lo(wkb.y), bf_hi(wkb.y)};
+    for (int e = tid; e < (kHP - REP) * kD; e += kCT) {  // padded heads stay zero
+      S.qh[REP * kD + e] = __float2bfloat16_rn(0.f);
+      S.ql[REP * kD + e] = __float2bfloat16_rn(0.f);
     }
-    cbar();
-    float* sQf = S.obuf;  // [9][128] staging, free until the merge
-    float y[kHP + 1];
+    if (!cwait(p.sync + 5 * it.layer + PH_QKV, gridDim.x, S, abort_w, p.err, s_abort)) return false;
+    if (tid == 0) STRACE(10 * it.layer + 2);
+    for (int i = warp; i <= REP; i += kCW) {
+      if (i == REP && !own_pos) break;
+      const int row = i < REP ? (g * REP + i) : (p.Hq + g);
+      const float4 xv4 = __ldcg((const float4*)(p.qkv + (size_t)row * kD + d0));
+      float4 vv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i == REP) vv4 = __ldcg((const float4*)(p.qkv + (size_t)(p.Hq + p.Hkv + g) * kD + d0));
+      const float x[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
+      const float inv = 1.0f / sqrtf(warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]) / (float)kD + p.eps);
+      float y[4], r[4];
 #pragma unroll
-    for (int i = 0; i <= kHP; ++i) {
-      const float tot = (S.ared[i] + S.ared[(kHP + 1) + i]) + (S.ared[2 * (kHP + 1) + i] + S.ared[3 * (kHP + 1) + i]);
-      const float inv = 1.0f / sqrtf(tot / (float)kD + p.eps);
-      const float n = round_bf16(xv[i] * inv);
-      y[i] = round_bf16((i < kHP ? wq : wk) * n);
-      if (dim_t) sQf[i * kD + d] = y[i];
-    }
-    cbar();
-    float r[kHP + 1];
+      for (int e = 0; e < 4; ++e) y[e] = round_bf16((i < REP ? wq[e] : wk[e]) * round_bf16(x[e] * inv));
 #pragma unroll
-    for (int i = 0; i <= kHP; ++i) {
-      const float other = sQf[i * kD + (d ^ 64)];
-      r[i] = (d < 64) ? (y[i] * cs.x - other * cs.y) : (y[i] * cs.x + other * cs.y);
-    }
-    if (dim_t) {
-#pragma unroll
-      for (int h = 0; h < kHP; ++h) {
-        const float qv = h < REP ? r[h] * p.scale_log2 : 0.f;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(qv);
-        S.qh[h * kD + d] = hi;
-        S.ql[h * kD + d] = __float2bfloat16_rn(qv - __bfloat162float(hi));
+      for (int e = 0; e < 4; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, y[e], 16);
+        r[e] = (d0 < 64) ? (y[e] * cs_c[e] - other * cs_s[e]) : (y[e] * cs_c[e] + other * cs_s[e]);
       }
-    }
-    if (own_pos && dim_t) {  // the current token's k, v into the cache
-      k_new = round_bf16(r[kHP]);
-      v_new = round_bf16(vx);
-      const int row = kv_row(p, g, pos);
-      if (row < 0) {
-        if (tid == 0) set_error(p.err, QD_DEVERR_PAGE);
-      } else {
-        Ly.k_cache[(size_t)row * kD + d] = __float2bfloat16_rn(k_new);
-        Ly.v_cache[(size_t)row * kD + d] = __float2bfloat16_rn(v_new);
+      if (i < REP) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float qv = r[e] * p.scale_log2;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(qv);
+          S.qh[i * kD + d0 + e] = hi;
+          S.ql[i * kD + d0 + e] = __float2bfloat16_rn(qv - __bfloat162float(hi));
+        }
+      } else {  // the current token's k (normed, rotated) and v: to the cache and to smem
+        const float vx[4] = {vv4.x, vv4.y, vv4.z, vv4.w};
+        __nv_bfloat16 kb[4], vb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          kb[e] = __float2bfloat16_rn(r[e]);
+          vb[e] = __float2bfloat16_rn(vx[e]);
+          s_knew[d0 + e] = __bfloat162float(kb[e]);
+          s_vnew[d0 + e] = __bfloat162float(vb[e]);
+        }
+        const int crow = kv_row(p, g, pos);
+        if (crow < 0) {
+          if (lane == 0) set_error(p.err, QD_DEVERR_PAGE);
+        } else {
+          *(uint2*)(Ly.k_cache + (size_t)crow * kD + d0) =
+              make_uint2(bf16x2(kb[0], kb[1]), bf16x2(kb[2], kb[3]));
+          *(uint2*)(Ly.v_cache + (size_t)crow * kD + d0) =
+              make_uint2(bf16x2(vb[0], vb[1]), bf16x2(vb[2], vb[3]));
+        }
       }
     }
     cbar();
   }
+  if (tid == 0) STRACE(2048 + 10 * it.layer + 0);
   // B fragments of Q^T for the 8 k-steps: head n = lane / 4, dims 16 ks + 2 (lane % 4) (+ 8)
   const int qn = lane >> 2, qk = (lane & 3) * 2;
   uint32_t qh[8][2], ql[8][2];
@@ -806,6 +873,8 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
       if (tid == 0) *s_abort = 1;
       return false;
     }
+    if (k == 0 && tid == 0) STRACE(2048 + 10 * it.layer + 1);
+    if (k < 4 && tid == 0) STRACE(3400 + 10 * it.layer + k);
     unsigned char* st = S.ring + (size_t)slot * kStageB;
     const uint32_t sK = smem_u32(st), sV = sK + kTokS * kD * 2;
     // rows past the split hold any bits: zero their V (their scores are masked);
@@ -822,8 +891,8 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
       if (tid < kD) {
         const int r = pos - ta;
         const uint32_t o16 = swz(r, tid >> 3) + (uint32_t)((tid & 7) * 2);
-        *(__nv_bfloat16*)(st + o16) = __float2bfloat16_rn(k_new);
-        *(__nv_bfloat16*)(st + kTokS * kD * 2 + o16) = __float2bfloat16_rn(v_new);
+        *(__nv_bfloat16*)(st + o16) = __float2bfloat16_rn(s_knew[tid]);
+        *(__nv_bfloat16*)(st + kTokS * kD * 2 + o16) = __float2bfloat16_rn(s_vnew[tid]);
       }
       wrote = true;
     }
@@ -833,21 +902,23 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
     }
     if (warp * 16 < nv) {
       // ---- S^T = K . Q^T for this warp's 16 tokens
-      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t a[8][4];
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) ldsm_x4(a[ks], sK + swz(warp * 16 + rA, 2 * ks + cA));
+      float sc[4][4] = {};
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(a, sK + swz(warp * 16 + rA, 2 * ks + cA));
-        mma16816(sc, a, qh[ks][0], qh[ks][1]);
-        mma16816(sl, a, ql[ks][0], ql[ks][1]);
+        mma16816(sc[ks & 1], a[ks], qh[ks][0], qh[ks][1]);
+        mma16816(sc[2 + (ks & 1)], a[ks], ql[ks][0], ql[ks][1]);
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sc[e] += sl[e];
+      for (int e = 0; e < 4; ++e) sc[0][e] = (sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e]);
+      float* scr = sc[0];
       const int tr0 = ta + warp * 16 + (lane >> 2), tr1 = tr0 + 8;
-      if (tr0 >= tb) { sc[0] = -INFINITY; sc[1] = -INFINITY; }
-      if (tr1 >= tb) { sc[2] = -INFINITY; sc[3] = -INFINITY; }
+      if (tr0 >= tb) { scr[0] = -INFINITY; scr[1] = -INFINITY; }
+      if (tr1 >= tb) { scr[2] = -INFINITY; scr[3] = -INFINITY; }
       // ---- online softmax over this warp's tokens
-      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+      float mx0 = fmaxf(scr[0], scr[2]), mx1 = fmaxf(scr[1], scr[3]);
 #pragma unroll
       for (int o2 = 4; o2 <= 16; o2 <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
@@ -856,10 +927,10 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
       const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
       const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-      const float p00 = sc[0] == -INFINITY ? 0.f : exp2f(sc[0] - mn0);
-      const float p01 = sc[1] == -INFINITY ? 0.f : exp2f(sc[1] - mn1);
-      const float p10 = sc[2] == -INFINITY ? 0.f : exp2f(sc[2] - mn0);
-      const float p11 = sc[3] == -INFINITY ? 0.f : exp2f(sc[3] - mn1);
+      const float p00 = scr[0] == -INFINITY ? 0.f : exp2f(scr[0] - mn0);
+      const float p01 = scr[1] == -INFINITY ? 0.f : exp2f(scr[1] - mn1);
+      const float p10 = scr[2] == -INFINITY ? 0.f : exp2f(scr[2] - mn0);
+      const float p11 = scr[3] == -INFINITY ? 0.f : exp2f(scr[3] - mn1);
       float ps0 = p00 + p10, ps1 = p01 + p11;
 #pragma unroll
       for (int o2 = 4; o2 <= 16; o2 <<= 1) {
@@ -893,12 +964,13 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
       const uint32_t pb0h = *(const uint32_t*)(sPh + qn * 16 + qk), pb1h = *(const uint32_t*)(sPh + qn * 16 + qk + 8);
       const uint32_t pb0l = *(const uint32_t*)(sPl + qn * 16 + qk), pb1l = *(const uint32_t*)(sPl + qn * 16 + qk + 8);
       // ---- O^T += V^T . P^T, 8 tiles of 16 dims
+      uint32_t av[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) ldsm_x4_t(av[mt], sV + swz(warp * 16 + rV, 2 * mt + cV));
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        uint32_t a[4];
-        ldsm_x4_t(a, sV + swz(warp * 16 + rV, 2 * mt + cV));
-        mma16816(o[mt], a, pb0h, pb1h);
-        mma16816(o[mt], a, pb0l, pb1l);
+        mma16816(o[mt], av[mt], pb0h, pb1h);
+        mma16816(o[mt], av[mt], pb0l, pb1l);
       }
     }
     __syncwarp();
@@ -906,6 +978,7 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
     ++gs;
   }
 
+  if (tid == 0) STRACE(2048 + 10 * it.layer + 2);
   // ---- merge the warps (heads in chunks of 4) into the split's partial
   const size_t slot0 = (size_t)g * kMaxSplit;
   const size_t sslot = slot0 + it.s;
@@ -954,51 +1027,73 @@ QD_DEV bool attn_item(const SParams& p, const Item& it, const Smem& S, int& gs, 
     cbar();
   }
   int* tickets = p.sync + 5 * p.n_layers;
-  if (tid == 0) {
-    __threadfence();
-    S.misc_i[0] = atomicAdd(tickets + g, 1);
+  if (tid == 0) STRACE(2048 + 10 * it.layer + 3);
+  if (tid == 0) S.misc_i[0] = atom_acq_rel_add(tickets + g, 1);
+  cbar();
+  if (tid == 0) STRACE(2048 + 10 * it.layer + 4);
+  if (S.misc_i[0] != it.n_split - 1) return true;
+  // ---- the last split combines: (max, sum) of every split staged together, the
+  // weights exp2(m_k - M) per head, then each output element from all splits' partials
+  // with the loads in flight together
+  float* sMk = S.red;                      // [n_split][REP] maxima -> weights
+  float* sLk = S.red + kMaxSplit * 8;      // [n_split][REP] sums
+  float* sTot = S.pair;                    // [REP] totals
+  for (int e = tid; e < it.n_split * REP; e += kCT) {
+    const float2 ml = __ldcg((const float2*)(p.part_ml + (slot0 * REP + e) * 2));
+    sMk[e] = ml.x;
+    sLk[e] = ml.y;
   }
   cbar();
-  if (S.misc_i[0] != it.n_split - 1) return true;
-  __threadfence();
-  // ---- the last split combines: weights of every split per head, then the sums
-  float* sW = S.red;  // [n_split][REP] weights, then [REP] totals after them
-  for (int e = tid; e < it.n_split * REP; e += kCT) sW[e] = __ldcg(p.part_ml + (slot0 * REP + e) * 2);
-  cbar();
+  if (tid == 0) STRACE(2048 + 10 * it.layer + 5);
   if (tid < REP) {
     float M = -INFINITY;
-    for (int k = 0; k < it.n_split; ++k) M = fmaxf(M, sW[k * REP + tid]);
+    for (int k = 0; k < it.n_split; ++k) M = fmaxf(M, sMk[k * REP + tid]);
     float L = 0.f;
     for (int k = 0; k < it.n_split; ++k) {
-      const float m = sW[k * REP + tid];
+      const float m = sMk[k * REP + tid];
       const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-      L = fmaf(w, __ldcg(p.part_ml + ((slot0 + k) * REP + tid) * 2 + 1), L);
-      sW[k * REP + tid] = w;
+      L = fmaf(w, sLk[k * REP + tid], L);
+      sMk[k * REP + tid] = w;
     }
-    sW[kMaxSplit * 8 + tid] = L;
+    sTot[tid] = L;
   }
   cbar();
-  for (int e = tid; e < REP * kD; e += kCT) {
-    const int h = e / kD, d = e % kD;
-    const float* ap = p.part + (slot0 * REP + h) * kD + d;
-    float O = 0.f;
-    int k = 0;
-    for (; k + 4 <= it.n_split; k += 4) {
-      const float a0 = __ldcg(ap + (size_t)(k + 0) * REP * kD), a1 = __ldcg(ap + (size_t)(k + 1) * REP * kD);
-      const float a2 = __ldcg(ap + (size_t)(k + 2) * REP * kD), a3 = __ldcg(ap + (size_t)(k + 3) * REP * kD);
-      O = fmaf(sW[(k + 0) * REP + h], a0, O);
-      O = fmaf(sW[(k + 1) * REP + h], a1, O);
-      O = fmaf(sW[(k + 2) * REP + h], a2, O);
-      O = fmaf(sW[(k + 3) * REP + h], a3, O);
+  {
+    constexpr int kE = kHP * kD / kCT;   // at most 4 output elements per thread
+    const int ne = REP * kD;
+    float O[kE];
+#pragma unroll
+    for (int j = 0; j < kE; ++j) O[j] = 0.f;
+    for (int k0 = 0; k0 < it.n_split; k0 += 8) {
+      float a[kE][8];
+#pragma unroll
+      for (int j = 0; j < kE; ++j) {
+        const int e = tid + j * kCT;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          a[j][u] = (e < ne && k0 + u < it.n_split)
+                        ? __ldcg(p.part + ((slot0 + k0 + u) * REP + e / kD) * kD + (e % kD)) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < kE; ++j) {
+        const int e = tid + j * kCT;
+        if (e >= ne) continue;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (k0 + u < it.n_split) O[j] = fmaf(sMk[(k0 + u) * REP + e / kD], a[j][u], O[j]);
+      }
     }
-    for (; k < it.n_split; ++k) O = fmaf(sW[k * REP + h], __ldcg(ap + (size_t)k * REP * kD), O);
-    p.attn[(size_t)(g * REP + h) * kD + d] = __float2bfloat16_rn(O / sW[kMaxSplit * 8 + h]);
+#pragma unroll
+    for (int j = 0; j < kE; ++j) {
+      const int e = tid + j * kCT;
+      if (e < ne) p.attn[(size_t)g * REP * kD + e] = __float2bfloat16_rn(O[j] / sTot[e / kD]);
+    }
   }
   cbar();
+  if (tid == 0) STRACE(2048 + 10 * it.layer + 6);
   if (tid == 0) {
     tickets[g] = 0;
-    __threadfence();
-    atomicAdd(p.sync + 5 * it.layer + PH_ATTN, 1);
+    red_release_add(p.sync + 5 * it.layer + PH_ATTN, 1);
   }
   return true;
 }
@@ -1024,6 +1119,7 @@ __global__ void __launch_bounds__(kST, 1)
   S.ared = (float*)(base + Carve::ared);
   S.sx = S.ared + 64;
   S.obuf = (float*)(base + Carve::obuf);
+  S.resown = (float*)(base + Carve::resown);
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1039,7 +1135,7 @@ __global__ void __launch_bounds__(kST, 1)
   }
   __syncthreads();
 
-  if (tid == 0) STRACE(1000);
+  if (tid == 0) STRACE(4095);
   Ctx x;
   x.c = blockIdx.x;
   x.n_cta = gridDim.x;
@@ -1066,34 +1162,24 @@ __global__ void __launch_bounds__(kST, 1)
   int gs = 0;
   Cand best{-INFINITY, INT_MAX};
   bool ok = true;
-  auto wait_phase = [&](int* cnt, int target) {
-    if (tid == 0) S.misc_i[1] = wait_count(cnt, target, abort_w, p.err) ? 1 : 0;
+  auto arrive = [&](int* cnt) {  // the phase's stores are ordered before the count
     cbar();
-    const bool r = S.misc_i[1] != 0;
-    if (!r && tid == 0) s_abort = 1;
-    return r;
-  };
-  auto arrive = [&](int* cnt) {
-    cbar();
-    if (tid == 0) {
-      __threadfence();
-      atomicAdd(cnt, 1);
-    }
+    if (tid == 0) red_release_add(cnt, 1);
   };
   const int n = gridDim.x;
   for (int l = 0; l < L && ok; ++l) {
     const SLayer& Ly = p.L[l];
     int* cnt = p.sync + 5 * l;
     // QKV projection of RMSNorm(res; ln_in) (the embedding row in the first layer)
-    if (l > 0) ok = wait_phase(p.sync + 5 * (l - 1) + PH_DOWN, n);
-    if (!ok) break;
-    if (tid == 0) STRACE(10 * l + 0);
     {
       const Item it = get_item(p, x, 5 * l + IT_QKV);
       GemvJob J = {};
+      J.wait_cnt = l > 0 ? p.sync + 5 * (l - 1) + PH_DOWN : nullptr;
+      J.wait_target = n;
+      J.trace_ev = 10 * l + 0;
       J.K = p.H; J.pro = l == 0 ? P_NORM_EMB : P_NORM_RES; J.xb = emb_row; J.nw = Ly.ln_in;
       J.epi = E_STORE; J.y = p.qkv;
-      ok = run_gemv(p, it, J, S, gs, best, &s_abort);
+      ok = run_gemv(p, it, J, S, gs, best, &s_abort, abort_w);
       if (!ok) break;
       arrive(cnt + PH_QKV);
       if (tid == 0) STRACE(10 * l + 1);
@@ -1102,49 +1188,46 @@ __global__ void __launch_bounds__(kST, 1)
     {
       const Item it = get_item(p, x, 5 * l + IT_KV);
       if (it.g >= 0) {
-        ok = wait_phase(cnt + PH_QKV, n);
-        if (!ok) break;
-        if (tid == 0) STRACE(10 * l + 2);
         ok = attn_item(p, it, S, gs, x.pos, x.len, &s_abort, abort_w);
         if (!ok) break;
         if (tid == 0) STRACE(10 * l + 3);
       }
     }
     // O projection + residual (the residual starts as the embedding row)
-    ok = wait_phase(cnt + PH_ATTN, p.Hkv);
-    if (!ok) break;
-    if (tid == 0) STRACE(10 * l + 4);
     {
       const Item it = get_item(p, x, 5 * l + IT_O);
       GemvJob J = {};
+      J.wait_cnt = cnt + PH_ATTN;
+      J.wait_target = p.Hkv;
+      J.trace_ev = 10 * l + 4;
       J.K = p.Hq * kD; J.pro = P_BF16; J.xb = p.attn; J.epi = E_RES; J.emb = l == 0 ? emb_row : nullptr;
-      ok = run_gemv(p, it, J, S, gs, best, &s_abort);
+      ok = run_gemv(p, it, J, S, gs, best, &s_abort, abort_w);
       if (!ok) break;
       arrive(cnt + PH_O);
       if (tid == 0) STRACE(10 * l + 5);
     }
     // gate+up projection of RMSNorm(res; ln_post), SwiGLU of the pairs
-    ok = wait_phase(cnt + PH_O, n);
-    if (!ok) break;
-    if (tid == 0) STRACE(10 * l + 6);
     {
       const Item it = get_item(p, x, 5 * l + IT_GU);
       GemvJob J = {};
+      J.wait_cnt = cnt + PH_O;
+      J.wait_target = n;
+      J.trace_ev = 10 * l + 6;
       J.K = p.H; J.pro = P_NORM_RES; J.nw = Ly.ln_post; J.epi = E_PAIR;
-      ok = run_gemv(p, it, J, S, gs, best, &s_abort);
+      ok = run_gemv(p, it, J, S, gs, best, &s_abort, abort_w);
       if (!ok) break;
       arrive(cnt + PH_GU);
       if (tid == 0) STRACE(10 * l + 7);
     }
     // down projection + residual
-    ok = wait_phase(cnt + PH_GU, n);
-    if (!ok) break;
-    if (tid == 0) STRACE(10 * l + 8);
     {
       const Item it = get_item(p, x, 5 * l + IT_DOWN);
       GemvJob J = {};
+      J.wait_cnt = cnt + PH_GU;
+      J.wait_target = n;
+      J.trace_ev = 10 * l + 8;
       J.K = p.F; J.pro = P_BF16; J.xb = p.h; J.epi = E_RES;
-      ok = run_gemv(p, it, J, S, gs, best, &s_abort);
+      ok = run_gemv(p, it, J, S, gs, best, &s_abort, abort_w);
       if (!ok) break;
       arrive(cnt + PH_DOWN);
       if (tid == 0) STRACE(10 * l + 9);
@@ -1152,13 +1235,14 @@ __global__ void __launch_bounds__(kST, 1)
   }
   if (!ok) return;
   // ---- final RMSNorm + LM head with a running argmax
-  if (!wait_phase(p.sync + 5 * (L - 1) + PH_DOWN, n)) return;
-  if (tid == 0) STRACE(10 * L + 0);
   {
     const Item it = get_item(p, x, 5 * L);
     GemvJob J = {};
+    J.wait_cnt = p.sync + 5 * (L - 1) + PH_DOWN;
+    J.wait_target = n;
+    J.trace_ev = 10 * L + 0;
     J.K = p.H; J.pro = P_NORM_RES; J.nw = p.final_norm; J.epi = E_LM; J.y = p.logits;
-    if (!run_gemv(p, it, J, S, gs, best, &s_abort)) return;
+    if (!run_gemv(p, it, J, S, gs, best, &s_abort, abort_w)) return;
   }
   if (tid == 0) STRACE(10 * L + 1);
   // CTA argmax (lowest index among equal maxima), candidate, ticket
@@ -1258,8 +1342,9 @@ bool stream_step_supported(const StreamStepArgs& a) {
   const int ks[3] = {a.H, a.Hq * kD, a.F};
   for (int K : ks)
     if (K < 8 || K % 8 || K / 8 > 6 * kCT || K * 2 > kStageB) return false;
-  // gate/up pairs per CTA fit the pair buffer
+  // gate/up pairs and residual rows per CTA fit their buffers
   if ((a.F + dev_info().sm_count - 1) / dev_info().sm_count > kMaxPair) return false;
+  if ((a.H + dev_info().sm_count - 1) / dev_info().sm_count > kMaxOwnRows) return false;
   // 16-token granules never cross a page
   if (!(a.max_pages == 1 || a.page_size % 16 == 0)) return false;
   if (dev_info().max_smem_optin < (int)kSmemBytes) return false;
