@@ -57,10 +57,10 @@ constexpr int kST = kCT + 32;           // plus the producer warp
 #define QD_STREAM_STAGES 4
 #endif
 #ifndef QD_STREAM_PF_AHEAD
-#define QD_STREAM_PF_AHEAD 4
+#define QD_STREAM_PF_AHEAD 0
 #endif
 #ifndef QD_STREAM_PF_STALL
-#define QD_STREAM_PF_STALL 12
+#define QD_STREAM_PF_STALL 0
 #endif
 constexpr int kStageB = QD_STREAM_STAGE_KB * 1024;  // bytes per ring stage
 constexpr int kNSt = QD_STREAM_STAGES;              // ring stages
