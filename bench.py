@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--batch", type=int, default=64,
                     help="rows of x for --kernel gemm_tc; sequences for --kernel attention_batched")
     ap.add_argument("--act", choices=["f32", "i8"], default="f32", help="Q8_0 activation lane (batch 1)")
+    ap.add_argument("--verify", type=int, default=0, metavar="K",
+                    help="time speculative verify passes of K tokens (K - 1 drafts) against K single-token steps "
+                         "on the batch-1 workload")
     ap.add_argument("--deq", type=int, choices=[0, 1, 2],
                     help="Q8_0 lanes by level: 0 = dp4a everywhere, 1 = dp4a in the layers and f32 activations for "
                          "the LM head, 2 = f32 activations everywhere (overrides --act)")
@@ -671,10 +674,82 @@ def run_kernel(args):
                       "peak_kind": kind, "copies": copies}), flush=True)
 
 
+def run_verify(args):
+    """Speculative verify passes of k tokens (tok + k - 1 drafts, one sequence) against
+    k plain decode steps, both as CUDA graphs on the batch-1 workload's model. Each
+    verify replay restores the decode state first (three 4-byte copies), so every pass
+    runs at the same positions; the drafts are random tokens (the pass costs the same
+    whatever is accepted). Reports the pass latency and the tokens per second it would
+    give if every draft were accepted."""
+    from transformer_decode_step_weight_gb300 import api
+    from transformer_decode_step_weight_gb300 import build as b
+    b.build()
+    dev = torch.device("cuda", 0)
+    k = args.verify
+    wl = synth.WORKLOADS[args.workload]
+    assert wl.batch == 1, "speculative verify runs on one sequence"
+    mt = synth.make_model(wl.shape, wl.wtype, args.seed, dev, ctx=wl.ctx, steps=4 * k + 16)
+    act, lm_act = q8_lanes(args)
+    dec = api.Decoder(mt, max_steps=4 * k + 16, act=api.QD_ACT_I8 if act == "i8" else api.QD_ACT_F32,
+                      lm_act=api.QD_ACT_I8 if lm_act == "i8" else api.QD_ACT_F32, device=dev, verify_k=k)
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed + 1)
+    draft = torch.randint(0, wl.shape.vocab, (k - 1,), generator=g, device=dev, dtype=torch.int64).to(torch.int32)
+    tok0, pos0 = dec.tok.clone(), dec.pos.clone()
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        dec.verify(draft, stream=s)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        dec.tok.copy_(tok0)
+        dec.pos.copy_(pos0)
+        dec.step_ctr.zero_()
+        dec.verify(draft, stream=s)
+
+    def timed(fn, n):
+        with torch.cuda.stream(s):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(n):
+                fn()
+            e1.record(s)
+        s.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    reps = max(1, args.reps)
+    n = max(1, args.steps // 4)
+    verify_ms = sorted(timed(graph.replay, n) for _ in range(reps))[reps // 2]
+    with torch.cuda.stream(s):
+        dec.tok.copy_(tok0)
+        dec.pos.copy_(pos0)
+        dec.step_ctr.zero_()
+        dec.capture(1, stream=s)
+
+    def one_step():
+        dec.replay(stream=s)
+
+    step_ms = sorted(timed(one_step, n) for _ in range(reps))[reps // 2]
+    assert api.check_device_error(s) == 0
+    out = {"metric": f"speculative verify pass, k = {k} tokens of one sequence", "value": round(k / (verify_ms / 1e3), 3),
+           "unit": "tok/s if all k accepted", "ms_per_pass": round(verify_ms, 4),
+           "ms_per_single_step": round(step_ms, 4), "pass_vs_k_steps": round(verify_ms / (k * step_ms), 4),
+           "higher_is_better": True, "dtype": dtype_label(wl, act, lm_act) if k == 1 else "bf16 tcgen05 rows",
+           "data": "synthetic", "config": {"workload": wl.name, "k": k, "drafts": "random tokens",
+                                           "passes_timed": n, "repetitions": reps}}
+    print(json.dumps(out), flush=True)
+    dec.close()
+
+
 def main():
     args = parse()
     if args.kernel:
         run_kernel(args)
+        return
+    if args.verify:
+        run_verify(args)
         return
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; other ranks exit without work

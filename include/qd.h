@@ -272,6 +272,30 @@ int qd_graph_create(const qd_step_args* args, int steps_per_launch, cudaStream_t
 int qd_graph_launch(qd_graph* g, cudaStream_t stream);
 int qd_graph_destroy(qd_graph* g);
 
+/* ------------------------------------------------------------------------ */
+/* Speculative verify ("qwen3-8b-rtx4080-cutedsl" README, "Speculative          */
+/* decoding": a draft proposes tokens and the target model checks k of them in  */
+/* one forward pass that reuses the weight bytes already streamed). For the one */
+/* sequence of `args` (batch 1): the k input tokens are tok[0] (the last token   */
+/* emitted) and draft[0 .. k-2], at positions pos[0] .. pos[0] + k - 1. They run  */
+/* as k rows of one pass: every projection is a tcgen05 GEMM over the k rows; the */
+/* k new K/V rows are written to the cache first, and row i attends to positions */
+/* 0 .. pos[0] + i (causal among the drafted tokens).                           */
+/* Outputs: logits f32 [k, vocab] (device, 16-byte aligned); target int32 [k]:   */
+/* the argmax of each row (the model's token after input i, as in               */
+/* qd_argmax_advance); n_accept int32 [1]: m = the number of leading drafts with  */
+/* draft[i] == target[i] (0 <= m <= k - 1). The state advances on the device:     */
+/* out_tokens[step .. step + m] = draft[0 .. m - 1], target[m]; tok = target[m];  */
+/* pos += m + 1; step += m + 1. Cache rows past pos[0] + m hold the rejected      */
+/* drafts' K/V until a later step overwrites them.                               */
+/* draft: int32 [k - 1] device (may be NULL when k == 1). 1 <= k <= 8. The       */
+/* projections' K must be multiples of 64 (bf16) or 256 (Q8_0, whose weights are  */
+/* widened on chip as in qd_gemm_q8_0). workspace: args->workspace of at least    */
+/* qd_verify_workspace_bytes(args, k) bytes, zero-filled before first use.        */
+size_t qd_verify_workspace_bytes(const qd_step_args* args, int k);
+int qd_verify_step(const qd_step_args* args, const int32_t* draft, int k, float* logits, int32_t* target,
+                   int32_t* n_accept, cudaStream_t stream);
+
 /* Reads and clears the sticky device error word (synchronises `stream`).      */
 /* *bits receives a mask of QD_DEVERR_*. Returns QD_OK or QD_ERR_CUDA.           */
 int qd_check_device_error(cudaStream_t stream, int* bits);

@@ -74,17 +74,17 @@ def teacher_forced(dec, mt, steps, lanes, b=0, floor_factor=None, lm_resync=Fals
     top-2 gap is below 4x the step's max-abs logit error (a near tie, logged). The
     first lane decides the token agreement figures.
 
-    floor_factor: the end-to-end limit of lane 0 becomes max(tol, floor_factor x the
-    oracle's own drift), the drift being how far the oracle's logits of step 0 move
-    when its sums are accumulated in binary32 instead of float64 (``acc="f32"``). In a
-    deep model of bf16-rounded activations, ulp-level differences flip roundings that
-    the following layers amplify; this measures that floor for the model at hand.
+    floor_factor: the end-to-end limit of lane 0 at each step becomes max(tol,
+    floor_factor x the oracle's own drift at that step), the drift being how far the
+    oracle's logits move when its sums are accumulated in binary32 instead of float64
+    (``acc="f32"``, a second oracle run on its own caches, teacher-forced on the same
+    tokens). In a deep model of bf16-rounded activations, ulp-level differences flip
+    roundings that the following layers amplify; this measures that floor for the
+    model at hand.
     lm_resync: at step 0 also hold the GPU logits to the oracle's LM head applied to
     the GPU's own final hidden state (every row), at the lane's tolerance.
     Returns the log dict.
     """
-    import copy
-
     import torch
 
     from transformer_decode_step_weight_gb300 import api
@@ -93,10 +93,11 @@ def teacher_forced(dec, mt, steps, lanes, b=0, floor_factor=None, lm_resync=Fals
     om = oracle_model(mt)
     pos0 = int(mt.seq_lens[b])
     caches = [oracle_caches(mt, b, pos0 + steps) for _ in lanes]
+    caches32 = oracle_caches(mt, b, pos0 + steps) if floor_factor is not None else None
     tok = int(mt.start_tok[b])
     tols = [ln[3] for ln in lanes]
     st = {"steps": steps, "strict": 0, "near_ties": [], "worst_rel_err": [0.0] * len(lanes),
-          "lanes": [f"{m}/{a}/{la or a}" for m, a, la, _ in lanes]}
+          "lanes": [f"{m}/{a}/{la or a}" for m, a, la, _ in lanes], "floor": [], "tol": []}
     for t in range(steps):
         dec.step()
         torch.cuda.synchronize()
@@ -104,16 +105,16 @@ def teacher_forced(dec, mt, steps, lanes, b=0, floor_factor=None, lm_resync=Fals
         gtok = int(dec.tok[b])
         assert gtok == oracle.argmax_first(g), t
         assert int(dec.out_tokens[b, t]) == gtok
-        for li, (mode, act, lm_act, _) in enumerate(lanes):
-            if t == 0 and li == 0 and floor_factor is not None:
-                kc, vc = copy.deepcopy(caches[0][0]), copy.deepcopy(caches[0][1])
-                r32 = oracle.decode_token(om, tok, pos0, kc, vc, mode=mode, act=act, lm_act=lm_act, acc="f32")
+        for li, (mode, act, lm_act, tol) in enumerate(lanes):
             ref = oracle.decode_token(om, tok, pos0 + t, caches[li][0], caches[li][1], mode=mode, act=act,
                                       lm_act=lm_act)
-            if t == 0 and li == 0 and floor_factor is not None:
-                st["floor"] = rel_max_abs(r32, ref)
-                tols[0] = max(tols[0], floor_factor * st["floor"])
-                st["tol"] = tols[0]
+            if li == 0 and floor_factor is not None:
+                r32 = oracle.decode_token(om, tok, pos0 + t, caches32[0], caches32[1], mode=mode, act=act,
+                                          lm_act=lm_act, acc="f32")
+                fl = rel_max_abs(r32, ref)
+                st["floor"].append(fl)
+                tols[0] = max(tol, floor_factor * fl)
+                st["tol"].append(tols[0])
             if t == 0 and li == 0 and lm_resync:
                 xf = oracle.rmsnorm(dec.residual()[b].double().cpu().numpy(), oracle.bf16_to_f64(om.final_norm),
                                     om.dims.rms_eps, mode)

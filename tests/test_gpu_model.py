@@ -25,7 +25,7 @@ import gc
 import pytest
 import torch
 
-from helpers import TOL, teacher_forced
+from helpers import TOL, per_layer_resync, teacher_forced
 from transformer_decode_step_weight_gb300 import api, synth
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]

@@ -74,6 +74,8 @@ _SIGS = {
     "qd_graph_launch": (_i, [_vp, _vp]),
     "qd_graph_destroy": (_i, [_vp]),
     "qd_check_device_error": (_i, [_vp, C.POINTER(_i)]),
+    "qd_verify_workspace_bytes": (_sz, [C.POINTER(StepArgs), _i]),
+    "qd_verify_step": (_i, [C.POINTER(StepArgs), _vp, _i, _vp, _vp, _vp, _vp]),
     "qd_debug_q8_block_dots": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "qd_debug_paged_indices": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
 }
@@ -250,7 +252,7 @@ class Decoder:
     """
 
     def __init__(self, model, max_steps: int, act: int = QD_ACT_F32, lm_act: int | None = None,
-                 device="cuda"):
+                 device="cuda", verify_k: int = 0):
         self.m = model
         s = model.shape
         self.device = torch.device(device)
@@ -303,6 +305,11 @@ class Decoder:
         a.logits = _p(self.logits)
         self.args = a
         nbytes = int(lib().qd_step_workspace_bytes(C.byref(a)))
+        if verify_k:  # room for speculative verify passes of up to verify_k tokens
+            nbytes = max(nbytes, int(lib().qd_verify_workspace_bytes(C.byref(a), verify_k)))
+            self.verify_logits = torch.empty((verify_k, s.vocab), dtype=torch.float32, device=self.device)
+            self.verify_target = torch.zeros(verify_k, dtype=torch.int32, device=self.device)
+            self.n_accept = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
         a.workspace = _p(self.workspace)
         a.workspace_bytes = nbytes
@@ -319,6 +326,13 @@ class Decoder:
 
     def step(self, stream=None):
         _check(lib().qd_decode_step(C.byref(self.args), _stream(stream)))
+
+    def verify(self, draft, stream=None):
+        """One speculative verify pass over tok and the k - 1 draft tokens (device int32):
+        fills verify_logits[:k], verify_target[:k] and n_accept, and advances the state."""
+        k = int(draft.numel()) + 1
+        _check(lib().qd_verify_step(C.byref(self.args), _p(draft) if k > 1 else None, k, _p(self.verify_logits),
+                                    _p(self.verify_target), _p(self.n_accept), _stream(stream)))
 
     def capture(self, steps_per_launch: int, stream=None):
         if self._graph is not None:

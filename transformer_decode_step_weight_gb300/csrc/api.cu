@@ -436,7 +436,10 @@ bool tc_step(const qd_step_args* a) {
   return a->batch > 8 || (a->layers[0]->dims.wtype == QD_W_Q8_0 && a->batch > 1);
 }
 
-StepWs step_ws_layout(const qd_step_args* a, void* base) {
+StepWs step_ws_layout_for(const qd_step_args* a, void* base, bool gemm_path);
+StepWs step_ws_layout(const qd_step_args* a, void* base) { return step_ws_layout_for(a, base, tc_step(a)); }
+// gemm_path: size the split-K GEMM workspace (the step runs its projections as GEMMs)
+StepWs step_ws_layout_for(const qd_step_args* a, void* base, bool gemm_path) {
   const qd_layer_dims& d = a->layers[0]->dims;
   const int B = a->batch;
   const size_t qkv = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
@@ -454,7 +457,7 @@ StepWs step_ws_layout(const qd_step_args* a, void* base) {
   w.claims = (int*)(p + off); off += al256((size_t)(5 * a->n_layers + 1) * 2 * sizeof(int));
   w.gemm_ws = (void*)(p + off);
   w.gemm_ws_bytes = 0;
-  if (tc_step(a)) {  // the batched step runs its projections as split-K tcgen05 GEMMs
+  if (gemm_path) {  // the batched step runs its projections as split-K tcgen05 GEMMs
     const bool q8 = d.wtype == QD_W_Q8_0, q8_head = a->lm_head_scales != nullptr;
     const int shapes[5][3] = {{(int)qkv, d.hidden, q8}, {d.hidden, d.n_q_heads * d.head_dim, q8},
                               {2 * d.ffn, d.hidden, q8}, {d.hidden, d.ffn, q8}, {a->vocab, d.hidden, q8_head}};
@@ -768,7 +771,129 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
   return QD_OK;
 }
 
+// ------------------------------------------------------------------ speculative verify
+// k rows of one sequence: the batched step's buffers for k rows (its projections on the
+// tcgen05 GEMMs), then the rows' tokens, positions, page-table rows and argmax scratch.
+struct VerifyWs {
+  StepWs w;
+  int32_t* tokens;   // [k]
+  int32_t* vpos;     // [k]
+  int32_t* vpt;      // [k, max_pages]
+  int32_t* scratch;  // [3k]: argmax position, step, output slot
+  size_t total;
+};
+
+VerifyWs verify_ws_layout(const qd_step_args* a, int k, void* base) {
+  qd_step_args ak = *a;
+  ak.batch = k;
+  VerifyWs v;
+  v.w = step_ws_layout_for(&ak, base, true);
+  unsigned char* p = (unsigned char*)base;
+  size_t off = v.w.total;
+  v.tokens = (int32_t*)(p + off); off += al256((size_t)k * 4);
+  v.vpos = (int32_t*)(p + off); off += al256((size_t)k * 4);
+  v.vpt = (int32_t*)(p + off); off += al256((size_t)k * a->max_pages * 4);
+  v.scratch = (int32_t*)(p + off); off += al256((size_t)3 * k * 4);
+  v.total = off;
+  return v;
+}
+
+constexpr int kMaxVerify = 8;
+
+int validate_verify(const qd_step_args* a, const int32_t* draft, int k, const float* logits, const int32_t* target,
+                    const int32_t* n_accept) {
+  if (!a) return fail(QD_ERR_INVALID_ARG, "qd_verify_step: null args");
+  if (a->batch != 1) return fail(QD_ERR_UNSUPPORTED, "qd_verify_step: one sequence (batch 1)");
+  if (k < 1 || k > kMaxVerify) return fail(QD_ERR_INVALID_ARG, "qd_verify_step: k=%d (1..%d)", k, kMaxVerify);
+  if ((k > 1 && !draft) || !logits || !target || !n_accept)
+    return fail(QD_ERR_INVALID_ARG, "qd_verify_step: null pointer");
+  if (!aligned16(logits)) return fail(QD_ERR_INVALID_ARG, "qd_verify_step: logits must be 16-byte aligned");
+  int rc = validate_step(a);
+  if (rc) return rc;
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const bool q8 = d.wtype == QD_W_Q8_0;
+  const int ks[3] = {d.hidden, d.n_q_heads * d.head_dim, d.ffn};
+  for (int K : ks)
+    if (q8 ? !gemm_tc_q8_supported(1, K, k) : !gemm_tc_supported(1, K, k))
+      return fail(QD_ERR_UNSUPPORTED, "qd_verify_step: projection K=%d needs a multiple of %d", K, q8 ? 256 : 64);
+  if (a->lm_head_scales && !gemm_tc_q8_supported(a->vocab, d.hidden, k))
+    return fail(QD_ERR_UNSUPPORTED, "qd_verify_step: Q8_0 LM head needs hidden %% 256 == 0");
+  if (q8)
+    for (int i = 0; i < a->n_layers; ++i) {
+      const qd_layer_weights& lw = a->layers[i]->w;
+      if (!aligned16(lw.s_qkv) || !aligned16(lw.s_o) || !aligned16(lw.s_gu) || !aligned16(lw.s_down))
+        return fail(QD_ERR_INVALID_ARG, "qd_verify_step: Q8_0 scales must be 16-byte aligned");
+    }
+  const VerifyWs v = verify_ws_layout(a, k, a->workspace);
+  if (a->workspace_bytes < v.total)
+    return fail(QD_ERR_WORKSPACE, "qd_verify_step: workspace %zu < %zu bytes", a->workspace_bytes, v.total);
+  return QD_OK;
+}
+
+int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits, int32_t* target,
+               int32_t* n_accept, cudaStream_t stream) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const bool q8 = d.wtype == QD_W_Q8_0;
+  const VerifyWs v = verify_ws_layout(a, k, a->workspace);
+  const StepWs& w = v.w;
+  const Launch L = make_launch(stream, true);
+  const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int QKV = (Hq + 2 * Hkv) * D;
+  auto gemm = [&](const void* W, const void* S, int R, int K, const void* X, int epi, float* y) {
+    GemmTcArgs g = {};
+    g.W = W; g.S = S; g.X = X; g.R = R; g.K = K; g.B = k; g.epi = epi; g.y = y;
+    g.ws = w.gemm_ws; g.ws_bytes = w.gemm_ws_bytes;
+    return launch_gemm_tc(g, L);
+  };
+  QD_TRY(launch_verify_prep(a->tok, a->pos, draft, k, a->page_table, a->max_pages, v.tokens, v.vpos, v.vpt,
+                            v.scratch, L),
+         "verify prep");
+  QD_TRY(launch_embed(a->embed, H, a->vocab, v.tokens, k, w.res, L), "embed");
+  for (int li = 0; li < a->n_layers; ++li) {
+    const qd_layer* l = a->layers[li];
+    QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_in, k, H, d.rms_eps, w.xn, L), "rmsnorm");
+    QD_TRY(gemm(l->w.w_qkv, q8 ? l->w.s_qkv : nullptr, QKV, H, w.xn, EPI_STORE, w.qkv), "qkv gemm");
+    // all k rows' K/V go to the cache first, so row i attends to rows pos .. pos + i
+    QD_TRY(launch_kv_write(w.qkv, k, Hq, Hkv, l->w.k_norm, a->rope_table, a->rope_max_pos, d.rms_eps, 1, v.vpos,
+                           v.vpt, a->page_size, a->max_pages, a->n_pages, a->k_cache[li], a->v_cache[li], L),
+           "kv write");
+    AttnArgs at = {};
+    at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
+    at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps; at.act_bf16 = 1;
+    at.pos = v.vpos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = v.vpt;
+    at.B = k; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
+    at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D); at.out_bf16 = w.attn;
+    at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.kv_ready = 1;
+    QD_TRY(launch_attention(at, L), "attention");
+    QD_TRY(gemm(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, EPI_RESID_ADD, w.res), "o gemm");
+    QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, k, H, d.rms_eps, w.xn, L), "rmsnorm");
+    QD_TRY(gemm(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, EPI_STORE, w.gu), "gu gemm");
+    QD_TRY(launch_swiglu_rows(w.gu, k, F, w.xn, L), "swiglu");
+    QD_TRY(gemm(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, EPI_RESID_ADD, w.res), "down gemm");
+  }
+  QD_TRY(launch_rmsnorm_rows(w.res, a->final_norm, k, H, d.rms_eps, w.xn, L), "final rmsnorm");
+  QD_TRY(gemm(a->lm_head, a->lm_head_scales, a->vocab, H, w.xn, EPI_STORE, logits), "lm head gemm");
+  QD_TRY(launch_argmax_advance(logits, a->vocab, k, target, v.scratch, v.scratch + k, v.scratch + 2 * k, 1,
+                               w.argmax_ws, L),
+         "argmax");
+  QD_TRY(launch_verify_accept(draft, target, k, a->tok, a->pos, a->step, a->out_tokens, a->max_steps, n_accept, L),
+         "accept");
+  return QD_OK;
+}
+
 }  // namespace
+
+size_t qd_verify_workspace_bytes(const qd_step_args* a, int k) {
+  if (!a || !a->layers || a->n_layers < 1 || !a->layers[0] || k < 1 || k > kMaxVerify) return 0;
+  return verify_ws_layout(a, k, nullptr).total;
+}
+
+int qd_verify_step(const qd_step_args* a, const int32_t* draft, int k, float* logits, int32_t* target,
+                   int32_t* n_accept, cudaStream_t stream) {
+  int rc = validate_verify(a, draft, k, logits, target, n_accept);
+  if (rc) return rc;
+  return run_verify(a, draft, k, logits, target, n_accept, stream);
+}
 
 size_t qd_step_workspace_bytes(const qd_step_args* a) {
   if (!a || !a->layers || a->n_layers < 1 || !a->layers[0] || a->batch < 1) return 0;

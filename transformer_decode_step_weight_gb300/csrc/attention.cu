@@ -81,6 +81,7 @@ struct AttnParams {
   const __nv_bfloat16* k_next;  // the next layer's caches: this split's rows go to L2
   const __nv_bfloat16* v_next;
   int kv_pf;                    // 0 off, 1 evict-normal, 2 evict-last
+  int kv_ready;                 // the current token's K/V rows are already in the cache
 };
 
 struct Carve {
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   }
   const int n_tiles = (t_end - t0 + kTile - 1) / kTile;
   // in the fused form the current token `pos` is not read from the cache
-  const int copy_end = FUSED ? min(t_end, pos) : t_end;
+  const int copy_end = (FUSED && !p.kv_ready) ? min(t_end, pos) : t_end;
 
   auto stage_k = [&](int st) { return sKV + (size_t)st * 2 * kTile * kD; };
   auto stage_v = [&](int st) { return sKV + (size_t)st * 2 * kTile * kD + kTile * kD; };
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
   // The RoPE row, the QK-norm weights and the cache page of the current token
   // do not come from the previous kernel either: load them before the wait.
   float k_new = 0.f, v_new = 0.f;
-  const bool own_pos = FUSED && pos >= t0 && pos < t_end;
+  const bool own_pos = FUSED && !p.kv_ready && pos >= t0 && pos < t_end;
   const int d = tid & (kD - 1);
   float2 cs = make_float2(0.f, 0.f);
   float wq = 0.f, wk = 0.f;
@@ -876,6 +877,7 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
   p.k_next = (const __nv_bfloat16*)a.k_next;
   p.v_next = (const __nv_bfloat16*)a.v_next;
   p.kv_pf = a.kv_pf;
+  p.kv_ready = a.kv_ready;
   const bool fused = a.qkv != nullptr;
   // the fused decode step splits each sequence across one thread block cluster;
   // the standalone call keeps the workspace split (its workspace is the scratch)
@@ -891,6 +893,59 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
     default: return cudaErrorInvalidValue;
   }
 #undef QD_ATTN_CASE
+}
+
+// One CTA of 128 threads per (kv head, row): the k head of the row normed and
+// rotated as in the fused prologue above (warp sums combined as (w0 + w1) + (w2 + w3)),
+// v as is, both rounded to bf16 and stored at the row's position.
+__global__ void __launch_bounds__(kD) kv_write_kernel(const float* qkv, int Hq, int Hkv, const __nv_bfloat16* k_norm,
+                                                      const float2* rope, int rope_max_pos, float eps, int act_bf16,
+                                                      const int32_t* pos, const int32_t* page_table, int page_size,
+                                                      int max_pages, int n_pages, __nv_bfloat16* k_pages,
+                                                      __nv_bfloat16* v_pages, int* err) {
+  __shared__ float red[4];
+  __shared__ float s_y[kD];
+  const int g = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31, warp = d >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int ps_ = pos[b];
+  if (ps_ < 0 || ps_ >= max_pages * page_size || ps_ >= rope_max_pos) {
+    if (d == 0) set_error(err, QD_DEVERR_POS);
+    return;
+  }
+  const int qkv_w = (Hq + 2 * Hkv) * kD;
+  const float x = qkv[(size_t)b * qkv_w + (Hq + g) * kD + d];
+  const float vx = qkv[(size_t)b * qkv_w + (Hq + Hkv + g) * kD + d];
+  const float ss = warp_sum(x * x);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  const float tot = (red[0] + red[1]) + (red[2] + red[3]);
+  const float inv = 1.0f / sqrtf(tot / (float)kD + eps);
+  float n = x * inv;
+  if (act_bf16) n = round_bf16(n);
+  float y = __bfloat162float(k_norm[d]) * n;
+  if (act_bf16) y = round_bf16(y);
+  s_y[d] = y;
+  __syncthreads();
+  const float2 cs = rope[(size_t)ps_ * (kD / 2) + (d & 63)];
+  const float other = s_y[d ^ 64];
+  const float r = (d < 64) ? (y * cs.x - other * cs.y) : (y * cs.x + other * cs.y);
+  const PagedSlot sl = paged_slot(page_table + (size_t)b * max_pages, ps_, page_size, n_pages);
+  if (!sl.ok) {
+    if (d == 0) set_error(err, QD_DEVERR_PAGE);
+    return;
+  }
+  const size_t off = (((size_t)sl.page * Hkv + g) * page_size + sl.slot) * kD + d;
+  k_pages[off] = __float2bfloat16_rn(round_bf16(r));
+  v_pages[off] = __float2bfloat16_rn(round_bf16(vx));
+}
+
+cudaError_t launch_kv_write(const float* qkv, int B, int Hq, int Hkv, const void* k_norm, const float* rope,
+                            int rope_max_pos, float eps, int act_bf16, const int32_t* pos, const int32_t* page_table,
+                            int page_size, int max_pages, int n_pages, void* k_pages, void* v_pages, const Launch& L) {
+  return launch_ex(kv_write_kernel, dim3(Hkv, B), dim3(kD), 0, L, qkv, Hq, Hkv, (const __nv_bfloat16*)k_norm,
+                   (const float2*)rope, rope_max_pos, eps, act_bf16, pos, page_table, page_size, max_pages, n_pages,
+                   (__nv_bfloat16*)k_pages, (__nv_bfloat16*)v_pages, L.err);
 }
 
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float theta, cudaStream_t s) {

@@ -65,6 +65,7 @@ struct MParams {
   int* ws_cnt;
   int* err;
   int trig_late;
+  int kv_ready;
 };
 
 // ---- warp-level MMA / ldmatrix / cp.async wrappers
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
   const int t0 = s * p.chunk;
   const int t_end = min(t0 + p.chunk, len);
   const int n_tiles = (t_end - t0 + kT - 1) / kT;
-  const int skip_tok = FUSED ? pos : -1;   // the current token comes from registers
+  const int skip_tok = (FUSED && !p.kv_ready) ? pos : -1;   // the current token comes from registers
   const uint32_t ring_u = smem_u32(ring);
   auto tileK = [&](int st) { return ring_u + (uint32_t)(st * 2 * kTileBytes); };
   auto tileV = [&](int st) { return ring_u + (uint32_t)(st * 2 * kTileBytes + kTileBytes); };
@@ -256,7 +257,7 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
   }
 
   float k_new = 0.f, v_new = 0.f;
-  const bool own_pos = FUSED && pos >= t0 && pos < t_end;
+  const bool own_pos = FUSED && !p.kv_ready && pos >= t0 && pos < t_end;
   if (FUSED) {
     const float2 cs = p.rope[(size_t)pos * (kD / 2) + (tid & 63)];
     float xv[REP + 1];
@@ -673,6 +674,7 @@ cudaError_t launch_attention_mma(const AttnArgs& a, int chunk, size_t slots, con
   p.ws_cnt = (int*)(ws + al(slots * rep * kD * 4) + al(slots * rep * 2 * 4));
   p.err = L.err;
   p.trig_late = L.trig_late;
+  p.kv_ready = a.kv_ready;
   const bool fused = a.qkv != nullptr;
   switch (rep) {
     case 1: return fused ? launch_ms<1, true>(p, L) : launch_ms<1, false>(p, L);

@@ -153,6 +153,9 @@ struct AttnArgs {
   int trig_loop;          // CUDA-core form: let the next kernel launch only once this
                           // CTA's K/V loop is done (its weight prefetch then does not
                           // compete with the K/V tiles); 0: at the start
+  int kv_ready;           // fused form: the current token's K/V rows are already in the
+                          // cache (written by launch_kv_write); read them from there and
+                          // do not write them (several rows of one sequence in one launch)
 };
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int max_ctx);
 int attn_chunk(int B, int Hkv, int max_ctx);
@@ -164,6 +167,13 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L);
 size_t attn_noalloc_scratch_bytes();
 cudaError_t attn_noalloc_scratch(int B, int Hq, int Hkv, int max_ctx, void** ptr, cudaStream_t stream);
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float theta, cudaStream_t s);
+// K/V rows of the current tokens into the cache: for row b < B and kv head g,
+// k = RoPE_pos[b](RMSNorm(qkv[b] k-head g; k_norm)) and v, both rounded to bf16, at
+// logical position pos[b] through page_table row b (the attention's fused prologue
+// arithmetic, with bf16 activations when act_bf16).
+cudaError_t launch_kv_write(const float* qkv, int B, int Hq, int Hkv, const void* k_norm, const float* rope,
+                            int rope_max_pos, float eps, int act_bf16, const int32_t* pos, const int32_t* page_table,
+                            int page_size, int max_pages, int n_pages, void* k_pages, void* v_pages, const Launch& L);
 
 // ----------------------------------------------------------------- persistent batch-1 step
 // The whole decode step of a BF16 model at batch 1 as one cooperative kernel
@@ -205,6 +215,17 @@ cudaError_t launch_argmax_advance(const float* logits, int V, int B, int32_t* to
                                   const Launch& L);
 cudaError_t launch_embed(const void* embed, int H, int V, const int32_t* tok, int B, float* res,
                          const Launch& L);
+// Speculative verify (one sequence, k rows): row inputs tokens[i] = i ? draft[i - 1]
+// : tok[0], positions pos[0] + i, page-table row 0 copied k times, and scratch
+// argmax state zeroed; then, after the rows' argmax into target[k], the accepted
+// prefix m (draft[i] == target[i] for i < m, m <= k - 1), out_tokens[step ..] =
+// draft[0 .. m - 1], target[m]; tok = target[m], pos += m + 1, step += m + 1.
+cudaError_t launch_verify_prep(const int32_t* tok, const int32_t* pos, const int32_t* draft, int k,
+                               const int32_t* page_table, int max_pages, int32_t* tokens, int32_t* vpos,
+                               int32_t* vpt, int32_t* scratch, const Launch& L);
+cudaError_t launch_verify_accept(const int32_t* draft, const int32_t* target, int k, int32_t* tok, int32_t* pos,
+                                 int32_t* step, int32_t* out_tokens, int max_steps, int32_t* n_accept,
+                                 const Launch& L);
 cudaError_t launch_paged_indices(const int32_t* pt, int B, int max_pages, int ps, int n_pages, int n_tokens,
                                  int32_t* idx, const Launch& L);
 

@@ -209,7 +209,56 @@ __global__ void paged_indices_kernel(const int32_t* pt, int B, int max_pages, in
   idx[i] = sl.ok ? sl.page * ps + sl.slot : -1;
 }
 
+// Row inputs of a speculative verify pass (one sequence, k rows).
+__global__ void verify_prep_kernel(const int32_t* tok, const int32_t* pos, const int32_t* draft, int k,
+                                   const int32_t* page_table, int max_pages, int32_t* tokens, int32_t* vpos,
+                                   int32_t* vpt, int32_t* scratch) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    tokens[i] = i == 0 ? tok[0] : draft[i - 1];
+    vpos[i] = pos[0] + i;
+    scratch[i] = 0;             // argmax scratch: position
+    scratch[k + i] = 0;         // ... and step (one output slot per row)
+  }
+  for (int e = threadIdx.x; e < k * max_pages; e += blockDim.x) vpt[e] = page_table[e % max_pages];
+}
+
+// The accepted prefix of the drafts and the state advance (one thread).
+__global__ void verify_accept_kernel(const int32_t* draft, const int32_t* target, int k, int32_t* tok, int32_t* pos,
+                                     int32_t* step, int32_t* out_tokens, int max_steps, int32_t* n_accept, int* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x != 0) return;
+  int m = 0;
+  while (m < k - 1 && draft[m] == target[m]) ++m;
+  const int st = step[0];
+  for (int i = 0; i <= m; ++i) {
+    const int t = i < m ? draft[i] : target[m];
+    if (st + i >= 0 && st + i < max_steps) out_tokens[st + i] = t;
+    else set_error(err, QD_DEVERR_STEPS);
+  }
+  tok[0] = target[m];
+  pos[0] += m + 1;
+  step[0] = st + m + 1;
+  n_accept[0] = m;
+}
+
 }  // namespace
+
+cudaError_t launch_verify_prep(const int32_t* tok, const int32_t* pos, const int32_t* draft, int k,
+                               const int32_t* page_table, int max_pages, int32_t* tokens, int32_t* vpos,
+                               int32_t* vpt, int32_t* scratch, const Launch& L) {
+  return launch_ex(verify_prep_kernel, dim3(1), dim3(256), 0, L, tok, pos, draft, k, page_table, max_pages, tokens,
+                   vpos, vpt, scratch);
+}
+
+cudaError_t launch_verify_accept(const int32_t* draft, const int32_t* target, int k, int32_t* tok, int32_t* pos,
+                                 int32_t* step, int32_t* out_tokens, int max_steps, int32_t* n_accept,
+                                 const Launch& L) {
+  return launch_ex(verify_accept_kernel, dim3(1), dim3(32), 0, L, draft, target, k, tok, pos, step, out_tokens,
+                   max_steps, n_accept, L.err);
+}
 
 size_t argmax_workspace_bytes(int B) {
   return (((size_t)B * kArgmaxBlocks * sizeof(Cand) + 255) & ~(size_t)255) + (size_t)B * 4;
