@@ -44,8 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3-8b-bf16",
-                    choices=["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-bf16-paged-b64",
-                             "qwen3-8b-q8_0-paged-b64"])
+                    choices=["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-int4",
+                             "qwen3-8b-bf16-paged-b64", "qwen3-8b-q8_0-paged-b64"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=128)
@@ -168,11 +168,21 @@ class ClockSampler:
 
 
 def weight_bytes(s: synth.Shape, wtype: str) -> int:
-    """Bytes of weights one token streams: every projection, the LM head, norms, one embedding row."""
-    per_w = 2.0 if wtype == "bf16" else 34.0 / 32.0
-    layer = (s.qkv_rows * s.hidden + s.hidden * s.n_q_heads * s.head_dim + 2 * s.ffn * s.hidden +
-             s.hidden * s.ffn) * per_w + (2 * s.hidden + 2 * s.head_dim) * 2
-    return int(s.n_layers * layer + s.vocab * s.hidden * per_w + s.hidden * 2 + s.hidden * 2)
+    """Bytes of weights one token streams: every projection, the LM head, norms, one embedding row.
+    BF16: 2 B per weight; Q8_0: 34 B per 32 weights; INT4: 0.5 B per weight plus a 2-byte
+    scale per output row."""
+    mats = [(s.qkv_rows, s.hidden), (s.hidden, s.n_q_heads * s.head_dim), (2 * s.ffn, s.hidden),
+            (s.hidden, s.ffn)]
+
+    def mbytes(r, k):
+        if wtype == "bf16":
+            return r * k * 2.0
+        if wtype == "q8_0":
+            return r * k * 34.0 / 32.0
+        return r * k * 0.5 + r * 2.0
+
+    layer = sum(mbytes(r, k) for r, k in mats) + (2 * s.hidden + 2 * s.head_dim) * 2
+    return int(s.n_layers * layer + mbytes(s.vocab, s.hidden) + s.hidden * 2 + s.hidden * 2)
 
 
 def kv_bytes(s: synth.Shape, pos: int) -> int:
@@ -221,10 +231,30 @@ def _oracle_layer(oracle, lt: synth.LayerTensors, wtype: str):
     if wtype == "bf16":
         w, sc = {k: synth.bits_u16(getattr(lt, k)) for k in mats}, {}
     else:
-        w = {k: synth.host_i8(getattr(lt, k)) for k in mats}
+        host = synth.host_u8 if wtype == "int4" else synth.host_i8
+        w = {k: host(getattr(lt, k)) for k in mats}
         sc = {k: synth.bits_u16(getattr(lt, k)) for k in ("s_qkv", "s_o", "s_gu", "s_down")}
     n = {k: synth.bits_u16(getattr(lt, k)) for k in ("ln_in", "ln_post", "q_norm", "k_norm")}
     return oracle.LayerWeights(**w, **n, **sc)
+
+
+def _oracle_lane(mt, wl, q8_act: str = "f32"):
+    """(mode, act) of the oracle lane that the GPU step runs for this workload."""
+    if mt.wtype == "bf16":
+        mode, act = "bf16", "bf16"
+    elif mt.wtype == "int4":
+        mode, act = "bf16", "w4"
+    else:  # the Q8_0 lane the GPU step runs at the workload's batch
+        mode, act = ("bf16", "w_bf16") if wl.batch > 1 else ("f32", q8_act)
+    return mode, act
+
+
+def _oracle_lm_rows(mt, idx):
+    """The LM head's rows `idx` (and their scales) as the oracle takes them."""
+    if mt.lm_head_scales is None:
+        return synth.bits_u16(mt.lm_head[idx]), None
+    host = synth.host_u8 if mt.lm_head.dtype == torch.uint8 else synth.host_i8
+    return host(mt.lm_head[idx]), synth.bits_u16(mt.lm_head_scales[idx])
 
 
 def _oracle_cache0(oracle, mt, n_tokens: int):
@@ -372,6 +402,8 @@ def dtype_label(wl, act, lm_act):
     """The arithmetic the step computes in: bf16 MMA / FMA, or the Q8_0 lanes."""
     if wl.wtype == "bf16":
         return "bf16"
+    if wl.wtype == "int4":
+        return "int4 weights x bf16 activations (f32 accumulate)"
     if wl.batch > 1:
         return "q8_0->bf16"          # weights widened on chip, bf16 tensor-core MMA
     return f"q8_0/{act}" if act == lm_act else f"q8_0/{act}+head_{lm_act}"
@@ -500,21 +532,18 @@ def cpu_baseline(mt, s, wl, ctx, n_layers_sample: int = 8):
     frac = n_layers_sample / s.n_layers
     rows = np.arange(0, s.vocab, int(round(1 / frac)))
     idx = torch.as_tensor(rows, device=mt.lm_head.device)
-    lm_bits = synth.bits_u16(mt.lm_head[idx]) if mt.lm_head_scales is None else None
-    if mt.wtype == "bf16":
-        mode, act = "bf16", "bf16"
-    else:  # the Q8_0 lane the GPU step runs at this batch
-        mode, act = ("bf16", "w_bf16") if wl.batch > 1 else ("f32", "f32")
+    lm, lms = _oracle_lm_rows(mt, idx)
+    mode, act = _oracle_lane(mt, wl)
     fn = synth.bits_u16(mt.final_norm)
     t0 = time.perf_counter()
     res = x0
     for _ in range(n_layers_sample):
         res = oracle.layer_step(od, ol, x0, k0, v0, ctx, mode=mode, act=act)
     xf = oracle.rmsnorm(res, oracle.bf16_to_f64(fn), s.rms_eps, mode)
-    if mt.lm_head_scales is None:
-        oracle.gemv_bf16(lm_bits, xf)
+    if lms is None:
+        oracle.gemv_bf16(lm, xf)
     else:
-        oracle.gemv_q8_0(synth.host_i8(mt.lm_head[idx]), synth.bits_u16(mt.lm_head_scales[idx]), x=xf, act=act)
+        oracle.project(lm, lms, xf, act)
     dt = time.perf_counter() - t0
     sec_per_tok = dt / frac
     return {"value": round(1.0 / sec_per_tok, 5), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
@@ -542,12 +571,8 @@ def run_reference(args, dist, rank, world, local):
     x0 = oracle.bf16_to_f64(synth.bits_u16(mt.embed[int(mt.start_tok[0])]))
     rows = np.arange(0, s.vocab, s.n_layers)
     idx = torch.as_tensor(rows, device=mt.lm_head.device)
-    if wl.wtype == "bf16":
-        mode, act = "bf16", "bf16"
-        lm, lms = synth.bits_u16(mt.lm_head[idx]), None
-    else:  # the Q8_0 lane the GPU step runs at the workload's batch
-        mode, act = ("bf16", "w_bf16") if wl.batch > 1 else ("f32", q8_lanes(args)[0])
-        lm, lms = synth.host_i8(mt.lm_head[idx]), synth.bits_u16(mt.lm_head_scales[idx])
+    mode, act = _oracle_lane(mt, wl, q8_lanes(args)[0])
+    lm, lms = _oracle_lm_rows(mt, idx)
     fn = oracle.bf16_to_f64(synth.bits_u16(mt.final_norm))
     del mt
 

@@ -71,7 +71,9 @@ enum {
   QD_DEVERR_TIMEOUT = 16,  /* a bounded wait on an asynchronous copy gave up */
 };
 
-typedef enum { QD_W_BF16 = 0, QD_W_Q8_0 = 1 } qd_wtype;
+/* Weight formats: BF16; Q8_0 (32-wide int8 blocks with an fp16 scale); INT4 (W4A16: */
+/* 4-bit codes with one fp16 scale per output row, see qd_gemv_w4).                  */
+typedef enum { QD_W_BF16 = 0, QD_W_Q8_0 = 1, QD_W_INT4 = 2 } qd_wtype;
 /* Q8_0 activation lanes ([EQ-SPEED] ``deq``): F32 = dequantising lane,
  * I8 = activation re-quantised per 32-block to int8 (dp4a lane). */
 typedef enum { QD_ACT_F32 = 0, QD_ACT_I8 = 1 } qd_act;
@@ -119,6 +121,27 @@ size_t qd_gemm_workspace_bytes(int rows, int cols, qd_wtype wtype);
 int qd_gemm_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const void* x_bf16,
                  int batch, float* y, void* workspace, size_t workspace_bytes,
                  cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* W4A16 GEMV ("GPU Kernel Lab" README, "Quantization experiments": W4A16 decode */
+/* GEMV, packed INT4 LM head with local top-k, per-output-channel weight          */
+/* quantization; "qwen3-8b-rtx4080-cutedsl" README, "W4A16 dequant-fused GEMM").   */
+/* W: uint8 [rows, cols/2], each byte two offset-binary nibbles u = q + 8 (q in    */
+/* [-8, 7]), the even column in the low nibble; d: f16 [rows], one scale per row:  */
+/* w[r, c] = f32(d[r]) * q[r, c].  y[r] = sum_c w[r, c] * x[c] with x bf16 [cols];  */
+/* y f32 [rows]; batch 1, f32 accumulation. Limits: cols % 32 == 0, cols <= 16384; */
+/* W and x 16-byte aligned, d 2-byte aligned.                                      */
+int qd_gemv_w4(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, float* y,
+               cudaStream_t stream);
+/* The INT4 LM-head form: y as qd_gemv_w4 (the logits), and the top k rows of y     */
+/* (value descending, the lower row first among equal values, NaN never chosen):  */
+/* topk_ids int32 [k] (-1 past the non-NaN rows), topk_vals f32 [k]. Each CTA picks */
+/* the top k of its rows; the last CTA merges them. 1 <= k <= 16. workspace:        */
+/* zero-filled device scratch of qd_w4_topk_workspace_bytes() bytes, left zero.   */
+size_t qd_w4_topk_workspace_bytes(void);
+int qd_gemv_w4_topk(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, int k,
+                    float* y, int32_t* topk_ids, float* topk_vals, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream);
 
 /* Activation re-quantisation per 32-block ([EQ-SPEED] item 3): amax = max|x|,  */
 /* d = amax / 127, q = round-half-away(x * (1/d)) in IEEE binary32 (0 if d = 0), */
@@ -200,7 +223,8 @@ typedef struct {
 /* Row order ([EQ-SPEED] item 1): w_qkv = [q rows (Hq*D); k rows (Hkv*D);       */
 /* v rows (Hkv*D)] x hidden; w_o = hidden x (Hq*D); w_gu = [gate rows (ffn);     */
 /* up rows (ffn)] x hidden; w_down = hidden x ffn. BF16: bf16 matrices, s_* NULL. */
-/* Q8_0: int8 matrices plus f16 scales [rows, cols/32]. Norm weights: bf16.     */
+/* Q8_0: int8 matrices plus f16 scales [rows, cols/32]. INT4: packed matrices    */
+/* [rows, cols/2] (as qd_gemv_w4) plus f16 scales [rows]. Norm weights: bf16.     */
 typedef struct {
   const void *w_qkv, *w_o, *w_gu, *w_down;
   const void *s_qkv, *s_o, *s_gu, *s_down;
@@ -232,7 +256,12 @@ int qd_destroy_layer(qd_layer* layer);
 /* tcgen05 GEMM over the batch (dims % 64 == 0). Q8_0 layers: batch 1 runs the   */
 /* Q8_0 GEMV lanes (act, lm_act); 2..64 runs the tcgen05 GEMMs with the weights  */
 /* widened to bf16 as in qd_gemm_q8_0 (act and lm_act unused; dims % 256 == 0,   */
-/* scales 16-byte aligned).                                                     */
+/* scales 16-byte aligned). INT4 layers: batch 1, the W4A16 GEMVs with bf16      */
+/* activations (dims % 32 == 0, <= 16384).                                       */
+/* LM head: lm_wtype QD_W_INT4 with lm_head_scales = the per-row f16 scales is an */
+/* INT4 head (batch 1): its GEMV also picks the top_k tokens (0: only the argmax)  */
+/* into topk_ids / topk_vals [top_k] and advances the step itself. Otherwise the  */
+/* head is Q8_0 when lm_head_scales is set, else bf16, followed by argmax_advance. */
 typedef struct {
   const qd_layer* const* layers;
   int n_layers;
@@ -254,6 +283,10 @@ typedef struct {
   float* logits;
   void* workspace;
   size_t workspace_bytes;
+  qd_wtype lm_wtype;   /* QD_W_INT4 for an INT4 head (see above) */
+  int top_k;           /* INT4 head: 0..16 tokens into topk_ids / topk_vals */
+  int32_t* topk_ids;
+  float* topk_vals;
 } qd_step_args;
 
 size_t qd_step_workspace_bytes(const qd_step_args* args);

@@ -37,7 +37,13 @@ Readings where those pages are silent (each also listed in the design notes):
     id = 1 / d (0 when d == 0), q = round-half-away-from-zero(x * id), all in
     IEEE binary32, d stored as fp16 (round to nearest even).
   * Argmax: the lowest index among equal maxima; NaN never wins; an all-NaN
-    row gives index 0.
+    row gives index 0. Top-k: the k largest in that order (value descending,
+    lowest index first among equal values), NaN never chosen.
+  * INT4 (W4A16, "GPU Kernel Lab" README, "Quantization experiments": W4A16
+    decode GEMV, packed INT4 LM head with local top-k, per-output-channel weight
+    quantization): q in [-8, 7] with one fp16 scale per output row,
+    w = f32(d_r) * q; two values per byte as offset-binary nibbles q + 8, the
+    even column in the low nibble. Activations stay bf16.
 
 Accumulation. Every product-sum (the projections) is accumulated in float64
 (``acc="f64"``, the default). ``acc="f32"`` evaluates the same sums in IEEE
@@ -299,8 +305,52 @@ def gemv_q8_0(qs, d_bits, x=None, xq=None, xd_bits=None, act: str = "f32",
 
 
 # --------------------------------------------------------------------------
-# argmax, paged addressing
+# INT4 (W4A16)
 # --------------------------------------------------------------------------
+
+
+def int4_unpack(packed) -> np.ndarray:
+    """Codes q [R, K] (int64, -8 .. 7) of packed rows [R, K / 2] (uint8)."""
+    b = np.asarray(packed, dtype=np.uint8).astype(np.int64)
+    r, kh = b.shape
+    q = np.empty((r, 2 * kh), dtype=np.int64)
+    q[:, 0::2] = (b & 0xF) - 8
+    q[:, 1::2] = (b >> 4) - 8
+    return q
+
+
+def int4_dequant(packed, d_bits) -> np.ndarray:
+    """W[r, k] = f32(d[r]) * q[r, k]."""
+    return int4_unpack(packed).astype(np.float64) * f16_to_f64(d_bits)[:, None]
+
+
+def gemv_w4(packed, d_bits, x, row_chunk: int = 8192, acc: str = "f64") -> np.ndarray:
+    """y = W x for INT4 rows with per-row scales; x is the bf16 activation."""
+    packed = np.asarray(packed)
+    x = np.asarray(x, dtype=np.float64)
+    r = packed.shape[0]
+    y = np.empty(r, dtype=np.float64)
+    for r0 in range(0, r, row_chunk):
+        y[r0:r0 + row_chunk] = _matvec(int4_dequant(packed[r0:r0 + row_chunk], np.asarray(d_bits)[r0:r0 + row_chunk]),
+                                       x, acc)
+    return y
+
+
+# --------------------------------------------------------------------------
+# argmax, top-k, paged addressing
+# --------------------------------------------------------------------------
+
+
+def topk_first(logits, k: int):
+    """The k largest logits, value descending, the lower index first among equal
+    values, NaN never chosen: (indices, values). Fewer than k non-NaN entries give
+    fewer results."""
+    raw = np.asarray(logits, dtype=np.float64)
+    idx = np.arange(raw.size)
+    ok = ~np.isnan(raw)
+    order = np.lexsort((idx[ok], -raw[ok]))   # last key primary: value descending, then index
+    sel = idx[ok][order][:k]
+    return sel, raw[sel]
 
 
 def argmax_first(logits) -> int:
@@ -361,7 +411,8 @@ class LayerWeights:
 
     BF16 model: ``w_*`` are uint16 bf16 bits [rows, cols] and ``s_*`` are None.
     Q8_0 model: ``w_*`` are int8 [rows, cols] and ``s_*`` uint16 fp16 bits
-    [rows, cols / 32]. Norm weights are uint16 bf16 bits.
+    [rows, cols / 32]. INT4 model: ``w_*`` are packed uint8 [rows, cols / 2] and
+    ``s_*`` uint16 fp16 bits [rows]. Norm weights are uint16 bf16 bits.
     Row order: w_qkv = [q rows (Hq*D); k rows (Hkv*D); v rows (Hkv*D)],
     w_gu = [gate rows (F); up rows (F)].
     """
@@ -386,6 +437,7 @@ def project(w, s, x, act: str, acc: str = "f64"):
     act == "f32":  Q8_0 dequantising lane (x binary32).
     act == "i8":   Q8_0 dp4a lane: x re-quantised per 32-block first.
     act == "w_bf16": Q8_0 weights widened to bf16, x bf16 (batched tensor-core step).
+    act == "w4":   INT4 weights with per-row scales (packed uint8, fp16 scales), x bf16.
     """
     if act == "bf16":
         return gemv_bf16(w, x, acc=acc)
@@ -396,6 +448,8 @@ def project(w, s, x, act: str, acc: str = "f64"):
         return gemv_q8_0(w, s, xq=xq, xd_bits=xd, act="i8", acc=acc)
     if act == "w_bf16":
         return gemv_q8_0(w, s, x=x, act="w_bf16", acc=acc)
+    if act == "w4":
+        return gemv_w4(w, s, x, acc=acc)
     raise ValueError(act)
 
 

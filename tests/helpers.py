@@ -3,6 +3,7 @@ teacher-forced comparison of a GPU decode run with the oracle."""
 from __future__ import annotations
 
 import numpy as np
+import torch
 
 import oracle
 from transformer_decode_step_weight_gb300 import synth
@@ -17,6 +18,9 @@ def oracle_layer(lt: synth.LayerTensors, wtype: str) -> oracle.LayerWeights:
     if wtype == "bf16":
         w = {k: synth.bits_u16(getattr(lt, k)) for k in ("w_qkv", "w_o", "w_gu", "w_down")}
         s = {}
+    elif wtype == "int4":
+        w = {k: synth.host_u8(getattr(lt, k)) for k in ("w_qkv", "w_o", "w_gu", "w_down")}
+        s = {k: synth.bits_u16(getattr(lt, k)) for k in ("s_qkv", "s_o", "s_gu", "s_down")}
     else:
         w = {k: synth.host_i8(getattr(lt, k)) for k in ("w_qkv", "w_o", "w_gu", "w_down")}
         s = {k: synth.bits_u16(getattr(lt, k)) for k in ("s_qkv", "s_o", "s_gu", "s_down")}
@@ -26,7 +30,9 @@ def oracle_layer(lt: synth.LayerTensors, wtype: str) -> oracle.LayerWeights:
 
 def oracle_model(mt: synth.ModelTensors) -> oracle.Model:
     layers = [oracle_layer(lt, mt.wtype) for lt in mt.layers]
-    if mt.lm_head_scales is not None:
+    if mt.lm_head_scales is not None and mt.lm_head.dtype == torch.uint8:
+        lm, lms = synth.host_u8(mt.lm_head), synth.bits_u16(mt.lm_head_scales)
+    elif mt.lm_head_scales is not None:
         lm, lms = synth.host_i8(mt.lm_head), synth.bits_u16(mt.lm_head_scales)
     else:
         lm, lms = synth.bits_u16(mt.lm_head), None

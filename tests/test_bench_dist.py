@@ -65,10 +65,14 @@ def test_weight_byte_accounting_matches_the_shapes():
     assert bench.kv_bytes(s, 4095) == 36 * 8 * 128 * 2 * 2 * 4096
     q8 = bench.weight_bytes(s, "q8_0")
     assert abs(q8 / wb - 1.0625 / 2) < 1e-3
+    # INT4: half a byte per weight plus one 2-byte scale per output row
+    w4 = bench.weight_bytes(s, "int4")
+    rows = 36 * (6144 + 4096 + 24576 + 4096) + 151936
+    assert w4 - layers // 4 - 151936 * 4096 // 2 - rows * 2 == 36 * (2 * 4096 + 2 * 128) * 2 + 2 * 4096 * 2
 
 
-@pytest.mark.parametrize("name", ["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-bf16-paged-b64",
-                                  "qwen3-8b-q8_0-paged-b64"])
+@pytest.mark.parametrize("name", ["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-int4",
+                                  "qwen3-8b-bf16-paged-b64", "qwen3-8b-q8_0-paged-b64"])
 def test_workloads_are_the_named_shapes(name):
     from transformer_decode_step_weight_gb300 import synth
     wl = synth.WORKLOADS[name]

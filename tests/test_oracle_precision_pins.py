@@ -255,3 +255,44 @@ def test_f32_accumulation_exact_on_integers_and_within_the_summation_bound():
     nb = K // 32
     assert np.all(np.abs(a32 - a64) <= (nb + 3) * u / (1 - (nb + 3) * u) * terms)
     assert np.any(a32 != a64)
+
+
+# ---------------------------------------------------------------- INT4 and top-k
+
+
+def test_int4_unpack_hand_packed_bytes():
+    # byte 0x3F: low nibble 15 -> 7, high nibble 3 -> -5; 0x80: 0 -> -8, 8 -> 0
+    packed = np.array([[0x3F, 0x80], [0x08, 0xF7]], dtype=np.uint8)
+    np.testing.assert_array_equal(oracle.int4_unpack(packed), [[7, -5, -8, 0], [0, -8, -1, 7]])
+    d = np.array([0x3C00, 0x4000], dtype=np.uint16)    # fp16 1.0, 2.0
+    np.testing.assert_array_equal(oracle.int4_dequant(packed, d), [[7, -5, -8, 0], [0, -16, -2, 14]])
+
+
+def test_gemv_w4_brute_force_and_unit_scale_exact():
+    rng = np.random.default_rng(41)
+    R, K = 7, 64
+    q = rng.integers(-8, 8, size=(R, K))
+    packed = ((q[:, 0::2] + 8) | ((q[:, 1::2] + 8) << 4)).astype(np.uint8)
+    x = rng.integers(-9, 10, size=K).astype(np.float64)
+    one = np.full(R, 0x3C00, dtype=np.uint16)
+    y = oracle.gemv_w4(packed, one, x)
+    assert list(y.astype(np.int64)) == [sum(int(q[r, c]) * int(x[c]) for c in range(K)) for r in range(R)]
+    d = (np.abs(rng.standard_normal(R)) * 0.01).astype(np.float16)
+    xb = oracle.round_bf16(rng.standard_normal(K))
+    y = oracle.gemv_w4(packed, d.view(np.uint16), xb)
+    for r in range(R):
+        ref = math.fsum(float(d[r]) * int(q[r, c]) * float(xb[c]) for c in range(K))
+        assert y[r] == pytest.approx(ref, rel=1e-13, abs=1e-15)
+
+
+def test_topk_first_order_ties_and_nan():
+    v = np.array([1.0, 5.0, np.nan, 5.0, -np.inf, 3.0, 5.0])
+    idx, val = oracle.topk_first(v, 4)
+    assert list(idx) == [1, 3, 6, 5] and list(val) == [5.0, 5.0, 5.0, 3.0]
+    idx, _ = oracle.topk_first(np.array([np.nan, -np.inf, -np.inf]), 3)
+    assert list(idx) == [1, 2]
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal(5000)
+    idx, _ = oracle.topk_first(x, 8)
+    assert idx[0] == oracle.argmax_first(x)
+    assert list(idx) == list(np.argsort(-x, kind="stable")[:8])

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libqd.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "qd.h")
 
 QD_OK = 0
-QD_W_BF16, QD_W_Q8_0 = 0, 1
+QD_W_BF16, QD_W_Q8_0, QD_W_INT4 = 0, 1, 2
 QD_ACT_F32, QD_ACT_I8 = 0, 1
 DEVERR = {1: "page", 2: "pos", 4: "nan", 8: "steps", 16: "timeout"}
 
@@ -48,7 +48,8 @@ class StepArgs(C.Structure):
                 ("rope_table", _vp), ("rope_max_pos", _i),
                 ("tok", _vp), ("pos", _vp), ("step", _vp), ("out_tokens", _vp),
                 ("max_steps", _i), ("batch", _i),
-                ("logits", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
+                ("logits", _vp), ("workspace", _vp), ("workspace_bytes", _sz),
+                ("lm_wtype", _i), ("top_k", _i), ("topk_ids", _vp), ("topk_vals", _vp)]
 
 
 _SIGS = {
@@ -57,6 +58,9 @@ _SIGS = {
     "qd_gemv_bf16": (_i, [_vp, _i, _i, _vp, _i, _vp, _i, _vp]),
     "qd_gemv_q8_0": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _i, _vp, _vp]),
     "qd_quantize_q8_0": (_i, [_vp, _i, _vp, _vp, _vp]),
+    "qd_gemv_w4": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp]),
+    "qd_w4_topk_workspace_bytes": (_sz, []),
+    "qd_gemv_w4_topk": (_i, [_vp, _vp, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "qd_gemm_workspace_bytes": (_sz, [_i, _i, _i]),
     "qd_gemm_q8_0": (_i, [_vp, _vp, _i, _i, _vp, _i, _vp, _vp, _sz, _vp]),
     "qd_attn_workspace_bytes": (_sz, [_i, _i, _i, _i]),
@@ -143,6 +147,29 @@ def gemv_q8_0(qs, d, x=None, xq=None, xd=None, act=QD_ACT_F32, y=None, stream=No
         y = torch.empty(R, dtype=torch.float32, device=qs.device)
     _check(lib().qd_gemv_q8_0(_p(qs), _p(d), R, K, _p(x), _p(xq), _p(xd), act, _p(y), _stream(stream)))
     return y
+
+
+def gemv_w4(W, d, x, y=None, stream=None):
+    """y = (d * q) @ x; W packed uint8 [R, K / 2], d f16 [R], x bf16 [K] -> f32 [R]."""
+    R, Kh = W.shape
+    if y is None:
+        y = torch.empty(R, dtype=torch.float32, device=W.device)
+    _check(lib().qd_gemv_w4(_p(W), _p(d), R, 2 * Kh, _p(x), _p(y), _stream(stream)))
+    return y
+
+
+def gemv_w4_topk(W, d, x, k, y=None, workspace=None, stream=None):
+    """(logits, top-k ids, top-k values) of the INT4 LM-head form."""
+    R, Kh = W.shape
+    if y is None:
+        y = torch.empty(R, dtype=torch.float32, device=W.device)
+    if workspace is None:
+        workspace = torch.zeros(int(lib().qd_w4_topk_workspace_bytes()), dtype=torch.uint8, device=W.device)
+    ids = torch.empty(k, dtype=torch.int32, device=W.device)
+    vals = torch.empty(k, dtype=torch.float32, device=W.device)
+    _check(lib().qd_gemv_w4_topk(_p(W), _p(d), R, 2 * Kh, _p(x), k, _p(y), _p(ids), _p(vals), _p(workspace),
+                                 workspace.numel(), _stream(stream)))
+    return y, ids, vals
 
 
 def gemm_workspace_bytes(rows, cols, wtype=QD_W_Q8_0):
@@ -252,13 +279,13 @@ class Decoder:
     """
 
     def __init__(self, model, max_steps: int, act: int = QD_ACT_F32, lm_act: int | None = None,
-                 device="cuda", verify_k: int = 0):
+                 device="cuda", verify_k: int = 0, top_k: int = 0):
         self.m = model
         s = model.shape
         self.device = torch.device(device)
-        q8 = model.wtype == "q8_0"
+        wt = {"bf16": QD_W_BF16, "q8_0": QD_W_Q8_0, "int4": QD_W_INT4}[model.wtype]
         dims = LayerDims(s.hidden, s.n_q_heads, s.n_kv_heads, s.head_dim, s.ffn, s.rms_eps, s.rope_theta,
-                         QD_W_Q8_0 if q8 else QD_W_BF16, act)
+                         wt, act)
         self._handles = []
         for lt in model.layers:
             w = LayerWeights(_p(lt.w_qkv), _p(lt.w_o), _p(lt.w_gu), _p(lt.w_down),
@@ -303,6 +330,12 @@ class Decoder:
         a.max_steps = max_steps
         a.batch = B
         a.logits = _p(self.logits)
+        a.lm_wtype = QD_W_INT4 if model.lm_head.dtype == torch.uint8 else QD_W_BF16
+        a.top_k = top_k
+        if top_k:
+            self.topk_ids = torch.full((top_k,), -1, dtype=torch.int32, device=self.device)
+            self.topk_vals = torch.zeros(top_k, dtype=torch.float32, device=self.device)
+            a.topk_ids, a.topk_vals = _p(self.topk_ids), _p(self.topk_vals)
         self.args = a
         nbytes = int(lib().qd_step_workspace_bytes(C.byref(a)))
         if verify_k:  # room for speculative verify passes of up to verify_k tokens

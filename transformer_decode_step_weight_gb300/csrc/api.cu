@@ -234,6 +234,38 @@ int qd_gemv_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const 
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_q8_0");
 }
 
+int qd_gemv_w4(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, float* y,
+               cudaStream_t stream) {
+  if (!W || !d_f16 || !x_bf16 || !y) return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4: null pointer");
+  if (rows < 1 || !gemv_w4_supported(cols))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4: rows=%d cols=%d (cols %% 32 == 0, <= 16384)", rows, cols);
+  if (!aligned16(W) || !aligned16(x_bf16) || !aligned16(y) || ((uintptr_t)d_f16 & 1u))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4: alignment");
+  GemvW4Args g = {};
+  g.W = W; g.d = d_f16; g.R = rows; g.K = cols; g.pro = PRO_X_BF16; g.x = x_bf16; g.epi = EPI_STORE; g.y = y;
+  cudaError_t e = launch_gemv_w4(g, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_w4");
+}
+
+size_t qd_w4_topk_workspace_bytes(void) { return w4_topk_workspace_bytes(); }
+
+int qd_gemv_w4_topk(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, int k, float* y,
+                    int32_t* topk_ids, float* topk_vals, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream) {
+  if (!W || !d_f16 || !x_bf16 || !y || !topk_ids || !topk_vals || !workspace)
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4_topk: null pointer");
+  if (rows < 1 || !gemv_w4_supported(cols) || k < 1 || k > 16)
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4_topk: rows=%d cols=%d k=%d", rows, cols, k);
+  if (!aligned16(W) || !aligned16(x_bf16) || !aligned16(y) || !aligned16(workspace) || ((uintptr_t)d_f16 & 1u))
+    return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4_topk: alignment");
+  if (workspace_bytes < w4_topk_workspace_bytes()) return fail(QD_ERR_WORKSPACE, "qd_gemv_w4_topk: workspace");
+  GemvW4Args g = {};
+  g.W = W; g.d = d_f16; g.R = rows; g.K = cols; g.pro = PRO_X_BF16; g.x = x_bf16; g.epi = EPI_TOPK; g.y = y;
+  g.top_k = k; g.ws = workspace; g.topk_ids = topk_ids; g.topk_vals = topk_vals;
+  cudaError_t e = launch_gemv_w4(g, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_w4_topk");
+}
+
 size_t qd_gemm_workspace_bytes(int rows, int cols, qd_wtype wtype) {
   if (rows < 1 || cols < 1) return 0;
   return gemm_tc_workspace_bytes(rows, cols, wtype == QD_W_Q8_0);
@@ -385,6 +417,11 @@ int qd_create_layer(const qd_layer_dims* d, const qd_layer_weights* w, qd_layer*
     if (d->hidden % 8 || d->ffn % 8 || !gemv_bf16_supported(d->hidden, 1) || !gemv_bf16_supported(d->ffn, 1) ||
         !gemv_bf16_supported(qdim, 1))
       return fail(QD_ERR_UNSUPPORTED, "qd_create_layer: bf16 dims not supported");
+  } else if (d->wtype == QD_W_INT4) {
+    if (!gemv_w4_supported(d->hidden) || !gemv_w4_supported(d->ffn) || !gemv_w4_supported(qdim))
+      return fail(QD_ERR_UNSUPPORTED, "qd_create_layer: INT4 dims need multiples of 32 up to 16384");
+    if (!w->s_qkv || !w->s_o || !w->s_gu || !w->s_down)
+      return fail(QD_ERR_INVALID_ARG, "qd_create_layer: INT4 scales missing");
   } else if (d->wtype == QD_W_Q8_0) {
     if (d->hidden % 32 || d->ffn % 32 || !gemv_q8_supported(d->hidden) || !gemv_q8_supported(d->ffn) ||
         !gemv_q8_supported(qdim))
@@ -425,8 +462,13 @@ struct StepWs {
   void* gemm_ws;    // batched path: split-K partials and tickets (one GEMM at a time)
   size_t gemm_ws_bytes;
   void* stream_ws;  // batch-1 BF16: the persistent step kernel's partials, counters, candidates
+  void* topk_ws;    // INT4 LM head: top-k candidates and ticket
   size_t total;
 };
+
+// The LM head's format: INT4 (lm_wtype), else Q8_0 when scales are given, else bf16.
+bool lm_is_w4(const qd_step_args* a) { return a->lm_wtype == QD_W_INT4; }
+bool lm_is_q8(const qd_step_args* a) { return a->lm_head_scales != nullptr && !lm_is_w4(a); }
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -458,7 +500,7 @@ StepWs step_ws_layout_for(const qd_step_args* a, void* base, bool gemm_path) {
   w.gemm_ws = (void*)(p + off);
   w.gemm_ws_bytes = 0;
   if (gemm_path) {  // the batched step runs its projections as split-K tcgen05 GEMMs
-    const bool q8 = d.wtype == QD_W_Q8_0, q8_head = a->lm_head_scales != nullptr;
+    const bool q8 = d.wtype == QD_W_Q8_0, q8_head = lm_is_q8(a);
     const int shapes[5][3] = {{(int)qkv, d.hidden, q8}, {d.hidden, d.n_q_heads * d.head_dim, q8},
                               {2 * d.ffn, d.hidden, q8}, {d.hidden, d.ffn, q8}, {a->vocab, d.hidden, q8_head}};
     for (const auto& sh : shapes)
@@ -467,6 +509,8 @@ StepWs step_ws_layout_for(const qd_step_args* a, void* base, bool gemm_path) {
   off += al256(w.gemm_ws_bytes);
   w.stream_ws = (void*)(p + off);
   if (a->batch == 1 && d.wtype == QD_W_BF16) off += al256(stream_ws_bytes(a->n_layers, d.n_q_heads, d.n_kv_heads));
+  w.topk_ws = (void*)(p + off);
+  if (lm_is_w4(a)) off += al256(w4_topk_workspace_bytes());
   w.total = off;
   return w;
 }
@@ -545,7 +589,16 @@ int validate_step(const qd_step_args* a) {
                             a->max_pages, a->n_pages);
   if (rc) return rc;
   if (a->rope_max_pos < 1) return fail(QD_ERR_INVALID_ARG, "qd_decode_step: rope_max_pos");
-  const bool q8_head = a->lm_head_scales != nullptr;
+  if (d0.wtype == QD_W_INT4 && a->batch != 1)
+    return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: INT4 layers run at batch 1");
+  if (lm_is_w4(a)) {
+    if (a->batch != 1) return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: an INT4 LM head runs at batch 1");
+    if (!a->lm_head_scales || ((uintptr_t)a->lm_head_scales & 1u) || !gemv_w4_supported(d0.hidden))
+      return fail(QD_ERR_INVALID_ARG, "qd_decode_step: INT4 LM head needs per-row scales and hidden %% 32 == 0");
+    if (a->top_k < 0 || a->top_k > 16 || (a->top_k > 0 && (!a->topk_ids || !a->topk_vals)))
+      return fail(QD_ERR_INVALID_ARG, "qd_decode_step: top_k=%d (0..16, with topk_ids and topk_vals)", a->top_k);
+  }
+  const bool q8_head = lm_is_q8(a);
   if (q8_head) {
     if (!gemv_q8_supported(d0.hidden)) return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 head dims");
     if (a->batch > 1 && !tc_step(a))
@@ -618,8 +671,80 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   return QD_OK;
 }
 
+// The INT4 LM head of a batch-1 step: the GEMV, its top-k and the argmax advance in
+// one launch.
+cudaError_t launch_lm_head_w4(const qd_step_args* a, const StepWs& w, const Launch& L) {
+  GemvW4Args g = {};
+  g.W = a->lm_head; g.d = a->lm_head_scales; g.R = a->vocab; g.K = a->layers[0]->dims.hidden;
+  g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = a->final_norm; g.eps = a->layers[0]->dims.rms_eps;
+  g.epi = EPI_TOPK; g.y = a->logits; g.w_evict_first = step_tuning().w_evict_first;
+  g.top_k = a->top_k > 0 ? a->top_k : 1; g.ws = w.topk_ws;
+  g.tok = a->tok; g.pos = a->pos; g.step = a->step; g.out_tokens = a->out_tokens; g.max_steps = a->max_steps;
+  g.topk_ids = a->top_k > 0 ? a->topk_ids : nullptr; g.topk_vals = a->top_k > 0 ? a->topk_vals : nullptr;
+  return launch_gemv_w4(g, L);
+}
+
+// Batch-1 step of INT4 (W4A16) layers: the BF16 step's order with the W4A16 GEMVs
+// (bf16 activations: the same rounding points as the BF16 model).
+int run_step_w4(const qd_step_args* a, cudaStream_t stream) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const StepWs w = step_ws_layout(a, a->workspace);
+  const Launch L = make_launch(stream, true);
+  const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int QKV = (Hq + 2 * Hkv) * D;
+  const int wef = step_tuning().w_evict_first;
+  auto gemv = [&](const void* W, const void* S, int R, int K, int pro, const void* x, const void* nw, int epi,
+                  float* y, void* y_bf16) {
+    GemvW4Args g = {};
+    g.W = W; g.d = S; g.R = R; g.K = K; g.pro = pro; g.x = x; g.norm_w = nw; g.eps = d.rms_eps; g.epi = epi;
+    g.y = y; g.y_bf16 = y_bf16; g.w_evict_first = wef;
+    return launch_gemv_w4(g, L);
+  };
+  QD_TRY(launch_embed(a->embed, H, a->vocab, a->tok, 1, w.res, L), "embed");
+  for (int li = 0; li < a->n_layers; ++li) {
+    const qd_layer* l = a->layers[li];
+    QD_TRY(gemv(l->w.w_qkv, l->w.s_qkv, QKV, H, PRO_RMSNORM, w.res, l->w.ln_in, EPI_STORE, w.qkv, nullptr),
+           "qkv gemv w4");
+    AttnArgs at = {};
+    at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
+    at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps; at.act_bf16 = 1;
+    at.pos = a->pos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = a->page_table;
+    at.B = 1; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
+    at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D); at.out_bf16 = w.attn;
+    at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size;
+    QD_TRY(launch_attention(at, L), "attention");
+    QD_TRY(gemv(l->w.w_o, l->w.s_o, H, Hq * D, PRO_X_BF16, w.attn, nullptr, EPI_RESID_ADD, w.res, nullptr),
+           "o gemv w4");
+    QD_TRY(gemv(l->w.w_gu, l->w.s_gu, 2 * F, H, PRO_RMSNORM, w.res, l->w.ln_post, EPI_SWIGLU, nullptr, w.xn),
+           "gu gemv w4");
+    QD_TRY(gemv(l->w.w_down, l->w.s_down, H, F, PRO_X_BF16, w.xn, nullptr, EPI_RESID_ADD, w.res, nullptr),
+           "down gemv w4");
+  }
+  if (lm_is_w4(a)) {
+    QD_TRY(launch_lm_head_w4(a, w, L), "lm head w4");
+    return QD_OK;
+  }
+  if (lm_is_q8(a)) {
+    GemvQ8Args g = {};
+    g.qs = (const int8_t*)a->lm_head; g.d = a->lm_head_scales; g.R = a->vocab; g.K = H; g.act = a->lm_act;
+    g.pro = PRO_RMSNORM; g.x = w.res; g.norm_w = a->final_norm; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = a->logits;
+    g.claim = w.claims + 2 * 5 * a->n_layers;
+    QD_TRY(launch_gemv_q8(g, L), "lm head q8");
+  } else {
+    GemvBf16Args g = {};
+    g.W = a->lm_head; g.R = a->vocab; g.K = H; g.batch = 1; g.pro = PRO_RMSNORM; g.x = w.res;
+    g.norm_w = a->final_norm; g.eps = d.rms_eps; g.epi = EPI_STORE; g.y = a->logits;
+    QD_TRY(launch_gemv_bf16(g, L), "lm head");
+  }
+  QD_TRY(launch_argmax_advance(a->logits, a->vocab, 1, a->tok, a->pos, a->step, a->out_tokens, a->max_steps,
+                               w.argmax_ws, L),
+         "argmax");
+  return QD_OK;
+}
+
 int run_step(const qd_step_args* a, cudaStream_t stream) {
   if (tc_step(a)) return run_step_tc(a, stream);
+  if (a->layers[0]->dims.wtype == QD_W_INT4) return run_step_w4(a, stream);
   const qd_layer_dims& d = a->layers[0]->dims;
   const StepWs w = step_ws_layout(a, a->workspace);
   if (!step_kernels_forced()) {
@@ -747,10 +872,15 @@ int run_step(const qd_step_args* a, cudaStream_t stream) {
       if (swiglu_epi) { g.pro = PRO_X_BF16; g.x = w.xn; }
       if (li + 1 < a->n_layers) g.pf = tail_plan(a->layers[li + 1]->w.w_qkv, QKV, H);
       else if (!a->lm_head_scales) g.pf = tail_plan(a->lm_head, a->vocab, H);
+      if (li + 1 == a->n_layers && lm_is_w4(a)) g.pf = L2Prefetch{};
       QD_TRY(launch_gemv_bf16(g, L), "down gemv");
     }
   }
   // final RMSNorm + LM head
+  if (lm_is_w4(a)) {
+    QD_TRY(launch_lm_head_w4(a, w, L), "lm head w4");
+    return QD_OK;
+  }
   if (a->lm_head_scales) {
     GemvQ8Args g = {};
     g.w_evict_first = pft.w_evict_first;
@@ -811,6 +941,8 @@ int validate_verify(const qd_step_args* a, const int32_t* draft, int k, const fl
   int rc = validate_step(a);
   if (rc) return rc;
   const qd_layer_dims& d = a->layers[0]->dims;
+  if (d.wtype == QD_W_INT4 || lm_is_w4(a))
+    return fail(QD_ERR_UNSUPPORTED, "qd_verify_step: INT4 weights run the batch-1 GEMV path only");
   const bool q8 = d.wtype == QD_W_Q8_0;
   const int ks[3] = {d.hidden, d.n_q_heads * d.head_dim, d.ffn};
   for (int K : ks)
@@ -903,6 +1035,7 @@ size_t qd_step_workspace_bytes(const qd_step_args* a) {
 int qd_step_launch_count(const qd_step_args* a) {
   if (!a || a->n_layers < 1 || !a->layers || !a->layers[0]) return 0;
   if (tc_step(a)) return 1 + 8 * a->n_layers + 3;
+  if (a->layers[0]->dims.wtype == QD_W_INT4 || lm_is_w4(a)) return 1 + 5 * a->n_layers + (lm_is_w4(a) ? 1 : 2);
   if (!step_kernels_forced()) {
     std::vector<StreamLayerPtrs> lp;
     StreamStepArgs sa;

@@ -44,7 +44,9 @@ enum GemvPro { PRO_X_BF16 = 0, PRO_X_F32 = 1, PRO_RMSNORM = 2, PRO_SWIGLU = 3 };
 // EPI_SWIGLU (batch-1 ring form only): W holds [gate (F rows); up (F rows)] and the
 // output is h = bf16(silu(gate . x) * (up . x)) [F] in y_bf16. Each CTA takes the
 // same pair range of both halves, so gate_j and up_j meet in one CTA.
-enum GemvEpi { EPI_STORE = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2 };
+// EPI_TOPK (INT4 LM head): y = logits; the launch's top-k tokens and, when tok is set,
+// the argmax advance of the step (see GemvW4Args).
+enum GemvEpi { EPI_STORE = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2, EPI_TOPK = 3 };
 
 struct GemvBf16Args {
   const void* W;          // bf16 [R, K]
@@ -68,6 +70,39 @@ bool gemv_bf16_supported(int K, int batch);
 bool gemv_bf16_ring_ok(int K, int batch);
 bool gemv_bf16_swiglu_ok(int K);
 cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L);
+
+// ----------------------------------------------------------------- GEMV W4A16 (INT4 weights)
+// W: packed rows [R, K / 2] (two offset-binary nibbles q + 8 per byte, even column
+// low), d: fp16 [R] per-row scales; y[r] = f32(d[r]) * sum_c q[r, c] x[c] with bf16
+// activations x. Prologues and epilogues as the BF16 GEMV (batch 1). EPI_SWIGLU:
+// y_bf16 [R / 2] = bf16(silu(gate) * up). EPI_TOPK: y [R] = logits, topk_ids / vals
+// [top_k] (value descending, lower row first, NaN never chosen; -1 past the non-NaN
+// rows) and, when tok is set, tok = the first of them, out_tokens[step] = tok,
+// pos += 1, step += 1 (all-NaN logits: token 0 and QD_DEVERR_NAN). ws: zero-filled
+// scratch of w4_topk_workspace_bytes() bytes, left zero-filled.
+struct GemvW4Args {
+  const void* W;
+  const void* d;
+  int R, K;
+  int pro;
+  const void* x;
+  const void* norm_w;
+  float eps;
+  int epi;
+  float* y;
+  void* y_bf16;
+  int w_evict_first;
+  L2Prefetch pf;
+  int top_k;
+  void* ws;
+  int32_t *tok, *pos, *step, *out_tokens;
+  int max_steps;
+  int32_t* topk_ids;
+  float* topk_vals;
+};
+bool gemv_w4_supported(int K);
+size_t w4_topk_workspace_bytes();
+cudaError_t launch_gemv_w4(const GemvW4Args& a, const Launch& L);
 
 // ----------------------------------------------------------------- batched GEMM (tcgen05)
 struct GemmTcArgs {

@@ -19,6 +19,8 @@ Storage layouts:
     v (Hkv*D)], w_gu rows = [gate (F); up (F)].
   * Q8_0 weights: int8 values [rows, cols] and fp16 scales [rows, cols/32],
     two separate row-major arrays.
+  * INT4 weights: packed uint8 [rows, cols/2] (two offset-binary nibbles q + 8 per
+    byte, the even column in the low nibble) and fp16 per-row scales [rows].
   * KV cache: bf16 [pages, Hkv, page_size, D]; a contiguous cache is one page of
     ``max_ctx`` tokens per sequence.
 """
@@ -58,6 +60,8 @@ SMALL = Shape("small", 512, 8, 2, 128, 1376, 3, 5003, False)
 SMALL64 = Shape("small64", 512, 8, 2, 128, 1408, 2, 2999, False)
 # dims that are multiples of 256, as the batched Q8_0 projections need
 SMALL256 = Shape("small256", 512, 4, 2, 128, 1536, 2, 3001, False)
+# an INT4 parity shape: several CTA row spans, K per row a few 32-column chunks
+SMALL_W4 = Shape("small_w4", 768, 4, 2, 128, 2080, 3, 4099, False)
 
 
 @dataclass
@@ -89,6 +93,10 @@ WORKLOADS = {
     "qwen3-8b-bf16": Workload(
         "qwen3-8b-bf16", QWEN3_8B, "bf16", ctx=4096, steps=128,
         description="Qwen3-8B-shaped BF16 model, batch 1, KV at context 4096, 128 greedy steps"),
+    "qwen3-8b-int4": Workload(
+        "qwen3-8b-int4", QWEN3_8B, "int4", ctx=4096, steps=128,
+        description="Qwen3-8B-shaped W4A16 model (INT4 per-row-scaled weights, LM head INT4 too), batch 1, "
+                    "context 4096"),
     "qwen3-8b-q8_0": Workload(
         "qwen3-8b-q8_0", QWEN3_8B, "q8_0", ctx=2048, steps=128,
         description="Qwen3-8B-shaped Q8_0 model (LM head Q8_0 too), batch 1, context 2048"),
@@ -108,6 +116,15 @@ def _normal_bf16(gen, shape, std, device, mean=0.0):
     if mean != 0.0:
         t.add_(mean)
     return t.to(torch.bfloat16)
+
+
+def _int4(gen, rows, cols, device):
+    """INT4 weights: codes uniform in [-8, 7] packed two per byte as offset-binary
+    nibbles (even column low), fp16 per-row scales |N(0, 0.01)|."""
+    q = torch.randint(0, 16, (rows, cols), generator=gen, device=device, dtype=torch.int16)
+    packed = (q[:, 0::2] | (q[:, 1::2] << 4)).to(torch.uint8)
+    d = torch.randn((rows,), generator=gen, device=device, dtype=torch.float32).abs_().mul_(0.01).to(torch.float16)
+    return packed, d
 
 
 def _q8_0(gen, rows, cols, device):
@@ -143,6 +160,8 @@ def make_layer(gen, s: Shape, wtype: str, device) -> LayerTensors:
             out[k] = _normal_bf16(gen, (r, c), 0.02, device)
         elif wtype == "q8_0":
             out[k], out["s" + k[1:]] = _q8_0(gen, r, c, device)
+        elif wtype == "int4":
+            out[k], out["s" + k[1:]] = _int4(gen, r, c, device)
         else:
             raise ValueError(wtype)
     out["ln_in"] = _normal_bf16(gen, (s.hidden,), 0.1, device, mean=1.0)
@@ -192,6 +211,8 @@ def make_model(s: Shape, wtype: str, seed: int, device, *, n_layers: int | None 
     lm_scales = None
     if lm_wtype == "q8_0":
         lm_head, lm_scales = _q8_0(gen, s.vocab, s.hidden, device)
+    elif lm_wtype == "int4":
+        lm_head, lm_scales = _int4(gen, s.vocab, s.hidden, device)
     elif s.tied:
         lm_head = embed
     else:
@@ -250,3 +271,7 @@ def bits_u16(t: torch.Tensor) -> np.ndarray:
 
 def host_i8(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().numpy().astype(np.int8)
+
+
+def host_u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().numpy().astype(np.uint8)
