@@ -50,8 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--no-probe", action="store_true", help="skip the dominant-kernel event probe")
-    ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "attention", "attention_batched",
-                                         "gemm_tc", "gemm_q8"],
+    ap.add_argument("--kernel", choices=["gemv_bf16", "gemv_q8_f32", "gemv_q8_i8", "gemv_w4", "gemv_w4_topk",
+                                         "attention", "attention_batched", "gemm_tc", "gemm_q8"],
                     help="time one kernel alone on a full-size shape (profiling aid) instead of the step")
     ap.add_argument("--rows", type=int, default=24576)
     ap.add_argument("--cols", type=int, default=4096)
@@ -203,7 +203,8 @@ def peaks():
 def traffic_record(kernel_src: str):
     """DRAM traffic per launch of the dominant kernel from the committed ncu summary,
     valid only while the kernel source is unchanged since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "gemv_bf16_traffic.json")
+    stem = os.path.splitext(os.path.basename(kernel_src))[0]
+    path = os.path.join(ROOT, "profiles", f"{stem}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -358,8 +359,9 @@ def run_ours(args, dist, rank, world, local):
     read_peak = measure_read_peak(dev, stream)
 
     # ---- dominant kernel: the BF16 GEMV, every launch of one token, events on its stream
-    roof = None if (args.no_probe or wl.batch > 8 or wl.wtype != "bf16") else dominant_kernel_roofline(api, mt, s, stream, hbm_peak,
-                                                                                 peak_kind)
+    roof = None
+    if not args.no_probe and wl.batch == 1 and wl.wtype in ("bf16", "int4"):
+        roof = dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind)
 
     # ---- end to end through the public API: per step H2D of the input token/position
     # from pinned memory, the step, D2H of the next token, host reads it
@@ -440,37 +442,54 @@ def measure_read_peak(dev, stream, gib=4, reps=5):
 
 
 def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
-    """Average duration of gemv_bf16 launches over one token's projections (36 x QKV,
-    O, gate+up at K = hidden, and the LM head), timed with CUDA events on the stream
-    they run on, three passes; algorithmic bytes = the weight bytes each launch reads."""
+    """Average duration of the weight GEMV's launches over one token's projections
+    (36 x QKV, O, gate+up at K = hidden, and the LM head), timed with CUDA events on the
+    stream they run on, three passes; algorithmic bytes = the weight bytes (and, for
+    INT4, the per-row scales) each launch reads."""
     x = torch.randn((1, max(s.hidden, s.n_q_heads * s.head_dim)), device=mt.embed.device).to(torch.bfloat16)
     xo = x[:, : s.n_q_heads * s.head_dim].contiguous()
     xh = x[:, : s.hidden].contiguous()
+    w4 = mt.wtype == "int4"
     mats = []
     for lt in mt.layers:
-        mats += [(lt.w_qkv, xh), (lt.w_o, xo), (lt.w_gu, xh)]
-    mats.append((mt.lm_head, xh))
-    ys = {id(w): torch.empty((1, w.shape[0]), dtype=torch.float32, device=x.device) for w, _ in mats}
+        if w4:
+            mats += [(lt.w_qkv, lt.s_qkv, xh[0]), (lt.w_o, lt.s_o, xo[0]), (lt.w_gu, lt.s_gu, xh[0])]
+        else:
+            mats += [(lt.w_qkv, None, xh), (lt.w_o, None, xo), (lt.w_gu, None, xh)]
+    mats.append((mt.lm_head, mt.lm_head_scales, xh[0] if w4 else xh))
+    ys = {id(w): torch.empty((1, w.shape[0]), dtype=torch.float32, device=x.device) for w, _, _ in mats}
+
+    def run(w, sc, xx):
+        if w4:
+            api.gemv_w4(w, sc, xx, ys[id(w)][0], stream=stream)
+        else:
+            api.gemv_bf16(w, xx, ys[id(w)], stream=stream)
+
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for w, xx in mats:   # warm
-            api.gemv_bf16(w, xx, ys[id(w)], stream=stream)
+        for m in mats:   # warm
+            run(*m)
         e0.record(stream)
         for _ in range(3):
-            for w, xx in mats:
-                api.gemv_bf16(w, xx, ys[id(w)], stream=stream)
+            for m in mats:
+                run(*m)
         e1.record(stream)
     stream.synchronize()
     ms = e0.elapsed_time(e1)
     n = 3 * len(mats)
-    bytes_per_launch = sum(w.numel() * 2 for w, _ in mats) / len(mats)
+    if w4:
+        bytes_per_launch = sum(w.numel() + 2 * w.shape[0] for w, _, _ in mats) / len(mats)
+    else:
+        bytes_per_launch = sum(w.numel() * 2 for w, _, _ in mats) / len(mats)
     avg_s = ms / 1e3 / n
     achieved = bytes_per_launch / avg_s / 1e9
-    rec = traffic_record(os.path.join(ROOT, "transformer_decode_step_weight_gb300", "csrc", "gemv_bf16.cu"))
+    src = "gemv_w4.cu" if w4 else "gemv_bf16.cu"
+    rec = traffic_record(os.path.join(ROOT, "transformer_decode_step_weight_gb300", "csrc", src))
     traffic = None
     if rec is not None:
         traffic = rec.get("traffic_bytes_per_launch")
-    return {"bound": "hbm", "kernel": "gemv_bf16_kernel (K = hidden launches of one token)",
+    kname = "gemv_w4_kernel" if w4 else "gemv_bf16_kernel"
+    return {"bound": "hbm", "kernel": f"{kname} (K = hidden launches of one token)",
             "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
             "peak_kind": peak_kind, "avg_launch_us": round(avg_s * 1e6, 3),
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "traffic": traffic}
@@ -631,6 +650,18 @@ def run_kernel(args):
         lane = api.QD_ACT_I8 if args.kernel.endswith("i8") else api.QD_ACT_F32
         nbytes = R * K + R * (K // 32) * 2
         fn = lambda i: api.gemv_q8_0(qs[i % copies], ds[i % copies], x=x, act=lane, y=y, stream=stream)  # noqa: E731
+    elif args.kernel in ("gemv_w4", "gemv_w4_topk"):
+        Ws = [torch.randint(0, 256, (R, K // 2), generator=g, device=dev, dtype=torch.int16).to(torch.uint8)
+              for _ in range(copies)]
+        ds = [(torch.randn(R, generator=g, device=dev).abs() * 0.01).to(torch.float16) for _ in range(copies)]
+        x = torch.randn(K, generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty(R, device=dev)
+        nbytes = R * K // 2 + R * 2
+        if args.kernel == "gemv_w4":
+            fn = lambda i: api.gemv_w4(Ws[i % copies], ds[i % copies], x, y, stream=stream)  # noqa: E731
+        else:
+            ws = torch.zeros(int(api.lib().qd_w4_topk_workspace_bytes()), dtype=torch.uint8, device=dev)
+            fn = lambda i: api.gemv_w4_topk(Ws[i % copies], ds[i % copies], x, 8, y, ws, stream=stream)  # noqa
     elif args.kernel == "gemm_tc":
         Ws = [(torch.randn((R, K), generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(copies)]
         x = torch.randn((args.batch, K), generator=g, device=dev).to(torch.bfloat16)

@@ -324,10 +324,32 @@ int qd_graph_destroy(qd_graph* g);
 /* draft: int32 [k - 1] device (may be NULL when k == 1). 1 <= k <= 8. The       */
 /* projections' K must be multiples of 64 (bf16) or 256 (Q8_0, whose weights are  */
 /* widened on chip as in qd_gemm_q8_0). workspace: args->workspace of at least    */
-/* qd_verify_workspace_bytes(args, k) bytes, zero-filled before first use.        */
+/* qd_verify_workspace_bytes(args, k) bytes, zero-filled before first use; the   */
+/* pass's scratch follows the first qd_step_workspace_bytes(args) bytes (the      */
+/* decode step's, left untouched), so passes and decode steps may alternate.     */
 size_t qd_verify_workspace_bytes(const qd_step_args* args, int k);
 int qd_verify_step(const qd_step_args* args, const int32_t* draft, int k, float* logits, int32_t* target,
                    int32_t* n_accept, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Prefill ("qwen3-8b-rtx4080-cutedsl" README, "Flash Attention 2" and           */
+/* "Baseline tiled GEMM": the prompt is processed as one batch of rows with      */
+/* tiled attention that never forms the full score matrix). For the one sequence */
+/* of `args` (batch 1): tokens int32 [n_tokens] (device) sit at positions         */
+/* pos[0] .. pos[0] + n_tokens - 1. Every layer runs over all rows at once: the   */
+/* projections are tcgen05 GEMMs over 64-token tiles, the rows' K/V are written   */
+/* to the cache first, and row i attends causally to positions 0 .. pos[0] + i    */
+/* (the keys already cached included). The last row alone goes through the final */
+/* norm and the LM head: logits f32 [vocab] (device, 16-byte aligned). The state  */
+/* then advances as one decode step from the last row: tok = argmax (first index */
+/* among equal maxima), out_tokens[step] = tok, pos += n_tokens, step += 1.      */
+/* Position errors (pos[0] + n_tokens past the cache or the RoPE table) set      */
+/* QD_DEVERR_POS. 1 <= n_tokens <= 32768; BF16 or Q8_0 weights (K multiples of 64 */
+/* or 256 as in qd_verify_step). workspace: args->workspace of at least           */
+/* qd_prefill_workspace_bytes(args, n_tokens) bytes, zero-filled before first use; */
+/* as in qd_verify_step, the decode step's part of it is left untouched.          */
+size_t qd_prefill_workspace_bytes(const qd_step_args* args, int n_tokens);
+int qd_prefill(const qd_step_args* args, const int32_t* tokens, int n_tokens, float* logits, cudaStream_t stream);
 
 /* Reads and clears the sticky device error word (synchronises `stream`).      */
 /* *bits receives a mask of QD_DEVERR_*. Returns QD_OK or QD_ERR_CUDA.           */

@@ -124,6 +124,31 @@ def test_verify_equals_greedy_steps(cuda_lib):
     assert api.check_device_error() == 0
 
 
+def test_verify_then_decode(cuda_lib):
+    # a verify pass leaves the decode step's workspace as it was: greedy steps after it
+    # follow the oracle from the cache the pass wrote
+    k = 4
+    mt = synth.make_model(synth.SMALL64, "bf16", 13, DEV, ctx=50, steps=k + 3)
+    om = oracle_model(mt)
+    dec = api.Decoder(mt, max_steps=k + 3, verify_k=k)
+    pos0 = int(mt.seq_lens[0])
+    draft = [int(t) for t in np.random.default_rng(4).integers(0, mt.shape.vocab, k - 1)]
+    dec.verify(torch.tensor(draft, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    m = int(dec.n_accept[0])
+    hist = ([int(mt.start_tok[0])] + draft)[:m + 1]
+    ks, vs = oracle_caches(mt, 0, pos0 + m + 1 + 2)
+    for i, t in enumerate(hist):
+        oracle.decode_token(om, t, pos0 + i, ks, vs)
+    for i in range(2):
+        t = int(dec.tok[0])
+        dec.step()
+        torch.cuda.synchronize()
+        ref = oracle.decode_token(om, t, pos0 + m + 1 + i, ks, vs)
+        assert rel_max_abs(dec.logits[0].double().cpu().numpy(), ref) < TOL["bf16"], i
+    assert api.check_device_error() == 0
+
+
 def test_verify_qwen3_8b_layer_k8(cuda_lib, parity_log):
     """Full Qwen3-8B shapes: one layer at context 4096 and the 151936-row LM head, k = 8
     rows, each row's residual checked whole and its LM-head rows sampled."""
@@ -136,7 +161,7 @@ def test_verify_qwen3_8b_layer_k8(cuda_lib, parity_log):
     dec.verify(torch.tensor(draft, dtype=torch.int32, device=DEV))
     torch.cuda.synchronize()
     inputs = [int(mt.start_tok[0])] + draft
-    res = dec.workspace[: k * s.hidden * 4].view(torch.float32).view(k, s.hidden).double().cpu().numpy()
+    res = dec.rows_residual(k).double().cpu().numpy()
     ks, vs = oracle_caches(mt, 0, 4096 + k)
     rows = np.arange(0, s.vocab, 211)
     worst = 0.0

@@ -27,13 +27,20 @@ def _w4(R, K, seed):
     return W, d, x
 
 
-@pytest.mark.parametrize("R,K", [(37, 64), (1000, 1024), (333, 2048), (4096, 3072), (6144, 4096), (4096, 12288),
-                                 (151936, 1024)])
+@pytest.mark.parametrize("R,K", [(37, 64), (1000, 1024), (333, 2048), (300, 2080), (4096, 3072), (6144, 4096),
+                                 (4096, 12288), (77, 16384), (151936, 1024)])
 def test_gemv_w4(cuda_lib, R, K):
     W, d, x = _w4(R, K, R + K)
     y = api.gemv_w4(W, d, x)
     ref = oracle.gemv_w4(synth.host_u8(W), synth.bits_u16(d), oracle.bf16_to_f64(synth.bits_u16(x)))
     assert rel_max_abs(y.cpu().numpy(), ref) < GEMV_TOL
+
+
+def test_gemv_w4_rejects_unsupported_k(cuda_lib):
+    for K in (48, 16416):   # not a multiple of 32; above the 16384-column maximum
+        W, d, x = _w4(16, K, 1)
+        with pytest.raises(api.QDError):
+            api.gemv_w4(W, d, x)
 
 
 def test_gemv_w4_unit_scales_integer_exact(cuda_lib):

@@ -66,6 +66,8 @@ def test_host_validation_without_gpu(lib):
     d.n_q_heads = 12
     assert lib.qd_create_layer(C.byref(d), C.byref(w), C.byref(h)) == -1      # Hq % Hkv != 0
     assert lib.qd_decode_step(None, None) == -1
+    assert lib.qd_prefill(None, None, 4, None, None) == -1
+    assert lib.qd_prefill_workspace_bytes(None, 4) == 0
     # the batched Q8_0 GEMM: null pointers, cols not a multiple of 32, and cols that are a
     # multiple of 32 but not of 256 (its scale boxes) are refused before any launch;
     # the non-null pointers below are never dereferenced

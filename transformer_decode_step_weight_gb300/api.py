@@ -80,6 +80,8 @@ _SIGS = {
     "qd_check_device_error": (_i, [_vp, C.POINTER(_i)]),
     "qd_verify_workspace_bytes": (_sz, [C.POINTER(StepArgs), _i]),
     "qd_verify_step": (_i, [C.POINTER(StepArgs), _vp, _i, _vp, _vp, _vp, _vp]),
+    "qd_prefill_workspace_bytes": (_sz, [C.POINTER(StepArgs), _i]),
+    "qd_prefill": (_i, [C.POINTER(StepArgs), _vp, _i, _vp, _vp]),
     "qd_debug_q8_block_dots": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "qd_debug_paged_indices": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
 }
@@ -279,7 +281,7 @@ class Decoder:
     """
 
     def __init__(self, model, max_steps: int, act: int = QD_ACT_F32, lm_act: int | None = None,
-                 device="cuda", verify_k: int = 0, top_k: int = 0):
+                 device="cuda", verify_k: int = 0, top_k: int = 0, prefill_max: int = 0):
         self.m = model
         s = model.shape
         self.device = torch.device(device)
@@ -343,6 +345,9 @@ class Decoder:
             self.verify_logits = torch.empty((verify_k, s.vocab), dtype=torch.float32, device=self.device)
             self.verify_target = torch.zeros(verify_k, dtype=torch.int32, device=self.device)
             self.n_accept = torch.zeros(1, dtype=torch.int32, device=self.device)
+        if prefill_max:  # room for prompts of up to prefill_max tokens
+            nbytes = max(nbytes, int(lib().qd_prefill_workspace_bytes(C.byref(a), prefill_max)))
+            self.prefill_logits = torch.empty(s.vocab, dtype=torch.float32, device=self.device)
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
         a.workspace = _p(self.workspace)
         a.workspace_bytes = nbytes
@@ -357,6 +362,13 @@ class Decoder:
         H = self.m.shape.hidden
         return self.workspace[: self.batch * H * 4].view(torch.float32).view(self.batch, H)
 
+    def rows_residual(self, n: int) -> torch.Tensor:
+        """The f32 residual rows [n, H] of the last verify pass or prefill (their scratch
+        follows the decode step's workspace)."""
+        H = self.m.shape.hidden
+        off = int(lib().qd_step_workspace_bytes(C.byref(self.args)))
+        return self.workspace[off: off + n * H * 4].view(torch.float32).view(n, H)
+
     def step(self, stream=None):
         _check(lib().qd_decode_step(C.byref(self.args), _stream(stream)))
 
@@ -366,6 +378,13 @@ class Decoder:
         k = int(draft.numel()) + 1
         _check(lib().qd_verify_step(C.byref(self.args), _p(draft) if k > 1 else None, k, _p(self.verify_logits),
                                     _p(self.verify_target), _p(self.n_accept), _stream(stream)))
+
+    def prefill(self, tokens, stream=None):
+        """The prompt `tokens` (device int32 [n]) at positions pos .. pos + n - 1 in one
+        pass: writes their K/V, fills prefill_logits with the last row's logits and
+        advances the state (tok = its argmax, pos += n, step += 1)."""
+        _check(lib().qd_prefill(C.byref(self.args), _p(tokens), int(tokens.numel()), _p(self.prefill_logits),
+                                _stream(stream)))
 
     def capture(self, steps_per_launch: int, stream=None):
         if self._graph is not None:

@@ -913,18 +913,21 @@ struct VerifyWs {
   size_t total;
 };
 
+// The verify and prefill scratch follows the decode step's own workspace, so the
+// step's counters (zero between launches) are never overwritten by a pass.
 VerifyWs verify_ws_layout(const qd_step_args* a, int k, void* base) {
   qd_step_args ak = *a;
   ak.batch = k;
   VerifyWs v;
-  v.w = step_ws_layout_for(&ak, base, true);
-  unsigned char* p = (unsigned char*)base;
+  const size_t step_bytes = step_ws_layout(a, nullptr).total;
+  unsigned char* p = (unsigned char*)base + step_bytes;
+  v.w = step_ws_layout_for(&ak, p, true);
   size_t off = v.w.total;
   v.tokens = (int32_t*)(p + off); off += al256((size_t)k * 4);
   v.vpos = (int32_t*)(p + off); off += al256((size_t)k * 4);
   v.vpt = (int32_t*)(p + off); off += al256((size_t)k * a->max_pages * 4);
   v.scratch = (int32_t*)(p + off); off += al256((size_t)3 * k * 4);
-  v.total = off;
+  v.total = step_bytes + off;
   return v;
 }
 
@@ -987,7 +990,8 @@ int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits
     QD_TRY(gemm(l->w.w_qkv, q8 ? l->w.s_qkv : nullptr, QKV, H, w.xn, EPI_STORE, w.qkv), "qkv gemm");
     // all k rows' K/V go to the cache first, so row i attends to rows pos .. pos + i
     QD_TRY(launch_kv_write(w.qkv, k, Hq, Hkv, l->w.k_norm, a->rope_table, a->rope_max_pos, d.rms_eps, 1, v.vpos,
-                           v.vpt, a->page_size, a->max_pages, a->n_pages, a->k_cache[li], a->v_cache[li], L),
+                           v.vpt, a->max_pages, a->page_size, a->max_pages, a->n_pages, a->k_cache[li],
+                           a->v_cache[li], L),
            "kv write");
     AttnArgs at = {};
     at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
@@ -1013,6 +1017,115 @@ int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits
   return QD_OK;
 }
 
+// ---- prefill: the prompt's n tokens of one sequence through every layer at once
+struct PrefillWs {
+  float* res;        // [n, H]
+  float* qkv;        // [n, QKV]
+  void* attn;        // bf16 [n, Hq D]
+  float* gu;         // [n, 2F]
+  void* xn;          // bf16 [n, max(H, F)]
+  int32_t* vpos;     // [n] positions of the rows
+  void* argmax_ws;
+  size_t total;
+};
+
+constexpr int kMaxPrefill = 32768;
+
+PrefillWs prefill_ws_layout(const qd_step_args* a, int n, void* base) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const size_t qkv = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const size_t step_bytes = step_ws_layout(a, nullptr).total;
+  unsigned char* p = (unsigned char*)base + step_bytes;
+  PrefillWs w;
+  size_t off = 0;
+  w.res = (float*)(p + off); off += al256((size_t)n * d.hidden * 4);
+  w.qkv = (float*)(p + off); off += al256((size_t)n * qkv * 4);
+  w.attn = (void*)(p + off); off += al256((size_t)n * d.n_q_heads * d.head_dim * 2);
+  w.gu = (float*)(p + off); off += al256((size_t)n * 2 * d.ffn * 4);
+  w.xn = (void*)(p + off); off += al256((size_t)n * std::max(d.hidden, d.ffn) * 2);
+  w.vpos = (int32_t*)(p + off); off += al256((size_t)n * 4);
+  w.argmax_ws = (void*)(p + off); off += al256(argmax_workspace_bytes(1));
+  w.total = step_bytes + off;
+  return w;
+}
+
+int validate_prefill(const qd_step_args* a, const int32_t* tokens, int n, const float* logits) {
+  if (!a) return fail(QD_ERR_INVALID_ARG, "qd_prefill: null args");
+  if (a->batch != 1) return fail(QD_ERR_UNSUPPORTED, "qd_prefill: one sequence (batch 1)");
+  if (n < 1 || n > kMaxPrefill) return fail(QD_ERR_INVALID_ARG, "qd_prefill: n_tokens=%d (1..%d)", n, kMaxPrefill);
+  if (!tokens || !logits) return fail(QD_ERR_INVALID_ARG, "qd_prefill: null pointer");
+  if (!aligned16(logits)) return fail(QD_ERR_INVALID_ARG, "qd_prefill: logits must be 16-byte aligned");
+  int rc = validate_step(a);
+  if (rc) return rc;
+  const qd_layer_dims& d = a->layers[0]->dims;
+  if (d.wtype == QD_W_INT4 || lm_is_w4(a))
+    return fail(QD_ERR_UNSUPPORTED, "qd_prefill: INT4 weights run the batch-1 GEMV path only");
+  const bool q8 = d.wtype == QD_W_Q8_0;
+  const int ks[3] = {d.hidden, d.n_q_heads * d.head_dim, d.ffn};
+  for (int K : ks)
+    if (!gemm_tc_rows_supported(1, K, n, q8) || (n <= 64 && !(q8 ? gemm_tc_q8_supported(1, K, n)
+                                                                 : gemm_tc_supported(1, K, n))))
+      return fail(QD_ERR_UNSUPPORTED, "qd_prefill: projection K=%d needs a multiple of %d", K, q8 ? 256 : 64);
+  if (a->lm_head_scales && !gemm_tc_q8_supported(a->vocab, d.hidden, 1))
+    return fail(QD_ERR_UNSUPPORTED, "qd_prefill: Q8_0 LM head needs hidden %% 256 == 0");
+  if (q8)
+    for (int i = 0; i < a->n_layers; ++i) {
+      const qd_layer_weights& lw = a->layers[i]->w;
+      if (!aligned16(lw.s_qkv) || !aligned16(lw.s_o) || !aligned16(lw.s_gu) || !aligned16(lw.s_down))
+        return fail(QD_ERR_INVALID_ARG, "qd_prefill: Q8_0 scales must be 16-byte aligned");
+    }
+  const PrefillWs w = prefill_ws_layout(a, n, a->workspace);
+  if (a->workspace_bytes < w.total)
+    return fail(QD_ERR_WORKSPACE, "qd_prefill: workspace %zu < %zu bytes", a->workspace_bytes, w.total);
+  return QD_OK;
+}
+
+int run_prefill(const qd_step_args* a, const int32_t* tokens, int n, float* logits, cudaStream_t stream) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const bool q8 = d.wtype == QD_W_Q8_0;
+  const PrefillWs w = prefill_ws_layout(a, n, a->workspace);
+  const Launch L = make_launch(stream, true);
+  const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int QKV = (Hq + 2 * Hkv) * D;
+  auto gemm = [&](const void* W, const void* S, int R, int K, const void* X, int B, int epi, float* y) {
+    GemmTcArgs g = {};
+    g.W = W; g.S = S; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
+    return launch_gemm_tc(g, L);
+  };
+  QD_TRY(launch_prefill_prep(a->pos, n, w.vpos, L), "prefill prep");
+  QD_TRY(launch_embed(a->embed, H, a->vocab, tokens, n, w.res, L), "embed");
+  for (int li = 0; li < a->n_layers; ++li) {
+    const qd_layer* l = a->layers[li];
+    QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_in, n, H, d.rms_eps, w.xn, L), "rmsnorm");
+    QD_TRY(gemm(l->w.w_qkv, q8 ? l->w.s_qkv : nullptr, QKV, H, w.xn, n, EPI_STORE, w.qkv), "qkv gemm");
+    // every row's K/V reaches the cache before the attention reads keys up to its own position
+    QD_TRY(launch_kv_write(w.qkv, n, Hq, Hkv, l->w.k_norm, a->rope_table, a->rope_max_pos, d.rms_eps, 1, w.vpos,
+                           a->page_table, 0, a->page_size, a->max_pages, a->n_pages, a->k_cache[li],
+                           a->v_cache[li], L),
+           "kv write");
+    PrefillAttnArgs at = {};
+    at.qkv = w.qkv; at.n = n; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.q_norm = l->w.q_norm;
+    at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps; at.act_bf16 = 1;
+    at.pos = a->pos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = a->page_table;
+    at.page_size = a->page_size; at.max_pages = a->max_pages; at.n_pages = a->n_pages;
+    at.scale = 1.0f / sqrtf((float)D); at.out = w.attn;
+    QD_TRY(launch_prefill_attention(at, L), "prefill attention");
+    QD_TRY(gemm(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, n, EPI_RESID_ADD, w.res), "o gemm");
+    QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, n, H, d.rms_eps, w.xn, L), "rmsnorm");
+    QD_TRY(gemm(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, n, EPI_STORE, w.gu), "gu gemm");
+    QD_TRY(launch_swiglu_rows(w.gu, n, F, w.xn, L), "swiglu");
+    QD_TRY(gemm(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, n, EPI_RESID_ADD, w.res), "down gemm");
+  }
+  // the last row alone goes through the final norm, the LM head and the argmax advance
+  QD_TRY(launch_rmsnorm_rows(w.res + (size_t)(n - 1) * H, a->final_norm, 1, H, d.rms_eps, w.xn, L), "final rmsnorm");
+  QD_TRY(gemm(a->lm_head, a->lm_head_scales, a->vocab, H, w.xn, 1, EPI_STORE, logits), "lm head gemm");
+  QD_TRY(launch_prefill_finish(a->pos, n, L), "prefill finish");
+  QD_TRY(launch_argmax_advance(logits, a->vocab, 1, a->tok, a->pos, a->step, a->out_tokens, a->max_steps,
+                               w.argmax_ws, L),
+         "argmax");
+  return QD_OK;
+}
+
 }  // namespace
 
 size_t qd_verify_workspace_bytes(const qd_step_args* a, int k) {
@@ -1025,6 +1138,17 @@ int qd_verify_step(const qd_step_args* a, const int32_t* draft, int k, float* lo
   int rc = validate_verify(a, draft, k, logits, target, n_accept);
   if (rc) return rc;
   return run_verify(a, draft, k, logits, target, n_accept, stream);
+}
+
+size_t qd_prefill_workspace_bytes(const qd_step_args* a, int n_tokens) {
+  if (!a || !a->layers || a->n_layers < 1 || !a->layers[0] || n_tokens < 1 || n_tokens > kMaxPrefill) return 0;
+  return prefill_ws_layout(a, n_tokens, nullptr).total;
+}
+
+int qd_prefill(const qd_step_args* a, const int32_t* tokens, int n_tokens, float* logits, cudaStream_t stream) {
+  int rc = validate_prefill(a, tokens, n_tokens, logits);
+  if (rc) return rc;
+  return run_prefill(a, tokens, n_tokens, logits, stream);
 }
 
 size_t qd_step_workspace_bytes(const qd_step_args* a) {

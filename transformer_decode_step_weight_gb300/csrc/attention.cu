@@ -900,8 +900,8 @@ cudaError_t launch_attention(const AttnArgs& a, const Launch& L) {
 // v as is, both rounded to bf16 and stored at the row's position.
 __global__ void __launch_bounds__(kD) kv_write_kernel(const float* qkv, int Hq, int Hkv, const __nv_bfloat16* k_norm,
                                                       const float2* rope, int rope_max_pos, float eps, int act_bf16,
-                                                      const int32_t* pos, const int32_t* page_table, int page_size,
-                                                      int max_pages, int n_pages, __nv_bfloat16* k_pages,
+                                                      const int32_t* pos, const int32_t* page_table, int pt_stride,
+                                                      int page_size, int max_pages, int n_pages, __nv_bfloat16* k_pages,
                                                       __nv_bfloat16* v_pages, int* err) {
   __shared__ float red[4];
   __shared__ float s_y[kD];
@@ -930,7 +930,7 @@ __global__ void __launch_bounds__(kD) kv_write_kernel(const float* qkv, int Hq, 
   const float2 cs = rope[(size_t)ps_ * (kD / 2) + (d & 63)];
   const float other = s_y[d ^ 64];
   const float r = (d < 64) ? (y * cs.x - other * cs.y) : (y * cs.x + other * cs.y);
-  const PagedSlot sl = paged_slot(page_table + (size_t)b * max_pages, ps_, page_size, n_pages);
+  const PagedSlot sl = paged_slot(page_table + (size_t)b * pt_stride, ps_, page_size, n_pages);
   if (!sl.ok) {
     if (d == 0) set_error(err, QD_DEVERR_PAGE);
     return;
@@ -942,10 +942,11 @@ __global__ void __launch_bounds__(kD) kv_write_kernel(const float* qkv, int Hq, 
 
 cudaError_t launch_kv_write(const float* qkv, int B, int Hq, int Hkv, const void* k_norm, const float* rope,
                             int rope_max_pos, float eps, int act_bf16, const int32_t* pos, const int32_t* page_table,
-                            int page_size, int max_pages, int n_pages, void* k_pages, void* v_pages, const Launch& L) {
+                            int pt_stride, int page_size, int max_pages, int n_pages, void* k_pages, void* v_pages,
+                            const Launch& L) {
   return launch_ex(kv_write_kernel, dim3(Hkv, B), dim3(kD), 0, L, qkv, Hq, Hkv, (const __nv_bfloat16*)k_norm,
-                   (const float2*)rope, rope_max_pos, eps, act_bf16, pos, page_table, page_size, max_pages, n_pages,
-                   (__nv_bfloat16*)k_pages, (__nv_bfloat16*)v_pages, L.err);
+                   (const float2*)rope, rope_max_pos, eps, act_bf16, pos, page_table, pt_stride, page_size, max_pages,
+                   n_pages, (__nv_bfloat16*)k_pages, (__nv_bfloat16*)v_pages, L.err);
 }
 
 cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float theta, cudaStream_t s) {

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * kBM;
+  const int n0 = blockIdx.z * kBN;   // this CTA's first token (grid z: 64-token tiles)
   // this CTA's K blocks [kb0, kb0 + n_k) of split blockIdx.y
   const int n_kt = p.K / kBK;
   const int kb0 = (int)(((long long)n_kt * blockIdx.y) / p.splits);
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
         tma_load_2d(sA + i * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[i]);
       }
       pdl_wait();
-      for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[i]);
+      for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * kTileB, &tmX, (kb0 + i) * kBK, n0, &full[i]);
       int issued = pre;
       for (int i = pre; i < n_k; ++i) {
         const int s = i % kStagesTc;
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
         }
         mbar_arrive_expect_tx(&full[s], kTileA + kTileB);
         tma_load_2d(sA + s * kTileA, &tmW, (kb0 + i) * kBK, row0, &full[s]);
-        tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[s]);
+        tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, n0, &full[s]);
         issued = i + 1;
       }
       drain_ring(full, kStagesTc, issued, p.err);
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
           break;
         }
         mbar_arrive_expect_tx(&full[s], kTileB);
-        tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, 0, &full[s]);
+        tma_load_2d(sB + s * kTileB, &tmX, (kb0 + i) * kBK, n0, &full[s]);
         issued = i + 1;
       }
       drain_ring(full, kBSt, issued, p.err);
@@ -376,20 +377,20 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
   const int rl = warp * 32 + lane;          // this thread's row of the tile
   const int r = row0 + rl;
   bool write = rows_here && ok && !s_abort;
-  // y[n0 + j, r] (+)= o[j] for 16 tokens; the residual values are all loaded
+  // y[t + j, r] (+)= o[j] for 16 tokens from t; the residual values are all loaded
   // before any store, so the 16 read-modify-writes overlap instead of queueing
-  auto store_rows = [&](int n0, const float* o) {
+  auto store_rows = [&](int t, const float* o) {
     float old[16];
     if (p.epi == EPI_RESID_ADD) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) old[j] = n0 + j < p.B ? p.y[(size_t)(n0 + j) * p.R + r] : 0.f;
+      for (int j = 0; j < 16; ++j) old[j] = t + j < p.B ? p.y[(size_t)(t + j) * p.R + r] : 0.f;
     } else {
 #pragma unroll
       for (int j = 0; j < 16; ++j) old[j] = 0.f;
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (n0 + j < p.B) p.y[(size_t)(n0 + j) * p.R + r] = p.epi == EPI_RESID_ADD ? old[j] + o[j] : o[j];
+      if (t + j < p.B) p.y[(size_t)(t + j) * p.R + r] = p.epi == EPI_RESID_ADD ? old[j] + o[j] : o[j];
   };
   if (p.splits > 1) {
     // publish this split's partial tile [kBN tokens][kBM rows] (each warp access
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
   }
   if (write && r < p.R) {
 #pragma unroll
-    for (int c = 0; c < kBN / 16; ++c) store_rows(c * 16, v + c * 16);
+    for (int c = 0; c < kBN / 16; ++c) store_rows(n0 + c * 16, v + c * 16);
   }
   tc_fence_before();
   __syncthreads();
@@ -499,8 +500,8 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const CUtens
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(k, dim3(tiles, p.splits), dim3(Q8 ? kThreadsQ8 : kThreadsTc), smem_tc(ST, Q8), L, tw, tx, ts,
-                   p);
+  return launch_ex(k, dim3(tiles, p.splits, ceil_div(p.B, kBN)), dim3(Q8 ? kThreadsQ8 : kThreadsTc), smem_tc(ST, Q8), L,
+                   tw, tx, ts, p);
 }
 
 }  // namespace
@@ -510,6 +511,11 @@ cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint
 }
 
 bool gemm_tc_supported(int R, int K, int B) { return R >= 1 && K >= kBK && K % kBK == 0 && B >= 1 && B <= kBN; }
+
+// Many rows (prefill): 64-token tiles over grid z, no K split.
+bool gemm_tc_rows_supported(int R, int K, int B, bool q8) {
+  return R >= 1 && K >= kBK && K % kBK == 0 && (!q8 || K % 256 == 0) && B >= 1 && B <= 65535 * kBN;
+}
 
 // Q8_0 weights: the scale rows are read as 16-byte TMA boxes (256 columns), so
 // their stride K/32 x 2 bytes must be a multiple of 16.
@@ -560,7 +566,10 @@ size_t gemm_tc_workspace_bytes(int R, int K, bool q8) {
 
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   const bool q8 = a.S != nullptr;
-  if (!(q8 ? gemm_tc_q8_supported(a.R, a.K, a.B) : gemm_tc_supported(a.R, a.K, a.B))) return cudaErrorInvalidValue;
+  const bool rows = a.B > kBN;   // several token tiles: no K split
+  if (rows ? !gemm_tc_rows_supported(a.R, a.K, a.B, q8)
+           : !(q8 ? gemm_tc_q8_supported(a.R, a.K, a.B) : gemm_tc_supported(a.R, a.K, a.B)))
+    return cudaErrorInvalidValue;
   CUtensorMap tw, tx, ts;
   cudaError_t e;
   if (q8) {
@@ -584,7 +593,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   const int tiles = (a.R + kBM - 1) / kBM;
   p.splits = 1;
   const size_t need = gemm_tc_workspace_bytes(a.R, a.K, q8);
-  if (a.ws && need > 0 && a.ws_bytes >= need) {
+  if (!rows && a.ws && need > 0 && a.ws_bytes >= need) {
     p.splits = gemm_tc_splits(a.R, a.K, q8);
     p.cnt = (int*)a.ws;
     p.part = (float*)((unsigned char*)a.ws + kTicketBytes);
@@ -595,7 +604,8 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
     const char* v = getenv("QD_GEMM_STAGES");
     return v ? atoi(v) : 0;
   }();
-  const bool deep = forced == 6 || (forced != 3 && (long long)tiles * p.splits <= dev_info().sm_count);
+  const bool deep =
+      forced == 6 || (forced != 3 && (long long)tiles * p.splits * ceil_div(a.B, kBN) <= dev_info().sm_count);
   return deep ? launch_tc<6, false>(tw, tx, ts, p, tiles, L) : launch_tc<3, false>(tw, tx, ts, p, tiles, L);
 }
 

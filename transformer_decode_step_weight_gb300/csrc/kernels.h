@@ -109,7 +109,7 @@ struct GemmTcArgs {
   const void* W;          // bf16 [R, K], or Q8_0 int8 values [R, K] when S is set
   const void* S;          // Q8_0 fp16 scales [R, K/32], or null (bf16 W)
   const void* X;          // bf16 [B, K]
-  int R, K, B;            // B <= 64
+  int R, K, B;            // B <= 64, or more rows in 64-token tiles (no K split)
   int epi;                // GemvEpi
   float* y;               // f32 [B, R]
   void* ws;               // split-K partials and tile tickets (zero-filled before first use,
@@ -117,6 +117,8 @@ struct GemmTcArgs {
 };
 bool gemm_tc_supported(int R, int K, int B);
 bool gemm_tc_q8_supported(int R, int K, int B);
+// B > 64 rows (prefill): token tiles over grid z, no K split; B <= 64: the forms above.
+bool gemm_tc_rows_supported(int R, int K, int B, bool q8);
 // Tensor map (CUtensorMap, 128-byte aligned storage of 128 bytes) of a row-major
 // bf16 [rows, cols] matrix: boxes of box_rows x 64 columns, 128-byte swizzle.
 cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
@@ -206,9 +208,34 @@ cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, float the
 // k = RoPE_pos[b](RMSNorm(qkv[b] k-head g; k_norm)) and v, both rounded to bf16, at
 // logical position pos[b] through page_table row b (the attention's fused prologue
 // arithmetic, with bf16 activations when act_bf16).
+// Row b's page table starts at page_table + b * pt_stride (0: all rows share one).
 cudaError_t launch_kv_write(const float* qkv, int B, int Hq, int Hkv, const void* k_norm, const float* rope,
                             int rope_max_pos, float eps, int act_bf16, const int32_t* pos, const int32_t* page_table,
-                            int page_size, int max_pages, int n_pages, void* k_pages, void* v_pages, const Launch& L);
+                            int pt_stride, int page_size, int max_pages, int n_pages, void* k_pages, void* v_pages,
+                            const Launch& L);
+
+// ----------------------------------------------------------------- prefill (prefill.cu)
+// Causal attention of the n prompt rows of one sequence (positions pos[0] + i) over
+// the cached keys 0 .. pos[0] + i, with the queries' QK-RMSNorm and RoPE fused in.
+struct PrefillAttnArgs {
+  const float* qkv;        // f32 [n, (Hq + 2 Hkv) D] (the QKV projection of the rows)
+  int n, Hq, Hkv, D;       // D == 128
+  const void* q_norm;      // bf16 [D]
+  const float* rope;       // (cos, sin) table [rope_max_pos, D / 2]
+  int rope_max_pos;
+  float eps;
+  int act_bf16;
+  const int32_t* pos;      // pos[0]: position of row 0
+  const void* k_pages;     // bf16 [n_pages, Hkv, page_size, D], the rows' K/V already written
+  const void* v_pages;
+  const int32_t* page_table;   // the sequence's page table [max_pages]
+  int page_size, max_pages, n_pages;
+  float scale;
+  void* out;               // bf16 [n, Hq D]
+};
+cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const Launch& L);
+cudaError_t launch_prefill_prep(const int32_t* pos, int n, int32_t* vpos, const Launch& L);
+cudaError_t launch_prefill_finish(int32_t* pos, int n, const Launch& L);
 
 // ----------------------------------------------------------------- persistent batch-1 step
 // The whole decode step of a BF16 model at batch 1 as one cooperative kernel
