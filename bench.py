@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=64,
                     help="rows of x for --kernel gemm_tc; sequences for --kernel attention_batched")
     ap.add_argument("--act", choices=["f32", "i8"], default="f32", help="Q8_0 activation lane (batch 1)")
+    ap.add_argument("--prefill", type=int, default=0, metavar="N",
+                    help="time the prefill of an N-token prompt (positions 0 .. N-1) instead of decode")
     ap.add_argument("--verify", type=int, default=0, metavar="K",
                     help="time speculative verify passes of K tokens (K - 1 drafts) against K single-token steps "
                          "on the batch-1 workload")
@@ -198,6 +200,17 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tensor_peak(sustained: bool):
+    """The measured dense bf16 tensor peak in TFLOP/s (burst, or the seconds-long
+    sustained figure for kernels timed inside a long run)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops_sustained" if sustained else "bf16_tflops"]), "measured"
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback"
 
 
 def traffic_record(kernel_src: str):
@@ -799,10 +812,110 @@ def run_verify(args):
     dec.close()
 
 
+def prefill_flops(s: synth.Shape, n: int, pos0: int = 0):
+    """Algorithmic flops of one prefill: 2 per weight per row for the projections, the
+    LM head for the last row, and the causal attention (q.k and p.v over the keys
+    0 .. pos0 + i of row i, every q head)."""
+    per_layer = (s.qkv_rows + 2 * s.ffn) * s.hidden + s.hidden * s.n_q_heads * s.head_dim + s.hidden * s.ffn
+    gemm = 2.0 * n * per_layer * s.n_layers + 2.0 * s.vocab * s.hidden
+    keys = n * pos0 + n * (n + 1) / 2
+    attn = 4.0 * s.head_dim * s.n_q_heads * keys * s.n_layers
+    return gemm, attn
+
+
+def run_prefill_bench(args):
+    """Prefill of one N-token prompt at positions 0 .. N - 1 on the workload's model,
+    as a CUDA graph that restores the decode state first (three 4-byte copies), so every
+    replay writes the same cache rows. Reports prompt tokens per second, the whole
+    pass's achieved TFLOP/s, and the dominant kernel (the gate+up GEMM over the N rows)
+    timed alone with CUDA events against the measured bf16 tensor peak."""
+    from transformer_decode_step_weight_gb300 import api
+    from transformer_decode_step_weight_gb300 import build as b
+    b.build()
+    dev = torch.device("cuda", 0)
+    n = args.prefill
+    wl = synth.WORKLOADS[args.workload]
+    s = wl.shape
+    assert wl.batch == 1 and wl.wtype in ("bf16", "q8_0"), "prefill runs on one sequence, BF16 or Q8_0 weights"
+    mt = synth.make_model(s, wl.wtype, args.seed, dev, ctx=0, steps=n + 1)
+    dec = api.Decoder(mt, max_steps=n + 1, device=dev, prefill_max=n)
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed + 2)
+    tokens = torch.randint(0, s.vocab, (n,), generator=g, device=dev, dtype=torch.int64).to(torch.int32)
+    tok0, pos0 = dec.tok.clone(), dec.pos.clone()
+    st = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(st):
+        dec.prefill(tokens, stream=st)
+    st.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        dec.tok.copy_(tok0)
+        dec.pos.copy_(pos0)
+        dec.step_ctr.zero_()
+        dec.prefill(tokens, stream=st)
+
+    def timed(fn, k):
+        with torch.cuda.stream(st):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(k):
+                fn()
+            e1.record(st)
+        st.synchronize()
+        return e0.elapsed_time(e1) / k
+
+    reps = max(1, args.reps)
+    k = max(1, min(args.steps, 8))
+    clocks = ClockSampler(0)
+    clocks.start()
+    ms_all = [timed(graph.replay, k) for _ in range(reps)]
+    clk = clocks.stop()
+    ms = sorted(ms_all)[reps // 2]
+    assert api.check_device_error(st) == 0
+    gemm_f, attn_f = prefill_flops(s, n)
+    peak, kind = tensor_peak(sustained=True)
+    total_tf = (gemm_f + attn_f) / (ms / 1e3) / 1e12
+    # dominant kernel: the gate+up GEMM [2F, H] over the N rows, alone
+    lt = mt.layers[0]
+    x = torch.randn((n, s.hidden), generator=g, device=dev).to(torch.bfloat16)
+    y = torch.empty((n, 2 * s.ffn), dtype=torch.float32, device=dev)
+    if wl.wtype == "bf16":
+        fn = lambda: api.gemv_bf16(lt.w_gu, x, y, stream=st)  # noqa: E731
+    else:
+        fn = lambda: api.gemm_q8_0(lt.w_gu, lt.s_gu, x, y, stream=st)  # noqa: E731
+    gu_ms = sorted(timed(fn, 10) for _ in range(3))[1]
+    gu_flops = 2.0 * n * 2 * s.ffn * s.hidden
+    gu_tf = gu_flops / (gu_ms / 1e3) / 1e12
+    bpeak, bkind = tensor_peak(sustained=False)
+    out = {"metric": f"prefill of an {n}-token prompt (one sequence)", "value": round(n / (ms / 1e3), 1),
+           "unit": "prompt tok/s", "ms_per_prefill": round(ms, 3), "higher_is_better": True,
+           "dtype": "bf16 tcgen05 GEMMs + bf16 mma.sync attention" if wl.wtype == "bf16" else
+                    "q8_0 widened to bf16, tcgen05 GEMMs + bf16 mma.sync attention",
+           "data": "synthetic",
+           "config": {"workload": wl.name, "prompt_tokens": n, "positions": f"0..{n - 1}",
+                      "graph": "one CUDA graph per prefill", "repetitions": reps, "prefills_each": k},
+           "roofline": {"bound": "tensor", "kernel": f"gemm_tc_kernel (gate+up, {2 * s.ffn} x {s.hidden} x {n} rows)",
+                        "achieved": round(gu_tf, 1), "peak": bpeak, "unit": "TFLOP/s",
+                        "frac": round(gu_tf / bpeak, 4), "peak_kind": f"{bkind} burst", "us_per_launch": round(gu_ms * 1e3, 2),
+                        "traffic": None},
+           "step_roofline": {"bound": "tensor", "achieved": round(total_tf, 1), "peak": peak, "unit": "TFLOP/s",
+                             "frac": round(total_tf / peak, 4), "peak_kind": f"{kind} sustained",
+                             "gemm_tflop": round(gemm_f / 1e12, 3), "attention_tflop": round(attn_f / 1e12, 3)},
+           "repetitions": {"ms": [round(v, 3) for v in ms_all]},
+           "clocks": clk}
+    print(json.dumps(out), flush=True)
+    dec.close()
+
+
 def main():
     args = parse()
     if args.kernel:
         run_kernel(args)
+        return
+    if args.prefill:
+        run_prefill_bench(args)
         return
     if args.verify:
         run_verify(args)

@@ -88,9 +88,10 @@ int qd_version(void);
 /* W: bf16 [rows, cols]. x: bf16 [batch, cols] (x_is_f32 = 0) or f32            */
 /* [batch, cols] (x_is_f32 = 1; the kernel rounds x to bf16 first). y: f32      */
 /* [batch, rows]. Accumulation in f32, deterministic order.                   */
-/* batch <= 8: CUDA-core GEMV (cols % 8 == 0). 9 <= batch <= 64: the product is */
-/* a dense contraction and runs on the tcgen05 tensor cores ("qwen3-8b-rtx4080- */
-/* cutedsl" README, "Baseline tiled GEMM"); needs bf16 x and cols % 64 == 0.    */
+/* batch <= 8: CUDA-core GEMV (cols % 8 == 0). batch >= 9: the product is a    */
+/* dense contraction and runs on the tcgen05 tensor cores ("qwen3-8b-rtx4080-   */
+/* cutedsl" README, "Baseline tiled GEMM"), one CTA per 128 rows x 64 batch     */
+/* rows (a prompt's tokens, for prefill); needs bf16 x and cols % 64 == 0.      */
 int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
                  float* y, int batch, cudaStream_t stream);
 
@@ -116,7 +117,8 @@ int qd_gemv_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols,
 /* scratch of qd_gemm_workspace_bytes(rows, cols, QD_W_Q8_0) bytes, zero-filled  */
 /* before its first use (each call leaves it zero-filled); with it, grids that   */
 /* do not fill the SMs split K and sum the partials in split order.              */
-/* Limits: cols % 256 == 0, 1 <= batch <= 64, every pointer 16-byte aligned.     */
+/* Limits: cols % 256 == 0, batch >= 1 (above 64: 64-row tiles, no K split and   */
+/* the workspace unused), every pointer 16-byte aligned.                         */
 size_t qd_gemm_workspace_bytes(int rows, int cols, qd_wtype wtype);
 int qd_gemm_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const void* x_bf16,
                  int batch, float* y, void* workspace, size_t workspace_bytes,

@@ -43,9 +43,11 @@ def test_gemv_bf16(cuda_lib, R, K, B):
 
 
 @pytest.mark.parametrize("R,K,B", [(128, 64, 9), (300, 1024, 16), (4096, 4096, 64), (1000, 12288, 33),
-                                   (6144, 4096, 64), (151936, 4096, 64)])
+                                   (6144, 4096, 64), (151936, 4096, 64), (300, 1024, 65), (1000, 4096, 200),
+                                   (4096, 4096, 512)])
 def test_gemm_bf16_tensor_cores(cuda_lib, R, K, B):
-    # 9 <= batch <= 64: the tcgen05 path (ragged last 128-row tile, batch below 64)
+    # batch >= 9: the tcgen05 path (ragged last 128-row tile, batch below 64; above 64
+    # the prompt-row form, 64-row tiles of x over the grid with a ragged last one)
     g = _gen(R * 7 + B)
     W = (torch.randn((R, K), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
     x = torch.randn((B, K), generator=g, device=DEV).to(torch.bfloat16)
@@ -61,10 +63,11 @@ def test_gemm_bf16_tensor_cores(cuda_lib, R, K, B):
 def test_gemm_bf16_tensor_cores_integer_exact(cuda_lib):
     g = _gen(13)
     W = torch.randint(-8, 9, (384, 512), generator=g, device=DEV).to(torch.bfloat16)
-    x = torch.randint(-8, 9, (24, 512), generator=g, device=DEV).to(torch.bfloat16)
-    y = api.gemv_bf16(W, x)
-    ref = x.double().cpu() @ W.double().cpu().T
-    assert torch.equal(y.cpu().double(), ref)
+    for B in (24, 130):
+        x = torch.randint(-8, 9, (B, 512), generator=g, device=DEV).to(torch.bfloat16)
+        y = api.gemv_bf16(W, x)
+        ref = x.double().cpu() @ W.double().cpu().T
+        assert torch.equal(y.cpu().double(), ref), B
 
 
 def test_gemv_bf16_f32_input_rounds_to_bf16(cuda_lib):
@@ -157,7 +160,7 @@ def test_gemv_q8_0_unit_scales_integer_exact(cuda_lib):
 
 @pytest.mark.parametrize("R,K,B,split", [(128, 256, 2, False), (300, 768, 17, False), (1000, 1536, 64, True),
                                          (6144, 4096, 64, True), (4096, 12288, 64, True),
-                                         (151936, 4096, 64, False)])
+                                         (151936, 4096, 64, False), (300, 768, 130, False)])
 def test_gemm_q8_0_tensor_cores(cuda_lib, R, K, B, split, parity_log):
     # Q8_0 weights widened to bf16 on chip: ragged last 128-row tile, batch below 64,
     # K split across CTAs (partials summed in split order) where the grid is small.

@@ -76,7 +76,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.qd_gemm_q8_0(fake, fake, 128, 300, fake, 2, fake, None, 0, None) == -1
     assert lib.qd_gemm_q8_0(fake, fake, 128, 288, fake, 2, fake, None, 0, None) == -2
     assert b"256" in lib.qd_last_error()
-    assert lib.qd_gemm_q8_0(fake, fake, 128, 256, fake, 65, fake, None, 0, None) == -2   # batch > 64
+    assert lib.qd_gemm_q8_0(fake, fake, 128, 256, fake, 0, fake, None, 0, None) == -1    # batch 0
     # workspace sizing is pure host arithmetic
     assert lib.qd_attn_workspace_bytes(1, 32, 8, 4224) > 0
     assert lib.qd_attn_workspace_bytes(0, 32, 8, 4224) == 0

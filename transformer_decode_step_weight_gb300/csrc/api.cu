@@ -193,8 +193,9 @@ int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
   if (!aligned16(W) || !aligned16(x) || !aligned16(y))
     return fail(QD_ERR_INVALID_ARG, "qd_gemv_bf16: pointers must be 16-byte aligned");
   if (batch > 8) {  // a real contraction: tcgen05 tensor cores
-    if (x_is_f32 || !gemm_tc_supported(rows, cols, batch))
-      return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: batch %d needs bf16 x, cols %% 64 == 0 and batch <= 64", batch);
+    const bool ok = batch <= 64 ? gemm_tc_supported(rows, cols, batch) : gemm_tc_rows_supported(rows, cols, batch, false);
+    if (x_is_f32 || !ok)
+      return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: batch %d needs bf16 x and cols %% 64 == 0", batch);
     GemmTcArgs g = {};
     g.W = W; g.X = x; g.R = rows; g.K = cols; g.B = batch; g.epi = EPI_STORE; g.y = y;
     cudaError_t e = launch_gemm_tc(g, make_launch(stream, false));
@@ -276,9 +277,8 @@ int qd_gemm_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const 
   if (!qs || !d_f16 || !x_bf16 || !y) return fail(QD_ERR_INVALID_ARG, "qd_gemm_q8_0: null pointer");
   if (rows < 1 || cols < 32 || cols % 32 || batch < 1)
     return fail(QD_ERR_INVALID_ARG, "qd_gemm_q8_0: rows=%d cols=%d batch=%d", rows, cols, batch);
-  if (!gemm_tc_q8_supported(rows, cols, batch))
-    return fail(QD_ERR_UNSUPPORTED, "qd_gemm_q8_0: need cols %% 256 == 0 and batch <= 64 (cols=%d batch=%d)", cols,
-                batch);
+  if (batch <= 64 ? !gemm_tc_q8_supported(rows, cols, batch) : !gemm_tc_rows_supported(rows, cols, batch, true))
+    return fail(QD_ERR_UNSUPPORTED, "qd_gemm_q8_0: need cols %% 256 == 0 (cols=%d batch=%d)", cols, batch);
   if (!aligned16(qs) || !aligned16(d_f16) || !aligned16(x_bf16) || !aligned16(y) ||
       (workspace && !aligned16(workspace)))
     return fail(QD_ERR_INVALID_ARG, "qd_gemm_q8_0: pointers must be 16-byte aligned");
