@@ -46,7 +46,6 @@ constexpr int kBK = 64;         // K elements per stage (128 bytes of bf16)
 // runs in one wave). QD_GEMM_STAGES = 3 or 6 forces one. The Q8_0 form's rings
 // are set below (kQSt, kBSt, kASt).
 constexpr int kTileA = kBM * kBK * 2;    // 16 KB
-constexpr int kTileB = kBN * kBK * 2;    // 8 KB
 constexpr int kTileQ = kBM * kBK;        // 8 KB: int8 values of a Q8_0 tile
 constexpr int kTileS = kBM * 16;         // 2 KB: 8 fp16 scales (256 columns) per row
 constexpr int kThreadsTc = 128;
@@ -90,11 +89,14 @@ QD_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: D f32, A and B bf16, both K-major, M = 128, N = 64.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kBM >> 4) << 24);
+// Instruction descriptor: D f32, A and B bf16, both K-major, M = 128, N = bn.
+__host__ __device__ constexpr uint32_t idesc_for(int bn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
 
+template <int BN>
 QD_DEV void mma_bf16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+  constexpr uint32_t kIdesc = idesc_for(BN);
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -171,8 +173,9 @@ QD_DEV void drain_ring(uint64_t* full, int slots, int issued, int* err) {
   for (int i = max(0, issued - slots); i < issued; ++i) mbar_wait_bounded(&full[i % slots], (uint32_t)((i / slots) & 1), err);
 }
 
-template <int kStagesTc, bool kQ8>
-__global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStagesTc <= 3) ? 3 : 1)
+// BN: tokens per CTA (the MMA's N and the TMEM columns): 64, or 256 for many rows
+template <int kStagesTc, bool kQ8, int BN>
+__global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStagesTc <= 3 && BN == kBN) ? 3 : 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmS, const TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -181,8 +184,9 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
   constexpr int nA = kQ8 ? kASt : kStagesTc;  // A tiles (bf16 W, or widened Q8_0)
   constexpr int nB = kQ8 ? kBSt : kStagesTc;  // X tiles
   constexpr int nQ = kQ8 ? kQSt : 0;          // int8 + scale tiles
+  constexpr int kTileB = BN * kBK * 2;        // X tile bytes
   unsigned char* sA = smem;                   // [nA][128 x 128 B]
-  unsigned char* sB = sA + nA * kTileA;       // [nB][64 x 128 B]
+  unsigned char* sB = sA + nA * kTileA;       // [nB][BN x 128 B]
   unsigned char* sQ = sB + nB * kTileB;       // [nQ][128 x 64 B]
   unsigned char* sS = sQ + nQ * kTileQ;       // [nQ][128 x 16 B]
   // bf16 form: full/empty per stage cover both A and B tiles
@@ -198,7 +202,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * kBM;
-  const int n0 = blockIdx.z * kBN;   // this CTA's first token (grid z: 64-token tiles)
+  const int n0 = blockIdx.z * BN;    // this CTA's first token (grid z: BN-token tiles)
   // this CTA's K blocks [kb0, kb0 + n_k) of split blockIdx.y
   const int n_kt = p.K / kBK;
   const int kb0 = (int)(((long long)n_kt * blockIdx.y) / p.splits);
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
     fence_mbar_init();
     s_abort = 0;
   }
-  if (warp == 0) tmem_alloc(tmem_slot, kBN);
+  if (warp == 0) tmem_alloc(tmem_slot, BN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
   auto mma_stage = [&](uint32_t a0, uint32_t b0, int i) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk)
-      mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), (i | kk) != 0);
+      mma_bf16<BN>(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), (i | kk) != 0);
   };
 
   if constexpr (!kQ8) {
@@ -438,13 +442,20 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
     if (s_ticket == p.splits - 1 && tid == 0) p.cnt[tile] = 0;
     write = false;  // the tile's output is written above (or by another split)
   }
-  if (write && r < p.R) {
+  if (p.splits <= 1 && rows_here) {
+    // 64 TMEM columns (tokens) at a time; the loads are warp-wide, the stores per row
+#pragma unroll 1
+    for (int c4 = 0; c4 < BN / 64; ++c4) {
+      if (c4 > 0) tmem_ld_32x64(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c4 * 64), v);
+      if (write && r < p.R) {
 #pragma unroll
-    for (int c = 0; c < kBN / 16; ++c) store_rows(n0 + c * 16, v + c * 16);
+        for (int c = 0; c < 4; ++c) store_rows(n0 + c4 * 64 + c * 16, v + c * 16);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kBN);
+  if (warp == 0) tmem_dealloc(tmem, BN);
 }
 
 // --- host: tensor maps --------------------------------------------------------
@@ -484,24 +495,24 @@ cudaError_t encode_rowmajor_bf16(CUtensorMap* m, const void* base, uint64_t rows
                          CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-constexpr size_t smem_tc(int st, bool q8) {
-  return q8 ? 1024 + (size_t)kASt * kTileA + (size_t)kBSt * kTileB + (size_t)kQSt * (kTileQ + kTileS) +
+constexpr size_t smem_tc(int st, bool q8, int bn) {
+  return q8 ? 1024 + (size_t)kASt * kTileA + (size_t)kBSt * bn * kBK * 2 + (size_t)kQSt * (kTileQ + kTileS) +
                   (2 * kBSt + 2 * kQSt + 2 * kASt + 1) * 8 + 16
-            : 1024 + (size_t)st * (kTileA + kTileB) + (2 * st + 1) * 8 + 16;
+            : 1024 + (size_t)st * (kTileA + (size_t)bn * kBK * 2) + (2 * st + 1) * 8 + 16;
 }
 
-template <int ST, bool Q8>
+template <int ST, bool Q8, int BN = kBN>
 cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& ts, const TcParams& p,
                       int tiles, const Launch& L) {
-  auto k = gemm_tc_kernel<ST, Q8>;
+  auto k = gemm_tc_kernel<ST, Q8, BN>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tc(ST, Q8));
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tc(ST, Q8, BN));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(k, dim3(tiles, p.splits, ceil_div(p.B, kBN)), dim3(Q8 ? kThreadsQ8 : kThreadsTc), smem_tc(ST, Q8), L,
-                   tw, tx, ts, p);
+  return launch_ex(k, dim3(tiles, p.splits, ceil_div(p.B, BN)), dim3(Q8 ? kThreadsQ8 : kThreadsTc),
+                   smem_tc(ST, Q8, BN), L, tw, tx, ts, p);
 }
 
 }  // namespace
@@ -585,8 +596,14 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
     ts = tw;  // unused
   }
   if (e != cudaSuccess) return e;
-  // X has B rows; the 64-row box reads zeros past them
-  e = encode_rowmajor_bf16(&tx, a.X, (uint64_t)a.B, (uint64_t)a.K, kBN);
+  // many rows (bf16): 256-token tiles (QD_GEMM_BN=64 keeps 64)
+  static const int forced_bn = [] {
+    const char* v = getenv("QD_GEMM_BN");
+    return v ? atoi(v) : 0;
+  }();
+  const bool wide = !q8 && rows && a.B > 2 * kBN && forced_bn != kBN;
+  // X has B rows; the box reads zeros past them
+  e = encode_rowmajor_bf16(&tx, a.X, (uint64_t)a.B, (uint64_t)a.K, wide ? 256 : kBN);
   if (e != cudaSuccess) return e;
   TcParams p = {};
   p.R = a.R; p.K = a.K; p.B = a.B; p.epi = a.epi; p.y = a.y; p.err = L.err;
@@ -600,6 +617,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   }
   // Q8_0: one 384-thread CTA per SM with its own ring depths
   if (q8) return launch_tc<kASt, true>(tw, tx, ts, p, tiles, L);
+  if (wide) return launch_tc<4, false, 256>(tw, tx, ts, p, tiles, L);
   static const int forced = [] {
     const char* v = getenv("QD_GEMM_STAGES");
     return v ? atoi(v) : 0;
