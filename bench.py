@@ -757,9 +757,13 @@ def run_verify(args):
     k = args.verify
     wl = synth.WORKLOADS[args.workload]
     assert wl.batch == 1, "speculative verify runs on one sequence"
-    mt = synth.make_model(wl.shape, wl.wtype, args.seed, dev, ctx=wl.ctx, steps=4 * k + 16)
+    reps = max(1, args.reps)
+    n = max(1, args.steps // 4)
+    # room for every timed decode step (that leg does not restore the state)
+    run_len = 4 * k + 16 + reps * (max(3, args.warmup) + n) + 8
+    mt = synth.make_model(wl.shape, wl.wtype, args.seed, dev, ctx=wl.ctx, steps=run_len)
     act, lm_act = q8_lanes(args)
-    dec = api.Decoder(mt, max_steps=4 * k + 16, act=api.QD_ACT_I8 if act == "i8" else api.QD_ACT_F32,
+    dec = api.Decoder(mt, max_steps=run_len, act=api.QD_ACT_I8 if act == "i8" else api.QD_ACT_F32,
                       lm_act=api.QD_ACT_I8 if lm_act == "i8" else api.QD_ACT_F32, device=dev, verify_k=k)
     g = torch.Generator(device=dev)
     g.manual_seed(args.seed + 1)
@@ -788,8 +792,6 @@ def run_verify(args):
         s.synchronize()
         return e0.elapsed_time(e1) / n
 
-    reps = max(1, args.reps)
-    n = max(1, args.steps // 4)
     verify_ms = sorted(timed(graph.replay, n) for _ in range(reps))[reps // 2]
     with torch.cuda.stream(s):
         dec.tok.copy_(tok0)

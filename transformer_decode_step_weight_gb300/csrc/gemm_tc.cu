@@ -61,6 +61,8 @@ struct TcParams {
   int splits;     // K splits (grid y); > 1: partials through part / cnt
   float* part;    // [tiles][splits][kBN][kBM] f32 partial tiles
   int* cnt;       // [tiles] tickets, zero between launches
+  int zfast;      // many rows: grid x = token tiles, y = weight tiles (the token tiles of a
+                  // weight tile run together and share it through L2)
 };
 
 // --- tcgen05 / TMA wrappers -------------------------------------------------
@@ -201,12 +203,13 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row0 = blockIdx.x * kBM;
-  const int n0 = blockIdx.z * BN;    // this CTA's first token (grid z: BN-token tiles)
-  // this CTA's K blocks [kb0, kb0 + n_k) of split blockIdx.y
+  const int row0 = (p.zfast ? blockIdx.y : blockIdx.x) * kBM;
+  const int n0 = (p.zfast ? blockIdx.x : blockIdx.z) * BN;   // this CTA's first token
+  // this CTA's K blocks [kb0, kb0 + n_k) of its split (grid y unless token tiles lead)
+  const int split = p.zfast ? 0 : (int)blockIdx.y;
   const int n_kt = p.K / kBK;
-  const int kb0 = (int)(((long long)n_kt * blockIdx.y) / p.splits);
-  const int n_k = (int)(((long long)n_kt * (blockIdx.y + 1)) / p.splits) - kb0;
+  const int kb0 = (int)(((long long)n_kt * split) / p.splits);
+  const int n_k = (int)(((long long)n_kt * (split + 1)) / p.splits) - kb0;
   __shared__ int s_ticket;
 
   if (tid == 0) {
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
     // partial in split order, 16 tokens at a time with all their loads (and the
     // residual's) in flight together
     const size_t tile = blockIdx.x;
-    float* part = p.part + (tile * p.splits + blockIdx.y) * (size_t)(kBN * kBM);
+    float* part = p.part + (tile * p.splits + split) * (size_t)(kBN * kBM);
     if (rows_here) {
 #pragma unroll
       for (int n = 0; n < kBN; ++n) part[(size_t)n * kBM + rl] = v[n];
@@ -511,8 +514,8 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tx, const CUtens
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(k, dim3(tiles, p.splits, ceil_div(p.B, BN)), dim3(Q8 ? kThreadsQ8 : kThreadsTc),
-                   smem_tc(ST, Q8, BN), L, tw, tx, ts, p);
+  const dim3 grid = p.zfast ? dim3(ceil_div(p.B, BN), tiles) : dim3(tiles, p.splits, ceil_div(p.B, BN));
+  return launch_ex(k, grid, dim3(Q8 ? kThreadsQ8 : kThreadsTc), smem_tc(ST, Q8, BN), L, tw, tx, ts, p);
 }
 
 }  // namespace
@@ -607,6 +610,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   if (e != cudaSuccess) return e;
   TcParams p = {};
   p.R = a.R; p.K = a.K; p.B = a.B; p.epi = a.epi; p.y = a.y; p.err = L.err;
+  p.zfast = rows ? 1 : 0;
   const int tiles = (a.R + kBM - 1) / kBM;
   p.splits = 1;
   const size_t need = gemm_tc_workspace_bytes(a.R, a.K, q8);

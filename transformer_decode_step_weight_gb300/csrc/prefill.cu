@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(kPTh) prefill_attn_kernel(const PfParams p) {
   unsigned char* sQh = smem;                          // [64 rows][256 B], swizzled
   unsigned char* sQl = sQh + kPQ * kPD * 2;
   unsigned char* ring = sQl + kPQ * kPD * 2;          // [stage][K, V]
-  const int qt = blockIdx.x, h = blockIdx.y;
+  // the last query tiles see the most keys: launch them first so the short ones fill the tail
+  const int qt = (int)(gridDim.x - 1 - blockIdx.x), h = blockIdx.y;
   const int g = h / (p.Hq / p.Hkv);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
