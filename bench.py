@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3-8b-bf16",
                     choices=["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-int4",
-                             "qwen3-8b-bf16-paged-b64", "qwen3-8b-q8_0-paged-b64"])
+                             "qwen3-8b-bf16-paged-b64", "qwen3-8b-q8_0-paged-b64", "qwen3-0.6b-layer"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=128)
@@ -911,6 +911,76 @@ def run_prefill_bench(args):
     dec.close()
 
 
+def run_layer_bench(args):
+    """One Qwen3-0.6B-shaped decoder layer at position 128 (the single-layer workload),
+    timed with its weights coming from HBM: a 17-layer model (17 distinct random layers,
+    535 MB, more than four times L2) and a 1-layer model of the same shape each replay
+    their whole step as a CUDA graph, and the layer's time is the difference divided by
+    16 (embedding, LM head and argmax cancel). Median of `reps` repetitions of each."""
+    from transformer_decode_step_weight_gb300 import api
+    from transformer_decode_step_weight_gb300 import build as b
+    b.build()
+    dev = torch.device("cuda", 0)
+    wl = synth.WORKLOADS["qwen3-0.6b-layer"]
+    s = wl.shape
+    reps = max(1, args.reps)
+    k = max(8, args.steps)
+    run_len = reps * (k + max(3, args.warmup)) + 8
+    st = torch.cuda.Stream(device=dev)
+
+    def timed_model(n_layers):
+        mt = synth.make_model(s, wl.wtype, args.seed + n_layers, dev, n_layers=n_layers, ctx=wl.ctx, steps=run_len)
+        dec = api.Decoder(mt, max_steps=run_len, device=dev)
+        with torch.cuda.stream(st):
+            dec.capture(1, stream=st)
+        out = []
+        for _ in range(reps):
+            with torch.cuda.stream(st):
+                for _ in range(max(3, args.warmup)):
+                    dec.replay(stream=st)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                for _ in range(k):
+                    dec.replay(stream=st)
+                e1.record(st)
+            st.synchronize()
+            out.append(e0.elapsed_time(e1) / k)
+        assert api.check_device_error(st) == 0
+        dec.close()
+        del mt
+        torch.cuda.empty_cache()
+        return sorted(out)[reps // 2], out
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    t17, all17 = timed_model(17)
+    t1, all1 = timed_model(1)
+    clk = clocks.stop()
+    layer_ms = (t17 - t1) / 16
+    per_layer = (s.qkv_rows * s.hidden + s.hidden * s.n_q_heads * s.head_dim + 3 * s.ffn * s.hidden) * 2
+    kv = s.n_kv_heads * s.head_dim * 2 * 2 * (wl.ctx + 1)
+    # positions advance over the timed steps; the K/V term uses the mean position
+    kv_mean = s.n_kv_heads * s.head_dim * 2 * 2 * (wl.ctx + 1 + run_len // 2)
+    gbs = (per_layer + kv_mean) / (layer_ms / 1e3) / 1e9
+    peak, kind = peaks()
+    out = {"metric": "single-layer decode step (Qwen3-0.6B-shaped layer, position 128)",
+           "value": round(1e3 / layer_ms, 1), "unit": "layer steps/s", "ms_per_layer": round(layer_ms, 5),
+           "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": wl.name, "description": wl.description,
+                      "l2": "17 distinct layers (535 MB) per step, more than 4x L2; layer time = (T17 - T1) / 16",
+                      "steps_each": k, "repetitions": reps},
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                        "frac": round(gbs / peak, 4), "peak_kind": peak_kind_label(kind),
+                        "algorithmic_bytes_per_layer": int(per_layer + kv), "traffic": None},
+           "repetitions": {"ms_17_layers": [round(v, 4) for v in all17], "ms_1_layer": [round(v, 4) for v in all1]},
+           "clocks": clk}
+    print(json.dumps(out), flush=True)
+
+
+def peak_kind_label(kind):
+    return f"{kind} copy peak"
+
+
 def main():
     args = parse()
     if args.kernel:
@@ -918,6 +988,9 @@ def main():
         return
     if args.prefill:
         run_prefill_bench(args)
+        return
+    if args.workload == "qwen3-0.6b-layer" and args.impl != "reference":
+        run_layer_bench(args)
         return
     if args.verify:
         run_verify(args)

@@ -376,6 +376,11 @@ int qd_debug_q8_block_dots(const int8_t* qs, const void* d_f16, int rows, int co
 int qd_debug_paged_indices(const int32_t* page_table, int batch, int max_pages,
                            int page_size, int n_pages, int n_tokens, int32_t* idx,
                            cudaStream_t stream);
+/* The timeout path of the kernels' bounded waits: one thread arms an mbarrier   */
+/* for bytes no copy will deliver (none is issued) and waits on it for limit_us  */
+/* microseconds (1 .. 1000000); the wait gives up, sets QD_DEVERR_TIMEOUT and the */
+/* kernel returns, leaving the context usable. Asynchronous on `stream`.          */
+int qd_debug_wait_timeout(int limit_us, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

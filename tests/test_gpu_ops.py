@@ -379,3 +379,23 @@ def test_argmax_advance_rules(cuda_lib):
     assert tok[5].item() == 0
     assert api.check_device_error() == (4 | 8)
     assert api.check_device_error() == 0
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(cuda_lib):
+    # a wait on an mbarrier that no copy completes gives up after its limit, sets the
+    # timeout bit and returns; the next kernel runs normally
+    import time
+    assert api.check_device_error() == 0
+    t0 = time.perf_counter()
+    api.debug_wait_timeout(2000)
+    bits = api.check_device_error()
+    dt = time.perf_counter() - t0
+    assert bits == 16, bits            # QD_DEVERR_TIMEOUT alone
+    assert dt < 5.0
+    g = _gen(99)
+    W = (torch.randn((300, 512), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    x = torch.randn((1, 512), generator=g, device=DEV).to(torch.bfloat16)
+    y = api.gemv_bf16(W, x)
+    ref = oracle.gemv_bf16(synth.bits_u16(W), oracle.bf16_to_f64(synth.bits_u16(x[0])))
+    assert rel_max_abs(y[0].cpu().numpy(), ref) < GEMV_TOL
+    assert api.check_device_error() == 0

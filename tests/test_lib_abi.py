@@ -68,6 +68,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.qd_decode_step(None, None) == -1
     assert lib.qd_prefill(None, None, 4, None, None) == -1
     assert lib.qd_prefill_workspace_bytes(None, 4) == 0
+    assert lib.qd_debug_wait_timeout(0, None) == -1      # the limit is checked on the host
     # the batched Q8_0 GEMM: null pointers, cols not a multiple of 32, and cols that are a
     # multiple of 32 but not of 256 (its scale boxes) are refused before any launch;
     # the non-null pointers below are never dereferenced

@@ -82,6 +82,7 @@ _SIGS = {
     "qd_verify_step": (_i, [C.POINTER(StepArgs), _vp, _i, _vp, _vp, _vp, _vp]),
     "qd_prefill_workspace_bytes": (_sz, [C.POINTER(StepArgs), _i]),
     "qd_prefill": (_i, [C.POINTER(StepArgs), _vp, _i, _vp, _vp]),
+    "qd_debug_wait_timeout": (_i, [_i, _vp]),
     "qd_debug_q8_block_dots": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "qd_debug_paged_indices": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
 }
@@ -149,6 +150,11 @@ def gemv_q8_0(qs, d, x=None, xq=None, xd=None, act=QD_ACT_F32, y=None, stream=No
         y = torch.empty(R, dtype=torch.float32, device=qs.device)
     _check(lib().qd_gemv_q8_0(_p(qs), _p(d), R, K, _p(x), _p(xq), _p(xd), act, _p(y), _stream(stream)))
     return y
+
+
+def debug_wait_timeout(limit_us: int, stream=None):
+    """Run a bounded wait that nothing completes (QD_DEVERR_TIMEOUT afterwards)."""
+    _check(lib().qd_debug_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def gemv_w4(W, d, x, y=None, stream=None):

@@ -1267,4 +1267,10 @@ int qd_debug_paged_indices(const int32_t* page_table, int batch, int max_pages, 
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_debug_paged_indices");
 }
 
+int qd_debug_wait_timeout(int limit_us, cudaStream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return fail(QD_ERR_INVALID_ARG, "qd_debug_wait_timeout: limit_us=%d", limit_us);
+  cudaError_t e = launch_wait_timeout(limit_us, make_launch(stream, false));
+  return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_debug_wait_timeout");
+}
+
 }  // extern "C"

@@ -143,17 +143,23 @@ QD_DEV uint64_t global_ns() {
   return t;
 }
 
-// Wait for `phase` of the barrier to complete, giving up after about one
-// second (sets QD_DEVERR_TIMEOUT = 16 and returns false). Never unbounded.
-QD_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, int* err) {
+// Wait for `phase` of the barrier to complete, giving up after limit_ns
+// nanoseconds (or 2^24 polls; sets QD_DEVERR_TIMEOUT = 16 and returns false).
+// Never unbounded.
+QD_DEV bool mbar_wait_limit(uint64_t* bar, uint32_t phase, int* err, uint64_t limit_ns) {
   if (mbar_try_wait(bar, phase)) return true;
   const uint64_t t0 = global_ns();
   for (int i = 0; i < (1 << 24); ++i) {
     if (mbar_try_wait(bar, phase)) return true;
-    if ((i & 255) == 255 && global_ns() - t0 > 1000000000ull) break;
+    if ((i & 255) == 255 && global_ns() - t0 > limit_ns) break;
   }
   set_error(err, QD_DEVERR_TIMEOUT);
   return false;
+}
+
+// The kernels' wait: about one second.
+QD_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, int* err) {
+  return mbar_wait_limit(bar, phase, err, 1000000000ull);
 }
 
 // 2D tiled TMA load of the box at (x, y) of a tensor map into shared memory,

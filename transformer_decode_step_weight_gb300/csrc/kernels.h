@@ -285,6 +285,8 @@ cudaError_t launch_embed(const void* embed, int H, int V, const int32_t* tok, in
 cudaError_t launch_verify_prep(const int32_t* tok, const int32_t* pos, const int32_t* draft, int k,
                                const int32_t* page_table, int max_pages, int32_t* tokens, int32_t* vpos,
                                int32_t* vpt, int32_t* scratch, const Launch& L);
+// A bounded wait that runs out after limit_us (test of the timeout path).
+cudaError_t launch_wait_timeout(int limit_us, const Launch& L);
 cudaError_t launch_verify_accept(const int32_t* draft, const int32_t* target, int k, int32_t* tok, int32_t* pos,
                                  int32_t* step, int32_t* out_tokens, int max_steps, int32_t* n_accept,
                                  const Launch& L);

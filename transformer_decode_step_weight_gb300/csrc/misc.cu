@@ -246,6 +246,23 @@ __global__ void verify_accept_kernel(const int32_t* draft, const int32_t* target
 
 }  // namespace
 
+// A wait that runs out: one thread arms an mbarrier for 16 bytes that no copy will
+// ever deliver (nothing is issued, so nothing is in flight), then waits on it with a
+// limit of limit_us microseconds; the wait gives up, sets QD_DEVERR_TIMEOUT and the
+// kernel returns.
+__global__ void wait_timeout_kernel(int limit_us, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_arrive_expect_tx(&bar, 16);
+  mbar_wait_limit(&bar, 0, err, (uint64_t)limit_us * 1000ull);
+}
+
+cudaError_t launch_wait_timeout(int limit_us, const Launch& L) {
+  return launch_ex(wait_timeout_kernel, dim3(1), dim3(32), 0, L, limit_us, L.err);
+}
+
 cudaError_t launch_verify_prep(const int32_t* tok, const int32_t* pos, const int32_t* draft, int k,
                                const int32_t* page_table, int max_pages, int32_t* tokens, int32_t* vpos,
                                int32_t* vpt, int32_t* scratch, const Launch& L) {
