@@ -135,47 +135,67 @@ __global__ void __launch_bounds__(kPTh) prefill_attn_kernel(const PfParams p) {
   pf_load_tile(p, g, 0, kend, tK(0), tV(0));
   pf_commit();
 
-  // ---- queries: warp w builds rows 16w .. 16w + 15; lane holds dims 4 lane .. + 3
+  // ---- queries: warp w builds rows 16w .. 16w + 15; lane holds dims 4 lane .. + 3.
+  // Four rows at a time: their activations and RoPE rows are all requested before
+  // any is used, so a warp waits for four L2 round trips instead of 32.
   {
     const int qkv_w = (p.Hq + 2 * p.Hkv) * kPD;
     const int d0 = 4 * lane;
     const uint2 wq = *(const uint2*)(p.q_norm + d0);
     const float nw[4] = {bf_lo(wq.x), bf_hi(wq.x), bf_lo(wq.y), bf_hi(wq.y)};
-    for (int rr = 0; rr < 16; ++rr) {
-      const int lr = warp * 16 + rr, row = r0 + lr;
-      float qv[4] = {0.f, 0.f, 0.f, 0.f};
-      if (row < p.n) {
-        const float4 x = *(const float4*)(p.qkv + (size_t)row * qkv_w + (size_t)h * kPD + d0);
-        const float xs[4] = {x.x, x.y, x.z, x.w};
-        const float ss = warp_sum(xs[0] * xs[0] + xs[1] * xs[1] + xs[2] * xs[2] + xs[3] * xs[3]);
-        const float inv = 1.0f / sqrtf(ss / (float)kPD + p.eps);
-        float y[4];
+    constexpr int kRB = 4;
+    for (int rb = 0; rb < 16; rb += kRB) {
+      float4 xr[kRB];
+      float4 cr[kRB][2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float nv = xs[e] * inv;
-          if (p.act_bf16) nv = round_bf16(nv);
-          y[e] = nw[e] * nv;
-          if (p.act_bf16) y[e] = round_bf16(y[e]);
-        }
-        const float2* cs = p.rope + (size_t)(pos0 + row) * (kPD / 2) + (d0 & 63);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float other = __shfl_xor_sync(0xffffffffu, y[e], 16);   // dim d ^ 64
-          const float2 c = cs[e];
-          const float r = lane < 16 ? (y[e] * c.x - other * c.y) : (y[e] * c.x + other * c.y);
-          qv[e] = r * p.scale_log2;
+      for (int i = 0; i < kRB; ++i) {
+        const int row = r0 + warp * 16 + rb + i;
+        if (row < p.n) {
+          xr[i] = *(const float4*)(p.qkv + (size_t)row * qkv_w + (size_t)h * kPD + d0);
+          const float4* cs = (const float4*)(p.rope + (size_t)(pos0 + row) * (kPD / 2) + (d0 & 63));
+          cr[i][0] = cs[0];
+          cr[i][1] = cs[1];
+        } else {
+          xr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          cr[i][0] = cr[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      uint32_t hi[2], lo[2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(qv[2 * e]), h1 = __float2bfloat16_rn(qv[2 * e + 1]);
-        hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lo[e] = pack_bf16(qv[2 * e] - __bfloat162float(h0), qv[2 * e + 1] - __bfloat162float(h1));
+      for (int i = 0; i < kRB; ++i) {
+        const int lr = warp * 16 + rb + i, row = r0 + lr;
+        float qv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row < p.n) {   // uniform over the warp
+          const float xs[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+          const float ss = warp_sum(xs[0] * xs[0] + xs[1] * xs[1] + xs[2] * xs[2] + xs[3] * xs[3]);
+          const float inv = 1.0f / sqrtf(ss / (float)kPD + p.eps);
+          float y[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float nv = xs[e] * inv;
+            if (p.act_bf16) nv = round_bf16(nv);
+            y[e] = nw[e] * nv;
+            if (p.act_bf16) y[e] = round_bf16(y[e]);
+          }
+          const float cc[4][2] = {{cr[i][0].x, cr[i][0].y}, {cr[i][0].z, cr[i][0].w},
+                                  {cr[i][1].x, cr[i][1].y}, {cr[i][1].z, cr[i][1].w}};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float other = __shfl_xor_sync(0xffffffffu, y[e], 16);   // dim d ^ 64
+            const float r = lane < 16 ? (y[e] * cc[e][0] - other * cc[e][1]) : (y[e] * cc[e][0] + other * cc[e][1]);
+            qv[e] = r * p.scale_log2;
+          }
+        }
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(qv[2 * e]), h1 = __float2bfloat16_rn(qv[2 * e + 1]);
+          hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          lo[e] = pack_bf16(qv[2 * e] - __bfloat162float(h0), qv[2 * e + 1] - __bfloat162float(h1));
+        }
+        const uint32_t o = pf_swz(lr, lane >> 1) + (uint32_t)((lane & 1) * 8);
+        *(uint2*)(sQh + o) = make_uint2(hi[0], hi[1]);
+        *(uint2*)(sQl + o) = make_uint2(lo[0], lo[1]);
       }
-      const uint32_t o = pf_swz(lr, lane >> 1) + (uint32_t)((lane & 1) * 8);
-      *(uint2*)(sQh + o) = make_uint2(hi[0], hi[1]);
-      *(uint2*)(sQl + o) = make_uint2(lo[0], lo[1]);
     }
   }
   __syncthreads();
