@@ -136,37 +136,23 @@ QD_DEV void tma_box(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t
       : "memory");
 }
 
-// Issue the TMA copies of one tile's K and V rows [t, t + kT) as 16-row page
-// segments (two 64-column boxes each) onto `bar`; segments at or past
-// t_valid_end are not copied. The page size is a multiple of 16, so a segment
-// never crosses a page. Returns nothing; the expected bytes are set here.
-QD_DEV void load_tile_tma(const MParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int b, int g, int t,
-                          int t_valid_end, uint32_t sK, uint32_t sV, uint64_t* bar) {
-  const int ps = p.page_size;
-  const int32_t* pt = p.page_table + (size_t)b * p.max_pages;
-  int nseg = 0;
-  int rows[kT / 16];
-#pragma unroll
-  for (int k = 0; k < kT / 16; ++k) {
-    const int tok = t + 16 * k;
-    rows[k] = -1;
-    if (tok < t_valid_end) {
-      const PagedSlot sl = paged_slot(pt, tok, ps, p.n_pages);
-      if (!sl.ok) set_error(p.err, QD_DEVERR_PAGE);
-      rows[k] = (sl.page * p.Hkv + g) * ps + sl.slot;
-      ++nseg;
-    }
+// One warp's share of a tile: the 16-row page segment of K and of V starting at token
+// tok0 (two 64-column boxes each) onto the warp's own barrier; a segment at or past
+// t_valid_end is not copied and the barrier completes on the arrival alone.
+QD_DEV void load_seg_tma(const MParams& p, const CUtensorMap* tmK, const CUtensorMap* tmV, int b, int g, int tok0,
+                         int t_valid_end, uint32_t dk, uint32_t dv, uint64_t* bar) {
+  if (tok0 >= t_valid_end) {
+    mbar_arrive(bar);
+    return;
   }
-  mbar_arrive_expect_tx(bar, (uint32_t)nseg * 4 * 16 * 128);
-#pragma unroll
-  for (int k = 0; k < kT / 16; ++k) {
-    if (rows[k] < 0) continue;
-    const uint32_t dk = sK + k * 16 * 128, dv = sV + k * 16 * 128;
-    tma_box(dk, tmK, 0, rows[k], bar);
-    tma_box(dk + kT * 128, tmK, 64, rows[k], bar);
-    tma_box(dv, tmV, 0, rows[k], bar);
-    tma_box(dv + kT * 128, tmV, 64, rows[k], bar);
-  }
+  const PagedSlot sl = paged_slot(p.page_table + (size_t)b * p.max_pages, tok0, p.page_size, p.n_pages);
+  if (!sl.ok) set_error(p.err, QD_DEVERR_PAGE);
+  const int row = (sl.page * p.Hkv + g) * p.page_size + sl.slot;
+  mbar_arrive_expect_tx(bar, 4 * 16 * 128);
+  tma_box(dk, tmK, 0, row, bar);
+  tma_box(dk + kT * 128, tmK, 64, row, bar);
+  tma_box(dv, tmV, 0, row, bar);
+  tma_box(dv + kT * 128, tmV, 64, row, bar);
 }
 
 template <int REP, bool FUSED, int kSt, bool TMA>
@@ -183,9 +169,14 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
   float* sM = sQf + REP * kD;                                          // [kW][8]
   float* sL = sM + kW * kHP;                                           // [kW][8]
   float* sRed = sL + kW * kHP;                                         // scratch [4][REP + 1]
-  uint64_t* bars = (uint64_t*)(((uintptr_t)(sRed + 4 * 9) + 7) & ~(uintptr_t)7);  // TMA: full[kSt]
+  // TMA: full[kSt][kW], one barrier per stage and warp (each warp loads and reads its
+  // own 16-token segment of every tile, so the warps never wait for one another)
+  uint64_t* bars = (uint64_t*)(((uintptr_t)(sRed + 4 * 9) + 7) & ~(uintptr_t)7);
   __shared__ int s_ticket;
+  __shared__ int s_fail;
   __shared__ float s_x[kD];
+  __shared__ __align__(16) __nv_bfloat16 s_knew[kD];
+  __shared__ __align__(16) __nv_bfloat16 s_vnew[kD];
 
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -229,12 +220,15 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
   // ---- start streaming the first tiles, then wait for and build q (and the new k, v)
   if constexpr (TMA) {
     if (tid == 0) {
-      for (int st = 0; st < kSt; ++st) mbar_init(&bars[st], 1);
+      for (int e = 0; e < kSt * kW; ++e) mbar_init(&bars[e], 1);
       fence_mbar_init();
-      for (int st = 0; st < kSt - 1 && st < n_tiles; ++st)
-        load_tile_tma(p, &tmK, &tmV, b, g, t0 + st * kT, t_end, tileK(st), tileV(st), &bars[st]);
+      s_fail = 0;
     }
-    __syncthreads();  // the barriers are initialised before anyone waits on them
+    __syncthreads();  // the barriers are initialised before anyone issues or waits
+    if (lane == 0)
+      for (int st = 0; st < kSt - 1 && st < n_tiles; ++st)
+        load_seg_tma(p, &tmK, &tmV, b, g, t0 + st * kT + 16 * warp, t_end, tileK(st) + warp * 16 * 128,
+                     tileV(st) + warp * 16 * 128, &bars[st * kW + warp]);
   } else {
 #pragma unroll
     for (int st = 0; st < kSt - 1; ++st) {
@@ -297,6 +291,8 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
     if (own_pos) {
       k_new = round_bf16(r[REP]);
       v_new = round_bf16(vx);
+      s_knew[tid] = __float2bfloat16_rn(k_new);
+      s_vnew[tid] = __float2bfloat16_rn(v_new);
       const PagedSlot own = paged_slot(p.page_table + (size_t)b * p.max_pages, pos, p.page_size, p.n_pages);
       if (!own.ok) {
         if (tid == 0) set_error(p.err, QD_DEVERR_PAGE);
@@ -349,25 +345,36 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
     const int st = it % kSt;
     const int ts = t0 + it * kT;
     if constexpr (TMA) {
-      const int nt = it + kSt - 1;   // keep kSt - 1 tiles in flight
-      if (tid == 0 && nt < n_tiles) {
-        fence_proxy_async_smem();    // the stage's earlier reads come before the copies
-        load_tile_tma(p, &tmK, &tmV, b, g, t0 + nt * kT, t_end, tileK(nt % kSt), tileV(nt % kSt), &bars[nt % kSt]);
+      const int nt = it + kSt - 1;   // keep kSt - 1 tiles in flight, this warp's segments only
+      if (lane == 0 && nt < n_tiles) {
+        fence_proxy_async_smem();    // the warp's earlier reads and writes of the stage come first
+        load_seg_tma(p, &tmK, &tmV, b, g, t0 + nt * kT + 16 * warp, t_end, tileK(nt % kSt) + warp * 16 * 128,
+                     tileV(nt % kSt) + warp * 16 * 128, &bars[(nt % kSt) * kW + warp]);
       }
-      const bool got = mbar_wait_bounded(&bars[st], (uint32_t)((it / kSt) & 1), p.err);
-      if (ts + kT > t_end) {  // rows past the sequence: whole 16-row boxes may hold any bits
-        const int nv = max(0, t_end - ts);
-        unsigned char* sVg = ring + st * 2 * kTileBytes + kTileBytes;
-        for (int e = tid; e < (kT - nv) * 16; e += kTh) {
-          const int r = nv + (e >> 4), c = e & 15;
+      const bool got = mbar_wait_bounded(&bars[st * kW + warp], (uint32_t)((it / kSt) & 1), p.err);
+      if (!__all_sync(0xffffffffu, got)) {  // a copy never arrived: let this warp's others land, then stop
+        for (int k = 1; k < kSt && it + k < n_tiles; ++k)
+          mbar_wait_bounded(&bars[((it + k) % kSt) * kW + warp], (uint32_t)(((it + k) / kSt) & 1), p.err);
+        if (lane == 0) s_fail = 1;
+        break;
+      }
+      unsigned char* sVg = ring + st * 2 * kTileBytes + kTileBytes;
+      const int rw = warp * 16;      // this warp's rows of the tile
+      if (ts + rw + 16 > t_end) {    // its rows past the sequence: V zeroed (K rows are masked)
+        const int r_lo = max(rw, t_end - ts);
+        for (int e = lane; e < (rw + 16 - r_lo) * 16; e += 32) {
+          const int r = r_lo + (e >> 4), c = e & 15;
           *(uint4*)(sVg + swz_tma(r, c)) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (!__syncthreads_and(got)) {  // a copy never arrived: let the others land, then leave
-        for (int k = 1; k < kSt && it + k < n_tiles; ++k)
-          mbar_wait_bounded(&bars[(it + k) % kSt], (uint32_t)(((it + k) / kSt) & 1), p.err);
-        return;
+      if (own_pos && pos >= ts + rw && pos < ts + rw + 16) {  // the current token's row, from registers
+        const int r = pos - ts;
+        const int d0 = 4 * lane;
+        const uint32_t o16 = swz_tma(r, d0 >> 3) + (uint32_t)((d0 & 7) * 2);
+        *(uint2*)(ring + st * 2 * kTileBytes + o16) = *(const uint2*)(s_knew + d0);
+        *(uint2*)(sVg + o16) = *(const uint2*)(s_vnew + d0);
       }
+      __syncwarp();
     } else {
       {  // keep kSt - 1 tiles in flight
         const int nt = it + kSt - 1;
@@ -376,13 +383,13 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
       }
       cp_async_wait<kSt - 1>();
       __syncthreads();  // every thread's copies of this tile have landed
-    }
-    if (own_pos && pos >= ts && pos < ts + kT) {  // the current token's row, swizzled like the copies
-      const int r = pos - ts;
-      const uint32_t o16 = swz_t<TMA>(r, tid >> 3) + (uint32_t)((tid & 7) * 2);
-      *(__nv_bfloat16*)(ring + st * 2 * kTileBytes + o16) = __float2bfloat16_rn(k_new);
-      *(__nv_bfloat16*)(ring + st * 2 * kTileBytes + kTileBytes + o16) = __float2bfloat16_rn(v_new);
-      __syncthreads();
+      if (own_pos && pos >= ts && pos < ts + kT) {  // the current token's row, swizzled like the copies
+        const int r = pos - ts;
+        const uint32_t o16 = swz(r, tid >> 3) + (uint32_t)((tid & 7) * 2);
+        *(__nv_bfloat16*)(ring + st * 2 * kTileBytes + o16) = __float2bfloat16_rn(k_new);
+        *(__nv_bfloat16*)(ring + st * 2 * kTileBytes + kTileBytes + o16) = __float2bfloat16_rn(v_new);
+        __syncthreads();
+      }
     }
 
     // ---- S^T = K . Q^T for this warp's 16 tokens
@@ -460,9 +467,14 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
       mma16816(o[mt], a, pb0l, pb1l);
     }
     __syncwarp();
-    __syncthreads();  // the stage is refilled by the next iteration's copies
+    if constexpr (!TMA) __syncthreads();  // the stage is refilled by the next iteration's copies
   }
-  if constexpr (!TMA) cp_async_wait<0>();
+  if constexpr (!TMA) {
+    cp_async_wait<0>();
+  } else {
+    __syncthreads();  // every warp has left the ring, its copies all landed, before the ring is reused
+    if (s_fail) return;
+  }
   pdl_launch_dependents();
 
   // ---- merge the four warps: O^T fragments -> [warp][head][dim] f32 (ring is idle now)
@@ -579,7 +591,7 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
 
 constexpr size_t smem_bytes(int rep, int kSt) {
   return 1024 + (size_t)kSt * 2 * kTileBytes + 2 * kHP * kD * 2 + (size_t)kW * 2 * kHP * 16 * 2 +
-         (size_t)rep * kD * 4 + 2 * kW * kHP * 4 + 4 * 9 * 4 + 64 + (size_t)kSt * 8;
+         (size_t)rep * kD * 4 + 2 * kW * kHP * 4 + 4 * 9 * 4 + 64 + (size_t)kSt * kW * 8;
 }
 
 // QD_ATTN_TMA=0 keeps the cp.async loads on every page size.
