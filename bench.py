@@ -472,9 +472,15 @@ def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
     mats.append((mt.lm_head, mt.lm_head_scales, xh[0] if w4 else xh))
     ys = {id(w): torch.empty((1, w.shape[0]), dtype=torch.float32, device=x.device) for w, _, _ in mats}
 
+    w4ws = {}
+    if w4:   # the step's split-K workspace, one per shape
+        for w, _, _ in mats:
+            nb = api.gemv_w4_workspace_bytes(w.shape[0], 2 * w.shape[1])
+            w4ws[tuple(w.shape)] = torch.zeros(max(nb, 16), dtype=torch.uint8, device=x.device) if nb else None
+
     def run(w, sc, xx):
         if w4:
-            api.gemv_w4(w, sc, xx, ys[id(w)][0], stream=stream)
+            api.gemv_w4(w, sc, xx, ys[id(w)][0], workspace=w4ws[tuple(w.shape)], stream=stream)
         else:
             api.gemv_bf16(w, xx, ys[id(w)], stream=stream)
 
@@ -671,7 +677,9 @@ def run_kernel(args):
         y = torch.empty(R, device=dev)
         nbytes = R * K // 2 + R * 2
         if args.kernel == "gemv_w4":
-            fn = lambda i: api.gemv_w4(Ws[i % copies], ds[i % copies], x, y, stream=stream)  # noqa: E731
+            wsb = api.gemv_w4_workspace_bytes(R, K)
+            w4ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev) if wsb else None
+            fn = lambda i: api.gemv_w4(Ws[i % copies], ds[i % copies], x, y, workspace=w4ws, stream=stream)  # noqa
         else:
             ws = torch.zeros(int(api.lib().qd_w4_topk_workspace_bytes()), dtype=torch.uint8, device=dev)
             fn = lambda i: api.gemv_w4_topk(Ws[i % copies], ds[i % copies], x, 8, y, ws, stream=stream)  # noqa

@@ -135,6 +135,15 @@ int qd_gemm_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const 
 /* W and x 16-byte aligned, d 2-byte aligned.                                      */
 int qd_gemv_w4(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, float* y,
                cudaStream_t stream);
+/* The same with a workspace: with cols % 256 == 0 the product runs on the tcgen05  */
+/* tensor cores (each weight code widened to bf16 in tensor memory, the activation */
+/* as the other operand), and a matrix whose 128-row tiles underfill the SMs      */
+/* splits K across CTAs, adding the partials in split order. workspace: NULL (no  */
+/* split; what qd_gemv_w4 does) or zero-filled device scratch of                  */
+/* qd_gemv_w4_workspace_bytes(rows, cols) bytes (0: no split), left zero-filled.  */
+size_t qd_gemv_w4_workspace_bytes(int rows, int cols);
+int qd_gemv_w4_ex(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, float* y,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
 /* The INT4 LM-head form: y as qd_gemv_w4 (the logits), and the top k rows of y     */
 /* (value descending, the lower row first among equal values, NaN never chosen):  */
 /* topk_ids int32 [k] (-1 past the non-NaN rows), topk_vals f32 [k]. Each CTA picks */

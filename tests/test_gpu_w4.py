@@ -17,6 +17,14 @@ DEV = "cuda"
 GEMV_TOL = 2e-5
 
 
+@pytest.fixture(params=["mma", "tc"], autouse=True)
+def w4_impl(request, monkeypatch):
+    """Every test runs on both INT4 forms: mma.sync (the default) and tcgen05 (K a
+    multiple of 256; the library reads QD_W4_IMPL on every call)."""
+    monkeypatch.setenv("QD_W4_IMPL", request.param)
+    return request.param
+
+
 def _w4(R, K, seed):
     g = torch.Generator(device=DEV)
     g.manual_seed(seed)
@@ -34,6 +42,23 @@ def test_gemv_w4(cuda_lib, R, K):
     y = api.gemv_w4(W, d, x)
     ref = oracle.gemv_w4(synth.host_u8(W), synth.bits_u16(d), oracle.bf16_to_f64(synth.bits_u16(x)))
     assert rel_max_abs(y.cpu().numpy(), ref) < GEMV_TOL
+
+
+@pytest.mark.parametrize("R,K", [(37, 1024), (4096, 4096), (6144, 4096), (4096, 12288), (300, 16384),
+                                 (1000, 256)])
+def test_gemv_w4_split_k(cuda_lib, R, K):
+    # the tcgen05 form with a workspace: tiles that underfill the SMs split K, the last
+    # split adds the partials in split order; two calls (the tickets are left at zero)
+    W, d, x = _w4(R, K, 3 * R + K)
+    nbytes = api.gemv_w4_workspace_bytes(R, K)
+    ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=DEV)
+    y1 = api.gemv_w4(W, d, x, workspace=ws)
+    y2 = api.gemv_w4(W, d, x, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    ref = oracle.gemv_w4(synth.host_u8(W), synth.bits_u16(d), oracle.bf16_to_f64(synth.bits_u16(x)))
+    assert rel_max_abs(y1.cpu().numpy(), ref) < GEMV_TOL
+    assert api.check_device_error() == 0
 
 
 def test_gemv_w4_rejects_unsupported_k(cuda_lib):

@@ -83,6 +83,8 @@ _SIGS = {
     "qd_prefill_workspace_bytes": (_sz, [C.POINTER(StepArgs), _i]),
     "qd_prefill": (_i, [C.POINTER(StepArgs), _vp, _i, _vp, _vp]),
     "qd_debug_wait_timeout": (_i, [_i, _vp]),
+    "qd_gemv_w4_workspace_bytes": (_sz, [_i, _i]),
+    "qd_gemv_w4_ex": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "qd_debug_q8_block_dots": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "qd_debug_paged_indices": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp]),
 }
@@ -157,12 +159,21 @@ def debug_wait_timeout(limit_us: int, stream=None):
     _check(lib().qd_debug_wait_timeout(int(limit_us), _stream(stream)))
 
 
-def gemv_w4(W, d, x, y=None, stream=None):
-    """y = (d * q) @ x; W packed uint8 [R, K / 2], d f16 [R], x bf16 [K] -> f32 [R]."""
+def gemv_w4_workspace_bytes(R: int, K: int) -> int:
+    return int(lib().qd_gemv_w4_workspace_bytes(R, K))
+
+
+def gemv_w4(W, d, x, y=None, workspace=None, stream=None):
+    """y = (d * q) @ x; W packed uint8 [R, K / 2], d f16 [R], x bf16 [K] -> f32 [R].
+    `workspace` (zero-filled uint8, gemv_w4_workspace_bytes) lets small matrices split K."""
     R, Kh = W.shape
     if y is None:
         y = torch.empty(R, dtype=torch.float32, device=W.device)
-    _check(lib().qd_gemv_w4(_p(W), _p(d), R, 2 * Kh, _p(x), _p(y), _stream(stream)))
+    if workspace is None:
+        _check(lib().qd_gemv_w4(_p(W), _p(d), R, 2 * Kh, _p(x), _p(y), _stream(stream)))
+    else:
+        _check(lib().qd_gemv_w4_ex(_p(W), _p(d), R, 2 * Kh, _p(x), _p(y), _p(workspace), workspace.numel(),
+                                   _stream(stream)))
     return y
 
 

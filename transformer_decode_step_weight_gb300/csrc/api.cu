@@ -235,17 +235,29 @@ int qd_gemv_q8_0(const int8_t* qs, const void* d_f16, int rows, int cols, const 
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_q8_0");
 }
 
-int qd_gemv_w4(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, float* y,
-               cudaStream_t stream) {
+size_t qd_gemv_w4_workspace_bytes(int rows, int cols) {
+  if (rows < 1 || !gemv_w4_tc_supported(cols)) return 0;
+  return gemv_w4_tc_workspace_bytes(rows, cols, false);
+}
+
+int qd_gemv_w4_ex(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, float* y,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!W || !d_f16 || !x_bf16 || !y) return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4: null pointer");
   if (rows < 1 || !gemv_w4_supported(cols))
     return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4: rows=%d cols=%d (cols %% 32 == 0, <= 16384)", rows, cols);
-  if (!aligned16(W) || !aligned16(x_bf16) || !aligned16(y) || ((uintptr_t)d_f16 & 1u))
+  if (!aligned16(W) || !aligned16(x_bf16) || !aligned16(y) || ((uintptr_t)d_f16 & 1u) ||
+      (workspace && !aligned16(workspace)))
     return fail(QD_ERR_INVALID_ARG, "qd_gemv_w4: alignment");
   GemvW4Args g = {};
   g.W = W; g.d = d_f16; g.R = rows; g.K = cols; g.pro = PRO_X_BF16; g.x = x_bf16; g.epi = EPI_STORE; g.y = y;
+  g.split_ws = workspace; g.split_ws_bytes = workspace ? workspace_bytes : 0;
   cudaError_t e = launch_gemv_w4(g, make_launch(stream, false));
   return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_w4");
+}
+
+int qd_gemv_w4(const uint8_t* W, const void* d_f16, int rows, int cols, const void* x_bf16, float* y,
+               cudaStream_t stream) {
+  return qd_gemv_w4_ex(W, d_f16, rows, cols, x_bf16, y, nullptr, 0, stream);
 }
 
 size_t qd_w4_topk_workspace_bytes(void) { return w4_topk_workspace_bytes(); }
@@ -463,6 +475,8 @@ struct StepWs {
   size_t gemm_ws_bytes;
   void* stream_ws;  // batch-1 BF16: the persistent step kernel's partials, counters, candidates
   void* topk_ws;    // INT4 LM head: top-k candidates and ticket
+  void* w4_ws;      // INT4 layers: split-K partials and tickets of the tcgen05 GEMVs (one at a time)
+  size_t w4_ws_bytes;
   size_t total;
 };
 
@@ -511,6 +525,15 @@ StepWs step_ws_layout_for(const qd_step_args* a, void* base, bool gemm_path) {
   if (a->batch == 1 && d.wtype == QD_W_BF16) off += al256(stream_ws_bytes(a->n_layers, d.n_q_heads, d.n_kv_heads));
   w.topk_ws = (void*)(p + off);
   if (lm_is_w4(a)) off += al256(w4_topk_workspace_bytes());
+  w.w4_ws = (void*)(p + off);
+  w.w4_ws_bytes = 0;
+  if (d.wtype == QD_W_INT4) {
+    const int shapes[4][3] = {{(int)qkv, d.hidden, 0}, {d.hidden, d.n_q_heads * d.head_dim, 0},
+                              {2 * d.ffn, d.hidden, 1}, {d.hidden, d.ffn, 0}};
+    for (const auto& sh : shapes)
+      w.w4_ws_bytes = std::max(w.w4_ws_bytes, gemv_w4_tc_workspace_bytes(sh[0], sh[1], sh[2] != 0));
+  }
+  off += al256(w.w4_ws_bytes);
   w.total = off;
   return w;
 }
@@ -698,6 +721,7 @@ int run_step_w4(const qd_step_args* a, cudaStream_t stream) {
     GemvW4Args g = {};
     g.W = W; g.d = S; g.R = R; g.K = K; g.pro = pro; g.x = x; g.norm_w = nw; g.eps = d.rms_eps; g.epi = epi;
     g.y = y; g.y_bf16 = y_bf16; g.w_evict_first = wef;
+    g.split_ws = w.w4_ws; g.split_ws_bytes = w.w4_ws_bytes;
     return launch_gemv_w4(g, L);
   };
   QD_TRY(launch_embed(a->embed, H, a->vocab, a->tok, 1, w.res, L), "embed");

@@ -524,6 +524,11 @@ cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint
   return encode_rowmajor_bf16((CUtensorMap*)map, base, rows, cols, box_rows);
 }
 
+cudaError_t encode_tmap_u8_sw128(void* map, const void* base, uint64_t rows, uint64_t cols_bytes, uint32_t box_rows) {
+  return encode_rowmajor((CUtensorMap*)map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols_bytes, 128, box_rows,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool gemm_tc_supported(int R, int K, int B) { return R >= 1 && K >= kBK && K % kBK == 0 && B >= 1 && B <= kBN; }
 
 // Many rows (prefill): 64-token tiles over grid z, no K split.

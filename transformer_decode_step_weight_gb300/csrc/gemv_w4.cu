@@ -475,6 +475,8 @@ size_t w4_topk_workspace_bytes() {
 }
 
 cudaError_t launch_gemv_w4(const GemvW4Args& a, const Launch& L) {
+  // K a multiple of 256: the tcgen05 form (gemv_w4_tc.cu); this form covers the rest
+  if (gemv_w4_tc_supported(a.K)) return launch_gemv_w4_tc(a, a.split_ws, a.split_ws_bytes, L);
   if (!gemv_w4_supported(a.K) || a.R < 1) return cudaErrorInvalidValue;
   const bool pair = a.epi == EPI_SWIGLU, topk = a.epi == EPI_TOPK;
   if (pair && a.R % 2) return cudaErrorInvalidValue;

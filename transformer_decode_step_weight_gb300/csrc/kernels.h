@@ -99,10 +99,20 @@ struct GemvW4Args {
   int max_steps;
   int32_t* topk_ids;
   float* topk_vals;
+  void* split_ws;         // tcgen05 form: split-K partials and tickets (null: no split)
+  size_t split_ws_bytes;
 };
 bool gemv_w4_supported(int K);
 size_t w4_topk_workspace_bytes();
 cudaError_t launch_gemv_w4(const GemvW4Args& a, const Launch& L);
+// The tcgen05 form (gemv_w4_tc.cu): K % 256 == 0, K <= 16384. `ws` (zero-filled
+// before first use, left so) lets tiles that underfill the SMs split K; null: no split.
+bool gemv_w4_tc_supported(int K);
+size_t gemv_w4_tc_workspace_bytes(int R, int K, bool pair);
+cudaError_t launch_gemv_w4_tc(const GemvW4Args& a, void* ws, size_t ws_bytes, const Launch& L);
+// Tensor map of a row-major uint8 [rows, cols_bytes] matrix: boxes of 128 bytes x
+// box_rows rows, 128-byte swizzle (CUtensorMap storage, 128 bytes, 128-byte aligned).
+cudaError_t encode_tmap_u8_sw128(void* map, const void* base, uint64_t rows, uint64_t cols_bytes, uint32_t box_rows);
 
 // ----------------------------------------------------------------- batched GEMM (tcgen05)
 struct GemmTcArgs {
