@@ -610,11 +610,8 @@ __global__ void __launch_bounds__(threads_for(REP)) attn_kernel(const AttnParams
     p.ws_ml[(slot * REP + tid) * 2 + 1] = sRun[8 + tid];
   }
   __syncthreads();  // every thread's share of the partial is written
-  if (tid == 0) {   // release the CTA's writes, take a ticket, acquire the others'
-    __threadfence();
-    s_ticket = atomicAdd(p.ws_cnt + (size_t)b * p.Hkv + g, 1);
-    __threadfence();
-  }
+  if (tid == 0)     // release the CTA's writes, take a ticket, acquire the others' (one round trip)
+    s_ticket = atom_add_acq_rel_gpu(p.ws_cnt + (size_t)b * p.Hkv + g, 1);
   __syncthreads();
   if (s_ticket != n_act - 1) return;
 

@@ -534,13 +534,10 @@ __global__ void __launch_bounds__(kTh) attn_mma_kernel(const __grid_constant__ C
     p.ws_ml[(slot * REP + tid) * 2 + 1] = LL[tid];
   }
   __syncthreads();
-  if (tid == 0) {  // the fence is cumulative over the CTA's writes ordered by the barrier
-    __threadfence();
-    s_ticket = atomicAdd(p.ws_cnt + (size_t)b * p.Hkv + g, 1);
-  }
+  if (tid == 0)  // release the CTA's writes (ordered by the barrier), acquire the others', one round trip
+    s_ticket = atom_add_acq_rel_gpu(p.ws_cnt + (size_t)b * p.Hkv + g, 1);
   __syncthreads();
   if (s_ticket != n_act - 1) return;
-  __threadfence();
 
   float* sW = (float*)ring + kW * kHP * kD;   // [kMaxSplitsM][REP] weights, then [REP] totals
   float* sLk = sW + kMaxSplitsM * REP;

@@ -157,6 +157,15 @@ QD_DEV bool mbar_wait_limit(uint64_t* bar, uint32_t phase, int* err, uint64_t li
   return false;
 }
 
+// Add with acquire-release semantics at GPU scope: one round trip that publishes
+// this thread's earlier writes (and, after a CTA barrier, the CTA's) and makes the
+// writes published before the other arrivals visible to it.
+QD_DEV int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // The kernels' wait: about one second.
 QD_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, int* err) {
   return mbar_wait_limit(bar, phase, err, 1000000000ull);

@@ -586,9 +586,10 @@ static int ring_c(int K) {
 // QD_GEMV_SMEM_PAD_KB override the ring size / add padding (tuning);
 // QD_GEMV_RING=0 selects the register-streaming kernel.
 struct RingTuning {
-  int enabled = 1, ring_kb = 128, pad_kb = 0;
+  int enabled = 1, ring_kb = 128, pad_kb = 0, one_per_sm = 1;
   RingTuning() {
     if (const char* v = getenv("QD_GEMV_RING")) enabled = atoi(v) != 0;
+    if (const char* v = getenv("QD_GEMV_ONE_PER_SM")) one_per_sm = atoi(v) != 0;
     if (const char* v = getenv("QD_GEMV_SMEM_PAD_KB")) pad_kb = std::max(0, std::min(64, atoi(v)));
     if (const char* v = getenv("QD_GEMV_RING_KB")) ring_kb = std::max(16, std::min(kRingMax / 1024, atoi(v)));
   }
@@ -653,7 +654,7 @@ cudaError_t launch_gemv_bf16(const GemvBf16Args& a, const Launch& L) {
     size_t smem = (size_t)p.ring_bytes + 32 * 8 + (size_t)kPhaseRows * (p.T / 32) * 4 + (size_t)tu.pad_kb * 1024;
     if (pair) smem += (size_t)2 * (p.rows_base + 1) * 4;
     if (smem > (size_t)dev_info().max_smem_optin - 1024) return cudaErrorInvalidValue;
-    smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
+    if (tu.one_per_sm) smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
     switch (rc) {
       case 1: return launch_ring_c<1>(p, grid, smem, L);
       case 2: return launch_ring_c<2>(p, grid, smem, L);
