@@ -43,7 +43,7 @@ def _check_kv(mt, ks, vs, p, n, tol=2e-2):
             assert rel_max_abs(got[:, p:p + n], ref[:, p:p + n]) < tol, li
 
 
-@pytest.mark.parametrize("n", [1, 63, 130])
+@pytest.mark.parametrize("n", [1, 63, 130, 1030])
 def test_prefill_bf16(cuda_lib, parity_log, n):
     mt = synth.make_model(synth.SMALL64, "bf16", 60 + n, DEV, ctx=37, steps=n + 4)
     om = oracle_model(mt)

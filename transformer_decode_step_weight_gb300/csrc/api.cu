@@ -1136,9 +1136,15 @@ int run_prefill(const qd_step_args* a, const int32_t* tokens, int n, float* logi
     QD_TRY(launch_prefill_attention(at, L), "prefill attention");
     QD_TRY(gemm(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, n, EPI_RESID_ADD, w.res), "o gemm");
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, n, H, d.rms_eps, w.xn, L), "rmsnorm");
-    QD_TRY(gemm(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, n, EPI_STORE, w.gu), "gu gemm");
-    QD_TRY(launch_swiglu_rows(w.gu, n, F, w.xn, L), "swiglu");
-    QD_TRY(gemm(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, n, EPI_RESID_ADD, w.res), "down gemm");
+    if (!q8 && gemm_tc_swiglu_supported(F, H, n)) {  // SwiGLU in the gate+up GEMM's epilogue
+      // h (bf16 [n, F]) goes where the f32 gate/up rows would have gone
+      QD_TRY(launch_gemm_tc_swiglu(l->w.w_gu, w.xn, F, H, n, w.gu, L), "gu swiglu gemm");
+      QD_TRY(gemm(l->w.w_down, nullptr, H, F, w.gu, n, EPI_RESID_ADD, w.res), "down gemm");
+    } else {
+      QD_TRY(gemm(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, n, EPI_STORE, w.gu), "gu gemm");
+      QD_TRY(launch_swiglu_rows(w.gu, n, F, w.xn, L), "swiglu");
+      QD_TRY(gemm(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, n, EPI_RESID_ADD, w.res), "down gemm");
+    }
   }
   // the last row alone goes through the final norm, the LM head and the argmax advance
   QD_TRY(launch_rmsnorm_rows(w.res + (size_t)(n - 1) * H, a->final_norm, 1, H, d.rms_eps, w.xn, L), "final rmsnorm");

@@ -136,6 +136,10 @@ cudaError_t encode_tmap_bf16_2d(void* map, const void* base, uint64_t rows, uint
 int gemm_tc_splits(int R, int K, bool q8 = false);
 size_t gemm_tc_workspace_bytes(int R, int K, bool q8 = false);
 cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L);
+// Prefill gate+up (BF16, more than 128 rows): h[t, j] = bf16(silu(g) u) with g = row j
+// and u = row F + j of W [2F, K] applied to X [B, K] bf16, written to h [B, F] bf16.
+bool gemm_tc_swiglu_supported(int F, int K, int B);
+cudaError_t launch_gemm_tc_swiglu(const void* W, const void* X, int F, int K, int B, void* h, const Launch& L);
 
 // row-wise helpers of the batched step
 cudaError_t launch_rmsnorm_rows(const float* x, const void* w, int B, int K, float eps, void* out_bf16,
