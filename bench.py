@@ -654,9 +654,11 @@ def run_kernel(args):
     stream = torch.cuda.Stream(device=dev)
     copies = max(1, min(4, int(2 * 129e6 // max(1, R * K)) + 1))
     if args.kernel == "gemv_bf16":
+        # --batch 1..8: x rows of the CUDA-core GEMV (larger batches take the tensor cores)
+        nb = args.batch if 1 <= args.batch <= 8 else 1
         Ws = [(torch.randn((R, K), generator=g, device=dev) * 0.02).to(torch.bfloat16) for _ in range(copies)]
-        x = torch.randn((1, K), generator=g, device=dev).to(torch.bfloat16)
-        y = torch.empty((1, R), device=dev)
+        x = torch.randn((nb, K), generator=g, device=dev).to(torch.bfloat16)
+        y = torch.empty((nb, R), device=dev)
         nbytes = R * K * 2
         fn = lambda i: api.gemv_bf16(Ws[i % copies], x, y, stream=stream)  # noqa: E731
     elif args.kernel in ("gemv_q8_f32", "gemv_q8_i8"):
