@@ -263,8 +263,11 @@ int qd_destroy_layer(qd_layer* layer);
 /* rope_table: from qd_rope_table_init with max_pos >= every position reached.  */
 /* logits: f32 [batch, vocab] device output. workspace: device scratch of        */
 /* qd_step_workspace_bytes(args) bytes, zero-filled before first use.           */
-/* BF16 layers: batch <= 8 runs the GEMV path; 9..64 runs every projection as a  */
-/* tcgen05 GEMM over the batch (dims % 64 == 0). Q8_0 layers: batch 1 runs the   */
+/* BF16 layers: batch 1..2 runs the GEMV path (batch 2: K <= 12288); 3..64 runs  */
+/* every projection as a tcgen05 GEMM over the batch when hidden, n_q_heads *    */
+/* head_dim and ffn are multiples of 64 (else batch <= 8 stays on the GEMV path; */
+/* the environment variable QD_TC_MIN_BATCH moves the lower bound, minimum 2).   */
+/* Q8_0 layers: batch 1 runs the                                                 */
 /* Q8_0 GEMV lanes (act, lm_act); 2..64 runs the tcgen05 GEMMs with the weights  */
 /* widened to bf16 as in qd_gemm_q8_0 (act and lm_act unused; dims % 256 == 0,   */
 /* scales 16-byte aligned). INT4 layers: batch 1, the W4A16 GEMVs with bf16      */

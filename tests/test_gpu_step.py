@@ -60,9 +60,10 @@ def test_small_bf16_batch_paged_teacher_forced(cuda_lib):
     assert api.check_device_error() == 0
 
 
-@pytest.mark.parametrize("batch", [12, 64])
+@pytest.mark.parametrize("batch", [3, 8, 12, 64])
 def test_batched_tensor_core_step_teacher_forced(cuda_lib, batch):
-    # 9..64 sequences: projections on tcgen05, paged KV through a random page table
+    # 3..64 sequences (dims multiples of 64): projections on tcgen05, paged KV through
+    # a random page table
     mt = synth.make_model(synth.SMALL64, "bf16", 7, DEV, batch=batch, ctx=None, steps=3, paged=True)
     om = oracle_model(mt)
     check = sorted({0, batch // 3, batch - 1})

@@ -486,10 +486,22 @@ bool lm_is_q8(const qd_step_args* a) { return a->lm_head_scales != nullptr && !l
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// The tensor-core step: BF16 models from batch 9, Q8_0 models from batch 2 (the
-// Q8_0 GEMV lanes take one activation vector).
+// The tensor-core step: BF16 models from batch 3, Q8_0 models from batch 2 (the
+// Q8_0 GEMV lanes take one activation vector). The batch 2..8 CUDA-core GEMV
+// streams 3.84 / 2.67 / 0.96 TB/s at batch 2 / 4 / 8 against ~3.9 for the tcgen05
+// GEMM, and its K limit rejects the 12288-wide down projection above batch 2
+// (Qwen3-8B step at batch 2: 432 tok/s GEMV, 422 tensor cores). QD_TC_MIN_BATCH
+// moves the boundary.
 bool tc_step(const qd_step_args* a) {
-  return a->batch > 8 || (a->layers[0]->dims.wtype == QD_W_Q8_0 && a->batch > 1);
+  static const int min_b = [] {
+    const char* v = getenv("QD_TC_MIN_BATCH");
+    return v ? std::max(2, atoi(v)) : 3;
+  }();
+  const qd_layer_dims& d = a->layers[0]->dims;
+  if (d.wtype == QD_W_Q8_0) return a->batch > 1;
+  if (a->batch > 8) return true;
+  // batch min_b .. 8: the tensor cores where their K rule holds, else the GEMV
+  return a->batch >= min_b && d.hidden % 64 == 0 && (d.n_q_heads * d.head_dim) % 64 == 0 && d.ffn % 64 == 0;
 }
 
 StepWs step_ws_layout_for(const qd_step_args* a, void* base, bool gemm_path);
@@ -602,9 +614,9 @@ int validate_step(const qd_step_args* a) {
   if (d0.wtype == QD_W_BF16) {
     const int ks[3] = {d0.hidden, d0.n_q_heads * d0.head_dim, d0.ffn};
     for (int k : ks) {
-      if (a->batch <= 8 && !gemv_bf16_supported(k, a->batch))
+      if (!tc_step(a) && !gemv_bf16_supported(k, a->batch))
         return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: GEMV K=%d with batch %d not supported", k, a->batch);
-      if (a->batch > 8 && !gemm_tc_supported(1, k, a->batch))
+      if (tc_step(a) && !gemm_tc_supported(1, k, a->batch))
         return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batched K=%d must be a multiple of 64", k);
     }
   }
