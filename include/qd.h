@@ -88,8 +88,11 @@ int qd_version(void);
 /* W: bf16 [rows, cols]. x: bf16 [batch, cols] (x_is_f32 = 0) or f32            */
 /* [batch, cols] (x_is_f32 = 1; the kernel rounds x to bf16 first). y: f32      */
 /* [batch, rows]. Accumulation in f32, deterministic order.                   */
-/* batch <= 8: CUDA-core GEMV (cols % 8 == 0). batch >= 9: the product is a    */
-/* dense contraction and runs on the tcgen05 tensor cores ("qwen3-8b-rtx4080-   */
+/* batch 1: CUDA-core ring GEMV (cols % 8 == 0). batch 2..8 with bf16 x and     */
+/* cols % 32 == 0: the weight-streaming GEMV with its multiply-add on mma.sync   */
+/* (each weight read once for all rows); otherwise batch <= 8 runs the CUDA-core */
+/* GEMV (QD_SMALLB_IMPL=simt forces it). batch >= 9: the product is a dense     */
+/* contraction and runs on the tcgen05 tensor cores ("qwen3-8b-rtx4080-         */
 /* cutedsl" README, "Baseline tiled GEMM"), one CTA per 128 rows x 64 batch     */
 /* rows (a prompt's tokens, for prefill); needs bf16 x and cols % 64 == 0.      */
 int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
@@ -263,10 +266,13 @@ int qd_destroy_layer(qd_layer* layer);
 /* rope_table: from qd_rope_table_init with max_pos >= every position reached.  */
 /* logits: f32 [batch, vocab] device output. workspace: device scratch of        */
 /* qd_step_workspace_bytes(args) bytes, zero-filled before first use.           */
-/* BF16 layers: batch 1..2 runs the GEMV path (batch 2: K <= 12288); 3..64 runs  */
-/* every projection as a tcgen05 GEMM over the batch when hidden, n_q_heads *    */
-/* head_dim and ffn are multiples of 64 (else batch <= 8 stays on the GEMV path; */
-/* the environment variable QD_TC_MIN_BATCH moves the lower bound, minimum 2).   */
+/* BF16 layers: batch 1 runs the ring GEMV path. Batch 2..8 with a bf16 LM head  */
+/* and hidden, n_q_heads * head_dim, ffn multiples of 32 runs every projection   */
+/* on the mma.sync weight-streaming GEMV (five launches per layer, RMSNorm and   */
+/* SwiGLU fused). Batch 9..64 (and 3..8 with QD_SMALLB_IMPL=tc, from           */
+/* QD_TC_MIN_BATCH, default 3) runs every projection as a tcgen05 GEMM over the  */
+/* batch when those dims are multiples of 64; otherwise batch <= 8 runs the      */
+/* CUDA-core GEMV path (batch 2: K <= 12288).                                    */
 /* Q8_0 layers: batch 1 runs the                                                 */
 /* Q8_0 GEMV lanes (act, lm_act); 2..64 runs the tcgen05 GEMMs with the weights  */
 /* widened to bf16 as in qd_gemm_q8_0 (act and lm_act unused; dims % 256 == 0,   */
@@ -325,7 +331,9 @@ int qd_graph_destroy(qd_graph* g);
 /* one forward pass that reuses the weight bytes already streamed). For the one */
 /* sequence of `args` (batch 1): the k input tokens are tok[0] (the last token   */
 /* emitted) and draft[0 .. k-2], at positions pos[0] .. pos[0] + k - 1. They run  */
-/* as k rows of one pass: every projection is a tcgen05 GEMM over the k rows; the */
+/* as k rows of one pass: every projection streams its weights once for the k   */
+/* rows (bf16: the mma.sync GEMV when the dims are multiples of 32; Q8_0, or     */
+/* QD_SMALLB_IMPL=tc: tcgen05 GEMMs); the                                        */
 /* k new K/V rows are written to the cache first, and row i attends to positions */
 /* 0 .. pos[0] + i (causal among the drafted tokens).                           */
 /* Outputs: logits f32 [k, vocab] (device, 16-byte aligned); target int32 [k]:   */
@@ -336,7 +344,8 @@ int qd_graph_destroy(qd_graph* g);
 /* pos += m + 1; step += m + 1. Cache rows past pos[0] + m hold the rejected      */
 /* drafts' K/V until a later step overwrites them.                               */
 /* draft: int32 [k - 1] device (may be NULL when k == 1). 1 <= k <= 8. The       */
-/* projections' K must be multiples of 64 (bf16) or 256 (Q8_0, whose weights are  */
+/* projections' K must be multiples of 32 (bf16 on the mma.sync GEMV), 64 (bf16 */
+/* on tcgen05) or 256 (Q8_0, whose weights are                                   */
 /* widened on chip as in qd_gemm_q8_0). workspace: args->workspace of at least    */
 /* qd_verify_workspace_bytes(args, k) bytes, zero-filled before first use; the   */
 /* pass's scratch follows the first qd_step_workspace_bytes(args) bytes (the      */

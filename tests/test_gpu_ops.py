@@ -42,6 +42,45 @@ def test_gemv_bf16(cuda_lib, R, K, B):
         assert rel_max_abs(y[b].cpu().numpy(), ref) < GEMV_TOL
 
 
+# batch 2..8, bf16 x: the mma.sync weight-streaming GEMV (QD_SMALLB_IMPL=simt: the
+# CUDA-core GEMV). Rows below the SM count, ragged 32-row stages, K in one 32-column
+# chunk, past the 4096 columns held in registers with a ragged last stage, and the
+# Qwen3-8B / 0.6B projection and LM-head shapes.
+@pytest.mark.parametrize("R,K,B", [(1, 32, 2), (37, 96, 2), (151, 4128, 5), (153, 544, 8), (2000, 3072, 2),
+                                   (513, 4096, 3), (1024, 4096, 8), (4096, 12288, 8), (3000, 8224, 7),
+                                   (24576, 4096, 4), (151936, 1024, 4), (151936, 4096, 8)])
+@pytest.mark.parametrize("impl", ["mma", "simt"])
+def test_gemv_bf16_small_batch(cuda_lib, monkeypatch, impl, R, K, B):
+    monkeypatch.setenv("QD_SMALLB_IMPL", impl)
+    g = _gen(R * 3 + K + B)
+    W = (torch.randn((R, K), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    x = torch.randn((B, K), generator=g, device=DEV).to(torch.bfloat16)
+    try:
+        y = api.gemv_bf16(W, x)
+    except api.QDError:
+        if impl == "mma":
+            raise
+        pytest.skip("the CUDA-core GEMV takes this K only at a smaller batch")
+    torch.cuda.synchronize()
+    Wb, xb = synth.bits_u16(W), synth.bits_u16(x)
+    rows = np.arange(R) if R <= 8192 else np.arange(0, R, 53)
+    for b in range(B):
+        ref = oracle.gemv_bf16(Wb[rows], oracle.bf16_to_f64(xb[b]))
+        assert rel_max_abs(y[b].cpu().numpy()[rows], ref) < GEMV_TOL, b
+
+
+def test_gemv_bf16_small_batch_integer_exact(cuda_lib):
+    # small integers: every product and partial sum exact in binary32, so the mma.sync
+    # GEMV must give the exact integer result at every batch 2..8
+    g = _gen(29)
+    W = torch.randint(-8, 9, (333, 4160), generator=g, device=DEV).to(torch.bfloat16)
+    for B in range(2, 9):
+        x = torch.randint(-8, 9, (B, 4160), generator=g, device=DEV).to(torch.bfloat16)
+        y = api.gemv_bf16(W, x)
+        ref = x.double().cpu() @ W.double().cpu().T
+        assert torch.equal(y.cpu().double(), ref), B
+
+
 @pytest.mark.parametrize("R,K,B", [(128, 64, 9), (300, 1024, 16), (4096, 4096, 64), (1000, 12288, 33),
                                    (6144, 4096, 64), (151936, 4096, 64), (300, 1024, 65), (1000, 4096, 200),
                                    (4096, 4096, 512)])

@@ -61,15 +61,41 @@ def test_small_bf16_batch_paged_teacher_forced(cuda_lib):
 
 
 @pytest.mark.parametrize("batch", [3, 8, 12, 64])
-def test_batched_tensor_core_step_teacher_forced(cuda_lib, batch):
-    # 3..64 sequences (dims multiples of 64): projections on tcgen05, paged KV through
-    # a random page table
+def test_batched_tensor_core_step_teacher_forced(cuda_lib, monkeypatch, batch):
+    # 3..64 sequences (dims multiples of 64): projections on tcgen05 (below 9 only with
+    # QD_SMALLB_IMPL=tc), paged KV through a random page table
+    monkeypatch.setenv("QD_SMALLB_IMPL", "tc")
     mt = synth.make_model(synth.SMALL64, "bf16", 7, DEV, batch=batch, ctx=None, steps=3, paged=True)
     om = oracle_model(mt)
     check = sorted({0, batch // 3, batch - 1})
     caches = {b: oracle_caches(mt, b, int(mt.seq_lens[b]) + 3) for b in check}
     dec = api.Decoder(mt, max_steps=3)
     assert dec.launches_per_step == 1 + 8 * 2 + 3
+    toks = {b: int(mt.start_tok[b]) for b in check}
+    for t in range(3):
+        dec.step()
+        torch.cuda.synchronize()
+        for b in check:
+            g = dec.logits[b].double().cpu().numpy()
+            ref = oracle.decode_token(om, toks[b], int(mt.seq_lens[b]) + t, caches[b][0], caches[b][1],
+                                      mode="bf16", act="bf16")
+            assert rel_max_abs(g, ref) < TOL["bf16"], (t, b)
+            toks[b] = int(dec.tok[b])
+            assert toks[b] == oracle.argmax_first(g)
+    assert api.check_device_error() == 0
+
+
+@pytest.mark.parametrize("shape,batch", [("SMALL64", 2), ("SMALL", 5), ("SMALL64", 8), ("TINY", 7)])
+def test_small_batch_mma_step_teacher_forced(cuda_lib, shape, batch):
+    # 2..8 sequences: every projection on the mma.sync GEMV (RMSNorm prologue, SwiGLU
+    # epilogue), five launches per layer; paged KV through a random page table
+    mt = synth.make_model(getattr(synth, shape), "bf16", 17 + batch, DEV, batch=batch, ctx=None, steps=3,
+                          paged=True)
+    om = oracle_model(mt)
+    check = sorted({0, batch // 2, batch - 1})
+    caches = {b: oracle_caches(mt, b, int(mt.seq_lens[b]) + 3) for b in check}
+    dec = api.Decoder(mt, max_steps=3)
+    assert dec.launches_per_step == 1 + 5 * mt.shape.n_layers + 2
     toks = {b: int(mt.start_tok[b]) for b in check}
     for t in range(3):
         dec.step()
@@ -116,17 +142,18 @@ def test_batched_q8_step_teacher_forced(cuda_lib, batch, parity_log):
     assert api.check_device_error() == 0
 
 
-@pytest.mark.parametrize("wtype,acts", [("bf16", ("bf16",)), ("q8_0", ("f32", "w_bf16"))])
-def test_qwen3_8b_batched_paged_layer(cuda_lib, wtype, acts, parity_log):
-    """The batched workload's shapes: 64 sequences, Qwen3-8B layer, 16-token pages through a
-    random page table, context uniform in [128, 4096]; sampled sequences checked whole.
-    Q8_0: held to the pages' Q8_0 definition ("f32", on the bf16 activations) and to the
-    widened-weight lane."""
+@pytest.mark.parametrize("wtype,acts,batch", [("bf16", ("bf16",), 64), ("bf16", ("bf16",), 8),
+                                              ("q8_0", ("f32", "w_bf16"), 64)])
+def test_qwen3_8b_batched_paged_layer(cuda_lib, wtype, acts, batch, parity_log):
+    """The batched workload's shapes: 64 sequences (and 8, on the mma.sync GEMV), Qwen3-8B
+    layer, 16-token pages through a random page table, context uniform in [128, 4096];
+    sampled sequences checked whole. Q8_0: held to the pages' Q8_0 definition ("f32", on
+    the bf16 activations) and to the widened-weight lane."""
     s = synth.QWEN3_8B
-    mt = synth.make_model(s, wtype, 9, DEV, n_layers=1, batch=64, ctx=None, steps=1, paged=True)
+    mt = synth.make_model(s, wtype, 9, DEV, n_layers=1, batch=batch, ctx=None, steps=1, paged=True)
     om = oracle_model(mt)
     dec = api.Decoder(mt, max_steps=1)
-    check = [0, 31, 63]
+    check = sorted({0, batch // 2 - 1, batch - 1})
     dec.step()
     torch.cuda.synchronize()
     res = dec.residual()
@@ -148,7 +175,7 @@ def test_qwen3_8b_batched_paged_layer(cuda_lib, wtype, acts, parity_log):
             worst[f"lm_head/{act}"] = max(worst.get(f"lm_head/{act}", 0.0), err)
             assert err < TOL[act if act != "f32" else "w_bf16"], (b, act, err)
             assert int(dec.tok[b]) == oracle.argmax_first(lg)
-    parity_log[f"qwen3_8b_batched_paged_layer/{wtype}"] = worst
+    parity_log[f"qwen3_8b_batched_paged_layer/{wtype}/b{batch}"] = worst
     assert api.check_device_error() == 0
 
 

@@ -79,8 +79,11 @@ def _greedy(om, mt, history, tok, pos0, n, act="bf16", mode="bf16"):
     return out
 
 
-@pytest.mark.parametrize("k", [2, 4, 8])
-def test_verify_teacher_forced_bf16(cuda_lib, parity_log, k):
+# QD_SMALLB_IMPL: "mma" (default) runs the pass's projections on the mma.sync GEMV,
+# "tc" on the tcgen05 GEMMs
+@pytest.mark.parametrize("k,impl", [(2, "mma"), (4, "mma"), (8, "mma"), (4, "tc"), (8, "tc")])
+def test_verify_teacher_forced_bf16(cuda_lib, parity_log, monkeypatch, k, impl):
+    monkeypatch.setenv("QD_SMALLB_IMPL", impl)
     mt = synth.make_model(synth.SMALL64, "bf16", 21 + k, DEV, ctx=100, steps=2 * k + 2)
     om = oracle_model(mt)
     dec = api.Decoder(mt, max_steps=2 * k + 2, verify_k=k)
@@ -97,7 +100,7 @@ def test_verify_teacher_forced_bf16(cuda_lib, parity_log, k):
     torch.cuda.synchronize()
     _, m2, w2 = _check_pass(dec, mt, om, hist, draft, pos0, step1, ["bf16"], TOL["bf16"])
     assert m2 >= k - 2
-    parity_log[f"verify_bf16_k{k}"] = {"accepted": [m1, m2], "worst_rel_err": max(w1["bf16"], w2["bf16"])}
+    parity_log[f"verify_bf16_k{k}_{impl}"] = {"accepted": [m1, m2], "worst_rel_err": max(w1["bf16"], w2["bf16"])}
     assert api.check_device_error() == 0
 
 
@@ -149,9 +152,11 @@ def test_verify_then_decode(cuda_lib):
     assert api.check_device_error() == 0
 
 
-def test_verify_qwen3_8b_layer_k8(cuda_lib, parity_log):
+@pytest.mark.parametrize("impl", ["mma", "tc"])
+def test_verify_qwen3_8b_layer_k8(cuda_lib, parity_log, monkeypatch, impl):
     """Full Qwen3-8B shapes: one layer at context 4096 and the 151936-row LM head, k = 8
     rows, each row's residual checked whole and its LM-head rows sampled."""
+    monkeypatch.setenv("QD_SMALLB_IMPL", impl)
     s = synth.QWEN3_8B
     k = 8
     mt = synth.make_model(s, "bf16", 3, DEV, n_layers=1, ctx=4096, steps=k)
@@ -174,7 +179,7 @@ def test_verify_qwen3_8b_layer_k8(cuda_lib, parity_log):
         lg = dec.verify_logits[i].double().cpu().numpy()
         assert rel_max_abs(lg[rows], oracle.lm_head_rows(om, res[i], rows)) < 1e-3
         assert int(dec.verify_target[i]) == oracle.argmax_first(lg)
-    parity_log["verify_qwen3_8b_layer_k8"] = worst
+    parity_log[f"verify_qwen3_8b_layer_k8_{impl}"] = worst
     assert api.check_device_error() == 0
 
 
@@ -193,12 +198,27 @@ def test_verify_q8_0(cuda_lib, parity_log):
     assert api.check_device_error() == 0
 
 
-def test_verify_rejects_bad_arguments(cuda_lib):
+def test_verify_rejects_bad_arguments(cuda_lib, monkeypatch):
     mt = synth.make_model(synth.SMALL64, "bf16", 1, DEV, ctx=10, steps=4)
     dec = api.Decoder(mt, max_steps=4, verify_k=4)
     with pytest.raises(api.QDError):
         dec.verify(torch.zeros(8, dtype=torch.int32, device=DEV))    # k = 9 > 8
-    bad = synth.make_model(synth.SMALL, "bf16", 1, DEV, ctx=10, steps=4)   # K = 1376 is not a multiple of 64
+    # K = 1376: a multiple of 32 (the mma.sync GEMV takes it), not of 64 (the tcgen05 GEMM)
+    monkeypatch.setenv("QD_SMALLB_IMPL", "tc")
+    bad = synth.make_model(synth.SMALL, "bf16", 1, DEV, ctx=10, steps=4)
     d2 = api.Decoder(bad, max_steps=4, verify_k=4)
     with pytest.raises(api.QDError):
         d2.verify(torch.zeros(3, dtype=torch.int32, device=DEV))
+
+
+def test_verify_k_not_multiple_of_64_on_mma(cuda_lib):
+    # the same K = 1376 model on the mma.sync GEMV: the pass runs and matches the oracle
+    k = 4
+    mt = synth.make_model(synth.SMALL, "bf16", 2, DEV, ctx=40, steps=k)
+    om = oracle_model(mt)
+    dec = api.Decoder(mt, max_steps=k, verify_k=k)
+    draft = [int(t) for t in np.random.default_rng(5).integers(0, mt.shape.vocab, k - 1)]
+    dec.verify(torch.tensor(draft, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    _check_pass(dec, mt, om, [], draft, int(mt.seq_lens[0]), 0, ["bf16"], TOL["bf16"])
+    assert api.check_device_error() == 0

@@ -156,6 +156,17 @@ static const StepTuning& step_tuning() {
   return t;
 }
 
+// Small-batch BF16 implementation, QD_SMALLB_IMPL (read per call): "mma" (default) runs
+// batch 2..8 on the mma.sync weight-streaming GEMV; "tc" on the tcgen05 GEMMs from
+// QD_TC_MIN_BATCH; "simt" on the CUDA-core GEMV up to batch 8.
+enum { SMALLB_MMA = 0, SMALLB_TC = 1, SMALLB_SIMT = 2 };
+static int small_batch_impl() {
+  const char* e = getenv("QD_SMALLB_IMPL");
+  if (e && strcmp(e, "tc") == 0) return SMALLB_TC;
+  if (e && strcmp(e, "simt") == 0) return SMALLB_SIMT;
+  return SMALLB_MMA;
+}
+
 static Launch make_launch(cudaStream_t s, bool pdl) {
   Launch L;
   L.stream = s;
@@ -200,6 +211,13 @@ int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
     g.W = W; g.X = x; g.R = rows; g.K = cols; g.B = batch; g.epi = EPI_STORE; g.y = y;
     cudaError_t e = launch_gemm_tc(g, make_launch(stream, false));
     return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_bf16 (tensor cores)");
+  }
+  if (batch >= 2 && !x_is_f32 && small_batch_impl() == SMALLB_MMA && gemv_mma_supported(rows, cols, batch)) {
+    GemvMmaArgs g = {};
+    g.W = W; g.R = rows; g.K = cols; g.B = batch; g.pro = PRO_X_BF16; g.x = x; g.epi = EPI_STORE; g.y = y;
+    g.w_evict_first = 1;
+    cudaError_t e = launch_gemv_mma(g, make_launch(stream, false));
+    return e == cudaSuccess ? QD_OK : cuda_fail(e, "qd_gemv_bf16 (mma.sync)");
   }
   if (!gemv_bf16_supported(cols, batch))
     return fail(QD_ERR_UNSUPPORTED, "qd_gemv_bf16: cols=%d batch=%d (need cols%%8==0, cols<=32768, 1<=batch<=8)",
@@ -486,12 +504,23 @@ bool lm_is_q8(const qd_step_args* a) { return a->lm_head_scales != nullptr && !l
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// The tensor-core step: BF16 models from batch 3, Q8_0 models from batch 2 (the
-// Q8_0 GEMV lanes take one activation vector). The batch 2..8 CUDA-core GEMV
-// streams 3.84 / 2.67 / 0.96 TB/s at batch 2 / 4 / 8 against ~3.9 for the tcgen05
-// GEMM, and its K limit rejects the 12288-wide down projection above batch 2
-// (Qwen3-8B step at batch 2: 432 tok/s GEMV, 422 tensor cores). QD_TC_MIN_BATCH
-// moves the boundary.
+// The mma.sync step: BF16 layers and LM head at batch 2..8 with every K a multiple
+// of 32. Each projection streams its weights once for all rows at the batch-1
+// GEMV's rate, with the RMSNorm in the prologue and SwiGLU in the gate+up epilogue.
+bool mma_step(const qd_step_args* a) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const int B = a->batch;
+  return d.wtype == QD_W_BF16 && !a->lm_head_scales && B >= 2 && B <= 8 && small_batch_impl() == SMALLB_MMA &&
+         gemv_mma_supported(1, d.hidden, B) && gemv_mma_supported(1, d.n_q_heads * d.head_dim, B) &&
+         gemv_mma_supported(1, d.ffn, B);
+}
+
+// The tcgen05 step: BF16 models from batch 9 (from QD_TC_MIN_BATCH, default 3, when
+// the small-batch implementation is "tc", or where the mma.sync step does not apply),
+// Q8_0 models from batch 2 (the Q8_0 GEMV lanes take one activation vector). The
+// batch 2..8 CUDA-core GEMV streams 3.84 / 2.67 / 0.96 TB/s at batch 2 / 4 / 8
+// against ~3.9 for the tcgen05 GEMM, and its K limit rejects the 12288-wide down
+// projection above batch 2.
 bool tc_step(const qd_step_args* a) {
   static const int min_b = [] {
     const char* v = getenv("QD_TC_MIN_BATCH");
@@ -500,6 +529,7 @@ bool tc_step(const qd_step_args* a) {
   const qd_layer_dims& d = a->layers[0]->dims;
   if (d.wtype == QD_W_Q8_0) return a->batch > 1;
   if (a->batch > 8) return true;
+  if (mma_step(a) || small_batch_impl() == SMALLB_SIMT) return false;
   // batch min_b .. 8: the tensor cores where their K rule holds, else the GEMV
   return a->batch >= min_b && d.hidden % 64 == 0 && (d.n_q_heads * d.head_dim) % 64 == 0 && d.ffn % 64 == 0;
 }
@@ -614,6 +644,7 @@ int validate_step(const qd_step_args* a) {
   if (d0.wtype == QD_W_BF16) {
     const int ks[3] = {d0.hidden, d0.n_q_heads * d0.head_dim, d0.ffn};
     for (int k : ks) {
+      if (mma_step(a)) break;
       if (!tc_step(a) && !gemv_bf16_supported(k, a->batch))
         return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: GEMV K=%d with batch %d not supported", k, a->batch);
       if (tc_step(a) && !gemm_tc_supported(1, k, a->batch))
@@ -637,7 +668,8 @@ int validate_step(const qd_step_args* a) {
   if (q8_head) {
     if (!gemv_q8_supported(d0.hidden)) return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: Q8_0 head dims");
     if (a->batch > 1 && !tc_step(a))
-      return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: a Q8_0 LM head over BF16 layers needs batch 1 or 9..64");
+      return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: a Q8_0 LM head over BF16 layers at batch %d needs the "
+                  "tcgen05 step (every K a multiple of 64)", a->batch);
     if (a->batch > 1 && (!gemm_tc_q8_supported(a->vocab, d0.hidden, a->batch) || !aligned16(a->lm_head_scales)))
       return fail(QD_ERR_UNSUPPORTED, "qd_decode_step: batched Q8_0 LM head needs hidden %% 256 == 0");
   }
@@ -700,6 +732,70 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   }
   QD_TRY(launch_rmsnorm_rows(w.res, a->final_norm, B, H, d.rms_eps, w.xn, L), "final rmsnorm");
   QD_TRY(gemm(a->lm_head, a->lm_head_scales, a->vocab, H, w.xn, EPI_STORE, a->logits), "lm head gemm");
+  QD_TRY(launch_argmax_advance(a->logits, a->vocab, B, a->tok, a->pos, a->step, a->out_tokens, a->max_steps,
+                               w.argmax_ws, L),
+         "argmax");
+  return QD_OK;
+}
+
+// Small-batch BF16 decode (2..8 sequences): five launches per layer like batch 1,
+// every projection on the mma.sync weight-streaming GEMV (RMSNorm prologue, SwiGLU
+// epilogue of the gate+up projection writing bf16 h), paged split-KV attention.
+struct MmaProj {
+  const StepTuning& tu;
+  int B;
+  const Launch& L;
+  cudaError_t operator()(const void* W, int R, int K, int pro, const void* x, const void* norm_w, float eps,
+                         int epi, float* y, void* y_bf16 = nullptr) const {
+    GemvMmaArgs g = {};
+    g.W = W; g.R = R; g.K = K; g.B = B; g.pro = pro; g.x = x; g.norm_w = norm_w; g.eps = eps;
+    g.epi = epi; g.y = y; g.y_bf16 = y_bf16; g.w_evict_first = tu.w_evict_first;
+    return launch_gemv_mma(g, L);
+  }
+};
+
+// One layer of the small-batch path over B rows whose residual is w.res. `verify`:
+// the B rows are consecutive tokens of one sequence, so all their K/V rows go to the
+// cache first and row i attends to positions up to its own.
+int mma_layer(const qd_step_args* a, const qd_layer* l, int li, const StepWs& w, int B, const int32_t* pos,
+              const int32_t* page_table, int verify, const MmaProj& proj, const Launch& L) {
+  const qd_layer_dims& d = l->dims;
+  const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
+  const int QKV = (Hq + 2 * Hkv) * D;
+  QD_TRY(proj(l->w.w_qkv, QKV, H, PRO_RMSNORM, w.res, l->w.ln_in, d.rms_eps, EPI_STORE, w.qkv), "qkv gemv");
+  if (verify)
+    QD_TRY(launch_kv_write(w.qkv, B, Hq, Hkv, l->w.k_norm, a->rope_table, a->rope_max_pos, d.rms_eps, 1, pos,
+                           page_table, a->max_pages, a->page_size, a->max_pages, a->n_pages, a->k_cache[li],
+                           a->v_cache[li], L),
+           "kv write");
+  AttnArgs at = {};
+  at.qkv = w.qkv; at.q_norm = l->w.q_norm; at.k_norm = l->w.k_norm;
+  at.rope = a->rope_table; at.rope_max_pos = a->rope_max_pos; at.eps = d.rms_eps; at.act_bf16 = 1;
+  at.pos = pos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = page_table;
+  at.B = B; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
+  at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D); at.out_bf16 = w.attn;
+  at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.kv_ready = verify;
+  QD_TRY(launch_attention(at, L), "attention");
+  QD_TRY(proj(l->w.w_o, H, Hq * D, PRO_X_BF16, w.attn, nullptr, 0.f, EPI_RESID_ADD, w.res), "o gemv");
+  QD_TRY(proj(l->w.w_gu, 2 * F, H, PRO_RMSNORM, w.res, l->w.ln_post, d.rms_eps, EPI_SWIGLU, nullptr, w.xn),
+         "gu gemv");
+  QD_TRY(proj(l->w.w_down, H, F, PRO_X_BF16, w.xn, nullptr, 0.f, EPI_RESID_ADD, w.res), "down gemv");
+  return QD_OK;
+}
+
+int run_step_mma(const qd_step_args* a, cudaStream_t stream) {
+  const qd_layer_dims& d = a->layers[0]->dims;
+  const StepWs w = step_ws_layout(a, a->workspace);
+  const Launch L = make_launch(stream, true);
+  const int B = a->batch;
+  const MmaProj proj{step_tuning(), B, L};
+  QD_TRY(launch_embed(a->embed, d.hidden, a->vocab, a->tok, B, w.res, L), "embed");
+  for (int li = 0; li < a->n_layers; ++li) {
+    const int rc = mma_layer(a, a->layers[li], li, w, B, a->pos, a->page_table, 0, proj, L);
+    if (rc) return rc;
+  }
+  QD_TRY(proj(a->lm_head, a->vocab, d.hidden, PRO_RMSNORM, w.res, a->final_norm, d.rms_eps, EPI_STORE, a->logits),
+         "lm head gemv");
   QD_TRY(launch_argmax_advance(a->logits, a->vocab, B, a->tok, a->pos, a->step, a->out_tokens, a->max_steps,
                                w.argmax_ws, L),
          "argmax");
@@ -779,6 +875,7 @@ int run_step_w4(const qd_step_args* a, cudaStream_t stream) {
 }
 
 int run_step(const qd_step_args* a, cudaStream_t stream) {
+  if (mma_step(a)) return run_step_mma(a, stream);
   if (tc_step(a)) return run_step_tc(a, stream);
   if (a->layers[0]->dims.wtype == QD_W_INT4) return run_step_w4(a, stream);
   const qd_layer_dims& d = a->layers[0]->dims;
@@ -969,6 +1066,14 @@ VerifyWs verify_ws_layout(const qd_step_args* a, int k, void* base) {
 
 constexpr int kMaxVerify = 8;
 
+// A verify pass on the mma.sync GEMVs: the small-batch step's rule for k rows (k = 1
+// included: the GEMV takes one row as well).
+bool mma_verify(const qd_step_args* a, int k) {
+  qd_step_args ak = *a;
+  ak.batch = std::max(k, 2);
+  return mma_step(&ak);
+}
+
 int validate_verify(const qd_step_args* a, const int32_t* draft, int k, const float* logits, const int32_t* target,
                     const int32_t* n_accept) {
   if (!a) return fail(QD_ERR_INVALID_ARG, "qd_verify_step: null args");
@@ -985,7 +1090,7 @@ int validate_verify(const qd_step_args* a, const int32_t* draft, int k, const fl
   const bool q8 = d.wtype == QD_W_Q8_0;
   const int ks[3] = {d.hidden, d.n_q_heads * d.head_dim, d.ffn};
   for (int K : ks)
-    if (q8 ? !gemm_tc_q8_supported(1, K, k) : !gemm_tc_supported(1, K, k))
+    if (!mma_verify(a, k) && (q8 ? !gemm_tc_q8_supported(1, K, k) : !gemm_tc_supported(1, K, k)))
       return fail(QD_ERR_UNSUPPORTED, "qd_verify_step: projection K=%d needs a multiple of %d", K, q8 ? 256 : 64);
   if (a->lm_head_scales && !gemm_tc_q8_supported(a->vocab, d.hidden, k))
     return fail(QD_ERR_UNSUPPORTED, "qd_verify_step: Q8_0 LM head needs hidden %% 256 == 0");
@@ -1020,7 +1125,16 @@ int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits
                             v.scratch, L),
          "verify prep");
   QD_TRY(launch_embed(a->embed, H, a->vocab, v.tokens, k, w.res, L), "embed");
-  for (int li = 0; li < a->n_layers; ++li) {
+  const bool mma = mma_verify(a, k);
+  const MmaProj proj{step_tuning(), k, L};
+  for (int li = 0; li < a->n_layers && mma; ++li) {
+    const int rc = mma_layer(a, a->layers[li], li, w, k, v.vpos, v.vpt, 1, proj, L);
+    if (rc) return rc;
+  }
+  if (mma)
+    QD_TRY(proj(a->lm_head, a->vocab, H, PRO_RMSNORM, w.res, a->final_norm, d.rms_eps, EPI_STORE, logits),
+           "lm head gemv");
+  for (int li = 0; li < a->n_layers && !mma; ++li) {
     const qd_layer* l = a->layers[li];
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_in, k, H, d.rms_eps, w.xn, L), "rmsnorm");
     QD_TRY(gemm(l->w.w_qkv, q8 ? l->w.s_qkv : nullptr, QKV, H, w.xn, EPI_STORE, w.qkv), "qkv gemm");
@@ -1043,8 +1157,10 @@ int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits
     QD_TRY(launch_swiglu_rows(w.gu, k, F, w.xn, L), "swiglu");
     QD_TRY(gemm(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, EPI_RESID_ADD, w.res), "down gemm");
   }
-  QD_TRY(launch_rmsnorm_rows(w.res, a->final_norm, k, H, d.rms_eps, w.xn, L), "final rmsnorm");
-  QD_TRY(gemm(a->lm_head, a->lm_head_scales, a->vocab, H, w.xn, EPI_STORE, logits), "lm head gemm");
+  if (!mma) {
+    QD_TRY(launch_rmsnorm_rows(w.res, a->final_norm, k, H, d.rms_eps, w.xn, L), "final rmsnorm");
+    QD_TRY(gemm(a->lm_head, a->lm_head_scales, a->vocab, H, w.xn, EPI_STORE, logits), "lm head gemm");
+  }
   QD_TRY(launch_argmax_advance(logits, a->vocab, k, target, v.scratch, v.scratch + k, v.scratch + 2 * k, 1,
                                w.argmax_ws, L),
          "argmax");
@@ -1200,6 +1316,7 @@ size_t qd_step_workspace_bytes(const qd_step_args* a) {
 
 int qd_step_launch_count(const qd_step_args* a) {
   if (!a || a->n_layers < 1 || !a->layers || !a->layers[0]) return 0;
+  if (mma_step(a)) return 1 + 5 * a->n_layers + 2;
   if (tc_step(a)) return 1 + 8 * a->n_layers + 3;
   if (a->layers[0]->dims.wtype == QD_W_INT4 || lm_is_w4(a)) return 1 + 5 * a->n_layers + (lm_is_w4(a) ? 1 : 2);
   if (!step_kernels_forced()) {

@@ -125,6 +125,23 @@ struct GemmTcArgs {
   void* ws;               // split-K partials and tile tickets (zero-filled before first use,
   size_t ws_bytes;        // left so); null: no split
 };
+
+// Weight-streaming GEMV over B <= 8 activation rows on mma.sync (gemv_mma.cu).
+struct GemvMmaArgs {
+  const void* W;          // bf16 [R, K]; EPI_SWIGLU: [gate F rows; up F rows], R = 2F
+  int R, K, B;            // K % 32 == 0, 1 <= B <= 8
+  int pro;                // PRO_X_BF16: x bf16 [B, K]; PRO_RMSNORM: x f32 [B, K], norm_w bf16 [K]
+  const void* x;
+  const void* norm_w;
+  float eps;
+  int epi;                // EPI_STORE / EPI_RESID_ADD: y f32 [B, R]; EPI_SWIGLU: y_bf16 [B, F]
+  float* y;
+  void* y_bf16;
+  int w_evict_first;
+};
+bool gemv_mma_supported(int R, int K, int B);
+cudaError_t launch_gemv_mma(const GemvMmaArgs& a, const Launch& L);
+
 bool gemm_tc_supported(int R, int K, int B);
 bool gemm_tc_q8_supported(int R, int K, int B);
 // B > 64 rows (prefill): token tiles over grid z, no K split; B <= 64: the forms above.
