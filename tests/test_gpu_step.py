@@ -85,17 +85,21 @@ def test_batched_tensor_core_step_teacher_forced(cuda_lib, monkeypatch, batch):
     assert api.check_device_error() == 0
 
 
-@pytest.mark.parametrize("shape,batch", [("SMALL64", 2), ("SMALL", 5), ("SMALL64", 8), ("TINY", 7)])
-def test_small_batch_mma_step_teacher_forced(cuda_lib, shape, batch):
-    # 2..8 sequences: every projection on the mma.sync GEMV (RMSNorm prologue, SwiGLU
-    # epilogue), five launches per layer; paged KV through a random page table
+@pytest.mark.parametrize("shape,batch,norm_rows", [("SMALL64", 2, 1), ("SMALL", 5, 1), ("SMALL64", 8, 1),
+                                                    ("TINY", 7, 1), ("SMALL64", 3, 0), ("SMALL", 8, 0)])
+def test_small_batch_mma_step_teacher_forced(cuda_lib, monkeypatch, shape, batch, norm_rows):
+    # 2..8 sequences: every projection on the mma.sync GEMV (SwiGLU epilogue), the
+    # RMSNorms as row kernels (seven launches per layer) or, with QD_MMA_NORM_ROWS=0, in
+    # the GEMV prologues (five); paged KV through a random page table
+    monkeypatch.setenv("QD_MMA_NORM_ROWS", str(norm_rows))
     mt = synth.make_model(getattr(synth, shape), "bf16", 17 + batch, DEV, batch=batch, ctx=None, steps=3,
                           paged=True)
     om = oracle_model(mt)
     check = sorted({0, batch // 2, batch - 1})
     caches = {b: oracle_caches(mt, b, int(mt.seq_lens[b]) + 3) for b in check}
     dec = api.Decoder(mt, max_steps=3)
-    assert dec.launches_per_step == 1 + 5 * mt.shape.n_layers + 2
+    L = mt.shape.n_layers
+    assert dec.launches_per_step == (1 + 7 * L + 3 if norm_rows else 1 + 5 * L + 2)
     toks = {b: int(mt.start_tok[b]) for b in check}
     for t in range(3):
         dec.step()

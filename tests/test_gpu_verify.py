@@ -104,6 +104,26 @@ def test_verify_teacher_forced_bf16(cuda_lib, parity_log, monkeypatch, k, impl):
     assert api.check_device_error() == 0
 
 
+@pytest.mark.parametrize("k", [3, 8])
+def test_verify_paged_cache(cuda_lib, k):
+    # 16-token pages through a random page table: the pass's shared-K/V attention
+    # follows the sequence's page-table row; every row's logits and argmax against
+    # the oracle
+    mt = synth.make_model(synth.SMALL64, "bf16", 51 + k, DEV, ctx=[333], steps=k + 1, paged=True)
+    om = oracle_model(mt)
+    dec = api.Decoder(mt, max_steps=k + 1, verify_k=k)
+    draft = [int(t) for t in np.random.default_rng(k).integers(0, mt.shape.vocab, k - 1)]
+    dec.verify(torch.tensor(draft, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    inputs = [int(mt.start_tok[0])] + draft
+    refs, _, _ = _oracle_run(om, mt, [], inputs, int(mt.seq_lens[0]))
+    g = dec.verify_logits[:k].double().cpu().numpy()
+    for i in range(k):
+        assert rel_max_abs(g[i], refs[i]) < TOL["bf16"], i
+        assert int(dec.verify_target[i]) == oracle.argmax_first(g[i])
+    assert api.check_device_error() == 0
+
+
 def test_verify_equals_greedy_steps(cuda_lib):
     # drafts = the GPU's own next greedy tokens: all accepted, and the state and tokens
     # are those of k plain greedy steps

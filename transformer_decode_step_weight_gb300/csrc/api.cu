@@ -167,6 +167,16 @@ static int small_batch_impl() {
   return SMALLB_MMA;
 }
 
+// Small-batch GEMVs, QD_MMA_NORM_ROWS (read per call): 1 (default) runs each RMSNorm
+// as a row kernel writing the bf16 rows once, 0 in every GEMV CTA's prologue. The row
+// kernel measured faster on the Qwen3-8B step: 609 / 1135 / 1790 against
+// 524 / 997 / 1606 tok/s at batch 2 / 4 / 8 (each prologue re-read the f32 rows
+// before its first MMA).
+static bool mma_norm_rows() {
+  const char* v = getenv("QD_MMA_NORM_ROWS");
+  return v == nullptr || atoi(v) != 0;
+}
+
 static Launch make_launch(cudaStream_t s, bool pdl) {
   Launch L;
   L.stream = s;
@@ -738,15 +748,23 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   return QD_OK;
 }
 
-// Small-batch BF16 decode (2..8 sequences): five launches per layer like batch 1,
-// every projection on the mma.sync weight-streaming GEMV (RMSNorm prologue, SwiGLU
-// epilogue of the gate+up projection writing bf16 h), paged split-KV attention.
+// Small-batch BF16 decode (2..8 sequences): every projection on the mma.sync
+// weight-streaming GEMV (the SwiGLU in the gate+up epilogue writing bf16 h), each
+// RMSNorm as one row kernel writing bf16 rows (or in the GEMV prologue), paged
+// split-KV attention: seven launches per layer (five with the prologue norm).
 struct MmaProj {
   const StepTuning& tu;
   int B;
   const Launch& L;
+  void* norm_scratch;   // bf16 [B, K] rows for the separate RMSNorm (QD_MMA_NORM_ROWS)
   cudaError_t operator()(const void* W, int R, int K, int pro, const void* x, const void* norm_w, float eps,
                          int epi, float* y, void* y_bf16 = nullptr) const {
+    if (pro == PRO_RMSNORM && mma_norm_rows()) {
+      cudaError_t e = launch_rmsnorm_rows((const float*)x, norm_w, B, K, eps, norm_scratch, L);
+      if (e != cudaSuccess) return e;
+      pro = PRO_X_BF16;
+      x = norm_scratch;
+    }
     GemvMmaArgs g = {};
     g.W = W; g.R = R; g.K = K; g.B = B; g.pro = pro; g.x = x; g.norm_w = norm_w; g.eps = eps;
     g.epi = epi; g.y = y; g.y_bf16 = y_bf16; g.w_evict_first = tu.w_evict_first;
@@ -775,7 +793,10 @@ int mma_layer(const qd_step_args* a, const qd_layer* l, int li, const StepWs& w,
   at.B = B; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
   at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D); at.out_bf16 = w.attn;
   at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.kv_ready = verify;
-  QD_TRY(launch_attention(at, L), "attention");
+  if (verify && verify_attention_supported(B, Hq, Hkv))
+    QD_TRY(launch_verify_attention(at, B, L), "verify attention");
+  else
+    QD_TRY(launch_attention(at, L), "attention");
   QD_TRY(proj(l->w.w_o, H, Hq * D, PRO_X_BF16, w.attn, nullptr, 0.f, EPI_RESID_ADD, w.res), "o gemv");
   QD_TRY(proj(l->w.w_gu, 2 * F, H, PRO_RMSNORM, w.res, l->w.ln_post, d.rms_eps, EPI_SWIGLU, nullptr, w.xn),
          "gu gemv");
@@ -788,7 +809,7 @@ int run_step_mma(const qd_step_args* a, cudaStream_t stream) {
   const StepWs w = step_ws_layout(a, a->workspace);
   const Launch L = make_launch(stream, true);
   const int B = a->batch;
-  const MmaProj proj{step_tuning(), B, L};
+  const MmaProj proj{step_tuning(), B, L, w.gu};
   QD_TRY(launch_embed(a->embed, d.hidden, a->vocab, a->tok, B, w.res, L), "embed");
   for (int li = 0; li < a->n_layers; ++li) {
     const int rc = mma_layer(a, a->layers[li], li, w, B, a->pos, a->page_table, 0, proj, L);
@@ -1126,7 +1147,7 @@ int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits
          "verify prep");
   QD_TRY(launch_embed(a->embed, H, a->vocab, v.tokens, k, w.res, L), "embed");
   const bool mma = mma_verify(a, k);
-  const MmaProj proj{step_tuning(), k, L};
+  const MmaProj proj{step_tuning(), k, L, w.gu};
   for (int li = 0; li < a->n_layers && mma; ++li) {
     const int rc = mma_layer(a, a->layers[li], li, w, k, v.vpos, v.vpt, 1, proj, L);
     if (rc) return rc;
@@ -1150,7 +1171,10 @@ int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits
     at.B = k; at.Hq = Hq; at.Hkv = Hkv; at.D = D; at.page_size = a->page_size; at.max_pages = a->max_pages;
     at.n_pages = a->n_pages; at.scale = 1.0f / sqrtf((float)D); at.out_bf16 = w.attn;
     at.workspace = w.attn_ws; at.max_ctx = a->max_pages * a->page_size; at.kv_ready = 1;
-    QD_TRY(launch_attention(at, L), "attention");
+    if (verify_attention_supported(k, Hq, Hkv))
+      QD_TRY(launch_verify_attention(at, k, L), "verify attention");
+    else
+      QD_TRY(launch_attention(at, L), "attention");
     QD_TRY(gemm(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, EPI_RESID_ADD, w.res), "o gemm");
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, k, H, d.rms_eps, w.xn, L), "rmsnorm");
     QD_TRY(gemm(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, EPI_STORE, w.gu), "gu gemm");
@@ -1316,7 +1340,7 @@ size_t qd_step_workspace_bytes(const qd_step_args* a) {
 
 int qd_step_launch_count(const qd_step_args* a) {
   if (!a || a->n_layers < 1 || !a->layers || !a->layers[0]) return 0;
-  if (mma_step(a)) return 1 + 5 * a->n_layers + 2;
+  if (mma_step(a)) return mma_norm_rows() ? 1 + 7 * a->n_layers + 3 : 1 + 5 * a->n_layers + 2;
   if (tc_step(a)) return 1 + 8 * a->n_layers + 3;
   if (a->layers[0]->dims.wtype == QD_W_INT4 || lm_is_w4(a)) return 1 + 5 * a->n_layers + (lm_is_w4(a) ? 1 : 2);
   if (!step_kernels_forced()) {

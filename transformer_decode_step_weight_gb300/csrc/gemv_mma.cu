@@ -210,27 +210,35 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams
   // ---- consumers
   const int g = lane >> 2, t = lane & 3;
   pdl_wait();
-  if (p.pro == PRO_RMSNORM) {  // 1 / rms of every activation row: all threads, one pass
-    float ss[kMaxB];
+  if (p.pro == PRO_RMSNORM) {
+    // 1 / rms of every activation row. Lane (g, t) of warp w reads exactly the columns
+    // of row g its fragments hold (every column of every row once over the CTA), all
+    // loads in flight; sums over the four lanes of a row, then over the warps. load_x
+    // reads the same addresses again (L1 hits).
+    float ss = 0.f;
+    for (int q = 0; q < nq; ++q) {
+      float4 v[kXR][2];
 #pragma unroll
-    for (int b = 0; b < kMaxB; ++b) ss[b] = 0.f;
-#pragma unroll 2
-    for (int c = tid * 4; c < K; c += kCons * 4) {
-#pragma unroll
-      for (int b = 0; b < kMaxB; ++b) {
-        if (b >= p.B) break;
-        const float4 v = *(const float4*)((const float*)p.x + (size_t)b * K + c);
-        ss[b] = fmaf(v.x, v.x, ss[b]);
-        ss[b] = fmaf(v.y, v.y, ss[b]);
-        ss[b] = fmaf(v.z, v.z, ss[b]);
-        ss[b] = fmaf(v.w, v.w, ss[b]);
+      for (int j = 0; j < kXR; ++j) {
+        const int col = q * kKR + 32 * (w + kWarps * j) + 8 * t;
+        const bool in = g < p.B && col < K;
+        const float* xp = (const float*)p.x + (size_t)g * K + col;
+        v[j][0] = in ? *(const float4*)xp : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[j][1] = in ? *(const float4*)(xp + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+#pragma unroll
+      for (int j = 0; j < kXR; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          ss = fmaf(v[j][h].x, v[j][h].x, ss);
+          ss = fmaf(v[j][h].y, v[j][h].y, ss);
+          ss = fmaf(v[j][h].z, v[j][h].z, ss);
+          ss = fmaf(v[j][h].w, v[j][h].w, ss);
+        }
     }
-#pragma unroll
-    for (int b = 0; b < kMaxB; ++b) ss[b] = warp_sum(ss[b]);
-    if (lane == 0)
-#pragma unroll
-      for (int b = 0; b < kMaxB; ++b) s_ss[w][b] = ss[b];
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    if (t == 0) s_ss[w][g] = ss;
     cons_sync_m();
     if (tid < p.B) {
       float tot = 0.f;

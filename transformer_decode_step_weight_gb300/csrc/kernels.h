@@ -245,6 +245,14 @@ cudaError_t launch_kv_write(const float* qkv, int B, int Hq, int Hkv, const void
                             int pt_stride, int page_size, int max_pages, int n_pages, void* k_pages, void* v_pages,
                             const Launch& L);
 
+// Speculative-verify attention (attention_verify.cu): the k rows of one sequence at
+// positions pos[0..k) (their K/V already in the cache), q from qkv [k, QKV] with the
+// QK-RMSNorm and RoPE fused in, every K/V tile read once for all k * Hq / Hkv query
+// columns; page_table: the sequence's row. The workspace is the decode attention's for
+// B = k rows.
+bool verify_attention_supported(int k, int Hq, int Hkv);
+cudaError_t launch_verify_attention(const AttnArgs& a, int k, const Launch& L);
+
 // ----------------------------------------------------------------- prefill (prefill.cu)
 // Causal attention of the n prompt rows of one sequence (positions pos[0] + i) over
 // the cached keys 0 .. pos[0] + i, with the queries' QK-RMSNorm and RoPE fused in.
