@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3-8b-bf16",
                     choices=["qwen3-8b-bf16", "qwen3-0.6b", "qwen3-8b-q8_0", "qwen3-8b-int4",
+                             "qwen3-8b-bf16-b2", "qwen3-8b-bf16-b4", "qwen3-8b-bf16-b8",
                              "qwen3-8b-bf16-paged-b64", "qwen3-8b-q8_0-paged-b64", "qwen3-0.6b-layer"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -748,6 +748,8 @@ int run_step_tc(const qd_step_args* a, cudaStream_t stream) {
   return QD_OK;
 }
 
+static int qkv_rows(const qd_layer_dims& d) { return (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim; }
+
 // Small-batch BF16 decode (2..8 sequences): every projection on the mma.sync
 // weight-streaming GEMV (the SwiGLU in the gate+up epilogue writing bf16 h), each
 // RMSNorm as one row kernel writing bf16 rows (or in the GEMV prologue), paged
@@ -758,7 +760,7 @@ struct MmaProj {
   const Launch& L;
   void* norm_scratch;   // bf16 [B, K] rows for the separate RMSNorm (QD_MMA_NORM_ROWS)
   cudaError_t operator()(const void* W, int R, int K, int pro, const void* x, const void* norm_w, float eps,
-                         int epi, float* y, void* y_bf16 = nullptr) const {
+                         int epi, float* y, void* y_bf16 = nullptr, L2Prefetch pf = {}) const {
     if (pro == PRO_RMSNORM && mma_norm_rows()) {
       cudaError_t e = launch_rmsnorm_rows((const float*)x, norm_w, B, K, eps, norm_scratch, L);
       if (e != cudaSuccess) return e;
@@ -768,18 +770,28 @@ struct MmaProj {
     GemvMmaArgs g = {};
     g.W = W; g.R = R; g.K = K; g.B = B; g.pro = pro; g.x = x; g.norm_w = norm_w; g.eps = eps;
     g.epi = epi; g.y = y; g.y_bf16 = y_bf16; g.w_evict_first = tu.w_evict_first;
+    g.pf = pf;
     return launch_gemv_mma(g, L);
   }
 };
 
 // One layer of the small-batch path over B rows whose residual is w.res. `verify`:
 // the B rows are consecutive tokens of one sequence, so all their K/V rows go to the
-// cache first and row i attends to positions up to its own.
+// cache first and row i attends to positions up to its own. next_w / next_R: the
+// GEMV after this layer's down projection (its weights' heads go to L2 early).
 int mma_layer(const qd_step_args* a, const qd_layer* l, int li, const StepWs& w, int B, const int32_t* pos,
-              const int32_t* page_table, int verify, const MmaProj& proj, const Launch& L) {
+              const int32_t* page_table, int verify, const MmaProj& proj, const Launch& L, const void* next_w,
+              int next_R) {
   const qd_layer_dims& d = l->dims;
   const int H = d.hidden, F = d.ffn, D = d.head_dim, Hq = d.n_q_heads, Hkv = d.n_kv_heads;
   const int QKV = (Hq + 2 * Hkv) * D;
+  // head of every CTA span of the next GEMV (R rows of K; the gate+up GEMV's spans are
+  // its pair ranges, so the gate half's partition)
+  auto tail = [&](const void* Wn, int R, int K) {
+    L2Prefetch pf = {};
+    if (proj.tu.tail_kb > 0 && Wn) pf = l2_plan_rows(Wn, R, (size_t)K * 2, (size_t)proj.tu.tail_kb << 10);
+    return pf;
+  };
   QD_TRY(proj(l->w.w_qkv, QKV, H, PRO_RMSNORM, w.res, l->w.ln_in, d.rms_eps, EPI_STORE, w.qkv), "qkv gemv");
   if (verify)
     QD_TRY(launch_kv_write(w.qkv, B, Hq, Hkv, l->w.k_norm, a->rope_table, a->rope_max_pos, d.rms_eps, 1, pos,
@@ -797,10 +809,15 @@ int mma_layer(const qd_step_args* a, const qd_layer* l, int li, const StepWs& w,
     QD_TRY(launch_verify_attention(at, B, L), "verify attention");
   else
     QD_TRY(launch_attention(at, L), "attention");
-  QD_TRY(proj(l->w.w_o, H, Hq * D, PRO_X_BF16, w.attn, nullptr, 0.f, EPI_RESID_ADD, w.res), "o gemv");
-  QD_TRY(proj(l->w.w_gu, 2 * F, H, PRO_RMSNORM, w.res, l->w.ln_post, d.rms_eps, EPI_SWIGLU, nullptr, w.xn),
+  QD_TRY(proj(l->w.w_o, H, Hq * D, PRO_X_BF16, w.attn, nullptr, 0.f, EPI_RESID_ADD, w.res, nullptr,
+              tail(l->w.w_gu, F, H)),
+         "o gemv");
+  QD_TRY(proj(l->w.w_gu, 2 * F, H, PRO_RMSNORM, w.res, l->w.ln_post, d.rms_eps, EPI_SWIGLU, nullptr, w.xn,
+              tail(l->w.w_down, H, F)),
          "gu gemv");
-  QD_TRY(proj(l->w.w_down, H, F, PRO_X_BF16, w.xn, nullptr, 0.f, EPI_RESID_ADD, w.res), "down gemv");
+  QD_TRY(proj(l->w.w_down, H, F, PRO_X_BF16, w.xn, nullptr, 0.f, EPI_RESID_ADD, w.res, nullptr,
+              tail(next_w, next_R, H)),
+         "down gemv");
   return QD_OK;
 }
 
@@ -812,7 +829,9 @@ int run_step_mma(const qd_step_args* a, cudaStream_t stream) {
   const MmaProj proj{step_tuning(), B, L, w.gu};
   QD_TRY(launch_embed(a->embed, d.hidden, a->vocab, a->tok, B, w.res, L), "embed");
   for (int li = 0; li < a->n_layers; ++li) {
-    const int rc = mma_layer(a, a->layers[li], li, w, B, a->pos, a->page_table, 0, proj, L);
+    const bool last = li + 1 == a->n_layers;
+    const int rc = mma_layer(a, a->layers[li], li, w, B, a->pos, a->page_table, 0, proj, L,
+                             last ? a->lm_head : a->layers[li + 1]->w.w_qkv, last ? a->vocab : qkv_rows(d));
     if (rc) return rc;
   }
   QD_TRY(proj(a->lm_head, a->vocab, d.hidden, PRO_RMSNORM, w.res, a->final_norm, d.rms_eps, EPI_STORE, a->logits),
@@ -1149,7 +1168,9 @@ int run_verify(const qd_step_args* a, const int32_t* draft, int k, float* logits
   const bool mma = mma_verify(a, k);
   const MmaProj proj{step_tuning(), k, L, w.gu};
   for (int li = 0; li < a->n_layers && mma; ++li) {
-    const int rc = mma_layer(a, a->layers[li], li, w, k, v.vpos, v.vpt, 1, proj, L);
+    const bool last = li + 1 == a->n_layers;
+    const int rc = mma_layer(a, a->layers[li], li, w, k, v.vpos, v.vpt, 1, proj, L,
+                             last ? a->lm_head : a->layers[li + 1]->w.w_qkv, last ? a->vocab : qkv_rows(d));
     if (rc) return rc;
   }
   if (mma)

@@ -67,6 +67,7 @@ struct MmaParams {
   __nv_bfloat16* y_bf16;
   int* err;
   int w_evict_first;
+  L2Prefetch pf;
 };
 
 QD_DEV void cons_sync_m() { asm volatile("bar.sync 1, %0;" ::"n"(kCons) : "memory"); }
@@ -204,6 +205,9 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams
       for (int rg = 0; rg < nrg && go; ++rg)
         for (int kp = 0; kp < npk && go; ++kp) go = issue(rg, kp);
     }
+    // the ring's last refills are in flight: DRAM would idle while the consumers
+    // drain, so fetch the head of the next GEMV's spans into L2
+    l2_prefetch_spans(p.pf, blockIdx.x, gridDim.x, lane);
     return;
   }
 
@@ -436,6 +440,7 @@ cudaError_t launch_gemv_mma(const GemvMmaArgs& a, const Launch& L) {
   p.epi = a.epi; p.y = a.y; p.y_bf16 = (__nv_bfloat16*)a.y_bf16;
   p.err = L.err;
   p.w_evict_first = a.w_evict_first;
+  p.pf = a.pf;
   const size_t smem = (size_t)p.ring_bytes + fixed;
   return tu.cpw == 8 ? launch_mma_c<8>(p, grid, smem, L) : launch_mma_c<16>(p, grid, smem, L);
 }

@@ -138,6 +138,7 @@ struct GemvMmaArgs {
   float* y;
   void* y_bf16;
   int w_evict_first;
+  L2Prefetch pf;          // weights of the next GEMV, fetched once this CTA's copies are issued
 };
 bool gemv_mma_supported(int R, int K, int B);
 cudaError_t launch_gemv_mma(const GemvMmaArgs& a, const Launch& L);

@@ -100,6 +100,10 @@ WORKLOADS = {
     "qwen3-8b-q8_0": Workload(
         "qwen3-8b-q8_0", QWEN3_8B, "q8_0", ctx=2048, steps=128,
         description="Qwen3-8B-shaped Q8_0 model (LM head Q8_0 too), batch 1, context 2048"),
+    **{f"qwen3-8b-bf16-b{n}": Workload(
+        f"qwen3-8b-bf16-b{n}", QWEN3_8B, "bf16", ctx=2048, steps=128, batch=n,
+        description=f"Qwen3-8B-shaped BF16 model, {n} sequences, contiguous KV at context 2048 each")
+       for n in (2, 4, 8)},
     "qwen3-8b-bf16-paged-b64": Workload(
         "qwen3-8b-bf16-paged-b64", QWEN3_8B, "bf16", ctx=4096, steps=64, batch=64, paged=True,
         description="64 sequences, context uniform in [128, 4096], 16-token pages, random page table"),
