@@ -295,7 +295,10 @@ def _attn_ref(q, kp, vp, pt, lens):
     (1, 4, 2, [1], 16, False), (1, 4, 2, [64], 16, False), (1, 4, 2, [65], 16, False),
     (1, 16, 8, [129], 16, False), (1, 32, 8, [4224], 16, False), (2, 8, 8, [5, 1000], 16, False),
     (3, 32, 8, [1, 37, 300], 16, True), (4, 16, 2, [17, 64, 128, 700], 16, True),
-    (2, 8, 1, [100, 33], 7, True), (5, 4, 4, [0, 3, 64, 65, 2000], 32, True)])
+    (2, 8, 1, [100, 33], 7, True), (5, 4, 4, [0, 3, 64, 65, 2000], 32, True),
+    # 32 .. SM-count (sequence, kv head) pairs: the tensor-core form with the CUDA-core
+    # form's split sizing (TMA boxes at 16-token pages, cp.async at 8)
+    (6, 32, 8, [1, 64, 65, 700, 1500, 3000], 16, True), (4, 16, 8, [3, 129, 640, 2049], 8, True)])
 def test_attention_parity(cuda_lib, B, hq, hkv, lens, ps, paged):
     q, kp, vp, pt, sl = _attn_case(B, hq, hkv, lens, ps, B * 100 + hq + sum(lens), paged)
     out = api.attn_decode_paged(q, kp, vp, pt, sl, 1 / math.sqrt(128))
