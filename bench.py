@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--verify", type=int, default=0, metavar="K",
                     help="time speculative verify passes of K tokens (K - 1 drafts) against K single-token steps "
                          "on the batch-1 workload")
+    ap.add_argument("--layers", type=int, default=0, metavar="N",
+                    help="--verify only: a model of N decoder layers instead of the workload's (profiling aid)")
     ap.add_argument("--deq", type=int, choices=[0, 1, 2],
                     help="Q8_0 lanes by level: 0 = dp4a everywhere, 1 = dp4a in the layers and f32 activations for "
                          "the LM head, 2 = f32 activations everywhere (overrides --act)")
@@ -374,8 +376,9 @@ def run_ours(args, dist, rank, world, local):
 
     # ---- dominant kernel: the BF16 GEMV, every launch of one token, events on its stream
     roof = None
-    if not args.no_probe and wl.batch == 1 and wl.wtype in ("bf16", "int4"):
-        roof = dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind)
+    if not args.no_probe and ((wl.batch == 1 and wl.wtype in ("bf16", "int4")) or
+                              (wl.wtype == "bf16" and 2 <= wl.batch <= 8)):
+        roof = dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind, batch=wl.batch)
 
     # ---- end to end through the public API: per step H2D of the input token/position
     # from pinned memory, the step, D2H of the next token, host reads it
@@ -455,14 +458,18 @@ def measure_read_peak(dev, stream, gib=4, reps=5):
         return None
 
 
-def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
-    """Average duration of the weight GEMV's launches over one token's projections
-    (36 x QKV, O, gate+up at K = hidden, and the LM head), timed with CUDA events on the
-    stream they run on, three passes; algorithmic bytes = the weight bytes (and, for
-    INT4, the per-row scales) each launch reads."""
-    x = torch.randn((1, max(s.hidden, s.n_q_heads * s.head_dim)), device=mt.embed.device).to(torch.bfloat16)
+def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind, batch=1):
+    """Average duration of the weight GEMV's launches over one step's projections, timed
+    with CUDA events on the stream they run on, three passes; algorithmic bytes = the
+    weight bytes (and, for INT4, the per-row scales) each launch reads. Batch 1: the
+    ring GEMV's K = hidden launches (36 x QKV, O, gate+up, and the LM head); batch 2..8:
+    the mma.sync GEMV over `batch` activation rows, every projection (down included)."""
+    B = batch
+    x = torch.randn((B, max(s.hidden, s.n_q_heads * s.head_dim, s.ffn)),
+                    device=mt.embed.device).to(torch.bfloat16)
     xo = x[:, : s.n_q_heads * s.head_dim].contiguous()
     xh = x[:, : s.hidden].contiguous()
+    xf = x[:, : s.ffn].contiguous()
     w4 = mt.wtype == "int4"
     mats = []
     for lt in mt.layers:
@@ -470,8 +477,10 @@ def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
             mats += [(lt.w_qkv, lt.s_qkv, xh[0]), (lt.w_o, lt.s_o, xo[0]), (lt.w_gu, lt.s_gu, xh[0])]
         else:
             mats += [(lt.w_qkv, None, xh), (lt.w_o, None, xo), (lt.w_gu, None, xh)]
+            if B > 1:
+                mats.append((lt.w_down, None, xf))
     mats.append((mt.lm_head, mt.lm_head_scales, xh[0] if w4 else xh))
-    ys = {id(w): torch.empty((1, w.shape[0]), dtype=torch.float32, device=x.device) for w, _, _ in mats}
+    ys = {id(w): torch.empty((B, w.shape[0]), dtype=torch.float32, device=x.device) for w, _, _ in mats}
 
     w4ws = {}
     if w4:   # the step's split-K workspace, one per shape
@@ -503,13 +512,16 @@ def dominant_kernel_roofline(api, mt, s, stream, hbm_peak, peak_kind):
         bytes_per_launch = sum(w.numel() * 2 for w, _, _ in mats) / len(mats)
     avg_s = ms / 1e3 / n
     achieved = bytes_per_launch / avg_s / 1e9
-    src = "gemv_w4.cu" if w4 else "gemv_bf16.cu"
+    src = "gemv_w4.cu" if w4 else "gemv_bf16.cu" if B == 1 else "gemv_mma.cu"
     rec = traffic_record(os.path.join(ROOT, "transformer_decode_step_weight_gb300", "csrc", src))
     traffic = None
     if rec is not None:
         traffic = rec.get("traffic_bytes_per_launch")
-    kname = "gemv_w4_kernel" if w4 else "gemv_bf16_kernel"
-    return {"bound": "hbm", "kernel": f"{kname} (K = hidden launches of one token)",
+    if B > 1:
+        kname, which = "gemv_mma_kernel", f"every projection of one step, {B} rows"
+    else:
+        kname, which = ("gemv_w4_kernel" if w4 else "gemv_bf16_kernel"), "K = hidden launches of one token"
+    return {"bound": "hbm", "kernel": f"{kname} ({which})",
             "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
             "peak_kind": peak_kind, "avg_launch_us": round(avg_s * 1e6, 3),
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "traffic": traffic}
@@ -772,7 +784,8 @@ def run_verify(args):
     n = max(1, args.steps // 4)
     # room for every timed decode step (that leg does not restore the state)
     run_len = 4 * k + 16 + reps * (max(3, args.warmup) + n) + 8
-    mt = synth.make_model(wl.shape, wl.wtype, args.seed, dev, ctx=wl.ctx, steps=run_len)
+    mt = synth.make_model(wl.shape, wl.wtype, args.seed, dev, ctx=wl.ctx, steps=run_len,
+                          n_layers=args.layers if args.layers > 0 else None)
     act, lm_act = q8_lanes(args)
     dec = api.Decoder(mt, max_steps=run_len, act=api.QD_ACT_I8 if act == "i8" else api.QD_ACT_F32,
                       lm_act=api.QD_ACT_I8 if lm_act == "i8" else api.QD_ACT_F32, device=dev, verify_k=k)
@@ -818,9 +831,11 @@ def run_verify(args):
     out = {"metric": f"speculative verify pass, k = {k} tokens of one sequence", "value": round(k / (verify_ms / 1e3), 3),
            "unit": "tok/s if all k accepted", "ms_per_pass": round(verify_ms, 4),
            "ms_per_single_step": round(step_ms, 4), "pass_vs_k_steps": round(verify_ms / (k * step_ms), 4),
-           "higher_is_better": True, "dtype": dtype_label(wl, act, lm_act) if k == 1 else "bf16 tcgen05 rows",
+           "higher_is_better": True,
+           "dtype": "bf16 mma.sync rows" if wl.wtype == "bf16" else "q8_0 widened to bf16, tcgen05 rows",
            "data": "synthetic", "config": {"workload": wl.name, "k": k, "drafts": "random tokens",
-                                           "passes_timed": n, "repetitions": reps}}
+                                           "passes_timed": n, "repetitions": reps,
+                                           "layers": args.layers or wl.shape.n_layers}}
     print(json.dumps(out), flush=True)
     dec.close()
 

@@ -24,6 +24,7 @@
 #include "launch.cuh"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace qd {
 namespace {
@@ -146,21 +147,29 @@ __global__ void __launch_bounds__(32 * kMaxWarps) verify_attn_kernel(const VPara
   // softmax scale (log2 e folded in), then bf16 hi + lo. Lane l holds dims l + 32e; the
   // RoPE pairs (d, d + 64) are e = 0, 2 and e = 1, 3 of the same lane.
   const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
-  float xin[8][4];   // the warp's 8 columns, all loads in flight at once
+  // the warp's 8 columns, their RoPE rows and the norm weights: every load in flight at once
+  float xin[8][4];
+  float2 rc[8][2];
+  float qw[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) qw[e] = __bfloat162float(p.q_norm[lane + 32 * e]);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int c = warp * 8 + j;
     const int row = c / p.rep, h = c - row * p.rep;
+    const bool in = c < p.ncols;
     const float* src = p.qkv + (size_t)row * qkv_w + (size_t)(g * p.rep + h) * kD;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) xin[j][e] = c < p.ncols ? src[lane + 32 * e] : 0.f;
+    for (int e = 0; e < 4; ++e) xin[j][e] = in ? src[lane + 32 * e] : 0.f;
+    const float2* cs = p.rope + (size_t)(in ? s_pos[row] : 0) * (kD / 2);
+    rc[j][0] = cs[lane];
+    rc[j][1] = cs[lane + 32];
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int c = warp * 8 + j;
     float qv[4] = {0.f, 0.f, 0.f, 0.f};
     if (c < p.ncols) {
-      const int row = c / p.rep;
       float x[4], y[4];
       float ss = 0.f;
 #pragma unroll
@@ -174,11 +183,10 @@ __global__ void __launch_bounds__(32 * kMaxWarps) verify_attn_kernel(const VPara
       for (int e = 0; e < 4; ++e) {
         float n = x[e] * inv;
         if (p.act_bf16) n = round_bf16(n);
-        y[e] = __bfloat162float(p.q_norm[lane + 32 * e]) * n;
+        y[e] = qw[e] * n;
         if (p.act_bf16) y[e] = round_bf16(y[e]);
       }
-      const float2* cs = p.rope + (size_t)s_pos[row] * (kD / 2);
-      const float2 c0 = cs[lane], c1 = cs[lane + 32];
+      const float2 c0 = rc[j][0], c1 = rc[j][1];
       qv[0] = (y[0] * c0.x - y[2] * c0.y) * p.scale_log2;   // d = lane
       qv[1] = (y[1] * c1.x - y[3] * c1.y) * p.scale_log2;   // d = lane + 32
       qv[2] = (y[2] * c0.x + y[0] * c0.y) * p.scale_log2;   // d = lane + 64
@@ -384,38 +392,47 @@ __global__ void __launch_bounds__(32 * kMaxWarps) verify_attn_kernel(const VPara
 __global__ void __launch_bounds__(kD) verify_combine_kernel(const VParams p) {
   __shared__ float sW[kMaxSplitsV];
   __shared__ float s_tot;
+  __shared__ int s_nact;
   const int c = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
-  int lmax = 0;
-  for (int i = 0; i < p.k; ++i) lmax = max(lmax, p.pos[i] + 1);
-  const int cap = p.max_pages * p.page_size;
-  if (lmax <= 0 || lmax > cap) return;   // the attention kernel flagged it
-  const int n_act = (lmax + p.chunk - 1) / p.chunk;
-  if (n_act <= 1) return;
   const size_t slot0 = (size_t)g * p.n_splits;
-  if (d < 32) {  // weights per split, in split order
-    float mk[kMaxSplitsV / 32], M = -INFINITY;
+  if (d < 32) {
+    // the active splits (from the rows' positions, one lane each), then the weights
+    // exp2(m_s - M) and the total sum of l_s weights: lane d takes splits d and d + 32,
+    // summed over the lanes by a fixed butterfly
+    int lm = d < p.k ? p.pos[d] + 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, o));
+    const int cap = p.max_pages * p.page_size;
+    const int n_act = (lm <= 0 || lm > cap) ? 0 : (lm + p.chunk - 1) / p.chunk;   // 0: flagged by the attention
+    float mk[kMaxSplitsV / 32], lk[kMaxSplitsV / 32], M = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kMaxSplitsV / 32; ++u) {
       const int k = d + 32 * u;
-      mk[u] = k < n_act ? __ldcg(p.ws_ml + ((slot0 + k) * p.ncols + c) * 2) : -INFINITY;
+      const bool in = k < n_act;
+      mk[u] = in ? __ldcg(p.ws_ml + ((slot0 + k) * p.ncols + c) * 2) : -INFINITY;
+      lk[u] = in ? __ldcg(p.ws_ml + ((slot0 + k) * p.ncols + c) * 2 + 1) : 0.f;
       M = fmaxf(M, mk[u]);
     }
     M = warp_max(M);
+    float L = 0.f;
 #pragma unroll
     for (int u = 0; u < kMaxSplitsV / 32; ++u) {
       const int k = d + 32 * u;
-      if (k < n_act) sW[k] = mk[u] == -INFINITY ? 0.f : exp2f(mk[u] - M);
+      const float wk = mk[u] == -INFINITY ? 0.f : exp2f(mk[u] - M);
+      if (k < n_act) sW[k] = wk;
+      L = fmaf(wk, lk[u], L);
     }
-    __syncwarp();
+    L = warp_sum(L);
     if (d == 0) {
-      float L = 0.f;
-      for (int k = 0; k < n_act; ++k) L = fmaf(sW[k], __ldcg(p.ws_ml + ((slot0 + k) * p.ncols + c) * 2 + 1), L);
       s_tot = L;
+      s_nact = n_act;
     }
   }
   __syncthreads();
+  const int n_act = s_nact;
+  if (n_act <= 1) return;   // one split wrote the output itself (or nothing to merge)
   const float* src = p.ws_acc + (slot0 * p.ncols + c) * kD + d;
   const size_t stride = (size_t)p.ncols * kD;
   constexpr int kU = 16;
@@ -459,8 +476,13 @@ cudaError_t launch_verify_attention(const AttnArgs& a, int k, const Launch& L) {
   p.v_pages = (const __nv_bfloat16*)a.v_pages;
   p.k = k; p.Hq = a.Hq; p.Hkv = a.Hkv; p.rep = a.Hq / a.Hkv; p.ncols = k * p.rep;
   p.page_size = a.page_size; p.max_pages = a.max_pages; p.n_pages = a.n_pages;
-  // about two CTAs per SM over (split, kv head), 64-token multiples, at most kMaxSplitsV
-  const int ctas = 2 * dev_info().sm_count;
+  // about two CTAs per SM over (split, kv head) (QD_VERIFY_ATTN_PER_SM), 64-token
+  // multiples, at most kMaxSplitsV
+  static const int per_sm = [] {
+    const char* v = getenv("QD_VERIFY_ATTN_PER_SM");
+    return v ? std::max(1, std::min(8, atoi(v))) : 2;
+  }();
+  const int ctas = per_sm * dev_info().sm_count;
   int chunk = (int)(((long long)a.max_ctx * a.Hkv + ctas - 1) / ctas);
   chunk = std::max(kT, ((chunk + kT - 1) / kT) * kT);
   while ((a.max_ctx + chunk - 1) / chunk > kMaxSplitsV) chunk += kT;
