@@ -317,8 +317,20 @@ int pick_c(int K) {
 // with two cp.async.bulk copies; eight consumer warps own 16-weight half-blocks
 // of every row with the activation slice (f32, or int8 + scale) in registers.
 constexpr int kConsQ = 256;
-constexpr int kRingQ = 96 * 1024;
+constexpr int kRingQMax = 200 * 1024;   // largest ring a launch may take
 constexpr int kPhaseQ = 128;
+// Ring bytes per lane (QD_Q8_RING_KB overrides both, read once). The dp4a lane is
+// latency-bound, so more bytes in flight help it: at 24576 x 4096 it streamed 4.46 /
+// 4.71 / 4.71 / 4.65 TB/s with 96 / 128 / 160 / 192 KB (Qwen3-8B Q8_0 step 485 -> 510
+// tok/s at 160); the f32 lane is issue-bound and keeps 96 KB (398 vs 391 tok/s).
+int ring_q_bytes(int act) {
+  static const int forced = [] {
+    const char* e = getenv("QD_Q8_RING_KB");
+    return e ? std::max(64, std::min(200, atoi(e))) * 1024 : 0;
+  }();
+  if (forced) return forced;
+  return (act == 1 ? 160 : 96) * 1024;
+}
 
 struct RingQ8Params {
   const int8_t* qs;
@@ -761,7 +773,7 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
     p.P = std::max(1, kConsQ / p.T);
     const size_t row_bytes = (size_t)a.K + (size_t)a.K / 16;
     p.stage_bytes = (int)((((size_t)p.P * rps * row_bytes) + 127) / 128 * 128);
-    p.ns = std::max(2, std::min(16, kRingQ / p.stage_bytes));
+    p.ns = std::max(2, std::min(16, ring_q_bytes(a.act) / p.stage_bytes));
     p.ring_bytes = p.ns * p.stage_bytes;
     p.pro = a.pro; p.x = (const float*)a.x; p.xq = a.xq; p.xd = (const __half*)a.xd;
     if (a.act == 1 && a.xq != nullptr) p.pro = PRO_Q8_GIVEN;
@@ -771,7 +783,7 @@ cudaError_t launch_gemv_q8(const GemvQ8Args& a, const Launch& L) {
                   (size_t)kPhaseQ * 4 * 2 + (size_t)kPhaseQ / 2 * 4;
     smem = std::max(smem, (size_t)dev_info().max_smem_optin / 2 + 1024);  // one GEMV CTA per SM
     p.dots = a.dots;
-    if ((size_t)p.ns * p.stage_bytes <= (size_t)kRingQ * 2) {
+    if ((size_t)p.ns * p.stage_bytes <= (size_t)kRingQMax) {
       if (a.dots) {
         switch (rc) {
           case 1: return launch_ring_q<1, 1, true>(p, grid, smem, L);
