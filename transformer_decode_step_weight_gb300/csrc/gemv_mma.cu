@@ -23,8 +23,7 @@
 // bf16 product summed in binary32. A warp keeps the activation fragments of 4096
 // columns in registers (16 per lane): K up to 4096 reads x once per CTA; a wider K
 // runs range by range over all of a CTA's row groups (up to 64 rows, their sums in
-// registers), so x is read once per CTA there too, each fragment of the next range
-// loading right after its last use in the current one. The warps' partial sums reduce in
+// registers), so x is read once per CTA there too. The warps' partial sums reduce in
 // a fixed order through shared memory, 32 rows at a time.
 //
 // Prologue: x as bf16 rows, or RMSNorm of f32 residual rows (bf16(w * bf16(x / rms))
@@ -86,28 +85,27 @@ QD_DEV uint32_t pack2(float lo, float hi) { return f2bf_bits(lo) | (f2bf_bits(hi
 // Activation fragments of lane (g, t) of warp w for columns [k0, k0 + kKR): fragment j
 // holds columns 8t .. 8t + 7 of 32-column chunk w + 8j, activation row g; zero past K
 // or past the B rows.
-QD_DEV uint4 load_frag(const MmaParams& p, int k0, int j, int w, int g, int t, const float* s_inv) {
-  const int col = k0 + 32 * (w + kWarps * j) + 8 * t;
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (g < p.B && col < p.K) {
-    if (p.pro == PRO_X_BF16) {
-      v = *(const uint4*)((const __nv_bfloat16*)p.x + (size_t)g * p.K + col);
-    } else {  // PRO_RMSNORM
-      const float* xp = (const float*)p.x + (size_t)g * p.K + col;
-      const float4 a = *(const float4*)xp, c = *(const float4*)(xp + 4);
-      const uint4 nw = *(const uint4*)(p.norm_w + col);
-      const float inv = s_inv[g];
-      v.x = pack2(bf_lo(nw.x) * round_bf16(a.x * inv), bf_hi(nw.x) * round_bf16(a.y * inv));
-      v.y = pack2(bf_lo(nw.y) * round_bf16(a.z * inv), bf_hi(nw.y) * round_bf16(a.w * inv));
-      v.z = pack2(bf_lo(nw.z) * round_bf16(c.x * inv), bf_hi(nw.z) * round_bf16(c.y * inv));
-      v.w = pack2(bf_lo(nw.w) * round_bf16(c.z * inv), bf_hi(nw.w) * round_bf16(c.w * inv));
-    }
-  }
-  return v;
-}
 QD_DEV void load_x(const MmaParams& p, int k0, int w, int g, int t, const float* s_inv, uint4 (&xr)[kXR]) {
 #pragma unroll
-  for (int j = 0; j < kXR; ++j) xr[j] = load_frag(p, k0, j, w, g, t, s_inv);
+  for (int j = 0; j < kXR; ++j) {
+    const int col = k0 + 32 * (w + kWarps * j) + 8 * t;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (g < p.B && col < p.K) {
+      if (p.pro == PRO_X_BF16) {
+        v = *(const uint4*)((const __nv_bfloat16*)p.x + (size_t)g * p.K + col);
+      } else {  // PRO_RMSNORM
+        const float* xp = (const float*)p.x + (size_t)g * p.K + col;
+        const float4 a = *(const float4*)xp, c = *(const float4*)(xp + 4);
+        const uint4 nw = *(const uint4*)(p.norm_w + col);
+        const float inv = s_inv[g];
+        v.x = pack2(bf_lo(nw.x) * round_bf16(a.x * inv), bf_hi(nw.x) * round_bf16(a.y * inv));
+        v.y = pack2(bf_lo(nw.y) * round_bf16(a.z * inv), bf_hi(nw.y) * round_bf16(a.w * inv));
+        v.z = pack2(bf_lo(nw.z) * round_bf16(c.x * inv), bf_hi(nw.z) * round_bf16(c.y * inv));
+        v.w = pack2(bf_lo(nw.w) * round_bf16(c.z * inv), bf_hi(nw.w) * round_bf16(c.w * inv));
+      }
+    }
+    xr[j] = v;
+  }
 }
 
 // CPW: 32-column chunks per warp per stage (a stage spans PK = 256 * CPW columns).
@@ -115,7 +113,6 @@ template <int CPW>
 __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams p) {
   constexpr int PK = 32 * kWarps * CPW;
   constexpr int kPPR = kKR / PK;   // stages per register range
-  constexpr int kRgQ = CPW >= 16 ? kMaxRgQ : kMaxRgQ / 2;   // the narrower stages hold fewer (registers)
   static_assert(kKR % PK == 0, "a register range holds whole stages");
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
@@ -154,12 +151,12 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams
   pdl_launch_dependents();
 
   // Stage order. K up to 4096: row group by row group, each over its K range. Wider K
-  // with at most kRgQ row groups: register range by register range (4096 columns),
+  // with at most kMaxRgQ row groups: register range by register range (4096 columns),
   // each over every row group, so the activation fragments load once per range and the
   // row groups' sums stay in registers; otherwise row group by row group with the
   // fragments reloaded per range.
   const int nq = (K + kKR - 1) / kKR;
-  const bool qouter = nq > 1 && nrg <= kRgQ;
+  const bool qouter = nq > 1 && nrg <= kMaxRgQ;
 
   if (w == kWarps) {  // ---- producer warp: weights only, so no dependency wait
     const uint64_t pol = policy_evict_first();
@@ -262,7 +259,7 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams
   bool ok = true;
   // One stage: MMAs of this warp's chunks of stage i (columns k0 ..) into acc, with the
   // activation fragments xbase .. of the current range. false: the wait gave up.
-  auto run_stage = [&](int k0, int xbase, float* acc, int next_k0 = -1) -> bool {
+  auto run_stage = [&](int k0, int xbase, float* acc) -> bool {
     const int slot = i % ns;
     if (!mbar_wait_bounded(&full[slot], (uint32_t)((i / ns) & 1), p.err)) {
       // drain the copies that may still land in this CTA's ring, then stop
@@ -279,12 +276,7 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams
       const uint4 wv = *(const uint4*)(wp + cl * 64);
       mma_a8(acc, xf.x, xf.y, wv.x, wv.y);
       mma_a8(acc, xf.z, xf.w, wv.z, wv.w);
-      if (next_k0 >= 0) xr[xbase + ci] = load_frag(p, next_k0, xbase + ci, w, g, t, s_inv);
     }
-    if (next_k0 >= 0)   // fragments of chunks this stage did not reach (past K here)
-#pragma unroll
-      for (int ci = 0; ci < CPW; ++ci)
-        if (k0 + 32 * (w + kWarps * ci) >= K) xr[xbase + ci] = load_frag(p, next_k0, xbase + ci, w, g, t, s_inv);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
     ++i;
@@ -325,24 +317,21 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams
 
   if (qouter) {
     // C fragment per row group: [0] = (activation row g, weight row 2t), [1] = (g, 2t + 1)
-    float acc[kRgQ][4];
+    float acc[kMaxRgQ][4];
 #pragma unroll
-    for (int r = 0; r < kRgQ; ++r)
+    for (int r = 0; r < kMaxRgQ; ++r)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
-    // each fragment of the next range loads into its register right after its last
-    // use in this range (the last row group's stage), so the loads overlap that stage
-    load_x(p, 0, w, g, t, s_inv, xr);
     for (int q = 0; q < nq && ok; ++q) {
+      load_x(p, q * kKR, w, g, t, s_inv, xr);
 #pragma unroll
-      for (int rg = 0; rg < kRgQ; ++rg) {
+      for (int rg = 0; rg < kMaxRgQ; ++rg) {
         if (rg >= nrg || !ok) break;
 #pragma unroll
         for (int pp = 0; pp < kPPR; ++pp) {
           const int k0 = q * kKR + pp * PK;
           if (k0 >= K) break;
-          const bool refill = kPPR == 1 && rg + 1 == nrg && q + 1 < nq;
-          if (!run_stage(k0, pp * CPW, acc[rg], refill ? (q + 1) * kKR : -1)) {
+          if (!run_stage(k0, pp * CPW, acc[rg])) {
             ok = false;
             break;
           }
@@ -350,7 +339,7 @@ __global__ void __launch_bounds__(kCons + 32, 1) gemv_mma_kernel(const MmaParams
       }
     }
 #pragma unroll
-    for (int rg = 0; rg < kRgQ; ++rg) {
+    for (int rg = 0; rg < kMaxRgQ; ++rg) {
       if (rg >= nrg) break;
       if (!put(rg, acc[rg][0], acc[rg][1])) return;
     }
