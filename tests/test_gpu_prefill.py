@@ -43,8 +43,10 @@ def _check_kv(mt, ks, vs, p, n, tol=2e-2):
             assert rel_max_abs(got[:, p:p + n], ref[:, p:p + n]) < tol, li
 
 
-@pytest.mark.parametrize("n", [1, 63, 130, 1030])
-def test_prefill_bf16(cuda_lib, parity_log, n):
+# QD_PREFILL_P_HILO: the attention's P as bf16 hi + lo (1) or its bf16 value alone (0)
+@pytest.mark.parametrize("n,hilo", [(1, 1), (63, 1), (130, 1), (1030, 1), (130, 0), (1030, 0)])
+def test_prefill_bf16(cuda_lib, parity_log, monkeypatch, n, hilo):
+    monkeypatch.setenv("QD_PREFILL_P_HILO", str(hilo))
     mt = synth.make_model(synth.SMALL64, "bf16", 60 + n, DEV, ctx=37, steps=n + 4)
     om = oracle_model(mt)
     dec = api.Decoder(mt, max_steps=n + 4, prefill_max=n)
@@ -63,7 +65,7 @@ def test_prefill_bf16(cuda_lib, parity_log, n):
     if oracle.argmax_first(ref) != tk:   # only at a near tie
         top = np.sort(ref)[-2:]
         assert top[1] - top[0] < 4 * np.max(np.abs(got - ref))
-    parity_log[f"prefill_bf16_n{n}"] = err
+    parity_log[f"prefill_bf16_n{n}_hilo{hilo}"] = err
     assert api.check_device_error() == 0
 
 
@@ -128,9 +130,11 @@ def test_prefill_q8_0(cuda_lib, parity_log):
     assert api.check_device_error() == 0
 
 
-def test_prefill_qwen3_8b_layer(cuda_lib, parity_log):
+@pytest.mark.parametrize("hilo", [1, 0])
+def test_prefill_qwen3_8b_layer(cuda_lib, parity_log, monkeypatch, hilo):
     """Full Qwen3-8B shapes: one layer after a 4096-token cache, a 70-token prompt;
     sampled rows' residuals whole, every K/V row, and sampled LM-head rows."""
+    monkeypatch.setenv("QD_PREFILL_P_HILO", str(hilo))
     s = synth.QWEN3_8B
     n = 70
     mt = synth.make_model(s, "bf16", 5, DEV, n_layers=1, ctx=4096, steps=n)
@@ -154,7 +158,7 @@ def test_prefill_qwen3_8b_layer(cuda_lib, parity_log):
     lg = dec.prefill_logits.double().cpu().numpy()
     assert rel_max_abs(lg[rows], oracle.lm_head_rows(om, res[n - 1], rows)) < 1e-3
     assert int(dec.tok[0]) == oracle.argmax_first(lg)
-    parity_log["prefill_qwen3_8b_layer"] = worst
+    parity_log[f"prefill_qwen3_8b_layer_hilo{hilo}"] = worst
     assert api.check_device_error() == 0
 
 

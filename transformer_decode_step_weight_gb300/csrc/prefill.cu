@@ -23,6 +23,8 @@
 #include "kernels.h"
 #include "launch.cuh"
 
+#include <cstdlib>
+
 #include <algorithm>
 
 namespace qd {
@@ -106,6 +108,8 @@ QD_DEV void pf_load_tile(const PfParams& p, int g, int t, int kend, uint32_t sK,
   }
 }
 
+// PLO: P as bf16 hi + lo (two MMAs per P fragment) or its bf16 value alone.
+template <bool PLO>
 __global__ void __launch_bounds__(kPTh) prefill_attn_kernel(const PfParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -288,7 +292,7 @@ __global__ void __launch_bounds__(kPTh) prefill_attn_kernel(const PfParams p) {
         o[j][2] *= al1;
         o[j][3] *= al1;
       }
-      // ---- O += P V: P (bf16 hi + lo) from the S accumulators, 16 keys per step
+      // ---- O += P V: P (bf16 hi + lo, or bf16) from the S accumulators, 16 keys per step
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const float* pa = s[2 * kk];
@@ -299,16 +303,16 @@ __global__ void __launch_bounds__(kPTh) prefill_attn_kernel(const PfParams p) {
         for (int i = 0; i < 4; ++i) {
           const __nv_bfloat16 h0 = __float2bfloat16_rn(pv[i][0]), h1 = __float2bfloat16_rn(pv[i][1]);
           ph[i] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-          pl[i] = pack_bf16(pv[i][0] - __bfloat162float(h0), pv[i][1] - __bfloat162float(h1));
+          if (PLO) pl[i] = pack_bf16(pv[i][0] - __bfloat162float(h0), pv[i][1] - __bfloat162float(h1));
         }
 #pragma unroll
         for (int dp = 0; dp < 8; ++dp) {
           uint32_t b[4];
           pf_ldsm_t(b, sV + pf_swz(16 * kk + (mi & 1) * 8 + mr, 2 * dp + (mi >> 1)));
           pf_mma(o[2 * dp], ph[0], ph[1], ph[2], ph[3], b[0], b[1]);
-          pf_mma(o[2 * dp], pl[0], pl[1], pl[2], pl[3], b[0], b[1]);
+          if (PLO) pf_mma(o[2 * dp], pl[0], pl[1], pl[2], pl[3], b[0], b[1]);
           pf_mma(o[2 * dp + 1], ph[0], ph[1], ph[2], ph[3], b[2], b[3]);
-          pf_mma(o[2 * dp + 1], pl[0], pl[1], pl[2], pl[3], b[2], b[3]);
+          if (PLO) pf_mma(o[2 * dp + 1], pl[0], pl[1], pl[2], pl[3], b[2], b[3]);
         }
       }
     }
@@ -362,13 +366,17 @@ cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const Launch& L) 
   p.page_table = a.page_table; p.page_size = a.page_size; p.max_pages = a.max_pages; p.n_pages = a.n_pages;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.out = (__nv_bfloat16*)a.out; p.err = L.err;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
+  // QD_PREFILL_P_HILO (read per call): 1 keeps P as bf16 hi + lo, 0 its bf16 value alone
+  const char* hl = getenv("QD_PREFILL_P_HILO");
+  const bool plo = hl == nullptr || atoi(hl) != 0;
+  auto k = plo ? prefill_attn_kernel<true> : prefill_attn_kernel<false>;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[plo]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[plo] = true;
   }
-  return launch_ex(prefill_attn_kernel, dim3(ceil_div(a.n, kPQ), a.Hq), dim3(kPTh), kPSmem, L, p);
+  return launch_ex(k, dim3(ceil_div(a.n, kPQ), a.Hq), dim3(kPTh), kPSmem, L, p);
 }
 
 cudaError_t launch_prefill_prep(const int32_t* pos, int n, int32_t* vpos, const Launch& L) {
