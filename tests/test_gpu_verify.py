@@ -231,6 +231,20 @@ def test_verify_rejects_bad_arguments(cuda_lib, monkeypatch):
         d2.verify(torch.zeros(3, dtype=torch.int32, device=DEV))
 
 
+def test_verify_past_the_cache_flags_the_position(cuda_lib):
+    # a pass whose rows run past the cache: K/V write, attention and its merge skip the
+    # rows out of range and the position error bit is set (nothing written out of range)
+    mt = synth.make_model(synth.SMALL64, "bf16", 7, DEV, ctx=20, steps=4)
+    dec = api.Decoder(mt, max_steps=4, verify_k=8)
+    before = [c.clone() for c in mt.k_cache]
+    dec.verify(torch.zeros(7, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    assert api.check_device_error() & 2   # QD_DEVERR_POS
+    # the cached rows below the pass's first position are untouched
+    for b, a in zip(before, mt.k_cache):
+        assert torch.equal(b[..., :20, :], a[..., :20, :])
+
+
 def test_verify_k_not_multiple_of_64_on_mma(cuda_lib):
     # the same K = 1376 model on the mma.sync GEMV: the pass runs and matches the oracle
     k = 4

@@ -401,11 +401,14 @@ __global__ void __launch_bounds__(kD) verify_combine_kernel(const VParams p) {
     // the active splits (from the rows' positions, one lane each), then the weights
     // exp2(m_s - M) and the total sum of l_s weights: lane d takes splits d and d + 32,
     // summed over the lanes by a fixed butterfly
-    int lm = d < p.k ? p.pos[d] + 1 : 0;
+    const int cap = p.max_pages * p.page_size;
+    const int ps_ = d < p.k ? p.pos[d] : 0;
+    const bool bad = d < p.k && (ps_ < 0 || ps_ >= cap || ps_ >= p.rope_max_pos);
+    int lm = d < p.k ? ps_ + 1 : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, o));
-    const int cap = p.max_pages * p.page_size;
-    const int n_act = (lm <= 0 || lm > cap) ? 0 : (lm + p.chunk - 1) / p.chunk;   // 0: flagged by the attention
+    // a row out of range: the attention kernel flagged it and wrote no partials
+    const int n_act = __any_sync(0xffffffffu, bad) ? 0 : (lm + p.chunk - 1) / p.chunk;
     float mk[kMaxSplitsV / 32], lk[kMaxSplitsV / 32], M = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kMaxSplitsV / 32; ++u) {
