@@ -43,10 +43,15 @@ def _check_kv(mt, ks, vs, p, n, tol=2e-2):
             assert rel_max_abs(got[:, p:p + n], ref[:, p:p + n]) < tol, li
 
 
-# QD_PREFILL_P_HILO: the attention's P as bf16 hi + lo (1) or its bf16 value alone (0)
-@pytest.mark.parametrize("n,hilo", [(1, 1), (63, 1), (130, 1), (1030, 1), (130, 0), (1030, 0)])
-def test_prefill_bf16(cuda_lib, parity_log, monkeypatch, n, hilo):
+# QD_PREFILL_P_HILO: the mma.sync attention's P as bf16 hi + lo (1) or its bf16 value
+# alone (0); QD_PREFILL_ATTN=tc: the tcgen05 attention (128-row query tiles: ragged
+# tiles at 1, 63, 130 and 1030 rows)
+@pytest.mark.parametrize("n,hilo,attn", [(1, 1, "mma"), (63, 1, "mma"), (130, 1, "mma"), (1030, 1, "mma"),
+                                         (130, 0, "mma"), (1030, 0, "mma"), (1, 1, "tc"), (63, 1, "tc"),
+                                         (130, 1, "tc"), (1030, 1, "tc")])
+def test_prefill_bf16(cuda_lib, parity_log, monkeypatch, n, hilo, attn):
     monkeypatch.setenv("QD_PREFILL_P_HILO", str(hilo))
+    monkeypatch.setenv("QD_PREFILL_ATTN", attn)
     mt = synth.make_model(synth.SMALL64, "bf16", 60 + n, DEV, ctx=37, steps=n + 4)
     om = oracle_model(mt)
     dec = api.Decoder(mt, max_steps=n + 4, prefill_max=n)
@@ -65,7 +70,7 @@ def test_prefill_bf16(cuda_lib, parity_log, monkeypatch, n, hilo):
     if oracle.argmax_first(ref) != tk:   # only at a near tie
         top = np.sort(ref)[-2:]
         assert top[1] - top[0] < 4 * np.max(np.abs(got - ref))
-    parity_log[f"prefill_bf16_n{n}_hilo{hilo}"] = err
+    parity_log[f"prefill_bf16_n{n}_hilo{hilo}_{attn}"] = err
     assert api.check_device_error() == 0
 
 
@@ -92,9 +97,11 @@ def test_prefill_then_decode(cuda_lib, parity_log):
     assert api.check_device_error() == 0
 
 
-def test_prefill_paged_cache(cuda_lib):
+@pytest.mark.parametrize("attn", ["mma", "tc"])
+def test_prefill_paged_cache(cuda_lib, monkeypatch, attn):
     # a paged cache (16-token pages through a permuted page table): same logits and
     # K/V as the oracle on the logical sequence
+    monkeypatch.setenv("QD_PREFILL_ATTN", attn)
     n = 75
     mt = synth.make_model(synth.SMALL64, "bf16", 88, DEV, batch=1, ctx=None, steps=n + 2, paged=True)
     om = oracle_model(mt)
@@ -130,11 +137,12 @@ def test_prefill_q8_0(cuda_lib, parity_log):
     assert api.check_device_error() == 0
 
 
-@pytest.mark.parametrize("hilo", [1, 0])
-def test_prefill_qwen3_8b_layer(cuda_lib, parity_log, monkeypatch, hilo):
+@pytest.mark.parametrize("hilo,attn", [(1, "mma"), (0, "mma"), (1, "tc")])
+def test_prefill_qwen3_8b_layer(cuda_lib, parity_log, monkeypatch, hilo, attn):
     """Full Qwen3-8B shapes: one layer after a 4096-token cache, a 70-token prompt;
     sampled rows' residuals whole, every K/V row, and sampled LM-head rows."""
     monkeypatch.setenv("QD_PREFILL_P_HILO", str(hilo))
+    monkeypatch.setenv("QD_PREFILL_ATTN", attn)
     s = synth.QWEN3_8B
     n = 70
     mt = synth.make_model(s, "bf16", 5, DEV, n_layers=1, ctx=4096, steps=n)
@@ -158,7 +166,7 @@ def test_prefill_qwen3_8b_layer(cuda_lib, parity_log, monkeypatch, hilo):
     lg = dec.prefill_logits.double().cpu().numpy()
     assert rel_max_abs(lg[rows], oracle.lm_head_rows(om, res[n - 1], rows)) < 1e-3
     assert int(dec.tok[0]) == oracle.argmax_first(lg)
-    parity_log[f"prefill_qwen3_8b_layer_hilo{hilo}"] = worst
+    parity_log[f"prefill_qwen3_8b_layer_hilo{hilo}_{attn}"] = worst
     assert api.check_device_error() == 0
 
 

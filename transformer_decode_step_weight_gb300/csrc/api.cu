@@ -1223,6 +1223,8 @@ struct PrefillWs {
   void* xn;          // bf16 [n, max(H, F)]
   int32_t* vpos;     // [n] positions of the rows
   void* argmax_ws;
+  void* kv_pack;     // the tcgen05 attention's packed K / V copies
+  size_t kv_pack_bytes;
   size_t total;
 };
 
@@ -1242,6 +1244,9 @@ PrefillWs prefill_ws_layout(const qd_step_args* a, int n, void* base) {
   w.xn = (void*)(p + off); off += al256((size_t)n * std::max(d.hidden, d.ffn) * 2);
   w.vpos = (int32_t*)(p + off); off += al256((size_t)n * 4);
   w.argmax_ws = (void*)(p + off); off += al256(argmax_workspace_bytes(1));
+  w.kv_pack = (void*)(p + off);
+  w.kv_pack_bytes = prefill_attention_tc_scratch_bytes(d.n_kv_heads, a->max_pages * a->page_size);
+  off += al256(w.kv_pack_bytes);
   w.total = step_bytes + off;
   return w;
 }
@@ -1289,6 +1294,10 @@ int run_prefill(const qd_step_args* a, const int32_t* tokens, int n, float* logi
     g.W = W; g.S = S; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
     return launch_gemm_tc(g, L);
   };
+  // QD_PREFILL_ATTN (read per call): "tc" runs the attention on tcgen05, otherwise the
+  // mma.sync kernel
+  const char* pa = getenv("QD_PREFILL_ATTN");
+  const bool tc_attn = pa && strcmp(pa, "tc") == 0;
   QD_TRY(launch_prefill_prep(a->pos, n, w.vpos, L), "prefill prep");
   QD_TRY(launch_embed(a->embed, H, a->vocab, tokens, n, w.res, L), "embed");
   for (int li = 0; li < a->n_layers; ++li) {
@@ -1306,7 +1315,10 @@ int run_prefill(const qd_step_args* a, const int32_t* tokens, int n, float* logi
     at.pos = a->pos; at.k_pages = a->k_cache[li]; at.v_pages = a->v_cache[li]; at.page_table = a->page_table;
     at.page_size = a->page_size; at.max_pages = a->max_pages; at.n_pages = a->n_pages;
     at.scale = 1.0f / sqrtf((float)D); at.out = w.attn;
-    QD_TRY(launch_prefill_attention(at, L), "prefill attention");
+    if (tc_attn)
+      QD_TRY(launch_prefill_attention_tc(at, w.kv_pack, w.kv_pack_bytes, L), "prefill attention (tcgen05)");
+    else
+      QD_TRY(launch_prefill_attention(at, L), "prefill attention");
     QD_TRY(gemm(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, n, EPI_RESID_ADD, w.res), "o gemm");
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, n, H, d.rms_eps, w.xn, L), "rmsnorm");
     if (!q8 && gemm_tc_swiglu_supported(F, H, n)) {  // SwiGLU in the gate+up GEMM's epilogue

@@ -274,6 +274,12 @@ struct PrefillAttnArgs {
   void* out;               // bf16 [n, Hq D]
 };
 cudaError_t launch_prefill_attention(const PrefillAttnArgs& a, const Launch& L);
+// The tcgen05 form (prefill_tc.cu): a packing kernel copies the kv heads' keys [0, pos[0]
+// + n) into `scratch` (K as is, V transposed; prefill_attention_tc_scratch_bytes bytes,
+// cap = max_pages * page_size), then the attention reads them by TMA.
+size_t prefill_attention_tc_scratch_bytes(int Hkv, int cap);
+cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, void* scratch, size_t scratch_bytes,
+                                        const Launch& L);
 cudaError_t launch_prefill_prep(const int32_t* pos, int n, int32_t* vpos, const Launch& L);
 cudaError_t launch_prefill_finish(int32_t* pos, int n, const Launch& L);
 

@@ -1,0 +1,447 @@
+// Causal prefill attention on the tcgen05 tensor cores.
+//
+// "qwen3-8b-rtx4080-cutedsl" README, "Flash Attention 2": the prompt's rows attend
+// causally in key tiles with an online softmax, the score and probability tiles never
+// leaving the chip; "GQA + QK-Norm": per-head RMSNorm of q and RoPE before the scores.
+// Row i of the prompt sits at position pos[0] + i and attends to keys 0 .. pos[0] + i.
+//
+// GB300 layout: one CTA per (128 query rows, q head). The queries (norm, RoPE, softmax
+// scale with log2 e folded in) are staged once as bf16 hi + lo in 128-byte-swizzled
+// K-major tiles. Per 64-key tile:
+//   * S[128 x 64] = Q K^T on tcgen05 into TMEM (16 MMAs: M 128, N 64, K 16, the hi and
+//     the lo half of q), K streamed by TMA from a packed copy of the kv head's keys;
+//   * each of 128 threads owns one query row (its TMEM lane): it loads its 64 scores,
+//     masks keys past its position, and keeps a reference maximum that moves only when
+//     a score passes it by more than 8 (a factor 256) so the accumulator in TMEM is
+//     rescaled rarely; p = exp2(s - m_ref) goes to shared memory as bf16 hi + lo in
+//     the swizzled layout the MMA reads;
+//   * O[128 x 128] += P V on tcgen05 (8 MMAs: M 128, N 128, K 16) with V streamed as a
+//     transposed copy [128 dims x keys], so both operands are K-major.
+// A producer/issuer thread keeps two K / V tiles in flight and issues S of the next
+// tile while the threads finish the current one. Every wait is bounded.
+#include "common.cuh"
+#include "kernels.h"
+#include "launch.cuh"
+#include "tc_common.cuh"
+
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+
+namespace qd {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kQT = 128;               // query rows per CTA (the MMA's M, TMEM lanes)
+constexpr int kKT = 64;                // keys per tile (S columns)
+constexpr int kSt = 2;                 // K / V ring stages
+constexpr int kQChunk = kQT * 128;     // [128 rows x 64 bf16] swizzled chunk: 16 KB
+constexpr int kKChunk = kKT * 128;     // [64 keys x 64 bf16]: 8 KB
+constexpr int kKTile = 2 * kKChunk;    // a K tile: dims 0-63, 64-127
+constexpr int kVTile = kD * 128;       // a V^T tile [128 dims x 64 keys]: 16 KB
+constexpr int kThreads = 160;          // 4 row warps + 1 producer / issuer warp
+constexpr int kOffQh = 0;
+constexpr int kOffQl = kOffQh + 2 * kQChunk;
+constexpr int kOffK = kOffQl + 2 * kQChunk;
+constexpr int kOffV = kOffK + kSt * kKTile;
+constexpr int kOffPh = kOffV + kSt * kVTile;
+constexpr int kOffPl = kOffPh + kQChunk;
+constexpr int kOffBar = kOffPl + kQChunk;
+constexpr size_t kSmem = (size_t)kOffBar + 128 + 1024;   // barriers, slack for the 1024-byte alignment
+constexpr uint32_t kTmemCols = 256;    // S at column 0 (64), O at column 128 (128)
+constexpr float kRescale = 8.0f;       // log2 units a score may pass the reference maximum
+
+struct TcPfParams {
+  const float* qkv;                    // f32 [n, (Hq + 2 Hkv) D]
+  int n, Hq, Hkv;
+  const __nv_bfloat16* q_norm;
+  const float2* rope;
+  int rope_max_pos;
+  float eps;
+  int act_bf16;
+  const int32_t* pos;                  // pos[0]: the first prompt row's position
+  int L;                               // keys per kv head in the packed copies (a multiple of 64)
+  int cap;                             // cache capacity in tokens
+  float scale_log2;
+  __nv_bfloat16* out;                  // bf16 [n, Hq D]
+  int* err;
+};
+
+QD_DEV uint32_t pack_bf(float lo, float hi) { return f2bf_bits(lo) | (f2bf_bits(hi) << 16); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           const TcPfParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bar = (uint64_t*)(smem + kOffBar);
+  uint64_t* kv_full = bar;        // [kSt] K and V^T of a tile landed
+  uint64_t* kv_empty = bar + 2;   // [kSt] the tile's MMAs are done with it
+  uint64_t* s_full = bar + 4;     // S of the current tile in TMEM
+  uint64_t* p_full = bar + 5;     // 128 rows: S read, P written (and O rescaled)
+  uint64_t* o_done = bar + 6;     // the P V MMAs of a tile completed
+  uint32_t* tslot = (uint32_t*)(bar + 7);
+  int* s_abort = (int*)(tslot + 1);
+
+  const int qt = (int)(gridDim.x - 1 - blockIdx.x), h = blockIdx.y;   // longest query tiles first
+  const int g = h / (p.Hq / p.Hkv);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  pdl_wait();   // q, the packed K / V come from the kernels before this one
+  pdl_launch_dependents();
+  const int pos0 = p.pos[0];
+  if (pos0 < 0 || pos0 + p.n > p.cap || pos0 + p.n > p.rope_max_pos || pos0 + p.n > p.L) {
+    if (qt == 0 && h == 0 && tid == 0) set_error(p.err, QD_DEVERR_POS);
+    return;
+  }
+  const int r0 = qt * kQT;
+  const int nrows = min(kQT, p.n - r0);
+  const int kend = pos0 + r0 + nrows;                 // keys [0, kend) are visible to some row
+  const int n_kt = (kend + kKT - 1) / kKT;
+
+  if (tid == 0) {
+    for (int i = 0; i < kSt; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kQT);
+    mbar_init(o_done, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tc::alloc(tslot, kTmemCols);
+
+  // ---- queries: warp w builds rows 32w .. 32w + 31, four at a time; lane holds dims
+  // 4 lane .. + 3 (the arithmetic and order of the mma.sync prefill kernel)
+  if (warp < 4) {
+    const int qkv_w = (p.Hq + 2 * p.Hkv) * kD;
+    const int d0 = 4 * lane;
+    const uint2 wq = *(const uint2*)(p.q_norm + d0);
+    const float nw[4] = {bf_lo(wq.x), bf_hi(wq.x), bf_lo(wq.y), bf_hi(wq.y)};
+    constexpr int kRB = 4;
+    for (int rb = 0; rb < 32; rb += kRB) {
+      float4 xr[kRB];
+      float4 cr[kRB][2];
+#pragma unroll
+      for (int i = 0; i < kRB; ++i) {
+        const int row = r0 + warp * 32 + rb + i;
+        if (row < p.n) {
+          xr[i] = *(const float4*)(p.qkv + (size_t)row * qkv_w + (size_t)h * kD + d0);
+          const float4* cs = (const float4*)(p.rope + (size_t)(pos0 + row) * (kD / 2) + (d0 & 63));
+          cr[i][0] = cs[0];
+          cr[i][1] = cs[1];
+        } else {
+          xr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          cr[i][0] = cr[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRB; ++i) {
+        const int lr = warp * 32 + rb + i, row = r0 + lr;
+        float qv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row < p.n) {   // uniform over the warp
+          const float xs[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+          const float ss = warp_sum(xs[0] * xs[0] + xs[1] * xs[1] + xs[2] * xs[2] + xs[3] * xs[3]);
+          const float inv = 1.0f / sqrtf(ss / (float)kD + p.eps);
+          float y[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float nv = xs[e] * inv;
+            if (p.act_bf16) nv = round_bf16(nv);
+            y[e] = nw[e] * nv;
+            if (p.act_bf16) y[e] = round_bf16(y[e]);
+          }
+          const float cc[4][2] = {{cr[i][0].x, cr[i][0].y}, {cr[i][0].z, cr[i][0].w},
+                                  {cr[i][1].x, cr[i][1].y}, {cr[i][1].z, cr[i][1].w}};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float other = __shfl_xor_sync(0xffffffffu, y[e], 16);   // dim d ^ 64
+            const float r = lane < 16 ? (y[e] * cc[e][0] - other * cc[e][1]) : (y[e] * cc[e][0] + other * cc[e][1]);
+            qv[e] = r * p.scale_log2;
+          }
+        }
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(qv[2 * e]), h1 = __float2bfloat16_rn(qv[2 * e + 1]);
+          hi[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          lo[e] = pack_bf(qv[2 * e] - __bfloat162float(h0), qv[2 * e + 1] - __bfloat162float(h1));
+        }
+        // dims d0 .. d0 + 3: chunk d0 / 64, 16-byte piece (d0 % 64) / 8, half (d0 % 8) / 4
+        const uint32_t o = (uint32_t)((lane >> 4) * kQChunk) + tc::sw128_off(lr, (lane & 15) >> 1) +
+                           (uint32_t)((lane & 1) * 8);
+        *(uint2*)(smem + kOffQh + o) = make_uint2(hi[0], hi[1]);
+        *(uint2*)(smem + kOffQl + o) = make_uint2(lo[0], lo[1]);
+      }
+    }
+    fence_proxy_async_smem();   // the MMAs read these tiles through the async proxy
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase, tO = tbase + 128;
+
+  if (warp == 4) {
+    if (lane == 0) {  // ---- producer and MMA issuer
+      const uint32_t sQh = smem_u32(smem + kOffQh), sQl = smem_u32(smem + kOffQl);
+      const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+      const uint32_t sPh = smem_u32(smem + kOffPh), sPl = smem_u32(smem + kOffPl);
+      int issued = 0, landed = 0;   // tiles whose copies were issued / waited for
+      auto load = [&](int i) {  // tile i into stage i % kSt
+        const int st = i % kSt;
+        issued = i + 1;
+        unsigned char* k = smem + kOffK + st * kKTile;
+        mbar_arrive_expect_tx(&kv_full[st], kKTile + kVTile);
+        tma_load_2d(k, &tmK, 0, g * p.L + i * kKT, &kv_full[st]);
+        tma_load_2d(k + kKChunk, &tmK, 64, g * p.L + i * kKT, &kv_full[st]);
+        tma_load_2d(smem + kOffV + st * kVTile, &tmV, i * kKT, g * kD, &kv_full[st]);
+      };
+      auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i
+        const int st = i % kSt;
+        if (!mbar_wait_bounded(&kv_full[st], (uint32_t)((i / kSt) & 1), p.err)) return false;
+        landed = i + 1;
+        tc::fence_after();
+        const uint32_t k0 = sK + st * kKTile;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t qo = (j >> 2) * kQChunk + (j & 3) * 32, ko = (j >> 2) * kKChunk + (j & 3) * 32;
+          tc::mma<kKT>(tS, tc::desc_sw128(sQh + qo), tc::desc_sw128(k0 + ko), j != 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t qo = (j >> 2) * kQChunk + (j & 3) * 32, ko = (j >> 2) * kKChunk + (j & 3) * 32;
+          tc::mma<kKT>(tS, tc::desc_sw128(sQl + qo), tc::desc_sw128(k0 + ko), 1);
+        }
+        tc::commit(s_full);
+        return true;
+      };
+      load(0);
+      if (n_kt > 1) load(1);
+      bool ok = mma_s(0);
+      for (int i = 0; i < n_kt && ok; ++i) {
+        // the rows read S(i), wrote P(i) and rescaled O where needed
+        if (!mbar_wait_bounded(p_full, (uint32_t)(i & 1), p.err)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after();
+        const int st = i % kSt;
+        const uint32_t v0 = sV + st * kVTile;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma<kD>(tO, tc::desc_sw128(sPh + kk * 32), tc::desc_sw128(v0 + kk * 32), (i | kk) != 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) tc::mma<kD>(tO, tc::desc_sw128(sPl + kk * 32), tc::desc_sw128(v0 + kk * 32), 1);
+        tc::commit(o_done);
+        tc::commit(&kv_empty[st]);
+        if (i + 1 < n_kt && !(ok = mma_s(i + 1))) break;   // S is free: the rows read it before P(i)
+        if (i + 2 < n_kt) {  // refill this stage once tile i's MMAs are done with it
+          if (!mbar_wait_bounded(&kv_empty[st], (uint32_t)((i / kSt) & 1), p.err)) {
+            ok = false;
+            break;
+          }
+          load(i + 2);
+        }
+      }
+      if (!ok) *(volatile int*)s_abort = 1;
+      // copies still in flight after an early stop land before the CTA leaves (bounded)
+      for (int t = landed; t < issued; ++t)
+        mbar_wait_limit(&kv_full[t % kSt], (uint32_t)((t / kSt) & 1), p.err, 10000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ---- one query row per thread (TMEM lane tid)
+    const int r = tid, row = r0 + r;
+    const bool valid = row < p.n;
+    const int rowpos = pos0 + row;
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool fail = false;
+    for (int i = 0; i < n_kt; ++i) {
+      const bool got = mbar_wait_bounded(s_full, (uint32_t)(i & 1), p.err) && !*(volatile int*)s_abort;
+      if (!__all_sync(0xffffffffu, got)) {   // the same decision in every lane (warp-wide TMEM loads)
+        fail = true;
+        break;
+      }
+      tc::fence_after();
+      float s[kKT];
+      tc::ld_32x32(tS + lanes, s);
+      tc::ld_32x32(tS + lanes + 32, s + 32);
+      const int key0 = i * kKT;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kKT; ++j) {
+        if (!valid || key0 + j > rowpos) s[j] = -INFINITY;
+        mx = fmaxf(mx, s[j]);
+      }
+      // move the reference maximum where a score passes it by more than kRescale; O and
+      // l follow it. The O rows of the warp are rescaled together (warp-wide TMEM access);
+      // every P V MMA so far has completed (waited at the end of the last tile).
+      const bool move = mx > m_ref + kRescale;
+      const float alpha = move ? exp2f(m_ref - mx) : 1.f;   // 0 while m_ref is -inf
+      if (i > 0 && __any_sync(0xffffffffu, move)) {
+#pragma unroll
+        for (int c = 0; c < kD; c += 32) {
+          float ov[32];
+          tc::ld_32x32(tO + lanes + c, ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] *= alpha;
+          tc::st_32x32(tO + lanes + c, ov);
+        }
+      }
+      if (move) {
+        l *= alpha;
+        m_ref = mx;
+      }
+      float ps = 0.f;
+      unsigned char* ph = smem + kOffPh;
+      unsigned char* pl = smem + kOffPl;
+#pragma unroll
+      for (int c = 0; c < kKT / 8; ++c) {   // 8 keys per 16-byte piece
+        float pv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float sv = s[8 * c + e];
+          pv[e] = sv == -INFINITY ? 0.f : exp2f(sv - m_ref);
+          ps += pv[e];
+        }
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(pv[2 * e]), h1 = __float2bfloat16_rn(pv[2 * e + 1]);
+          hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          lw[e] = pack_bf(pv[2 * e] - __bfloat162float(h0), pv[2 * e + 1] - __bfloat162float(h1));
+        }
+        const uint32_t o = tc::sw128_off(r, c);
+        *(uint4*)(ph + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *(uint4*)(pl + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      l += ps;
+      fence_proxy_async_smem();
+      tc::fence_before();
+      mbar_arrive(p_full);
+      // the P V MMAs of this tile read P: wait for them before the next tile's P
+      const bool done = mbar_wait_bounded(o_done, (uint32_t)(i & 1), p.err);
+      if (!__all_sync(0xffffffffu, done)) {
+        fail = true;
+        break;
+      }
+    }
+    if (fail) *(volatile int*)s_abort = 1;
+    if (!fail) {   // warp-uniform; rows past the prompt load too (warp-wide) but store nothing
+      tc::fence_after();
+      const float inv = valid ? 1.0f / l : 0.f;
+      __nv_bfloat16* out = p.out + (size_t)(valid ? row : 0) * p.Hq * kD + (size_t)h * kD;
+#pragma unroll
+      for (int c = 0; c < kD; c += 32) {
+        float ov[32];
+        tc::ld_32x32(tO + lanes + c, ov);
+        if (valid)
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            *(uint4*)(out + c + e) =
+                make_uint4(pack_bf(ov[e] * inv, ov[e + 1] * inv), pack_bf(ov[e + 2] * inv, ov[e + 3] * inv),
+                           pack_bf(ov[e + 4] * inv, ov[e + 5] * inv), pack_bf(ov[e + 6] * inv, ov[e + 7] * inv));
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after();
+    tc::dealloc(tbase, kTmemCols);
+  }
+}
+
+// Packed copies of one kv head's keys for the kernel above: K [L][128] as is, V
+// transposed to [128][L], rows past the prompt's last position zero. One CTA per 64
+// keys and kv head.
+__global__ void __launch_bounds__(128) prefill_kv_pack_kernel(const __nv_bfloat16* k_pages,
+                                                              const __nv_bfloat16* v_pages, const int32_t* pt,
+                                                              int page_size, int n_pages, int Hkv, const int32_t* pos,
+                                                              int n, int L, __nv_bfloat16* ks, __nv_bfloat16* vt,
+                                                              int* err) {
+  __shared__ __align__(16) __nv_bfloat16 sv[kKT][kD + 8];
+  const int t0 = blockIdx.x * kKT, g = blockIdx.y, tid = threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int kv_len = min(pos[0] + n, L);
+  if (t0 >= kv_len) return;   // never read
+  for (int i = tid; i < kKT * 16; i += 128) {
+    const int r = i >> 4, c = i & 15;
+    const int key = t0 + r;
+    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+    if (key < kv_len) {
+      const PagedSlot sl = paged_slot(pt, key, page_size, n_pages);
+      if (!sl.ok) {
+        set_error(err, QD_DEVERR_PAGE);
+      } else {
+        const size_t off = (((size_t)sl.page * Hkv + g) * page_size + sl.slot) * kD + c * 8;
+        kv = *(const uint4*)(k_pages + off);
+        vv = *(const uint4*)(v_pages + off);
+      }
+    }
+    *(uint4*)(ks + ((size_t)g * L + key) * kD + c * 8) = kv;
+    *(uint4*)(&sv[r][c * 8]) = vv;
+  }
+  __syncthreads();
+  // thread d writes V^T row d for these 64 keys (128 bytes)
+  const int d = tid;
+  __nv_bfloat16* dst = vt + ((size_t)g * kD + d) * L + t0;
+#pragma unroll
+  for (int j = 0; j < kKT; j += 8) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = (uint32_t)__bfloat16_as_ushort(sv[j + 2 * e][d]) |
+             ((uint32_t)__bfloat16_as_ushort(sv[j + 2 * e + 1][d]) << 16);
+    *(uint4*)(dst + j) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+}  // namespace
+
+size_t prefill_attention_tc_scratch_bytes(int Hkv, int cap) {
+  const size_t L = ((size_t)cap + kKT - 1) / kKT * kKT;
+  return 2 * (size_t)Hkv * L * kD * 2;
+}
+
+cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, void* scratch, size_t scratch_bytes,
+                                        const Launch& L) {
+  if (a.n < 1 || a.D != kD || a.Hkv < 1 || a.Hq % a.Hkv) return cudaErrorInvalidValue;
+  const int cap = a.max_pages * a.page_size;
+  const int Lk = (cap + kKT - 1) / kKT * kKT;
+  if (!scratch || scratch_bytes < prefill_attention_tc_scratch_bytes(a.Hkv, cap)) return cudaErrorInvalidValue;
+  __nv_bfloat16* ks = (__nv_bfloat16*)scratch;
+  __nv_bfloat16* vt = ks + (size_t)a.Hkv * Lk * kD;
+  cudaError_t e = launch_ex(prefill_kv_pack_kernel, dim3(Lk / kKT, a.Hkv), dim3(128), 0, L,
+                            (const __nv_bfloat16*)a.k_pages, (const __nv_bfloat16*)a.v_pages, a.page_table,
+                            a.page_size, a.n_pages, a.Hkv, a.pos, a.n, Lk, ks, vt, L.err);
+  if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  e = encode_tmap_bf16_2d(&tk, ks, (uint64_t)a.Hkv * Lk, kD, kKT);
+  if (e != cudaSuccess) return e;
+  e = encode_tmap_bf16_2d(&tv, vt, (uint64_t)a.Hkv * kD, (uint64_t)Lk, kD);
+  if (e != cudaSuccess) return e;
+  TcPfParams p = {};
+  p.qkv = a.qkv; p.n = a.n; p.Hq = a.Hq; p.Hkv = a.Hkv;
+  p.q_norm = (const __nv_bfloat16*)a.q_norm; p.rope = (const float2*)a.rope; p.rope_max_pos = a.rope_max_pos;
+  p.eps = a.eps; p.act_bf16 = a.act_bf16; p.pos = a.pos; p.L = Lk; p.cap = cap;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.out = (__nv_bfloat16*)a.out; p.err = L.err;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(prefill_attn_tc_kernel, dim3(ceil_div(a.n, kQT), a.Hq), dim3(kThreads), kSmem, L, tk, tv, p);
+}
+
+}  // namespace qd
