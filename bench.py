@@ -919,7 +919,7 @@ def run_prefill_bench(args):
     bpeak, bkind = tensor_peak(sustained=False)
     out = {"metric": f"prefill of an {n}-token prompt (one sequence)", "value": round(n / (ms / 1e3), 1),
            "unit": "prompt tok/s", "ms_per_prefill": round(ms, 3), "higher_is_better": True,
-           "dtype": "bf16 tcgen05 GEMMs + bf16 mma.sync attention" if wl.wtype == "bf16" else
+           "dtype": ("bf16 tcgen05 GEMMs + bf16 mma.sync attention" if os.environ.get("QD_PREFILL_ATTN") == "mma" else "bf16 tcgen05 GEMMs + bf16 tcgen05 attention") if wl.wtype == "bf16" else
                     "q8_0 widened to bf16, tcgen05 GEMMs + bf16 mma.sync attention",
            "data": "synthetic",
            "config": {"workload": wl.name, "prompt_tokens": n, "positions": f"0..{n - 1}",

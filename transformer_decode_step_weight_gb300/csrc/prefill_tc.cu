@@ -44,13 +44,13 @@ constexpr int kVTile = kD * 128;       // a V^T tile [128 dims x 64 keys]: 16 KB
 constexpr int kThreads = 160;          // 4 row warps + 1 producer / issuer warp
 constexpr int kOffQh = 0;
 constexpr int kOffQl = kOffQh + 2 * kQChunk;
-constexpr int kOffK = kOffQl + 2 * kQChunk;
-constexpr int kOffV = kOffK + kSt * kKTile;
-constexpr int kOffPh = kOffV + kSt * kVTile;
-constexpr int kOffPl = kOffPh + kQChunk;
-constexpr int kOffBar = kOffPl + kQChunk;
+constexpr int kOffK = kOffQl + 2 * kQChunk;      // K ring [kSt]
+constexpr int kOffV = kOffK + kSt * kKTile;      // V^T ring [kSt]
+constexpr int kOffPh = kOffV + kSt * kVTile;     // P hi [2 buffers]
+constexpr int kOffPl = kOffPh + 2 * kQChunk;     // P lo [2 buffers]
+constexpr int kOffBar = kOffPl + 2 * kQChunk;
 constexpr size_t kSmem = (size_t)kOffBar + 128 + 1024;   // barriers, slack for the 1024-byte alignment
-constexpr uint32_t kTmemCols = 256;    // S at column 0 (64), O at column 128 (128)
+constexpr uint32_t kTmemCols = 256;    // S buffers at columns 0 and 64, O at column 128 (128)
 constexpr float kRescale = 8.0f;       // log2 units a score may pass the reference maximum
 
 struct TcPfParams {
@@ -77,12 +77,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bar = (uint64_t*)(smem + kOffBar);
-  uint64_t* kv_full = bar;        // [kSt] K and V^T of a tile landed
-  uint64_t* kv_empty = bar + 2;   // [kSt] the tile's MMAs are done with it
-  uint64_t* s_full = bar + 4;     // S of the current tile in TMEM
-  uint64_t* p_full = bar + 5;     // 128 rows: S read, P written (and O rescaled)
-  uint64_t* o_done = bar + 6;     // the P V MMAs of a tile completed
-  uint32_t* tslot = (uint32_t*)(bar + 7);
+  uint64_t* k_full = bar;         // [kSt] a K tile landed
+  uint64_t* k_empty = bar + 2;    // [kSt] its S MMAs are done with it
+  uint64_t* v_full = bar + 4;     // [kSt] a V^T tile landed
+  uint64_t* v_empty = bar + 6;    // [kSt] its P V MMAs are done with it (and with that P buffer)
+  uint64_t* s_full = bar + 8;     // [2] S of a tile in its TMEM buffer
+  uint64_t* p_full = bar + 10;    // [2] 128 rows read S and wrote P into that buffer (O rescaled)
+  uint64_t* o_done = bar + 12;    // [2] the P V MMAs of a tile completed
+  uint32_t* tslot = (uint32_t*)(bar + 14);
   int* s_abort = (int*)(tslot + 1);
 
   const int qt = (int)(gridDim.x - 1 - blockIdx.x), h = blockIdx.y;   // longest query tiles first
@@ -102,13 +104,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kt = (kend + kKT - 1) / kKT;
 
   if (tid == 0) {
-    for (int i = 0; i < kSt; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kQT);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, kQT);
-    mbar_init(o_done, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -183,74 +187,99 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tO = tbase + 128;
+  const uint32_t tS = tbase, tO = tbase + 128;   // S buffer b at tS + 64 b
 
   if (warp == 4) {
     if (lane == 0) {  // ---- producer and MMA issuer
       const uint32_t sQh = smem_u32(smem + kOffQh), sQl = smem_u32(smem + kOffQl);
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sPh = smem_u32(smem + kOffPh), sPl = smem_u32(smem + kOffPl);
-      int issued = 0, landed = 0;   // tiles whose copies were issued / waited for
-      auto load = [&](int i) {  // tile i into stage i % kSt
-        const int st = i % kSt;
-        issued = i + 1;
-        unsigned char* k = smem + kOffK + st * kKTile;
-        mbar_arrive_expect_tx(&kv_full[st], kKTile + kVTile);
-        tma_load_2d(k, &tmK, 0, g * p.L + i * kKT, &kv_full[st]);
-        tma_load_2d(k + kKChunk, &tmK, 64, g * p.L + i * kKT, &kv_full[st]);
-        tma_load_2d(smem + kOffV + st * kVTile, &tmV, i * kKT, g * kD, &kv_full[st]);
+      int k_issued = 0, k_landed = 0, v_issued = 0, v_landed = 0;   // tiles issued / waited for
+      auto load_k = [&](int i) {  // K tile i into stage i % 2
+        const int b = i & 1;
+        unsigned char* k = smem + kOffK + b * kKTile;
+        mbar_arrive_expect_tx(&k_full[b], kKTile);
+        tma_load_2d(k, &tmK, 0, g * p.L + i * kKT, &k_full[b]);
+        tma_load_2d(k + kKChunk, &tmK, 64, g * p.L + i * kKT, &k_full[b]);
+        k_issued = i + 1;
       };
-      auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i
-        const int st = i % kSt;
-        if (!mbar_wait_bounded(&kv_full[st], (uint32_t)((i / kSt) & 1), p.err)) return false;
-        landed = i + 1;
+      auto load_v = [&](int i) {  // V^T tile i into stage i % 2
+        const int b = i & 1;
+        mbar_arrive_expect_tx(&v_full[b], kVTile);
+        tma_load_2d(smem + kOffV + b * kVTile, &tmV, i * kKT, g * kD, &v_full[b]);
+        v_issued = i + 1;
+      };
+      auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i into S buffer i % 2
+        const int b = i & 1;
+        if (!mbar_wait_bounded(&k_full[b], (uint32_t)((i >> 1) & 1), p.err)) return false;
+        k_landed = i + 1;
         tc::fence_after();
-        const uint32_t k0 = sK + st * kKTile;
+        const uint32_t k0 = sK + b * kKTile, ts = tS + 64 * b;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t qo = (j >> 2) * kQChunk + (j & 3) * 32, ko = (j >> 2) * kKChunk + (j & 3) * 32;
-          tc::mma<kKT>(tS, tc::desc_sw128(sQh + qo), tc::desc_sw128(k0 + ko), j != 0);
+          tc::mma<kKT>(ts, tc::desc_sw128(sQh + qo), tc::desc_sw128(k0 + ko), j != 0);
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t qo = (j >> 2) * kQChunk + (j & 3) * 32, ko = (j >> 2) * kKChunk + (j & 3) * 32;
-          tc::mma<kKT>(tS, tc::desc_sw128(sQl + qo), tc::desc_sw128(k0 + ko), 1);
+          tc::mma<kKT>(ts, tc::desc_sw128(sQl + qo), tc::desc_sw128(k0 + ko), 1);
         }
-        tc::commit(s_full);
+        tc::commit(&s_full[b]);
+        tc::commit(&k_empty[b]);
         return true;
       };
-      load(0);
-      if (n_kt > 1) load(1);
+      load_k(0);
+      load_v(0);
+      if (n_kt > 1) {
+        load_k(1);
+        load_v(1);
+      }
       bool ok = mma_s(0);
+      if (ok && n_kt > 1) ok = mma_s(1);
       for (int i = 0; i < n_kt && ok; ++i) {
-        // the rows read S(i), wrote P(i) and rescaled O where needed
-        if (!mbar_wait_bounded(p_full, (uint32_t)(i & 1), p.err)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after();
-        const int st = i % kSt;
-        const uint32_t v0 = sV + st * kVTile;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma<kD>(tO, tc::desc_sw128(sPh + kk * 32), tc::desc_sw128(v0 + kk * 32), (i | kk) != 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) tc::mma<kD>(tO, tc::desc_sw128(sPl + kk * 32), tc::desc_sw128(v0 + kk * 32), 1);
-        tc::commit(o_done);
-        tc::commit(&kv_empty[st]);
-        if (i + 1 < n_kt && !(ok = mma_s(i + 1))) break;   // S is free: the rows read it before P(i)
-        if (i + 2 < n_kt) {  // refill this stage once tile i's MMAs are done with it
-          if (!mbar_wait_bounded(&kv_empty[st], (uint32_t)((i / kSt) & 1), p.err)) {
+        const int b = i & 1;
+        const uint32_t ph = (uint32_t)((i >> 1) & 1);
+        // K tile i + 2 into this stage as soon as the S MMAs of tile i are done with it
+        if (i + 2 < n_kt) {
+          if (!mbar_wait_bounded(&k_empty[b], ph, p.err)) {
             ok = false;
             break;
           }
-          load(i + 2);
+          load_k(i + 2);
+        }
+        // the rows read S(i), wrote P(i) into buffer b and rescaled O where needed
+        if (!mbar_wait_bounded(&p_full[b], ph, p.err) || !mbar_wait_bounded(&v_full[b], ph, p.err)) {
+          ok = false;
+          break;
+        }
+        v_landed = i + 1;
+        tc::fence_after();
+        const uint32_t v0 = sV + b * kVTile, p_h = sPh + b * kQChunk, p_l = sPl + b * kQChunk;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma<kD>(tO, tc::desc_sw128(p_h + kk * 32), tc::desc_sw128(v0 + kk * 32), (i | kk) != 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) tc::mma<kD>(tO, tc::desc_sw128(p_l + kk * 32), tc::desc_sw128(v0 + kk * 32), 1);
+        tc::commit(&o_done[b]);
+        tc::commit(&v_empty[b]);
+        if (i + 2 < n_kt) {
+          // V tile i + 2 once these MMAs are done with the stage; then S of tile i + 2 into
+          // S buffer b (the rows read S(i) before P(i))
+          if (!mbar_wait_bounded(&v_empty[b], ph, p.err)) {
+            ok = false;
+            break;
+          }
+          load_v(i + 2);
+          if (!(ok = mma_s(i + 2))) break;
         }
       }
       if (!ok) *(volatile int*)s_abort = 1;
       // copies still in flight after an early stop land before the CTA leaves (bounded)
-      for (int t = landed; t < issued; ++t)
-        mbar_wait_limit(&kv_full[t % kSt], (uint32_t)((t / kSt) & 1), p.err, 10000000ull);
+      for (int t = k_landed; t < k_issued; ++t)
+        mbar_wait_limit(&k_full[t & 1], (uint32_t)((t >> 1) & 1), p.err, 10000000ull);
+      for (int t = v_landed; t < v_issued; ++t)
+        mbar_wait_limit(&v_full[t & 1], (uint32_t)((t >> 1) & 1), p.err, 10000000ull);
     }
     __syncwarp();
   } else {
@@ -261,16 +290,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;
     bool fail = false;
+    // wait (bounded) on a barrier phase; false in every lane if any lane gave up
+    auto wait_all = [&](uint64_t* bb, uint32_t ph) -> bool {
+      const bool got = mbar_wait_bounded(bb, ph, p.err) && !*(volatile int*)s_abort;
+      return __all_sync(0xffffffffu, got);
+    };
     for (int i = 0; i < n_kt; ++i) {
-      const bool got = mbar_wait_bounded(s_full, (uint32_t)(i & 1), p.err) && !*(volatile int*)s_abort;
-      if (!__all_sync(0xffffffffu, got)) {   // the same decision in every lane (warp-wide TMEM loads)
+      const int b = i & 1;
+      if (!wait_all(&s_full[b], (uint32_t)((i >> 1) & 1))) {   // the same decision in every lane
         fail = true;
         break;
       }
       tc::fence_after();
       float s[kKT];
-      tc::ld_32x32(tS + lanes, s);
-      tc::ld_32x32(tS + lanes + 32, s + 32);
+      tc::ld_32x32(tS + 64 * b + lanes, s);
+      tc::ld_32x32(tS + 64 * b + lanes + 32, s + 32);
       const int key0 = i * kKT;
       float mx = -INFINITY;
 #pragma unroll
@@ -279,11 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx = fmaxf(mx, s[j]);
       }
       // move the reference maximum where a score passes it by more than kRescale; O and
-      // l follow it. The O rows of the warp are rescaled together (warp-wide TMEM access);
-      // every P V MMA so far has completed (waited at the end of the last tile).
+      // l follow it. The O rows of the warp are rescaled together (warp-wide TMEM access)
+      // once every P V MMA so far (tiles up to i - 1) has completed.
       const bool move = mx > m_ref + kRescale;
       const float alpha = move ? exp2f(m_ref - mx) : 1.f;   // 0 while m_ref is -inf
       if (i > 0 && __any_sync(0xffffffffu, move)) {
+        if (!wait_all(&o_done[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1))) {
+          fail = true;
+          break;
+        }
+        tc::fence_after();
 #pragma unroll
         for (int c = 0; c < kD; c += 32) {
           float ov[32];
@@ -297,9 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
         m_ref = mx;
       }
+      // P buffer b is free once the P V MMAs of tile i - 2 are done
+      if (i >= 2 && !wait_all(&o_done[b], (uint32_t)(((i - 2) >> 1) & 1))) {
+        fail = true;
+        break;
+      }
       float ps = 0.f;
-      unsigned char* ph = smem + kOffPh;
-      unsigned char* pl = smem + kOffPl;
+      unsigned char* ph = smem + kOffPh + b * kQChunk;
+      unsigned char* pl = smem + kOffPl + b * kQChunk;
 #pragma unroll
       for (int c = 0; c < kKT / 8; ++c) {   // 8 keys per 16-byte piece
         float pv[8];
@@ -323,14 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       l += ps;
       fence_proxy_async_smem();
       tc::fence_before();
-      mbar_arrive(p_full);
-      // the P V MMAs of this tile read P: wait for them before the next tile's P
-      const bool done = mbar_wait_bounded(o_done, (uint32_t)(i & 1), p.err);
-      if (!__all_sync(0xffffffffu, done)) {
-        fail = true;
-        break;
-      }
+      mbar_arrive(&p_full[b]);
     }
+    // the last tile's P V MMAs complete before O is read
+    if (!fail && !wait_all(&o_done[(n_kt - 1) & 1], (uint32_t)(((n_kt - 1) >> 1) & 1))) fail = true;
     if (fail) *(volatile int*)s_abort = 1;
     if (!fail) {   // warp-uniform; rows past the prompt load too (warp-wide) but store nothing
       tc::fence_after();
