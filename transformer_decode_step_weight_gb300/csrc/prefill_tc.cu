@@ -403,14 +403,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(128) prefill_kv_pack_kernel(const __nv_bfloat16* k_pages,
                                                               const __nv_bfloat16* v_pages, const int32_t* pt,
                                                               int page_size, int n_pages, int Hkv, const int32_t* pos,
-                                                              int n, int L, __nv_bfloat16* ks, __nv_bfloat16* vt,
-                                                              int* err) {
+                                                              int n, int cap, int L, __nv_bfloat16* ks,
+                                                              __nv_bfloat16* vt, int* err) {
   __shared__ __align__(16) __nv_bfloat16 sv[kKT][kD + 8];
   const int t0 = blockIdx.x * kKT, g = blockIdx.y, tid = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
-  const int kv_len = min(pos[0] + n, L);
-  if (t0 >= kv_len) return;   // never read
+  // keys past the cache are never looked up (the attention kernel flags such a prompt)
+  const int kv_len = min(min(pos[0] + n, cap), L);
+  if (pos[0] < 0 || t0 >= kv_len) return;   // never read
   for (int i = tid; i < kKT * 16; i += 128) {
     const int r = i >> 4, c = i & 15;
     const int key = t0 + r;
@@ -460,7 +461,7 @@ cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, void* scratch,
   __nv_bfloat16* vt = ks + (size_t)a.Hkv * Lk * kD;
   cudaError_t e = launch_ex(prefill_kv_pack_kernel, dim3(Lk / kKT, a.Hkv), dim3(128), 0, L,
                             (const __nv_bfloat16*)a.k_pages, (const __nv_bfloat16*)a.v_pages, a.page_table,
-                            a.page_size, a.n_pages, a.Hkv, a.pos, a.n, Lk, ks, vt, L.err);
+                            a.page_size, a.n_pages, a.Hkv, a.pos, a.n, cap, Lk, ks, vt, L.err);
   if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap tk, tv;
   memset(&tk, 0, sizeof(tk));
