@@ -360,9 +360,11 @@ int qd_verify_step(const qd_step_args* args, const int32_t* draft, int k, float*
 /* tiled attention that never forms the full score matrix). For the one sequence */
 /* of `args` (batch 1): tokens int32 [n_tokens] (device) sit at positions         */
 /* pos[0] .. pos[0] + n_tokens - 1. Every layer runs over all rows at once: the   */
-/* projections are tcgen05 GEMMs over 64-token tiles, the rows' K/V are written   */
-/* to the cache first, and row i attends causally to positions 0 .. pos[0] + i    */
-/* (the keys already cached included). The last row alone goes through the final */
+/* projections are tcgen05 GEMMs over 64- or 256-token tiles, the rows' K/V are   */
+/* written to the cache first, and row i attends causally to positions 0 ..       */
+/* pos[0] + i (the keys already cached included) on tcgen05 (QD_PREFILL_ATTN=mma: */
+/* the mma.sync kernel). The workspace includes a packed copy of the kv heads'    */
+/* keys up to the cache capacity. The last row alone goes through the final       */
 /* norm and the LM head: logits f32 [vocab] (device, 16-byte aligned). The state  */
 /* then advances as one decode step from the last row: tok = argmax (first index */
 /* among equal maxima), out_tokens[step] = tok, pos += n_tokens, step += 1.      */
