@@ -924,7 +924,10 @@ def run_prefill_bench(args):
            "data": "synthetic",
            "config": {"workload": wl.name, "prompt_tokens": n, "positions": f"0..{n - 1}",
                       "graph": "one CUDA graph per prefill", "repetitions": reps, "prefills_each": k},
-           "roofline": {"bound": "tensor", "kernel": f"gemm_tc_kernel (gate+up, {2 * s.ffn} x {s.hidden} x {n} rows)",
+           "roofline": {"bound": "tensor",
+                        "kernel": (f"gemm_wide_kernel (the gate+up weights {2 * s.ffn} x {s.hidden} over {n} rows, f32 "
+                                   "out; the pass runs these MMAs with the SwiGLU epilogue)") if wl.wtype == "bf16" else
+                                  f"gemm_tc_kernel Q8_0 (gate+up, {2 * s.ffn} x {s.hidden} x {n} rows)",
                         "achieved": round(gu_tf, 1), "peak": bpeak, "unit": "TFLOP/s",
                         "frac": round(gu_tf / bpeak, 4), "peak_kind": f"{bkind} burst", "us_per_launch": round(gu_ms * 1e3, 2),
                         "traffic": None},

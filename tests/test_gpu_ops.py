@@ -99,6 +99,27 @@ def test_gemm_bf16_tensor_cores(cuda_lib, R, K, B):
         assert rel_max_abs(y[b].cpu().numpy()[rows], ref) < GEMV_TOL, b
 
 
+# many token rows (prefill): the persistent form (one CTA per SM over (weight tile,
+# 256-token tile) items, two TMEM accumulators, the default) and the one-CTA-per-tile
+# form (QD_GEMM_WIDE=tiles); ragged weight and token tiles, and more items than CTAs.
+# The residual-add epilogue runs in the prefill tests (O and down projections).
+@pytest.mark.parametrize("R,K,B", [(300, 1024, 300), (1000, 4096, 200), (4096, 4096, 512), (6144, 4096, 2048),
+                                   (24576, 4096, 1030)])
+@pytest.mark.parametrize("form", ["persistent", "tiles"])
+def test_gemm_bf16_wide(cuda_lib, monkeypatch, R, K, B, form):
+    monkeypatch.setenv("QD_GEMM_WIDE", form)
+    g = _gen(R + B + K)
+    W = (torch.randn((R, K), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    x = torch.randn((B, K), generator=g, device=DEV).to(torch.bfloat16)
+    y = api.gemv_bf16(W, x)
+    torch.cuda.synchronize()
+    Wb, xb = synth.bits_u16(W), synth.bits_u16(x)
+    rows = np.arange(R) if R <= 8192 else np.arange(0, R, 97)
+    for b in sorted({0, B // 3, B - 1}):
+        ref = oracle.gemv_bf16(Wb[rows], oracle.bf16_to_f64(xb[b]))
+        assert rel_max_abs(y[b].cpu().numpy()[rows], ref) < GEMV_TOL, b
+
+
 def test_gemm_bf16_tensor_cores_integer_exact(cuda_lib):
     g = _gen(13)
     W = torch.randint(-8, 9, (384, 512), generator=g, device=DEV).to(torch.bfloat16)

@@ -52,6 +52,20 @@ def _check_kv(mt, ks, vs, p, n, tol=2e-2):
 def test_prefill_bf16(cuda_lib, parity_log, monkeypatch, n, hilo, attn):
     monkeypatch.setenv("QD_PREFILL_P_HILO", str(hilo))
     monkeypatch.setenv("QD_PREFILL_ATTN", attn)
+    _prefill_case(parity_log, n, f"prefill_bf16_n{n}_hilo{hilo}_{attn}")
+
+
+# The prefill GEMMs above 128 rows: the persistent kernels (default) and one CTA per
+# tile (QD_GEMM_WIDE=tiles). 2100 rows = 9 token tiles (the last ragged); the gate+up
+# projection (F = 1408: 22 tiles of 64 gate over 64 up rows) gives 198 items, so CTAs
+# take a second item and reuse both accumulators and exchange buffers.
+@pytest.mark.parametrize("form", ["persistent", "tiles"])
+def test_prefill_bf16_gemm_forms(cuda_lib, parity_log, monkeypatch, form):
+    monkeypatch.setenv("QD_GEMM_WIDE", form)
+    _prefill_case(parity_log, 2100, f"prefill_bf16_n2100_{form}")
+
+
+def _prefill_case(parity_log, n, key):
     mt = synth.make_model(synth.SMALL64, "bf16", 60 + n, DEV, ctx=37, steps=n + 4)
     om = oracle_model(mt)
     dec = api.Decoder(mt, max_steps=n + 4, prefill_max=n)
@@ -70,7 +84,7 @@ def test_prefill_bf16(cuda_lib, parity_log, monkeypatch, n, hilo, attn):
     if oracle.argmax_first(ref) != tk:   # only at a near tie
         top = np.sort(ref)[-2:]
         assert top[1] - top[0] < 4 * np.max(np.abs(got - ref))
-    parity_log[f"prefill_bf16_n{n}_hilo{hilo}_{attn}"] = err
+    parity_log[key] = err
     assert api.check_device_error() == 0
 
 

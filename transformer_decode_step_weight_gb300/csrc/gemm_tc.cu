@@ -33,6 +33,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 namespace qd {
@@ -461,6 +462,247 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreadsTc, (!kQ8 && kStage
   if (warp == 0) tmem_dealloc(tmem, BN);
 }
 
+// ---- persistent wide form (many token rows, bf16 weights) ----------------------
+// One CTA per SM loops over (128-row weight tile, 256-token tile) items, the token
+// tiles of a weight tile consecutive (they share it through L2). Warp 0 streams the
+// W and X boxes through a 4-stage ring, warp 1 issues the MMAs into one of two
+// 256-column TMEM accumulators, and warps 2..5 drain the other one to y (warp w
+// reads TMEM lane quarter w % 4), so one tile's epilogue runs under the next tile's
+// MMAs instead of leaving the tensor pipe idle while the SM's next CTA refills its ring.
+constexpr int kWdSt = 4;
+constexpr int kWdBN = 256;
+constexpr int kWdTileX = kWdBN * kBK * 2;   // 32 KB
+constexpr int kWdThreads = 192;
+constexpr int kWdXch = 2 * 2 * 64 * 32 * 4;   // SwiGLU form: [2 lane pairs][2 buffers][64 columns][32 lanes] f32
+// shared memory: ring, (SwiGLU) exchange buffers, then the barriers
+__host__ __device__ constexpr size_t wd_smem(bool sw) {
+  return 1024 + (size_t)kWdSt * (kTileA + kWdTileX) + (sw ? kWdXch : 0) + (2 * kWdSt + 4 + 8) * 8 + 16;
+}
+
+// kSw = false: y[t, r] (+)= sum_k W[r, k] X[t, k], weight tiles of 128 rows.
+// kSw = true (the gate+up projection with SwiGLU): a weight tile is gate rows
+// j0 .. j0 + 63 (TMEM lanes 0..63) over up rows F + j0 .. (lanes 64..127), two 64-row
+// boxes per stage, so one M = 128 x N = 256 accumulator covers 64 outputs of h and two
+// accumulators still fit in TMEM. The up warps (lane quarters 2, 3) hand their values
+// to the gate warps (quarters 0, 1) through shared memory, 64 columns at a time, and
+// the gate warps write h[t, j] = bf16(silu(g) u) with the SwiGLU rows kernel's arithmetic.
+template <bool kSw>
+__global__ void __launch_bounds__(kWdThreads, 1) gemm_wide_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                   const __grid_constant__ CUtensorMap tmX,
+                                                                   const TcParams p, __nv_bfloat16* h, int F) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sA = smem;                              // [kWdSt][128 x 128 B]
+  unsigned char* sB = sA + kWdSt * kTileA;               // [kWdSt][256 x 128 B]
+  float* xch = (float*)(sB + kWdSt * kWdTileX);          // kSw: [pair][buf][64][32]
+  uint64_t* full = (uint64_t*)((unsigned char*)xch + (kSw ? kWdXch : 0));   // [kWdSt] W and X boxes landed
+  uint64_t* empty = full + kWdSt;                        // [kWdSt] the stage's MMAs are done
+  uint64_t* acc_full = empty + kWdSt;                    // [2] an accumulator holds a finished tile
+  uint64_t* acc_empty = acc_full + 2;                    // [2] the epilogue drained it (4 warps)
+  uint64_t* xfull = acc_empty + 2;                       // kSw: [pair * 2 + buf] up values written (32 lanes)
+  uint64_t* xempty = xfull + 4;                          // kSw: [pair * 2 + buf] up values read (32 lanes)
+  uint32_t* tmem_slot = (uint32_t*)(xempty + 4);
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_kt = p.K / kBK;
+  const int NT = (p.B + kWdBN - 1) / kWdBN;
+  constexpr int kRows = kSw ? kBM / 2 : kBM;   // output rows per weight tile
+  const int items = (((kSw ? F : p.R) + kRows - 1) / kRows) * NT;
+  if (tid == 0) {
+    for (int i = 0; i < kWdSt; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&xfull[i], 32);
+      mbar_init(&xempty[i], 32);
+    }
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 2 * kWdBN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- producer: W boxes need no dependency, X boxes (activations) do
+      int it = 0, issued = 0;
+      bool waited = false, ok = true;
+      for (int item = blockIdx.x; item < items && ok; item += gridDim.x) {
+        const int rt = item / NT, nt = item - rt * NT;
+        for (int kb = 0; kb < n_kt; ++kb, ++it) {
+          const int st = it % kWdSt;
+          if (it >= kWdSt && !mbar_wait_bounded(&empty[st], (uint32_t)(((it / kWdSt) - 1) & 1), p.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], kTileA + kWdTileX);
+          if (kSw) {
+            tma_load_2d(sA + st * kTileA, &tmW, kb * kBK, rt * kRows, &full[st]);
+            tma_load_2d(sA + st * kTileA + kTileA / 2, &tmW, kb * kBK, F + rt * kRows, &full[st]);
+          } else {
+            tma_load_2d(sA + st * kTileA, &tmW, kb * kBK, rt * kBM, &full[st]);
+          }
+          if (!waited) {
+            pdl_wait();
+            waited = true;
+          }
+          tma_load_2d(sB + st * kWdTileX, &tmX, kb * kBK, nt * kWdBN, &full[st]);
+          issued = it + 1;
+        }
+      }
+      if (!ok) *(volatile int*)&s_abort = 1;
+      drain_ring(full, kWdSt, issued, p.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer
+      int it = 0, j = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < items && ok; item += gridDim.x, ++j) {
+        const int a = j & 1;
+        if (j >= 2 && !mbar_wait_bounded(&acc_empty[a], (uint32_t)(((j >> 1) - 1) & 1), p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(a * kWdBN);
+        for (int kb = 0; kb < n_kt; ++kb, ++it) {
+          const int st = it % kWdSt;
+          if (!mbar_wait_bounded(&full[st], (uint32_t)((it / kWdSt) & 1), p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + st * kTileA), b0 = smem_u32(sB + st * kWdTileX);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16<kWdBN>(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), (kb | kk) != 0);
+          mma_commit(&empty[st]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[a]);
+      }
+      if (!ok) *(volatile int*)&s_abort = 1;
+    }
+  } else {
+    // ---- epilogue warps 2..5: TMEM lane quarter q = warp % 4, rows 32 q + lane of a tile
+    pdl_wait();   // y (the residual stream) comes from earlier kernels
+    const int q = warp & 3;
+    const uint32_t lanes = (uint32_t)(q * 32) << 16;
+    const int pair = q & 1;   // kSw: gate quarter `pair` takes the values of up quarter 2 + pair
+    const bool up = q >= 2;
+    float v[64];
+    int j = 0, xc = 0;
+    bool live = true;
+    for (int item = blockIdx.x; item < items && live; item += gridDim.x, ++j) {
+      const int a = j & 1;
+      const bool got = mbar_wait_bounded(&acc_full[a], (uint32_t)((j >> 1) & 1), p.err) && !*(volatile int*)&s_abort;
+      if (!__all_sync(0xffffffffu, got)) break;   // warp-wide TMEM loads: one decision per warp
+      tc_fence_after();
+      const int rt = item / NT, nt = item - rt * NT;
+      const int n0 = nt * kWdBN;
+      if (kSw) {
+        const int jr = rt * kRows + pair * 32 + lane;   // the h column of this lane (gate warps)
+#pragma unroll 1
+        for (int c4 = 0; c4 < kWdBN / 64; ++c4, ++xc) {
+          tmem_ld_32x64(tmem + lanes + (uint32_t)(a * kWdBN + c4 * 64), v);
+          const int bsel = pair * 2 + (xc & 1), use = xc >> 1;
+          float* xb = xch + bsel * (64 * 32);
+          if (up) {
+            const bool free_ = use == 0 || mbar_wait_bounded(&xempty[bsel], (uint32_t)((use - 1) & 1), p.err);
+            if (!__all_sync(0xffffffffu, free_)) {
+              live = false;
+              break;
+            }
+#pragma unroll
+            for (int c = 0; c < 64; ++c) xb[c * 32 + lane] = v[c];
+            mbar_arrive(&xfull[bsel]);
+          } else {
+            const bool ready = mbar_wait_bounded(&xfull[bsel], (uint32_t)(use & 1), p.err);
+            if (!__all_sync(0xffffffffu, ready)) {
+              live = false;
+              break;
+            }
+#pragma unroll
+            for (int c = 0; c < 64; ++c) v[c] = v[c] / (1.0f + expf(-v[c])) * xb[c * 32 + lane];
+            mbar_arrive(&xempty[bsel]);
+            if (jr < F) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const int n = n0 + c4 * 64 + c;
+                if (n < p.B) h[(size_t)n * F + jr] = __float2bfloat16_rn(v[c]);
+              }
+            }
+          }
+        }
+        if (!live) {
+          *(volatile int*)&s_abort = 1;
+          break;
+        }
+      } else {
+        const int r = rt * kBM + q * 32 + lane;
+        // y[t + j, r] (+)= o[j] for 16 tokens from t, the residual values loaded first
+        auto store_rows = [&](int t, const float* o) {
+          float old[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            old[e] = (p.epi == EPI_RESID_ADD && t + e < p.B) ? p.y[(size_t)(t + e) * p.R + r] : 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (t + e < p.B) p.y[(size_t)(t + e) * p.R + r] = p.epi == EPI_RESID_ADD ? old[e] + o[e] : o[e];
+        };
+#pragma unroll 1
+        for (int c4 = 0; c4 < kWdBN / 64; ++c4) {
+          tmem_ld_32x64(tmem + lanes + (uint32_t)(a * kWdBN + c4 * 64), v);
+          if (r < p.R && n0 + c4 * 64 < p.B) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) store_rows(n0 + c4 * 64 + c * 16, v + c * 16);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kWdBN);
+  }
+}
+
+// QD_GEMM_WIDE (read per call): the many-row bf16 GEMMs run on the persistent form
+// above (24576 x 4096 weights x 2048 tokens: 262 us against 285 us for one CTA per
+// tile); "tiles" keeps one CTA per 128 x 256 tile.
+bool gemm_wide_persistent() {
+  const char* v = getenv("QD_GEMM_WIDE");
+  return !(v && strcmp(v, "tiles") == 0);
+}
+
+cudaError_t launch_wide(const CUtensorMap& tw, const CUtensorMap& tx, const TcParams& p, const Launch& L) {
+  const int items = ((p.R + kBM - 1) / kBM) * ((p.B + kWdBN - 1) / kWdBN);
+  const int grid = std::min(items, dev_info().sm_count);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_wide_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wd_smem(false));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_ex(gemm_wide_kernel<false>, dim3(grid), dim3(kWdThreads), wd_smem(false), L, tw, tx, p,
+                   (__nv_bfloat16*)nullptr, 0);
+}
+
 // ---- prefill gate+up with SwiGLU in the epilogue ------------------------------
 // The gate rows j0 .. j0 + 127 and the up rows F + j0 .. of W_gu against one
 // 256-token tile of X: two M = 128 x N = 256 accumulators (all 512 TMEM
@@ -766,7 +1008,7 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   }
   // Q8_0: one 384-thread CTA per SM with its own ring depths
   if (q8) return launch_tc<kASt, true>(tw, tx, ts, p, tiles, L);
-  if (wide) return launch_tc<4, false, 256>(tw, tx, ts, p, tiles, L);
+  if (wide) return gemm_wide_persistent() ? launch_wide(tw, tx, p, L) : launch_tc<4, false, 256>(tw, tx, ts, p, tiles, L);
   static const int forced = [] {
     const char* v = getenv("QD_GEMM_STAGES");
     return v ? atoi(v) : 0;
@@ -790,6 +1032,23 @@ cudaError_t launch_gemm_tc_swiglu(const void* W, const void* X, int F, int K, in
   if (e != cudaSuccess) return e;
   e = encode_rowmajor_bf16(&tx, X, (uint64_t)B, (uint64_t)K, kSwBN);
   if (e != cudaSuccess) return e;
+  if (gemm_wide_persistent()) {
+    // persistent form: 64 gate rows over 64 up rows per weight tile (two 64-row boxes)
+    e = encode_rowmajor_bf16(&tw, W, (uint64_t)2 * F, (uint64_t)K, kBM / 2);
+    if (e != cudaSuccess) return e;
+    TcParams tp = {};
+    tp.R = 2 * F; tp.K = K; tp.B = B; tp.err = L.err;
+    const int items = ceil_div(F, kBM / 2) * ceil_div(B, kWdBN);
+    const int grid = std::min(items, dev_info().sm_count);
+    static bool wd_attr_set = false;
+    if (!wd_attr_set) {
+      e = cudaFuncSetAttribute(gemm_wide_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wd_smem(true));
+      if (e != cudaSuccess) return e;
+      wd_attr_set = true;
+    }
+    return launch_ex(gemm_wide_kernel<true>, dim3(grid), dim3(kWdThreads), wd_smem(true), L, tw, tx, tp,
+                     (__nv_bfloat16*)h, F);
+  }
   SwParams p = {};
   p.F = F; p.K = K; p.B = B; p.h = (__nv_bfloat16*)h; p.err = L.err;
   const size_t smem = 1024 + (size_t)kSwSt * (2 * kTileA + kTileX256) + (2 * kSwSt + 1) * 8 + 16;
