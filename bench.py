@@ -66,7 +66,8 @@ def parse():
                     help="time speculative verify passes of K tokens (K - 1 drafts) against K single-token steps "
                          "on the batch-1 workload")
     ap.add_argument("--layers", type=int, default=0, metavar="N",
-                    help="--verify only: a model of N decoder layers instead of the workload's (profiling aid)")
+                    help="--verify and --prefill: a model of N decoder layers instead of the workload's "
+                         "(profiling aid)")
     ap.add_argument("--deq", type=int, choices=[0, 1, 2],
                     help="Q8_0 lanes by level: 0 = dp4a everywhere, 1 = dp4a in the layers and f32 activations for "
                          "the LM head, 2 = f32 activations everywhere (overrides --act)")
@@ -865,7 +866,8 @@ def run_prefill_bench(args):
     wl = synth.WORKLOADS[args.workload]
     s = wl.shape
     assert wl.batch == 1 and wl.wtype in ("bf16", "q8_0"), "prefill runs on one sequence, BF16 or Q8_0 weights"
-    mt = synth.make_model(s, wl.wtype, args.seed, dev, ctx=0, steps=n + 1)
+    mt = synth.make_model(s, wl.wtype, args.seed, dev, ctx=0, steps=n + 1,
+                          n_layers=args.layers if args.layers > 0 else None)
     dec = api.Decoder(mt, max_steps=n + 1, device=dev, prefill_max=n)
     g = torch.Generator(device=dev)
     g.manual_seed(args.seed + 2)
@@ -923,7 +925,8 @@ def run_prefill_bench(args):
                     "q8_0 widened to bf16, tcgen05 GEMMs + bf16 mma.sync attention",
            "data": "synthetic",
            "config": {"workload": wl.name, "prompt_tokens": n, "positions": f"0..{n - 1}",
-                      "graph": "one CUDA graph per prefill", "repetitions": reps, "prefills_each": k},
+                      "graph": "one CUDA graph per prefill", "repetitions": reps, "prefills_each": k,
+                      "layers": args.layers or s.n_layers},
            "roofline": {"bound": "tensor",
                         "kernel": (f"gemm_wide_kernel (the gate+up weights {2 * s.ffn} x {s.hidden} over {n} rows, f32 "
                                    "out; the pass runs these MMAs with the SwiGLU epilogue)") if wl.wtype == "bf16" else

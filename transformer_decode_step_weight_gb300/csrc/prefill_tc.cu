@@ -70,6 +70,21 @@ struct TcPfParams {
 };
 
 QD_DEV uint32_t pack_bf(float lo, float hi) { return f2bf_bits(lo) | (f2bf_bits(hi) << 16); }
+// bf16(lo) in the low half, bf16(hi) in the high half, both rounded to nearest even by
+// one paired conversion
+QD_DEV uint32_t bf2_bits(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  return u;
+}
+// 2^x by the hardware's approximate base-2 exponential (-inf gives +0, subnormal
+// results flush to zero); the relative error is far below the bf16 hi + lo weights'
+QD_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -264,14 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&o_done[b]);
         tc::commit(&v_empty[b]);
         if (i + 2 < n_kt) {
-          // V tile i + 2 once these MMAs are done with the stage; then S of tile i + 2 into
-          // S buffer b (the rows read S(i) before P(i))
+          // S of tile i + 2 into S buffer b right behind them (the rows read S(i) before
+          // P(i)); then V tile i + 2 once these MMAs are done with the stage
+          if (!(ok = mma_s(i + 2))) break;
           if (!mbar_wait_bounded(&v_empty[b], ph, p.err)) {
             ok = false;
             break;
           }
           load_v(i + 2);
-          if (!(ok = mma_s(i + 2))) break;
         }
       }
       if (!ok) *(volatile int*)s_abort = 1;
@@ -306,11 +321,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::ld_32x32(tS + 64 * b + lanes, s);
       tc::ld_32x32(tS + 64 * b + lanes + 32, s + 32);
       const int key0 = i * kKT;
+      // the causal mask (and rows past the prompt) only where the tile crosses the
+      // diagonal of some row of the warp or the warp holds such rows (warp-uniform)
+      const bool masked = key0 + kKT - 1 > pos0 + r0 + warp * 32 || r0 + warp * 32 + 31 >= p.n;
       float mx = -INFINITY;
+      if (masked) {
 #pragma unroll
-      for (int j = 0; j < kKT; ++j) {
-        if (!valid || key0 + j > rowpos) s[j] = -INFINITY;
-        mx = fmaxf(mx, s[j]);
+        for (int j = 0; j < kKT; ++j) {
+          if (!valid || key0 + j > rowpos) s[j] = -INFINITY;
+          mx = fmaxf(mx, s[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < kKT; ++j) mx = fmaxf(mx, s[j]);
       }
       // move the reference maximum where a score passes it by more than kRescale; O and
       // l follow it. The O rows of the warp are rescaled together (warp-wide TMEM access)
@@ -347,18 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kKT / 8; ++c) {   // 8 keys per 16-byte piece
         float pv[8];
+        // a masked score (-inf) gives 0; m_ref is finite in every row with a visible key
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float sv = s[8 * c + e];
-          pv[e] = sv == -INFINITY ? 0.f : exp2f(sv - m_ref);
+          pv[e] = masked ? (sv == -INFINITY ? 0.f : ex2_approx(sv - m_ref)) : ex2_approx(sv - m_ref);
           ps += pv[e];
         }
         uint32_t hw[4], lw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(pv[2 * e]), h1 = __float2bfloat16_rn(pv[2 * e + 1]);
-          hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-          lw[e] = pack_bf(pv[2 * e] - __bfloat162float(h0), pv[2 * e + 1] - __bfloat162float(h1));
+          hw[e] = bf2_bits(pv[2 * e], pv[2 * e + 1]);
+          lw[e] = bf2_bits(pv[2 * e] - bf_lo(hw[e]), pv[2 * e + 1] - bf_hi(hw[e]));
         }
         const uint32_t o = tc::sw128_off(r, c);
         *(uint4*)(ph + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
