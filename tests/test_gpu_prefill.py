@@ -130,10 +130,12 @@ def test_prefill_paged_cache(cuda_lib, monkeypatch, attn):
     assert api.check_device_error() == 0
 
 
-def test_prefill_q8_0(cuda_lib, parity_log):
-    # Q8_0 weights: the rows run on the tensor cores with each weight widened to bf16;
-    # held to the pages' Q8_0 definition and to the widened-weight lane
-    n = 70
+# Q8_0 weights: the rows run on the tensor cores with each weight widened to bf16, in
+# the Q8_0 GEMM's converters up to 128 rows and above that by a widening pass ahead of
+# the bf16 GEMMs (from 1024 rows the gate+up one with the SwiGLU epilogue); held to the
+# pages' Q8_0 definition and to the widened-weight lane
+@pytest.mark.parametrize("n", [70, 300, 1030])
+def test_prefill_q8_0(cuda_lib, parity_log, n):
     mt = synth.make_model(synth.SMALL256, "q8_0", 45, DEV, ctx=30, steps=n + 2)
     om = oracle_model(mt)
     dec = api.Decoder(mt, max_steps=n + 2, prefill_max=n)
@@ -147,7 +149,7 @@ def test_prefill_q8_0(cuda_lib, parity_log):
         ref, _, _ = _oracle_prefill(om, mt, toks, pos0, act=act)
         worst[act] = rel_max_abs(got, ref)
         assert worst[act] < TOL["w_bf16"], (act, worst[act])
-    parity_log["prefill_q8_0"] = worst
+    parity_log[f"prefill_q8_0_n{n}"] = worst
     assert api.check_device_error() == 0
 
 

@@ -1225,8 +1225,15 @@ struct PrefillWs {
   void* argmax_ws;
   void* kv_pack;     // the tcgen05 attention's packed K / V copies
   size_t kv_pack_bytes;
+  void* wide_w;      // Q8_0 above kPrefillWidenRows rows: bf16 copy of one projection's weights
   size_t total;
 };
+
+// Q8_0 prefill of more rows than this: each projection's weights are widened to bf16
+// once (bf16(f32(d) q), the tensor-core lane's own widening) and the rows run on the
+// many-row bf16 GEMMs, which are compute-bound there; up to it the Q8_0 GEMM, which
+// reads 1.0625 bytes per weight, is the faster one.
+constexpr int kPrefillWidenRows = 128;
 
 constexpr int kMaxPrefill = 32768;
 
@@ -1247,6 +1254,13 @@ PrefillWs prefill_ws_layout(const qd_step_args* a, int n, void* base) {
   w.kv_pack = (void*)(p + off);
   w.kv_pack_bytes = prefill_attention_tc_scratch_bytes(d.n_kv_heads, a->max_pages * a->page_size);
   off += al256(w.kv_pack_bytes);
+  w.wide_w = nullptr;
+  if (d.wtype == QD_W_Q8_0 && n > kPrefillWidenRows) {
+    const size_t H = d.hidden, F = d.ffn, A = (size_t)d.n_q_heads * d.head_dim;
+    const size_t most = std::max(std::max(qkv * H, H * A), std::max(2 * F * H, H * F));
+    w.wide_w = (void*)(p + off);
+    off += al256(most * 2);
+  }
   w.total = step_bytes + off;
   return w;
 }
@@ -1294,6 +1308,24 @@ int run_prefill(const qd_step_args* a, const int32_t* tokens, int n, float* logi
     g.W = W; g.S = S; g.X = X; g.R = R; g.K = K; g.B = B; g.epi = epi; g.y = y;
     return launch_gemm_tc(g, L);
   };
+  // Q8_0 over many rows: widen the projection's weights into w.wide_w, then the bf16
+  // GEMM. The GEMM issues its first weight loads before its dependency wait, so it
+  // launches without the programmatic dependency (it starts once the widening is done);
+  // the widening itself waits for the kernels before it, the last reader of w.wide_w
+  // among them, before its first store.
+  const bool widen = w.wide_w != nullptr;
+  const Launch L_full = make_launch(stream, false);
+  auto widened = [&](const void* W, const void* S, int R, int K) -> cudaError_t {
+    return launch_q8_widen(W, S, R, K, w.wide_w, L);
+  };
+  auto proj = [&](const void* W, const void* S, int R, int K, const void* X, int epi, float* y) -> cudaError_t {
+    if (!widen) return gemm(W, S, R, K, X, n, epi, y);
+    cudaError_t e = widened(W, S, R, K);
+    if (e != cudaSuccess) return e;
+    GemmTcArgs g = {};
+    g.W = w.wide_w; g.X = X; g.R = R; g.K = K; g.B = n; g.epi = epi; g.y = y;
+    return launch_gemm_tc(g, L_full);
+  };
   // QD_PREFILL_ATTN (read per call): "mma" keeps the attention on the mma.sync kernel;
   // otherwise tcgen05 (2048 / 4096-token prefill 53.0K / 44.0K -> 60.4K / 54.7K tok/s)
   const char* pa = getenv("QD_PREFILL_ATTN");
@@ -1303,7 +1335,7 @@ int run_prefill(const qd_step_args* a, const int32_t* tokens, int n, float* logi
   for (int li = 0; li < a->n_layers; ++li) {
     const qd_layer* l = a->layers[li];
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_in, n, H, d.rms_eps, w.xn, L), "rmsnorm");
-    QD_TRY(gemm(l->w.w_qkv, q8 ? l->w.s_qkv : nullptr, QKV, H, w.xn, n, EPI_STORE, w.qkv), "qkv gemm");
+    QD_TRY(proj(l->w.w_qkv, q8 ? l->w.s_qkv : nullptr, QKV, H, w.xn, EPI_STORE, w.qkv), "qkv gemm");
     // every row's K/V reaches the cache before the attention reads keys up to its own position
     QD_TRY(launch_kv_write(w.qkv, n, Hq, Hkv, l->w.k_norm, a->rope_table, a->rope_max_pos, d.rms_eps, 1, w.vpos,
                            a->page_table, 0, a->page_size, a->max_pages, a->n_pages, a->k_cache[li],
@@ -1319,16 +1351,21 @@ int run_prefill(const qd_step_args* a, const int32_t* tokens, int n, float* logi
       QD_TRY(launch_prefill_attention_tc(at, w.kv_pack, w.kv_pack_bytes, L), "prefill attention (tcgen05)");
     else
       QD_TRY(launch_prefill_attention(at, L), "prefill attention");
-    QD_TRY(gemm(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, n, EPI_RESID_ADD, w.res), "o gemm");
+    QD_TRY(proj(l->w.w_o, q8 ? l->w.s_o : nullptr, H, Hq * D, w.attn, EPI_RESID_ADD, w.res), "o gemm");
     QD_TRY(launch_rmsnorm_rows(w.res, l->w.ln_post, n, H, d.rms_eps, w.xn, L), "rmsnorm");
-    if (!q8 && gemm_tc_swiglu_supported(F, H, n)) {  // SwiGLU in the gate+up GEMM's epilogue
+    if ((!q8 || widen) && gemm_tc_swiglu_supported(F, H, n)) {  // SwiGLU in the gate+up GEMM's epilogue
       // h (bf16 [n, F]) goes where the f32 gate/up rows would have gone
-      QD_TRY(launch_gemm_tc_swiglu(l->w.w_gu, w.xn, F, H, n, w.gu, L), "gu swiglu gemm");
-      QD_TRY(gemm(l->w.w_down, nullptr, H, F, w.gu, n, EPI_RESID_ADD, w.res), "down gemm");
+      if (widen) {
+        QD_TRY(widened(l->w.w_gu, l->w.s_gu, 2 * F, H), "gu widen");
+        QD_TRY(launch_gemm_tc_swiglu(w.wide_w, w.xn, F, H, n, w.gu, L_full), "gu swiglu gemm");
+      } else {
+        QD_TRY(launch_gemm_tc_swiglu(l->w.w_gu, w.xn, F, H, n, w.gu, L), "gu swiglu gemm");
+      }
+      QD_TRY(proj(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.gu, EPI_RESID_ADD, w.res), "down gemm");
     } else {
-      QD_TRY(gemm(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, n, EPI_STORE, w.gu), "gu gemm");
+      QD_TRY(proj(l->w.w_gu, q8 ? l->w.s_gu : nullptr, 2 * F, H, w.xn, EPI_STORE, w.gu), "gu gemm");
       QD_TRY(launch_swiglu_rows(w.gu, n, F, w.xn, L), "swiglu");
-      QD_TRY(gemm(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, n, EPI_RESID_ADD, w.res), "down gemm");
+      QD_TRY(proj(l->w.w_down, q8 ? l->w.s_down : nullptr, H, F, w.xn, EPI_RESID_ADD, w.res), "down gemm");
     }
   }
   // the last row alone goes through the final norm, the LM head and the argmax advance

@@ -1018,6 +1018,34 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L) {
   return deep ? launch_tc<6, false>(tw, tx, ts, p, tiles, L) : launch_tc<3, false>(tw, tx, ts, p, tiles, L);
 }
 
+// ---- Q8_0 weights widened to bf16 for the prefill's many-row GEMMs ---------
+// out[r, k] = bf16(f32(d) * q) for every weight of a Q8_0 matrix (int8 [R, K], fp16
+// scales [R, K / 32]), the converters' arithmetic above, one 32-weight block per thread
+// per grid-stride step. The stores wait for the kernels before this one, which may still
+// read the output buffer.
+__global__ void __launch_bounds__(256) q8_widen_kernel(const uint4* __restrict__ q, const __half* __restrict__ sc,
+                                                       uint4* __restrict__ out, size_t n_blocks) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (size_t b = (size_t)blockIdx.x * blockDim.x + threadIdx.x; b < n_blocks; b += (size_t)gridDim.x * blockDim.x) {
+    const uint4 w0 = __ldg(q + 2 * b), w1 = __ldg(q + 2 * b + 1);
+    const float d = __half2float(sc[b]);
+    out[4 * b] = widen8_q8(w0.x, w0.y, d);
+    out[4 * b + 1] = widen8_q8(w0.z, w0.w, d);
+    out[4 * b + 2] = widen8_q8(w1.x, w1.y, d);
+    out[4 * b + 3] = widen8_q8(w1.z, w1.w, d);
+  }
+}
+
+cudaError_t launch_q8_widen(const void* W, const void* S, int R, int K, void* out, const Launch& L) {
+  if (R < 1 || K < 32 || K % 32 != 0 || !W || !S || !out || ((uintptr_t)W & 15) || ((uintptr_t)out & 15))
+    return cudaErrorInvalidValue;
+  const size_t n_blocks = (size_t)R * (K / 32);
+  const int grid = (int)std::min<size_t>((n_blocks + 255) / 256, (size_t)dev_info().sm_count * 8);
+  return launch_ex(q8_widen_kernel, dim3(grid), dim3(256), 0, L, (const uint4*)W, (const __half*)S, (uint4*)out,
+                   n_blocks);
+}
+
 // From 1024 rows: below that the paired tiles (one CTA per SM for their shared
 // memory) leave too few CTAs to balance the SMs (512 rows measured 4 % slower than
 // the GEMM + SwiGLU rows pair; 2048 / 4096 rows 1 / 2.5 % faster).

@@ -158,6 +158,9 @@ cudaError_t launch_gemm_tc(const GemmTcArgs& a, const Launch& L);
 // and u = row F + j of W [2F, K] applied to X [B, K] bf16, written to h [B, F] bf16.
 bool gemm_tc_swiglu_supported(int F, int K, int B);
 cudaError_t launch_gemm_tc_swiglu(const void* W, const void* X, int F, int K, int B, void* h, const Launch& L);
+// Q8_0 matrix (int8 [R, K], fp16 scales [R, K / 32]) widened to bf16 [R, K], each weight
+// bf16(f32(d) * q); K a multiple of 32, W and out 16-byte aligned.
+cudaError_t launch_q8_widen(const void* W, const void* S, int R, int K, void* out, const Launch& L);
 
 // row-wise helpers of the batched step
 cudaError_t launch_rmsnorm_rows(const float* x, const void* w, int B, int K, float eps, void* out_bf16,
