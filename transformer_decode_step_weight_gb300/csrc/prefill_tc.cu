@@ -10,8 +10,8 @@
 // K-major tiles. Per 64-key tile:
 //   * S[128 x 64] = Q K^T on tcgen05 into TMEM (16 MMAs: M 128, N 64, K 16, the hi and
 //     the lo half of q), K streamed by TMA from a packed copy of the kv head's keys;
-//   * each of 128 threads owns one query row (its TMEM lane): it loads its 64 scores,
-//     masks keys past its position, and keeps a reference maximum that moves only when
+//   * the threads of each query row (its TMEM lane) load its 64 scores, mask keys past
+//     its position, and keep a reference maximum that moves only when
 //     a score passes it by more than 8 (a factor 256) so the accumulator in TMEM is
 //     rescaled rarely; p = exp2(s - m_ref) goes to shared memory as bf16 hi + lo in
 //     the swizzled layout the MMA reads;
@@ -19,6 +19,8 @@
 //     transposed copy [128 dims x keys], so both operands are K-major.
 // A producer/issuer thread keeps two K / V tiles in flight and issues S of the next
 // tile while the threads finish the current one. Every wait is bounded.
+// Each query row is shared by two threads in two warps (TMEM lane quarters are per warp
+// modulo 4), each taking half of the tile's keys, so two row warps run per SM sub-partition.
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.cuh"
@@ -41,7 +43,9 @@ constexpr int kQChunk = kQT * 128;     // [128 rows x 64 bf16] swizzled chunk: 1
 constexpr int kKChunk = kKT * 128;     // [64 keys x 64 bf16]: 8 KB
 constexpr int kKTile = 2 * kKChunk;    // a K tile: dims 0-63, 64-127
 constexpr int kVTile = kD * 128;       // a V^T tile [128 dims x 64 keys]: 16 KB
-constexpr int kThreads = 160;          // 4 row warps + 1 producer / issuer warp
+constexpr int kRowWarps = 8;           // two warps per TMEM lane quarter (32 of a tile's 64 keys each)
+constexpr int kIssuer = kRowWarps;     // the producer / issuer warp
+constexpr int kThreads = 32 * (kRowWarps + 1);
 constexpr int kOffQh = 0;
 constexpr int kOffQl = kOffQh + 2 * kQChunk;
 constexpr int kOffK = kOffQl + 2 * kQChunk;      // K ring [kSt]
@@ -49,7 +53,8 @@ constexpr int kOffV = kOffK + kSt * kKTile;      // V^T ring [kSt]
 constexpr int kOffPh = kOffV + kSt * kVTile;     // P hi [2 buffers]
 constexpr int kOffPl = kOffPh + 2 * kQChunk;     // P lo [2 buffers]
 constexpr int kOffBar = kOffPl + 2 * kQChunk;
-constexpr size_t kSmem = (size_t)kOffBar + 128 + 1024;   // barriers, slack for the 1024-byte alignment
+constexpr int kOffXm = kOffBar + 256;            // the row pairs' traded maxima / sums [2][2][kQT] f32
+constexpr size_t kSmem = (size_t)kOffXm + 2 * 2 * kQT * 4 + 1024;   // slack for the 1024-byte alignment
 constexpr uint32_t kTmemCols = 256;    // S buffers at columns 0 and 64, O at column 128 (128)
 constexpr float kRescale = 8.0f;       // log2 units a score may pass the reference maximum
 
@@ -99,8 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = bar + 8;     // [2] S of a tile in its TMEM buffer
   uint64_t* p_full = bar + 10;    // [2] 128 rows read S and wrote P into that buffer (O rescaled)
   uint64_t* o_done = bar + 12;    // [2] the P V MMAs of a tile completed
-  uint32_t* tslot = (uint32_t*)(bar + 14);
+  uint64_t* x_bar = bar + 14;     // [2 parities][4 lane quarters] both warps of a pair traded (64 lanes)
+  uint32_t* tslot = (uint32_t*)(bar + 22);
   int* s_abort = (int*)(tslot + 1);
+  float* xm = (float*)(smem + kOffXm);
 
   const int qt = (int)(gridDim.x - 1 - blockIdx.x), h = blockIdx.y;   // longest query tiles first
   const int g = h / (p.Hq / p.Hkv);
@@ -125,9 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kQT);
+      mbar_init(&p_full[i], kQT * kRowWarps / 4);
       mbar_init(&o_done[i], 1);
     }
+    for (int i = 0; i < 8; ++i) mbar_init(&x_bar[i], 64);
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tslot;
   const uint32_t tS = tbase, tO = tbase + 128;   // S buffer b at tS + 64 b
 
-  if (warp == 4) {
+  if (warp == kIssuer) {
     if (lane == 0) {  // ---- producer and MMA issuer
       const uint32_t sQh = smem_u32(smem + kOffQh), sQl = smem_u32(smem + kOffQl);
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
@@ -298,17 +306,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---- one query row per thread (TMEM lane tid)
-    const int r = tid, row = r0 + r;
+    // ---- query rows: warps w and w + 4 share TMEM lane quarter q = w % 4 (rows 32 q ..
+    // 32 q + 31, one per lane); half hf = w / 4 takes key columns 32 hf .. 32 hf + 31 of
+    // every tile and O columns 64 hf .. 64 hf + 63. The pair trades its rows' maxima each
+    // tile (and the row sums at the end) through shared memory, so both halves move the
+    // same reference maximum at the same tile.
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int r = q4 * 32 + lane, row = r0 + r;
     const bool valid = row < p.n;
     const int rowpos = pos0 + row;
-    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+    const uint32_t lanes = (uint32_t)(q4 * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;
     bool fail = false;
     // wait (bounded) on a barrier phase; false in every lane if any lane gave up
     auto wait_all = [&](uint64_t* bb, uint32_t ph) -> bool {
       const bool got = mbar_wait_bounded(bb, ph, p.err) && !*(volatile int*)s_abort;
       return __all_sync(0xffffffffu, got);
+    };
+    // trade number u with the partner warp: this lane's v in, the partner's value out.
+    // A slot is written again two trades later, after the partner has passed the trade
+    // in between (and so has read it).
+    auto trade = [&](int u, float v, float& other) -> bool {
+      const int par = u & 1;
+      xm[(par * 2 + hf) * kQT + r] = v;
+      mbar_arrive(&x_bar[par * 4 + q4]);
+      if (!wait_all(&x_bar[par * 4 + q4], (uint32_t)((u >> 1) & 1))) return false;
+      other = xm[(par * 2 + (hf ^ 1)) * kQT + r];
+      return true;
     };
     for (int i = 0; i < n_kt; ++i) {
       const int b = i & 1;
@@ -317,27 +341,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after();
-      float s[kKT];
-      tc::ld_32x32(tS + 64 * b + lanes, s);
-      tc::ld_32x32(tS + 64 * b + lanes + 32, s + 32);
-      const int key0 = i * kKT;
-      // the causal mask (and rows past the prompt) only where the tile crosses the
+      float s[32];
+      tc::ld_32x32(tS + 64 * b + lanes + 32 * hf, s);
+      const int key0 = i * kKT + 32 * hf;
+      // the causal mask (and rows past the prompt) only where these 32 keys cross the
       // diagonal of some row of the warp or the warp holds such rows (warp-uniform)
-      const bool masked = key0 + kKT - 1 > pos0 + r0 + warp * 32 || r0 + warp * 32 + 31 >= p.n;
-      float mx = -INFINITY;
+      const bool masked = key0 + 31 > pos0 + r0 + q4 * 32 || r0 + q4 * 32 + 31 >= p.n;
       if (masked) {
 #pragma unroll
-        for (int j = 0; j < kKT; ++j) {
+        for (int j = 0; j < 32; ++j)
           if (!valid || key0 + j > rowpos) s[j] = -INFINITY;
-          mx = fmaxf(mx, s[j]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < kKT; ++j) mx = fmaxf(mx, s[j]);
       }
+      // the row maximum as a tree (exact in any order; a serial chain of dependent steps
+      // would sit on the row's critical path), then the pair's
+      float mt[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) mt[j] = fmaxf(s[j], s[j + 16]);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) mt[j] = fmaxf(mt[j], mt[j + w]);
+      float mo;
+      if (!trade(i, mt[0], mo)) {
+        fail = true;
+        break;
+      }
+      const float mx = fmaxf(mt[0], mo);
       // move the reference maximum where a score passes it by more than kRescale; O and
-      // l follow it. The O rows of the warp are rescaled together (warp-wide TMEM access)
-      // once every P V MMA so far (tiles up to i - 1) has completed.
+      // l follow it. Each half rescales its O columns (warp-wide TMEM access) once every
+      // P V MMA so far (tiles up to i - 1) has completed.
       const bool move = mx > m_ref + kRescale;
       const float alpha = move ? exp2f(m_ref - mx) : 1.f;   // 0 while m_ref is -inf
       if (i > 0 && __any_sync(0xffffffffu, move)) {
@@ -347,12 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after();
 #pragma unroll
-        for (int c = 0; c < kD; c += 32) {
+        for (int c = 0; c < kD / 2; c += 32) {
           float ov[32];
-          tc::ld_32x32(tO + lanes + c, ov);
+          tc::ld_32x32(tO + lanes + 64 * hf + c, ov);
 #pragma unroll
           for (int e = 0; e < 32; ++e) ov[e] *= alpha;
-          tc::st_32x32(tO + lanes + c, ov);
+          tc::st_32x32(tO + lanes + 64 * hf + c, ov);
         }
       }
       if (move) {
@@ -364,18 +396,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail = true;
         break;
       }
-      float ps = 0.f;
+      float psum[4] = {0.f, 0.f, 0.f, 0.f};   // four interleaved partial sums
       unsigned char* ph = smem + kOffPh + b * kQChunk;
       unsigned char* pl = smem + kOffPl + b * kQChunk;
 #pragma unroll
-      for (int c = 0; c < kKT / 8; ++c) {   // 8 keys per 16-byte piece
+      for (int c = 0; c < 4; ++c) {   // 8 keys per 16-byte piece
         float pv[8];
         // a masked score (-inf) gives 0; m_ref is finite in every row with a visible key
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float sv = s[8 * c + e];
           pv[e] = masked ? (sv == -INFINITY ? 0.f : ex2_approx(sv - m_ref)) : ex2_approx(sv - m_ref);
-          ps += pv[e];
+          psum[e & 3] += pv[e];
         }
         uint32_t hw[4], lw[4];
 #pragma unroll
@@ -383,26 +415,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           hw[e] = bf2_bits(pv[2 * e], pv[2 * e + 1]);
           lw[e] = bf2_bits(pv[2 * e] - bf_lo(hw[e]), pv[2 * e + 1] - bf_hi(hw[e]));
         }
-        const uint32_t o = tc::sw128_off(r, c);
+        const uint32_t o = tc::sw128_off(r, 4 * hf + c);
         *(uint4*)(ph + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         *(uint4*)(pl + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
-      l += ps;
+      l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
       fence_proxy_async_smem();
       tc::fence_before();
       mbar_arrive(&p_full[b]);
     }
-    // the last tile's P V MMAs complete before O is read
+    // the last tile's P V MMAs complete before O is read; the halves' sums are added in
+    // the same order in both warps
     if (!fail && !wait_all(&o_done[(n_kt - 1) & 1], (uint32_t)(((n_kt - 1) >> 1) & 1))) fail = true;
+    float l_other = 0.f;
+    if (!fail && !trade(n_kt, l, l_other)) fail = true;
     if (fail) *(volatile int*)s_abort = 1;
     if (!fail) {   // warp-uniform; rows past the prompt load too (warp-wide) but store nothing
       tc::fence_after();
-      const float inv = valid ? 1.0f / l : 0.f;
-      __nv_bfloat16* out = p.out + (size_t)(valid ? row : 0) * p.Hq * kD + (size_t)h * kD;
+      const float lt = hf == 0 ? l + l_other : l_other + l;
+      const float inv = valid ? 1.0f / lt : 0.f;
+      __nv_bfloat16* out = p.out + (size_t)(valid ? row : 0) * p.Hq * kD + (size_t)h * kD + 64 * hf;
 #pragma unroll
-      for (int c = 0; c < kD; c += 32) {
+      for (int c = 0; c < kD / 2; c += 32) {
         float ov[32];
-        tc::ld_32x32(tO + lanes + c, ov);
+        tc::ld_32x32(tO + lanes + 64 * hf + c, ov);
         if (valid)
 #pragma unroll
           for (int e = 0; e < 32; e += 8)
