@@ -17,8 +17,9 @@
 //     the swizzled layout the MMA reads;
 //   * O[128 x 128] += P V on tcgen05 (8 MMAs: M 128, N 128, K 16) with V streamed as a
 //     transposed copy [128 dims x keys], so both operands are K-major.
-// A producer/issuer thread keeps two K / V tiles in flight and issues S of the next
-// tile while the threads finish the current one. Every wait is bounded.
+// Producer threads keep two K and two V tiles in flight, refilling a stage as soon as its
+// MMAs are done, and an issuer thread issues S of the next tiles while the rows finish
+// the current one. Every wait is bounded.
 // Each query row is shared by two threads in two warps (TMEM lane quarters are per warp
 // modulo 4), each taking half of the tile's keys, so two row warps run per SM sub-partition.
 #include "common.cuh"
@@ -44,8 +45,10 @@ constexpr int kKChunk = kKT * 128;     // [64 keys x 64 bf16]: 8 KB
 constexpr int kKTile = 2 * kKChunk;    // a K tile: dims 0-63, 64-127
 constexpr int kVTile = kD * 128;       // a V^T tile [128 dims x 64 keys]: 16 KB
 constexpr int kRowWarps = 8;           // two warps per TMEM lane quarter (32 of a tile's 64 keys each)
-constexpr int kIssuer = kRowWarps;     // the producer / issuer warp
-constexpr int kThreads = 32 * (kRowWarps + 1);
+constexpr int kIssuer = kRowWarps;     // the MMA issuer warp
+constexpr int kProdK = kRowWarps + 1;  // the K producer warp
+constexpr int kProdV = kRowWarps + 2;  // the V^T producer warp
+constexpr int kThreads = 32 * (kRowWarps + 3);
 constexpr int kOffQh = 0;
 constexpr int kOffQl = kOffQh + 2 * kQChunk;
 constexpr int kOffK = kOffQl + 2 * kQChunk;      // K ring [kSt]
@@ -212,30 +215,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tslot;
   const uint32_t tS = tbase, tO = tbase + 128;   // S buffer b at tS + 64 b
 
-  if (warp == kIssuer) {
-    if (lane == 0) {  // ---- producer and MMA issuer
+  if (warp == kProdK || warp == kProdV) {
+    if (lane == 0) {
+      // ---- producers: K (or V^T) tile i into stage i % 2 as soon as the MMAs of tile
+      // i - 2 are done with the stage, independent of the issuer's other waits
+      const bool is_k = warp == kProdK;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      int issued = 0;
+      for (int i = 0; i < n_kt; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && (!mbar_wait_bounded(&empty[st], (uint32_t)(((i - 2) >> 1) & 1), p.err) ||
+                       *(volatile int*)s_abort))
+          break;
+        if (is_k) {
+          unsigned char* k = smem + kOffK + st * kKTile;
+          mbar_arrive_expect_tx(&full[st], kKTile);
+          tma_load_2d(k, &tmK, 0, g * p.L + i * kKT, &full[st]);
+          tma_load_2d(k + kKChunk, &tmK, 64, g * p.L + i * kKT, &full[st]);
+        } else {
+          mbar_arrive_expect_tx(&full[st], kVTile);
+          tma_load_2d(smem + kOffV + st * kVTile, &tmV, i * kKT, g * kD, &full[st]);
+        }
+        issued = i + 1;
+      }
+      // the last copy into each stage lands before the CTA leaves (bounded; at once when
+      // the issuer consumed it). No later phase of the stage's barrier can exist.
+      for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
+        mbar_wait_limit(&full[t & 1], (uint32_t)((t >> 1) & 1), p.err, 10000000ull);
+    }
+    __syncwarp();
+  } else if (warp == kIssuer) {
+    if (lane == 0) {  // ---- MMA issuer
       const uint32_t sQh = smem_u32(smem + kOffQh), sQl = smem_u32(smem + kOffQl);
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sPh = smem_u32(smem + kOffPh), sPl = smem_u32(smem + kOffPl);
-      int k_issued = 0, k_landed = 0, v_issued = 0, v_landed = 0;   // tiles issued / waited for
-      auto load_k = [&](int i) {  // K tile i into stage i % 2
-        const int b = i & 1;
-        unsigned char* k = smem + kOffK + b * kKTile;
-        mbar_arrive_expect_tx(&k_full[b], kKTile);
-        tma_load_2d(k, &tmK, 0, g * p.L + i * kKT, &k_full[b]);
-        tma_load_2d(k + kKChunk, &tmK, 64, g * p.L + i * kKT, &k_full[b]);
-        k_issued = i + 1;
-      };
-      auto load_v = [&](int i) {  // V^T tile i into stage i % 2
-        const int b = i & 1;
-        mbar_arrive_expect_tx(&v_full[b], kVTile);
-        tma_load_2d(smem + kOffV + b * kVTile, &tmV, i * kKT, g * kD, &v_full[b]);
-        v_issued = i + 1;
-      };
       auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i into S buffer i % 2
         const int b = i & 1;
         if (!mbar_wait_bounded(&k_full[b], (uint32_t)((i >> 1) & 1), p.err)) return false;
-        k_landed = i + 1;
         tc::fence_after();
         const uint32_t k0 = sK + b * kKTile, ts = tS + 64 * b;
 #pragma unroll
@@ -252,31 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&k_empty[b]);
         return true;
       };
-      load_k(0);
-      load_v(0);
-      if (n_kt > 1) {
-        load_k(1);
-        load_v(1);
-      }
       bool ok = mma_s(0);
       if (ok && n_kt > 1) ok = mma_s(1);
       for (int i = 0; i < n_kt && ok; ++i) {
         const int b = i & 1;
         const uint32_t ph = (uint32_t)((i >> 1) & 1);
-        // K tile i + 2 into this stage as soon as the S MMAs of tile i are done with it
-        if (i + 2 < n_kt) {
-          if (!mbar_wait_bounded(&k_empty[b], ph, p.err)) {
-            ok = false;
-            break;
-          }
-          load_k(i + 2);
-        }
         // the rows read S(i), wrote P(i) into buffer b and rescaled O where needed
         if (!mbar_wait_bounded(&p_full[b], ph, p.err) || !mbar_wait_bounded(&v_full[b], ph, p.err)) {
           ok = false;
           break;
         }
-        v_landed = i + 1;
         tc::fence_after();
         const uint32_t v0 = sV + b * kVTile, p_h = sPh + b * kQChunk, p_l = sPl + b * kQChunk;
 #pragma unroll
@@ -286,23 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 4; ++kk) tc::mma<kD>(tO, tc::desc_sw128(p_l + kk * 32), tc::desc_sw128(v0 + kk * 32), 1);
         tc::commit(&o_done[b]);
         tc::commit(&v_empty[b]);
-        if (i + 2 < n_kt) {
-          // S of tile i + 2 into S buffer b right behind them (the rows read S(i) before
-          // P(i)); then V tile i + 2 once these MMAs are done with the stage
-          if (!(ok = mma_s(i + 2))) break;
-          if (!mbar_wait_bounded(&v_empty[b], ph, p.err)) {
-            ok = false;
-            break;
-          }
-          load_v(i + 2);
-        }
+        // S of tile i + 2 into S buffer b right behind them (the rows read S(i) before P(i))
+        if (i + 2 < n_kt && !(ok = mma_s(i + 2))) break;
       }
       if (!ok) *(volatile int*)s_abort = 1;
-      // copies still in flight after an early stop land before the CTA leaves (bounded)
-      for (int t = k_landed; t < k_issued; ++t)
-        mbar_wait_limit(&k_full[t & 1], (uint32_t)((t >> 1) & 1), p.err, 10000000ull);
-      for (int t = v_landed; t < v_issued; ++t)
-        mbar_wait_limit(&v_full[t & 1], (uint32_t)((t >> 1) & 1), p.err, 10000000ull);
     }
     __syncwarp();
   } else {
