@@ -94,7 +94,9 @@ int qd_version(void);
 /* GEMV (QD_SMALLB_IMPL=simt forces it). batch >= 9: the product is a dense     */
 /* contraction and runs on the tcgen05 tensor cores ("qwen3-8b-rtx4080-         */
 /* cutedsl" README, "Baseline tiled GEMM"), one CTA per 128 rows x 64 batch     */
-/* rows (a prompt's tokens, for prefill); needs bf16 x and cols % 64 == 0.      */
+/* rows; above 128 batch rows (a prompt's tokens, for prefill) a persistent     */
+/* kernel, one CTA per SM over 128 x 256 tiles (QD_GEMM_WIDE=tiles: one CTA per */
+/* tile). Needs bf16 x and cols % 64 == 0.                                      */
 int qd_gemv_bf16(const void* W, int rows, int cols, const void* x, int x_is_f32,
                  float* y, int batch, cudaStream_t stream);
 
@@ -360,11 +362,14 @@ int qd_verify_step(const qd_step_args* args, const int32_t* draft, int k, float*
 /* tiled attention that never forms the full score matrix). For the one sequence */
 /* of `args` (batch 1): tokens int32 [n_tokens] (device) sit at positions         */
 /* pos[0] .. pos[0] + n_tokens - 1. Every layer runs over all rows at once: the   */
-/* projections are tcgen05 GEMMs over 64- or 256-token tiles, the rows' K/V are   */
+/* projections are tcgen05 GEMMs over 64- or 256-token tiles (Q8_0 weights above */
+/* 128 rows widened to bf16 once per projection, bf16(f32(d) q), into the        */
+/* workspace first), the rows' K/V are                                           */
 /* written to the cache first, and row i attends causally to positions 0 ..       */
 /* pos[0] + i (the keys already cached included) on tcgen05 (QD_PREFILL_ATTN=mma: */
 /* the mma.sync kernel). The workspace includes a packed copy of the kv heads'    */
-/* keys up to the cache capacity. The last row alone goes through the final       */
+/* keys up to the cache capacity (and, for Q8_0 above 128 rows, the bf16 copy of */
+/* the largest projection). The last row alone goes through the final            */
 /* norm and the LM head: logits f32 [vocab] (device, 16-byte aligned). The state  */
 /* then advances as one decode step from the last row: tok = argmax (first index */
 /* among equal maxima), out_tokens[step] = tok, pos += n_tokens, step += 1.      */
