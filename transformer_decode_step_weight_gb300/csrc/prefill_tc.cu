@@ -39,7 +39,8 @@ namespace {
 constexpr int kD = 128;
 constexpr int kQT = 128;               // query rows per CTA (the MMA's M, TMEM lanes)
 constexpr int kKT = 64;                // keys per tile (S columns)
-constexpr int kSt = 2;                 // K / V ring stages
+constexpr int kKSt = 3;                // K ring stages (S of tile i + 2 waits on its K tile)
+constexpr int kVSt = 2;                // V^T ring stages
 constexpr int kQChunk = kQT * 128;     // [128 rows x 64 bf16] swizzled chunk: 16 KB
 constexpr int kKChunk = kKT * 128;     // [64 keys x 64 bf16]: 8 KB
 constexpr int kKTile = 2 * kKChunk;    // a K tile: dims 0-63, 64-127
@@ -51,9 +52,9 @@ constexpr int kProdV = kRowWarps + 2;  // the V^T producer warp
 constexpr int kThreads = 32 * (kRowWarps + 3);
 constexpr int kOffQh = 0;
 constexpr int kOffQl = kOffQh + 2 * kQChunk;
-constexpr int kOffK = kOffQl + 2 * kQChunk;      // K ring [kSt]
-constexpr int kOffV = kOffK + kSt * kKTile;      // V^T ring [kSt]
-constexpr int kOffPh = kOffV + kSt * kVTile;     // P hi [2 buffers]
+constexpr int kOffK = kOffQl + 2 * kQChunk;      // K ring [kKSt]
+constexpr int kOffV = kOffK + kKSt * kKTile;     // V^T ring [kVSt]
+constexpr int kOffPh = kOffV + kVSt * kVTile;    // P hi [2 buffers]
 constexpr int kOffPl = kOffPh + 2 * kQChunk;     // P lo [2 buffers]
 constexpr int kOffBar = kOffPl + 2 * kQChunk;
 constexpr int kOffXm = kOffBar + 256;            // the row pairs' traded maxima / sums [2][2][kQT] f32
@@ -100,15 +101,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bar = (uint64_t*)(smem + kOffBar);
-  uint64_t* k_full = bar;         // [kSt] a K tile landed
-  uint64_t* k_empty = bar + 2;    // [kSt] its S MMAs are done with it
-  uint64_t* v_full = bar + 4;     // [kSt] a V^T tile landed
-  uint64_t* v_empty = bar + 6;    // [kSt] its P V MMAs are done with it (and with that P buffer)
-  uint64_t* s_full = bar + 8;     // [2] S of a tile in its TMEM buffer
-  uint64_t* p_full = bar + 10;    // [2] 128 rows read S and wrote P into that buffer (O rescaled)
-  uint64_t* o_done = bar + 12;    // [2] the P V MMAs of a tile completed
-  uint64_t* x_bar = bar + 14;     // [2 parities][4 lane quarters] both warps of a pair traded (64 lanes)
-  uint32_t* tslot = (uint32_t*)(bar + 22);
+  uint64_t* k_full = bar;         // [kKSt] a K tile landed
+  uint64_t* k_empty = bar + 3;    // [kKSt] its S MMAs are done with it
+  uint64_t* v_full = bar + 6;     // [kVSt] a V^T tile landed
+  uint64_t* v_empty = bar + 8;    // [kVSt] its P V MMAs are done with it (and with that P buffer)
+  uint64_t* s_full = bar + 10;    // [2] S of a tile in its TMEM buffer
+  uint64_t* p_full = bar + 12;    // [2] 128 rows read S and wrote P into that buffer (O rescaled)
+  uint64_t* o_done = bar + 14;    // [2] the P V MMAs of a tile completed
+  uint64_t* x_bar = bar + 16;     // [2 parities][4 lane quarters] both warps of a pair traded (64 lanes)
+  uint32_t* tslot = (uint32_t*)(bar + 24);
   int* s_abort = (int*)(tslot + 1);
   float* xm = (float*)(smem + kOffXm);
 
@@ -129,9 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kt = (kend + kKT - 1) / kKT;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKSt; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
@@ -217,16 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProdK || warp == kProdV) {
     if (lane == 0) {
-      // ---- producers: K (or V^T) tile i into stage i % 2 as soon as the MMAs of tile
-      // i - 2 are done with the stage, independent of the issuer's other waits
+      // ---- producers: K (or V^T) tile i into stage i % ns as soon as the MMAs of tile
+      // i - ns are done with the stage, independent of the issuer's other waits
       const bool is_k = warp == kProdK;
+      const int ns = is_k ? kKSt : kVSt;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       int issued = 0;
       for (int i = 0; i < n_kt; ++i) {
-        const int st = i & 1;
-        if (i >= 2 && (!mbar_wait_bounded(&empty[st], (uint32_t)(((i - 2) >> 1) & 1), p.err) ||
-                       *(volatile int*)s_abort))
+        const int st = i % ns;
+        if (i >= ns && (!mbar_wait_bounded(&empty[st], (uint32_t)(((i - ns) / ns) & 1), p.err) ||
+                        *(volatile int*)s_abort))
           break;
         if (is_k) {
           unsigned char* k = smem + kOffK + st * kKTile;
@@ -241,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the last copy into each stage lands before the CTA leaves (bounded; at once when
       // the issuer consumed it). No later phase of the stage's barrier can exist.
-      for (int t = issued > 2 ? issued - 2 : 0; t < issued; ++t)
-        mbar_wait_limit(&full[t & 1], (uint32_t)((t >> 1) & 1), p.err, 10000000ull);
+      for (int t = issued > ns ? issued - ns : 0; t < issued; ++t)
+        mbar_wait_limit(&full[t % ns], (uint32_t)((t / ns) & 1), p.err, 10000000ull);
     }
     __syncwarp();
   } else if (warp == kIssuer) {
@@ -250,11 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQh = smem_u32(smem + kOffQh), sQl = smem_u32(smem + kOffQl);
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sPh = smem_u32(smem + kOffPh), sPl = smem_u32(smem + kOffPl);
-      auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i into S buffer i % 2
-        const int b = i & 1;
-        if (!mbar_wait_bounded(&k_full[b], (uint32_t)((i >> 1) & 1), p.err)) return false;
+      auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i (K stage i % kKSt) into S buffer i % 2
+        const int b = i & 1, kb = i % kKSt;
+        if (!mbar_wait_bounded(&k_full[kb], (uint32_t)((i / kKSt) & 1), p.err)) return false;
         tc::fence_after();
-        const uint32_t k0 = sK + b * kKTile, ts = tS + 64 * b;
+        const uint32_t k0 = sK + kb * kKTile, ts = tS + 64 * b;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t qo = (j >> 2) * kQChunk + (j & 3) * 32, ko = (j >> 2) * kKChunk + (j & 3) * 32;
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma<kKT>(ts, tc::desc_sw128(sQl + qo), tc::desc_sw128(k0 + ko), 1);
         }
         tc::commit(&s_full[b]);
-        tc::commit(&k_empty[b]);
+        tc::commit(&k_empty[kb]);
         return true;
       };
       bool ok = mma_s(0);
