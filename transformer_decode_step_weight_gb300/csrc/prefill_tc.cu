@@ -39,7 +39,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kQT = 128;               // query rows per CTA (the MMA's M, TMEM lanes)
 constexpr int kKT = 64;                // keys per tile (S columns)
-constexpr int kKSt = 3;                // K ring stages (S of tile i + 2 waits on its K tile)
+constexpr int kKSt = 3;                // K ring stages
 constexpr int kVSt = 2;                // V^T ring stages
 constexpr int kQChunk = kQT * 128;     // [128 rows x 64 bf16] swizzled chunk: 16 KB
 constexpr int kKChunk = kKT * 128;     // [64 keys x 64 bf16]: 8 KB
@@ -59,7 +59,9 @@ constexpr int kOffPl = kOffPh + 2 * kQChunk;     // P lo [2 buffers]
 constexpr int kOffBar = kOffPl + 2 * kQChunk;
 constexpr int kOffXm = kOffBar + 256;            // the row pairs' traded maxima / sums [2][2][kQT] f32
 constexpr size_t kSmem = (size_t)kOffXm + 2 * 2 * kQT * 4 + 1024;   // slack for the 1024-byte alignment
-constexpr uint32_t kTmemCols = 256;    // S buffers at columns 0 and 64, O at column 128 (128)
+constexpr int kSBuf = 3;               // TMEM S buffers: S of tile i + 3 goes out behind P V of tile i
+constexpr uint32_t kTmemCols = 512;    // S buffers at columns 0, 64, 128; O at column 256 (128)
+constexpr uint32_t kTmemO = 256;
 constexpr float kRescale = 8.0f;       // log2 units a score may pass the reference maximum
 
 struct TcPfParams {
@@ -105,11 +107,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = bar + 3;    // [kKSt] its S MMAs are done with it
   uint64_t* v_full = bar + 6;     // [kVSt] a V^T tile landed
   uint64_t* v_empty = bar + 8;    // [kVSt] its P V MMAs are done with it (and with that P buffer)
-  uint64_t* s_full = bar + 10;    // [2] S of a tile in its TMEM buffer
-  uint64_t* p_full = bar + 12;    // [2] 128 rows read S and wrote P into that buffer (O rescaled)
-  uint64_t* o_done = bar + 14;    // [2] the P V MMAs of a tile completed
-  uint64_t* x_bar = bar + 16;     // [2 parities][4 lane quarters] both warps of a pair traded (64 lanes)
-  uint32_t* tslot = (uint32_t*)(bar + 24);
+  uint64_t* s_full = bar + 10;    // [kSBuf] S of a tile in its TMEM buffer
+  uint64_t* p_full = bar + 13;    // [2] 128 rows read S and wrote P into that buffer (O rescaled)
+  uint64_t* o_done = bar + 15;    // [2] the P V MMAs of a tile completed
+  uint64_t* x_bar = bar + 17;     // [2 parities][4 lane quarters] both warps of a pair traded (64 lanes)
+  uint32_t* tslot = (uint32_t*)(bar + 25);
   int* s_abort = (int*)(tslot + 1);
   float* xm = (float*)(smem + kOffXm);
 
@@ -134,10 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
     }
+    for (int i = 0; i < kSBuf; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kQT * kRowWarps / 4);
       mbar_init(&o_done[i], 1);
     }
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tO = tbase + 128;   // S buffer b at tS + 64 b
+  const uint32_t tS = tbase, tO = tbase + kTmemO;   // S buffer b at tS + 64 b
 
   if (warp == kProdK || warp == kProdV) {
     if (lane == 0) {
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQh = smem_u32(smem + kOffQh), sQl = smem_u32(smem + kOffQl);
       const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
       const uint32_t sPh = smem_u32(smem + kOffPh), sPl = smem_u32(smem + kOffPl);
-      auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i (K stage i % kKSt) into S buffer i % 2
-        const int b = i & 1, kb = i % kKSt;
+      auto mma_s = [&](int i) -> bool {  // S = Q K^T of tile i (K stage i % kKSt) into S buffer i % kSBuf
+        const int b = i % kSBuf, kb = i % kKSt;
         if (!mbar_wait_bounded(&k_full[kb], (uint32_t)((i / kKSt) & 1), p.err)) return false;
         tc::fence_after();
         const uint32_t k0 = sK + kb * kKTile, ts = tS + 64 * b;
@@ -273,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(&k_empty[kb]);
         return true;
       };
-      bool ok = mma_s(0);
-      if (ok && n_kt > 1) ok = mma_s(1);
+      bool ok = true;
+      for (int i = 0; i < kSBuf && i < n_kt && ok; ++i) ok = mma_s(i);
       for (int i = 0; i < n_kt && ok; ++i) {
         const int b = i & 1;
         const uint32_t ph = (uint32_t)((i >> 1) & 1);
@@ -292,8 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 4; ++kk) tc::mma<kD>(tO, tc::desc_sw128(p_l + kk * 32), tc::desc_sw128(v0 + kk * 32), 1);
         tc::commit(&o_done[b]);
         tc::commit(&v_empty[b]);
-        // S of tile i + 2 into S buffer b right behind them (the rows read S(i) before P(i))
-        if (i + 2 < n_kt && !(ok = mma_s(i + 2))) break;
+        // S of tile i + kSBuf into S(i)'s buffer right behind them (the rows read S(i)
+        // before they wrote P(i))
+        if (i + kSBuf < n_kt && !(ok = mma_s(i + kSBuf))) break;
       }
       if (!ok) *(volatile int*)s_abort = 1;
     }
@@ -329,13 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int i = 0; i < n_kt; ++i) {
       const int b = i & 1;
-      if (!wait_all(&s_full[b], (uint32_t)((i >> 1) & 1))) {   // the same decision in every lane
+      if (!wait_all(&s_full[i % kSBuf], (uint32_t)((i / kSBuf) & 1))) {   // the same decision in every lane
         fail = true;
         break;
       }
       tc::fence_after();
       float s[32];
-      tc::ld_32x32(tS + 64 * b + lanes + 32 * hf, s);
+      tc::ld_32x32(tS + 64 * (i % kSBuf) + lanes + 32 * hf, s);
       const int key0 = i * kKT + 32 * hf;
       // the causal mask (and rows past the prompt) only where these 32 keys cross the
       // diagonal of some row of the warp or the warp holds such rows (warp-uniform)
