@@ -1225,15 +1225,22 @@ struct PrefillWs {
   void* argmax_ws;
   void* kv_pack;     // the tcgen05 attention's packed K / V copies
   size_t kv_pack_bytes;
-  void* wide_w;      // Q8_0 above kPrefillWidenRows rows: bf16 copy of one projection's weights
+  void* wide_w;      // Q8_0 above prefill_widen_rows() rows: bf16 copy of one projection's weights
   size_t total;
 };
 
 // Q8_0 prefill of more rows than this: each projection's weights are widened to bf16
 // once (bf16(f32(d) q), the tensor-core lane's own widening) and the rows run on the
-// many-row bf16 GEMMs, which are compute-bound there; up to it the Q8_0 GEMM, which
-// reads 1.0625 bytes per weight, is the faster one.
-constexpr int kPrefillWidenRows = 128;
+// bf16 GEMMs, which are compute-bound there; up to it the Q8_0 GEMM, which reads 1.0625
+// bytes per weight, is the faster one. QD_PREFILL_WIDEN_ROWS overrides it, read once per
+// process so that the workspace size and the pass agree.
+int prefill_widen_rows() {
+  static const int v = [] {
+    const char* e = getenv("QD_PREFILL_WIDEN_ROWS");
+    return e ? std::max(0, atoi(e)) : 128;
+  }();
+  return v;
+}
 
 constexpr int kMaxPrefill = 32768;
 
@@ -1255,7 +1262,7 @@ PrefillWs prefill_ws_layout(const qd_step_args* a, int n, void* base) {
   w.kv_pack_bytes = prefill_attention_tc_scratch_bytes(d.n_kv_heads, a->max_pages * a->page_size);
   off += al256(w.kv_pack_bytes);
   w.wide_w = nullptr;
-  if (d.wtype == QD_W_Q8_0 && n > kPrefillWidenRows) {
+  if (d.wtype == QD_W_Q8_0 && n > prefill_widen_rows()) {
     const size_t H = d.hidden, F = d.ffn, A = (size_t)d.n_q_heads * d.head_dim;
     const size_t most = std::max(std::max(qkv * H, H * A), std::max(2 * F * H, H * F));
     w.wide_w = (void*)(p + off);
