@@ -115,7 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_abort = (int*)(tslot + 1);
   float* xm = (float*)(smem + kOffXm);
 
-  const int qt = (int)(gridDim.x - 1 - blockIdx.x), h = blockIdx.y;   // longest query tiles first
+  // grid (q head, query tile), blocks dispatched in that order: the longest query tiles
+  // of every head first, so the short ones fill the SMs at the end of the causal
+  // triangle (head by head, the last heads' longest tiles would start late and run alone)
+  const int h = blockIdx.x, qt = (int)(gridDim.y - 1 - blockIdx.y);
   const int g = h / (p.Hq / p.Hkv);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -537,7 +540,7 @@ cudaError_t launch_prefill_attention_tc(const PrefillAttnArgs& a, void* scratch,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_ex(prefill_attn_tc_kernel, dim3(ceil_div(a.n, kQT), a.Hq), dim3(kThreads), kSmem, L, tk, tv, p);
+  return launch_ex(prefill_attn_tc_kernel, dim3(a.Hq, ceil_div(a.n, kQT)), dim3(kThreads), kSmem, L, tk, tv, p);
 }
 
 }  // namespace qd
